@@ -1,0 +1,238 @@
+"""FAVOR+ forward attention in plain float64 NumPy -- the oracle.
+
+TEST INFRASTRUCTURE.  This module states, as directly as possible, what the
+FAVOR+ forward path computes, so that the CUDA library can be checked against
+it.  It is slow on purpose: no blocking, fusion or reordering beyond what the
+definitions below state, except that the causal prefix sum is carried block by
+block so the [L, m, dv+1] prefix tensor is never held whole (the two are the
+same sums).  Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import it; the library never does.
+
+Sources (page title, then section / equation):
+  [P]  Rethinking Attention with Performers (Choromanski et al.)
+  [LA] Exploring Linear Attention: Does Attention Require a Softmax? (kexue)
+  [EX] 040 . Performer explainer (wq-win.github.io)
+  [PF] PermuteFormer: Efficient Relative Position Encoding for Long Sequences
+  [RFA] Random Feature Attention (paperlayer summary of arXiv 2103.02143)
+
+Readings taken where the pages are silent or garbled:
+  * data scale s: x = s*q and y = s*k before the feature map ([P] §2.3 after
+    Eq. 6: the sqrt(d) temperature is moved into the inputs; [EX] §1 uses
+    s = d^-1/4).  V is never scaled.
+  * no numerical stabiliser and no epsilon in the oracle (their values are
+    lost on the page, [P] App. A.3/A.4); features are the plain definition.
+  * a denominator that is exactly 0 (possible only for ReLU features) gives an
+    output row of zeros.
+  * causal attention includes the diagonal ([P] Eq. 2, tril keeps it).
+  * the error measure is row-normwise: max over rows i and columns e of
+    |g_ie - o_ie| / max_e' |o_ie'|.
+
+Every function takes float arrays of any float dtype and computes in float64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "feature_map_positive", "feature_map_relu", "feature_map",
+    "bidir_state", "attn_from_features_bidir", "attn_from_features_causal",
+    "explicit_from_features", "rnn_causal_from_features",
+    "favor_bidir", "favor_causal", "favor_feature_map",
+    "softmax_attention", "row_rel_err", "KINDS",
+]
+
+KINDS = ("softmax_pos", "relu")
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def feature_map_positive(x, omega):
+    """Positive random features of inputs x [..., d] (already scaled).
+
+    [P] §2.3, Lemma 1 (Eq. 7) with h(x) = exp(-||x||^2/2), l = 1, f = exp in
+    the general map of Eq. 5:  phi_r(x) = m^-1/2 * exp(omega_r . x - ||x||^2/2).
+    [EX] §2 states the same per-feature formula.
+    """
+    x = _f64(x)
+    omega = _f64(omega)
+    m = omega.shape[0]
+    proj = x @ omega.T
+    sq = 0.5 * np.sum(x * x, axis=-1, keepdims=True)
+    return np.exp(proj - sq) / np.sqrt(m)
+
+
+def feature_map_relu(x, omega):
+    """ReLU generalized-attention features: phi_r(x) = max(omega_r . x, 0) / sqrt(m).
+
+    [P] §4.4 and App. A.4 (generalized attention with kernel = ReLU, i.e. f =
+    ReLU, h = 1 in Eq. 5); [PF] §Performer uses phi(x) = max(x, 0) on the
+    projected features.
+    """
+    x = _f64(x)
+    omega = _f64(omega)
+    m = omega.shape[0]
+    return np.maximum(x @ omega.T, 0.0) / np.sqrt(m)
+
+
+def feature_map(x, omega, kind):
+    if kind == "softmax_pos":
+        return feature_map_positive(x, omega)
+    if kind == "relu":
+        return feature_map_relu(x, omega)
+    raise ValueError(f"unknown feature kind {kind!r}")
+
+
+def _divide_rows(num, den):
+    """out_i = num_i / den_i, and 0 where den_i == 0 exactly."""
+    out = np.zeros_like(num)
+    nz = den != 0.0
+    out[nz] = num[nz] / den[nz, None]
+    return out
+
+
+def bidir_state(phi_k, v):
+    """S = Phi_K^T V (m x dv) and z = Phi_K^T 1_L (m): the key/value summary of
+    [EX] §2 (S = sum_j phi(k_j) v_j^T, z = sum_j phi(k_j)); together they are
+    Buf1 = K'^T [V 1_L] of [P] App. B Alg. 1."""
+    phi_k, v = _f64(phi_k), _f64(v)
+    return phi_k.T @ v, phi_k.sum(axis=0)
+
+
+def attn_from_features_bidir(phi_q, phi_k, v):
+    """Bidirectional FAVOR attention from given features.
+
+    [P] §2.2 Eq. 4 and App. B Alg. 1 (bidirectional branch):
+        C = [V 1_L],  Buf1 = K'^T C  (m x (dv+1)),  Buf2 = Q' Buf1,
+        split Buf2 = [Buf3 buf4] and return diag(buf4)^-1 Buf3.
+    Equivalently S = Phi_K^T V, z = sum_j phi(k_j), out_i = phi(q_i)^T S /
+    phi(q_i)^T z ([EX] §2).
+    phi_q [Lq, m], phi_k [Lk, m], v [Lk, dv] -> out [Lq, dv].
+    """
+    phi_q, phi_k, v = _f64(phi_q), _f64(phi_k), _f64(v)
+    c = np.concatenate([v, np.ones((v.shape[0], 1))], axis=1)
+    buf1 = phi_k.T @ c
+    buf2 = phi_q @ buf1
+    return _divide_rows(buf2[:, :-1], buf2[:, -1])
+
+
+def attn_from_features_causal(phi_q, phi_k, v, block=512):
+    """Causal (unidirectional) FAVOR attention from given features.
+
+    [P] App. B.1 Eq. 11: G_j = K'_j C_j^T, G^PS_i = sum_{j<=i} G_j, row i of
+    tril(Q'K'^T) C equals G^PS_i^T Q'_i; then the same split/divide as Alg. 1.
+    The prefix sum is carried across blocks of ``block`` rows: inside a block,
+    sum_{j<=i} G_j = (state before the block) + sum over the block's rows
+    j <= i, the latter written as tril(Q'_b K'_b^T) C_b.
+    phi_q, phi_k [L, m], v [L, dv] -> out [L, dv].
+    """
+    phi_q, phi_k, v = _f64(phi_q), _f64(phi_k), _f64(v)
+    L, m = phi_q.shape
+    c = np.concatenate([v, np.ones((L, 1))], axis=1)
+    state = np.zeros((m, c.shape[1]))
+    buf2 = np.empty((L, c.shape[1]))
+    for b0 in range(0, L, block):
+        b1 = min(L, b0 + block)
+        pq, pk, cb = phi_q[b0:b1], phi_k[b0:b1], c[b0:b1]
+        buf2[b0:b1] = np.tril(pq @ pk.T) @ cb + pq @ state
+        state = state + pk.T @ cb
+    return _divide_rows(buf2[:, :-1], buf2[:, -1])
+
+
+def explicit_from_features(phi_q, phi_k, v, causal):
+    """The L x L form: A_hat = Q' K'^T (masked by tril if causal), D^-1 A_hat V.
+
+    [P] Eq. 1/2 with A replaced by the kernel estimate of Eq. 3-4; only for
+    small L (it builds the L x L matrix the method avoids).
+    """
+    a = _f64(phi_q) @ _f64(phi_k).T
+    if causal:
+        a = np.tril(a)
+    return _divide_rows(a @ _f64(v), a.sum(axis=1))
+
+
+def rnn_causal_from_features(phi_q, phi_k, v):
+    """Token-by-token recurrence S_t = S_{t-1} + phi(k_t) v_t^T, z_t = z_{t-1} + phi(k_t),
+    out_t = phi(q_t)^T S_t / phi(q_t)^T z_t ([LA] "Autoregressive Generation";
+    [RFA] causal RFA).  A pure-Python loop: small L only."""
+    phi_q, phi_k, v = _f64(phi_q), _f64(phi_k), _f64(v)
+    L, m = phi_q.shape
+    s = np.zeros((m, v.shape[1]))
+    z = np.zeros(m)
+    out = np.zeros((L, v.shape[1]))
+    for t in range(L):
+        s += np.outer(phi_k[t], v[t])
+        z += phi_k[t]
+        den = phi_q[t] @ z
+        out[t] = (phi_q[t] @ s) / den if den != 0.0 else 0.0
+    return out
+
+
+def _per_head(q, k, v, omega, data_scale, kind, fn):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    omega = _f64(omega)
+    B, H, L, _ = q.shape
+    out = np.empty((B, H, L, v.shape[-1]))
+    for b in range(B):
+        for h in range(H):
+            pq = feature_map(data_scale * q[b, h], omega[h], kind)
+            pk = feature_map(data_scale * k[b, h], omega[h], kind)
+            out[b, h] = fn(pq, pk, v[b, h])
+    return out
+
+
+def favor_bidir(q, k, v, omega, data_scale, kind="softmax_pos"):
+    """FAVOR+ bidirectional forward on [B,H,L,d] inputs with omega [H,m,d]."""
+    return _per_head(q, k, v, omega, data_scale, kind, attn_from_features_bidir)
+
+
+def favor_causal(q, k, v, omega, data_scale, kind="softmax_pos"):
+    """FAVOR+ causal forward on [B,H,L,d] inputs with omega [H,m,d]."""
+    return _per_head(q, k, v, omega, data_scale, kind, attn_from_features_causal)
+
+
+def favor_feature_map(x, omega, data_scale, kind="softmax_pos"):
+    """phi(s*x) for x [B,H,L,d], omega [H,m,d] -> [B,H,L,m]."""
+    x = _f64(x)
+    omega = _f64(omega)
+    B, H, L, _ = x.shape
+    out = np.empty((B, H, L, omega.shape[1]))
+    for h in range(H):
+        out[:, h] = feature_map(data_scale * x[:, h], omega[h], kind)
+    return out
+
+
+def softmax_attention(q, k, v, data_scale, causal=False):
+    """Exact softmax attention of [P] Eq. 1 (bidirectional) / Eq. 2 (causal) with
+    A = exp(x_i . y_j), x = s*q, y = s*k (s = d^-1/4 gives q.k/sqrt(d)).
+
+    Each row is shifted by its max before exp; the shift cancels in D^-1 A V.
+    Inputs [L, d] / [L, dv] (one head) or [B,H,L,*] (looped).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim == 4:
+        out = np.empty(q.shape[:3] + (v.shape[-1],))
+        for b in range(q.shape[0]):
+            for h in range(q.shape[1]):
+                out[b, h] = softmax_attention(q[b, h], k[b, h], v[b, h], data_scale, causal)
+        return out
+    logits = (data_scale * q) @ (data_scale * k).T
+    if causal:
+        mask = np.tril(np.ones(logits.shape, dtype=bool))
+        logits = np.where(mask, logits, -np.inf)
+    logits = logits - logits.max(axis=1, keepdims=True)
+    a = np.exp(logits)
+    return (a @ v) / a.sum(axis=1, keepdims=True)
+
+
+def row_rel_err(got, ref):
+    """max_{rows i, cols e} |got_ie - ref_ie| / max_e' |ref_ie'| over the last axis.
+
+    Rows whose reference is all zeros use an absolute error instead.
+    """
+    got = _f64(got)
+    ref = _f64(ref)
+    scale = np.max(np.abs(ref), axis=-1, keepdims=True)
+    scale = np.where(scale > 0, scale, 1.0)
+    return float(np.max(np.abs(got - ref) / scale)) if ref.size else 0.0
