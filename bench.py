@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""FAVOR+ forward attention throughput on GB300: tokens*heads per second.
+
+One step = one pass of the whole forward hot path over one batch of the
+very-long-context workload (B=1, H=16, L=65536, d=dv=64, m=256, bf16,
+Q/K/V ~ N(0, 0.5^2), orthogonal omega per head): bidirectional and causal
+attention, each with positive softmax features and with ReLU features (four
+library calls).  value = token*heads processed per second, whole job.
+
+Arms:
+  --impl ours (default)  the CUDA library through its C ABI, inputs resident
+                         in HBM; plus an end-to-end number with host buffers
+                         (host->device copies and the device->host read of
+                         the outputs inside the timed region).
+  --impl reference       the float64 CPU oracle on this host's cores, each
+                         step a bounded sample (a few heads) of the workload.
+
+Multi-GPU (torchrun, one process per GPU): each rank runs an independent
+replica of the workload with its own seed (no collective on the data path);
+scaling is weak and value sums over ranks, time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from synth import CONFIGS, make_workload  # noqa: E402
+
+STEP_CALLS = (("bidir", "softmax_pos"), ("causal", "softmax_pos"), ("bidir", "relu"), ("causal", "relu"))
+UNIT = "tokens*heads/s"
+METRIC = "FAVOR+ forward tokens*heads/sec (bidir & causal)"
+SFU_EX2_PER_CLK_PER_SM = 16   # MUFU throughput per SM per clock (exp2)
+GB300_SMS = 152
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="long_bf16", choices=sorted(CONFIGS))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-heads", type=int, default=2, help="heads of the workload in the CPU oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks/throttle samples for one GPU while the work runs."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.samples = []          # (t, sm_mhz, max_mhz, reasons)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+            reasons = [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, mx, reasons))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1, fallback_t0):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = "timed region"
+        if not win:
+            win = [s for s in self.samples if fallback_t0 <= s[0] <= t1]
+            note = "warm-up and timed region (timed region shorter than the sampling period)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+        reasons = sorted({r for s in win for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": max(s[2] for s in win),
+                "reasons": reasons, "samples": len(win), "window": note}
+
+
+# ------------------------------------------------------------- algorithmic work
+def per_token_head(w, slot, kind):
+    """Algorithmic (bytes, flops, exps) per token*head for one kernel slot."""
+    b = 2 if w.dtype == "bf16" else 4
+    d, dv, m = w.d, w.dv, w.m
+    e = m if kind == "softmax_pos" else 0
+    if slot == "segment_state":          # reads K, V; phi_K and Phi_K^T [V 1]
+        return (d + dv) * b, 2 * m * d + 2 * m * (dv + 1), e
+    if slot == "bidir_readout":          # reads Q, writes out; phi_Q and Phi_Q [S z]
+        return (d + dv) * b, 2 * m * d + 2 * m * (dv + 1), e
+    if slot == "causal_chunks":          # reads Q, K, V, writes out (the method's whole per-token work)
+        return (2 * d + 2 * dv) * b, 4 * m * d + 4 * m * (dv + 1), 2 * e
+    if slot == "feature_map":
+        return d * b + m * b, 2 * m * d, e
+    return 0, 0, 0
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "random_feature_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(slot):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernels."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(slot)
+    if not ent or ent.get("source_digest") != source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------- CPU oracle arm
+def cpu_sample(w, heads, seed=0):
+    """Time the oracle on the first `heads` heads of the workload, all four calls."""
+    import oracle as O
+    wh = w.replace(H=heads)
+    omega, q, k, v = make_workload(wh, seed)
+    t0 = time.perf_counter()
+    for mode, kind in STEP_CALLS:
+        fn = O.favor_causal if mode == "causal" else O.favor_bidir
+        fn(q, k, v, omega, w.data_scale, kind)
+    dt = time.perf_counter() - t0
+    units = len(STEP_CALLS) * wh.B * wh.H * wh.L
+    return units / dt, dt, units
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = CONFIGS[args.workload]
+    heads = max(1, min(args.cpu_heads, w.H))
+    for _ in range(max(0, min(args.warmup, 1))):
+        cpu_sample(w.replace(L=min(w.L, 4096)), 1)
+    total_units = 0
+    total_t = 0.0
+    for _ in range(args.steps):
+        _, dt, units = cpu_sample(w, heads)
+        total_units += units
+        total_t += dt
+    value = total_units / total_t
+    sample = (f"{heads} of {w.H} heads of {w.name} (B={w.B}, L={w.L}, d={w.d}, m={w.m}), all four calls "
+              f"(bidir/causal x softmax_pos/relu) per step, float64 NumPy")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "sample_heads": heads},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import random_feature_gb300 as R
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    w = CONFIGS[args.workload]
+    peaks = load_peaks()
+    omega, q, k, v = make_workload(w, seed=rank)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    qd, kd, vd = (torch.from_numpy(a).to(device=dev, dtype=tdt).contiguous() for a in (q, k, v))
+    handles = {kind: R.Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, omega, w.data_scale, w.B, w.L)
+               for kind in sorted({kd_ for _, kd_ in STEP_CALLS})}
+    outs = [torch.empty((w.B, w.H, w.L, w.dv), dtype=tdt, device=dev) for _ in STEP_CALLS]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(qq=qd, kk=kd, vv=vd, oo=outs):
+        for (mode, kind), o in zip(STEP_CALLS, oo):
+            handles[kind].attn(qq, kk, vv, causal=(mode == "causal"), out=o, stream=stream)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    t_warm = time.time()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    for hd in handles.values():
+        R.favor_profile_reset(hd.handle)
+        R.favor_profile_enable(hd.handle, True)
+    launches0 = R.favor_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    launches = R.favor_launch_count() - launches0
+    sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    for hd in handles.values():
+        R.favor_profile_enable(hd.handle, False)
+
+    # per-kernel device time over the timed region
+    slots = {}
+    for hd in handles.values():
+        for sl in range(R.favor_profile_slots()):
+            ms, n = R.favor_profile_read(hd.handle, sl)
+            name = R.favor_profile_name(sl)
+            a = slots.setdefault(name, [0.0, 0, {}])
+            a[0] += ms
+            a[1] += n
+            a[2][hd.kind] = a[2].get(hd.kind, 0) + n
+
+    ms_step = ms_total / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    units_step = len(STEP_CALLS) * w.B * w.H * w.L
+    value = world * units_step / (ms_step / 1e3)
+
+    # end to end through the public API: pinned host inputs in, outputs back, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        hq, hk, hv = (torch.from_numpy(a).to(tdt).pin_memory() for a in (q, k, v))
+        hout = [torch.empty((w.B, w.H, w.L, w.dv), dtype=tdt).pin_memory() for _ in STEP_CALLS]
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            step()
+            for o, ho in zip(outs, hout):
+                ho.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a0.elapsed_time(a1) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        nb = 2 if tdt == torch.bfloat16 else 4
+        e2e = {"value": world * units_step / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(nb * (q.size + k.size + v.size)),
+               "d2h_bytes_per_step": int(nb * sum(o.numel() for o in outs)), "ms_per_step": e_ms}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    clocks = sampler.summary(t0, t1, t_warm)
+    # roofline of the dominant kernel
+    dom = max(slots.items(), key=lambda kv: kv[1][0])
+    dname, (dms, dn, by_kind) = dom
+    per_launch_ms = dms / max(dn, 1)
+    T = w.B * w.H * w.L
+    b_sum = f_sum = e_sum = 0.0
+    for kind, n in by_kind.items():
+        bb, ff, ee = per_token_head(w, dname, kind)
+        b_sum += n * bb * T
+        f_sum += n * ff * T
+        e_sum += n * ee * T
+    bytes_l, flops_l, exps_l = b_sum / max(dn, 1), f_sum / max(dn, 1), e_sum / max(dn, 1)
+    sec = per_launch_ms / 1e3
+    sm_mhz = clocks["sm_mhz"] or peaks["sm_max_mhz"]
+    sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * sm_mhz * 1e6
+    cands = {
+        "hbm": (bytes_l / sec / 1e9, peaks["hbm_gbs"], "GB/s", bytes_l / (peaks["hbm_gbs"] * 1e9)),
+        "tensor": (flops_l / sec / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s",
+                   flops_l / (peaks["bf16_tflops_sustained"] * 1e12)),
+        "alu": (exps_l / sec / 1e9, sfu_peak / 1e9, "Gexp/s", exps_l / sfu_peak),
+    }
+    bound = max(cands, key=lambda kk: cands[kk][3])
+    ach, pk, unit, _ = cands[bound]
+    traffic = ncu_traffic(dname)
+    roofline = {"bound": bound, "achieved": ach, "peak": pk, "unit": unit, "frac": ach / pk,
+                "traffic": traffic, "kernel": dname, "launch_ms": per_launch_ms,
+                "peak_source": peaks["source"] + (" (sustained bf16)" if bound == "tensor" else "")
+                + (" (16 ex2/clk/SM x 152 SMs x median SM clock)" if bound == "alu" else "")}
+    roofline_all = {kk: {"achieved": c[0], "peak": c[1], "unit": c[2], "frac": c[0] / c[1]} for kk, c in cands.items()}
+    kernels = {name: {"ms_total": v_[0], "launches": v_[1], "share": v_[0] / max(1e-12, sum(x[0] for x in slots.values()))}
+               for name, v_ in slots.items() if v_[1]}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        heads = max(1, min(args.cpu_heads, w.H))
+        cval, cdt, _ = cpu_sample(w, heads)
+        cpu = {"value": cval, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{heads} of {w.H} heads of {w.name}, all four calls, float64 NumPy, {cdt:.1f} s"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"{w.name}: B={w.B} H={w.H} L={w.L} d={w.d} dv={w.dv} m={w.m}, "
+                                   f"calls per step: bidir+causal x softmax_pos+relu",
+                       "global_batch": w.B * world, "seq_len": w.L, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (Q,K,V 384 MB per replica)"},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
+            "roofline_all": roofline_all, "kernels": kernels, "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+    for hd in handles.values():
+        hd.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

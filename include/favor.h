@@ -1,0 +1,163 @@
+/*
+ * favor.h -- C ABI of the FAVOR+ forward-attention library for one GB300 (sm_103a).
+ *
+ * FAVOR+ (Rethinking Attention with Performers, §2.2-2.4 and App. B Alg. 1)
+ * replaces the L x L softmax attention matrix by random features:
+ *
+ *   positive features (Lemma 1, Eq. 7):  phi_r(x) = m^-1/2 exp(omega_r . x - ||x||^2 / 2)
+ *   ReLU features (§4.4, App. A.4):      phi_r(x) = m^-1/2 max(omega_r . x, 0)
+ *
+ * with x = s*q for queries and y = s*k for keys (s = data_scale; §2.3 after
+ * Eq. 6 moves the sqrt(d) temperature into the inputs, s = d^-1/4 reproduces
+ * exp(q.k / sqrt(d))).  Attention is then the reordered product of Eq. 4:
+ *
+ *   bidirectional:  S = Phi_K^T V, z = Phi_K^T 1,  out_i = phi(q_i)^T S / phi(q_i)^T z
+ *   causal (App. B.1, Eq. 11): the same with S_i, z_i summed over keys j <= i.
+ *
+ * All tensors are contiguous row-major device buffers of the handle's dtype:
+ *   q, k, x: [B, H, L, d]    v, out: [B, H, L, dv]    phi: [B, H, L, m]
+ * The caller owns them.  Every call only enqueues work on `stream` (a
+ * cudaStream_t passed as void*, NULL = legacy default stream) and returns;
+ * launch errors are returned, execution errors appear at the caller's next
+ * synchronisation, as usual in CUDA.  All argument checks happen on the host
+ * before anything is launched; nothing traps on the device.
+ *
+ * A handle owns device copies of omega, per-head constants and a workspace
+ * sized at creation for max_B and max_L.  Calls on one handle must not overlap
+ * in time on the device (they share the workspace); use one handle per
+ * concurrent stream.  A handle belongs to the device that was current at
+ * favor_create; call it with that device current.
+ */
+#ifndef FAVOR_H
+#define FAVOR_H
+
+#if defined(__GNUC__)
+#define FAVOR_API __attribute__((visibility("default")))
+#else
+#define FAVOR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FAVOR_OK = 0,
+    FAVOR_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, size above the handle's maximum */
+    FAVOR_ERR_UNSUPPORTED = 2,   /* shape or enum value this library does not implement */
+    FAVOR_ERR_NOMEM = 3,         /* device or host allocation failed in favor_create */
+    FAVOR_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
+} favor_status;
+
+/* Feature map f in Eq. 5 of Rethinking Attention with Performers. */
+typedef enum {
+    FAVOR_KERNEL_SOFTMAX_POS = 0,  /* positive random features for the softmax kernel (Lemma 1) */
+    FAVOR_KERNEL_RELU = 1          /* generalized attention with f = ReLU (§4.4, App. A.4) */
+} favor_kernel;
+
+/* Storage type of q, k, v, out, x and phi.  Arithmetic: F32 computes in fp32
+ * throughout; BF16 rounds the features to bf16 for the tensor-core
+ * contractions and accumulates in fp32. */
+typedef enum {
+    FAVOR_DTYPE_F32 = 0,
+    FAVOR_DTYPE_BF16 = 1
+} favor_dtype;
+
+typedef struct favor_handle_s* favor_handle;
+
+/*
+ * favor_create -- build a handle for H heads with m features of width d and
+ * values of width dv.
+ *
+ *   omega_host  host float array [H, m, d], row r of head h is omega_r
+ *               (Eq. 5; drawn by the caller, e.g. orthogonal blocks as in §2.4
+ *               and App. B.2 (1)).  Copied synchronously; the caller may free
+ *               it on return.  The BF16 dtype rounds omega to bf16 (nearest
+ *               even) for the tensor-core projection.
+ *   data_scale  s > 0: features are taken of s*q and s*k.
+ *   max_B, max_L  upper bounds for later calls; they size the workspace.
+ *
+ * Supported: d, dv in {16, 32, 64, 128}; m a multiple of 16 in [16, 256];
+ * H >= 1.  Anything else gives FAVOR_ERR_UNSUPPORTED (enum values out of
+ * range: FAVOR_ERR_INVALID_ARG).  Fails with FAVOR_ERR_NOMEM if device memory
+ * runs out, FAVOR_ERR_CUDA if no device is usable.  *out is set to NULL on
+ * any failure.
+ */
+FAVOR_API favor_status favor_create(favor_handle* out, int H, int m, int d, int dv,
+                          favor_kernel kind, favor_dtype dtype,
+                          const float* omega_host, float data_scale,
+                          int max_B, int max_L);
+
+/*
+ * favor_feature_map -- phi = feature map of s*x, exactly as defined above
+ * (Lemma 1 with the m^-1/2 factor and the -||x||^2/2 term, or the ReLU form),
+ * with no stabilising shift.  x [B,H,L,d] -> phi [B,H,L,m], both of the
+ * handle's dtype; phi is only written.  1 <= B <= max_B, 1 <= L <= max_L.
+ * (Positive features overflow to inf only when omega_r . x - ||x||^2/2 > 88,
+ * which needs ||omega_r||^2 > 176.)
+ */
+FAVOR_API favor_status favor_feature_map(favor_handle h, const void* x, void* phi,
+                               int B, int L, void* stream);
+
+/*
+ * favor_attn_bidir -- bidirectional FAVOR+ attention (Eq. 4; Alg. 1 with
+ * isBidirectional): out_i = phi(q_i)^T S / phi(q_i)^T z over all L keys of
+ * the same (b, h).  q, k [B,H,L,d], v [B,H,L,dv] are read; out [B,H,L,dv] is
+ * only written.  A row whose denominator is exactly 0 (possible only with
+ * ReLU features) is written as zeros.  Shifts that cancel between numerator
+ * and denominator are applied for range safety (a per-query-row shift and a
+ * per-head key shift); they do not change the result beyond rounding.
+ */
+FAVOR_API favor_status favor_attn_bidir(favor_handle h, const void* q, const void* k,
+                              const void* v, void* out, int B, int L, void* stream);
+
+/*
+ * favor_attn_causal -- unidirectional FAVOR+ attention (App. B.1, Eq. 11):
+ * out_i = phi(q_i)^T S_i / phi(q_i)^T z_i with S_i, z_i summed over keys
+ * j <= i (the diagonal included, as tril in Eq. 2).  Same layouts, ownership
+ * and zero-denominator rule as favor_attn_bidir.  No L x L matrix and no
+ * per-token prefix tensor is built.
+ */
+FAVOR_API favor_status favor_attn_causal(favor_handle h, const void* q, const void* k,
+                               const void* v, void* out, int B, int L, void* stream);
+
+/* favor_destroy -- free everything the handle owns (after synchronising its
+ * device).  Accepts NULL. */
+FAVOR_API favor_status favor_destroy(favor_handle h);
+
+/* Name of a status code (static string). */
+FAVOR_API const char* favor_status_str(favor_status s);
+
+/* Text of the most recent failure in the calling thread (static buffer,
+ * empty if none). */
+FAVOR_API const char* favor_last_error(void);
+
+/* Number of kernels this library has launched in this process (all handles,
+ * all threads); a counter for measurement. */
+FAVOR_API unsigned long long favor_launch_count(void);
+
+/*
+ * Per-kernel timing for measurement (no counterpart on the pages).
+ *
+ * favor_profile_enable(h, 1) makes every later kernel launch through h record
+ * a pair of CUDA events on the launching stream around the kernel;
+ * favor_profile_read(h, slot, &ms, &n) synchronises those events and returns
+ * the summed device time in milliseconds and the number of launches recorded
+ * for one kernel slot since the last reset; favor_profile_enable(h, 0) stops
+ * recording and favor_profile_reset(h) clears the totals.  Slots are numbered
+ * 0 .. favor_profile_slots()-1 and named by favor_profile_name(slot).  Recording
+ * allocates events lazily on the host thread that launches; errors come back
+ * as FAVOR_ERR_CUDA.
+ */
+FAVOR_API favor_status favor_profile_enable(favor_handle h, int enable);
+FAVOR_API favor_status favor_profile_reset(favor_handle h);
+FAVOR_API favor_status favor_profile_read(favor_handle h, int slot, double* ms_total,
+                                          unsigned long long* launches);
+FAVOR_API int favor_profile_slots(void);
+FAVOR_API const char* favor_profile_name(int slot);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FAVOR_H */

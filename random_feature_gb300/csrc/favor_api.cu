@@ -1,0 +1,353 @@
+// Host side of the C ABI: argument checks, handle lifetime, workspace, dispatch.
+//
+// Every check runs before anything is enqueued; a failing call launches nothing.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "favor_internal.h"
+
+namespace favor {
+
+static std::atomic<unsigned long long> g_launches{0};
+static thread_local char g_err[512] = "";
+
+void count_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+favor_status set_error(favor_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+favor_status check_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return set_error(FAVOR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return FAVOR_OK;
+}
+
+SegPlan plan_segments(int BH, int L, int num_sms) {
+    SegPlan p;
+    p.tiles = (L + 127) / 128;
+    // Aim for about two independent segments per SM across all heads, but keep
+    // segments at least 4 tiles long so the per-segment state write stays small
+    // next to the segment's own traffic.
+    long target = 2L * num_sms;
+    int want = (int)((target + BH - 1) / BH);
+    int max_seg = (p.tiles + 3) / 4;
+    if (want > max_seg) want = max_seg;
+    if (want < 1) want = 1;
+    p.cap = want;   // n_seg <= want, and want does not decrease with L
+    p.seg_tiles = (p.tiles + want - 1) / want;
+    p.n_seg = (p.tiles + p.seg_tiles - 1) / p.seg_tiles;
+    return p;
+}
+
+static cudaEvent_t take_event(Profile* p) {
+    if (!p->spare.empty()) {
+        cudaEvent_t e = p->spare.back();
+        p->spare.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) { cudaGetLastError(); return nullptr; }
+    return e;
+}
+
+ProfScope::ProfScope(const Handle& hh, int sl, cudaStream_t s) : h(hh), slot(sl), st(s) {
+    if (!h.prof || !h.prof->on) return;
+    cudaEvent_t a = take_event(h.prof);
+    b = take_event(h.prof);
+    if (!a || !b) { b = nullptr; return; }
+    cudaEventRecord(a, st);
+    h.prof->pending.push_back({slot, a, b});
+}
+
+ProfScope::~ProfScope() {
+    if (b) cudaEventRecord(b, st);
+}
+
+static bool shape_ok(int x) { return x == 16 || x == 32 || x == 64 || x == 128; }
+
+}  // namespace favor
+
+using namespace favor;
+
+extern "C" {
+
+const char* favor_status_str(favor_status s) {
+    switch (s) {
+        case FAVOR_OK: return "FAVOR_OK";
+        case FAVOR_ERR_INVALID_ARG: return "FAVOR_ERR_INVALID_ARG";
+        case FAVOR_ERR_UNSUPPORTED: return "FAVOR_ERR_UNSUPPORTED";
+        case FAVOR_ERR_NOMEM: return "FAVOR_ERR_NOMEM";
+        case FAVOR_ERR_CUDA: return "FAVOR_ERR_CUDA";
+    }
+    return "FAVOR_ERR_UNKNOWN";
+}
+
+const char* favor_last_error(void) { return g_err; }
+
+unsigned long long favor_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+static void free_handle(Handle* h) {
+    if (!h) return;
+    cudaFree(h->omega_f32);
+    cudaFree(h->omega_bf16);
+    cudaFree(h->kshift);
+    cudaFree(h->ws_partial);
+    cudaFree(h->ws_state);
+    cudaFree(h->ws_tc);
+    free(h->omega_sqnorm_half_host);
+    if (h->prof) {
+        for (auto& pe : h->prof->pending) { cudaEventDestroy(pe.a); cudaEventDestroy(pe.b); }
+        for (auto e : h->prof->spare) cudaEventDestroy(e);
+        delete h->prof;
+    }
+    delete h;
+}
+
+favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_kernel kind,
+                          favor_dtype dtype, const float* omega_host, float data_scale,
+                          int max_B, int max_L) {
+    g_err[0] = 0;
+    if (!out) return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: out is NULL");
+    *out = nullptr;
+    if (!omega_host) return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: omega_host is NULL");
+    if (H < 1 || m < 1 || d < 1 || dv < 1 || max_B < 1 || max_L < 1)
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: sizes must be >= 1 (H=%d m=%d d=%d dv=%d max_B=%d max_L=%d)",
+                         H, m, d, dv, max_B, max_L);
+    if (kind != FAVOR_KERNEL_SOFTMAX_POS && kind != FAVOR_KERNEL_RELU)
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: unknown kernel kind %d", (int)kind);
+    if (dtype != FAVOR_DTYPE_F32 && dtype != FAVOR_DTYPE_BF16)
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: unknown dtype %d", (int)dtype);
+    if (!(data_scale > 0.0f) || !std::isfinite(data_scale))
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: data_scale must be finite and > 0");
+    if (!shape_ok(d) || !shape_ok(dv))
+        return set_error(FAVOR_ERR_UNSUPPORTED, "favor_create: d=%d dv=%d (supported: 16, 32, 64, 128)", d, dv);
+    if (m % 16 != 0 || m < 16 || m > 256)
+        return set_error(FAVOR_ERR_UNSUPPORTED, "favor_create: m=%d (supported: multiples of 16 in [16, 256])", m);
+    if ((long long)max_B * H * (long long)max_L * (d > dv ? d : dv) > (1LL << 40))
+        return set_error(FAVOR_ERR_UNSUPPORTED, "favor_create: max_B*H*max_L too large");
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(FAVOR_ERR_CUDA, "favor_create: no usable CUDA device");
+    }
+    Handle* h = new (std::nothrow) Handle();
+    if (!h) return set_error(FAVOR_ERR_NOMEM, "favor_create: host allocation failed");
+    std::memset(h, 0, sizeof(*h));
+    h->prof = new (std::nothrow) Profile();
+    if (!h->prof) { delete h; return set_error(FAVOR_ERR_NOMEM, "favor_create: host allocation failed"); }
+    h->H = H; h->m = m; h->d = d; h->dv = dv; h->kind = kind; h->dtype = dtype;
+    h->s = data_scale; h->max_B = max_B; h->max_L = max_L; h->device = dev;
+    cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (h->num_sms < 1) h->num_sms = 1;
+
+    const size_t n_om = (size_t)H * m * d;
+    std::vector<float> om(omega_host, omega_host + n_om);
+    for (size_t i = 0; i < n_om; ++i) {
+        if (!std::isfinite(om[i])) {
+            free_handle(h);
+            return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: omega has a non-finite entry at %zu", i);
+        }
+    }
+    std::vector<__nv_bfloat16> om_bf;
+    if (dtype == FAVOR_DTYPE_BF16) {
+        om_bf.resize(n_om);
+        for (size_t i = 0; i < n_om; ++i) {
+            om_bf[i] = __float2bfloat16_rn(om[i]);
+            om[i] = __bfloat162float(om_bf[i]);   // the fp32 copy holds exactly what the MMA sees
+        }
+    }
+    // Per-head key shift: kappa_h = max(0, max_r ||omega_r||^2/2 - headroom).
+    std::vector<float> ks(H);
+    h->omega_sqnorm_half_host = (float*)malloc(sizeof(float) * H);
+    if (!h->omega_sqnorm_half_host) { free_handle(h); return set_error(FAVOR_ERR_NOMEM, "favor_create: host allocation failed"); }
+    for (int hh = 0; hh < H; ++hh) {
+        double mx = 0.0;
+        for (int r = 0; r < m; ++r) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) {
+                double w = om[((size_t)hh * m + r) * d + c];
+                acc += w * w;
+            }
+            if (acc > mx) mx = acc;
+        }
+        h->omega_sqnorm_half_host[hh] = (float)(0.5 * mx);
+        double k = 0.5 * mx - (double)KSHIFT_HEADROOM;
+        ks[hh] = (float)(k > 0.0 ? k : 0.0);
+    }
+
+    // Workspace: per-(head, segment) states for the largest call the bounds allow.
+    size_t rows = 0;
+    for (int b = 1; b <= max_B; ++b) {
+        SegPlan p = plan_segments(b * H, max_L, h->num_sms);
+        size_t r = (size_t)b * H * p.cap;
+        if (r > rows) rows = r;
+    }
+    h->ws_partial_rows = rows;
+    const size_t st_elems = (size_t)m * (dv + 1);
+
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = cudaMalloc(&h->omega_f32, n_om * sizeof(float));
+    if (e == cudaSuccess && dtype == FAVOR_DTYPE_BF16) e = cudaMalloc(&h->omega_bf16, n_om * sizeof(__nv_bfloat16));
+    if (e == cudaSuccess) e = cudaMalloc(&h->kshift, H * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->ws_partial, rows * st_elems * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->ws_state, (size_t)max_B * H * st_elems * sizeof(float));
+    if (e != cudaSuccess) {
+        favor_status st = (e == cudaErrorMemoryAllocation) ? FAVOR_ERR_NOMEM : FAVOR_ERR_CUDA;
+        set_error(st, "favor_create: cudaMalloc: %s", cudaGetErrorString(e));
+        cudaGetLastError();
+        free_handle(h);
+        return st;
+    }
+    if (tc_supported(*h)) {
+        // bf16 copies of the reduced states in the tensor-core operand layout.
+        h->ws_tc_bytes = (size_t)max_B * H * 80 * m * sizeof(__nv_bfloat16);
+        e = cudaMalloc(&h->ws_tc, h->ws_tc_bytes);
+        if (e != cudaSuccess) {
+            favor_status st = (e == cudaErrorMemoryAllocation) ? FAVOR_ERR_NOMEM : FAVOR_ERR_CUDA;
+            set_error(st, "favor_create: cudaMalloc: %s", cudaGetErrorString(e));
+            cudaGetLastError();
+            free_handle(h);
+            return st;
+        }
+    }
+    e = cudaMemcpy(h->omega_f32, om.data(), n_om * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && dtype == FAVOR_DTYPE_BF16)
+        e = cudaMemcpy(h->omega_bf16, om_bf.data(), n_om * sizeof(__nv_bfloat16), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(h->kshift, ks.data(), H * sizeof(float), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        set_error(FAVOR_ERR_CUDA, "favor_create: cudaMemcpy: %s", cudaGetErrorString(e));
+        cudaGetLastError();
+        free_handle(h);
+        return FAVOR_ERR_CUDA;
+    }
+    *out = reinterpret_cast<favor_handle>(h);
+    return FAVOR_OK;
+}
+
+favor_status favor_destroy(favor_handle hd) {
+    if (!hd) return FAVOR_OK;
+    Handle* h = reinterpret_cast<Handle*>(hd);
+    const int dev = h->device;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (cur != dev) cudaSetDevice(dev);
+    cudaDeviceSynchronize();
+    free_handle(h);
+    if (cur != dev) cudaSetDevice(cur);
+    cudaGetLastError();
+    return FAVOR_OK;
+}
+
+static favor_status check_call(const char* fn, favor_handle hd, int B, int L) {
+    g_err[0] = 0;
+    if (!hd) return set_error(FAVOR_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+    const Handle* h = reinterpret_cast<const Handle*>(hd);
+    if (B < 1 || L < 1) return set_error(FAVOR_ERR_INVALID_ARG, "%s: B=%d L=%d must be >= 1", fn, B, L);
+    if (B > h->max_B || L > h->max_L)
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: B=%d L=%d exceed the handle's max_B=%d max_L=%d",
+                         fn, B, L, h->max_B, h->max_L);
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: current device %d is not the handle's device %d",
+                         fn, cur, h->device);
+    }
+    return FAVOR_OK;
+}
+
+favor_status favor_feature_map(favor_handle hd, const void* x, void* phi, int B, int L, void* stream) {
+    favor_status st = check_call("favor_feature_map", hd, B, L);
+    if (st != FAVOR_OK) return st;
+    if (!x || !phi) return set_error(FAVOR_ERR_INVALID_ARG, "favor_feature_map: null tensor pointer");
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (tc_supported(h)) return tc_feature_map(h, x, phi, B, L, s);
+    return simt_feature_map(h, x, phi, B, L, s);
+}
+
+favor_status favor_attn_bidir(favor_handle hd, const void* q, const void* k, const void* v, void* out,
+                              int B, int L, void* stream) {
+    favor_status st = check_call("favor_attn_bidir", hd, B, L);
+    if (st != FAVOR_OK) return st;
+    if (!q || !k || !v || !out) return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_bidir: null tensor pointer");
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (tc_supported(h)) return tc_bidir(h, q, k, v, out, B, L, s);
+    return simt_bidir(h, q, k, v, out, B, L, s);
+}
+
+favor_status favor_attn_causal(favor_handle hd, const void* q, const void* k, const void* v, void* out,
+                               int B, int L, void* stream) {
+    favor_status st = check_call("favor_attn_causal", hd, B, L);
+    if (st != FAVOR_OK) return st;
+    if (!q || !k || !v || !out) return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_causal: null tensor pointer");
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (tc_supported(h)) return tc_causal(h, q, k, v, out, B, L, s);
+    return simt_causal(h, q, k, v, out, B, L, s);
+}
+
+static const char* kSlotNames[PROF_NSLOTS] = {"feature_map", "segment_state", "segment_combine",
+                                               "bidir_readout", "causal_chunks"};
+
+int favor_profile_slots(void) { return PROF_NSLOTS; }
+
+const char* favor_profile_name(int slot) {
+    return (slot >= 0 && slot < PROF_NSLOTS) ? kSlotNames[slot] : "";
+}
+
+favor_status favor_profile_enable(favor_handle hd, int enable) {
+    if (!hd) return set_error(FAVOR_ERR_INVALID_ARG, "favor_profile_enable: handle is NULL");
+    reinterpret_cast<Handle*>(hd)->prof->on = enable != 0;
+    return FAVOR_OK;
+}
+
+favor_status favor_profile_reset(favor_handle hd) {
+    if (!hd) return set_error(FAVOR_ERR_INVALID_ARG, "favor_profile_reset: handle is NULL");
+    Profile* p = reinterpret_cast<Handle*>(hd)->prof;
+    for (auto& pe : p->pending) { p->spare.push_back(pe.a); p->spare.push_back(pe.b); }
+    p->pending.clear();
+    for (int i = 0; i < PROF_NSLOTS; ++i) { p->ms[i] = 0.0; p->n[i] = 0; }
+    return FAVOR_OK;
+}
+
+favor_status favor_profile_read(favor_handle hd, int slot, double* ms_total, unsigned long long* launches) {
+    if (!hd || !ms_total || !launches)
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_profile_read: null argument");
+    if (slot < 0 || slot >= PROF_NSLOTS) return set_error(FAVOR_ERR_INVALID_ARG, "favor_profile_read: bad slot %d", slot);
+    Profile* p = reinterpret_cast<Handle*>(hd)->prof;
+    for (auto& pe : p->pending) {
+        if (cudaEventSynchronize(pe.b) != cudaSuccess) {
+            cudaGetLastError();
+            return set_error(FAVOR_ERR_CUDA, "favor_profile_read: event synchronize failed");
+        }
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, pe.a, pe.b) != cudaSuccess) {
+            cudaGetLastError();
+            return set_error(FAVOR_ERR_CUDA, "favor_profile_read: elapsed time failed");
+        }
+        p->ms[pe.slot] += ms;
+        p->n[pe.slot] += 1;
+        p->spare.push_back(pe.a);
+        p->spare.push_back(pe.b);
+    }
+    p->pending.clear();
+    *ms_total = p->ms[slot];
+    *launches = p->n[slot];
+    return FAVOR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// Internal declarations shared by the host API and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/favor.h"
+
+namespace favor {
+
+// Kernel slots for the optional per-kernel event timing.
+enum ProfSlot {
+    PROF_FEATURE_MAP = 0,
+    PROF_STATE,         // per-segment key/value state (bidirectional partials, causal totals)
+    PROF_COMBINE,       // fixed-order reduce / exclusive scan of segment states
+    PROF_READOUT,       // bidirectional query readout
+    PROF_CAUSAL,        // causal chunked attention
+    PROF_NSLOTS
+};
+
+struct ProfEvent {
+    int slot;
+    cudaEvent_t a, b;
+};
+
+struct Profile {
+    bool on = false;
+    std::vector<ProfEvent> pending;   // recorded, not yet read
+    std::vector<cudaEvent_t> spare;   // reusable events
+    double ms[PROF_NSLOTS] = {};
+    unsigned long long n[PROF_NSLOTS] = {};
+};
+
+// Everything a handle owns.  Device pointers unless noted.
+struct Handle {
+    int H, m, d, dv;
+    favor_kernel kind;
+    favor_dtype dtype;
+    float s;                  // data scale: x = s*q, y = s*k
+    int max_B, max_L;
+    int device;
+    int num_sms;
+
+    float* omega_f32;         // [H, m, d] (bf16-rounded values for the BF16 dtype)
+    __nv_bfloat16* omega_bf16;// [H, m, d] (BF16 dtype only)
+    float* kshift;            // [H] per-head key shift kappa_h (natural-log units)
+    float* omega_sqnorm_half_host; // host [H]: max_r ||omega_r||^2 / 2
+
+    float* ws_partial;        // [rows][m][dv+1] per-segment states (bidir partials / causal prefixes)
+    float* ws_state;          // [max_B*H][m][dv+1] reduced bidirectional states
+    size_t ws_partial_rows;   // capacity of ws_partial in (head, segment) rows
+    void* ws_tc;              // tensor-core path scratch (bf16 operand copies), may be null
+    size_t ws_tc_bytes;
+    Profile* prof;            // per-kernel timing (host object)
+};
+
+// Bracket one kernel launch with timing events when the handle's profiling is on.
+struct ProfScope {
+    const Handle& h;
+    int slot;
+    cudaStream_t st;
+    cudaEvent_t b = nullptr;
+    ProfScope(const Handle& hh, int sl, cudaStream_t s);
+    ~ProfScope();
+};
+
+// Work split of a (B*H, L) call into per-head segments of whole 128-token tiles.
+struct SegPlan {
+    int tiles;        // ceil(L / 128)
+    int seg_tiles;    // tiles per segment
+    int n_seg;        // segments per head
+    int cap;          // upper bound of n_seg for this BH and any L' <= L (sizes the workspace)
+};
+
+SegPlan plan_segments(int BH, int L, int num_sms);
+
+// Bookkeeping shared by every launcher.
+void count_launch(int n = 1);
+favor_status set_error(favor_status st, const char* fmt, ...);
+favor_status check_launch(const char* what);
+
+// The key-side shift is kappa_h = max(0, max_r ||omega_r||^2/2 - KSHIFT_HEADROOM): it
+// bounds every key feature by exp(KSHIFT_HEADROOM) whatever the input, since
+// omega.y - ||y||^2/2 = (||omega||^2 - ||y - omega||^2)/2 <= ||omega||^2/2.
+constexpr float KSHIFT_HEADROOM = 60.0f;
+
+// ---- generic SIMT kernels (any supported shape, fp32 or bf16 storage) ----
+favor_status simt_feature_map(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st);
+favor_status simt_bidir(const Handle& h, const void* q, const void* k, const void* v, void* out,
+                        int B, int L, cudaStream_t st);
+favor_status simt_causal(const Handle& h, const void* q, const void* k, const void* v, void* out,
+                         int B, int L, cudaStream_t st);
+
+// ---- tensor-core (tcgen05) kernels: bf16, d = dv = 64, m = 256 ----
+bool tc_supported(const Handle& h);
+favor_status tc_feature_map(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st);
+favor_status tc_bidir(const Handle& h, const void* q, const void* k, const void* v, void* out,
+                      int B, int L, cudaStream_t st);
+favor_status tc_causal(const Handle& h, const void* q, const void* k, const void* v, void* out,
+                       int B, int L, cudaStream_t st);
+
+// ---- fixed-order combines of per-segment states (shared by both paths) ----
+favor_status launch_reduce_segments(const Handle& h, int BH, int n_seg, cudaStream_t st);
+favor_status launch_scan_segments(const Handle& h, int BH, int n_seg, cudaStream_t st);
+
+}  // namespace favor

@@ -1,0 +1,457 @@
+// Generic FAVOR+ kernels on the CUDA cores (FFMA), for every supported shape
+// and for fp32 storage.  fp32 storage computes everything in fp32 with the
+// accurate expf; bf16 storage reads bf16 and computes in fp32 too.
+//
+// Feature conventions inside attention (all shifts cancel between numerator
+// and denominator, so the output equals Eq. 4 / Eq. 11 of Rethinking Attention
+// with Performers up to rounding):
+//   key   features  exp(s*p - s^2||k||^2/2 - kappa_h)   (positive)  | max(s*p, 0) (ReLU)
+//   query features  exp(s*(p - max_r p_r))               (positive)  | max(s*p, 0) (ReLU)
+// where p = omega_r . k (or q).  The query shift drops the -||x||^2/2 term and
+// the m^-1/2 factor, both common to a query row; the key shift kappa_h is
+// common to a head.  favor_feature_map returns the unshifted definition.
+#include <cmath>
+
+#include "favor_internal.h"
+
+namespace favor {
+namespace {
+
+template <typename T> __device__ __forceinline__ float ldf(const T* p);
+template <> __device__ __forceinline__ float ldf<float>(const float* p) { return *p; }
+template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+template <typename T> __device__ __forceinline__ void stf(T* p, float x);
+template <> __device__ __forceinline__ void stf<float>(float* p, float x) { *p = x; }
+template <> __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+constexpr int kTokTile = 32;  // tokens staged per shared-memory tile in the state/causal kernels
+
+// ---------------------------------------------------------------- feature map
+// grid (ceil(L/16), B*H), 256 threads.  Output phi[bh, i, r] = plain definition.
+template <typename T, int KIND>
+__global__ void __launch_bounds__(256) k_feature_map(const T* __restrict__ x, T* __restrict__ phi,
+                                                     const float* __restrict__ omega, int H, int L,
+                                                     int m, int d, float s) {
+    constexpr int TQ = 16;
+    extern __shared__ float sm[];
+    float* xs = sm;                 // [TQ][d]
+    float* nrm = xs + TQ * d;       // [TQ]
+    const int bh = blockIdx.y, h = bh % H;
+    const int i0 = blockIdx.x * TQ;
+    const int nq = min(TQ, L - i0);
+    const T* xb = x + ((size_t)bh * L + i0) * d;
+    for (int idx = threadIdx.x; idx < nq * d; idx += blockDim.x) xs[idx] = ldf(xb + idx);
+    __syncthreads();
+    if (threadIdx.x < nq) {
+        float a = 0.f;
+        for (int c = 0; c < d; ++c) a = fmaf(xs[threadIdx.x * d + c], xs[threadIdx.x * d + c], a);
+        nrm[threadIdx.x] = a;
+    }
+    __syncthreads();
+    const float inv_sqrt_m = rsqrtf((float)m);
+    const float* om = omega + (size_t)h * m * d;
+    T* out = phi + ((size_t)bh * L + i0) * m;
+    for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) {
+        const int i = idx / m, r = idx - i * m;
+        float p = 0.f;
+        for (int c = 0; c < d; ++c) p = fmaf(__ldg(om + r * d + c), xs[i * d + c], p);
+        float f;
+        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) f = expf(s * p - 0.5f * s * s * nrm[i]) * inv_sqrt_m;
+        else f = fmaxf(s * p, 0.f) * inv_sqrt_m;
+        stf(out + idx, f);
+    }
+}
+
+// ------------------------------------------------------- per-segment key state
+// grid (n_seg, B*H), m threads.  Thread r accumulates S[r, 0:dv] and z[r] over
+// its segment's keys and writes them to part[(bh*n_seg + seg)][r][0:dv+1].
+template <typename T, int KIND, int DV>
+__global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, const T* __restrict__ v,
+                                                       const float* __restrict__ omega,
+                                                       const float* __restrict__ kshift, float* __restrict__ part,
+                                                       int H, int L, int m, int d, float s, int seg_len, int n_seg) {
+    extern __shared__ float sm[];
+    const int dp = d + 1;
+    float* oms = sm;                       // [m][d+1]
+    float* ks = oms + m * dp;              // [kTokTile][d]
+    float* vs = ks + kTokTile * d;         // [kTokTile][DV]
+    float* nrm = vs + kTokTile * DV;       // [kTokTile]
+    const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int r = threadIdx.x;
+    for (int idx = threadIdx.x; idx < m * d; idx += blockDim.x)
+        oms[(idx / d) * dp + idx % d] = omega[(size_t)h * m * d + idx];
+    const float kap = kshift[h];
+    float S[DV];
+#pragma unroll
+    for (int e = 0; e < DV; ++e) S[e] = 0.f;
+    float z = 0.f;
+    const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    for (int t0 = j0; t0 < j1; t0 += kTokTile) {
+        const int nt = min(kTokTile, j1 - t0);
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x)
+            ks[idx] = ldf(k + ((size_t)bh * L + t0) * d + idx);
+        for (int idx = threadIdx.x; idx < nt * DV; idx += blockDim.x)
+            vs[idx] = ldf(v + ((size_t)bh * L + t0) * DV + idx);
+        __syncthreads();
+        if (threadIdx.x < nt) {
+            float a = 0.f;
+            for (int c = 0; c < d; ++c) a = fmaf(ks[threadIdx.x * d + c], ks[threadIdx.x * d + c], a);
+            nrm[threadIdx.x] = a;
+        }
+        __syncthreads();
+        for (int j = 0; j < nt; ++j) {
+            float p = 0.f;
+            for (int c = 0; c < d; ++c) p = fmaf(oms[r * dp + c], ks[j * d + c], p);
+            float f;
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) f = expf(s * p - 0.5f * s * s * nrm[j] - kap);
+            else f = fmaxf(s * p, 0.f);
+#pragma unroll
+            for (int e = 0; e < DV; ++e) S[e] = fmaf(f, vs[j * DV + e], S[e]);
+            z += f;
+        }
+    }
+    float* o = part + ((size_t)bh * n_seg + seg) * m * (DV + 1) + (size_t)r * (DV + 1);
+#pragma unroll
+    for (int e = 0; e < DV; ++e) o[e] = S[e];
+    o[DV] = z;
+}
+
+// ------------------------------------------------- fixed-order segment combines
+// Bidirectional: state[bh] = sum over seg (in order) of part[bh, seg].
+__global__ void k_reduce_segments(const float* __restrict__ part, float* __restrict__ state, int n_seg, int n) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float* p = part + (size_t)bh * n_seg * n + i;
+    float a = 0.f;
+    for (int sg = 0; sg < n_seg; ++sg) a += p[(size_t)sg * n];
+    state[(size_t)bh * n + i] = a;
+}
+
+// Causal: part[bh, seg] <- sum of part[bh, 0..seg-1] (exclusive prefix, in order).
+__global__ void k_scan_segments(float* __restrict__ part, int n_seg, int n) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float* p = part + (size_t)bh * n_seg * n + i;
+    float run = 0.f;
+    for (int sg = 0; sg < n_seg; ++sg) {
+        const float t = p[(size_t)sg * n];
+        p[(size_t)sg * n] = run;
+        run += t;
+    }
+}
+
+// ------------------------------------------------------- bidirectional readout
+// grid (ceil(L/16), B*H), 256 threads.  out_i = phi(q_i)^T S / phi(q_i)^T z.
+template <typename T, int KIND>
+__global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const float* __restrict__ state,
+                                                 const float* __restrict__ omega, T* __restrict__ out,
+                                                 int H, int L, int m, int d, int dv, float s) {
+    constexpr int TQ = 16;
+    extern __shared__ float sm[];
+    const int sw = dv + 1;
+    float* sts = sm;                 // [m][dv+1]
+    float* fq = sts + m * sw;        // [TQ][m]
+    float* xs = fq + TQ * m;         // [TQ][d]
+    float* num = xs + TQ * d;        // [TQ][dv+1]
+    float* rmax = num + TQ * sw;     // [TQ]
+    const int bh = blockIdx.y, h = bh % H;
+    const int i0 = blockIdx.x * TQ;
+    const int nq = min(TQ, L - i0);
+    const float* stg = state + (size_t)bh * m * sw;
+    for (int idx = threadIdx.x; idx < m * sw; idx += blockDim.x) sts[idx] = stg[idx];
+    for (int idx = threadIdx.x; idx < nq * d; idx += blockDim.x) xs[idx] = ldf(q + ((size_t)bh * L + i0) * d + idx);
+    __syncthreads();
+    const float* om = omega + (size_t)h * m * d;
+    for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) {
+        const int i = idx / m, r = idx - i * m;
+        float p = 0.f;
+        for (int c = 0; c < d; ++c) p = fmaf(__ldg(om + r * d + c), xs[i * d + c], p);
+        fq[idx] = s * p;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+        for (int i = warp; i < nq; i += blockDim.x / 32) {
+            float mx = -INFINITY;
+            for (int r = lane; r < m; r += 32) mx = fmaxf(mx, fq[i * m + r]);
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) rmax[i] = mx;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) fq[idx] = expf(fq[idx] - rmax[idx / m]);
+    } else {
+        for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) fq[idx] = fmaxf(fq[idx], 0.f);
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < nq * sw; idx += blockDim.x) {
+        const int i = idx / sw, e = idx - i * sw;
+        float a = 0.f;
+        for (int r = 0; r < m; ++r) a = fmaf(fq[i * m + r], sts[r * sw + e], a);
+        num[idx] = a;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < nq * dv; idx += blockDim.x) {
+        const int i = idx / dv, e = idx - i * dv;
+        const float den = num[i * sw + dv];
+        stf(out + ((size_t)bh * L + i0) * dv + idx, den != 0.f ? num[i * sw + e] / den : 0.f);
+    }
+}
+
+// --------------------------------------------------------- causal, per segment
+// grid (n_seg, B*H), m threads.  Thread r holds S[r, :], z[r] starting from the
+// segment's exclusive prefix state and walks the segment token by token:
+// S += phi(k_i) v_i^T, z += phi(k_i) (inclusive of i), then
+// out_i = phi(q_i)^T S / phi(q_i)^T z, the sum over r done across the block.
+template <typename T, int KIND, int DV>
+__global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q, const T* __restrict__ k,
+                                                        const T* __restrict__ v, const float* __restrict__ omega,
+                                                        const float* __restrict__ kshift,
+                                                        const float* __restrict__ prefix, T* __restrict__ out,
+                                                        int H, int L, int m, int d, float s, int seg_len, int n_seg) {
+    extern __shared__ float sm[];
+    const int dp = d + 1;
+    const int nwarps = (m + 31) / 32;
+    float* oms = sm;                        // [m][d+1]
+    float* qs = oms + m * dp;               // [kTokTile][d]
+    float* ks = qs + kTokTile * d;          // [kTokTile][d]
+    float* vs = ks + kTokTile * d;          // [kTokTile][DV]
+    float* nrm = vs + kTokTile * DV;        // [kTokTile]
+    float* red = nrm + kTokTile;            // [nwarps][DV+1]
+    float* wmax = red + nwarps * (DV + 1);  // [nwarps]
+    const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int r = threadIdx.x, warp = r / 32, lane = r % 32;
+    for (int idx = threadIdx.x; idx < m * d; idx += blockDim.x)
+        oms[(idx / d) * dp + idx % d] = omega[(size_t)h * m * d + idx];
+    const float kap = kshift[h];
+    float S[DV];
+    const float* pre = prefix + ((size_t)bh * n_seg + seg) * m * (DV + 1) + (size_t)r * (DV + 1);
+#pragma unroll
+    for (int e = 0; e < DV; ++e) S[e] = pre[e];
+    float z = pre[DV];
+    // m is a multiple of 16, so only a last warp of 16 lanes can be partial.
+    const int width = (m % 32 != 0 && warp == nwarps - 1) ? 16 : 32;
+    const unsigned full = width == 32 ? 0xffffffffu : 0x0000ffffu;
+    const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    for (int t0 = j0; t0 < j1; t0 += kTokTile) {
+        const int nt = min(kTokTile, j1 - t0);
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
+            qs[idx] = ldf(q + ((size_t)bh * L + t0) * d + idx);
+            ks[idx] = ldf(k + ((size_t)bh * L + t0) * d + idx);
+        }
+        for (int idx = threadIdx.x; idx < nt * DV; idx += blockDim.x)
+            vs[idx] = ldf(v + ((size_t)bh * L + t0) * DV + idx);
+        __syncthreads();
+        if (threadIdx.x < nt) {
+            float a = 0.f;
+            for (int c = 0; c < d; ++c) a = fmaf(ks[threadIdx.x * d + c], ks[threadIdx.x * d + c], a);
+            nrm[threadIdx.x] = a;
+        }
+        __syncthreads();
+        for (int j = 0; j < nt; ++j) {
+            float pk = 0.f, pq = 0.f;
+            for (int c = 0; c < d; ++c) {
+                pk = fmaf(oms[r * dp + c], ks[j * d + c], pk);
+                pq = fmaf(oms[r * dp + c], qs[j * d + c], pq);
+            }
+            float fk;
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) fk = expf(s * pk - 0.5f * s * s * nrm[j] - kap);
+            else fk = fmaxf(s * pk, 0.f);
+#pragma unroll
+            for (int e = 0; e < DV; ++e) S[e] = fmaf(fk, vs[j * DV + e], S[e]);
+            z += fk;
+            float fq;
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                float mx = s * pq;
+                for (int o = width / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(full, mx, o));
+                if (lane == 0) wmax[warp] = mx;
+                __syncthreads();
+                mx = wmax[0];
+                for (int w = 1; w < nwarps; ++w) mx = fmaxf(mx, wmax[w]);
+                fq = expf(s * pq - mx);
+            } else {
+                fq = fmaxf(s * pq, 0.f);
+            }
+            // sum over r of fq * [S | z]: warp shuffles, then across warps in smem.
+#pragma unroll
+            for (int e = 0; e <= DV; ++e) {
+                float a = fq * (e < DV ? S[e] : z);
+                for (int o = width / 2; o > 0; o >>= 1) a += __shfl_xor_sync(full, a, o);
+                if (lane == 0) red[warp * (DV + 1) + e] = a;
+            }
+            __syncthreads();
+            if (threadIdx.x < DV) {
+                float a = 0.f, den = 0.f;
+                for (int w = 0; w < nwarps; ++w) {
+                    a += red[w * (DV + 1) + threadIdx.x];
+                    den += red[w * (DV + 1) + DV];
+                }
+                stf(out + ((size_t)bh * L + t0 + j) * DV + threadIdx.x, den != 0.f ? a / den : 0.f);
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <typename K>
+static void set_smem(K kern, size_t bytes) {
+    if (bytes > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <typename T, int KIND>
+favor_status feature_map_t(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st) {
+    const size_t smem = (16 * h.d + 16) * sizeof(float);
+    dim3 grid((L + 15) / 16, B * h.H);
+    ProfScope ps(h, PROF_FEATURE_MAP, st);
+    k_feature_map<T, KIND><<<grid, 256, smem, st>>>((const T*)x, (T*)phi, h.omega_f32, h.H, L, h.m, h.d, h.s);
+    count_launch();
+    return check_launch("feature map kernel");
+}
+
+template <typename T, int KIND, int DV>
+favor_status state_t(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan& p,
+                     cudaStream_t st) {
+    const size_t smem = (size_t)(h.m * (h.d + 1) + kTokTile * h.d + kTokTile * DV + kTokTile) * sizeof(float);
+    auto kern = k_segment_state<T, KIND, DV>;
+    set_smem(kern, smem);
+    dim3 grid(p.n_seg, BH);
+    ProfScope ps(h, PROF_STATE, st);
+    kern<<<grid, h.m, smem, st>>>((const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial, h.H, L, h.m,
+                                  h.d, h.s, p.seg_tiles * 128, p.n_seg);
+    count_launch();
+    return check_launch("segment state kernel");
+}
+
+template <typename T, int KIND>
+favor_status readout_t(const Handle& h, const void* q, void* out, int BH, int L, cudaStream_t st) {
+    const int sw = h.dv + 1;
+    const size_t smem = (size_t)(h.m * sw + 16 * h.m + 16 * h.d + 16 * sw + 16) * sizeof(float);
+    auto kern = k_readout<T, KIND>;
+    set_smem(kern, smem);
+    dim3 grid((L + 15) / 16, BH);
+    ProfScope ps(h, PROF_READOUT, st);
+    kern<<<grid, 256, smem, st>>>((const T*)q, h.ws_state, h.omega_f32, (T*)out, h.H, L, h.m, h.d, h.dv, h.s);
+    count_launch();
+    return check_launch("readout kernel");
+}
+
+template <typename T, int KIND, int DV>
+favor_status causal_t(const Handle& h, const void* q, const void* k, const void* v, void* out, int BH, int L,
+                      const SegPlan& p, cudaStream_t st) {
+    const int nwarps = (h.m + 31) / 32;
+    const size_t smem = (size_t)(h.m * (h.d + 1) + 2 * kTokTile * h.d + kTokTile * DV + kTokTile +
+                                 nwarps * (DV + 1) + nwarps) * sizeof(float);
+    auto kern = k_causal_segment<T, KIND, DV>;
+    set_smem(kern, smem);
+    dim3 grid(p.n_seg, BH);
+    ProfScope ps(h, PROF_CAUSAL, st);
+    kern<<<grid, h.m, smem, st>>>((const T*)q, (const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial,
+                                  (T*)out, h.H, L, h.m, h.d, h.s, p.seg_tiles * 128, p.n_seg);
+    count_launch();
+    return check_launch("causal segment kernel");
+}
+
+// Runtime (dtype, kind, dv) -> template instantiation.
+template <template <typename, int, int> class F, typename... A>
+favor_status dispatch3(const Handle& h, A... a) {
+#define FAVOR_DV_CASES(T, KIND)                                   \
+    switch (h.dv) {                                               \
+        case 16: return F<T, KIND, 16>::run(h, a...);             \
+        case 32: return F<T, KIND, 32>::run(h, a...);             \
+        case 64: return F<T, KIND, 64>::run(h, a...);             \
+        case 128: return F<T, KIND, 128>::run(h, a...);           \
+    }
+    if (h.dtype == FAVOR_DTYPE_F32) {
+        if (h.kind == FAVOR_KERNEL_SOFTMAX_POS) { FAVOR_DV_CASES(float, FAVOR_KERNEL_SOFTMAX_POS) }
+        else { FAVOR_DV_CASES(float, FAVOR_KERNEL_RELU) }
+    } else {
+        if (h.kind == FAVOR_KERNEL_SOFTMAX_POS) { FAVOR_DV_CASES(__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS) }
+        else { FAVOR_DV_CASES(__nv_bfloat16, FAVOR_KERNEL_RELU) }
+    }
+#undef FAVOR_DV_CASES
+    return set_error(FAVOR_ERR_UNSUPPORTED, "unsupported dv=%d", h.dv);
+}
+
+template <typename T, int KIND, int DV>
+struct StateF {
+    static favor_status run(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan* p,
+                            cudaStream_t st) {
+        return state_t<T, KIND, DV>(h, k, v, BH, L, *p, st);
+    }
+};
+
+template <typename T, int KIND, int DV>
+struct CausalF {
+    static favor_status run(const Handle& h, const void* q, const void* k, const void* v, void* out, int BH,
+                            int L, const SegPlan* p, cudaStream_t st) {
+        return causal_t<T, KIND, DV>(h, q, k, v, out, BH, L, *p, st);
+    }
+};
+
+}  // namespace
+
+favor_status launch_reduce_segments(const Handle& h, int BH, int n_seg, cudaStream_t st) {
+    const int n = h.m * (h.dv + 1);
+    dim3 grid((n + 255) / 256, BH);
+    ProfScope ps(h, PROF_COMBINE, st);
+    k_reduce_segments<<<grid, 256, 0, st>>>(h.ws_partial, h.ws_state, n_seg, n);
+    count_launch();
+    return check_launch("segment reduce kernel");
+}
+
+favor_status launch_scan_segments(const Handle& h, int BH, int n_seg, cudaStream_t st) {
+    const int n = h.m * (h.dv + 1);
+    dim3 grid((n + 255) / 256, BH);
+    ProfScope ps(h, PROF_COMBINE, st);
+    k_scan_segments<<<grid, 256, 0, st>>>(h.ws_partial, n_seg, n);
+    count_launch();
+    return check_launch("segment scan kernel");
+}
+
+favor_status simt_feature_map(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st) {
+    if (h.dtype == FAVOR_DTYPE_F32)
+        return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? feature_map_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, x, phi, B, L, st)
+                                                  : feature_map_t<float, FAVOR_KERNEL_RELU>(h, x, phi, B, L, st);
+    return h.kind == FAVOR_KERNEL_SOFTMAX_POS
+               ? feature_map_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, x, phi, B, L, st)
+               : feature_map_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, x, phi, B, L, st);
+}
+
+favor_status simt_bidir(const Handle& h, const void* q, const void* k, const void* v, void* out, int B, int L,
+                        cudaStream_t st) {
+    const int BH = B * h.H;
+    SegPlan p = plan_segments(BH, L, h.num_sms);
+    favor_status s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, st);
+    if (s != FAVOR_OK) return s;
+    s = launch_reduce_segments(h, BH, p.n_seg, st);
+    if (s != FAVOR_OK) return s;
+    if (h.dtype == FAVOR_DTYPE_F32)
+        return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
+                                                  : readout_t<float, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
+    return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
+                                              : readout_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
+}
+
+favor_status simt_causal(const Handle& h, const void* q, const void* k, const void* v, void* out, int B, int L,
+                         cudaStream_t st) {
+    const int BH = B * h.H;
+    SegPlan p = plan_segments(BH, L, h.num_sms);
+    favor_status s = FAVOR_OK;
+    if (p.n_seg > 1) {
+        s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, st);
+        if (s != FAVOR_OK) return s;
+        s = launch_scan_segments(h, BH, p.n_seg, st);
+    } else {
+        s = cudaMemsetAsync(h.ws_partial, 0, (size_t)BH * h.m * (h.dv + 1) * sizeof(float), st) == cudaSuccess
+                ? FAVOR_OK
+                : set_error(FAVOR_ERR_CUDA, "cudaMemsetAsync failed");
+    }
+    if (s != FAVOR_OK) return s;
+    return dispatch3<CausalF>(h, q, k, v, out, BH, L, (const SegPlan*)&p, st);
+}
+
+}  // namespace favor

@@ -1,0 +1,243 @@
+"""ctypes binding of the FAVOR+ C ABI (include/favor.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libfavor.so.  The functions keep the C names; tensors may be torch
+CUDA tensors (their data_ptr() is passed) or raw integer device addresses.
+The stream defaults to torch's current stream on the tensor's device.
+
+If the shared library has not been built, importing works but the first call
+raises ``FavorLibraryMissing`` -- there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "FAVOR_OK", "FAVOR_ERR_INVALID_ARG", "FAVOR_ERR_UNSUPPORTED", "FAVOR_ERR_NOMEM", "FAVOR_ERR_CUDA",
+    "FAVOR_KERNEL_SOFTMAX_POS", "FAVOR_KERNEL_RELU", "FAVOR_DTYPE_F32", "FAVOR_DTYPE_BF16",
+    "FavorError", "FavorLibraryMissing", "lib", "lib_path",
+    "favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal", "favor_destroy",
+    "favor_status_str", "favor_last_error", "favor_launch_count", "Favor", "EXPORTED_SYMBOLS",
+    "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
+    "favor_profile_name",
+]
+
+FAVOR_OK, FAVOR_ERR_INVALID_ARG, FAVOR_ERR_UNSUPPORTED, FAVOR_ERR_NOMEM, FAVOR_ERR_CUDA = range(5)
+FAVOR_KERNEL_SOFTMAX_POS, FAVOR_KERNEL_RELU = 0, 1
+FAVOR_DTYPE_F32, FAVOR_DTYPE_BF16 = 0, 1
+KIND_CODES = {"softmax_pos": FAVOR_KERNEL_SOFTMAX_POS, "relu": FAVOR_KERNEL_RELU}
+DTYPE_CODES = {"f32": FAVOR_DTYPE_F32, "bf16": FAVOR_DTYPE_BF16}
+
+EXPORTED_SYMBOLS = ("favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal",
+                    "favor_destroy", "favor_status_str", "favor_last_error", "favor_launch_count",
+                    "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
+                    "favor_profile_name")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "_lib", "libfavor.so")
+
+
+class FavorLibraryMissing(RuntimeError):
+    pass
+
+
+class FavorError(RuntimeError):
+    def __init__(self, status: int, fn: str, msg: str):
+        super().__init__(f"{fn} -> {favor_status_str(status)}: {msg}")
+        self.status = status
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfavor.so once; raise if it is missing."""
+    global _LIB
+    if _LIB is None:
+        p = lib_path()
+        if not os.path.exists(p):
+            raise FavorLibraryMissing(f"{p} is not built; run random_feature_gb300.build.build() first")
+        L = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.favor_create.argtypes = [ctypes.POINTER(vp), i, i, i, i, i, i, ctypes.POINTER(ctypes.c_float), f, i, i]
+        L.favor_feature_map.argtypes = [vp, vp, vp, i, i, vp]
+        L.favor_attn_bidir.argtypes = [vp, vp, vp, vp, vp, i, i, vp]
+        L.favor_attn_causal.argtypes = [vp, vp, vp, vp, vp, i, i, vp]
+        L.favor_destroy.argtypes = [vp]
+        for fn in ("favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal", "favor_destroy"):
+            getattr(L, fn).restype = ctypes.c_int
+        L.favor_status_str.argtypes = [i]
+        L.favor_status_str.restype = ctypes.c_char_p
+        L.favor_last_error.argtypes = []
+        L.favor_last_error.restype = ctypes.c_char_p
+        L.favor_launch_count.argtypes = []
+        L.favor_launch_count.restype = ctypes.c_ulonglong
+        L.favor_profile_enable.argtypes = [vp, i]
+        L.favor_profile_reset.argtypes = [vp]
+        L.favor_profile_read.argtypes = [vp, i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_ulonglong)]
+        for fn in ("favor_profile_enable", "favor_profile_reset", "favor_profile_read"):
+            getattr(L, fn).restype = ctypes.c_int
+        L.favor_profile_slots.argtypes = []
+        L.favor_profile_slots.restype = i
+        L.favor_profile_name.argtypes = [i]
+        L.favor_profile_name.restype = ctypes.c_char_p
+        _LIB = L
+    return _LIB
+
+
+def favor_status_str(status: int) -> str:
+    return lib().favor_status_str(int(status)).decode()
+
+
+def favor_last_error() -> str:
+    return lib().favor_last_error().decode()
+
+
+def favor_launch_count() -> int:
+    return int(lib().favor_launch_count())
+
+
+def _check(status: int, fn: str) -> None:
+    if status != FAVOR_OK:
+        raise FavorError(status, fn, favor_last_error())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream, like):
+    if stream is None:
+        import torch
+        dev = like.device if hasattr(like, "device") else None
+        return torch.cuda.current_stream(dev).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def favor_create(H, m, d, dv, kind, dtype, omega, data_scale, max_B, max_L) -> int:
+    """Create a handle; ``omega`` is a host float32 array [H, m, d].  Returns the handle (int)."""
+    kind = KIND_CODES.get(kind, kind)
+    dtype = DTYPE_CODES.get(dtype, dtype)
+    om = np.ascontiguousarray(omega, dtype=np.float32)
+    if om.shape != (H, m, d):
+        raise ValueError(f"omega must have shape {(H, m, d)}, got {om.shape}")
+    h = ctypes.c_void_p()
+    st = lib().favor_create(ctypes.byref(h), int(H), int(m), int(d), int(dv), int(kind), int(dtype),
+                            om.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), float(data_scale),
+                            int(max_B), int(max_L))
+    _check(st, "favor_create")
+    return h.value
+
+
+def favor_feature_map(h, x, phi, B, L, stream=None) -> None:
+    _check(lib().favor_feature_map(h, _ptr(x), _ptr(phi), int(B), int(L), _stream(stream, x)), "favor_feature_map")
+
+
+def favor_attn_bidir(h, q, k, v, out, B, L, stream=None) -> None:
+    _check(lib().favor_attn_bidir(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), int(B), int(L), _stream(stream, q)),
+           "favor_attn_bidir")
+
+
+def favor_attn_causal(h, q, k, v, out, B, L, stream=None) -> None:
+    _check(lib().favor_attn_causal(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), int(B), int(L), _stream(stream, q)),
+           "favor_attn_causal")
+
+
+def favor_destroy(h) -> None:
+    _check(lib().favor_destroy(h), "favor_destroy")
+
+
+def favor_profile_enable(h, enable=True) -> None:
+    _check(lib().favor_profile_enable(h, 1 if enable else 0), "favor_profile_enable")
+
+
+def favor_profile_reset(h) -> None:
+    _check(lib().favor_profile_reset(h), "favor_profile_reset")
+
+
+def favor_profile_read(h, slot):
+    """(total device ms, launches) recorded for one kernel slot (synchronises)."""
+    ms = ctypes.c_double()
+    n = ctypes.c_ulonglong()
+    _check(lib().favor_profile_read(h, int(slot), ctypes.byref(ms), ctypes.byref(n)), "favor_profile_read")
+    return ms.value, n.value
+
+
+def favor_profile_slots() -> int:
+    return int(lib().favor_profile_slots())
+
+
+def favor_profile_name(slot) -> str:
+    return lib().favor_profile_name(int(slot)).decode()
+
+
+class Favor:
+    """Owns one handle; checks torch tensor shapes/dtypes before calling the C ABI."""
+
+    def __init__(self, H, m, d, dv, kind, dtype, omega, data_scale, max_B, max_L):
+        self.H, self.m, self.d, self.dv = H, m, d, dv
+        self.kind, self.dtype = kind, dtype
+        self.max_B, self.max_L = max_B, max_L
+        self.handle = favor_create(H, m, d, dv, kind, dtype, omega, data_scale, max_B, max_L)
+
+    def _tdtype(self):
+        import torch
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    def _chk(self, t, B, L, w, name):
+        if tuple(t.shape) != (B, self.H, L, w) or t.dtype != self._tdtype() or not t.is_cuda \
+                or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous CUDA {self._tdtype()} [{B},{self.H},{L},{w}], "
+                             f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+    def _new(self, like, B, L, w, out):
+        import torch
+        if out is None:
+            out = torch.empty((B, self.H, L, w), dtype=self._tdtype(), device=like.device)
+        self._chk(out, B, L, w, "out")
+        return out
+
+    def feature_map(self, x, out=None, stream=None):
+        B, _, L, _ = x.shape
+        self._chk(x, B, L, self.d, "x")
+        out = self._new(x, B, L, self.m, out)
+        favor_feature_map(self.handle, x, out, B, L, stream)
+        return out
+
+    def attn(self, q, k, v, causal=False, out=None, stream=None):
+        B, _, L, _ = q.shape
+        self._chk(q, B, L, self.d, "q")
+        self._chk(k, B, L, self.d, "k")
+        self._chk(v, B, L, self.dv, "v")
+        out = self._new(q, B, L, self.dv, out)
+        (favor_attn_causal if causal else favor_attn_bidir)(self.handle, q, k, v, out, B, L, stream)
+        return out
+
+    def close(self):
+        if self.handle:
+            favor_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

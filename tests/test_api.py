@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/favor.h declares, and rejects bad arguments before
+touching a device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import random_feature_gb300 as R
+from random_feature_gb300 import build as _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built_library():
+    _build.build()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "favor.h")).read()
+    return set(re.findall(r"FAVOR_API\s+[\w\s\*]+?\b(favor_\w+)\s*\(", text))
+
+
+def test_library_builds_and_exports_header_symbols():
+    declared = _declared_symbols()
+    assert {"favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal",
+            "favor_destroy"} <= declared
+    L = R.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+    assert declared == set(R.EXPORTED_SYMBOLS)
+
+
+def test_status_strings():
+    assert R.favor_status_str(R.FAVOR_OK) == "FAVOR_OK"
+    assert R.favor_status_str(R.FAVOR_ERR_UNSUPPORTED) == "FAVOR_ERR_UNSUPPORTED"
+    assert R.favor_status_str(99) == "FAVOR_ERR_UNKNOWN"
+
+
+def _raw_create(H=1, m=32, d=16, dv=16, kind=0, dtype=0, omega=True, s=1.0, max_B=1, max_L=64, out=True):
+    L = R.lib()
+    h = ctypes.c_void_p(12345)
+    om = np.zeros((H, m, d), np.float32) if omega else None
+    ptr = om.ctypes.data_as(ctypes.POINTER(ctypes.c_float)) if omega else None
+    st = L.favor_create(ctypes.byref(h) if out else None, H, m, d, dv, kind, dtype, ptr, s, max_B, max_L)
+    return st, h.value
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(out=False), R.FAVOR_ERR_INVALID_ARG),
+    (dict(omega=False), R.FAVOR_ERR_INVALID_ARG),
+    (dict(H=0), R.FAVOR_ERR_INVALID_ARG),
+    (dict(max_L=0), R.FAVOR_ERR_INVALID_ARG),
+    (dict(kind=7), R.FAVOR_ERR_INVALID_ARG),
+    (dict(dtype=5), R.FAVOR_ERR_INVALID_ARG),
+    (dict(s=0.0), R.FAVOR_ERR_INVALID_ARG),
+    (dict(s=float("nan")), R.FAVOR_ERR_INVALID_ARG),
+    (dict(d=48), R.FAVOR_ERR_UNSUPPORTED),
+    (dict(dv=8), R.FAVOR_ERR_UNSUPPORTED),
+    (dict(m=24), R.FAVOR_ERR_UNSUPPORTED),
+    (dict(m=512), R.FAVOR_ERR_UNSUPPORTED),
+])
+def test_create_rejects_bad_arguments(kw, want):
+    st, h = _raw_create(**kw)
+    assert st == want, R.favor_last_error()
+    assert R.favor_last_error()
+    if kw.get("out", True):
+        assert h is None          # *out is cleared on failure
+
+
+def test_calls_reject_null_handle():
+    L = R.lib()
+    assert L.favor_attn_bidir(None, 1, 1, 1, 1, 1, 1, None) == R.FAVOR_ERR_INVALID_ARG
+    assert L.favor_attn_causal(None, 1, 1, 1, 1, 1, 1, None) == R.FAVOR_ERR_INVALID_ARG
+    assert L.favor_feature_map(None, 1, 1, 1, 1, None) == R.FAVOR_ERR_INVALID_ARG
+    assert L.favor_destroy(None) == R.FAVOR_OK
+
+
+def test_launch_counter_is_monotone():
+    a = R.favor_launch_count()
+    assert R.favor_launch_count() >= a >= 0
+
+
+def test_python_binding_has_c_names():
+    for name in R.EXPORTED_SYMBOLS:
+        assert callable(getattr(R, name))

@@ -1,0 +1,151 @@
+"""GPU parity: the CUDA library (through its C ABI) against the float64 oracle.
+
+Tolerance: row-normwise max relative error (oracle.row_rel_err) <= 1e-4 for
+fp32 storage and <= 2e-2 for bf16 storage with fp32 accumulation.  Inputs are
+the seeded synthetic workloads; bf16 inputs and omega are bf16 values, so
+both sides see identical numbers.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from synth import CONFIGS, make_workload
+from _util import TOL, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, mode, kind, omega, q, k, v, seed_note=""):
+    import torch
+    from random_feature_gb300 import Favor
+    with Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, omega, w.data_scale, w.B, w.L) as f:
+        qd, kd, vd = (to_dev(a, w.dtype) for a in (q, k, v))
+        out = f.attn(qd, kd, vd, causal=(mode == "causal"))
+        torch.cuda.synchronize()
+        return to_host(out)
+
+
+def _oracle(mode, kind, q, k, v, omega, s):
+    fn = O.favor_causal if mode == "causal" else O.favor_bidir
+    return fn(q, k, v, omega, s, kind)
+
+
+def _check(w, mode, kind, seed=0):
+    omega, q, k, v = make_workload(w, seed)
+    got = _run(w, mode, kind, omega, q, k, v)
+    ref = _oracle(mode, kind, q, k, v, omega, w.data_scale)
+    assert np.isfinite(got).all()
+    err = O.row_rel_err(got, ref)
+    assert err <= TOL[w.dtype], f"{w.name} {mode} {kind}: row-normwise error {err:.3e}"
+    return err
+
+
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+def test_tiny_f32(mode):
+    _check(CONFIGS["tiny_f32"], mode, "softmax_pos")
+
+
+@pytest.mark.parametrize("m", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("ortho", [True, False])
+def test_approx_f32(m, ortho):
+    _check(CONFIGS["approx_f32"].replace(m=m, ortho=ortho), "bidir", "softmax_pos")
+
+
+def test_approx_f32_error_vs_softmax_falls_with_m():
+    """Performer §4.2 / Fig. 4 shape on the device path: error of the FAVOR+
+    output against exact softmax attention decreases as m grows."""
+    base = CONFIGS["approx_f32"].replace(H=2)
+    errs = []
+    for m in (16, 256):
+        e = []
+        for seed in range(3):
+            w = base.replace(m=m)
+            omega, q, k, v = make_workload(w, seed)
+            got = _run(w, "bidir", "softmax_pos", omega, q, k, v)
+            exact = O.softmax_attention(q, k, v, w.data_scale)
+            e.append(np.mean((got - exact) ** 2))
+        errs.append(np.mean(e))
+    assert errs[1] < errs[0]
+
+
+def test_bidir_bf16_full():
+    _check(CONFIGS["bidir_bf16"], "bidir", "softmax_pos")
+
+
+def test_causal_bf16_full():
+    _check(CONFIGS["causal_bf16"], "causal", "softmax_pos")
+
+
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+@pytest.mark.parametrize("kind", ["softmax_pos", "relu"])
+def test_long_bf16_full(mode, kind):
+    _check(CONFIGS["long_bf16"], mode, kind)
+
+
+# ----------------------------------------------------------------- edge cases
+SMALL = CONFIGS["bidir_bf16"].replace(name="small", B=2, H=3, L=1000)
+
+
+@pytest.mark.parametrize("L", [1, 2, 127, 128, 129, 383, 1000])
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+@pytest.mark.parametrize("kind", ["softmax_pos", "relu"])
+def test_ragged_lengths_bf16(L, mode, kind):
+    _check(SMALL.replace(L=L), mode, kind)
+
+
+@pytest.mark.parametrize("d,dv,m", [(16, 16, 16), (32, 64, 48), (64, 32, 256), (128, 128, 128), (64, 64, 64)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+def test_other_shapes(d, dv, m, dtype, mode):
+    w = SMALL.replace(d=d, dv=dv, m=m, dtype=dtype, L=300, data_scale=d ** -0.25)
+    _check(w, mode, "softmax_pos")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", ["softmax_pos", "relu"])
+def test_feature_map(dtype, kind):
+    import torch
+    from random_feature_gb300 import Favor
+    w = SMALL.replace(dtype=dtype, L=777)
+    omega, q, k, v = make_workload(w, 3)
+    with Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, omega, w.data_scale, w.B, w.L) as f:
+        got = to_host(f.feature_map(to_dev(q, dtype)))
+    torch.cuda.synchronize()
+    ref = O.favor_feature_map(q, omega, w.data_scale, kind)
+    err = O.row_rel_err(got, ref)
+    assert err <= (1e-5 if dtype == "f32" else 8e-3), err
+
+
+def test_relu_zero_denominator_row_is_zero():
+    """Query features that are all zero (omega . x <= 0 for every r) give den = 0:
+    the output row is zeros on both sides."""
+    w = SMALL.replace(L=64, B=1, H=1, m=16, d=16, dv=16, dtype="f32", data_scale=1.0)
+    omega, q, k, v = make_workload(w, 0)
+    omega = np.abs(omega)
+    q[0, 0, 5] = -np.abs(q[0, 0, 5]) - 0.1
+    got = _run(w, "bidir", "relu", omega, q, k, v)
+    ref = _oracle("bidir", "relu", q, k, v, omega, 1.0)
+    assert np.all(ref[0, 0, 5] == 0) and np.all(got[0, 0, 5] == 0)
+    assert O.row_rel_err(got, ref) <= 1e-4
+
+
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+def test_deterministic(mode):
+    w = SMALL.replace(L=4096, B=1, H=4)
+    omega, q, k, v = make_workload(w, 1)
+    a = _run(w, mode, "softmax_pos", omega, q, k, v)
+    b = _run(w, mode, "softmax_pos", omega, q, k, v)
+    assert np.array_equal(a, b)
+
+
+def test_call_errors_on_device():
+    import torch
+    from random_feature_gb300 import Favor, FavorError, FAVOR_ERR_INVALID_ARG
+    w = SMALL
+    omega, q, k, v = make_workload(w.replace(L=16), 0)
+    with Favor(w.H, w.m, w.d, w.dv, "softmax_pos", "bf16", omega, w.data_scale, 1, 16) as f:
+        qd, kd, vd = (to_dev(a, "bf16") for a in (q, k, v))
+        with pytest.raises(FavorError) as e:
+            f.attn(qd, kd, vd)           # B=2 > max_B=1
+        assert e.value.status == FAVOR_ERR_INVALID_ARG
+    torch.cuda.synchronize()
