@@ -95,10 +95,10 @@ __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, 
         for (int idx = threadIdx.x; idx < nt * DV; idx += blockDim.x)
             vs[idx] = ldf(v + ((size_t)bh * L + t0) * DV + idx);
         __syncthreads();
-        if (threadIdx.x < nt) {
+        for (int j = threadIdx.x; j < nt; j += blockDim.x) {   // blockDim may be below kTokTile
             float a = 0.f;
-            for (int c = 0; c < d; ++c) a = fmaf(ks[threadIdx.x * d + c], ks[threadIdx.x * d + c], a);
-            nrm[threadIdx.x] = a;
+            for (int c = 0; c < d; ++c) a = fmaf(ks[j * d + c], ks[j * d + c], a);
+            nrm[j] = a;
         }
         __syncthreads();
         for (int j = 0; j < nt; ++j) {
@@ -246,10 +246,10 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
         for (int idx = threadIdx.x; idx < nt * DV; idx += blockDim.x)
             vs[idx] = ldf(v + ((size_t)bh * L + t0) * DV + idx);
         __syncthreads();
-        if (threadIdx.x < nt) {
+        for (int j = threadIdx.x; j < nt; j += blockDim.x) {   // blockDim may be below kTokTile
             float a = 0.f;
-            for (int c = 0; c < d; ++c) a = fmaf(ks[threadIdx.x * d + c], ks[threadIdx.x * d + c], a);
-            nrm[threadIdx.x] = a;
+            for (int c = 0; c < d; ++c) a = fmaf(ks[j * d + c], ks[j * d + c], a);
+            nrm[j] = a;
         }
         __syncthreads();
         for (int j = 0; j < nt; ++j) {
@@ -284,13 +284,13 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
                 if (lane == 0) red[warp * (DV + 1) + e] = a;
             }
             __syncthreads();
-            if (threadIdx.x < DV) {
+            for (int e = threadIdx.x; e < DV; e += blockDim.x) {   // blockDim = m may be below DV
                 float a = 0.f, den = 0.f;
                 for (int w = 0; w < nwarps; ++w) {
-                    a += red[w * (DV + 1) + threadIdx.x];
+                    a += red[w * (DV + 1) + e];
                     den += red[w * (DV + 1) + DV];
                 }
-                stf(out + ((size_t)bh * L + t0 + j) * DV + threadIdx.x, den != 0.f ? a / den : 0.f);
+                stf(out + ((size_t)bh * L + t0 + j) * DV + e, den != 0.f ? a / den : 0.f);
             }
             __syncthreads();
         }

@@ -53,8 +53,11 @@ def test_approx_f32(m, ortho):
 
 def test_approx_f32_error_vs_softmax_falls_with_m():
     """Performer §4.2 / Fig. 4 shape on the device path: error of the FAVOR+
-    output against exact softmax attention decreases as m grows."""
-    base = CONFIGS["approx_f32"].replace(H=2)
+    output against exact softmax attention decreases as m grows.  Inputs use
+    std 0.5 (before the d^-1/4 scale) so the Monte Carlo error is in its 1/m
+    regime; with std 1 the per-entry relative variance ~ exp(||x + y||^2) is
+    too heavy-tailed for m <= 256 to order reliably over three seeds."""
+    base = CONFIGS["approx_f32"].replace(H=2, std=0.5)
     errs = []
     for m in (16, 256):
         e = []
