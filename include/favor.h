@@ -137,6 +137,16 @@ FAVOR_API const char* favor_last_error(void);
 FAVOR_API unsigned long long favor_launch_count(void);
 
 /*
+ * favor_device_error -- synchronise with the handle's device (a blocking copy)
+ * and report its device-side error word in *code: 0 if every bounded wait in
+ * the kernels completed, otherwise the code of the first wait that gave up
+ * (the kernel then skipped the rest of its work and returned).  No
+ * counterpart on the pages; it exists so that a stalled pipeline surfaces as
+ * an error instead of a hang.
+ */
+FAVOR_API favor_status favor_device_error(favor_handle h, int* code);
+
+/*
  * Per-kernel timing for measurement (no counterpart on the pages).
  *
  * favor_profile_enable(h, 1) makes every later kernel launch through h record

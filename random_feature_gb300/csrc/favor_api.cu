@@ -103,6 +103,7 @@ static void free_handle(Handle* h) {
     cudaFree(h->omega_f32);
     cudaFree(h->omega_bf16);
     cudaFree(h->kshift);
+    cudaFree(h->dev_err);
     cudaFree(h->ws_partial);
     cudaFree(h->ws_state);
     cudaFree(h->ws_tc);
@@ -152,6 +153,7 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     h->s = data_scale; h->max_B = max_B; h->max_L = max_L; h->device = dev;
     cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (h->num_sms < 1) h->num_sms = 1;
+    cudaDeviceGetAttribute(&h->cc_major, cudaDevAttrComputeCapabilityMajor, dev);
 
     const size_t n_om = (size_t)H * m * d;
     std::vector<float> om(omega_host, omega_host + n_om);
@@ -202,6 +204,8 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     if (e == cudaSuccess) e = cudaMalloc(&h->omega_f32, n_om * sizeof(float));
     if (e == cudaSuccess && dtype == FAVOR_DTYPE_BF16) e = cudaMalloc(&h->omega_bf16, n_om * sizeof(__nv_bfloat16));
     if (e == cudaSuccess) e = cudaMalloc(&h->kshift, H * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->dev_err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->dev_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_partial, rows * st_elems * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_state, (size_t)max_B * H * st_elems * sizeof(float));
     if (e != cudaSuccess) {
@@ -298,6 +302,17 @@ favor_status favor_attn_causal(favor_handle hd, const void* q, const void* k, co
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tc_supported(h)) return tc_causal(h, q, k, v, out, B, L, s);
     return simt_causal(h, q, k, v, out, B, L, s);
+}
+
+favor_status favor_device_error(favor_handle hd, int* code) {
+    if (!hd || !code) return set_error(FAVOR_ERR_INVALID_ARG, "favor_device_error: null argument");
+    const Handle* h = reinterpret_cast<const Handle*>(hd);
+    cudaError_t e = cudaMemcpy(code, h->dev_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(FAVOR_ERR_CUDA, "favor_device_error: %s", cudaGetErrorString(e));
+    }
+    return FAVOR_OK;
 }
 
 static const char* kSlotNames[PROF_NSLOTS] = {"feature_map", "segment_state", "segment_combine",

@@ -43,6 +43,8 @@ struct Handle {
     int max_B, max_L;
     int device;
     int num_sms;
+    int cc_major;             // compute capability of the device
+    int* dev_err;             // device error word: 0, or the code of the first bounded wait that gave up
 
     float* omega_f32;         // [H, m, d] (bf16-rounded values for the BF16 dtype)
     __nv_bfloat16* omega_bf16;// [H, m, d] (BF16 dtype only)

@@ -22,7 +22,7 @@ __all__ = [
     "favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal", "favor_destroy",
     "favor_status_str", "favor_last_error", "favor_launch_count", "Favor", "EXPORTED_SYMBOLS",
     "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
-    "favor_profile_name",
+    "favor_profile_name", "favor_device_error",
 ]
 
 FAVOR_OK, FAVOR_ERR_INVALID_ARG, FAVOR_ERR_UNSUPPORTED, FAVOR_ERR_NOMEM, FAVOR_ERR_CUDA = range(5)
@@ -34,7 +34,7 @@ DTYPE_CODES = {"f32": FAVOR_DTYPE_F32, "bf16": FAVOR_DTYPE_BF16}
 EXPORTED_SYMBOLS = ("favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal",
                     "favor_destroy", "favor_status_str", "favor_last_error", "favor_launch_count",
                     "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
-                    "favor_profile_name")
+                    "favor_profile_name", "favor_device_error")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.favor_profile_slots.restype = i
         L.favor_profile_name.argtypes = [i]
         L.favor_profile_name.restype = ctypes.c_char_p
+        L.favor_device_error.argtypes = [vp, ctypes.POINTER(i)]
+        L.favor_device_error.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -173,6 +175,13 @@ def favor_profile_read(h, slot):
     n = ctypes.c_ulonglong()
     _check(lib().favor_profile_read(h, int(slot), ctypes.byref(ms), ctypes.byref(n)), "favor_profile_read")
     return ms.value, n.value
+
+
+def favor_device_error(h) -> int:
+    """Synchronise and return the handle's device error word (0 = no bounded wait gave up)."""
+    code = ctypes.c_int()
+    _check(lib().favor_device_error(h, ctypes.byref(code)), "favor_device_error")
+    return code.value
 
 
 def favor_profile_slots() -> int:
