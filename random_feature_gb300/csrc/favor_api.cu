@@ -190,13 +190,10 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
         ks[hh] = (float)(k > 0.0 ? k : 0.0);
     }
 
-    // Workspace: per-(head, segment) states for the largest call the bounds allow.
-    size_t rows = 0;
-    for (int b = 1; b <= max_B; ++b) {
-        SegPlan p = plan_segments(b * H, max_L, h->num_sms);
-        size_t r = (size_t)b * H * p.cap;
-        if (r > rows) rows = r;
-    }
+    // Workspace: per-(head, segment) states.  Both work splits stay within
+    // 2*SMs + 2*B*H rows: the CUDA-core segments use at most
+    // B*H*ceil(2*SMs/(B*H)) rows, the tensor-core ranges B*H*(ceil(SMs/(B*H))+1).
+    size_t rows = 2 * (size_t)h->num_sms + 2 * (size_t)max_B * H;
     h->ws_partial_rows = rows;
     const size_t st_elems = (size_t)m * (dv + 1);
 

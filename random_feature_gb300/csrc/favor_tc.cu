@@ -10,7 +10,7 @@
 // A [rows x 256] feature tile is four such images of 64 columns, 16 KB apart.
 //
 // Tensor-memory use (512 columns, lane = tile row):
-//   state kernel : [0,256) projection | [256,384) S halves (2 x 64) | [384,416) z halves (2 x 16)
+//   state kernel : [0,256) projection halves P0, P1 | [256,416) [S | z] halves (2 x 80 columns)
 //   readout      : [0,256) projection, then Phi_Q as packed bf16 in [0,128) | [128,208) output num|den
 //   causal       : [0,128) Phi_Q bf16 (from a 256-column projection) | [128,256) key projection
 //                  half, then Phi_Q Phi_K^T, then its masked bf16 copy | [256,336) output |
@@ -39,6 +39,7 @@ constexpr uint32_t kPhiBlock = kTile * 128;       // one 64-column image of a 12
 constexpr uint32_t kSBytes = kM * 128;            // S~ image [256 rows][64] = 32 KB
 constexpr uint32_t kZBytes = kM * 32;             // z~ image [256 rows][16] = 8 KB
 constexpr uint32_t kImageBytes = kSBytes + kZBytes;
+constexpr uint32_t kOnesBlock = kTile * 128;      // [128 rows][64] SW128 image: column 0 = 1, rest 0
 constexpr float kLog2e = 1.4426950408889634f;
 
 // byte offset of chunk `c` (16 B) of row `r` inside an SW128 image
@@ -53,6 +54,16 @@ struct Bars {
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// The second 64-column block of the MN-major operand [V | 1 | 0 ...]: in row j
+// only column 0 (logical chunk 0, stored at chunk j & 7) holds bf16 1.0.
+__device__ __forceinline__ void fill_ones_block(uint8_t* blk, int t, int nt) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(blk);
+    for (int i = t; i < (int)(kOnesBlock / 4); i += nt) {
+        const int r = i / 32, chunk = (i % 32) / 4, word = i % 4;
+        w[i] = (chunk == (r & 7) && word == 0) ? 0x00003F80u : 0u;
+    }
 }
 
 // Squared norm of row `r` of a bf16 SW128 tile.
@@ -119,6 +130,60 @@ __device__ __forceinline__ void key_features32(const uint32_t (&p)[32], float a,
         }
         w[i] = live ? pack_bf16(f0, f1) : 0u;
     }
+}
+
+// Key features for 64 consecutive projection columns -> 32 packed bf16 words.
+// Dead rows (past L) get c = -inf for positive features (exp -> 0); for ReLU
+// their projection is already 0 (TMA fills rows past L with zeros).
+template <int KIND>
+__device__ __forceinline__ void key_features64(const uint32_t (&p)[64], float a, float c, uint32_t (&w)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float f0, f1;
+        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+            f0 = ex2(fmaf(__uint_as_float(p[2 * i]), a, c));
+            f1 = ex2(fmaf(__uint_as_float(p[2 * i + 1]), a, c));
+        } else {
+            f0 = fmaxf(__uint_as_float(p[2 * i]), 0.f);
+            f1 = fmaxf(__uint_as_float(p[2 * i + 1]), 0.f);
+        }
+        w[i] = pack_bf16(f0, f1);
+    }
+}
+
+// Write 32 packed words (64 features, one full SW128 row) into row r of image `blk`.
+__device__ __forceinline__ void store_feat64(uint32_t blk, uint32_t r, const uint32_t (&w)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        st_shared_v4(blk + sw128(r, q), w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+// Partial squared norm over chunks [c0, c0+4) of row r of a bf16 SW128 tile.
+__device__ __forceinline__ float row_sqnorm_half(uint32_t tile, uint32_t r, uint32_t c0) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (uint32_t c = c0; c < c0 + 4; ++c) {
+        uint4 v = ld_shared_v4(tile + sw128(r, c));
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float lo = bf16lo(w[i]), hi = bf16hi(w[i]);
+            a0 = fmaf(lo, lo, a0);
+            a1 = fmaf(hi, hi, a1);
+        }
+    }
+    return a0 + a1;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+    uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+    tmem_ld32(taddr, lo);
+    tmem_ld32(taddr + 32, hi);
 }
 
 // Write 16 packed words (32 features starting at feature f0) into row r of a
@@ -213,131 +278,351 @@ __device__ __forceinline__ void store_state_row(uint32_t simg, uint32_t zimg, ui
     st_shared_v4(zimg + r * 32 + 16, zz, zz, zz, zz);
 }
 
+// ======================================================== persistent ranges
+// The flattened (head, tile) space of a call is cut into G contiguous ranges
+// of `per` tiles, one per CTA.  A head's tiles are covered by CTAs
+// first_cta(bh) .. last_cta(bh); CTA c writes the state of its part of head bh
+// to piece c - first_cta(bh) of that head (pstride pieces per head).
+struct Ranges {
+    int tph;      // tiles per head
+    int T;        // total tiles
+    int per;      // tiles per CTA
+    int G;        // CTAs
+    int pstride;  // piece slots per head
+};
+
+__host__ __device__ __forceinline__ int first_cta(const Ranges& r, int bh) { return (bh * r.tph) / r.per; }
+__host__ __device__ __forceinline__ int last_cta(const Ranges& r, int bh) { return ((bh + 1) * r.tph - 1) / r.per; }
+
 // ====================================================================== state
-// grid (n_seg, B*H), 128 threads.  Partial S (as [r][0:64]) and z ([r][64]) of
-// one segment's keys, fp32, to part[(bh*n_seg + seg)][256][65].
+// Persistent, warp-specialised.  The key projection is computed transposed,
+// D[feature r, token j] = omega_r . k_j + c_j / a, per half of 128 features
+// (tensor-memory slots P0, P1: lane = feature, column = token), where the
+// per-token exponent offset c_j = -(s^2 ||k_j||^2 / 2 + kappa) log2(e) enters
+// through one extra K-step: [c_j/a as bf16 hi + lo] against a pair of ones.
+// Feature warps then need only f = 2^(a * D): they read a slot once
+// (releasing it at once for the next tile's projection), accumulate z_r in
+// registers, and write the features packed (bf16) to Phi0 / Phi1, the A
+// operand (tensor memory) of S_half += Phi^T_half V.
+//   tensor memory: P0 [0,128) P1 [128,256) Phi0 [256,320) Phi1 [320,384) S0 [384,448) S1 [448,512)
+//   warp 0: TMA producer   warp 1: projection MMAs   warp 2: state MMAs
+//   warp 3: key norms -> offsets (positive features)
+//   warps 4..11: features; lane quarter q = warp % 4, half h = (warp - 4) / 4
+// The two MMA streams are independent (projections read omega and K, state
+// updates read Phi and V) and a single issuing thread is the bottleneck, so each
+// has its own thread; a K/V stage is released when both have committed.
+constexpr int kNS = 5;                 // K/V pipeline stages
+constexpr int kStateThreads = 384;
+constexpr uint32_t kExtStage = kTile * 32;        // K-side extra K-step: [128 tokens][16] bf16, no swizzle
+constexpr uint32_t kExtOmega = kM * 32;           // omega side: [256 features][16] bf16 = (1, 1, 0, ...)
+
+// Row r of a no-swizzle K-major [rows][16] bf16 operand: core matrices of
+// 8 rows x 16 B (SBO = 256 between row groups, LBO = 128 to elements 8..15).
+__device__ __forceinline__ uint32_t ext_row(uint32_t r) { return (r >> 3) * 256u + (r & 7u) * 16u; }
+
+struct StBars {
+    uint64_t kv_full[kNS], kv_empty[kNS];
+    uint64_t ext_full[kNS];
+    uint64_t w_full, w_empty;
+    uint64_t p_full[2], p_empty[2];
+    uint64_t phi_full[2], phi_empty[2];
+    uint64_t acc_full, acc_empty;
+    uint32_t tmem_base;
+};
+
 template <int KIND>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kStateThreads, 1)
 k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ kshift, float* __restrict__ part,
-           int H, int L, float s, int seg_tiles, int n_seg, int* err) {
+           int H, int L, float s, Ranges R, int* err) {
+    constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
-    const uint32_t s_k = s_w + kOmegaBytes;
-    const uint32_t s_v = s_k + kTileBytes;
-    const uint32_t s_phi = s_v + kTileBytes;
-    const uint32_t s_one = s_phi + 4 * kPhiBlock;
-    Bars* bars = reinterpret_cast<Bars*>(sm + (s_one - s_w) + 1024);
-    const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
-    const int tid = threadIdx.x, warp = tid / 32;
-    const uint32_t row = tid;   // tile row = tensor-memory lane
+    const uint32_t s_kv = s_w + kOmegaBytes;                 // stage i: K at +2i*16K, V at +(2i+1)*16K
+    const uint32_t s_ext = s_kv + kNS * 2 * kTileBytes;      // stage i: K-side extra block at +i*4K
+    const uint32_t s_wext = s_ext + kNS * kExtStage;         // omega-side extra block
+    StBars* bars = reinterpret_cast<StBars*>(sm + (s_wext - s_w) + kExtOmega);
+    const int c = blockIdx.x;
+    const int g0 = c * R.per;
+    const int g1 = min(R.T, g0 + R.per);
+    const int n = g1 - g0;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const float a = s * kLog2e;
 
-    setup(bars, 512);
-    for (int i = tid; i < 256; i += 128)
-        reinterpret_cast<uint32_t*>(sm + (s_one - s_w))[i] = 0x3F803F80u;   // bf16 1.0 pairs
-    fence_async_smem();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(&bars->kv_full[i], 1);
+            mbar_init(&bars->kv_empty[i], 2);
+            mbar_init(&bars->ext_full[i], 1);
+        }
+        mbar_init(&bars->w_full, 1);
+        mbar_init(&bars->w_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->p_full[i], 1);
+            mbar_init(&bars->p_empty[i], 4);
+            mbar_init(&bars->phi_full[i], 4);
+            mbar_init(&bars->phi_empty[i], 1);
+        }
+        mbar_init(&bars->acc_full, 1);
+        mbar_init(&bars->acc_empty, 8);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (POS && warp >= 4) {
+        // zero the K-side extra blocks; omega side = 1 in elements 0 and 1 of every row
+        uint32_t* e = reinterpret_cast<uint32_t*>(sm + (s_ext - s_w));
+        for (int i = threadIdx.x - 128; i < (int)(kNS * kExtStage / 4); i += kStateThreads - 128) e[i] = 0u;
+        uint32_t* wx = reinterpret_cast<uint32_t*>(sm + (s_wext - s_w));
+        for (int i = threadIdx.x - 128; i < (int)(kExtOmega / 4); i += kStateThreads - 128)
+            wx[i] = ((i & 63) < 32 && (i & 3) == 0) ? 0x3F803F80u : 0u;   // word 0 of core 0 of each row
+        fence_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
 
-    uint32_t tma_ph = 0, mma_ph = 0;
-    bool ok = true;
-    if (tid == 0) {
-        mbar_expect_tx(&bars->tma, kOmegaBytes);
-        tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
-    }
-    ok = __syncthreads_and(mbar_wait(&bars->tma, tma_ph, err, 1));
-    tma_ph ^= 1;
-
-    const float a = s * kLog2e;
-    const float kap = kshift[h];
-    int done = 0;
-    for (int t = 0; t < seg_tiles && ok; ++t) {
-        const int tok0 = (seg * seg_tiles + t) * kTile;
-        if (tok0 >= L) break;
-        if (tid == 0) {
-            mbar_expect_tx(&bars->tma, 2 * kTileBytes);
-            tma_load_3d(sm + (s_k - s_w), &tm_k, &bars->tma, 0, tok0, bh);
-            tma_load_3d(sm + (s_v - s_w), &tm_v, &bars->tma, 0, tok0, bh);
-        }
-        ok = __syncthreads_and(mbar_wait(&bars->tma, tma_ph, err, 2));
-        tma_ph ^= 1;
-        if (!ok) break;
-        const float c = -(0.5f * s * s * row_sqnorm(s_k, row) + kap) * kLog2e;
-        const bool live = tok0 + (int)row < L;
-        if (tid == 0) {
-            tc_fence_after();
-            issue_projection(tmem, s_k, s_w, 256);
-            mma_commit(&bars->mma);
-        }
-        ok = __syncthreads_and(mbar_wait(&bars->mma, mma_ph, err, 3));
-        mma_ph ^= 1;
-        tc_fence_after();
-        if (!ok) break;
-        for (int cc = 0; cc < 8; ++cc) {
-            uint32_t p[32], w[16];
-            tmem_ld32(tl + 32 * cc, p);
-            tmem_ld_wait();
-            key_features32<KIND>(p, a, c, live, w);
-            store_feat32(s_phi, row, 32 * cc, w);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id_s = make_idesc(128, 64, 1, 1);
-            const uint32_t id_z = make_idesc(128, 16, 1, 0);
-            const uint64_t b1 = make_desc(s_one, 128, 256, SW_NONE);
-            for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t av = make_desc(s_phi + 2 * hh * kPhiBlock + kk * 2048, kPhiBlock, 1024, SW_128B);
-                    const uint64_t bv = make_desc(s_v + kk * 2048, kPhiBlock, 1024, SW_128B);
-                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                    mma_ss(tmem + 256 + 64 * hh, av, bv, id_s, acc);
-                    mma_ss(tmem + 384 + 16 * hh, av, b1, id_z, acc);
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int cur_h = -1;
+            uint32_t wph = 0;
+            for (int i = 0; i < n; ++i) {
+                const int g = g0 + i, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
+                const int st = i % kNS;
+                if (i >= kNS && !mbar_wait(&bars->kv_empty[st], ((i / kNS) - 1) & 1, err, 101)) break;
+                if (h != cur_h) {
+                    if (cur_h >= 0) {
+                        if (!mbar_wait(&bars->w_empty, wph, err, 102)) break;
+                        wph ^= 1;
+                    }
+                    mbar_expect_tx(&bars->w_full, kOmegaBytes);
+                    tma_load_2d(sm, &tm_w, &bars->w_full, 0, h * kM);
+                    cur_h = h;
                 }
+                mbar_expect_tx(&bars->kv_full[st], 2 * kTileBytes);
+                tma_load_3d(sm + (s_kv - s_w) + 2 * st * kTileBytes, &tm_k, &bars->kv_full[st], 0, tok0, bh);
+                tma_load_3d(sm + (s_kv - s_w) + (2 * st + 1) * kTileBytes, &tm_v, &bars->kv_full[st], 0, tok0, bh);
             }
-            mma_commit(&bars->mma);
         }
-        ok = __syncthreads_and(mbar_wait(&bars->mma, mma_ph, err, 4));
-        mma_ph ^= 1;
-        tc_fence_after();
-        ++done;
-    }
-    if (ok && done > 0) {
-        for (int hh = 0; hh < 2; ++hh) {
-            uint32_t s0[32], s1[32], z[16];
-            tmem_ld32(tl + 256 + 64 * hh, s0);
-            tmem_ld32(tl + 256 + 64 * hh + 32, s1);
-            tmem_ld16(tl + 384 + 16 * hh, z);
+    } else if (warp == 1) {
+        // ------------------------------------------------------ projection MMAs
+        // P_h (features 128h.., tokens) = omega rows x K tile (+ offsets for positive features)
+        if (lane == 0 && n > 0) {
+            const uint32_t id_p = make_idesc(128, 128, 0, 0);
+            uint32_t wph = 0;
+            int tih = g0 % R.tph;               // tile index within the current head
+            const bool multi_head = H > 1;      // a new bh means new omega only when H > 1
+            int st = 0;
+            for (int i = 0; i < n; ++i) {
+                if (i == 0 || (tih == 0 && multi_head)) {
+                    if (!mbar_wait(&bars->w_full, wph, err, 111)) break;
+                    wph ^= 1;
+                }
+                if (!mbar_wait(&bars->kv_full[st], (i / kNS) & 1, err, 112)) break;
+                if (POS && !mbar_wait(&bars->ext_full[st], (i / kNS) & 1, err, 113)) break;
+                bool ok = true;
+                for (int hp = 0; hp < 2; ++hp) {
+                    if (i > 0 && !mbar_wait(&bars->p_empty[hp], (i - 1) & 1, err, 114 + hp)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a0 = make_desc(s_w + hp * 128 * 128, 16, 1024, SW_128B);
+                    const uint64_t b0 = make_desc(s_kv + 2 * st * kTileBytes, 16, 1024, SW_128B);
+                    const uint32_t d = tmem + 128 * hp;
+                    mma_ss(d, a0, b0, id_p, 0u);
+                    mma_ss(d, a0 + 2, b0 + 2, id_p, 1u);
+                    mma_ss(d, a0 + 4, b0 + 4, id_p, 1u);
+                    mma_ss(d, a0 + 6, b0 + 6, id_p, 1u);
+                    if (POS)
+                        mma_ss(d, make_desc(s_wext + hp * 128 * 32, 128, 256, SW_NONE),
+                               make_desc(s_ext + st * kExtStage, 128, 256, SW_NONE), id_p, 1u);
+                    mma_commit(&bars->p_full[hp]);
+                }
+                if (!ok) break;
+                mma_commit(&bars->kv_empty[st]);                       // K side of the stage is read
+                if (i + 1 < n && tih == R.tph - 1 && multi_head) mma_commit(&bars->w_empty);
+                tih = (tih + 1 == R.tph) ? 0 : tih + 1;
+                st = (st + 1 == kNS) ? 0 : st + 1;
+            }
+        }
+    } else if (warp == 2) {
+        // ----------------------------------------------------------- state MMAs
+        // S_h += Phi^T_h (tensor memory, packed bf16) x V tile (smem, MN-major)
+        if (lane == 0 && n > 0) {
+            const uint32_t id_s = make_idesc(128, 64, 0, 1);
+            int piece = 0;
+            int tih = g0 % R.tph;
+            int st = 0;
+            bool ok = true;
+            for (int i = 0; i < n && ok; ++i) {
+                const bool first = (i == 0) || tih == 0;
+                const bool last = (i == n - 1) || tih == R.tph - 1;
+                if (first && i > 0) {
+                    ok = mbar_wait(&bars->acc_empty, (piece - 1) & 1, err, 117);
+                    if (!ok) break;
+                }
+                for (int hp = 0; hp < 2 && ok; ++hp) {
+                    ok = mbar_wait(&bars->phi_full[hp], i & 1, err, 118 + hp);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t b0 = make_desc(s_kv + (2 * st + 1) * kTileBytes, 8192, 1024, SW_128B);
+                    const uint32_t d = tmem + 384 + 64 * hp;
+                    const uint32_t ap = tmem + 256 + 64 * hp;
+                    mma_ts(d, ap, b0, id_s, first ? 0u : 1u);
+#pragma unroll
+                    for (int kk = 1; kk < 8; ++kk) mma_ts(d, ap + 8 * kk, b0 + 128 * kk, id_s, 1u);
+                    mma_commit(&bars->phi_empty[hp]);
+                }
+                if (!ok) break;
+                mma_commit(&bars->kv_empty[st]);                       // V side of the stage is read
+                if (last) {
+                    mma_commit(&bars->acc_full);
+                    ++piece;
+                }
+                tih = (tih + 1 == R.tph) ? 0 : tih + 1;
+                st = (st + 1 == kNS) ? 0 : st + 1;
+            }
+        }
+    } else if (warp == 3) {
+        // ---------------------------------------------------------- key norms
+        // Per token: x = c_j / a with c_j = -(s^2 ||k_j||^2 / 2 + kappa_h) log2(e)
+        // (a huge negative value past L), written as bf16 hi + lo into the
+        // stage's K-side extra block.  Four tokens per lane.
+        if (POS) {
+            int kap_h = -1;
+            float kap = 0.f;
+            for (int i = 0; i < n; ++i) {
+                const int g = g0 + i, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
+                const int st = i % kNS;
+                if (h != kap_h) {
+                    kap = __ldg(kshift + h);
+                    kap_h = h;
+                }
+                if (!mbar_wait(&bars->kv_full[st], (i / kNS) & 1, err, 131)) break;
+                float nrm[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) nrm[t] = row_sqnorm(s_kv + 2 * st * kTileBytes, (uint32_t)(lane + 32 * t));
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t j = (uint32_t)(lane + 32 * t);
+                    const float x = (tok0 + (int)j < L) ? -(0.5f * s * s * nrm[t] + kap) / s : -1.0e30f;
+                    const float hi = __bfloat162float(__float2bfloat16_rn(x));
+                    const float lo = x - hi;
+                    st_shared_v4(s_ext + st * kExtStage + ext_row(j), pack_bf16(hi, lo), 0u, 0u, 0u);
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->ext_full[st]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ features
+        const int q = warp & 3;
+        const int hp = (warp - 4) >> 2;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        const uint32_t tp = tmem + lane_off + 128 * hp;           // projection slot
+        const uint32_t tf = tmem + lane_off + 256 + 64 * hp;      // packed features
+        int piece = 0;
+        float z0 = 0.f, z1 = 0.f;
+        for (int i = 0; i < n; ++i) {
+            const int g = g0 + i, bh = g / R.tph;
+            const bool last = (i == n - 1) || ((g + 1) / R.tph) != bh;
+            if (!mbar_wait(&bars->p_full[hp], i & 1, err, 121)) break;
+            tc_fence_after();
+            uint32_t p[128];
+            {
+                uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[0]);
+                uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[32]);
+                uint32_t (&p2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[64]);
+                uint32_t (&p3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[96]);
+                tmem_ld32(tp, p0);
+                tmem_ld32(tp + 32, p1);
+                tmem_ld32(tp + 64, p2);
+                tmem_ld32(tp + 96, p3);
+            }
             tmem_ld_wait();
-            float* o = part + ((size_t)bh * n_seg + seg) * (kM * (kDV + 1)) + (size_t)(128 * hh + row) * (kDV + 1);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_empty[hp]);
+            // features into registers first: the exps overlap the previous tile's
+            // state MMAs, which still read this warp's Phi region
+            uint32_t w[64];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(s0[e]);
+            for (int k2 = 0; k2 < 64; ++k2) {
+                const float x0 = __uint_as_float(p[2 * k2]), x1 = __uint_as_float(p[2 * k2 + 1]);
+                float f0, f1;
+                if (POS) {
+                    f0 = ex2(x0 * a);
+                    f1 = ex2(x1 * a);
+                } else {
+                    // ReLU: rows past L are zero (TMA fill), so their projection is 0
+                    f0 = fmaxf(x0, 0.f);
+                    f1 = fmaxf(x1, 0.f);
+                }
+                z0 += f0;
+                z1 += f1;
+                w[k2] = pack_bf16(f0, f1);
+            }
+            if (i > 0 && !mbar_wait(&bars->phi_empty[hp], (i - 1) & 1, err, 123)) break;
+            tc_fence_after();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[32 + e] = __uint_as_float(s1[e]);
-            o[64] = __uint_as_float(z[0]);
+            for (int cc = 0; cc < 4; ++cc)
+                tmem_st16(tf + 16 * cc, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * cc]));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->phi_full[hp]);
+            if (last) {
+                if (!mbar_wait(&bars->acc_full, piece & 1, err, 124)) break;
+                tc_fence_after();
+                uint32_t sv[64];
+                tmem_ld64(tmem + lane_off + 384 + 64 * hp, sv);
+                tmem_ld_wait();
+                const int pc = c - first_cta(R, bh);
+                float* o = part + ((size_t)bh * R.pstride + pc) * (kM * (kDV + 1)) +
+                           (size_t)(128 * hp + 32 * q + lane) * (kDV + 1);
+#pragma unroll
+                for (int k2 = 0; k2 < 64; ++k2) o[k2] = __uint_as_float(sv[k2]);
+                o[64] = z0 + z1;
+                z0 = z1 = 0.f;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->acc_empty);
+                ++piece;
+            }
         }
     }
-    teardown(bars, tmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // ================================================ reduce + pack (bidirectional)
-// grid (ceil(256*65/256), B*H).  Sum the segment partials in order and write
-// the bf16 operand image: S~ ([256][64] SW128) then z~ ([256][16], z repeated).
-__global__ void k_reduce_pack(const float* __restrict__ part, uint8_t* __restrict__ image, int n_seg) {
+// grid (ceil(256*65/256), B*H).  Sum a head's pieces in order and write the
+// bf16 operand image: S~ ([256][64] SW128) then z~ ([256][16], z repeated).
+__global__ void k_reduce_pack(const float* __restrict__ part, uint8_t* __restrict__ image, Ranges R) {
     const int bh = blockIdx.y;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     constexpr int n = kM * (kDV + 1);
     if (i >= n) return;
-    const float* p = part + (size_t)bh * n_seg * n + i;
+    const int np = last_cta(R, bh) - first_cta(R, bh) + 1;
+    const float* p = part + (size_t)bh * R.pstride * n + i;
     float acc = 0.f;
-    for (int sg = 0; sg < n_seg; ++sg) acc += p[(size_t)sg * n];
+    int j = 0;
+    for (; j + 8 <= np; j += 8) {       // loads first, then the additions in order
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = p[(size_t)(j + u) * n];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc += v[u];
+    }
+    for (; j < np; ++j) acc += p[(size_t)j * n];
     const int r = i / (kDV + 1), e = i - r * (kDV + 1);
     uint8_t* img = image + (size_t)bh * kImageBytes;
     const __nv_bfloat16 b = __float2bfloat16_rn(acc);
@@ -348,6 +633,33 @@ __global__ void k_reduce_pack(const float* __restrict__ part, uint8_t* __restric
         __nv_bfloat16* z = reinterpret_cast<__nv_bfloat16*>(img + kSBytes + (size_t)r * 32);
 #pragma unroll
         for (int q = 0; q < 16; ++q) z[q] = b;
+    }
+}
+
+// Causal: piece j of head bh <- sum of pieces 0..j-1 (exclusive prefix, in order).
+__global__ void k_scan_pieces(float* __restrict__ part, Ranges R) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    constexpr int n = kM * (kDV + 1);
+    if (i >= n) return;
+    const int np = last_cta(R, bh) - first_cta(R, bh) + 1;
+    float* p = part + (size_t)bh * R.pstride * n + i;
+    float run = 0.f;
+    int j = 0;
+    for (; j + 8 <= np; j += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = p[(size_t)(j + u) * n];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            p[(size_t)(j + u) * n] = run;
+            run += v[u];
+        }
+    }
+    for (; j < np; ++j) {
+        const float t = p[(size_t)j * n];
+        p[(size_t)j * n] = run;
+        run += t;
     }
 }
 
@@ -416,14 +728,15 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 }
 
 // ===================================================================== causal
-// grid (n_seg, B*H), 128 threads.  Walks one segment chunk by chunk starting
-// from the segment's exclusive prefix state prefix[(bh*n_seg + seg)][256][65].
+// grid G (persistent ranges), 128 threads.  Walks the CTA's tile range chunk
+// by chunk; at the start of each head's part it loads that piece's exclusive
+// prefix state prefix[(bh*pstride + piece)][256][65].
 template <int KIND>
 __global__ void __launch_bounds__(128, 1)
 k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
             const float* __restrict__ kshift, const float* __restrict__ prefix, __nv_bfloat16* __restrict__ out,
-            int H, int L, float s, int seg_tiles, int n_seg, int* err) {
+            int H, int L, float s, Ranges R, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
@@ -435,7 +748,8 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t s_z = s_s + kSBytes;
     const uint32_t s_one = s_z + kZBytes;
     Bars* bars = reinterpret_cast<Bars*>(sm + (s_one - s_w) + 1024);
-    const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int cta = blockIdx.x;
+    const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
     const int tid = threadIdx.x, warp = tid / 32;
     const uint32_t row = tid;
 
@@ -449,44 +763,53 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
 
     uint32_t tma_ph = 0, mma_ph = 0;
-    if (tid == 0) {
-        mbar_expect_tx(&bars->tma, kOmegaBytes);
-        tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
-    }
-    // Initial state from the exclusive prefix: tensor memory (fp32 master) and
-    // the bf16 operand images.
-    const float* pre = prefix + ((size_t)bh * n_seg + seg) * (kM * (kDV + 1));
-    for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t r = 128 * hh + row;
-        float sv[64];
-#pragma unroll
-        for (int e = 0; e < 64; ++e) sv[e] = pre[(size_t)r * (kDV + 1) + e];
-        const float z = pre[(size_t)r * (kDV + 1) + 64];
-        uint32_t w[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(sv[16 * q + i]);
-            tmem_st16(tl + 384 + 64 * hh + 16 * q, w);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(z);
-        tmem_st16(tl + 336 + 16 * hh, w);
-        store_state_row(s_s, s_z, r, sv, z);
-    }
-    tmem_st_wait();
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    bool ok = __syncthreads_and(mbar_wait(&bars->tma, tma_ph, err, 21));
-    tma_ph ^= 1;
-
+    bool ok = true;
+    int cur_bh = -1, cur_h = -1;
     const float a = s * kLog2e;
-    const float kap = kshift[h];
-    for (int t = 0; t < seg_tiles && ok; ++t) {
-        const int tok0 = (seg * seg_tiles + t) * kTile;
-        if (tok0 >= L) break;
+    for (int g = g0; g < g1 && ok; ++g) {
+        const int bh = g / R.tph, h = bh % H;
+        const int tok0 = (g % R.tph) * kTile;
+        if (bh != cur_bh) {
+            if (h != cur_h) {
+                if (tid == 0) {
+                    mbar_expect_tx(&bars->tma, kOmegaBytes);
+                    tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
+                }
+                ok = __syncthreads_and(mbar_wait(&bars->tma, tma_ph, err, 21));
+                tma_ph ^= 1;
+                if (!ok) break;
+                cur_h = h;
+            }
+            // state of this head's piece: tensor memory (fp32 master) and the bf16 operand images
+            const float* pre = prefix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1));
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t r = 128 * hh + row;
+                float sv[64];
+#pragma unroll
+                for (int e = 0; e < 64; ++e) sv[e] = pre[(size_t)r * (kDV + 1) + e];
+                const float z = pre[(size_t)r * (kDV + 1) + 64];
+                uint32_t w[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(sv[16 * q + i]);
+                    tmem_st16(tl + 384 + 64 * hh + 16 * q, w);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(z);
+                tmem_st16(tl + 336 + 16 * hh, w);
+                store_state_row(s_s, s_z, r, sv, z);
+            }
+            tmem_st_wait();
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            cur_bh = bh;
+        }
+        const float kap = kshift[h];
+        {
+
         if (tid == 0) {
             mbar_expect_tx(&bars->tma, 3 * kTileBytes);
             tma_load_3d(sm + (s_q - s_w), &tm_q, &bars->tma, 0, tok0, bh);
@@ -624,6 +947,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        }
     }
     teardown(bars, tmem, 512);
 }
@@ -735,7 +1059,7 @@ bool map_omega(CUtensorMap* m, const void* base, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t kSmemState = 1024 + kOmegaBytes + 2 * kTileBytes + 4 * kPhiBlock + 1024 + 64;
+constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * kExtStage + kExtOmega + sizeof(StBars);
 constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kTileBytes + kImageBytes + 64;
 constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kImageBytes + 1024 + 64;
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
@@ -762,16 +1086,33 @@ void allow_all_once() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+Ranges plan_ranges(int BH, int L, int num_sms) {
+    Ranges r;
+    r.tph = (L + kTile - 1) / kTile;
+    r.T = BH * r.tph;
+    int G = num_sms < r.T ? num_sms : r.T;
+    r.per = (r.T + G - 1) / G;
+    r.G = (r.T + r.per - 1) / r.per;
+    int mx = 1;
+    for (int bh = 0; bh < BH; ++bh) {
+        const int np = last_cta(r, bh) - first_cta(r, bh) + 1;
+        if (np > mx) mx = np;
+    }
+    r.pstride = mx;
+    return r;
+}
+
 favor_status launch_state(const Handle& h, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mw,
-                          int BH, int L, const SegPlan& p, cudaStream_t st) {
-    dim3 grid(p.n_seg, BH);
+                          int BH, int L, const Ranges& R, cudaStream_t st) {
+    if ((size_t)BH * R.pstride > h.ws_partial_rows)
+        return set_error(FAVOR_ERR_INVALID_ARG, "state workspace too small (%d x %d rows)", BH, R.pstride);
     ProfScope ps(h, PROF_STATE, st);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
-        k_tc_state<FAVOR_KERNEL_SOFTMAX_POS><<<grid, 128, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial, h.H, L,
-                                                                              h.s, p.seg_tiles, p.n_seg, h.dev_err);
+        k_tc_state<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kStateThreads, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial,
+                                                                                      h.H, L, h.s, R, h.dev_err);
     else
-        k_tc_state<FAVOR_KERNEL_RELU><<<grid, 128, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial, h.H, L, h.s,
-                                                                       p.seg_tiles, p.n_seg, h.dev_err);
+        k_tc_state<FAVOR_KERNEL_RELU><<<R.G, kStateThreads, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial, h.H,
+                                                                               L, h.s, R, h.dev_err);
     count_launch();
     return check_launch("tensor-core state kernel");
 }
@@ -808,22 +1149,22 @@ favor_status tc_bidir(const Handle& h, const void* q, const void* k, const void*
         return simt_bidir(h, q, k, v, out, B, L, st);
     allow_all_once();
     const int BH = B * h.H;
-    SegPlan p = plan_segments(BH, L, h.num_sms);
+    Ranges R = plan_ranges(BH, L, h.num_sms);
     CUtensorMap mq, mk, mv, mw;
     if (!map_tokens(&mq, q, BH, L) || !map_tokens(&mk, k, BH, L) || !map_tokens(&mv, v, BH, L) ||
         !map_omega(&mw, h.omega_bf16, h.H))
         return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    favor_status s = launch_state(h, mk, mv, mw, BH, L, p, st);
+    favor_status s = launch_state(h, mk, mv, mw, BH, L, R, st);
     if (s != FAVOR_OK) return s;
     {
         dim3 grid((kM * (kDV + 1) + 255) / 256, BH);
         ProfScope ps(h, PROF_COMBINE, st);
-        k_reduce_pack<<<grid, 256, 0, st>>>(h.ws_partial, (uint8_t*)h.ws_tc, p.n_seg);
+        k_reduce_pack<<<grid, 256, 0, st>>>(h.ws_partial, (uint8_t*)h.ws_tc, R);
         count_launch();
         s = check_launch("reduce/pack kernel");
         if (s != FAVOR_OK) return s;
     }
-    dim3 grid(p.tiles, BH);
+    dim3 grid(R.tph, BH);
     ProfScope ps(h, PROF_READOUT, st);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
         k_tc_readout<FAVOR_KERNEL_SOFTMAX_POS><<<grid, 128, kSmemReadout, st>>>(
@@ -841,31 +1182,33 @@ favor_status tc_causal(const Handle& h, const void* q, const void* k, const void
         return simt_causal(h, q, k, v, out, B, L, st);
     allow_all_once();
     const int BH = B * h.H;
-    SegPlan p = plan_segments(BH, L, h.num_sms);
+    Ranges R = plan_ranges(BH, L, h.num_sms);
     CUtensorMap mq, mk, mv, mw;
     if (!map_tokens(&mq, q, BH, L) || !map_tokens(&mk, k, BH, L) || !map_tokens(&mv, v, BH, L) ||
         !map_omega(&mw, h.omega_bf16, h.H))
         return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     favor_status s;
-    if (p.n_seg > 1) {
-        s = launch_state(h, mk, mv, mw, BH, L, p, st);
+    if (R.pstride > 1) {
+        s = launch_state(h, mk, mv, mw, BH, L, R, st);
         if (s != FAVOR_OK) return s;
-        s = launch_scan_segments(h, BH, p.n_seg, st);
+        dim3 g2((kM * (kDV + 1) + 255) / 256, BH);
+        ProfScope ps(h, PROF_COMBINE, st);
+        k_scan_pieces<<<g2, 256, 0, st>>>(h.ws_partial, R);
+        count_launch();
+        s = check_launch("piece scan kernel");
     } else {
         s = cudaMemsetAsync(h.ws_partial, 0, (size_t)BH * kM * (kDV + 1) * sizeof(float), st) == cudaSuccess
                 ? FAVOR_OK
                 : set_error(FAVOR_ERR_CUDA, "cudaMemsetAsync failed");
     }
     if (s != FAVOR_OK) return s;
-    dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_CAUSAL, st);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
-        k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS><<<grid, 128, kSmemCausal, st>>>(
-            mq, mk, mv, mw, h.kshift, h.ws_partial, (__nv_bfloat16*)out, h.H, L, h.s, p.seg_tiles, p.n_seg, h.dev_err);
+        k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, 128, kSmemCausal, st>>>(
+            mq, mk, mv, mw, h.kshift, h.ws_partial, (__nv_bfloat16*)out, h.H, L, h.s, R, h.dev_err);
     else
-        k_tc_causal<FAVOR_KERNEL_RELU><<<grid, 128, kSmemCausal, st>>>(mq, mk, mv, mw, h.kshift, h.ws_partial,
-                                                                         (__nv_bfloat16*)out, h.H, L, h.s, p.seg_tiles,
-                                                                         p.n_seg, h.dev_err);
+        k_tc_causal<FAVOR_KERNEL_RELU><<<R.G, 128, kSmemCausal, st>>>(mq, mk, mv, mw, h.kshift, h.ws_partial,
+                                                                        (__nv_bfloat16*)out, h.H, L, h.s, R, h.dev_err);
     count_launch();
     return check_launch("tensor-core causal kernel");
 }

@@ -43,12 +43,30 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity
     return ok;
 }
 
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok;
+}
+
 // Wait for the phase with the given parity to complete, giving up after about
 // two seconds of SM clock: then the error word gets `code` and false returns.
+// Spins with the non-suspending probe (a suspended try_wait can resume long
+// after the phase completes), backing off with a short sleep once it has
+// waited a while.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    int spins = 0;
+    while (!mbar_test_wait(bar, parity)) {
+        if (++spins > 64) __nanosleep(20);
         if (clock64() - t0 > (4LL << 30)) {
             if (err) atomicExch(err, code);
             return false;
