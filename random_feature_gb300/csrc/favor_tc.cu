@@ -16,6 +16,7 @@
 //                  half, then Phi_Q Phi_K^T, then its masked bf16 copy | [256,336) output |
 //                  [336,368) z halves | [384,512) S halves
 #include <cmath>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -728,228 +729,461 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 }
 
 // ===================================================================== causal
-// grid G (persistent ranges), 128 threads.  Walks the CTA's tile range chunk
-// by chunk; at the start of each head's part it loads that piece's exclusive
-// prefix state prefix[(bh*pstride + piece)][256][65].
+// Persistent over ranges, chunks of 128 tokens.  For chunk t of head bh with
+// state S(t), z(t) (the sums over all earlier keys of the head):
+//   O = Phi_Q [S~ | z~](t) + tril(Phi_Q Phi_K^T) [V | 1]      out = O[:, :64] / O[:, 64]
+//   S(t+1) = S(t) + Phi_K^T V,   z(t+1) = z(t) + Phi_K^T 1
+// (App. B.1 Eq. 11 of Rethinking Attention with Performers, taken chunk by chunk).
+//   warp 0: TMA producer (single Q, K, V buffers, refilled as soon as each is consumed)
+//   warp 1: projection MMAs  P_Q = Q omega^T (lane = query), P_K^T = omega K^T (+ key offsets)
+//   warp 2: MMAs A = Phi_Q Phi_K^T and the intra-chunk term
+//   warp 3: MMAs for the inter-chunk term and the state update
+//   warps 4..7 (lane = query of the chunk): key norms, query features, causal mask, output
+//   warps 8..11 (lane = feature, one in each half): key features, z, state refresh
+// Tensor memory: [0,256) P_Q -> Phi_Q packed in [0,128); A in [128,256) -> masked packed in [128,192)
+//                [256,384) P_K^T half slot (feature x token), then O in [256,336)
+//                [384,512) S halves (fp32, lane = feature)
+// Shared memory holds Phi_K as [feature][token] (MN-major B of A, K-major A of the
+// state update) and [S~ | z~]^T as a K-major [80][256] bf16 image (rows 65..79 zero).
+constexpr int kCausalThreads = 384;
+constexpr uint32_t kStImage = 80 * 128;   // one 64-feature K-block of [S~ | z~]^T: 80 rows x 128 B
+
+struct CaBars {
+    uint64_t q_full, k_full, v_full, q_empty, k_empty, v_empty;
+    uint64_t w_full, w_empty, ext_full;
+    uint64_t pq_full, phiq_full, pk_full, pk_empty, pk_done, phik_full, phik_empty;
+    uint64_t a_full, am_full, inter_done, o_full, o_empty;
+    uint64_t s_full, s_ready, st_full;
+    uint32_t tmem_base;
+};
+
 template <int KIND>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kCausalThreads, 1)
 k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
             const float* __restrict__ kshift, const float* __restrict__ prefix, __nv_bfloat16* __restrict__ out,
             int H, int L, float s, Ranges R, int* err) {
+    constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
     const uint32_t s_q = s_w + kOmegaBytes;
     const uint32_t s_k = s_q + kTileBytes;
     const uint32_t s_v = s_k + kTileBytes;
-    const uint32_t s_phi = s_v + kTileBytes;
-    const uint32_t s_s = s_phi + 4 * kPhiBlock;
-    const uint32_t s_z = s_s + kSBytes;
-    const uint32_t s_one = s_z + kZBytes;
-    Bars* bars = reinterpret_cast<Bars*>(sm + (s_one - s_w) + 1024);
+    const uint32_t s_phi = s_v + kTileBytes;                  // [256 features][128 tokens]: 2 blocks of 64 tokens (32 KB each)
+    const uint32_t s_st = s_phi + 4 * kPhiBlock;              // [S~|z~]^T: 4 K-blocks of kStImage
+    const uint32_t s_one = s_st + 4 * kStImage;               // ones block
+    const uint32_t s_ext = s_one + kOnesBlock;                // K-side offsets [128][16]
+    const uint32_t s_wext = s_ext + kExtStage;                // omega side [256][16]
+    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_wext - s_w) + kExtOmega);
     const int cta = blockIdx.x;
     const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
-    const int tid = threadIdx.x, warp = tid / 32;
-    const uint32_t row = tid;
+    const int n = g1 - g0;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const float a = s * kLog2e;
 
-    setup(bars, 512);
-    for (int i = tid; i < 256; i += 128)
-        reinterpret_cast<uint32_t*>(sm + (s_one - s_w))[i] = 0x3F803F80u;
+    if (threadIdx.x == 0) {
+        uint64_t* b = reinterpret_cast<uint64_t*>(bars);
+        // order and arrival counts follow the fields of CaBars
+        const int counts[] = {1, 1, 1, 1, 5, 2,   1, 1, 4,   1, 4, 1, 4, 4, 4, 2,   1, 4, 1, 1, 4,   1, 4, 4};
+        static_assert(sizeof(counts) / sizeof(int) * sizeof(uint64_t) == offsetof(CaBars, tmem_base), "barrier table");
+        for (int i = 0; i < (int)(sizeof(counts) / sizeof(int)); ++i) mbar_init(b + i, counts[i]);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp >= 4) {
+        const int t = threadIdx.x - 128, nt = kCausalThreads - 128;
+        fill_ones_block(sm + (s_one - s_w), t, nt);
+        uint32_t* z = reinterpret_cast<uint32_t*>(sm + (s_st - s_w));
+        for (int i = t; i < (int)(4 * kStImage / 4); i += nt) z[i] = 0u;
+        uint32_t* e = reinterpret_cast<uint32_t*>(sm + (s_ext - s_w));
+        for (int i = t; i < (int)(kExtStage / 4); i += nt) e[i] = 0u;
+        uint32_t* wx = reinterpret_cast<uint32_t*>(sm + (s_wext - s_w));
+        for (int i = t; i < (int)(kExtOmega / 4); i += nt) wx[i] = ((i & 63) < 32 && (i & 3) == 0) ? 0x3F803F80u : 0u;
+        fence_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    const bool multi_head = H > 1;
 
-    uint32_t tma_ph = 0, mma_ph = 0;
-    bool ok = true;
-    int cur_bh = -1, cur_h = -1;
-    const float a = s * kLog2e;
-    for (int g = g0; g < g1 && ok; ++g) {
-        const int bh = g / R.tph, h = bh % H;
-        const int tok0 = (g % R.tph) * kTile;
-        if (bh != cur_bh) {
-            if (h != cur_h) {
-                if (tid == 0) {
-                    mbar_expect_tx(&bars->tma, kOmegaBytes);
-                    tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int cur_h = -1;
+            uint32_t wph = 0;
+            for (int t = 0; t < n; ++t) {
+                const int g = g0 + t, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
+                const uint32_t pp = (t - 1) & 1;
+                if (h != cur_h) {
+                    if (cur_h >= 0) {
+                        if (!mbar_wait(&bars->w_empty, wph, err, 201)) break;
+                        wph ^= 1;
+                    }
+                    mbar_expect_tx(&bars->w_full, kOmegaBytes);
+                    tma_load_2d(sm, &tm_w, &bars->w_full, 0, h * kM);
+                    cur_h = h;
                 }
-                ok = __syncthreads_and(mbar_wait(&bars->tma, tma_ph, err, 21));
-                tma_ph ^= 1;
-                if (!ok) break;
-                cur_h = h;
+                if (t > 0 && !mbar_wait(&bars->q_empty, pp, err, 202)) break;
+                mbar_expect_tx(&bars->q_full, kTileBytes);
+                tma_load_3d(sm + (s_q - s_w), &tm_q, &bars->q_full, 0, tok0, bh);
+                if (t > 0 && !mbar_wait(&bars->k_empty, pp, err, 203)) break;
+                mbar_expect_tx(&bars->k_full, kTileBytes);
+                tma_load_3d(sm + (s_k - s_w), &tm_k, &bars->k_full, 0, tok0, bh);
+                if (t > 0 && !mbar_wait(&bars->v_empty, pp, err, 204)) break;
+                mbar_expect_tx(&bars->v_full, kTileBytes);
+                tma_load_3d(sm + (s_v - s_w), &tm_v, &bars->v_full, 0, tok0, bh);
             }
-            // state of this head's piece: tensor memory (fp32 master) and the bf16 operand images
-            const float* pre = prefix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1));
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t r = 128 * hh + row;
-                float sv[64];
-#pragma unroll
-                for (int e = 0; e < 64; ++e) sv[e] = pre[(size_t)r * (kDV + 1) + e];
-                const float z = pre[(size_t)r * (kDV + 1) + 64];
-                uint32_t w[16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(sv[16 * q + i]);
-                    tmem_st16(tl + 384 + 64 * hh + 16 * q, w);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ projection MMAs
+        if (lane == 0) {
+            const uint32_t id_q = make_idesc(128, 256, 0, 0);
+            const uint32_t id_k = make_idesc(128, 128, 0, 0);
+            uint32_t wph = 0;
+            int tih = g0 % R.tph;
+            for (int t = 0; t < n; ++t) {
+                const uint32_t ph = t & 1, pp = (t - 1) & 1;
+                if (t == 0 || (tih == 0 && multi_head)) {
+                    if (!mbar_wait(&bars->w_full, wph, err, 211)) break;
+                    wph ^= 1;
                 }
+                // P_Q = Q omega^T into [0,256): the query region is free once O(t-1) was read
+                if (!mbar_wait(&bars->q_full, ph, err, 212)) break;
+                if (t > 0 && !mbar_wait(&bars->o_empty, pp, err, 213)) break;
+                tc_fence_after();
+                {
+                    const uint64_t a0 = make_desc(s_q, 16, 1024, SW_128B);
+                    const uint64_t b0 = make_desc(s_w, 16, 1024, SW_128B);
+                    mma_ss(tmem, a0, b0, id_q, 0u);
+                    mma_ss(tmem, a0 + 2, b0 + 2, id_q, 1u);
+                    mma_ss(tmem, a0 + 4, b0 + 4, id_q, 1u);
+                    mma_ss(tmem, a0 + 6, b0 + 6, id_q, 1u);
+                    mma_commit(&bars->pq_full);
+                    mma_commit(&bars->q_empty);
+                }
+                // P_K^T halves (features x tokens, + key offsets) through the slot [256,384)
+                if (!mbar_wait(&bars->k_full, ph, err, 214)) break;
+                if (!mbar_wait(&bars->ext_full, ph, err, 215)) break;
+                bool ok = true;
+                for (int hp = 0; hp < 2; ++hp) {
+                    if (hp == 1 && !mbar_wait(&bars->pk_empty, ph, err, 216)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t a0 = make_desc(s_w + hp * 128 * 128, 16, 1024, SW_128B);
+                    const uint64_t b0 = make_desc(s_k, 16, 1024, SW_128B);
+                    const uint32_t d = tmem + 256;
+                    mma_ss(d, a0, b0, id_k, 0u);
+                    mma_ss(d, a0 + 2, b0 + 2, id_k, 1u);
+                    mma_ss(d, a0 + 4, b0 + 4, id_k, 1u);
+                    mma_ss(d, a0 + 6, b0 + 6, id_k, 1u);
+                    mma_ss(d, make_desc(s_wext + hp * 128 * 32, 128, 256, SW_NONE), make_desc(s_ext, 128, 256, SW_NONE),
+                           id_k, 1u);
+                    mma_commit(&bars->pk_full);
+                }
+                if (!ok) break;
+                mma_commit(&bars->k_empty);
+                if (t + 1 < n && tih == R.tph - 1 && multi_head) mma_commit(&bars->w_empty);
+                tih = (tih + 1 == R.tph) ? 0 : tih + 1;
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------ A = Phi_Q Phi_K^T, intra
+        if (lane == 0) {
+            const uint32_t id_a = make_idesc(128, 128, 0, 1);
+            const uint32_t id_v = make_idesc(128, 80, 0, 1);
+            for (int t = 0; t < n; ++t) {
+                const uint32_t ph = t & 1;
+                if (!mbar_wait(&bars->phiq_full, ph, err, 221)) break;
+                if (!mbar_wait(&bars->phik_full, ph, err, 222)) break;
+                tc_fence_after();
+                // B = Phi_K [feature][token]: N = token (2 blocks of 64, LBO), K = feature (16 rows per step)
+                const uint64_t b0 = make_desc(s_phi, 2 * kPhiBlock, 1024, SW_128B);
+                mma_ts(tmem + 128, tmem, b0, id_a, 0u);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(z);
-                tmem_st16(tl + 336 + 16 * hh, w);
-                store_state_row(s_s, s_z, r, sv, z);
+                for (int kk = 1; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 8 * kk, b0 + 128 * kk, id_a, 1u);
+                mma_commit(&bars->a_full);
+                mma_commit(&bars->phik_empty);
+                // intra: O += masked A [V | 1], after the inter term initialised O
+                if (!mbar_wait(&bars->am_full, ph, err, 223)) break;
+                if (!mbar_wait(&bars->inter_done, ph, err, 224)) break;
+                if (!mbar_wait(&bars->v_full, ph, err, 225)) break;
+                tc_fence_after();
+                const uint64_t bv = make_desc(s_v, s_one - s_v, 1024, SW_128B);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) mma_ts(tmem + 256, tmem + 128 + 8 * kk, bv + 128 * kk, id_v, 1u);
+                mma_commit(&bars->o_full);
+                mma_commit(&bars->v_empty);
+            }
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------ inter, state update
+        if (lane == 0) {
+            const uint32_t id_o = make_idesc(128, 80, 0, 0);
+            const uint32_t id_s = make_idesc(128, 64, 0, 1);
+            for (int t = 0; t < n; ++t) {
+                const uint32_t ph = t & 1;
+                // inter: O = Phi_Q [S~ | z~] into the free key slot
+                if (!mbar_wait(&bars->phiq_full, ph, err, 231)) break;
+                if (!mbar_wait(&bars->st_full, ph, err, 232)) break;
+                if (!mbar_wait(&bars->pk_done, ph, err, 233)) break;
+                tc_fence_after();
+                {
+                    const uint64_t b0 = make_desc(s_st, 16, 1024, SW_128B);   // K-major, rows = 80 output columns
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk)
+                        mma_ts(tmem + 256, tmem + 8 * kk, b0 + (uint64_t)(((kk >> 2) * kStImage + (kk & 3) * 32) >> 4),
+                               id_o, kk > 0 ? 1u : 0u);
+                    mma_commit(&bars->inter_done);
+                }
+                // state: S_h += Phi_K^T_h V (A = Phi_K rows of half h, K-major over tokens)
+                if (!mbar_wait(&bars->phik_full, ph, err, 234)) break;
+                if (!mbar_wait(&bars->v_full, ph, err, 235)) break;
+                if (!mbar_wait(&bars->s_ready, ph, err, 236)) break;
+                tc_fence_after();
+                const uint64_t bv = make_desc(s_v, 8192, 1024, SW_128B);
+                for (int hp = 0; hp < 2; ++hp) {
+                    const uint64_t a0 = make_desc(s_phi + hp * 128 * 128, 16, 1024, SW_128B);
+                    const uint32_t d = tmem + 384 + 64 * hp;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(d, a0 + (uint64_t)((((kk >> 2) * 2 * kPhiBlock) + (kk & 3) * 32) >> 4), bv + 128 * kk,
+                               id_s, 1u);
+                }
+                mma_commit(&bars->s_full);
+                mma_commit(&bars->phik_empty);
+                mma_commit(&bars->v_empty);
+            }
+        }
+    } else if (warp < 8) {
+        // ---------------------------------------------------------- query side
+        const int q = warp & 3;
+        const uint32_t row = 32 * q + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+        int kap_h = -1;
+        float kap = 0.f;
+        for (int t = 0; t < n; ++t) {
+            const uint32_t ph = t & 1;
+            const int g = g0 + t, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
+            // key norm of this row -> offset c/a as bf16 hi + lo (positive features)
+            if (!mbar_wait(&bars->k_full, ph, err, 241)) break;
+            if (POS) {
+                if (h != kap_h) {
+                    kap = __ldg(kshift + h);
+                    kap_h = h;
+                }
+                const float nrm = row_sqnorm(s_k, row);
+                const float x = (tok0 + (int)row < L) ? -(0.5f * s * s * nrm + kap) / s : -1.0e30f;
+                const float hi = __bfloat162float(__float2bfloat16_rn(x));
+                st_shared_v4(s_ext + ext_row(row), pack_bf16(hi, x - hi), 0u, 0u, 0u);
+                fence_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars->ext_full);
+                mbar_arrive(&bars->k_empty);
+            }
+            // query features (row max over the 256 features), packed in place into [0,128)
+            if (!mbar_wait(&bars->pq_full, ph, err, 242)) break;
+            tc_fence_after();
+            float mx = 0.f;
+            if (POS) {
+                mx = -INFINITY;
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t p[32];
+                    tmem_ld32(tl + 32 * c, p);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(p[i]));
+                }
+            }
+            const float cm = -mx * a;
+            for (int c = 0; c < 8; ++c) {
+                uint32_t p[32], w[16];
+                tmem_ld32(tl + 32 * c, p);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float f0, f1;
+                    if (POS) {
+                        f0 = ex2(fmaf(__uint_as_float(p[2 * i]), a, cm));
+                        f1 = ex2(fmaf(__uint_as_float(p[2 * i + 1]), a, cm));
+                    } else {
+                        f0 = fmaxf(__uint_as_float(p[2 * i]), 0.f);
+                        f1 = fmaxf(__uint_as_float(p[2 * i + 1]), 0.f);
+                    }
+                    w[i] = pack_bf16(f0, f1);
+                }
+                tmem_st16(tl + 16 * c, w);
             }
             tmem_st_wait();
-            fence_async_smem();
             tc_fence_before();
-            __syncthreads();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->phiq_full);
+            // causal mask: keep key j <= query row, packed in place into [128,192)
+            if (!mbar_wait(&bars->a_full, ph, err, 243)) break;
             tc_fence_after();
-            cur_bh = bh;
-        }
-        const float kap = kshift[h];
-        {
-
-        if (tid == 0) {
-            mbar_expect_tx(&bars->tma, 3 * kTileBytes);
-            tma_load_3d(sm + (s_q - s_w), &tm_q, &bars->tma, 0, tok0, bh);
-            tma_load_3d(sm + (s_k - s_w), &tm_k, &bars->tma, 0, tok0, bh);
-            tma_load_3d(sm + (s_v - s_w), &tm_v, &bars->tma, 0, tok0, bh);
-        }
-        ok = __syncthreads_and(mbar_wait(&bars->tma, tma_ph, err, 22));
-        tma_ph ^= 1;
-        if (!ok) break;
-        const float c = -(0.5f * s * s * row_sqnorm(s_k, row) + kap) * kLog2e;
-        const bool live = tok0 + (int)row < L;
-        // query projection and features (bf16 pairs into [0,128))
-        if (tid == 0) {
-            tc_fence_after();
-            issue_projection(tmem, s_q, s_w, 256);
-            mma_commit(&bars->mma);
-        }
-        ok = __syncthreads_and(mbar_wait(&bars->mma, mma_ph, err, 23));
-        mma_ph ^= 1;
-        tc_fence_after();
-        if (!ok) break;
-        query_features_to_tmem<KIND>(tl, a);
-        tc_fence_before();
-        __syncthreads();
-        // key projection in two halves of 128 features -> Phi_K in shared memory
-        for (int hk = 0; hk < 2 && ok; ++hk) {
-            if (tid == 0) {
-                tc_fence_after();
-                issue_projection(tmem + 128, s_k, s_w + hk * 128 * 128, 128);
-                mma_commit(&bars->mma);
-            }
-            ok = __syncthreads_and(mbar_wait(&bars->mma, mma_ph, err, 24));
-            mma_ph ^= 1;
-            tc_fence_after();
-            if (!ok) break;
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t p[32], w[16];
-                tmem_ld32(tl + 128 + 32 * cc, p);
+                tmem_ld32(tl + 128 + 32 * c, p);
                 tmem_ld_wait();
-                key_features32<KIND>(p, a, c, live, w);
-                store_feat32(s_phi, row, 128 * hk + 32 * cc, w);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int j = 32 * c + 2 * i;
+                    const float f0 = (j <= (int)row) ? __uint_as_float(p[2 * i]) : 0.f;
+                    const float f1 = (j + 1 <= (int)row) ? __uint_as_float(p[2 * i + 1]) : 0.f;
+                    w[i] = pack_bf16(f0, f1);
+                }
+                tmem_st16(tl + 128 + 16 * c, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->am_full);
+            // output row
+            if (!mbar_wait(&bars->o_full, ph, err, 244)) break;
+            tc_fence_after();
+            {
+                const int tok = tok0 + (int)row;
+                store_output_row(tl + 256, out + ((size_t)bh * L + tok) * kDV, tok < L);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->o_empty);
+        }
+    } else {
+        // ------------------------------------------------------------ key side
+        // thread owns feature r0 = 32q + lane (half 0) and r0 + 128 (half 1)
+        const int q = warp & 3;
+        const uint32_t r0 = 32 * q + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+        float z[2] = {0.f, 0.f};
+        int cur_bh = -1;
+        for (int t = 0; t < n; ++t) {
+            const uint32_t ph = t & 1;
+            const int g = g0 + t, bh = g / R.tph;
+            if (bh != cur_bh) {
+                // a new head piece: state = its exclusive prefix (master S, image, z).
+                // The previous chunk's state update and inter term are complete.
+                if (t > 0) {
+                    if (!mbar_wait(&bars->s_full, (t - 1) & 1, err, 251)) break;
+                    if (!mbar_wait(&bars->inter_done, (t - 1) & 1, err, 252)) break;
+                    tc_fence_after();
+                }
+                const float* pre = prefix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1));
+                for (int hp = 0; hp < 2; ++hp) {
+                    const uint32_t r = r0 + 128 * hp;
+                    uint32_t w[16];
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(pre[(size_t)r * (kDV + 1) + 16 * c + i]);
+                        tmem_st16(tl + 384 + 64 * hp + 16 * c, w);
+                    }
+                    z[hp] = pre[(size_t)r * (kDV + 1) + 64];
+                    // image column r: rows e = 0..63 from S, row 64 = z
+                    uint8_t* img = sm + (s_st - s_w) + (r >> 6) * kStImage;
+                    const uint32_t cr = (r & 63) >> 3, pr = (r & 7) * 2;
+                    for (int e = 0; e < 64; ++e)
+                        *reinterpret_cast<__nv_bfloat16*>(img + e * 128 + ((cr ^ (e & 7)) << 4) + pr) =
+                            __float2bfloat16_rn(pre[(size_t)r * (kDV + 1) + e]);
+                    *reinterpret_cast<__nv_bfloat16*>(img + 64 * 128 + ((cr ^ 0) << 4) + pr) = __float2bfloat16_rn(z[hp]);
+                }
+                tmem_st_wait();
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars->s_ready);
+                    mbar_arrive(&bars->st_full);
+                }
+                cur_bh = bh;
+            }
+            // key features of both halves -> Phi_K [feature][token] in shared memory, z
+            for (int hp = 0; hp < 2; ++hp) {
+                if (!mbar_wait(&bars->pk_full, hp, err, 253)) break;
+                tc_fence_after();
+                uint32_t p[128];
+                {
+                    uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[0]);
+                    uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[32]);
+                    uint32_t (&p2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[64]);
+                    uint32_t (&p3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[96]);
+                    tmem_ld32(tl + 256, p0);
+                    tmem_ld32(tl + 256 + 32, p1);
+                    tmem_ld32(tl + 256 + 64, p2);
+                    tmem_ld32(tl + 256 + 96, p3);
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hp == 0 ? &bars->pk_empty : &bars->pk_done);
+                if (hp == 0 && t > 0 && !mbar_wait(&bars->phik_empty, (t - 1) & 1, err, 254)) break;
+                const uint32_t r = r0 + 128 * hp;
+                float zz0 = 0.f, zz1 = 0.f;
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float x0 = __uint_as_float(p[64 * blk + 8 * c + 2 * i]);
+                            const float x1 = __uint_as_float(p[64 * blk + 8 * c + 2 * i + 1]);
+                            float f0, f1;
+                            if (POS) {
+                                f0 = ex2(x0 * a);
+                                f1 = ex2(x1 * a);
+                            } else {
+                                f0 = fmaxf(x0, 0.f);
+                                f1 = fmaxf(x1, 0.f);
+                            }
+                            zz0 += f0;
+                            zz1 += f1;
+                            w4[i] = pack_bf16(f0, f1);
+                        }
+                        st_shared_v4(s_phi + blk * 2 * kPhiBlock + sw128(r, c), w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+                z[hp] += zz0 + zz1;
             }
             fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-        }
-        if (!ok) break;
-        // A = Phi_Q Phi_K^T (N = 128 keys) and the inter-chunk term Phi_Q [S~ | z~]
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id_a = make_idesc(128, 128, 0, 0);
-            const uint32_t id_s = make_idesc(128, 64, 0, 1);
-            const uint32_t id_z = make_idesc(128, 16, 0, 1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->phik_full);
+            // state refresh for the next chunk of the same head piece
+            const bool next_same = (t + 1 < n) && ((g + 1) / R.tph) == bh;
+            if (next_same) {
+                if (!mbar_wait(&bars->s_full, ph, err, 255)) break;
+                if (!mbar_wait(&bars->inter_done, ph, err, 256)) break;
+                tc_fence_after();
+                for (int hp = 0; hp < 2; ++hp) {
+                    const uint32_t r = r0 + 128 * hp;
+                    uint32_t sv[64];
+                    tmem_ld64(tl + 384 + 64 * hp, sv);
+                    tmem_ld_wait();
+                    uint8_t* img = sm + (s_st - s_w) + (r >> 6) * kStImage;
+                    const uint32_t cr = (r & 63) >> 3, pr = (r & 7) * 2;
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-                const uint64_t bk = make_desc(s_phi + (kk / 4) * kPhiBlock + (kk % 4) * 32, 16, 1024, SW_128B);
-                mma_ts(tmem + 128, tmem + 8 * kk, bk, id_a, kk > 0);
-                const uint64_t bs = make_desc(s_s + kk * 2048, 8192, 1024, SW_128B);
-                const uint64_t bz = make_desc(s_z + kk * 512, 8192, 256, SW_32B);
-                mma_ts(tmem + 256, tmem + 8 * kk, bs, id_s, kk > 0);
-                mma_ts(tmem + 320, tmem + 8 * kk, bz, id_z, kk > 0);
-            }
-            mma_commit(&bars->mma);
-        }
-        ok = __syncthreads_and(mbar_wait(&bars->mma, mma_ph, err, 25));
-        mma_ph ^= 1;
-        tc_fence_after();
-        if (!ok) break;
-        // causal mask (keep key j <= query i) and bf16 pairs in place into [128,192)
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t p[32], w[16];
-            tmem_ld32(tl + 128 + 32 * cc, p);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int j0 = 32 * cc + 2 * i;
-                const float f0 = (j0 <= (int)row) ? __uint_as_float(p[2 * i]) : 0.f;
-                const float f1 = (j0 + 1 <= (int)row) ? __uint_as_float(p[2 * i + 1]) : 0.f;
-                w[i] = pack_bf16(f0, f1);
-            }
-            tmem_st16(tl + 128 + 16 * cc, w);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncthreads();
-        // intra-chunk term tril(A) [V | 1] and the state update [S | z] += Phi_K^T [V | 1]
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id_v = make_idesc(128, 64, 0, 1);
-            const uint32_t id_1 = make_idesc(128, 16, 0, 0);
-            const uint32_t id_sv = make_idesc(128, 64, 1, 1);
-            const uint32_t id_s1 = make_idesc(128, 16, 1, 0);
-            const uint64_t b1 = make_desc(s_one, 128, 256, SW_NONE);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bv = make_desc(s_v + kk * 2048, 8192, 1024, SW_128B);
-                mma_ts(tmem + 256, tmem + 128 + 8 * kk, bv, id_v, 1);
-                mma_ts(tmem + 320, tmem + 128 + 8 * kk, b1, id_1, 1);
-            }
-            for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t av = make_desc(s_phi + 2 * hh * kPhiBlock + kk * 2048, kPhiBlock, 1024, SW_128B);
-                    const uint64_t bv = make_desc(s_v + kk * 2048, 8192, 1024, SW_128B);
-                    mma_ss(tmem + 384 + 64 * hh, av, bv, id_sv, 1);
-                    mma_ss(tmem + 336 + 16 * hh, av, b1, id_s1, 1);
+                    for (int e = 0; e < 64; ++e)
+                        *reinterpret_cast<__nv_bfloat16*>(img + e * 128 + ((cr ^ (e & 7)) << 4) + pr) =
+                            __float2bfloat16_rn(__uint_as_float(sv[e]));
+                    *reinterpret_cast<__nv_bfloat16*>(img + 64 * 128 + (cr << 4) + pr) = __float2bfloat16_rn(z[hp]);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars->s_ready);
+                    mbar_arrive(&bars->st_full);
                 }
             }
-            mma_commit(&bars->mma);
-        }
-        ok = __syncthreads_and(mbar_wait(&bars->mma, mma_ph, err, 26));
-        mma_ph ^= 1;
-        tc_fence_after();
-        if (!ok) break;
-        {
-            const int tok = tok0 + (int)row;
-            store_output_row(tl + 256, out + ((size_t)bh * L + tok) * kDV, tok < L);
-        }
-        // refresh the bf16 state images for the next chunk
-        for (int hh = 0; hh < 2; ++hh) {
-            uint32_t s0[32], s1[32], z[16];
-            tmem_ld32(tl + 384 + 64 * hh, s0);
-            tmem_ld32(tl + 384 + 64 * hh + 32, s1);
-            tmem_ld16(tl + 336 + 16 * hh, z);
-            tmem_ld_wait();
-            float sv[64];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                sv[e] = __uint_as_float(s0[e]);
-                sv[32 + e] = __uint_as_float(s1[e]);
-            }
-            store_state_row(s_s, s_z, 128 * hh + row, sv, __uint_as_float(z[0]));
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
         }
     }
-    teardown(bars, tmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // ================================================================ feature map
@@ -1061,7 +1295,8 @@ bool map_omega(CUtensorMap* m, const void* base, int H) {
 
 constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * kExtStage + kExtOmega + sizeof(StBars);
 constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kTileBytes + kImageBytes + 64;
-constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kImageBytes + 1024 + 64;
+constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + 4 * kStImage + kOnesBlock + kExtStage +
+                                kExtOmega + sizeof(CaBars);
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
 
 template <typename K>
@@ -1204,10 +1439,10 @@ favor_status tc_causal(const Handle& h, const void* q, const void* k, const void
     if (s != FAVOR_OK) return s;
     ProfScope ps(h, PROF_CAUSAL, st);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
-        k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, 128, kSmemCausal, st>>>(
+        k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kCausalThreads, kSmemCausal, st>>>(
             mq, mk, mv, mw, h.kshift, h.ws_partial, (__nv_bfloat16*)out, h.H, L, h.s, R, h.dev_err);
     else
-        k_tc_causal<FAVOR_KERNEL_RELU><<<R.G, 128, kSmemCausal, st>>>(mq, mk, mv, mw, h.kshift, h.ws_partial,
+        k_tc_causal<FAVOR_KERNEL_RELU><<<R.G, kCausalThreads, kSmemCausal, st>>>(mq, mk, mv, mw, h.kshift, h.ws_partial,
                                                                         (__nv_bfloat16*)out, h.H, L, h.s, R, h.dev_err);
     count_launch();
     return check_launch("tensor-core causal kernel");
