@@ -121,6 +121,40 @@ FAVOR_API favor_status favor_attn_bidir(favor_handle h, const void* q, const voi
 FAVOR_API favor_status favor_attn_causal(favor_handle h, const void* q, const void* k,
                                const void* v, void* out, int B, int L, void* stream);
 
+/*
+ * favor_attn_bidir_noalloc -- favor_attn_bidir without a handle and without
+ * any allocation.  The pages have no counterpart: this is an interface
+ * convenience.  It serves callers that may not allocate device memory through
+ * this library, e.g. a host framework whose caching allocator owns the device
+ * memory, or a serving process that reserves the device memory up front.
+ * favor_create allocates its workspace with cudaMalloc, so these callers
+ * cannot make a handle.
+ *
+ *   omega       DEVICE float array [H, m, d] (caller-owned, read only), used
+ *               as given (favor_create's bf16 rounding of omega is not
+ *               applied); entries must be finite.
+ *   H, m, d, dv, kind, dtype, data_scale   as in favor_create, same limits.
+ *   q, k, v, out, B, L, stream             as in favor_attn_bidir.
+ *
+ * Computes what favor_attn_bidir computes (Eq. 4 of Rethinking Attention with
+ * Performers), on the CUDA-core kernels, with the same zero-denominator rule and
+ * the same cancelling shifts (the per-head key shift is derived on the device
+ * from omega).  Scratch is one fixed 16 MiB device array inside the library
+ * (4,194,304 floats): calls need H (rounded up to 64) + 2*B*H*m*(dv+1) floats at
+ * least, and larger sizes fail with FAVOR_ERR_UNSUPPORTED before anything is
+ * launched; the work split is narrowed to fit.  No part of the array needs to
+ * start at zero.  Every device has its own copy.  Its address is looked up
+ * the first time the call runs on a device (cudaGetSymbolAddress, which may
+ * load the library's device code there); make that first call before any
+ * stream capture begins.  Calls on one device share the array: two calls
+ * that overlap in time on the device race and give wrong results, so order
+ * them (one stream, or events).
+ */
+FAVOR_API favor_status favor_attn_bidir_noalloc(const float* omega, int H, int m, int d, int dv,
+                                                favor_kernel kind, favor_dtype dtype, float data_scale,
+                                                const void* q, const void* k, const void* v, void* out,
+                                                int B, int L, void* stream);
+
 /* favor_destroy -- free everything the handle owns (after synchronising its
  * device).  Accepts NULL. */
 FAVOR_API favor_status favor_destroy(favor_handle h);

@@ -301,6 +301,50 @@ favor_status favor_attn_causal(favor_handle hd, const void* q, const void* k, co
     return simt_causal(h, q, k, v, out, B, L, s);
 }
 
+favor_status favor_attn_bidir_noalloc(const float* omega, int H, int m, int d, int dv, favor_kernel kind,
+                                      favor_dtype dtype, float data_scale, const void* q, const void* k,
+                                      const void* v, void* out, int B, int L, void* stream) {
+    const char* fn = "favor_attn_bidir_noalloc";
+    g_err[0] = 0;
+    if (!omega || !q || !k || !v || !out) return set_error(FAVOR_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (H < 1 || m < 1 || d < 1 || dv < 1 || B < 1 || L < 1)
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: sizes must be >= 1 (H=%d m=%d d=%d dv=%d B=%d L=%d)", fn, H, m,
+                         d, dv, B, L);
+    if (kind != FAVOR_KERNEL_SOFTMAX_POS && kind != FAVOR_KERNEL_RELU)
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: unknown kernel kind %d", fn, (int)kind);
+    if (dtype != FAVOR_DTYPE_F32 && dtype != FAVOR_DTYPE_BF16)
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+    if (!(data_scale > 0.0f) || !std::isfinite(data_scale))
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: data_scale must be finite and > 0", fn);
+    if (!shape_ok(d) || !shape_ok(dv))
+        return set_error(FAVOR_ERR_UNSUPPORTED, "%s: d=%d dv=%d (supported: 16, 32, 64, 128)", fn, d, dv);
+    if (m % 16 != 0 || m < 16 || m > 256)
+        return set_error(FAVOR_ERR_UNSUPPORTED, "%s: m=%d (supported: multiples of 16 in [16, 256])", fn, m);
+    if ((long long)B * H * (long long)L * (d > dv ? d : dv) > (1LL << 40))
+        return set_error(FAVOR_ERR_UNSUPPORTED, "%s: B*H*L too large", fn);
+    const long long BH = (long long)B * H;
+    if (BH > (1 << 20) || fixed_scratch_floats(H, (int)BH, m, dv, 1) > kFixedScratchFloats)
+        return set_error(FAVOR_ERR_UNSUPPORTED,
+                         "%s: B*H*m*(dv+1) = %lld needs more than the fixed scratch of %zu floats (at most %zu "
+                         "per state copy, two copies)", fn, BH * m * (dv + 1), kFixedScratchFloats,
+                         (kFixedScratchFloats - ((size_t)H + 63) / 64 * 64) / 2);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(FAVOR_ERR_CUDA, "%s: no usable CUDA device", fn);
+    }
+    Handle h;
+    std::memset(&h, 0, sizeof(h));
+    h.H = H; h.m = m; h.d = d; h.dv = dv; h.kind = kind; h.dtype = dtype; h.s = data_scale;
+    h.max_B = B; h.max_L = L; h.device = dev;
+    cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (h.num_sms < 1) h.num_sms = 1;
+    cudaDeviceGetAttribute(&h.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaGetLastError();
+    h.omega_f32 = const_cast<float*>(omega);
+    return simt_bidir_fixed_scratch(h, q, k, v, out, B, L, reinterpret_cast<cudaStream_t>(stream));
+}
+
 favor_status favor_device_error(favor_handle hd, int* code) {
     if (!hd || !code) return set_error(FAVOR_ERR_INVALID_ARG, "favor_device_error: null argument");
     const Handle* h = reinterpret_cast<const Handle*>(hd);

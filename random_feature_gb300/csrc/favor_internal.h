@@ -96,6 +96,16 @@ favor_status simt_bidir(const Handle& h, const void* q, const void* k, const voi
 favor_status simt_causal(const Handle& h, const void* q, const void* k, const void* v, void* out,
                          int B, int L, cudaStream_t st);
 
+// ---- bidirectional call on a fixed, statically sized device scratch array ----
+// 16 MiB: enough for B*H*m*(dv+1)*(1 + n_seg) + H floats with n_seg >= 1 up to
+// B*H = 63 at m = 256, dv = 128 (more heads at smaller m, dv).
+constexpr size_t kFixedScratchFloats = (size_t)4 << 20;
+size_t fixed_scratch_floats(int H, int BH, int m, int dv, int n_seg);
+// proto: H, m, d, dv, kind, dtype, s, device, num_sms and omega_f32 (the
+// caller's device omega) filled in; nothing else is read.
+favor_status simt_bidir_fixed_scratch(const Handle& proto, const void* q, const void* k, const void* v,
+                                      void* out, int B, int L, cudaStream_t st);
+
 // ---- tensor-core (tcgen05) kernels: bf16, d = dv = 64, m = 256 ----
 bool tc_supported(const Handle& h);
 favor_status tc_feature_map(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st);

@@ -11,6 +11,7 @@
 // the m^-1/2 factor, both common to a query row; the key shift kappa_h is
 // common to a head.  favor_feature_map returns the unshifted definition.
 #include <cmath>
+#include <mutex>
 
 #include "favor_internal.h"
 
@@ -452,6 +453,109 @@ favor_status simt_causal(const Handle& h, const void* q, const void* k, const vo
     }
     if (s != FAVOR_OK) return s;
     return dispatch3<CausalF>(h, q, k, v, out, BH, L, (const SegPlan*)&p, st);
+}
+
+// ------------------------------------------------ bidirectional call, fixed scratch
+// favor_attn_bidir_noalloc runs the CUDA-core bidirectional path above with no
+// handle and no allocation: its scratch (per-head key shifts, per-segment
+// partial states, reduced states) is one statically sized device array that
+// is part of this library's device image.  Each device has its own copy; the
+// address is looked up once per device with that device current.  No word of
+// the array needs to start at zero: every word a call reads was written
+// earlier in the same call.  Overlapping calls on one device share the array
+// and race; order them on one stream.
+
+static __device__ __align__(256) float g_fixed_scratch[kFixedScratchFloats];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_fixed_mu;
+float* g_fixed_ptr[kMaxDevices] = {};
+
+favor_status fixed_scratch_ptr(int dev, float** out) {
+    if (dev < 0 || dev >= kMaxDevices)
+        return set_error(FAVOR_ERR_UNSUPPORTED, "favor_attn_bidir_noalloc: device ordinal %d above %d", dev,
+                         kMaxDevices - 1);
+    std::lock_guard<std::mutex> lk(g_fixed_mu);
+    if (!g_fixed_ptr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_fixed_scratch);
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();
+            return set_error(FAVOR_ERR_CUDA, "favor_attn_bidir_noalloc: cudaGetSymbolAddress: %s",
+                             cudaGetErrorString(e));
+        }
+        g_fixed_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_fixed_ptr[dev];
+    return FAVOR_OK;
+}
+
+// kappa_h = max(0, max_r ||omega_r||^2/2 - KSHIFT_HEADROOM), one block per head.
+__global__ void __launch_bounds__(256) k_key_shift(const float* __restrict__ omega, float* __restrict__ kshift,
+                                                   int m, int d) {
+    __shared__ float red[8];
+    const int h = blockIdx.x;
+    float mx = 0.f;
+    for (int r = threadIdx.x; r < m; r += blockDim.x) {
+        const float* w = omega + ((size_t)h * m + r) * d;
+        float a = 0.f;
+        for (int c = 0; c < d; ++c) a = fmaf(w[c], w[c], a);
+        mx = fmaxf(mx, a);
+    }
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = red[0];
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = fmaxf(t, red[w]);
+        kshift[h] = fmaxf(0.f, 0.5f * t - KSHIFT_HEADROOM);
+    }
+}
+
+}  // namespace
+
+size_t fixed_scratch_floats(int H, int BH, int m, int dv, int n_seg) {
+    const size_t hpad = ((size_t)H + 63) / 64 * 64;
+    return hpad + (size_t)BH * m * (dv + 1) * (size_t)(1 + n_seg);
+}
+
+favor_status simt_bidir_fixed_scratch(const Handle& proto, const void* q, const void* k, const void* v,
+                                      void* out, int B, int L, cudaStream_t st) {
+    float* base = nullptr;
+    favor_status s = fixed_scratch_ptr(proto.device, &base);
+    if (s != FAVOR_OK) return s;
+    const int BH = B * proto.H;
+    SegPlan p = plan_segments(BH, L, proto.num_sms);
+    const size_t per_seg = (size_t)BH * proto.m * (proto.dv + 1);
+    const size_t hpad = fixed_scratch_floats(proto.H, BH, proto.m, proto.dv, 0) - per_seg;
+    if (kFixedScratchFloats < hpad + 2 * per_seg)
+        return set_error(FAVOR_ERR_UNSUPPORTED, "favor_attn_bidir_noalloc: B*H*m*(dv+1) too large for the fixed scratch");
+    const int max_seg = (int)((kFixedScratchFloats - hpad) / per_seg - 1);
+    if (p.n_seg > max_seg) {
+        p.seg_tiles = (p.tiles + max_seg - 1) / max_seg;
+        p.n_seg = (p.tiles + p.seg_tiles - 1) / p.seg_tiles;
+    }
+    Handle h = proto;
+    h.kshift = base;
+    h.ws_state = base + hpad;
+    h.ws_partial = h.ws_state + per_seg;
+    h.ws_partial_rows = (size_t)BH * p.n_seg;
+    h.prof = nullptr;
+    k_key_shift<<<h.H, 256, 0, st>>>(h.omega_f32, h.kshift, h.m, h.d);
+    count_launch();
+    s = check_launch("key shift kernel");
+    if (s != FAVOR_OK) return s;
+    s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, st);
+    if (s != FAVOR_OK) return s;
+    s = launch_reduce_segments(h, BH, p.n_seg, st);
+    if (s != FAVOR_OK) return s;
+    if (h.dtype == FAVOR_DTYPE_F32)
+        return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
+                                                  : readout_t<float, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
+    return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
+                                              : readout_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
 }
 
 }  // namespace favor

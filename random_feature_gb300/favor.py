@@ -22,7 +22,7 @@ __all__ = [
     "favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal", "favor_destroy",
     "favor_status_str", "favor_last_error", "favor_launch_count", "Favor", "EXPORTED_SYMBOLS",
     "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
-    "favor_profile_name", "favor_device_error",
+    "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc",
 ]
 
 FAVOR_OK, FAVOR_ERR_INVALID_ARG, FAVOR_ERR_UNSUPPORTED, FAVOR_ERR_NOMEM, FAVOR_ERR_CUDA = range(5)
@@ -34,7 +34,7 @@ DTYPE_CODES = {"f32": FAVOR_DTYPE_F32, "bf16": FAVOR_DTYPE_BF16}
 EXPORTED_SYMBOLS = ("favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal",
                     "favor_destroy", "favor_status_str", "favor_last_error", "favor_launch_count",
                     "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
-                    "favor_profile_name", "favor_device_error")
+                    "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.favor_profile_name.restype = ctypes.c_char_p
         L.favor_device_error.argtypes = [vp, ctypes.POINTER(i)]
         L.favor_device_error.restype = ctypes.c_int
+        L.favor_attn_bidir_noalloc.argtypes = [vp, i, i, i, i, i, i, f, vp, vp, vp, vp, i, i, vp]
+        L.favor_attn_bidir_noalloc.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -155,6 +157,17 @@ def favor_attn_bidir(h, q, k, v, out, B, L, stream=None) -> None:
 def favor_attn_causal(h, q, k, v, out, B, L, stream=None) -> None:
     _check(lib().favor_attn_causal(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), int(B), int(L), _stream(stream, q)),
            "favor_attn_causal")
+
+
+def favor_attn_bidir_noalloc(omega, H, m, d, dv, kind, dtype, data_scale, q, k, v, out, B, L,
+                             stream=None) -> None:
+    """Handle-free bidirectional call on the library's fixed device scratch; ``omega`` is a DEVICE
+    float32 [H, m, d] tensor or address."""
+    kind = KIND_CODES.get(kind, kind)
+    dtype = DTYPE_CODES.get(dtype, dtype)
+    _check(lib().favor_attn_bidir_noalloc(_ptr(omega), int(H), int(m), int(d), int(dv), int(kind), int(dtype),
+                                          float(data_scale), _ptr(q), _ptr(k), _ptr(v), _ptr(out), int(B), int(L),
+                                          _stream(stream, q)), "favor_attn_bidir_noalloc")
 
 
 def favor_destroy(h) -> None:
