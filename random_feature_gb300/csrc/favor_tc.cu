@@ -12,9 +12,8 @@
 // Tensor-memory use (512 columns, lane = tile row):
 //   state kernel : [0,256) projection halves P0, P1 | [256,416) [S | z] halves (2 x 80 columns)
 //   readout      : [0,256) projection, then Phi_Q as packed bf16 in [0,128) | [128,208) output num|den
-//   causal       : [0,128) Phi_Q bf16 (from a 256-column projection) | [128,256) key projection
-//                  half, then Phi_Q Phi_K^T, then its masked bf16 copy | [256,336) output |
-//                  [336,368) z halves | [384,512) S halves
+//   causal       : three rotating 128-column slots (query projection halves -> packed Phi_Q and
+//                  num; key projection halves -> A -> packed tril(A)) | [384,512) S halves
 #include <cmath>
 #include <cstddef>
 #include <cstring>
@@ -40,7 +39,6 @@ constexpr uint32_t kPhiBlock = kTile * 128;       // one 64-column image of a 12
 constexpr uint32_t kSBytes = kM * 128;            // S~ image [256 rows][64] = 32 KB
 constexpr uint32_t kZBytes = kM * 32;             // z~ image [256 rows][16] = 8 KB
 constexpr uint32_t kImageBytes = kSBytes + kZBytes;
-constexpr uint32_t kOnesBlock = kTile * 128;      // [128 rows][64] SW128 image: column 0 = 1, rest 0
 constexpr float kLog2e = 1.4426950408889634f;
 
 // byte offset of chunk `c` (16 B) of row `r` inside an SW128 image
@@ -55,16 +53,6 @@ struct Bars {
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-// The second 64-column block of the MN-major operand [V | 1 | 0 ...]: in row j
-// only column 0 (logical chunk 0, stored at chunk j & 7) holds bf16 1.0.
-__device__ __forceinline__ void fill_ones_block(uint8_t* blk, int t, int nt) {
-    uint32_t* w = reinterpret_cast<uint32_t*>(blk);
-    for (int i = t; i < (int)(kOnesBlock / 4); i += nt) {
-        const int r = i / 32, chunk = (i % 32) / 4, word = i % 4;
-        w[i] = (chunk == (r & 7) && word == 0) ? 0x00003F80u : 0u;
-    }
 }
 
 // Squared norm of row `r` of a bf16 SW128 tile.
@@ -133,68 +121,11 @@ __device__ __forceinline__ void key_features32(const uint32_t (&p)[32], float a,
     }
 }
 
-// Key features for 64 consecutive projection columns -> 32 packed bf16 words.
-// Dead rows (past L) get c = -inf for positive features (exp -> 0); for ReLU
-// their projection is already 0 (TMA fills rows past L with zeros).
-template <int KIND>
-__device__ __forceinline__ void key_features64(const uint32_t (&p)[64], float a, float c, uint32_t (&w)[32]) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        float f0, f1;
-        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-            f0 = ex2(fmaf(__uint_as_float(p[2 * i]), a, c));
-            f1 = ex2(fmaf(__uint_as_float(p[2 * i + 1]), a, c));
-        } else {
-            f0 = fmaxf(__uint_as_float(p[2 * i]), 0.f);
-            f1 = fmaxf(__uint_as_float(p[2 * i + 1]), 0.f);
-        }
-        w[i] = pack_bf16(f0, f1);
-    }
-}
-
-// Write 32 packed words (64 features, one full SW128 row) into row r of image `blk`.
-__device__ __forceinline__ void store_feat64(uint32_t blk, uint32_t r, const uint32_t (&w)[32]) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-        st_shared_v4(blk + sw128(r, q), w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-}
-
-// Partial squared norm over chunks [c0, c0+4) of row r of a bf16 SW128 tile.
-__device__ __forceinline__ float row_sqnorm_half(uint32_t tile, uint32_t r, uint32_t c0) {
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (uint32_t c = c0; c < c0 + 4; ++c) {
-        uint4 v = ld_shared_v4(tile + sw128(r, c));
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float lo = bf16lo(w[i]), hi = bf16hi(w[i]);
-            a0 = fmaf(lo, lo, a0);
-            a1 = fmaf(hi, hi, a1);
-        }
-    }
-    return a0 + a1;
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
     uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
     uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
     tmem_ld32(taddr, lo);
     tmem_ld32(taddr + 32, hi);
-}
-
-// Write 16 packed words (32 features starting at feature f0) into row r of a
-// [128 x 256] feature tile made of four SW128 images.
-__device__ __forceinline__ void store_feat32(uint32_t phi, uint32_t r, int f0, const uint32_t (&w)[16]) {
-    const uint32_t blk = phi + (uint32_t)(f0 / 64) * kPhiBlock;
-    const uint32_t c0 = (uint32_t)(f0 % 64) / 8;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        st_shared_v4(blk + sw128(r, c0 + q), w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
 }
 
 // Query features of one row into packed bf16 in tensor memory, in place:
@@ -265,18 +196,6 @@ __device__ __forceinline__ void store_output_row(uint32_t tl, __nv_bfloat16* dst
         v.w = pack_bf16(__uint_as_float(n1[8 * q + 6]) * inv, __uint_as_float(n1[8 * q + 7]) * inv);
         o[4 + q] = v;
     }
-}
-
-// Row r of the S~ / z~ operand images from 64 fp32 S values and z.
-__device__ __forceinline__ void store_state_row(uint32_t simg, uint32_t zimg, uint32_t r, const float* sv,
-                                                float z) {
-#pragma unroll
-    for (uint32_t c = 0; c < 8; ++c)
-        st_shared_v4(simg + sw128(r, c), pack_bf16(sv[8 * c], sv[8 * c + 1]), pack_bf16(sv[8 * c + 2], sv[8 * c + 3]),
-                     pack_bf16(sv[8 * c + 4], sv[8 * c + 5]), pack_bf16(sv[8 * c + 6], sv[8 * c + 7]));
-    const uint32_t zz = pack_bf16(z, z);
-    st_shared_v4(zimg + r * 32, zz, zz, zz, zz);
-    st_shared_v4(zimg + r * 32 + 16, zz, zz, zz, zz);
 }
 
 // ======================================================== persistent ranges
@@ -731,31 +650,256 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 // ===================================================================== causal
 // Persistent over ranges, chunks of 128 tokens.  For chunk t of head bh with
 // state S(t), z(t) (the sums over all earlier keys of the head):
-//   O = Phi_Q [S~ | z~](t) + tril(Phi_Q Phi_K^T) [V | 1]      out = O[:, :64] / O[:, 64]
-//   S(t+1) = S(t) + Phi_K^T V,   z(t+1) = z(t) + Phi_K^T 1
+//   num = Phi_Q S~(t) + tril(Phi_Q Phi_K^T) V       (tensor cores)
+//   den = Phi_Q z(t)  + rowsum tril(Phi_Q Phi_K^T)  (fp32 on the CUDA cores, from the same
+//                                                    bf16-rounded Phi_Q and tril(A) the numerator uses)
+//   out = num / den,   S(t+1) = S(t) + Phi_K^T V,   z(t+1) = z(t) + Phi_K^T 1
 // (App. B.1 Eq. 11 of Rethinking Attention with Performers, taken chunk by chunk).
-//   warp 0: TMA producer (single Q, K, V buffers, refilled as soon as each is consumed)
-//   warp 1: projection MMAs  P_Q = Q omega^T (lane = query), P_K^T = omega K^T (+ key offsets)
-//   warp 2: MMAs A = Phi_Q Phi_K^T and the intra-chunk term
-//   warp 3: MMAs for the inter-chunk term and the state update
-//   warps 4..7 (lane = query of the chunk): key norms, query features, causal mask, output
-//   warps 8..11 (lane = feature, one in each half): key features, z, state refresh
-// Tensor memory: [0,256) P_Q -> Phi_Q packed in [0,128); A in [128,256) -> masked packed in [128,192)
-//                [256,384) P_K^T half slot (feature x token), then O in [256,336)
-//                [384,512) S halves (fp32, lane = feature)
-// Shared memory holds Phi_K as [feature][token] (MN-major B of A, K-major A of the
-// state update) and [S~ | z~]^T as a K-major [80][256] bf16 image (rows 65..79 zero).
+//
+// Roles (384 threads):
+//   warp 0: TMA producer; lanes 0, 1, 2 own the Q, K, V tiles, lane 0 also omega
+//   warp 1: MMAs P_Q = Q omega^T, one 128-feature half at a time
+//   warp 2: MMAs P_K^T = omega K^T (+ key offsets) per half, then S += Phi_K^T V
+//   warp 3: MMAs A = Phi_Q Phi_K^T, num = Phi_Q S~, num += tril(A) V
+//   warps 4..7  (lane = query): query features and Phi_Q z, causal mask and its row sums, output
+//   warps 8..11 (lane = key for the norms, = feature otherwise): key offsets, key
+//               features and z, S~ / z~ refresh from the fp32 state
+//
+// Tensor memory: three rotating 128-column slots and the fp32 state in
+// [384,512) (two halves of 64 columns, lane = feature).  Chunk t uses slots
+//   X: P_Q half 0 -> Phi_Q half 0 packed in [0,64); num in [64,128)
+//   Y: P_Q half 1 -> Phi_Q half 1 packed in [0,64)
+//   Z: P_K^T half 0, half 1, then A, then tril(A) packed in [0,64)
+// and chunk t+1 takes X' = Z (free once the intra term has read tril(A)),
+// Y' = X (free once num was read), Z' = Y (free once A and the inter term have
+// read Phi_Q), so the projections of chunk t+1 overlap the tail of chunk t.
+//
+// Query shift: a half's features are exp2(a p - c) with an integer c.  Half 0
+// takes c0 = ceil(a max p) + kQMargin; half 1 keeps c0 unless its own maximum
+// exceeds it, and then takes c1 = ceil(a max p) and multiplies the packed half 0
+// by 2^(c0 - c1), which is exact in bf16.  Every feature is at most 1 and the
+// largest of a row at least 2^-(kQMargin+1), as with a row-max shift; the
+// common factor cancels between num and den.
 constexpr int kCausalThreads = 384;
-constexpr uint32_t kStImage = 80 * 128;   // one 64-feature K-block of [S~ | z~]^T: 80 rows x 128 B
+constexpr float kQMargin = 16.f;
 
 struct CaBars {
-    uint64_t q_full, k_full, v_full, q_empty, k_empty, v_empty;
-    uint64_t w_full, w_empty, ext_full;
-    uint64_t pq_full, phiq_full, pk_full, pk_empty, pk_done, phik_full, phik_empty;
-    uint64_t a_full, am_full, inter_done, o_full, o_empty;
-    uint64_t s_full, s_ready, st_full;
+    uint64_t q_full, k_full, v_full, q_empty, k_empty, v_empty, w_full, w_empty;
+    uint64_t ext_full, pk_full, pk_free, phik_full, phik_free, s_full, s_ready, st_full;
+    uint64_t pq0_full, pq1_full, phiq_full, a_full, ai_done, am_full, o_full, o_empty;
     uint32_t tmem_base;
 };
+
+// Slot of role 0 (X), 1 (Y) or 2 (Z) for a chunk with index t, r3 = t mod 3.
+__device__ __forceinline__ uint32_t ca_slot(int role, int r3) {
+    int i = role - r3;
+    i += (i < 0) ? 3 : 0;
+    return 128u * (uint32_t)i;
+}
+
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&p)[128]) {
+    tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+    tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+    tmem_ld32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&p[64]));
+    tmem_ld32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&p[96]));
+}
+
+// Largest of the 128 fp32 columns at taddr (one row per thread).
+__device__ __forceinline__ float tmem_rowmax128(uint32_t taddr) {
+    uint32_t p[128];
+    tmem_ld128(taddr, p);
+    tmem_ld_wait();
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 128; i += 4) {
+        m0 = fmaxf(m0, __uint_as_float(p[i]));
+        m1 = fmaxf(m1, __uint_as_float(p[i + 1]));
+        m2 = fmaxf(m2, __uint_as_float(p[i + 2]));
+        m3 = fmaxf(m3, __uint_as_float(p[i + 3]));
+    }
+    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// Features of one query half, 32 projections at a time, packed in place into
+// the first 64 columns at taddr; returns sum_r f_r z~_r over the half's z~
+// (fp32 in shared memory at zaddr), taken over the bf16-rounded features.
+// The block loop stays rolled: the kernel's roles run different code at the
+// same time, and unrolled bodies overflow the instruction cache.
+template <int KIND>
+__device__ __noinline__ float query_half(uint32_t taddr, float a, float c, uint32_t zaddr) {
+    float d0 = 0.f, d1 = 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t p[32], w[16];
+        tmem_ld32(taddr + 32 * blk, p);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 z4a = ld_shared_v4(zaddr + 4 * (32 * blk + 8 * j));
+            const uint4 z4b = ld_shared_v4(zaddr + 4 * (32 * blk + 8 * j + 4));
+            const float zz[8] = {__uint_as_float(z4a.x), __uint_as_float(z4a.y), __uint_as_float(z4a.z),
+                                 __uint_as_float(z4a.w), __uint_as_float(z4b.x), __uint_as_float(z4b.y),
+                                 __uint_as_float(z4b.z), __uint_as_float(z4b.w)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = 8 * j + 2 * i;
+                float f0, f1;
+                if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                    f0 = ex2(fmaf(__uint_as_float(p[e]), a, -c));
+                    f1 = ex2(fmaf(__uint_as_float(p[e + 1]), a, -c));
+                } else {
+                    f0 = fmaxf(__uint_as_float(p[e]), 0.f);
+                    f1 = fmaxf(__uint_as_float(p[e + 1]), 0.f);
+                }
+                const uint32_t pk = pack_bf16(f0, f1);
+                d0 = fmaf(bf16lo(pk), zz[2 * i], d0);
+                d1 = fmaf(bf16hi(pk), zz[2 * i + 1], d1);
+                w[4 * j + i] = pk;
+            }
+        }
+        // packed block blk lands in columns [16 blk, 16 blk + 16), all of which were read already
+        tmem_st16(taddr + 16 * blk, w);
+    }
+    return d0 + d1;
+}
+
+// Multiply the 64 packed bf16 columns at taddr by sc (an exact power of two).
+__device__ __noinline__ void scale_packed64(uint32_t taddr, float sc) {
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t w[16];
+        tmem_ld16(taddr + 16 * blk, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16(bf16lo(w[i]) * sc, bf16hi(w[i]) * sc);
+        tmem_st16(taddr + 16 * blk, w);
+    }
+}
+
+// Causal mask of one row of A (fp32, 128 columns at taddr), packed in place into
+// [0,64); returns the row sum of the kept bf16-rounded values.  Blocks of keys
+// entirely after every row of the warp (blk > q) are written as zeros unread.
+__device__ __noinline__ float mask_row(uint32_t taddr, int row, int q) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t w[16];
+        if (blk <= q) {
+            uint32_t p[32];
+            tmem_ld32(taddr + 32 * blk, p);
+            tmem_ld_wait();
+            const int lim = row - 32 * blk;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float f0 = (2 * i <= lim) ? __uint_as_float(p[2 * i]) : 0.f;
+                const float f1 = (2 * i + 1 <= lim) ? __uint_as_float(p[2 * i + 1]) : 0.f;
+                w[i] = pack_bf16(f0, f1);
+                s0 += bf16lo(w[i]);
+                s1 += bf16hi(w[i]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = 0u;
+        }
+        tmem_st16(taddr + 16 * blk, w);
+    }
+    return s0 + s1;
+}
+
+// out row = num / den, num = 64 fp32 columns at taddr.
+__device__ __noinline__ void store_out_row(uint32_t taddr, __nv_bfloat16* dst, bool live, float den) {
+    const float inv = den != 0.f ? 1.f / den : 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 2; ++blk) {
+        uint32_t nv[32];
+        tmem_ld32(taddr + 32 * blk, nv);
+        tmem_ld_wait();
+        if (live) {
+            uint4* o = reinterpret_cast<uint4*>(dst) + 4 * blk;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint4 v;
+                v.x = pack_bf16(__uint_as_float(nv[8 * c + 0]) * inv, __uint_as_float(nv[8 * c + 1]) * inv);
+                v.y = pack_bf16(__uint_as_float(nv[8 * c + 2]) * inv, __uint_as_float(nv[8 * c + 3]) * inv);
+                v.z = pack_bf16(__uint_as_float(nv[8 * c + 4]) * inv, __uint_as_float(nv[8 * c + 5]) * inv);
+                v.w = pack_bf16(__uint_as_float(nv[8 * c + 6]) * inv, __uint_as_float(nv[8 * c + 7]) * inv);
+                o[c] = v;
+            }
+        }
+    }
+}
+
+// Key features of feature row r over the 128 tokens at taddr (fp32, offsets
+// already folded in) into Phi_K [feature][token] (two token blocks of 64);
+// returns their sum.
+template <int KIND>
+__device__ __noinline__ float key_row(uint32_t taddr, uint32_t phi, uint32_t r, float a) {
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t p[32];
+        tmem_ld32(taddr + 32 * blk, p);
+        tmem_ld_wait();
+        const uint32_t base = phi + (uint32_t)(blk >> 1) * 2 * kPhiBlock;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x0 = __uint_as_float(p[8 * cc + 2 * i]);
+                const float x1 = __uint_as_float(p[8 * cc + 2 * i + 1]);
+                float f0, f1;
+                if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                    f0 = ex2(x0 * a);
+                    f1 = ex2(x1 * a);
+                } else {
+                    f0 = fmaxf(x0, 0.f);
+                    f1 = fmaxf(x1, 0.f);
+                }
+                z0 += f0;
+                z1 += f1;
+                w4[i] = pack_bf16(f0, f1);
+            }
+            st_shared_v4(base + sw128(r, (uint32_t)(4 * (blk & 1) + cc)), w4[0], w4[1], w4[2], w4[3]);
+        }
+    }
+    return z0 + z1;
+}
+
+// S~ image row r and z~[r] from the fp32 state row (64 columns at taddr).
+__device__ __noinline__ void refresh_row(uint32_t taddr, uint32_t img, uint32_t r) {
+#pragma unroll 1
+    for (int blk = 0; blk < 2; ++blk) {
+        uint32_t sv[32];
+        tmem_ld32(taddr + 32 * blk, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (uint32_t c = 0; c < 4; ++c)
+            st_shared_v4(img + sw128(r, 4 * blk + c),
+                         pack_bf16(__uint_as_float(sv[8 * c]), __uint_as_float(sv[8 * c + 1])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 2]), __uint_as_float(sv[8 * c + 3])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 4]), __uint_as_float(sv[8 * c + 5])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 6]), __uint_as_float(sv[8 * c + 7])));
+    }
+}
+
+// fp32 state row (64 columns at taddr), S~ image row r from a prefix row in global memory.
+__device__ __noinline__ void load_prefix_row(const float* src, uint32_t taddr, uint32_t img, uint32_t r) {
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t sv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(src[16 * blk + i]);
+        tmem_st16(taddr + 16 * blk, sv);
+#pragma unroll
+        for (uint32_t c = 0; c < 2; ++c)
+            st_shared_v4(img + sw128(r, 2 * blk + c),
+                         pack_bf16(__uint_as_float(sv[8 * c]), __uint_as_float(sv[8 * c + 1])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 2]), __uint_as_float(sv[8 * c + 3])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 4]), __uint_as_float(sv[8 * c + 5])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 6]), __uint_as_float(sv[8 * c + 7])));
+    }
+}
 
 template <int KIND>
 __global__ void __launch_bounds__(kCausalThreads, 1)
@@ -770,12 +914,12 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t s_q = s_w + kOmegaBytes;
     const uint32_t s_k = s_q + kTileBytes;
     const uint32_t s_v = s_k + kTileBytes;
-    const uint32_t s_phi = s_v + kTileBytes;                  // [256 features][128 tokens]: 2 blocks of 64 tokens (32 KB each)
-    const uint32_t s_st = s_phi + 4 * kPhiBlock;              // [S~|z~]^T: 4 K-blocks of kStImage
-    const uint32_t s_one = s_st + 4 * kStImage;               // ones block
-    const uint32_t s_ext = s_one + kOnesBlock;                // K-side offsets [128][16]
+    const uint32_t s_phi = s_v + kTileBytes;                  // Phi_K [256 features][128 tokens]: 2 blocks of 64 tokens
+    const uint32_t s_st = s_phi + 4 * kPhiBlock;              // S~ [256 features][64], MN-major B operand
+    const uint32_t s_ext = s_st + kSBytes;                    // key offsets [128][16]
     const uint32_t s_wext = s_ext + kExtStage;                // omega side [256][16]
-    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_wext - s_w) + kExtOmega);
+    const uint32_t s_z = s_wext + kExtOmega;                  // z~ fp32 [256]
+    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_z - s_w) + kM * 4);
     const int cta = blockIdx.x;
     const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
     const int n = g1 - g0;
@@ -785,7 +929,8 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (threadIdx.x == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bars);
         // order and arrival counts follow the fields of CaBars
-        const int counts[] = {1, 1, 1, 1, 5, 2,   1, 1, 4,   1, 4, 1, 4, 4, 4, 2,   1, 4, 1, 1, 4,   1, 4, 4};
+        // (each barrier completes at most once per chunk, so a parity wait cannot miss a phase)
+        const int counts[] = {1, 1, 1, 1, 5, 2, 1, 2,   4, 1, 4, 4, 2, 1, 4, 4,   1, 1, 4, 1, 1, 4, 1, 4};
         static_assert(sizeof(counts) / sizeof(int) * sizeof(uint64_t) == offsetof(CaBars, tmem_base), "barrier table");
         for (int i = 0; i < (int)(sizeof(counts) / sizeof(int)); ++i) mbar_init(b + i, counts[i]);
         fence_mbar_init();
@@ -796,9 +941,6 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     }
     if (warp >= 4) {
         const int t = threadIdx.x - 128, nt = kCausalThreads - 128;
-        fill_ones_block(sm + (s_one - s_w), t, nt);
-        uint32_t* z = reinterpret_cast<uint32_t*>(sm + (s_st - s_w));
-        for (int i = t; i < (int)(4 * kStImage / 4); i += nt) z[i] = 0u;
         uint32_t* e = reinterpret_cast<uint32_t*>(sm + (s_ext - s_w));
         for (int i = t; i < (int)(kExtStage / 4); i += nt) e[i] = 0u;
         uint32_t* wx = reinterpret_cast<uint32_t*>(sm + (s_wext - s_w));
@@ -813,138 +955,127 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // One thread keeps the Q, K and V streams independent: it polls each
+        // stream's empty barrier and issues whichever next load is free.  Lane
+        // 0 also reloads omega at a head change, before the first Q tile of
+        // the new head.  Gives up after about two seconds without progress.
         if (lane == 0) {
+            const CUtensorMap* maps[3] = {&tm_q, &tm_k, &tm_v};
+            uint64_t* fulls[3] = {&bars->q_full, &bars->k_full, &bars->v_full};
+            uint64_t* empties[3] = {&bars->q_empty, &bars->k_empty, &bars->v_empty};
+            const uint32_t dsts[3] = {s_q - s_w, s_k - s_w, s_v - s_w};
+            int next[3] = {0, 0, 0};
             int cur_h = -1;
             uint32_t wph = 0;
-            for (int t = 0; t < n; ++t) {
-                const int g = g0 + t, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
-                const uint32_t pp = (t - 1) & 1;
-                if (h != cur_h) {
-                    if (cur_h >= 0) {
-                        if (!mbar_wait(&bars->w_empty, wph, err, 201)) break;
-                        wph ^= 1;
+            long long t0 = clock64();
+            while (next[0] < n || next[1] < n || next[2] < n) {
+                bool progress = false;
+#pragma unroll
+                for (int sidx = 0; sidx < 3; ++sidx) {
+                    const int t = next[sidx];
+                    if (t >= n) continue;
+                    if (t > 0 && !mbar_test_wait(empties[sidx], (t - 1) & 1)) continue;
+                    const int g = g0 + t, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
+                    if (sidx == 0 && h != cur_h) {
+                        if (cur_h >= 0) {
+                            if (!mbar_test_wait(&bars->w_empty, wph)) continue;
+                            wph ^= 1;
+                        }
+                        mbar_expect_tx(&bars->w_full, kOmegaBytes);
+                        tma_load_2d(sm, &tm_w, &bars->w_full, 0, h * kM);
+                        cur_h = h;
                     }
-                    mbar_expect_tx(&bars->w_full, kOmegaBytes);
-                    tma_load_2d(sm, &tm_w, &bars->w_full, 0, h * kM);
-                    cur_h = h;
+                    mbar_expect_tx(fulls[sidx], kTileBytes);
+                    tma_load_3d(sm + dsts[sidx], maps[sidx], fulls[sidx], 0, tok0, bh);
+                    next[sidx] = t + 1;
+                    progress = true;
                 }
-                if (t > 0 && !mbar_wait(&bars->q_empty, pp, err, 202)) break;
-                mbar_expect_tx(&bars->q_full, kTileBytes);
-                tma_load_3d(sm + (s_q - s_w), &tm_q, &bars->q_full, 0, tok0, bh);
-                if (t > 0 && !mbar_wait(&bars->k_empty, pp, err, 203)) break;
-                mbar_expect_tx(&bars->k_full, kTileBytes);
-                tma_load_3d(sm + (s_k - s_w), &tm_k, &bars->k_full, 0, tok0, bh);
-                if (t > 0 && !mbar_wait(&bars->v_empty, pp, err, 204)) break;
-                mbar_expect_tx(&bars->v_full, kTileBytes);
-                tma_load_3d(sm + (s_v - s_w), &tm_v, &bars->v_full, 0, tok0, bh);
+                if (progress) {
+                    t0 = clock64();
+                } else {
+                    __nanosleep(32);
+                    if (clock64() - t0 > (4LL << 30)) {
+                        atomicExch(err, 201);
+                        break;
+                    }
+                }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------ projection MMAs
+        // ------------------------------------------------- query projection MMAs
         if (lane == 0) {
-            const uint32_t id_q = make_idesc(128, 256, 0, 0);
-            const uint32_t id_k = make_idesc(128, 128, 0, 0);
+            const uint32_t id_p = make_idesc(128, 128, 0, 0);
             uint32_t wph = 0;
-            int tih = g0 % R.tph;
+            int tih = g0 % R.tph, r3 = 0;
             for (int t = 0; t < n; ++t) {
                 const uint32_t ph = t & 1, pp = (t - 1) & 1;
                 if (t == 0 || (tih == 0 && multi_head)) {
                     if (!mbar_wait(&bars->w_full, wph, err, 211)) break;
                     wph ^= 1;
                 }
-                // P_Q = Q omega^T into [0,256): the query region is free once O(t-1) was read
                 if (!mbar_wait(&bars->q_full, ph, err, 212)) break;
-                if (t > 0 && !mbar_wait(&bars->o_empty, pp, err, 213)) break;
+                // half 0 into X (= Z of the previous chunk: free once the intra term read tril(A))
+                if (t > 0 && !mbar_wait(&bars->o_full, pp, err, 213)) break;
                 tc_fence_after();
-                {
-                    const uint64_t a0 = make_desc(s_q, 16, 1024, SW_128B);
-                    const uint64_t b0 = make_desc(s_w, 16, 1024, SW_128B);
-                    mma_ss(tmem, a0, b0, id_q, 0u);
-                    mma_ss(tmem, a0 + 2, b0 + 2, id_q, 1u);
-                    mma_ss(tmem, a0 + 4, b0 + 4, id_q, 1u);
-                    mma_ss(tmem, a0 + 6, b0 + 6, id_q, 1u);
-                    mma_commit(&bars->pq_full);
-                    mma_commit(&bars->q_empty);
+                const uint64_t a0 = make_desc(s_q, 16, 1024, SW_128B);
+                const uint64_t b0 = make_desc(s_w, 16, 1024, SW_128B);
+                const uint32_t dX = tmem + ca_slot(0, r3), dY = tmem + ca_slot(1, r3);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_ss(dX, a0 + 2 * kk, b0 + 2 * kk, id_p, kk > 0 ? 1u : 0u);
+                mma_commit(&bars->pq0_full);
+                // half 1 into Y (= X of the previous chunk: free once num was read)
+                if (t > 0 && !mbar_wait(&bars->o_empty, pp, err, 214)) break;
+                tc_fence_after();
+                const uint64_t b1 = make_desc(s_w + 128 * 128, 16, 1024, SW_128B);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_ss(dY, a0 + 2 * kk, b1 + 2 * kk, id_p, kk > 0 ? 1u : 0u);
+                mma_commit(&bars->pq1_full);
+                mma_commit(&bars->q_empty);
+                if (t + 1 < n && tih == R.tph - 1 && multi_head) mma_commit(&bars->w_empty);
+                tih = (tih + 1 == R.tph) ? 0 : tih + 1;
+                r3 = (r3 == 2) ? 0 : r3 + 1;
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------- key projection + state MMAs
+        if (lane == 0) {
+            const uint32_t id_k = make_idesc(128, 128, 0, 0);
+            const uint32_t id_s = make_idesc(128, 64, 0, 1);
+            uint32_t wph = 0;
+            int tih = g0 % R.tph, r3 = 0, done = 0;
+            for (int t = 0; t < n; ++t) {
+                const uint32_t ph = t & 1, pp = (t - 1) & 1;
+                if (t == 0 || (tih == 0 && multi_head)) {
+                    if (!mbar_wait(&bars->w_full, wph, err, 221)) break;
+                    wph ^= 1;
                 }
-                // P_K^T halves (features x tokens, + key offsets) through the slot [256,384)
-                if (!mbar_wait(&bars->k_full, ph, err, 214)) break;
-                if (!mbar_wait(&bars->ext_full, ph, err, 215)) break;
+                if (!mbar_wait(&bars->k_full, ph, err, 222)) break;
+                if (!mbar_wait(&bars->ext_full, ph, err, 223)) break;
+                // Z (= Y of the previous chunk) is free once A and the inter term read Phi_Q
+                if (t > 0 && !mbar_wait(&bars->ai_done, pp, err, 224)) break;
+                const uint32_t dZ = tmem + ca_slot(2, r3);
                 bool ok = true;
                 for (int hp = 0; hp < 2; ++hp) {
-                    if (hp == 1 && !mbar_wait(&bars->pk_empty, ph, err, 216)) { ok = false; break; }
+                    if (hp == 1 && !mbar_wait(&bars->pk_free, ph, err, 225)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t a0 = make_desc(s_w + hp * 128 * 128, 16, 1024, SW_128B);
                     const uint64_t b0 = make_desc(s_k, 16, 1024, SW_128B);
-                    const uint32_t d = tmem + 256;
-                    mma_ss(d, a0, b0, id_k, 0u);
-                    mma_ss(d, a0 + 2, b0 + 2, id_k, 1u);
-                    mma_ss(d, a0 + 4, b0 + 4, id_k, 1u);
-                    mma_ss(d, a0 + 6, b0 + 6, id_k, 1u);
-                    mma_ss(d, make_desc(s_wext + hp * 128 * 32, 128, 256, SW_NONE), make_desc(s_ext, 128, 256, SW_NONE),
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) mma_ss(dZ, a0 + 2 * kk, b0 + 2 * kk, id_k, kk > 0 ? 1u : 0u);
+                    mma_ss(dZ, make_desc(s_wext + hp * 128 * 32, 128, 256, SW_NONE), make_desc(s_ext, 128, 256, SW_NONE),
                            id_k, 1u);
                     mma_commit(&bars->pk_full);
                 }
                 if (!ok) break;
                 mma_commit(&bars->k_empty);
                 if (t + 1 < n && tih == R.tph - 1 && multi_head) mma_commit(&bars->w_empty);
-                tih = (tih + 1 == R.tph) ? 0 : tih + 1;
-            }
-        }
-    } else if (warp == 2) {
-        // ------------------------------------------------ A = Phi_Q Phi_K^T, intra
-        if (lane == 0) {
-            const uint32_t id_a = make_idesc(128, 128, 0, 1);
-            const uint32_t id_v = make_idesc(128, 80, 0, 1);
-            for (int t = 0; t < n; ++t) {
-                const uint32_t ph = t & 1;
-                if (!mbar_wait(&bars->phiq_full, ph, err, 221)) break;
-                if (!mbar_wait(&bars->phik_full, ph, err, 222)) break;
-                tc_fence_after();
-                // B = Phi_K [feature][token]: N = token (2 blocks of 64, LBO), K = feature (16 rows per step)
-                const uint64_t b0 = make_desc(s_phi, 2 * kPhiBlock, 1024, SW_128B);
-                mma_ts(tmem + 128, tmem, b0, id_a, 0u);
-#pragma unroll
-                for (int kk = 1; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 8 * kk, b0 + 128 * kk, id_a, 1u);
-                mma_commit(&bars->a_full);
-                mma_commit(&bars->phik_empty);
-                // intra: O += masked A [V | 1], after the inter term initialised O
-                if (!mbar_wait(&bars->am_full, ph, err, 223)) break;
-                if (!mbar_wait(&bars->inter_done, ph, err, 224)) break;
-                if (!mbar_wait(&bars->v_full, ph, err, 225)) break;
-                tc_fence_after();
-                const uint64_t bv = make_desc(s_v, s_one - s_v, 1024, SW_128B);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) mma_ts(tmem + 256, tmem + 128 + 8 * kk, bv + 128 * kk, id_v, 1u);
-                mma_commit(&bars->o_full);
-                mma_commit(&bars->v_empty);
-            }
-        }
-    } else if (warp == 3) {
-        // ------------------------------------------------------ inter, state update
-        if (lane == 0) {
-            const uint32_t id_o = make_idesc(128, 80, 0, 0);
-            const uint32_t id_s = make_idesc(128, 64, 0, 1);
-            for (int t = 0; t < n; ++t) {
-                const uint32_t ph = t & 1;
-                // inter: O = Phi_Q [S~ | z~] into the free key slot
-                if (!mbar_wait(&bars->phiq_full, ph, err, 231)) break;
-                if (!mbar_wait(&bars->st_full, ph, err, 232)) break;
-                if (!mbar_wait(&bars->pk_done, ph, err, 233)) break;
-                tc_fence_after();
-                {
-                    const uint64_t b0 = make_desc(s_st, 16, 1024, SW_128B);   // K-major, rows = 80 output columns
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk)
-                        mma_ts(tmem + 256, tmem + 8 * kk, b0 + (uint64_t)(((kk >> 2) * kStImage + (kk & 3) * 32) >> 4),
-                               id_o, kk > 0 ? 1u : 0u);
-                    mma_commit(&bars->inter_done);
-                }
                 // state: S_h += Phi_K^T_h V (A = Phi_K rows of half h, K-major over tokens)
-                if (!mbar_wait(&bars->phik_full, ph, err, 234)) break;
-                if (!mbar_wait(&bars->v_full, ph, err, 235)) break;
-                if (!mbar_wait(&bars->s_ready, ph, err, 236)) break;
+                if (!mbar_wait(&bars->phik_full, ph, err, 226)) break;
+                if (!mbar_wait(&bars->v_full, ph, err, 227)) break;
+                if (!mbar_wait(&bars->s_ready, ph, err, 228)) break;
                 tc_fence_after();
                 const uint64_t bv = make_desc(s_v, 8192, 1024, SW_128B);
+#pragma unroll
                 for (int hp = 0; hp < 2; ++hp) {
                     const uint64_t a0 = make_desc(s_phi + hp * 128 * 128, 16, 1024, SW_128B);
                     const uint32_t d = tmem + 384 + 64 * hp;
@@ -954,8 +1085,52 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                                id_s, 1u);
                 }
                 mma_commit(&bars->s_full);
-                mma_commit(&bars->phik_empty);
+                mma_commit(&bars->phik_free);
                 mma_commit(&bars->v_empty);
+                tih = (tih + 1 == R.tph) ? 0 : tih + 1;
+                r3 = (r3 == 2) ? 0 : r3 + 1;
+                done = t + 1;
+            }
+            // nobody else waits for the last state update: let it finish before tensor memory is freed
+            if (n > 0 && done == n) mbar_wait(&bars->s_full, (n - 1) & 1, err, 229);
+        }
+    } else if (warp == 3) {
+        // ----------------------------------------------- A, inter and intra MMAs
+        if (lane == 0) {
+            const uint32_t id_a = make_idesc(128, 128, 0, 1);
+            const uint32_t id_o = make_idesc(128, 64, 0, 1);
+            int r3 = 0;
+            for (int t = 0; t < n; ++t) {
+                const uint32_t ph = t & 1;
+                const uint32_t dX = tmem + ca_slot(0, r3), dY = tmem + ca_slot(1, r3), dZ = tmem + ca_slot(2, r3);
+                if (!mbar_wait(&bars->phiq_full, ph, err, 231)) break;
+                if (!mbar_wait(&bars->phik_full, ph, err, 232)) break;
+                tc_fence_after();
+                // A = Phi_Q Phi_K^T into Z; B = Phi_K [feature][token]: N = token (2 blocks, LBO), K = feature
+                const uint64_t bk = make_desc(s_phi, 2 * kPhiBlock, 1024, SW_128B);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk)
+                    mma_ts(dZ, kk < 8 ? dX + 8 * kk : dY + 8 * (kk - 8), bk + 128 * kk, id_a, kk > 0 ? 1u : 0u);
+                mma_commit(&bars->a_full);
+                mma_commit(&bars->phik_free);
+                // inter: num = Phi_Q S~ into X[64,128)
+                if (!mbar_wait(&bars->st_full, ph, err, 233)) break;
+                tc_fence_after();
+                const uint64_t bs = make_desc(s_st, 8192, 1024, SW_128B);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk)
+                    mma_ts(dX + 64, kk < 8 ? dX + 8 * kk : dY + 8 * (kk - 8), bs + 128 * kk, id_o, kk > 0 ? 1u : 0u);
+                mma_commit(&bars->ai_done);
+                // intra: num += tril(A) V
+                if (!mbar_wait(&bars->am_full, ph, err, 234)) break;
+                if (!mbar_wait(&bars->v_full, ph, err, 235)) break;
+                tc_fence_after();
+                const uint64_t bv = make_desc(s_v, 8192, 1024, SW_128B);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) mma_ts(dX + 64, dZ + 8 * kk, bv + 128 * kk, id_o, 1u);
+                mma_commit(&bars->o_full);
+                mma_commit(&bars->v_empty);
+                r3 = (r3 == 2) ? 0 : r3 + 1;
             }
         }
     } else if (warp < 8) {
@@ -963,22 +1138,85 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int q = warp & 3;
         const uint32_t row = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-        int kap_h = -1;
-        float kap = 0.f;
+        int r3 = 0;
         for (int t = 0; t < n; ++t) {
             const uint32_t ph = t & 1;
+            const int g = g0 + t, bh = g / R.tph, tok0 = (g % R.tph) * kTile;
+            const uint32_t X = tl + ca_slot(0, r3), Y = tl + ca_slot(1, r3), Z = tl + ca_slot(2, r3);
+            if (!mbar_wait(&bars->st_full, ph, err, 241)) break;   // z~ of this chunk's state
+            if (!mbar_wait(&bars->pq0_full, ph, err, 242)) break;
+            tc_fence_after();
+            float c0 = 0.f, den;
+            if (POS) c0 = ceilf(tmem_rowmax128(X) * a) + kQMargin;
+            den = query_half<KIND>(X, a, c0, s_z);
+            if (!mbar_wait(&bars->pq1_full, ph, err, 243)) break;
+            tc_fence_after();
+            {
+                float c1 = c0;
+                if (POS) {
+                    const float need = ceilf(tmem_rowmax128(Y) * a);
+                    c1 = need > c0 ? need : c0;
+                }
+                const float d1 = query_half<KIND>(Y, a, c1, s_z + 4 * 128);
+                if (POS && __any_sync(0xffffffffu, c1 > c0)) {
+                    // half 1 holds the row's maximum: scale the packed half 0 by 2^(c0 - c1) (exact)
+                    const int e = (int)(c0 - c1);
+                    const float sc = e >= -126 ? __int_as_float((127 + e) << 23) : 0.f;
+                    tmem_st_wait();
+                    scale_packed64(X, sc);
+                    den *= sc;
+                }
+                den += d1;
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->phiq_full);
+            // causal mask: keep key j <= query row, packed in place into Z[0,64); row sums into den
+            if (!mbar_wait(&bars->a_full, ph, err, 244)) break;
+            tc_fence_after();
+            den += mask_row(Z, (int)row, q);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->am_full);
+            // output row: num / den
+            if (!mbar_wait(&bars->o_full, ph, err, 245)) break;
+            tc_fence_after();
+            {
+                const int tok = tok0 + (int)row;
+                store_out_row(X + 64, out + ((size_t)bh * L + (tok < L ? tok : 0)) * kDV, tok < L, den);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->o_empty);
+            r3 = (r3 == 2) ? 0 : r3 + 1;
+        }
+    } else {
+        // ------------------------------------------------------------ key side
+        // thread owns key row r0 of the tile (offsets) and features r0, r0 + 128
+        const int q = warp & 3;
+        const uint32_t r0 = 32 * q + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+        float* zs = reinterpret_cast<float*>(sm + (s_z - s_w));
+        float z[2] = {0.f, 0.f};
+        int cur_bh = -1, kap_h = -1, r3 = 0;
+        float kap = 0.f;
+        for (int t = 0; t < n; ++t) {
+            const uint32_t ph = t & 1, pp = (t - 1) & 1;
             const int g = g0 + t, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
-            // key norm of this row -> offset c/a as bf16 hi + lo (positive features)
-            if (!mbar_wait(&bars->k_full, ph, err, 241)) break;
+            const uint32_t Z = tl + ca_slot(2, r3);
+            // key offsets of this chunk: -(s^2 ||k||^2 / 2 + kappa_h) / s as bf16 hi + lo
+            if (!mbar_wait(&bars->k_full, ph, err, 251)) break;
             if (POS) {
                 if (h != kap_h) {
                     kap = __ldg(kshift + h);
                     kap_h = h;
                 }
-                const float nrm = row_sqnorm(s_k, row);
-                const float x = (tok0 + (int)row < L) ? -(0.5f * s * s * nrm + kap) / s : -1.0e30f;
+                const float nrm = row_sqnorm(s_k, r0);
+                const float x = (tok0 + (int)r0 < L) ? -(0.5f * s * s * nrm + kap) / s : -1.0e30f;
                 const float hi = __bfloat162float(__float2bfloat16_rn(x));
-                st_shared_v4(s_ext + ext_row(row), pack_bf16(hi, x - hi), 0u, 0u, 0u);
+                st_shared_v4(s_ext + ext_row(r0), pack_bf16(hi, x - hi), 0u, 0u, 0u);
                 fence_async_smem();
             }
             __syncwarp();
@@ -986,199 +1224,61 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 mbar_arrive(&bars->ext_full);
                 mbar_arrive(&bars->k_empty);
             }
-            // query features (row max over the 256 features), packed in place into [0,128)
-            if (!mbar_wait(&bars->pq_full, ph, err, 242)) break;
-            tc_fence_after();
-            float mx = 0.f;
-            if (POS) {
-                mx = -INFINITY;
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t p[32];
-                    tmem_ld32(tl + 32 * c, p);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(p[i]));
-                }
+            // this chunk's state: the piece's prefix at a piece start, else S(t) from the master
+            if (t > 0) {
+                if (!mbar_wait(&bars->s_full, pp, err, 252)) break;
+                if (!mbar_wait(&bars->ai_done, pp, err, 253)) break;
+                tc_fence_after();
             }
-            const float cm = -mx * a;
-            for (int c = 0; c < 8; ++c) {
-                uint32_t p[32], w[16];
-                tmem_ld32(tl + 32 * c, p);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float f0, f1;
-                    if (POS) {
-                        f0 = ex2(fmaf(__uint_as_float(p[2 * i]), a, cm));
-                        f1 = ex2(fmaf(__uint_as_float(p[2 * i + 1]), a, cm));
-                    } else {
-                        f0 = fmaxf(__uint_as_float(p[2 * i]), 0.f);
-                        f1 = fmaxf(__uint_as_float(p[2 * i + 1]), 0.f);
-                    }
-                    w[i] = pack_bf16(f0, f1);
-                }
-                tmem_st16(tl + 16 * c, w);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->phiq_full);
-            // causal mask: keep key j <= query row, packed in place into [128,192)
-            if (!mbar_wait(&bars->a_full, ph, err, 243)) break;
-            tc_fence_after();
-            for (int c = 0; c < 4; ++c) {
-                uint32_t p[32], w[16];
-                tmem_ld32(tl + 128 + 32 * c, p);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int j = 32 * c + 2 * i;
-                    const float f0 = (j <= (int)row) ? __uint_as_float(p[2 * i]) : 0.f;
-                    const float f1 = (j + 1 <= (int)row) ? __uint_as_float(p[2 * i + 1]) : 0.f;
-                    w[i] = pack_bf16(f0, f1);
-                }
-                tmem_st16(tl + 128 + 16 * c, w);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->am_full);
-            // output row
-            if (!mbar_wait(&bars->o_full, ph, err, 244)) break;
-            tc_fence_after();
-            {
-                const int tok = tok0 + (int)row;
-                store_output_row(tl + 256, out + ((size_t)bh * L + tok) * kDV, tok < L);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->o_empty);
-        }
-    } else {
-        // ------------------------------------------------------------ key side
-        // thread owns feature r0 = 32q + lane (half 0) and r0 + 128 (half 1)
-        const int q = warp & 3;
-        const uint32_t r0 = 32 * q + lane;
-        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-        float z[2] = {0.f, 0.f};
-        int cur_bh = -1;
-        for (int t = 0; t < n; ++t) {
-            const uint32_t ph = t & 1;
-            const int g = g0 + t, bh = g / R.tph;
             if (bh != cur_bh) {
-                // a new head piece: state = its exclusive prefix (master S, image, z).
-                // The previous chunk's state update and inter term are complete.
-                if (t > 0) {
-                    if (!mbar_wait(&bars->s_full, (t - 1) & 1, err, 251)) break;
-                    if (!mbar_wait(&bars->inter_done, (t - 1) & 1, err, 252)) break;
-                    tc_fence_after();
-                }
                 const float* pre = prefix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1));
+#pragma unroll 1
                 for (int hp = 0; hp < 2; ++hp) {
                     const uint32_t r = r0 + 128 * hp;
-                    uint32_t w[16];
-                    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(pre[(size_t)r * (kDV + 1) + 16 * c + i]);
-                        tmem_st16(tl + 384 + 64 * hp + 16 * c, w);
-                    }
+                    load_prefix_row(pre + (size_t)r * (kDV + 1), tl + 384 + 64 * hp, s_st, r);
                     z[hp] = pre[(size_t)r * (kDV + 1) + 64];
-                    // image column r: rows e = 0..63 from S, row 64 = z
-                    uint8_t* img = sm + (s_st - s_w) + (r >> 6) * kStImage;
-                    const uint32_t cr = (r & 63) >> 3, pr = (r & 7) * 2;
-                    for (int e = 0; e < 64; ++e)
-                        *reinterpret_cast<__nv_bfloat16*>(img + e * 128 + ((cr ^ (e & 7)) << 4) + pr) =
-                            __float2bfloat16_rn(pre[(size_t)r * (kDV + 1) + e]);
-                    *reinterpret_cast<__nv_bfloat16*>(img + 64 * 128 + ((cr ^ 0) << 4) + pr) = __float2bfloat16_rn(z[hp]);
+                    zs[r] = z[hp];
                 }
                 tmem_st_wait();
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars->s_ready);
-                    mbar_arrive(&bars->st_full);
-                }
                 cur_bh = bh;
-            }
-            // key features of both halves -> Phi_K [feature][token] in shared memory, z
-            for (int hp = 0; hp < 2; ++hp) {
-                if (!mbar_wait(&bars->pk_full, hp, err, 253)) break;
-                tc_fence_after();
-                uint32_t p[128];
-                {
-                    uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[0]);
-                    uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[32]);
-                    uint32_t (&p2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[64]);
-                    uint32_t (&p3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[96]);
-                    tmem_ld32(tl + 256, p0);
-                    tmem_ld32(tl + 256 + 32, p1);
-                    tmem_ld32(tl + 256 + 64, p2);
-                    tmem_ld32(tl + 256 + 96, p3);
-                }
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(hp == 0 ? &bars->pk_empty : &bars->pk_done);
-                if (hp == 0 && t > 0 && !mbar_wait(&bars->phik_empty, (t - 1) & 1, err, 254)) break;
-                const uint32_t r = r0 + 128 * hp;
-                float zz0 = 0.f, zz1 = 0.f;
-#pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float x0 = __uint_as_float(p[64 * blk + 8 * c + 2 * i]);
-                            const float x1 = __uint_as_float(p[64 * blk + 8 * c + 2 * i + 1]);
-                            float f0, f1;
-                            if (POS) {
-                                f0 = ex2(x0 * a);
-                                f1 = ex2(x1 * a);
-                            } else {
-                                f0 = fmaxf(x0, 0.f);
-                                f1 = fmaxf(x1, 0.f);
-                            }
-                            zz0 += f0;
-                            zz1 += f1;
-                            w4[i] = pack_bf16(f0, f1);
-                        }
-                        st_shared_v4(s_phi + blk * 2 * kPhiBlock + sw128(r, c), w4[0], w4[1], w4[2], w4[3]);
-                    }
-                }
-                z[hp] += zz0 + zz1;
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->phik_full);
-            // state refresh for the next chunk of the same head piece
-            const bool next_same = (t + 1 < n) && ((g + 1) / R.tph) == bh;
-            if (next_same) {
-                if (!mbar_wait(&bars->s_full, ph, err, 255)) break;
-                if (!mbar_wait(&bars->inter_done, ph, err, 256)) break;
-                tc_fence_after();
+            } else {
+#pragma unroll 1
                 for (int hp = 0; hp < 2; ++hp) {
                     const uint32_t r = r0 + 128 * hp;
-                    uint32_t sv[64];
-                    tmem_ld64(tl + 384 + 64 * hp, sv);
-                    tmem_ld_wait();
-                    uint8_t* img = sm + (s_st - s_w) + (r >> 6) * kStImage;
-                    const uint32_t cr = (r & 63) >> 3, pr = (r & 7) * 2;
-#pragma unroll
-                    for (int e = 0; e < 64; ++e)
-                        *reinterpret_cast<__nv_bfloat16*>(img + e * 128 + ((cr ^ (e & 7)) << 4) + pr) =
-                            __float2bfloat16_rn(__uint_as_float(sv[e]));
-                    *reinterpret_cast<__nv_bfloat16*>(img + 64 * 128 + (cr << 4) + pr) = __float2bfloat16_rn(z[hp]);
-                }
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars->s_ready);
-                    mbar_arrive(&bars->st_full);
+                    refresh_row(tl + 384 + 64 * hp, s_st, r);
+                    zs[r] = z[hp];
                 }
             }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars->s_ready);
+                mbar_arrive(&bars->st_full);
+            }
+            // key features of both halves -> Phi_K [feature][token] in shared memory, z
+            bool ok = mbar_wait(&bars->pk_full, 0, err, 254);
+            if (ok) {
+                tc_fence_after();
+                if (t > 0) ok = mbar_wait(&bars->phik_free, pp, err, 255);
+            }
+            if (ok) {
+                z[0] += key_row<KIND>(Z, s_phi, r0, a);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->pk_free);
+                ok = mbar_wait(&bars->pk_full, 1, err, 256);
+            }
+            if (ok) {
+                tc_fence_after();
+                z[1] += key_row<KIND>(Z, s_phi, r0 + 128, a);
+            }
+            if (!ok) break;
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->phik_full);
+            r3 = (r3 == 2) ? 0 : r3 + 1;
         }
     }
     tc_fence_before();
@@ -1295,8 +1395,8 @@ bool map_omega(CUtensorMap* m, const void* base, int H) {
 
 constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * kExtStage + kExtOmega + sizeof(StBars);
 constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kTileBytes + kImageBytes + 64;
-constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + 4 * kStImage + kOnesBlock + kExtStage +
-                                kExtOmega + sizeof(CaBars);
+constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kSBytes + kExtStage + kExtOmega +
+                                kM * 4 + sizeof(CaBars);
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
 
 template <typename K>
