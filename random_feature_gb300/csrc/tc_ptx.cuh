@@ -58,15 +58,13 @@ __device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parit
 
 // Wait for the phase with the given parity to complete, giving up after about
 // two seconds of SM clock: then the error word gets `code` and false returns.
-// Spins with the non-suspending probe (a suspended try_wait can resume long
-// after the phase completes), backing off with a short sleep once it has
-// waited a while.
+// try_wait suspends the warp in hardware until the phase completes or a
+// system-dependent time limit passes, so a waiting warp takes no issue slots
+// from the warps that do the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
     if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    int spins = 0;
-    while (!mbar_test_wait(bar, parity)) {
-        if (++spins > 64) __nanosleep(20);
+    while (!mbar_try_wait(bar, parity)) {
         if (clock64() - t0 > (4LL << 30)) {
             if (err) atomicExch(err, code);
             return false;
@@ -100,6 +98,25 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 // Order this thread's generic-proxy shared-memory writes before later async-proxy
 // reads (tensor-core operands, TMA stores).
+// Tiled 3D store shared -> global through the tensor map (bulk-group completion).
+// Elements outside the tensor (rows past its end) are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(map), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until at most N committed bulk groups of this thread are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
