@@ -214,8 +214,11 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     }
     if (tc_supported(*h)) {
         // bf16 copies of the reduced states in the tensor-core operand layout.
-        h->ws_tc_bytes = (size_t)max_B * H * 80 * m * sizeof(__nv_bfloat16);
+        // bf16 readout operand images, two [m][64] blocks per (batch, head); the
+        // second block holds z~ in column 0 and zeros elsewhere, so it starts zeroed.
+        h->ws_tc_bytes = (size_t)max_B * H * 128 * m * sizeof(__nv_bfloat16);
         e = cudaMalloc(&h->ws_tc, h->ws_tc_bytes);
+        if (e == cudaSuccess) e = cudaMemset(h->ws_tc, 0, h->ws_tc_bytes);
         if (e != cudaSuccess) {
             favor_status st = (e == cudaErrorMemoryAllocation) ? FAVOR_ERR_NOMEM : FAVOR_ERR_CUDA;
             set_error(st, "favor_create: cudaMalloc: %s", cudaGetErrorString(e));

@@ -11,7 +11,8 @@
 //
 // Tensor-memory use (512 columns, lane = tile row):
 //   state kernel : [0,256) projection halves P0, P1 | [256,416) [S | z] halves (2 x 80 columns)
-//   readout      : [0,256) projection, then Phi_Q as packed bf16 in [0,128) | [128,208) output num|den
+//   readout      : two 256-column tile slots: projection, then Phi_Q packed in [0,64) and
+//                  [192,256), [num | den] in [64,144)
 //   causal       : three rotating 128-column slots (query projection halves -> packed Phi_Q and
 //                  num; key projection halves -> A -> packed tril(A)) | [384,512) S halves
 #include <cmath>
@@ -37,8 +38,6 @@ constexpr uint32_t kTileBytes = kTile * kD * 2;   // 16 KB
 constexpr uint32_t kOmegaBytes = kM * kD * 2;     // 32 KB
 constexpr uint32_t kPhiBlock = kTile * 128;       // one 64-column image of a 128-row tile
 constexpr uint32_t kSBytes = kM * 128;            // S~ image [256 rows][64] = 32 KB
-constexpr uint32_t kZBytes = kM * 32;             // z~ image [256 rows][16] = 8 KB
-constexpr uint32_t kImageBytes = kSBytes + kZBytes;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // byte offset of chunk `c` (16 B) of row `r` inside an SW128 image
@@ -126,76 +125,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
     uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
     tmem_ld32(taddr, lo);
     tmem_ld32(taddr + 32, hi);
-}
-
-// Query features of one row into packed bf16 in tensor memory, in place:
-// columns [col0, col0+256) hold the fp32 projection; afterwards
-// [col0, col0+128) hold the 256 features as bf16 pairs.
-template <int KIND>
-__device__ __forceinline__ void query_features_to_tmem(uint32_t tl, float a) {
-    float mx = 0.f;
-    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-        mx = -INFINITY;
-        for (int c = 0; c < 8; ++c) {
-            uint32_t p[32];
-            tmem_ld32(tl + 32 * c, p);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(p[i]));
-        }
-    }
-    const float cm = -mx * a;
-    for (int c = 0; c < 8; ++c) {
-        uint32_t p[32];
-        tmem_ld32(tl + 32 * c, p);
-        tmem_ld_wait();
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float f0, f1;
-            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-                f0 = ex2(fmaf(__uint_as_float(p[2 * i]), a, cm));
-                f1 = ex2(fmaf(__uint_as_float(p[2 * i + 1]), a, cm));
-            } else {
-                f0 = fmaxf(__uint_as_float(p[2 * i]), 0.f);
-                f1 = fmaxf(__uint_as_float(p[2 * i + 1]), 0.f);
-            }
-            w[i] = pack_bf16(f0, f1);
-        }
-        tmem_st16(tl + 16 * c, w);
-    }
-    tmem_st_wait();
-}
-
-// out row = num / den from tensor-memory columns [col, col+64) and col+64.
-__device__ __forceinline__ void store_output_row(uint32_t tl, __nv_bfloat16* dst, bool live) {
-    uint32_t n0[32], n1[32], z[16];
-    tmem_ld32(tl, n0);
-    tmem_ld32(tl + 32, n1);
-    tmem_ld16(tl + 64, z);
-    tmem_ld_wait();
-    if (!live) return;
-    const float den = __uint_as_float(z[0]);
-    const float inv = den != 0.f ? 1.f / den : 0.f;
-    uint4* o = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 v;
-        v.x = pack_bf16(__uint_as_float(n0[8 * q + 0]) * inv, __uint_as_float(n0[8 * q + 1]) * inv);
-        v.y = pack_bf16(__uint_as_float(n0[8 * q + 2]) * inv, __uint_as_float(n0[8 * q + 3]) * inv);
-        v.z = pack_bf16(__uint_as_float(n0[8 * q + 4]) * inv, __uint_as_float(n0[8 * q + 5]) * inv);
-        v.w = pack_bf16(__uint_as_float(n0[8 * q + 6]) * inv, __uint_as_float(n0[8 * q + 7]) * inv);
-        o[q] = v;
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 v;
-        v.x = pack_bf16(__uint_as_float(n1[8 * q + 0]) * inv, __uint_as_float(n1[8 * q + 1]) * inv);
-        v.y = pack_bf16(__uint_as_float(n1[8 * q + 2]) * inv, __uint_as_float(n1[8 * q + 3]) * inv);
-        v.z = pack_bf16(__uint_as_float(n1[8 * q + 4]) * inv, __uint_as_float(n1[8 * q + 5]) * inv);
-        v.w = pack_bf16(__uint_as_float(n1[8 * q + 6]) * inv, __uint_as_float(n1[8 * q + 7]) * inv);
-        o[4 + q] = v;
-    }
 }
 
 // ======================================================== persistent ranges
@@ -525,7 +454,9 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 
 // ================================================ reduce + pack (bidirectional)
 // grid (ceil(256*65/256), B*H).  Sum a head's pieces in order and write the
-// bf16 operand image: S~ ([256][64] SW128) then z~ ([256][16], z repeated).
+// bf16 operand image of the readout: S~ as a [256][64] SW128 block, then a
+// second [256][64] SW128 block with z~ in column 0 (its other columns stay at
+// the zeros the workspace was created with).
 __global__ void k_reduce_pack(const float* __restrict__ part, uint8_t* __restrict__ image, Ranges R) {
     const int bh = blockIdx.y;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -544,15 +475,13 @@ __global__ void k_reduce_pack(const float* __restrict__ part, uint8_t* __restric
     }
     for (; j < np; ++j) acc += p[(size_t)j * n];
     const int r = i / (kDV + 1), e = i - r * (kDV + 1);
-    uint8_t* img = image + (size_t)bh * kImageBytes;
+    uint8_t* img = image + (size_t)bh * (2 * kSBytes);
     const __nv_bfloat16 b = __float2bfloat16_rn(acc);
     if (e < kDV) {
         const uint32_t off = (uint32_t)r * 128u + ((((uint32_t)e >> 3) ^ ((uint32_t)r & 7u)) << 4) + ((uint32_t)e & 7u) * 2u;
         *reinterpret_cast<__nv_bfloat16*>(img + off) = b;
     } else {
-        __nv_bfloat16* z = reinterpret_cast<__nv_bfloat16*>(img + kSBytes + (size_t)r * 32);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) z[q] = b;
+        *reinterpret_cast<__nv_bfloat16*>(img + kSBytes + (uint32_t)r * 128u + (((uint32_t)r & 7u) << 4)) = b;
     }
 }
 
@@ -584,67 +513,276 @@ __global__ void k_scan_pieces(float* __restrict__ part, Ranges R) {
 }
 
 // ==================================================================== readout
-// grid (tiles, B*H), 128 threads: one 128-query tile per CTA.
+// Persistent over the same flattened (head, tile) ranges as the state kernel;
+// omega and the head's [S~ | z~] image are reloaded only when the range moves
+// to another head.  Per 128-query tile t (tensor-memory slot t mod 2, 256 columns):
+//   P = Q omega^T (N = 256)                     -> slot [0,256)
+//   Phi_Q = exp2(a P - a max_r P) packed bf16   -> [0,64) (half 0), [192,256) (half 1)
+//   [num | den] = Phi_Q [S~ | z~] (N = 80)      -> [64,144)
+//   out = num / den, staged in shared memory and written by one TMA store
+// (Eq. 4 of Rethinking Attention with Performers).  The feature and output
+// work of tile t+1 overlaps the contraction of tile t.
+//   warp 0: TMA producer (one thread polls the Q ring, omega and the image)
+//   warp 1: MMA issuer
+//   warps 4..7 / 8..11 (lane = query): features of half 0 / half 1 (the two
+//   groups swap row maxima), then output columns [0,32) / [32,64).
+constexpr int kReadoutThreads = 384;
+constexpr int kRStages = 3;
+constexpr uint32_t kRImage = 2 * kSBytes;   // [S~ | z~] image: two [256][64] SW128 blocks
+
+struct RdBars {
+    uint64_t q_full[kRStages], q_empty[kRStages];
+    uint64_t w_full, w_empty, img_full, img_empty;
+    uint64_t pq_full[2], phiq_full[2], o_full[2], slot_free[2];
+    uint64_t mx0, mx1, stage_full, stage_free[2];
+    uint32_t tmem_base;
+};
+
+// Features of 128 projections of one row into packed bf16: half 0 reads
+// [0,128) and writes [0,64) block by block; half 1 reads [128,256) and writes
+// [192,256) from the last block down, so no block is overwritten before it is read.
 template <int KIND>
-__global__ void __launch_bounds__(128, 1)
+__device__ __noinline__ void readout_half(uint32_t slot, int g, float a, float c) {
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+        const int blk = g ? 3 - k : k;
+        const uint32_t src = slot + (g ? 128u : 0u) + 32u * blk;
+        const uint32_t dst = slot + (g ? 192u : 0u) + 16u * blk;
+        uint32_t p[32], w[16];
+        tmem_ld32(src, p);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float f0, f1;
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                f0 = ex2(fmaf(__uint_as_float(p[2 * i]), a, -c));
+                f1 = ex2(fmaf(__uint_as_float(p[2 * i + 1]), a, -c));
+            } else {
+                f0 = fmaxf(__uint_as_float(p[2 * i]), 0.f);
+                f1 = fmaxf(__uint_as_float(p[2 * i + 1]), 0.f);
+            }
+            w[i] = pack_bf16(f0, f1);
+        }
+        tmem_st16(dst, w);
+    }
+}
+
+// Largest of 128 fp32 columns of one row.
+__device__ __noinline__ float rowmax128(uint32_t taddr) {
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        uint32_t p[64];
+        tmem_ld64(taddr + 64 * hh, p);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 64; i += 4) {
+            m0 = fmaxf(m0, __uint_as_float(p[i]));
+            m1 = fmaxf(m1, __uint_as_float(p[i + 1]));
+            m2 = fmaxf(m2, __uint_as_float(p[i + 2]));
+            m3 = fmaxf(m3, __uint_as_float(p[i + 3]));
+        }
+    }
+    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kReadoutThreads, 1)
 k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w,
-             const uint8_t* __restrict__ image, __nv_bfloat16* __restrict__ out, int H, int L, float s, int* err) {
+             const __grid_constant__ CUtensorMap tm_o, const uint8_t* __restrict__ image, int H, int L, float s,
+             Ranges R, int* err) {
+    constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
-    const uint32_t s_q = s_w + kOmegaBytes;
-    const uint32_t s_s = s_q + kTileBytes;
-    const uint32_t s_z = s_s + kSBytes;
-    Bars* bars = reinterpret_cast<Bars*>(sm + (s_z - s_w) + kZBytes);
-    const int tile = blockIdx.x, bh = blockIdx.y, h = bh % H;
-    const int tid = threadIdx.x, warp = tid / 32;
-    const uint32_t row = tid;
-    const int tok0 = tile * kTile;
+    const uint32_t s_q = s_w + kOmegaBytes;                   // Q ring
+    const uint32_t s_img = s_q + kRStages * kTileBytes;       // [S~ | z~]: 2 blocks of 32 KB
+    const uint32_t s_stage = s_img + kRImage;                 // output staging, 2 x 16 KB
+    const uint32_t s_mx = s_stage + 2 * kTileBytes;           // row maxima [2 tiles][2 halves][128]
+    RdBars* bars = reinterpret_cast<RdBars*>(sm + (s_mx - s_w) + 2 * 2 * kTile * 4);
+    const int cta = blockIdx.x;
+    const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
+    const int n = g1 - g0;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const float a = s * kLog2e;
 
-    setup(bars, 256);
+    if (threadIdx.x == 0) {
+        uint64_t* b = reinterpret_cast<uint64_t*>(bars);
+        // order and arrival counts follow the fields of RdBars
+        const int counts[] = {1, 1, 1, 1, 1, 1,   1, 1, 1, 1,   1, 1, 8, 8, 1, 1, 8, 8,   4, 4, 8, 1, 1};
+        static_assert(sizeof(counts) / sizeof(int) * sizeof(uint64_t) == offsetof(RdBars, tmem_base), "barrier table");
+        for (int i = 0; i < (int)(sizeof(counts) / sizeof(int)); ++i) mbar_init(b + i, counts[i]);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
 
-    if (tid == 0) {
-        mbar_expect_tx(&bars->tma, kOmegaBytes + kTileBytes + kImageBytes);
-        tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
-        tma_load_3d(sm + (s_q - s_w), &tm_q, &bars->tma, 0, tok0, bh);
-        bulk_load(sm + (s_s - s_w), image + (size_t)bh * kImageBytes, kImageBytes, &bars->tma);
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int nq = 0, nw = 0, ni = 0;               // next Q tile; tiles covered by loaded omega / image
+            int wseg = 0, iseg = 0;                   // omega / image loads done so far
+            long long t0 = clock64();
+            while (nq < n || nw < n || ni < n) {
+                bool progress = false;
+                if (nq < n && (nq < kRStages || mbar_test_wait(&bars->q_empty[nq % kRStages], ((nq / kRStages) + 1) & 1))) {
+                    const int g = g0 + nq;
+                    mbar_expect_tx(&bars->q_full[nq % kRStages], kTileBytes);
+                    tma_load_3d(sm + (s_q - s_w) + (nq % kRStages) * kTileBytes, &tm_q, &bars->q_full[nq % kRStages], 0,
+                                (g % R.tph) * kTile, g / R.tph);
+                    ++nq;
+                    progress = true;
+                }
+                if (nw < n && (wseg == 0 || mbar_test_wait(&bars->w_empty, (wseg - 1) & 1))) {
+                    const int h = ((g0 + nw) / R.tph) % H;
+                    mbar_expect_tx(&bars->w_full, kOmegaBytes);
+                    tma_load_2d(sm, &tm_w, &bars->w_full, 0, h * kM);
+                    while (nw < n && ((g0 + nw) / R.tph) % H == h) ++nw;   // tiles of this omega segment
+                    ++wseg;
+                    progress = true;
+                }
+                if (ni < n && (iseg == 0 || mbar_test_wait(&bars->img_empty, (iseg - 1) & 1))) {
+                    const int bh = (g0 + ni) / R.tph;
+                    mbar_expect_tx(&bars->img_full, kRImage);
+                    bulk_load(sm + (s_img - s_w), image + (size_t)bh * kRImage, kRImage, &bars->img_full);
+                    while (ni < n && (g0 + ni) / R.tph == bh) ++ni;
+                    ++iseg;
+                    progress = true;
+                }
+                if (progress) {
+                    t0 = clock64();
+                } else {
+                    __nanosleep(64);
+                    if (clock64() - t0 > (4LL << 30)) {
+                        atomicExch(err, 301);
+                        break;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t id_o = make_idesc(128, 80, 0, 1);
+            uint32_t wph = 0, iph = 0;
+            bool ok = true;
+            // P for tile u: omega segment starts wait w_full; the last P of a segment frees omega
+            auto issue_p = [&](int u) -> bool {
+                const int g = g0 + u, h = (g / R.tph) % H;
+                const bool seg_start = u == 0 || ((g - 1) / R.tph) % H != h;
+                const bool seg_end = u + 1 < n && ((g + 1) / R.tph) % H != h;
+                const uint32_t sl = tmem + 256u * (uint32_t)(u & 1);
+                if (seg_start) {
+                    if (!mbar_wait(&bars->w_full, wph, err, 311)) return false;
+                    wph ^= 1;
+                }
+                if (!mbar_wait(&bars->q_full[u % kRStages], (u / kRStages) & 1, err, 312)) return false;
+                if (u >= 2 && !mbar_wait(&bars->slot_free[u & 1], ((u >> 1) - 1) & 1, err, 313)) return false;
+                tc_fence_after();
+                issue_projection(sl, s_q + (u % kRStages) * kTileBytes, s_w, 256);
+                mma_commit(&bars->pq_full[u & 1]);
+                mma_commit(&bars->q_empty[u % kRStages]);
+                if (seg_end) mma_commit(&bars->w_empty);
+                return true;
+            };
+            if (n > 0) ok = issue_p(0);
+            for (int t = 0; t < n && ok; ++t) {
+                if (t + 1 < n && !(ok = issue_p(t + 1))) break;
+                const int bh = (g0 + t) / R.tph;
+                const bool seg_start = t == 0 || (g0 + t - 1) / R.tph != bh;
+                const bool seg_end = t + 1 < n && (g0 + t + 1) / R.tph != bh;
+                const uint32_t sl = tmem + 256u * (uint32_t)(t & 1);
+                if (seg_start) {
+                    if (!mbar_wait(&bars->img_full, iph, err, 314)) break;
+                    iph ^= 1;
+                }
+                if (!mbar_wait(&bars->phiq_full[t & 1], (t >> 1) & 1, err, 315)) break;
+                tc_fence_after();
+                // [num | den] = Phi_Q [S~ | z~]: B MN-major, N = 80 over two 64-wide blocks (LBO = 32 KB)
+                const uint64_t b0 = make_desc(s_img, kSBytes, 1024, SW_128B);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk)
+                    mma_ts(sl + 64, kk < 8 ? sl + 8 * kk : sl + 192 + 8 * (kk - 8), b0 + 128 * kk, id_o,
+                           kk > 0 ? 1u : 0u);
+                mma_commit(&bars->o_full[t & 1]);
+                if (seg_end) mma_commit(&bars->img_empty);
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ features and output
+        const int grp = (warp - 4) >> 2, q = warp & 3;
+        const uint32_t row = 32 * q + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+        float* mx = reinterpret_cast<float*>(sm + (s_mx - s_w));
+        bool ok = true;
+        auto features = [&](int u) -> bool {
+            const uint32_t sl = tl + 256u * (uint32_t)(u & 1);
+            if (!mbar_wait(&bars->pq_full[u & 1], (u >> 1) & 1, err, 321)) return false;
+            tc_fence_after();
+            float c = 0.f;
+            if (POS) {
+                const float m = rowmax128(sl + 128u * (uint32_t)grp);
+                mx[((u & 1) * 2 + grp) * kTile + row] = m;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(grp ? &bars->mx1 : &bars->mx0);
+                if (!mbar_wait(grp ? &bars->mx0 : &bars->mx1, u & 1, err, 322)) return false;
+                c = fmaxf(m, mx[((u & 1) * 2 + (grp ^ 1)) * kTile + row]) * a;
+            }
+            readout_half<KIND>(sl, grp, a, c);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->phiq_full[u & 1]);
+            return true;
+        };
+        if (n > 0) ok = features(0);
+        for (int t = 0; t < n && ok; ++t) {
+            if (t + 1 < n && !(ok = features(t + 1))) break;
+            // output tile t: this group's 32 columns of num / den
+            const int g = g0 + t, bh = g / R.tph, tok0 = (g % R.tph) * kTile;
+            const uint32_t sl = tl + 256u * (uint32_t)(t & 1);
+            if (!mbar_wait(&bars->o_full[t & 1], (t >> 1) & 1, err, 323)) break;
+            tc_fence_after();
+            uint32_t nv[32], dz[16];
+            tmem_ld32(sl + 64 + 32 * grp, nv);
+            tmem_ld16(sl + 128, dz);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->slot_free[t & 1]);
+            const uint32_t stage = s_stage + (uint32_t)(t & 1) * kTileBytes;
+            if (t >= 2 && !mbar_wait(&bars->stage_free[t & 1], ((t >> 1) - 1) & 1, err, 324)) break;
+            const float den = __uint_as_float(dz[0]);
+            const float inv = den != 0.f ? 1.f / den : 0.f;
+#pragma unroll
+            for (uint32_t c = 0; c < 4; ++c)
+                st_shared_v4(stage + sw128(row, 4 * grp + c),
+                             pack_bf16(__uint_as_float(nv[8 * c + 0]) * inv, __uint_as_float(nv[8 * c + 1]) * inv),
+                             pack_bf16(__uint_as_float(nv[8 * c + 2]) * inv, __uint_as_float(nv[8 * c + 3]) * inv),
+                             pack_bf16(__uint_as_float(nv[8 * c + 4]) * inv, __uint_as_float(nv[8 * c + 5]) * inv),
+                             pack_bf16(__uint_as_float(nv[8 * c + 6]) * inv, __uint_as_float(nv[8 * c + 7]) * inv));
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->stage_full);
+            if (warp == 4 && lane == 0) {
+                if (!mbar_wait(&bars->stage_full, t & 1, err, 325)) break;
+                tma_store_3d(&tm_o, stage, 0, tok0, bh);
+                bulk_commit();
+                bulk_wait_read<1>();   // the previous tile's store has read its buffer
+                if (t >= 1) mbar_arrive(&bars->stage_free[(t - 1) & 1]);
+            }
+        }
+        if (warp == 4 && lane == 0) bulk_wait<0>();   // output stores complete before exit
     }
-    bool ok = __syncthreads_and(mbar_wait(&bars->tma, 0, err, 11));
-    if (ok && tid == 0) {
-        tc_fence_after();
-        issue_projection(tmem, s_q, s_w, 256);
-        mma_commit(&bars->mma);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 0, err, 12));
-    tc_fence_after();
-    if (ok) query_features_to_tmem<KIND>(tl, s * kLog2e);
     tc_fence_before();
     __syncthreads();
-    if (ok && tid == 0) {
-        tc_fence_after();
-        const uint32_t id_s = make_idesc(128, 64, 0, 1);
-        const uint32_t id_z = make_idesc(128, 16, 0, 1);
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            const uint64_t bs = make_desc(s_s + kk * 2048, 8192, 1024, SW_128B);
-            const uint64_t bz = make_desc(s_z + kk * 512, 8192, 256, SW_32B);
-            mma_ts(tmem + 128, tmem + 8 * kk, bs, id_s, kk > 0);
-            mma_ts(tmem + 192, tmem + 8 * kk, bz, id_z, kk > 0);
-        }
-        mma_commit(&bars->mma);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 1, err, 13));
-    tc_fence_after();
-    if (ok) {
-        const int tok = tok0 + (int)row;
-        store_output_row(tl + 128, out + ((size_t)bh * L + tok) * kDV, tok < L);
-    }
-    teardown(bars, tmem, 256);
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // ===================================================================== causal
@@ -1394,7 +1532,8 @@ bool map_omega(CUtensorMap* m, const void* base, int H) {
 }
 
 constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * kExtStage + kExtOmega + sizeof(StBars);
-constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kTileBytes + kImageBytes + 64;
+constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kRStages * kTileBytes + kRImage + 2 * kTileBytes +
+                                 2 * 2 * kTile * 4 + sizeof(RdBars);
 constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kSBytes + kExtStage + kExtOmega +
                                 kM * 4 + sizeof(CaBars);
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
@@ -1499,14 +1638,15 @@ favor_status tc_bidir(const Handle& h, const void* q, const void* k, const void*
         s = check_launch("reduce/pack kernel");
         if (s != FAVOR_OK) return s;
     }
-    dim3 grid(R.tph, BH);
+    CUtensorMap mo;
+    if (!map_tokens(&mo, out, BH, L)) return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     ProfScope ps(h, PROF_READOUT, st);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
-        k_tc_readout<FAVOR_KERNEL_SOFTMAX_POS><<<grid, 128, kSmemReadout, st>>>(
-            mq, mw, (const uint8_t*)h.ws_tc, (__nv_bfloat16*)out, h.H, L, h.s, h.dev_err);
+        k_tc_readout<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kReadoutThreads, kSmemReadout, st>>>(
+            mq, mw, mo, (const uint8_t*)h.ws_tc, h.H, L, h.s, R, h.dev_err);
     else
-        k_tc_readout<FAVOR_KERNEL_RELU><<<grid, 128, kSmemReadout, st>>>(mq, mw, (const uint8_t*)h.ws_tc,
-                                                                           (__nv_bfloat16*)out, h.H, L, h.s, h.dev_err);
+        k_tc_readout<FAVOR_KERNEL_RELU><<<R.G, kReadoutThreads, kSmemReadout, st>>>(
+            mq, mw, mo, (const uint8_t*)h.ws_tc, h.H, L, h.s, R, h.dev_err);
     count_launch();
     return check_launch("tensor-core readout kernel");
 }

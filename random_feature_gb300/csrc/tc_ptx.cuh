@@ -96,8 +96,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
-// Order this thread's generic-proxy shared-memory writes before later async-proxy
-// reads (tensor-core operands, TMA stores).
 // Tiled 3D store shared -> global through the tensor map (bulk-group completion).
 // Elements outside the tensor (rows past its end) are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
@@ -117,6 +115,8 @@ __device__ __forceinline__ void bulk_wait() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later async-proxy
+// reads (tensor-core operands, TMA stores).
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
