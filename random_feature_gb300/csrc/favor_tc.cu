@@ -517,16 +517,18 @@ __global__ void k_scan_pieces(float* __restrict__ part, Ranges R) {
 // omega and the head's [S~ | z~] image are reloaded only when the range moves
 // to another head.  Per 128-query tile t (tensor-memory slot t mod 2, 256 columns):
 //   P = Q omega^T (N = 256)                     -> slot [0,256)
-//   Phi_Q = exp2(a P - a max_r P) packed bf16   -> [0,64) (half 0), [192,256) (half 1)
+//   Phi_Q = exp2(a P - a max_r P) packed bf16   -> [0,64) (features 0..127), [192,256) (128..255)
 //   [num | den] = Phi_Q [S~ | z~] (N = 80)      -> [64,144)
 //   out = num / den, staged in shared memory and written by one TMA store
 // (Eq. 4 of Rethinking Attention with Performers).  The feature and output
 // work of tile t+1 overlaps the contraction of tile t.
 //   warp 0: TMA producer (one thread polls the Q ring, omega and the image)
-//   warp 1: MMA issuer
-//   warps 4..7 / 8..11 (lane = query): features of half 0 / half 1 (the two
-//   groups swap row maxima), then output columns [0,32) / [32,64).
-constexpr int kReadoutThreads = 384;
+//   warp 1: projection MMAs; warp 2: [num | den] MMAs (separate issuers, so each
+//   goes as soon as its own inputs are ready)
+//   warps 4..19: four groups of four (lane = query), group g owns features
+//   [64g, 64g+64): it loads them once, the groups swap row maxima, and each
+//   writes its packed features and then output columns [16g, 16g+16).
+constexpr int kReadoutThreads = 640;
 constexpr int kRStages = 3;
 constexpr uint32_t kRImage = 2 * kSBytes;   // [S~ | z~] image: two [256][64] SW128 blocks
 
@@ -534,57 +536,12 @@ struct RdBars {
     uint64_t q_full[kRStages], q_empty[kRStages];
     uint64_t w_full, w_empty, img_full, img_empty;
     uint64_t pq_full[2], phiq_full[2], o_full[2], slot_free[2];
-    uint64_t mx0, mx1, stage_full, stage_free[2];
+    uint64_t mxb, stage_full, stage_free[2];
     uint32_t tmem_base;
 };
 
-// Features of 128 projections of one row into packed bf16: half 0 reads
-// [0,128) and writes [0,64) block by block; half 1 reads [128,256) and writes
-// [192,256) from the last block down, so no block is overwritten before it is read.
-template <int KIND>
-__device__ __noinline__ void readout_half(uint32_t slot, int g, float a, float c) {
-#pragma unroll 1
-    for (int k = 0; k < 4; ++k) {
-        const int blk = g ? 3 - k : k;
-        const uint32_t src = slot + (g ? 128u : 0u) + 32u * blk;
-        const uint32_t dst = slot + (g ? 192u : 0u) + 16u * blk;
-        uint32_t p[32], w[16];
-        tmem_ld32(src, p);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float f0, f1;
-            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-                f0 = ex2(fmaf(__uint_as_float(p[2 * i]), a, -c));
-                f1 = ex2(fmaf(__uint_as_float(p[2 * i + 1]), a, -c));
-            } else {
-                f0 = fmaxf(__uint_as_float(p[2 * i]), 0.f);
-                f1 = fmaxf(__uint_as_float(p[2 * i + 1]), 0.f);
-            }
-            w[i] = pack_bf16(f0, f1);
-        }
-        tmem_st16(dst, w);
-    }
-}
-
-// Largest of 128 fp32 columns of one row.
-__device__ __noinline__ float rowmax128(uint32_t taddr) {
-    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll 1
-    for (int hh = 0; hh < 2; ++hh) {
-        uint32_t p[64];
-        tmem_ld64(taddr + 64 * hh, p);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-            m0 = fmaxf(m0, __uint_as_float(p[i]));
-            m1 = fmaxf(m1, __uint_as_float(p[i + 1]));
-            m2 = fmaxf(m2, __uint_as_float(p[i + 2]));
-            m3 = fmaxf(m3, __uint_as_float(p[i + 3]));
-        }
-    }
-    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-}
+// Packed destination column of feature quarter g (16-column steps k = 0, 1).
+__device__ __forceinline__ uint32_t quarter_dst(int g) { return g < 2 ? 32u * g : 192u + 32u * (g - 2); }
 
 template <int KIND>
 __global__ void __launch_bounds__(kReadoutThreads, 1)
@@ -598,8 +555,8 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const uint32_t s_q = s_w + kOmegaBytes;                   // Q ring
     const uint32_t s_img = s_q + kRStages * kTileBytes;       // [S~ | z~]: 2 blocks of 32 KB
     const uint32_t s_stage = s_img + kRImage;                 // output staging, 2 x 16 KB
-    const uint32_t s_mx = s_stage + 2 * kTileBytes;           // row maxima [2 tiles][2 halves][128]
-    RdBars* bars = reinterpret_cast<RdBars*>(sm + (s_mx - s_w) + 2 * 2 * kTile * 4);
+    const uint32_t s_mx = s_stage + 2 * kTileBytes;           // row maxima [2 tiles][4 quarters][128]
+    RdBars* bars = reinterpret_cast<RdBars*>(sm + (s_mx - s_w) + 2 * 4 * kTile * 4);
     const int cta = blockIdx.x;
     const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
     const int n = g1 - g0;
@@ -609,7 +566,7 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     if (threadIdx.x == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bars);
         // order and arrival counts follow the fields of RdBars
-        const int counts[] = {1, 1, 1, 1, 1, 1,   1, 1, 1, 1,   1, 1, 8, 8, 1, 1, 8, 8,   4, 4, 8, 1, 1};
+        const int counts[] = {1, 1, 1, 1, 1, 1,   1, 1, 1, 1,   1, 1, 16, 16, 1, 1, 16, 16,   16, 16, 1, 1};
         static_assert(sizeof(counts) / sizeof(int) * sizeof(uint64_t) == offsetof(RdBars, tmem_base), "barrier table");
         for (int i = 0; i < (int)(sizeof(counts) / sizeof(int)); ++i) mbar_init(b + i, counts[i]);
         fence_mbar_init();
@@ -667,33 +624,34 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+        // --------------------------------------------------- projection MMAs
+        // P for tile u: an omega segment start waits w_full; the last P of a segment frees omega
         if (lane == 0) {
-            const uint32_t id_o = make_idesc(128, 80, 0, 1);
-            uint32_t wph = 0, iph = 0;
-            bool ok = true;
-            // P for tile u: omega segment starts wait w_full; the last P of a segment frees omega
-            auto issue_p = [&](int u) -> bool {
+            uint32_t wph = 0;
+            for (int u = 0; u < n; ++u) {
                 const int g = g0 + u, h = (g / R.tph) % H;
                 const bool seg_start = u == 0 || ((g - 1) / R.tph) % H != h;
                 const bool seg_end = u + 1 < n && ((g + 1) / R.tph) % H != h;
                 const uint32_t sl = tmem + 256u * (uint32_t)(u & 1);
                 if (seg_start) {
-                    if (!mbar_wait(&bars->w_full, wph, err, 311)) return false;
+                    if (!mbar_wait(&bars->w_full, wph, err, 311)) break;
                     wph ^= 1;
                 }
-                if (!mbar_wait(&bars->q_full[u % kRStages], (u / kRStages) & 1, err, 312)) return false;
-                if (u >= 2 && !mbar_wait(&bars->slot_free[u & 1], ((u >> 1) - 1) & 1, err, 313)) return false;
+                if (!mbar_wait(&bars->q_full[u % kRStages], (u / kRStages) & 1, err, 312)) break;
+                if (u >= 2 && !mbar_wait(&bars->slot_free[u & 1], ((u >> 1) - 1) & 1, err, 313)) break;
                 tc_fence_after();
                 issue_projection(sl, s_q + (u % kRStages) * kTileBytes, s_w, 256);
                 mma_commit(&bars->pq_full[u & 1]);
                 mma_commit(&bars->q_empty[u % kRStages]);
                 if (seg_end) mma_commit(&bars->w_empty);
-                return true;
-            };
-            if (n > 0) ok = issue_p(0);
-            for (int t = 0; t < n && ok; ++t) {
-                if (t + 1 < n && !(ok = issue_p(t + 1))) break;
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------- [num | den] MMAs
+        if (lane == 0) {
+            const uint32_t id_o = make_idesc(128, 80, 0, 1);
+            uint32_t iph = 0;
+            for (int t = 0; t < n; ++t) {
                 const int bh = (g0 + t) / R.tph;
                 const bool seg_start = t == 0 || (g0 + t - 1) / R.tph != bh;
                 const bool seg_end = t + 1 < n && (g0 + t + 1) / R.tph != bh;
@@ -704,7 +662,7 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 if (!mbar_wait(&bars->phiq_full[t & 1], (t >> 1) & 1, err, 315)) break;
                 tc_fence_after();
-                // [num | den] = Phi_Q [S~ | z~]: B MN-major, N = 80 over two 64-wide blocks (LBO = 32 KB)
+                // B MN-major, N = 80 over two 64-wide blocks (LBO = 32 KB)
                 const uint64_t b0 = make_desc(s_img, kSBytes, 1024, SW_128B);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk)
@@ -725,16 +683,52 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint32_t sl = tl + 256u * (uint32_t)(u & 1);
             if (!mbar_wait(&bars->pq_full[u & 1], (u >> 1) & 1, err, 321)) return false;
             tc_fence_after();
+            uint32_t p[64];
+            tmem_ld64(sl + 64u * (uint32_t)grp, p);
+            tmem_ld_wait();
+            float m = -INFINITY;
+            if (POS) {
+                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 64; i += 4) {
+                    m0 = fmaxf(m0, __uint_as_float(p[i]));
+                    m1 = fmaxf(m1, __uint_as_float(p[i + 1]));
+                    m2 = fmaxf(m2, __uint_as_float(p[i + 2]));
+                    m3 = fmaxf(m3, __uint_as_float(p[i + 3]));
+                }
+                m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+                mx[((u & 1) * 4 + grp) * kTile + row] = m;
+            }
+            // every group holds its projections in registers past this point, so
+            // the packed features may overwrite any group's fp32 columns
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->mxb);
+            if (!mbar_wait(&bars->mxb, u & 1, err, 322)) return false;
+            tc_fence_after();
             float c = 0.f;
             if (POS) {
-                const float m = rowmax128(sl + 128u * (uint32_t)grp);
-                mx[((u & 1) * 2 + grp) * kTile + row] = m;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(grp ? &bars->mx1 : &bars->mx0);
-                if (!mbar_wait(grp ? &bars->mx0 : &bars->mx1, u & 1, err, 322)) return false;
-                c = fmaxf(m, mx[((u & 1) * 2 + (grp ^ 1)) * kTile + row]) * a;
+                const float* mr = mx + (u & 1) * 4 * kTile + row;
+                c = fmaxf(fmaxf(mr[0], mr[kTile]), fmaxf(mr[2 * kTile], mr[3 * kTile])) * a;
             }
-            readout_half<KIND>(sl, grp, a, c);
+            const uint32_t dst = sl + quarter_dst(grp);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float f0, f1;
+                    if (POS) {
+                        f0 = ex2(fmaf(__uint_as_float(p[32 * k + 2 * i]), a, -c));
+                        f1 = ex2(fmaf(__uint_as_float(p[32 * k + 2 * i + 1]), a, -c));
+                    } else {
+                        f0 = fmaxf(__uint_as_float(p[32 * k + 2 * i]), 0.f);
+                        f1 = fmaxf(__uint_as_float(p[32 * k + 2 * i + 1]), 0.f);
+                    }
+                    w[i] = pack_bf16(f0, f1);
+                }
+                tmem_st16(dst + 16 * k, w);
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -744,13 +738,13 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (n > 0) ok = features(0);
         for (int t = 0; t < n && ok; ++t) {
             if (t + 1 < n && !(ok = features(t + 1))) break;
-            // output tile t: this group's 32 columns of num / den
+            // output tile t: this group's 16 columns of num / den
             const int g = g0 + t, bh = g / R.tph, tok0 = (g % R.tph) * kTile;
             const uint32_t sl = tl + 256u * (uint32_t)(t & 1);
             if (!mbar_wait(&bars->o_full[t & 1], (t >> 1) & 1, err, 323)) break;
             tc_fence_after();
-            uint32_t nv[32], dz[16];
-            tmem_ld32(sl + 64 + 32 * grp, nv);
+            uint32_t nv[16], dz[16];
+            tmem_ld16(sl + 64 + 16 * grp, nv);
             tmem_ld16(sl + 128, dz);
             tmem_ld_wait();
             tc_fence_before();
@@ -761,8 +755,8 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const float den = __uint_as_float(dz[0]);
             const float inv = den != 0.f ? 1.f / den : 0.f;
 #pragma unroll
-            for (uint32_t c = 0; c < 4; ++c)
-                st_shared_v4(stage + sw128(row, 4 * grp + c),
+            for (uint32_t c = 0; c < 2; ++c)
+                st_shared_v4(stage + sw128(row, 2 * grp + c),
                              pack_bf16(__uint_as_float(nv[8 * c + 0]) * inv, __uint_as_float(nv[8 * c + 1]) * inv),
                              pack_bf16(__uint_as_float(nv[8 * c + 2]) * inv, __uint_as_float(nv[8 * c + 3]) * inv),
                              pack_bf16(__uint_as_float(nv[8 * c + 4]) * inv, __uint_as_float(nv[8 * c + 5]) * inv),
@@ -1533,7 +1527,7 @@ bool map_omega(CUtensorMap* m, const void* base, int H) {
 
 constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * kExtStage + kExtOmega + sizeof(StBars);
 constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kRStages * kTileBytes + kRImage + 2 * kTileBytes +
-                                 2 * 2 * kTile * 4 + sizeof(RdBars);
+                                 2 * 4 * kTile * 4 + sizeof(RdBars);
 constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kSBytes + kExtStage + kExtOmega +
                                 kM * 4 + sizeof(CaBars);
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
