@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="long_bf16", choices=sorted(CONFIGS))
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override the workload's sequence length L (profiling a smaller case of the same shape)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-heads", type=int, default=2, help="heads of the workload in the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -188,7 +190,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    w = CONFIGS[args.workload]
+    w = workload_of(args)
     heads = max(1, min(args.cpu_heads, w.H))
     for _ in range(max(0, min(args.warmup, 1))):
         cpu_sample(w.replace(L=min(w.L, 4096)), 1)
@@ -227,7 +229,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
 
-    w = CONFIGS[args.workload]
+    w = workload_of(args)
     peaks = load_peaks()
     omega, q, k, v = make_workload(w, seed=replica_seed(0, rank))
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -382,6 +384,13 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def workload_of(args):
+    w = CONFIGS[args.workload]
+    if args.seq_len is not None:
+        w = w.replace(name=f"{w.name}_L{args.seq_len}", L=args.seq_len)
+    return w
 
 
 def main():
