@@ -51,7 +51,9 @@ struct Handle {
     float* kshift;            // [H] per-head key shift kappa_h (natural-log units)
     float* omega_sqnorm_half_host; // host [H]: max_r ||omega_r||^2 / 2
 
-    float* ws_partial;        // [rows][m][dv+1] per-segment states (bidir partials / causal prefixes)
+    float* ws_partial;        // [rows][m * (dv+1)] per-segment states (bidir partials / causal prefixes):
+                              // row-major [m][dv+1] on the CUDA-core path, column-major [dv+1][m]
+                              // on the tensor-core path (coalesced by feature)
     float* ws_state;          // [max_B*H][m][dv+1] reduced bidirectional states
     size_t ws_partial_rows;   // capacity of ws_partial in (head, segment) rows
     void* ws_tc;              // tensor-core path scratch (bf16 operand copies), may be null

@@ -434,11 +434,12 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
                 tmem_ld64(tmem + lane_off + 384 + 64 * hp, sv);
                 tmem_ld_wait();
                 const int pc = c - first_cta(R, bh);
-                float* o = part + ((size_t)bh * R.pstride + pc) * (kM * (kDV + 1)) +
-                           (size_t)(128 * hp + 32 * q + lane) * (kDV + 1);
+                // piece state stored column-major, [65][256]: a warp's 32 features are
+                // 128 contiguous bytes for every column
+                float* o = part + ((size_t)bh * R.pstride + pc) * (kM * (kDV + 1)) + (128 * hp + 32 * q + lane);
 #pragma unroll
-                for (int k2 = 0; k2 < 64; ++k2) o[k2] = __uint_as_float(sv[k2]);
-                o[64] = z0 + z1;
+                for (int k2 = 0; k2 < 64; ++k2) o[(size_t)k2 * kM] = __uint_as_float(sv[k2]);
+                o[(size_t)64 * kM] = z0 + z1;
                 z0 = z1 = 0.f;
                 tc_fence_before();
                 __syncwarp();
@@ -474,7 +475,7 @@ __global__ void k_reduce_pack(const float* __restrict__ part, uint8_t* __restric
         for (int u = 0; u < 8; ++u) acc += v[u];
     }
     for (; j < np; ++j) acc += p[(size_t)j * n];
-    const int r = i / (kDV + 1), e = i - r * (kDV + 1);
+    const int e = i / kM, r = i - e * kM;   // piece states are column-major [65][256]
     uint8_t* img = image + (size_t)bh * (2 * kSBytes);
     const __nv_bfloat16 b = __float2bfloat16_rn(acc);
     if (e < kDV) {
@@ -1015,13 +1016,14 @@ __device__ __noinline__ void refresh_row(uint32_t taddr, uint32_t img, uint32_t 
     }
 }
 
-// fp32 state row (64 columns at taddr), S~ image row r from a prefix row in global memory.
+// fp32 state row (64 columns at taddr), S~ image row r from a prefix in global
+// memory stored column-major (element e of the row at src[e * 256]).
 __device__ __noinline__ void load_prefix_row(const float* src, uint32_t taddr, uint32_t img, uint32_t r) {
 #pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {
         uint32_t sv[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(src[16 * blk + i]);
+        for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(src[(size_t)(16 * blk + i) * kM]);
         tmem_st16(taddr + 16 * blk, sv);
 #pragma unroll
         for (uint32_t c = 0; c < 2; ++c)
@@ -1367,8 +1369,8 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll 1
                 for (int hp = 0; hp < 2; ++hp) {
                     const uint32_t r = r0 + 128 * hp;
-                    load_prefix_row(pre + (size_t)r * (kDV + 1), tl + 384 + 64 * hp, s_st, r);
-                    z[hp] = pre[(size_t)r * (kDV + 1) + 64];
+                    load_prefix_row(pre + r, tl + 384 + 64 * hp, s_st, r);
+                    z[hp] = pre[(size_t)64 * kM + r];
                     zs[r] = z[hp];
                 }
                 tmem_st_wait();
