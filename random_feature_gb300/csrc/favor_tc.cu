@@ -487,29 +487,30 @@ __global__ void k_reduce_pack(const float* __restrict__ part, uint8_t* __restric
 }
 
 // Causal: piece j of head bh <- sum of pieces 0..j-1 (exclusive prefix, in order).
+// One thread per 4 consecutive elements (float4); pieces in register batches of 8.
 __global__ void k_scan_pieces(float* __restrict__ part, Ranges R) {
     const int bh = blockIdx.y;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int i4 = blockIdx.x * blockDim.x + threadIdx.x;
     constexpr int n = kM * (kDV + 1);
-    if (i >= n) return;
+    static_assert(n % 4 == 0, "float4 scan");
+    if (i4 >= n / 4) return;
     const int np = last_cta(R, bh) - first_cta(R, bh) + 1;
-    float* p = part + (size_t)bh * R.pstride * n + i;
-    float run = 0.f;
-    int j = 0;
-    for (; j + 8 <= np; j += 8) {
-        float v[8];
+    float4* p = reinterpret_cast<float4*>(part + (size_t)bh * R.pstride * n) + i4;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < np; j += 8) {
+        float4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = p[(size_t)(j + u) * n];
+        for (int u = 0; u < 8; ++u)
+            if (j + u < np) v[u] = p[(size_t)(j + u) * (n / 4)];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            p[(size_t)(j + u) * n] = run;
-            run += v[u];
-        }
-    }
-    for (; j < np; ++j) {
-        const float t = p[(size_t)j * n];
-        p[(size_t)j * n] = run;
-        run += t;
+        for (int u = 0; u < 8; ++u)
+            if (j + u < np) {
+                p[(size_t)(j + u) * (n / 4)] = run;
+                run.x += v[u].x;
+                run.y += v[u].y;
+                run.z += v[u].z;
+                run.w += v[u].w;
+            }
     }
 }
 
@@ -1662,7 +1663,7 @@ favor_status tc_causal(const Handle& h, const void* q, const void* k, const void
     if (R.pstride > 1) {
         s = launch_state(h, mk, mv, mw, BH, L, R, st);
         if (s != FAVOR_OK) return s;
-        dim3 g2((kM * (kDV + 1) + 255) / 256, BH);
+        dim3 g2((kM * (kDV + 1) / 4 + 255) / 256, BH);
         ProfScope ps(h, PROF_COMBINE, st);
         k_scan_pieces<<<g2, 256, 0, st>>>(h.ws_partial, R);
         count_launch();
