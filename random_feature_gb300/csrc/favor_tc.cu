@@ -54,21 +54,51 @@ __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Squared norm of row `r` of a bf16 SW128 tile.
-__device__ __forceinline__ float row_sqnorm(uint32_t tile, uint32_t r) {
-    float a = 0.f;
+// Squared norms of rows r0 and r1 of a bf16 SW128 tile: all sixteen 16-byte
+// loads first, then sixteen independent accumulation chains of depth 8.
+__device__ __forceinline__ void row_sqnorm2(uint32_t tile, uint32_t r0, uint32_t r1, float& n0, float& n1) {
+    uint4 v[16];
 #pragma unroll
     for (uint32_t c = 0; c < 8; ++c) {
-        uint4 v = ld_shared_v4(tile + sw128(r, c));
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        v[c] = ld_shared_v4(tile + sw128(r0, c));
+        v[8 + c] = ld_shared_v4(tile + sw128(r1, c));
+    }
+    float acc[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        float t = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float lo = bf16lo(w[i]), hi = bf16hi(w[i]);
-            a = fmaf(lo, lo, a);
-            a = fmaf(hi, hi, a);
+            const float lo = bf16lo(w[i]), hi = bf16hi(w[i]);
+            t = fmaf(lo, lo, t);
+            t = fmaf(hi, hi, t);
         }
+        acc[c] = t;
     }
-    return a;
+    n0 = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    n1 = ((acc[8] + acc[9]) + (acc[10] + acc[11])) + ((acc[12] + acc[13]) + (acc[14] + acc[15]));
+}
+
+// Squared norm of row `r` of a bf16 SW128 tile (loads first, eight chains).
+__device__ __forceinline__ float row_sqnorm(uint32_t tile, uint32_t r) {
+    uint4 v[8];
+#pragma unroll
+    for (uint32_t c = 0; c < 8; ++c) v[c] = ld_shared_v4(tile + sw128(r, c));
+    float acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = bf16lo(w[i]), hi = bf16hi(w[i]);
+            t = fmaf(lo, lo, t);
+            t = fmaf(hi, hi, t);
+        }
+        acc[c] = t;
+    }
+    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
 // Common prologue: barriers, tensor memory, optional all-ones operand.
@@ -346,6 +376,7 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         if (POS) {
             int kap_h = -1;
             float kap = 0.f;
+            const float inv_s = 1.f / s;
             for (int i = 0; i < n; ++i) {
                 const int g = g0 + i, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
                 const int st = i % kNS;
@@ -355,12 +386,12 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
                 }
                 if (!mbar_wait(&bars->kv_full[st], (i / kNS) & 1, err, 131)) break;
                 float nrm[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) nrm[t] = row_sqnorm(s_kv + 2 * st * kTileBytes, (uint32_t)(lane + 32 * t));
+                row_sqnorm2(s_kv + 2 * st * kTileBytes, (uint32_t)lane, (uint32_t)(lane + 32), nrm[0], nrm[1]);
+                row_sqnorm2(s_kv + 2 * st * kTileBytes, (uint32_t)(lane + 64), (uint32_t)(lane + 96), nrm[2], nrm[3]);
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const uint32_t j = (uint32_t)(lane + 32 * t);
-                    const float x = (tok0 + (int)j < L) ? -(0.5f * s * s * nrm[t] + kap) / s : -1.0e30f;
+                    const float x = (tok0 + (int)j < L) ? -(0.5f * s * nrm[t] + kap * inv_s) : -1.0e30f;
                     const float hi = __bfloat162float(__float2bfloat16_rn(x));
                     const float lo = x - hi;
                     st_shared_v4(s_ext + st * kExtStage + ext_row(j), pack_bf16(hi, lo), 0u, 0u, 0u);
@@ -1334,6 +1365,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const uint32_t r0 = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
         float* zs = reinterpret_cast<float*>(sm + (s_z - s_w));
+        const float inv_s = 1.f / s;
         float z[2] = {0.f, 0.f};
         int cur_bh = -1, kap_h = -1, r3 = 0;
         float kap = 0.f;
@@ -1349,7 +1381,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     kap_h = h;
                 }
                 const float nrm = row_sqnorm(s_k, r0);
-                const float x = (tok0 + (int)r0 < L) ? -(0.5f * s * s * nrm + kap) / s : -1.0e30f;
+                const float x = (tok0 + (int)r0 < L) ? -(0.5f * s * nrm + kap * inv_s) : -1.0e30f;
                 const float hi = __bfloat162float(__float2bfloat16_rn(x));
                 st_shared_v4(s_ext + ext_row(r0), pack_bf16(hi, x - hi), 0u, 0u, 0u);
                 fence_async_smem();
