@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--seq-len", type=int, default=None,
                     help="override the workload's sequence length L (profiling a smaller case of the same shape)")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-groups", type=int, default=4,
+                    help="head groups pipelined over upload / compute / download streams in the e2e leg")
     ap.add_argument("--cpu-heads", type=int, default=2, help="heads of the workload in the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -293,35 +295,75 @@ def run_ours(args):
     job_units, ms_step = job_aggregate(units_step, ms_total / args.steps, device=dev)
     value = job_units / (ms_step / 1e3)
 
-    # end to end through the public API: pinned host inputs in, outputs back, every step
+    # End to end through the public API: pinned host inputs in, outputs back, every
+    # step.  The heads are split into groups, one library handle per group (its
+    # slice of omega), and three streams overlap the upload of group g+1, the four
+    # calls on group g and the download of group g-1 (events order each group's
+    # copies and calls, across steps too).
     e2e = None
     if args.e2e_steps > 0:
-        hq, hk, hv = (torch.from_numpy(a).to(tdt).pin_memory() for a in (q, k, v))
-        hout = [torch.empty((w.B, w.H, w.L, w.dv), dtype=tdt).pin_memory() for _ in STEP_CALLS]
+        G = max(1, min(args.e2e_groups, w.H))
+        bounds = [(w.H * g_) // G for g_ in range(G + 1)]
+        groups = []
+        for g_ in range(G):
+            h0, h1 = bounds[g_], bounds[g_ + 1]
+            hw = h1 - h0
+            gh = {kind: R.Favor(hw, w.m, w.d, w.dv, kind, w.dtype, omega[h0:h1], w.data_scale, w.B, w.L)
+                  for kind in handles}
+            hin = [torch.from_numpy(np.ascontiguousarray(a[:, h0:h1])).to(tdt).pin_memory() for a in (q, k, v)]
+            din = [torch.empty_like(t, device=dev) for t in hin]
+            dout = [torch.empty((w.B, hw, w.L, w.dv), dtype=tdt, device=dev) for _ in STEP_CALLS]
+            hout = [torch.empty((w.B, hw, w.L, w.dv), dtype=tdt).pin_memory() for _ in STEP_CALLS]
+            ev = {k_: torch.cuda.Event() for k_ in ("in", "comp", "out")}
+            groups.append({"h": gh, "hin": hin, "din": din, "dout": dout, "hout": hout, "ev": ev, "first": True})
+        s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
 
         def e2e_step():
-            qd.copy_(hq, non_blocking=True)
-            kd.copy_(hk, non_blocking=True)
-            vd.copy_(hv, non_blocking=True)
-            step()
-            for o, ho in zip(outs, hout):
-                ho.copy_(o, non_blocking=True)
+            for gr in groups:
+                ev = gr["ev"]
+                with torch.cuda.stream(s_in):
+                    if not gr["first"]:
+                        s_in.wait_event(ev["comp"])          # previous step's calls have read the inputs
+                    for hd_, dd in zip(gr["hin"], gr["din"]):
+                        dd.copy_(hd_, non_blocking=True)
+                    ev["in"].record(s_in)
+                with torch.cuda.stream(s_comp):
+                    s_comp.wait_event(ev["in"])
+                    if not gr["first"]:
+                        s_comp.wait_event(ev["out"])         # previous step's outputs are downloaded
+                    for (mode, kind), o in zip(STEP_CALLS, gr["dout"]):
+                        gr["h"][kind].attn(*gr["din"], causal=(mode == "causal"), out=o, stream=s_comp)
+                    ev["comp"].record(s_comp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev["comp"])
+                    for o, ho in zip(gr["dout"], gr["hout"]):
+                        ho.copy_(o, non_blocking=True)
+                    ev["out"].record(s_out)
+                gr["first"] = False
 
         e2e_step()
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
+        a0.record(s_in)
+        s_comp.wait_event(a0)
+        s_out.wait_event(a0)
         for _ in range(args.e2e_steps):
             e2e_step()
-        a1.record(stream)
+        s_out.wait_stream(s_in)
+        s_out.wait_stream(s_comp)
+        a1.record(s_out)
         torch.cuda.synchronize(dev)
         e_units, e_ms = job_aggregate(units_step, a0.elapsed_time(a1) / args.e2e_steps, device=dev)
         nb = 2 if tdt == torch.bfloat16 else 4
         e2e = {"value": e_units / (e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(nb * (q.size + k.size + v.size)),
-               "d2h_bytes_per_step": int(nb * sum(o.numel() for o in outs)), "ms_per_step": e_ms}
+               "d2h_bytes_per_step": int(nb * len(STEP_CALLS) * w.B * w.H * w.L * w.dv), "ms_per_step": e_ms,
+               "head_groups": G}
+        for gr in groups:
+            for hd_ in gr["h"].values():
+                hd_.close()
 
     if rank != 0:
         if world > 1:
