@@ -826,7 +826,8 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 //   warp 1: MMAs P_Q = Q omega^T, one 128-feature half at a time
 //   warp 2: MMAs P_K^T = omega K^T (+ key offsets) per half, then S += Phi_K^T V
 //   warp 3: MMAs A = Phi_Q Phi_K^T, num = Phi_Q S~, num += tril(A) V
-//   warps 4..7  (lane = query): query features and Phi_Q z, causal mask and its row sums, output
+//   warps 4..7  (lane = query): query features and Phi_Q z, causal mask and its row sums,
+//               output tile (staged in shared memory, one TMA store; rows past L are clipped)
 //   warps 8..11 (lane = key for the norms, = feature otherwise): key offsets, key
 //               features and z, S~ / z~ refresh from the fp32 state
 //
@@ -852,6 +853,7 @@ struct CaBars {
     uint64_t q_full, k_full, v_full, q_empty, k_empty, v_empty, w_full, w_empty;
     uint64_t ext_full, pk_full, pk_free, phik_full, phik_free, s_full, s_ready, st_full;
     uint64_t pq0_full, pq1_full, phiq_full, a_full, ai_done, am_full, o_full, o_empty;
+    uint64_t stage_full, stage_free[2];
     uint32_t tmem_base;
 };
 
@@ -971,27 +973,25 @@ __device__ __noinline__ float mask_row(uint32_t taddr, int row, int q) {
     return s0 + s1;
 }
 
-// out row = num / den, num = 64 fp32 columns at taddr.
-__device__ __noinline__ void store_out_row(uint32_t taddr, __nv_bfloat16* dst, bool live, float den) {
+// Row `row` of the output tile (num / den, num = 64 fp32 columns at taddr)
+// into a [128][64] bf16 staging image in the 128-byte swizzled layout of the
+// output tensor map.  The columns are read first and `done` (the slot's
+// release) is arrived before the shared-memory writes.
+__device__ __noinline__ void stage_out_row(uint32_t taddr, uint32_t stage, uint32_t row, float den, uint64_t* done) {
+    uint32_t nv[64];
+    tmem_ld64(taddr, nv);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(done);
     const float inv = den != 0.f ? 1.f / den : 0.f;
-#pragma unroll 1
-    for (int blk = 0; blk < 2; ++blk) {
-        uint32_t nv[32];
-        tmem_ld32(taddr + 32 * blk, nv);
-        tmem_ld_wait();
-        if (live) {
-            uint4* o = reinterpret_cast<uint4*>(dst) + 4 * blk;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint4 v;
-                v.x = pack_bf16(__uint_as_float(nv[8 * c + 0]) * inv, __uint_as_float(nv[8 * c + 1]) * inv);
-                v.y = pack_bf16(__uint_as_float(nv[8 * c + 2]) * inv, __uint_as_float(nv[8 * c + 3]) * inv);
-                v.z = pack_bf16(__uint_as_float(nv[8 * c + 4]) * inv, __uint_as_float(nv[8 * c + 5]) * inv);
-                v.w = pack_bf16(__uint_as_float(nv[8 * c + 6]) * inv, __uint_as_float(nv[8 * c + 7]) * inv);
-                o[c] = v;
-            }
-        }
-    }
+    for (uint32_t c = 0; c < 8; ++c)
+        st_shared_v4(stage + sw128(row, c),
+                     pack_bf16(__uint_as_float(nv[8 * c + 0]) * inv, __uint_as_float(nv[8 * c + 1]) * inv),
+                     pack_bf16(__uint_as_float(nv[8 * c + 2]) * inv, __uint_as_float(nv[8 * c + 3]) * inv),
+                     pack_bf16(__uint_as_float(nv[8 * c + 4]) * inv, __uint_as_float(nv[8 * c + 5]) * inv),
+                     pack_bf16(__uint_as_float(nv[8 * c + 6]) * inv, __uint_as_float(nv[8 * c + 7]) * inv));
 }
 
 // Key features of feature row r over the 128 tokens at taddr (fp32, offsets
@@ -1071,8 +1071,8 @@ template <int KIND>
 __global__ void __launch_bounds__(kCausalThreads, 1)
 k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
-            const float* __restrict__ kshift, const float* __restrict__ prefix, __nv_bfloat16* __restrict__ out,
-            int H, int L, float s, Ranges R, int* err) {
+            const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ kshift,
+            const float* __restrict__ prefix, int H, int L, float s, Ranges R, int* err) {
     constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
@@ -1085,7 +1085,8 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t s_ext = s_st + kSBytes;                    // key offsets [128][16]
     const uint32_t s_wext = s_ext + kExtStage;                // omega side [256][16]
     const uint32_t s_z = s_wext + kExtOmega;                  // z~ fp32 [256]
-    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_z - s_w) + kM * 4);
+    const uint32_t s_stage = s_z + kM * 4;                    // output staging, 2 x [128][64] bf16 (1 KB aligned)
+    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_stage - s_w) + 2 * kTileBytes);
     const int cta = blockIdx.x;
     const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
     const int n = g1 - g0;
@@ -1096,7 +1097,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         uint64_t* b = reinterpret_cast<uint64_t*>(bars);
         // order and arrival counts follow the fields of CaBars
         // (each barrier completes at most once per chunk, so a parity wait cannot miss a phase)
-        const int counts[] = {1, 1, 1, 1, 5, 2, 1, 2,   4, 1, 4, 4, 2, 1, 4, 4,   1, 1, 4, 1, 1, 4, 1, 4};
+        const int counts[] = {1, 1, 1, 1, 5, 2, 1, 2,   4, 1, 4, 4, 2, 1, 4, 4,   1, 1, 4, 1, 1, 4, 1, 4,   4, 1, 1};
         static_assert(sizeof(counts) / sizeof(int) * sizeof(uint64_t) == offsetof(CaBars, tmem_base), "barrier table");
         for (int i = 0; i < (int)(sizeof(counts) / sizeof(int)); ++i) mbar_init(b + i, counts[i]);
         fence_mbar_init();
@@ -1346,16 +1347,24 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->am_full);
-            // output row: num / den
+            // output tile: num / den staged in shared memory, written by one TMA store
             if (!mbar_wait(&bars->o_full, ph, err, 245)) break;
             tc_fence_after();
+            if (t >= 2 && !mbar_wait(&bars->stage_free[t & 1], ((t >> 1) - 1) & 1, err, 246)) break;
             {
-                const int tok = tok0 + (int)row;
-                store_out_row(X + 64, out + ((size_t)bh * L + (tok < L ? tok : 0)) * kDV, tok < L, den);
+                const uint32_t stage = s_stage + (uint32_t)(t & 1) * kTileBytes;
+                stage_out_row(X + 64, stage, row, den, &bars->o_empty);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->stage_full);
+                if (warp == 4 && lane == 0) {
+                    if (!mbar_wait(&bars->stage_full, t & 1, err, 247)) break;
+                    tma_store_3d(&tm_o, stage, 0, tok0, bh);
+                    bulk_commit();
+                    bulk_wait_read<1>();   // the previous chunk's store has read its buffer
+                    if (t >= 1) mbar_arrive(&bars->stage_free[(t - 1) & 1]);
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->o_empty);
             r3 = (r3 == 2) ? 0 : r3 + 1;
         }
     } else {
@@ -1448,6 +1457,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             r3 = (r3 == 2) ? 0 : r3 + 1;
         }
     }
+    if (threadIdx.x == 4 * 32) bulk_wait<0>();   // output stores complete before exit
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, 512);
@@ -1564,7 +1574,8 @@ constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * 
 constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kRStages * kTileBytes + kRImage + 2 * kTileBytes +
                                  2 * 4 * kTile * 4 + sizeof(RdBars);
 constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kSBytes + kExtStage + kExtOmega +
-                                kM * 4 + sizeof(CaBars);
+                                kM * 4 + 2 * kTileBytes + sizeof(CaBars);
+static_assert(kSmemCausal <= 232448, "causal shared memory");
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
 
 template <typename K>
@@ -1687,9 +1698,9 @@ favor_status tc_causal(const Handle& h, const void* q, const void* k, const void
     allow_all_once();
     const int BH = B * h.H;
     Ranges R = plan_ranges(BH, L, h.num_sms);
-    CUtensorMap mq, mk, mv, mw;
+    CUtensorMap mq, mk, mv, mw, mo;
     if (!map_tokens(&mq, q, BH, L) || !map_tokens(&mk, k, BH, L) || !map_tokens(&mv, v, BH, L) ||
-        !map_omega(&mw, h.omega_bf16, h.H))
+        !map_tokens(&mo, out, BH, L) || !map_omega(&mw, h.omega_bf16, h.H))
         return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     favor_status s;
     if (R.pstride > 1) {
@@ -1709,10 +1720,10 @@ favor_status tc_causal(const Handle& h, const void* q, const void* k, const void
     ProfScope ps(h, PROF_CAUSAL, st);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
         k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kCausalThreads, kSmemCausal, st>>>(
-            mq, mk, mv, mw, h.kshift, h.ws_partial, (__nv_bfloat16*)out, h.H, L, h.s, R, h.dev_err);
+            mq, mk, mv, mw, mo, h.kshift, h.ws_partial, h.H, L, h.s, R, h.dev_err);
     else
-        k_tc_causal<FAVOR_KERNEL_RELU><<<R.G, kCausalThreads, kSmemCausal, st>>>(mq, mk, mv, mw, h.kshift, h.ws_partial,
-                                                                        (__nv_bfloat16*)out, h.H, L, h.s, R, h.dev_err);
+        k_tc_causal<FAVOR_KERNEL_RELU><<<R.G, kCausalThreads, kSmemCausal, st>>>(
+            mq, mk, mv, mw, mo, h.kshift, h.ws_partial, h.H, L, h.s, R, h.dev_err);
     count_launch();
     return check_launch("tensor-core causal kernel");
 }
