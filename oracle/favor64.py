@@ -38,6 +38,7 @@ __all__ = [
     "bidir_state", "attn_from_features_bidir", "attn_from_features_causal",
     "explicit_from_features", "rnn_causal_from_features",
     "favor_bidir", "favor_causal", "favor_feature_map",
+    "favor_kv_state", "favor_attn_from_state", "favor_causal_from_state",
     "softmax_attention", "row_rel_err", "KINDS",
 ]
 
@@ -201,6 +202,56 @@ def favor_feature_map(x, omega, data_scale, kind="softmax_pos"):
     for h in range(H):
         out[:, h] = feature_map(data_scale * x[:, h], omega[h], kind)
     return out
+
+
+def favor_kv_state(k, v, omega, data_scale, kind="softmax_pos"):
+    """Key/value state of [B,H,L,*] keys and values: state[b,h] = K'^T [V 1_L]
+    ([P] App. B Alg. 1, Buf1), i.e. columns 0..dv-1 hold S = sum_j phi(k_j) v_j^T
+    and column dv holds z = sum_j phi(k_j) ([EX] §2).  -> [B,H,m,dv+1]."""
+    k, v, omega = _f64(k), _f64(v), _f64(omega)
+    B, H, L, _ = k.shape
+    m, dv = omega.shape[1], v.shape[-1]
+    out = np.empty((B, H, m, dv + 1))
+    for b in range(B):
+        for h in range(H):
+            pk = feature_map(data_scale * k[b, h], omega[h], kind)
+            out[b, h] = pk.T @ np.concatenate([v[b, h], np.ones((L, 1))], axis=1)
+    return out
+
+
+def favor_attn_from_state(q, state, omega, data_scale, kind="softmax_pos"):
+    """Readout against a given state ([P] App. B Alg. 1: Buf2 = Q' Buf1, split,
+    divide): out_i = phi(q_i)^T S / phi(q_i)^T z for every query of [B,H,Lq,d];
+    the keys behind the state may be another sequence (cross attention)."""
+    q, state, omega = _f64(q), _f64(state), _f64(omega)
+    B, H, Lq, _ = q.shape
+    out = np.empty((B, H, Lq, state.shape[-1] - 1))
+    for b in range(B):
+        for h in range(H):
+            buf2 = feature_map(data_scale * q[b, h], omega[h], kind) @ state[b, h]
+            out[b, h] = _divide_rows(buf2[:, :-1], buf2[:, -1])
+    return out
+
+
+def favor_causal_from_state(q, k, v, state, omega, data_scale, kind="softmax_pos"):
+    """Causal attention over T new tokens that follow the keys summarised by
+    ``state`` ([P] App. B.1 Eq. 11 with the prefix sum started at ``state``
+    instead of 0; the RNN form of [LA] "Autoregressive Generation" / [RFA]):
+    out_i = phi(q_i)^T (S + sum_{j<=i} phi(k_j) v_j^T) / phi(q_i)^T (z + sum_{j<=i} phi(k_j)).
+    Returns (out [B,H,T,dv], new state = state + K'^T [V 1])."""
+    q, k, v, state, omega = _f64(q), _f64(k), _f64(v), _f64(state), _f64(omega)
+    B, H, T, _ = q.shape
+    out = np.empty((B, H, T, v.shape[-1]))
+    new = np.empty_like(state)
+    for b in range(B):
+        for h in range(H):
+            pq = feature_map(data_scale * q[b, h], omega[h], kind)
+            pk = feature_map(data_scale * k[b, h], omega[h], kind)
+            c = np.concatenate([v[b, h], np.ones((T, 1))], axis=1)
+            buf2 = np.tril(pq @ pk.T) @ c + pq @ state[b, h]
+            out[b, h] = _divide_rows(buf2[:, :-1], buf2[:, -1])
+            new[b, h] = state[b, h] + pk.T @ c
+    return out, new
 
 
 def softmax_attention(q, k, v, data_scale, causal=False):
