@@ -122,6 +122,56 @@ FAVOR_API favor_status favor_attn_causal(favor_handle h, const void* q, const vo
                                const void* v, void* out, int B, int L, void* stream);
 
 /*
+ * Stateful calls: the key/value summary carried across calls for decoding,
+ * chunked prefill and cross attention (the RNN form of causal linear
+ * attention: App. B.1 Eq. 11 of Rethinking Attention with Performers with the
+ * prefix sum started at a given state; the recurrence of Exploring Linear
+ * Attention, "Autoregressive Generation"; causal Random Feature Attention).
+ *
+ * A state is a caller-owned DEVICE float array [B, H, m, dv+1], row-major:
+ * row r of head (b, h) is (S_r0 .. S_r,dv-1, z_r) with
+ *     S = e^-kappa_h * sum_j phi(k_j) v_j^T,   z = e^-kappa_h * sum_j phi(k_j)
+ * over the keys it summarises (phi the plain feature map above, m^-1/2
+ * included; kappa_h = max(0, max_r ||omega_r||^2/2 - 60) is the handle's
+ * per-head key shift, 0 unless some ||omega_r||^2 > 120, which keeps every
+ * term finite).  A zero-filled array is the empty state.  Calls on one
+ * handle must not overlap; a state may be shared by calls on one stream.
+ */
+
+/*
+ * favor_kv_state -- state += the summary of keys k [B,H,L,d] and values v
+ * [B,H,L,dv] (App. B Alg. 1, Buf1 = K'^T [V 1]).  Accumulates, so a long
+ * sequence may be summarised chunk by chunk; fixed-order sums (bitwise
+ * repeatable).  1 <= B <= max_B, 1 <= L <= max_L.
+ */
+FAVOR_API favor_status favor_kv_state(favor_handle h, const void* k, const void* v, float* state,
+                                      int B, int L, void* stream);
+
+/*
+ * favor_attn_from_state -- out_i = phi(q_i)^T S / phi(q_i)^T z for queries q
+ * [B,H,L,d] against a given state (Eq. 4 with the key side given): with
+ * favor_kv_state of another sequence this is cross attention (query and key
+ * lengths differ).  out [B,H,L,dv] is only written; zero-denominator rows are
+ * 0.  1 <= B <= max_B, 1 <= L <= max_L.
+ */
+FAVOR_API favor_status favor_attn_from_state(favor_handle h, const void* q, const float* state, void* out,
+                                             int B, int L, void* stream);
+
+/*
+ * favor_attn_causal_step -- causal attention over T new tokens q, k [B,H,T,d],
+ * v [B,H,T,dv] that follow the keys summarised by state:
+ *     out_t = phi(q_t)^T (S + sum_{j<=t} phi(k_j) v_j^T) / phi(q_t)^T (z + sum_{j<=t} phi(k_j)),
+ * then state += the new tokens' summary.  Starting from a zero state and
+ * calling it block after block gives favor_attn_causal of the whole sequence
+ * (up to rounding).  Runs one CTA per (b, h) on the CUDA cores, tokens in
+ * order: meant for decoding (T = 1) and short blocks; a long prefix is better
+ * served by favor_attn_causal for its outputs and favor_kv_state for its
+ * state.  1 <= B <= max_B, 1 <= T <= max_L.
+ */
+FAVOR_API favor_status favor_attn_causal_step(favor_handle h, const void* q, const void* k, const void* v,
+                                              void* out, float* state, int B, int T, void* stream);
+
+/*
  * favor_attn_bidir_noalloc -- favor_attn_bidir without a handle and without
  * any allocation.  The pages have no counterpart: this is an interface
  * convenience.  It serves callers that may not allocate device memory through

@@ -348,6 +348,38 @@ favor_status favor_attn_bidir_noalloc(const float* omega, int H, int m, int d, i
     return simt_bidir_fixed_scratch(h, q, k, v, out, B, L, reinterpret_cast<cudaStream_t>(stream));
 }
 
+favor_status favor_kv_state(favor_handle hd, const void* k, const void* v, float* state, int B, int L,
+                            void* stream) {
+    favor_status st = check_call("favor_kv_state", hd, B, L);
+    if (st != FAVOR_OK) return st;
+    if (!k || !v || !state) return set_error(FAVOR_ERR_INVALID_ARG, "favor_kv_state: null pointer");
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (tc_supported(h)) return tc_kv_state(h, k, v, state, B, L, s);
+    return simt_kv_state(h, k, v, state, B, L, s);
+}
+
+favor_status favor_attn_from_state(favor_handle hd, const void* q, const float* state, void* out, int B, int L,
+                                   void* stream) {
+    favor_status st = check_call("favor_attn_from_state", hd, B, L);
+    if (st != FAVOR_OK) return st;
+    if (!q || !state || !out) return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_from_state: null pointer");
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (tc_supported(h)) return tc_attn_from_state(h, q, state, out, B, L, s);
+    return simt_attn_from_state(h, q, state, out, B, L, s);
+}
+
+favor_status favor_attn_causal_step(favor_handle hd, const void* q, const void* k, const void* v, void* out,
+                                    float* state, int B, int T, void* stream) {
+    favor_status st = check_call("favor_attn_causal_step", hd, B, T);
+    if (st != FAVOR_OK) return st;
+    if (!q || !k || !v || !out || !state)
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_causal_step: null pointer");
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    return simt_causal_step(h, q, k, v, out, state, B, T, reinterpret_cast<cudaStream_t>(stream));
+}
+
 favor_status favor_device_error(favor_handle hd, int* code) {
     if (!hd || !code) return set_error(FAVOR_ERR_INVALID_ARG, "favor_device_error: null argument");
     const Handle* h = reinterpret_cast<const Handle*>(hd);

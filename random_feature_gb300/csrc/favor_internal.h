@@ -98,6 +98,17 @@ favor_status simt_bidir(const Handle& h, const void* q, const void* k, const voi
 favor_status simt_causal(const Handle& h, const void* q, const void* k, const void* v, void* out,
                          int B, int L, cudaStream_t st);
 
+// ---- stateful calls: public state [B*H][m][dv+1] fp32 (S | z), see favor.h ----
+favor_status simt_kv_state(const Handle& h, const void* k, const void* v, float* state, int B, int L,
+                           cudaStream_t st);
+favor_status simt_attn_from_state(const Handle& h, const void* q, const float* state, void* out, int B, int L,
+                                  cudaStream_t st);
+favor_status simt_causal_step(const Handle& h, const void* q, const void* k, const void* v, void* out, float* state,
+                              int B, int Tn, cudaStream_t st);
+favor_status tc_kv_state(const Handle& h, const void* k, const void* v, float* state, int B, int L, cudaStream_t st);
+favor_status tc_attn_from_state(const Handle& h, const void* q, const float* state, void* out, int B, int L,
+                                cudaStream_t st);
+
 // ---- bidirectional call on a fixed, statically sized device scratch array ----
 // 16 MiB: enough for B*H*m*(dv+1)*(1 + n_seg) + H floats with n_seg >= 1 up to
 // B*H = 63 at m = 256, dv = 128 (more heads at smaller m, dv).

@@ -455,6 +455,167 @@ favor_status simt_causal(const Handle& h, const void* q, const void* k, const vo
     return dispatch3<CausalF>(h, q, k, v, out, BH, L, (const SegPlan*)&p, st);
 }
 
+// ------------------------------------------------------- stateful calls
+// Public state convention: state[b,h] is [m][dv+1] fp32, row r = (S_r, z_r) with
+// S = e^-kappa_h sum_j phi(k_j) v_j^T and z = e^-kappa_h sum_j phi(k_j), phi the
+// plain feature map (m^-1/2 included), kappa_h the handle's per-head key shift.
+// The segment kernels above leave out m^-1/2, so their sums are scaled here.
+
+namespace {
+
+// state[bh][i] += scale * sum over segments (in order) of part[bh, seg][i].
+__global__ void k_accum_rows(const float* __restrict__ part, float* __restrict__ state, int n_seg, int n, float scale) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float* p = part + (size_t)bh * n_seg * n + i;
+    float a = 0.f;
+    for (int sg = 0; sg < n_seg; ++sg) a += p[(size_t)sg * n];
+    state[(size_t)bh * n + i] += scale * a;
+}
+
+__device__ __forceinline__ float block_max(float x, float* red) {
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float y = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : -INFINITY;
+        for (int o = 16; o > 0; o >>= 1) y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, o));
+        if (threadIdx.x == 0) red[0] = y;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+// Causal attention over Tn new tokens continuing from state[bh] (App. B.1 Eq. 11
+// with the prefix started at the given state; the token recurrence
+// S_t = S_{t-1} + phi(k_t) v_t^T, z_t = z_{t-1} + phi(k_t), out_t = phi(q_t)^T S_t /
+// phi(q_t)^T z_t).  One CTA per (b, h), thread r owns feature r; the state lives
+// in shared memory for the whole call.  Meant for short blocks (decoding).
+template <typename T, int KIND>
+__global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, const T* __restrict__ k,
+                                                     const T* __restrict__ v, T* __restrict__ out,
+                                                     float* __restrict__ state, const float* __restrict__ omega,
+                                                     const float* __restrict__ kshift, int H, int Tn, int m, int d,
+                                                     int dv, float s) {
+    extern __shared__ float sm[];
+    const int dp = dv + 1;
+    float* S = sm;             // [m][dv+1]
+    float* xq = S + m * dp;    // [d]
+    float* xk = xq + d;        // [d]
+    float* xv = xk + d;        // [dv]
+    float* fq = xv + dv;       // [m]
+    float* rs = fq + m;        // [dv+1] readout sums
+    float* red = rs + dp;      // [32]
+    const int bh = blockIdx.x, h = bh % H, tid = threadIdx.x, nt = blockDim.x;
+    float* st = state + (size_t)bh * m * dp;
+    for (int i = tid; i < m * dp; i += nt) S[i] = st[i];
+    const float inv_sqrt_m = 1.f / sqrtf((float)m);
+    const float kap = kshift[h];
+    const float* w = omega + ((size_t)h * m + (tid < m ? tid : 0)) * d;
+    for (int t = 0; t < Tn; ++t) {
+        const size_t row = (size_t)bh * Tn + t;
+        __syncthreads();   // the previous token's readout is done with fq, rs and S
+        for (int i = tid; i < d; i += nt) {
+            xq[i] = ldf(q + row * d + i);
+            xk[i] = ldf(k + row * d + i);
+        }
+        for (int i = tid; i < dv; i += nt) xv[i] = ldf(v + row * dv + i);
+        __syncthreads();
+        float pq = 0.f, pk = 0.f, nk = 0.f;
+        if (tid < m)
+            for (int c = 0; c < d; ++c) {
+                const float wc = __ldg(w + c);
+                pq = fmaf(wc, xq[c], pq);
+                pk = fmaf(wc, xk[c], pk);
+                nk = fmaf(xk[c], xk[c], nk);
+            }
+        const float qx = s * pq;
+        const float mx = KIND == FAVOR_KERNEL_SOFTMAX_POS ? block_max(tid < m ? qx : -INFINITY, red) : 0.f;
+        if (tid < m) {
+            float fk, f;
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                fk = inv_sqrt_m * expf(s * pk - 0.5f * s * s * nk - kap);
+                f = expf(qx - mx);   // a per-query shift: cancels in num / den
+            } else {
+                fk = inv_sqrt_m * fmaxf(s * pk, 0.f);
+                f = fmaxf(qx, 0.f);
+            }
+            float* Sr = S + tid * dp;
+            for (int e = 0; e < dv; ++e) Sr[e] = fmaf(fk, xv[e], Sr[e]);
+            Sr[dv] += fk;
+            fq[tid] = f;
+        }
+        __syncthreads();
+        if (tid <= dv) {
+            float acc = 0.f;
+            for (int r = 0; r < m; ++r) acc = fmaf(fq[r], S[r * dp + tid], acc);
+            rs[tid] = acc;
+        }
+        __syncthreads();
+        if (tid < dv) {
+            const float den = rs[dv];
+            stf(out + row * dv + tid, den != 0.f ? rs[tid] / den : 0.f);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < m * dp; i += nt) st[i] = S[i];
+}
+
+template <typename T, int KIND>
+favor_status causal_step_t(const Handle& h, const void* q, const void* k, const void* v, void* out, float* state,
+                           int BH, int Tn, cudaStream_t st) {
+    const size_t smem = (size_t)(h.m * (h.dv + 1) + 2 * h.d + h.dv + h.m + (h.dv + 1) + 32) * sizeof(float);
+    auto kern = k_causal_step<T, KIND>;
+    set_smem(kern, smem);
+    ProfScope ps(h, PROF_CAUSAL, st);
+    kern<<<BH, 256, smem, st>>>((const T*)q, (const T*)k, (const T*)v, (T*)out, state, h.omega_f32, h.kshift, h.H,
+                                Tn, h.m, h.d, h.dv, h.s);
+    count_launch();
+    return check_launch("causal step kernel");
+}
+
+}  // namespace
+
+favor_status simt_kv_state(const Handle& h, const void* k, const void* v, float* state, int B, int L,
+                           cudaStream_t st) {
+    const int BH = B * h.H;
+    SegPlan p = plan_segments(BH, L, h.num_sms);
+    favor_status s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, st);
+    if (s != FAVOR_OK) return s;
+    const int n = h.m * (h.dv + 1);
+    dim3 grid((n + 255) / 256, BH);
+    ProfScope ps(h, PROF_COMBINE, st);
+    k_accum_rows<<<grid, 256, 0, st>>>(h.ws_partial, state, p.n_seg, n, 1.f / sqrtf((float)h.m));
+    count_launch();
+    return check_launch("state accumulate kernel");
+}
+
+favor_status simt_attn_from_state(const Handle& proto, const void* q, const float* state, void* out, int B, int L,
+                                  cudaStream_t st) {
+    Handle h = proto;
+    h.ws_state = const_cast<float*>(state);   // the readout only reads it
+    const int BH = B * h.H;
+    if (h.dtype == FAVOR_DTYPE_F32)
+        return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
+                                                  : readout_t<float, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
+    return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
+                                              : readout_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
+}
+
+favor_status simt_causal_step(const Handle& h, const void* q, const void* k, const void* v, void* out, float* state,
+                              int B, int Tn, cudaStream_t st) {
+    const int BH = B * h.H;
+    if (h.dtype == FAVOR_DTYPE_F32)
+        return h.kind == FAVOR_KERNEL_SOFTMAX_POS
+                   ? causal_step_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, q, k, v, out, state, BH, Tn, st)
+                   : causal_step_t<float, FAVOR_KERNEL_RELU>(h, q, k, v, out, state, BH, Tn, st);
+    return h.kind == FAVOR_KERNEL_SOFTMAX_POS
+               ? causal_step_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, q, k, v, out, state, BH, Tn, st)
+               : causal_step_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, q, k, v, out, state, BH, Tn, st);
+}
+
 // ------------------------------------------------ bidirectional call, fixed scratch
 // favor_attn_bidir_noalloc runs the CUDA-core bidirectional path above with no
 // handle and no allocation: its scratch (per-head key shifts, per-segment

@@ -545,6 +545,40 @@ __global__ void k_scan_pieces(float* __restrict__ part, Ranges R) {
     }
 }
 
+// ============================================================ stateful calls
+// state[bh][r][e] += scale * sum over the head's pieces (in order) of the
+// column-major piece states: public state rows from the state kernel's sums.
+__global__ void k_accum_cols(const float* __restrict__ part, float* __restrict__ state, Ranges R, float scale) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;   // column-major index e * 256 + r
+    constexpr int n = kM * (kDV + 1);
+    if (i >= n) return;
+    const int np = last_cta(R, bh) - first_cta(R, bh) + 1;
+    const float* p = part + (size_t)bh * R.pstride * n + i;
+    float a = 0.f;
+    for (int j = 0; j < np; ++j) a += p[(size_t)j * n];
+    const int e = i / kM, r = i - e * kM;
+    state[(size_t)bh * n + (size_t)r * (kDV + 1) + e] += scale * a;
+}
+
+// Readout operand image (as k_reduce_pack writes it) from a public state
+// [256][65] fp32: S~ block and z~ in column 0 of the second block, bf16.
+__global__ void k_pack_state(const float* __restrict__ state, uint8_t* __restrict__ image) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    constexpr int n = kM * (kDV + 1);
+    if (i >= n) return;
+    const int r = i / (kDV + 1), e = i - r * (kDV + 1);
+    uint8_t* img = image + (size_t)bh * (2 * kSBytes);
+    const __nv_bfloat16 b = __float2bfloat16_rn(state[(size_t)bh * n + i]);
+    if (e < kDV) {
+        const uint32_t off = (uint32_t)r * 128u + ((((uint32_t)e >> 3) ^ ((uint32_t)r & 7u)) << 4) + ((uint32_t)e & 7u) * 2u;
+        *reinterpret_cast<__nv_bfloat16*>(img + off) = b;
+    } else {
+        *reinterpret_cast<__nv_bfloat16*>(img + kSBytes + (uint32_t)r * 128u + (((uint32_t)r & 7u) << 4)) = b;
+    }
+}
+
 // ==================================================================== readout
 // Persistent over the same flattened (head, tile) ranges as the state kernel;
 // omega and the head's [S~ | z~] image are reloaded only when the range moves
@@ -1726,6 +1760,53 @@ favor_status tc_causal(const Handle& h, const void* q, const void* k, const void
             mq, mk, mv, mw, mo, h.kshift, h.ws_partial, h.H, L, h.s, R, h.dev_err);
     count_launch();
     return check_launch("tensor-core causal kernel");
+}
+
+favor_status tc_kv_state(const Handle& h, const void* k, const void* v, float* state, int B, int L, cudaStream_t st) {
+    if (!aligned16(k) || !aligned16(v)) return simt_kv_state(h, k, v, state, B, L, st);
+    allow_all_once();
+    const int BH = B * h.H;
+    Ranges R = plan_ranges(BH, L, h.num_sms);
+    CUtensorMap mk, mv, mw;
+    if (!map_tokens(&mk, k, BH, L) || !map_tokens(&mv, v, BH, L) || !map_omega(&mw, h.omega_bf16, h.H))
+        return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    favor_status s = launch_state(h, mk, mv, mw, BH, L, R, st);
+    if (s != FAVOR_OK) return s;
+    // the state kernel leaves out m^-1/2, and its ReLU features are of k, not s*k
+    const float scale = (h.kind == FAVOR_KERNEL_RELU ? h.s : 1.f) / sqrtf((float)kM);
+    dim3 grid((kM * (kDV + 1) + 255) / 256, BH);
+    ProfScope ps(h, PROF_COMBINE, st);
+    k_accum_cols<<<grid, 256, 0, st>>>(h.ws_partial, state, R, scale);
+    count_launch();
+    return check_launch("state accumulate kernel");
+}
+
+favor_status tc_attn_from_state(const Handle& h, const void* q, const float* state, void* out, int B, int L,
+                                cudaStream_t st) {
+    if (!aligned16(q) || !aligned16(out)) return simt_attn_from_state(h, q, state, out, B, L, st);
+    allow_all_once();
+    const int BH = B * h.H;
+    Ranges R = plan_ranges(BH, L, h.num_sms);
+    CUtensorMap mq, mw, mo;
+    if (!map_tokens(&mq, q, BH, L) || !map_tokens(&mo, out, BH, L) || !map_omega(&mw, h.omega_bf16, h.H))
+        return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    {
+        dim3 grid((kM * (kDV + 1) + 255) / 256, BH);
+        ProfScope ps(h, PROF_COMBINE, st);
+        k_pack_state<<<grid, 256, 0, st>>>(state, (uint8_t*)h.ws_tc);
+        count_launch();
+        favor_status s = check_launch("state pack kernel");
+        if (s != FAVOR_OK) return s;
+    }
+    ProfScope ps(h, PROF_READOUT, st);
+    if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
+        k_tc_readout<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kReadoutThreads, kSmemReadout, st>>>(
+            mq, mw, mo, (const uint8_t*)h.ws_tc, h.H, L, h.s, R, h.dev_err);
+    else
+        k_tc_readout<FAVOR_KERNEL_RELU><<<R.G, kReadoutThreads, kSmemReadout, st>>>(
+            mq, mw, mo, (const uint8_t*)h.ws_tc, h.H, L, h.s, R, h.dev_err);
+    count_launch();
+    return check_launch("tensor-core readout kernel");
 }
 
 }  // namespace favor

@@ -23,6 +23,7 @@ __all__ = [
     "favor_status_str", "favor_last_error", "favor_launch_count", "Favor", "EXPORTED_SYMBOLS",
     "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
     "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc",
+    "favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
 ]
 
 FAVOR_OK, FAVOR_ERR_INVALID_ARG, FAVOR_ERR_UNSUPPORTED, FAVOR_ERR_NOMEM, FAVOR_ERR_CUDA = range(5)
@@ -34,7 +35,8 @@ DTYPE_CODES = {"f32": FAVOR_DTYPE_F32, "bf16": FAVOR_DTYPE_BF16}
 EXPORTED_SYMBOLS = ("favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal",
                     "favor_destroy", "favor_status_str", "favor_last_error", "favor_launch_count",
                     "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
-                    "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc")
+                    "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc",
+                    "favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -91,6 +93,11 @@ def lib() -> ctypes.CDLL:
         L.favor_device_error.restype = ctypes.c_int
         L.favor_attn_bidir_noalloc.argtypes = [vp, i, i, i, i, i, i, f, vp, vp, vp, vp, i, i, vp]
         L.favor_attn_bidir_noalloc.restype = ctypes.c_int
+        L.favor_kv_state.argtypes = [vp, vp, vp, vp, i, i, vp]
+        L.favor_attn_from_state.argtypes = [vp, vp, vp, vp, i, i, vp]
+        L.favor_attn_causal_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, vp]
+        for fn in ("favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step"):
+            getattr(L, fn).restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -170,6 +177,20 @@ def favor_attn_bidir_noalloc(omega, H, m, d, dv, kind, dtype, data_scale, q, k, 
                                           _stream(stream, q)), "favor_attn_bidir_noalloc")
 
 
+def favor_kv_state(h, k, v, state, B, L, stream=None) -> None:
+    _check(lib().favor_kv_state(h, _ptr(k), _ptr(v), _ptr(state), int(B), int(L), _stream(stream, k)), "favor_kv_state")
+
+
+def favor_attn_from_state(h, q, state, out, B, L, stream=None) -> None:
+    _check(lib().favor_attn_from_state(h, _ptr(q), _ptr(state), _ptr(out), int(B), int(L), _stream(stream, q)),
+           "favor_attn_from_state")
+
+
+def favor_attn_causal_step(h, q, k, v, out, state, B, T, stream=None) -> None:
+    _check(lib().favor_attn_causal_step(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(state), int(B), int(T),
+                                        _stream(stream, q)), "favor_attn_causal_step")
+
+
 def favor_destroy(h) -> None:
     _check(lib().favor_destroy(h), "favor_destroy")
 
@@ -245,6 +266,48 @@ class Favor:
         self._chk(v, B, L, self.dv, "v")
         out = self._new(q, B, L, self.dv, out)
         (favor_attn_causal if causal else favor_attn_bidir)(self.handle, q, k, v, out, B, L, stream)
+        return out
+
+    def new_state(self, B):
+        """A zero (empty) state [B, H, m, dv+1] float32 on the current CUDA device."""
+        import torch
+        return torch.zeros((B, self.H, self.m, self.dv + 1), dtype=torch.float32, device="cuda")
+
+    def _chk_state(self, state, B):
+        import torch
+        if tuple(state.shape) != (B, self.H, self.m, self.dv + 1) or state.dtype != torch.float32 \
+                or not state.is_cuda or not state.is_contiguous():
+            raise ValueError(f"state: expected contiguous CUDA float32 [{B},{self.H},{self.m},{self.dv + 1}], "
+                             f"got {state.dtype} {tuple(state.shape)} on {state.device}")
+
+    def kv_state(self, k, v, state=None, stream=None):
+        """state += summary of (k, v); a new zero state if none is given.  Returns the state."""
+        B, _, L, _ = k.shape
+        self._chk(k, B, L, self.d, "k")
+        self._chk(v, B, L, self.dv, "v")
+        if state is None:
+            state = self.new_state(B)
+        self._chk_state(state, B)
+        favor_kv_state(self.handle, k, v, state, B, L, stream)
+        return state
+
+    def attn_from_state(self, q, state, out=None, stream=None):
+        B, _, L, _ = q.shape
+        self._chk(q, B, L, self.d, "q")
+        self._chk_state(state, B)
+        out = self._new(q, B, L, self.dv, out)
+        favor_attn_from_state(self.handle, q, state, out, B, L, stream)
+        return out
+
+    def causal_step(self, q, k, v, state, out=None, stream=None):
+        """Causal attention of T new tokens continuing from state (updated in place)."""
+        B, _, T, _ = q.shape
+        self._chk(q, B, T, self.d, "q")
+        self._chk(k, B, T, self.d, "k")
+        self._chk(v, B, T, self.dv, "v")
+        self._chk_state(state, B)
+        out = self._new(q, B, T, self.dv, out)
+        favor_attn_causal_step(self.handle, q, k, v, out, state, B, T, stream)
         return out
 
     def close(self):
