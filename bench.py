@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--seq-len", type=int, default=None,
                     help="override the workload's sequence length L (profiling a smaller case of the same shape)")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--decode-steps", type=int, default=200,
+                    help="one-token causal steps timed for the decode line (0 = skip)")
     ap.add_argument("--e2e-groups", type=int, default=4,
                     help="head groups pipelined over upload / compute / download streams in the e2e leg")
     ap.add_argument("--cpu-heads", type=int, default=2, help="heads of the workload in the CPU oracle sample")
@@ -295,6 +297,29 @@ def run_ours(args):
     job_units, ms_step = job_aggregate(units_step, ms_total / args.steps, device=dev)
     value = job_units / (ms_step / 1e3)
 
+    # Decoding: one new token per step continuing from a resident state
+    # (favor_attn_causal_step, T = 1), positive features, state prefilled from
+    # the workload's keys; timed with CUDA events on the stream.
+    decode = None
+    if args.decode_steps > 0:
+        hd_ = handles["softmax_pos"]
+        state = hd_.kv_state(kd, vd)
+        q1, k1, v1 = (t[:, :, :1].contiguous() for t in (qd, kd, vd))
+        o1 = torch.empty_like(v1)
+        for _ in range(10):
+            hd_.causal_step(q1, k1, v1, state, out=o1, stream=stream)
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(args.decode_steps):
+            hd_.causal_step(q1, k1, v1, state, out=o1, stream=stream)
+        d1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = d0.elapsed_time(d1) * 1e3 / args.decode_steps
+        nbytes = 2 * 4 * w.B * w.H * w.m * (w.dv + 1)
+        decode = {"us_per_step": us, "value": w.B * w.H / (us * 1e-6), "unit": "tokens*heads/s",
+                  "state_bytes_read_written": nbytes, "state_gbs": nbytes / (us * 1e-6) / 1e9,
+                  "config": f"B={w.B} H={w.H} m={w.m} d={w.d} dv={w.dv}, one token per step, positive features"}
+
     # End to end through the public API: pinned host inputs in, outputs back, every
     # step.  The heads are split into groups, one library handle per group (its
     # slice of omega), and three streams overlap the upload of group g+1, the four
@@ -418,7 +443,7 @@ def run_ours(args):
                                    f"calls per step: bidir+causal x softmax_pos+relu",
                        "global_batch": w.B * world, "seq_len": w.L, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (Q,K,V 384 MB per replica)"},
-            "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
+            "clocks": clocks, "e2e": e2e, "decode": decode, "gpu_launches": launches, "roofline": roofline,
             "roofline_all": roofline_all, "kernels": kernels, "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
     for hd in handles.values():

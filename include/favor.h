@@ -128,7 +128,8 @@ FAVOR_API favor_status favor_attn_causal(favor_handle h, const void* q, const vo
  * prefix sum started at a given state; the recurrence of Exploring Linear
  * Attention, "Autoregressive Generation"; causal Random Feature Attention).
  *
- * A state is a caller-owned DEVICE float array [B, H, m, dv+1], row-major:
+ * A state is a caller-owned DEVICE float array [B, H, m, dv+1], row-major,
+ * 16-byte aligned (else FAVOR_ERR_INVALID_ARG):
  * row r of head (b, h) is (S_r0 .. S_r,dv-1, z_r) with
  *     S = e^-kappa_h * sum_j phi(k_j) v_j^T,   z = e^-kappa_h * sum_j phi(k_j)
  * over the keys it summarises (phi the plain feature map above, m^-1/2

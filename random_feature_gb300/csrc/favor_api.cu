@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -353,6 +354,8 @@ favor_status favor_kv_state(favor_handle hd, const void* k, const void* v, float
     favor_status st = check_call("favor_kv_state", hd, B, L);
     if (st != FAVOR_OK) return st;
     if (!k || !v || !state) return set_error(FAVOR_ERR_INVALID_ARG, "favor_kv_state: null pointer");
+    if (reinterpret_cast<uintptr_t>(state) % 16)
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_kv_state: state must be 16-byte aligned");
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tc_supported(h)) return tc_kv_state(h, k, v, state, B, L, s);
@@ -364,6 +367,8 @@ favor_status favor_attn_from_state(favor_handle hd, const void* q, const float* 
     favor_status st = check_call("favor_attn_from_state", hd, B, L);
     if (st != FAVOR_OK) return st;
     if (!q || !state || !out) return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_from_state: null pointer");
+    if (reinterpret_cast<uintptr_t>(state) % 16)
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_from_state: state must be 16-byte aligned");
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tc_supported(h)) return tc_attn_from_state(h, q, state, out, B, L, s);
@@ -376,6 +381,8 @@ favor_status favor_attn_causal_step(favor_handle hd, const void* q, const void* 
     if (st != FAVOR_OK) return st;
     if (!q || !k || !v || !out || !state)
         return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_causal_step: null pointer");
+    if (reinterpret_cast<uintptr_t>(state) % 16)
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_causal_step: state must be 16-byte aligned");
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
     return simt_causal_step(h, q, k, v, out, state, B, T, reinterpret_cast<cudaStream_t>(stream));
 }

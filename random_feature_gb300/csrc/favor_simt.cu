@@ -498,9 +498,9 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
                                                      const T* __restrict__ v, T* __restrict__ out,
                                                      float* __restrict__ state, const float* __restrict__ omega,
                                                      const float* __restrict__ kshift, int H, int Tn, int m, int d,
-                                                     int dv, float s) {
+                                                     int dv, float s, int omega_in_smem) {
     extern __shared__ float sm[];
-    const int dp = dv + 1;
+    const int dp = dv + 1, wp = d + 1;
     float* S = sm;             // [m][dv+1]
     float* xq = S + m * dp;    // [d]
     float* xk = xq + d;        // [d]
@@ -508,15 +508,31 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
     float* fq = xv + dv;       // [m]
     float* rs = fq + m;        // [dv+1] readout sums
     float* red = rs + dp;      // [32]
+    float* ws = red + 32;      // [m][d+1] omega rows (when they fit)
     const int bh = blockIdx.x, h = bh % H, tid = threadIdx.x, nt = blockDim.x;
-    float* st = state + (size_t)bh * m * dp;
-    for (int i = tid; i < m * dp; i += nt) S[i] = st[i];
+    // state in: m*(dv+1) is a multiple of 4 (m is a multiple of 16), and so is every head's offset
+    const int n4 = m * dp / 4;
+    const float4* st4 = reinterpret_cast<const float4*>(state + (size_t)bh * m * dp);
+    for (int i = tid; i < n4; i += nt) {
+        const float4 x = st4[i];
+        S[4 * i] = x.x; S[4 * i + 1] = x.y; S[4 * i + 2] = x.z; S[4 * i + 3] = x.w;
+    }
+    const float* wg = omega + (size_t)h * m * d;
+    if (omega_in_smem) {
+        const float4* w4 = reinterpret_cast<const float4*>(wg);   // m*d is a multiple of 4
+        for (int i = tid; i < m * d / 4; i += nt) {
+            const float4 x = w4[i];
+            const int e = 4 * i, r = e / d, c = e - r * d;      // d is a multiple of 4: one row per float4
+            float* o = ws + r * wp + c;
+            o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+        }
+    }
     const float inv_sqrt_m = 1.f / sqrtf((float)m);
     const float kap = kshift[h];
-    const float* w = omega + ((size_t)h * m + (tid < m ? tid : 0)) * d;
+    const int rr = tid < m ? tid : 0;
     for (int t = 0; t < Tn; ++t) {
         const size_t row = (size_t)bh * Tn + t;
-        __syncthreads();   // the previous token's readout is done with fq, rs and S
+        __syncthreads();   // the previous token's readout is done with fq, rs and S (and the staging is done)
         for (int i = tid; i < d; i += nt) {
             xq[i] = ldf(q + row * d + i);
             xk[i] = ldf(k + row * d + i);
@@ -524,13 +540,24 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
         for (int i = tid; i < dv; i += nt) xv[i] = ldf(v + row * dv + i);
         __syncthreads();
         float pq = 0.f, pk = 0.f, nk = 0.f;
-        if (tid < m)
-            for (int c = 0; c < d; ++c) {
-                const float wc = __ldg(w + c);
-                pq = fmaf(wc, xq[c], pq);
-                pk = fmaf(wc, xk[c], pk);
-                nk = fmaf(xk[c], xk[c], nk);
+        if (tid < m) {
+            if (omega_in_smem) {
+                const float* w = ws + rr * wp;
+                for (int c = 0; c < d; ++c) {
+                    pq = fmaf(w[c], xq[c], pq);
+                    pk = fmaf(w[c], xk[c], pk);
+                    nk = fmaf(xk[c], xk[c], nk);
+                }
+            } else {
+                const float* w = wg + (size_t)rr * d;
+                for (int c = 0; c < d; ++c) {
+                    const float wc = __ldg(w + c);
+                    pq = fmaf(wc, xq[c], pq);
+                    pk = fmaf(wc, xk[c], pk);
+                    nk = fmaf(xk[c], xk[c], nk);
+                }
             }
+        }
         const float qx = s * pq;
         const float mx = KIND == FAVOR_KERNEL_SOFTMAX_POS ? block_max(tid < m ? qx : -INFINITY, red) : 0.f;
         if (tid < m) {
@@ -560,18 +587,22 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
         }
     }
     __syncthreads();
-    for (int i = tid; i < m * dp; i += nt) st[i] = S[i];
+    float4* so4 = reinterpret_cast<float4*>(state + (size_t)bh * m * dp);
+    for (int i = tid; i < n4; i += nt) so4[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
 }
 
 template <typename T, int KIND>
 favor_status causal_step_t(const Handle& h, const void* q, const void* k, const void* v, void* out, float* state,
                            int BH, int Tn, cudaStream_t st) {
-    const size_t smem = (size_t)(h.m * (h.dv + 1) + 2 * h.d + h.dv + h.m + (h.dv + 1) + 32) * sizeof(float);
+    const size_t base = (size_t)(h.m * (h.dv + 1) + 2 * h.d + h.dv + h.m + (h.dv + 1) + 32) * sizeof(float);
+    const size_t wbytes = (size_t)h.m * (h.d + 1) * sizeof(float);
+    const int in_smem = base + wbytes <= 200 * 1024 ? 1 : 0;
+    const size_t smem = base + (in_smem ? wbytes : 0);
     auto kern = k_causal_step<T, KIND>;
     set_smem(kern, smem);
     ProfScope ps(h, PROF_CAUSAL, st);
     kern<<<BH, 256, smem, st>>>((const T*)q, (const T*)k, (const T*)v, (T*)out, state, h.omega_f32, h.kshift, h.H,
-                                Tn, h.m, h.d, h.dv, h.s);
+                                Tn, h.m, h.d, h.dv, h.s, in_smem);
     count_launch();
     return check_launch("causal step kernel");
 }
