@@ -1,8 +1,8 @@
-"""FAVOR+ forward attention in plain float64 NumPy -- the oracle.
+"""FAVOR+ attention (forward and its gradients) in plain float64 NumPy -- the oracle.
 
 TEST INFRASTRUCTURE.  This module states, as directly as possible, what the
-FAVOR+ forward path computes, so that the CUDA library can be checked against
-it.  It is slow on purpose: no blocking, fusion or reordering beyond what the
+FAVOR+ forward path computes, and the exact derivative of it that the backward
+path computes, so that the CUDA library can be checked against it.  It is slow on purpose: no blocking, fusion or reordering beyond what the
 definitions below state, except that the causal prefix sum is carried block by
 block so the [L, m, dv+1] prefix tensor is never held whole (the two are the
 same sums).  Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
@@ -40,6 +40,8 @@ __all__ = [
     "favor_bidir", "favor_causal", "favor_feature_map",
     "favor_kv_state", "favor_attn_from_state", "favor_causal_from_state",
     "softmax_attention", "row_rel_err", "KINDS",
+    "feature_map_vjp", "attn_from_features_bidir_vjp", "attn_from_features_causal_vjp",
+    "favor_bidir_backward", "favor_causal_backward",
 ]
 
 KINDS = ("softmax_pos", "relu")
@@ -252,6 +254,125 @@ def favor_causal_from_state(q, k, v, state, omega, data_scale, kind="softmax_pos
             out[b, h] = _divide_rows(buf2[:, :-1], buf2[:, -1])
             new[b, h] = state[b, h] + pk.T @ c
     return out, new
+
+
+# ----------------------------------------------------------------- backward
+# The pages time the backward pass ([P] §4.1, Fig. 3) but print no formulas for
+# it, so the backward below is the exact reverse-mode derivative of the forward
+# steps above, taken step by step in reverse order.  For a scalar loss with
+# upstream gradient dO = d loss / d out:
+#   out_i = Buf3_i / buf4_i        ->  dBuf3_i = dO_i / buf4_i,
+#                                      dbuf4_i = -(dO_i . out_i) / buf4_i
+#   (a row with buf4_i == 0 has out_i = 0, a constant: both are 0 there)
+#   Buf2 = Q' Buf1                 ->  dQ' = dBuf2 Buf1^T,  dBuf1 = Q'^T dBuf2
+#   Buf1 = K'^T C, C = [V 1]       ->  dK' = C dBuf1^T,     dC = K' dBuf1
+# and the feature maps' own derivatives (feature_map_vjp).
+
+def feature_map_vjp(x, omega, kind, dphi):
+    """d loss / d x for phi = feature_map(x, omega, kind), given dphi = d loss / d phi.
+
+    Positive features ([P] Lemma 1): d phi_r / d x = phi_r (omega_r - x), so
+        dx = (dphi * phi) Omega - x * sum_r (dphi * phi)_r.
+    ReLU features ([P] App. A.4): d phi_r / d x = m^-1/2 [omega_r . x > 0] omega_r
+    (the derivative of max(u, 0) is taken as 0 at u = 0).
+    x [n, d], omega [m, d], dphi [n, m] -> [n, d].
+    """
+    x, omega, dphi = _f64(x), _f64(omega), _f64(dphi)
+    if kind == "softmax_pos":
+        g = dphi * feature_map_positive(x, omega)
+        return g @ omega - x * g.sum(axis=1, keepdims=True)
+    if kind == "relu":
+        mask = (x @ omega.T) > 0.0
+        return (np.where(mask, dphi, 0.0) @ omega) / np.sqrt(omega.shape[0])
+    raise ValueError(f"unknown feature kind {kind!r}")
+
+
+def _dbuf2(buf2, dout):
+    """[dBuf3 dbuf4] from Buf2 = [Buf3 buf4] and dO (rows with buf4 == 0 give 0)."""
+    num, den = buf2[:, :-1], buf2[:, -1]
+    out = _divide_rows(num, den)
+    d = np.zeros_like(buf2)
+    nz = den != 0.0
+    d[nz, :-1] = dout[nz] / den[nz, None]
+    d[nz, -1] = -np.sum(dout[nz] * out[nz], axis=1) / den[nz]
+    return d
+
+
+def attn_from_features_bidir_vjp(phi_q, phi_k, v, dout):
+    """Gradients of attn_from_features_bidir with respect to its three inputs.
+
+    Reverse of [P] App. B Alg. 1 (bidirectional branch), see the table above.
+    Returns (dphi_q [Lq, m], dphi_k [Lk, m], dv [Lk, dv]).
+    """
+    phi_q, phi_k, v, dout = _f64(phi_q), _f64(phi_k), _f64(v), _f64(dout)
+    c = np.concatenate([v, np.ones((v.shape[0], 1))], axis=1)
+    buf1 = phi_k.T @ c
+    d2 = _dbuf2(phi_q @ buf1, dout)
+    dbuf1 = phi_q.T @ d2
+    return d2 @ buf1.T, c @ dbuf1.T, (phi_k @ dbuf1)[:, :-1]
+
+
+def attn_from_features_causal_vjp(phi_q, phi_k, v, dout, block=512):
+    """Gradients of attn_from_features_causal with respect to its three inputs.
+
+    Reverse of [P] App. B.1 Eq. 11.  With G^PS_i = sum_{j<=i} K'_j C_j^T (the
+    forward prefix sums) and H_j = sum_{i>=j} Q'_i dBuf2_i^T (suffix sums of
+    the reverse pass):
+        dQ'_i = G^PS_i dBuf2_i,   dK'_j = H_j C_j,   dC_j = H_j^T K'_j.
+    Both sums are carried across blocks of ``block`` rows as in the forward:
+    the prefix from the first block on, the suffix from the last block back;
+    inside a block the within-block terms are written with tril of the
+    block's row-by-row products.
+    """
+    phi_q, phi_k, v, dout = _f64(phi_q), _f64(phi_k), _f64(v), _f64(dout)
+    L, m = phi_q.shape
+    c = np.concatenate([v, np.ones((L, 1))], axis=1)
+    # forward sweep: Buf2 (for dBuf2) and dQ' from the prefix sums
+    g_ps = np.zeros((m, c.shape[1]))
+    d2 = np.empty((L, c.shape[1]))
+    dphi_q = np.empty((L, m))
+    for b0 in range(0, L, block):
+        b1 = min(L, b0 + block)
+        pq, pk, cb = phi_q[b0:b1], phi_k[b0:b1], c[b0:b1]
+        d2[b0:b1] = _dbuf2(np.tril(pq @ pk.T) @ cb + pq @ g_ps, dout[b0:b1])
+        dphi_q[b0:b1] = np.tril(d2[b0:b1] @ cb.T) @ pk + d2[b0:b1] @ g_ps.T
+        g_ps = g_ps + pk.T @ cb
+    # reverse sweep: dK' and dC from the suffix sums
+    h_s = np.zeros((m, c.shape[1]))
+    dphi_k = np.empty((L, m))
+    dc = np.empty_like(c)
+    starts = list(range(0, L, block))
+    for b0 in reversed(starts):
+        b1 = min(L, b0 + block)
+        pq, pk, cb, db = phi_q[b0:b1], phi_k[b0:b1], c[b0:b1], d2[b0:b1]
+        dphi_k[b0:b1] = np.tril(db @ cb.T).T @ pq + cb @ h_s.T
+        dc[b0:b1] = np.tril(pq @ pk.T).T @ db + pk @ h_s
+        h_s = h_s + pq.T @ db
+    return dphi_q, dphi_k, dc[:, :-1]
+
+
+def _per_head_backward(q, k, v, dout, omega, data_scale, kind, vjp):
+    q, k, v, dout, omega = _f64(q), _f64(k), _f64(v), _f64(dout), _f64(omega)
+    dq, dk, dvv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    B, H = q.shape[:2]
+    for b in range(B):
+        for h in range(H):
+            x, y = data_scale * q[b, h], data_scale * k[b, h]
+            pq, pk = feature_map(x, omega[h], kind), feature_map(y, omega[h], kind)
+            dpq, dpk, dvv[b, h] = vjp(pq, pk, v[b, h], dout[b, h])
+            dq[b, h] = data_scale * feature_map_vjp(x, omega[h], kind, dpq)
+            dk[b, h] = data_scale * feature_map_vjp(y, omega[h], kind, dpk)
+    return dq, dk, dvv
+
+
+def favor_bidir_backward(q, k, v, dout, omega, data_scale, kind="softmax_pos"):
+    """(dq, dk, dv) of favor_bidir for the upstream gradient dout [B,H,L,dv]."""
+    return _per_head_backward(q, k, v, dout, omega, data_scale, kind, attn_from_features_bidir_vjp)
+
+
+def favor_causal_backward(q, k, v, dout, omega, data_scale, kind="softmax_pos"):
+    """(dq, dk, dv) of favor_causal for the upstream gradient dout [B,H,L,dv]."""
+    return _per_head_backward(q, k, v, dout, omega, data_scale, kind, attn_from_features_causal_vjp)
 
 
 def softmax_attention(q, k, v, data_scale, causal=False):

@@ -28,7 +28,7 @@ import math
 import numpy as np
 
 __all__ = ["CONFIGS", "Workload", "make_omega_orf", "make_omega_iid",
-           "make_qkv", "make_workload", "round_bf16"]
+           "make_qkv", "make_workload", "make_upstream_grad", "round_bf16"]
 
 
 def round_bf16(a: np.ndarray) -> np.ndarray:
@@ -151,3 +151,13 @@ def make_workload(w: Workload, seed: int = 0):
     if w.dtype == "bf16":
         omega, q, k, v = (round_bf16(a) for a in (omega, q, k, v))
     return omega, q, k, v
+
+
+def make_upstream_grad(w: Workload, seed: int = 0) -> np.ndarray:
+    """Upstream gradient dO [B,H,L,dv] for a backward call on workload ``w``:
+    N(0, 1) entries from Generator(PCG64(seed + 1_000_003)), a stream of its
+    own so that adding it leaves the forward inputs of ``seed`` unchanged;
+    rounded to bfloat16 values for bf16 workloads."""
+    rng = np.random.Generator(np.random.PCG64(seed + 1_000_003))
+    g = rng.standard_normal((w.B, w.H, w.L, w.dv), dtype=np.float32)
+    return round_bf16(g) if w.dtype == "bf16" else g

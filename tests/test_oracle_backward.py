@@ -1,0 +1,165 @@
+"""Pins for the oracle's backward (gradients of the forward attention).
+
+The pages print no backward formulas, so the gradients are pinned to the
+forward itself through routes that share none of the backward's algebra:
+central finite differences of the (separately pinned) forward, the explicit
+L x L form in which the output is linear in V, invariants of the normalised
+attention, and special cases whose gradients are known in closed form.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from synth import make_omega_orf
+
+
+def _inputs(seed, L=12, d=4, dv=3, m=8, std=0.6, H=1, B=1):
+    rng = np.random.default_rng(seed)
+    omega = np.stack([make_omega_orf(rng, m, d) for _ in range(H)])
+    q = rng.normal(0, std, (B, H, L, d))
+    k = rng.normal(0, std, (B, H, L, d))
+    v = rng.normal(0, 1.0, (B, H, L, dv))
+    g = rng.normal(0, 1.0, (B, H, L, dv))
+    return omega, q, k, v, g
+
+
+FWD = {"bidir": O.favor_bidir, "causal": O.favor_causal}
+BWD = {"bidir": O.favor_bidir_backward, "causal": O.favor_causal_backward}
+
+
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+@pytest.mark.parametrize("kind", O.KINDS)
+def test_gradients_match_central_differences(mode, kind):
+    """<grad, u> equals (f(x + h u) - f(x - h u)) / 2h for the loss <dO, out>,
+    along random directions u of q, k and v (every element perturbed)."""
+    omega, q, k, v, g = _inputs(1)
+    s = 0.8
+    grads = BWD[mode](q, k, v, g, omega, s, kind)
+    rng = np.random.default_rng(7)
+    h = 1e-6
+    for which in range(3):
+        for _ in range(3):
+            u = rng.normal(size=(q, k, v)[which].shape)
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[which] = args_p[which] + h * u
+            args_m[which] = args_m[which] - h * u
+            fp = np.sum(g * FWD[mode](*args_p, omega, s, kind))
+            fm = np.sum(g * FWD[mode](*args_m, omega, s, kind))
+            fd = (fp - fm) / (2 * h)
+            an = np.sum(grads[which] * u)
+            assert an == pytest.approx(fd, rel=2e-6, abs=1e-8), (which, an, fd)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dv_equals_explicit_transpose(causal):
+    """out = A V with A = D^-1 A_hat ([P] Eq. 1/2 with the kernel estimate), so
+    dV = A^T dO exactly; A built by explicit loops over (i, j)."""
+    omega, q, k, v, g = _inputs(2, L=9)
+    s = 0.9
+    pq = O.feature_map(s * q[0, 0], omega[0], "softmax_pos")
+    pk = O.feature_map(s * k[0, 0], omega[0], "softmax_pos")
+    L = pq.shape[0]
+    a = np.zeros((L, L))
+    for i in range(L):
+        for j in range(L):
+            if causal and j > i:
+                continue
+            a[i, j] = sum(pq[i, r] * pk[j, r] for r in range(pq.shape[1]))
+        a[i] /= a[i].sum()
+    dv_ref = a.T @ g[0, 0]
+    fn = O.favor_causal_backward if causal else O.favor_bidir_backward
+    _, _, dv = fn(q, k, v, g, omega, s)
+    np.testing.assert_allclose(dv[0, 0], dv_ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+def test_dv_columns_sum_to_upstream(mode):
+    """Rows of the normalised attention sum to 1, so sum_j dV_j = sum_i dO_i."""
+    omega, q, k, v, g = _inputs(3, L=40, d=8, dv=5, m=16)
+    _, _, dv = BWD[mode](q, k, v, g, omega, 0.7)
+    np.testing.assert_allclose(dv.sum(axis=2), g.sum(axis=2), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+def test_query_key_grads_invariant_to_value_shift(mode):
+    """out is a convex combination of value rows (positive features), so
+    V -> V + 1 c^T shifts every output row by c and leaves the q and k
+    gradients unchanged.  Dropping the denominator's term breaks this."""
+    omega, q, k, v, g = _inputs(4, L=30, d=6, dv=4, m=12)
+    c = np.array([3.0, -2.0, 0.5, 7.0])
+    dq0, dk0, dv0 = BWD[mode](q, k, v, g, omega, 0.8)
+    dq1, dk1, dv1 = BWD[mode](q, k, v + c, g, omega, 0.8)
+    np.testing.assert_allclose(dq1, dq0, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dk1, dk0, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dv1, dv0, rtol=1e-12, atol=1e-13)
+
+
+def test_zero_projection_gives_zero_query_gradient():
+    """omega = 0: phi(x) = m^-1/2 exp(-||x||^2/2) 1, the same factor for every
+    feature, so the bidirectional output does not depend on q and dq = 0;
+    dk follows the closed form out = sum_j w_j v_j / sum_j w_j with
+    w_j = exp(-s^2 ||k_j||^2 / 2):  dk_j = -s^2 k_j w_j (v_j - out) . dO_sum / W."""
+    omega, q, k, v, g = _inputs(5, L=10)
+    omega = np.zeros_like(omega)
+    s = 0.7
+    dq, dk, _ = O.favor_bidir_backward(q, k, v, g, omega, s)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-15)
+    kk, vv, gs = k[0, 0], v[0, 0], g[0, 0].sum(axis=0)
+    w = np.exp(-0.5 * s * s * np.sum(kk * kk, axis=1))
+    out = (w @ vv) / w.sum()
+    dk_ref = -(s * s) * kk * (w * ((vv - out) @ gs) / w.sum())[:, None]
+    np.testing.assert_allclose(dk[0, 0], dk_ref, rtol=1e-11, atol=1e-13)
+
+
+@pytest.mark.parametrize("kind", O.KINDS)
+def test_causal_last_row_gradient_equals_bidirectional(kind):
+    """Causal row L sees every key, as the bidirectional rows do ([P] Eq. 2 vs
+    Eq. 1): with dO nonzero only on the last row, both backwards agree."""
+    omega, q, k, v, g = _inputs(6, L=17)
+    g[:, :, :-1] = 0.0
+    a = O.favor_causal_backward(q, k, v, g, omega, 0.8, kind)
+    ga = O.favor_bidir_backward(q, k, v, g, omega, 0.8, kind)
+    np.testing.assert_allclose(a[0][:, :, -1], ga[0][:, :, -1], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(a[1], ga[1], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(a[2], ga[2], rtol=1e-11, atol=1e-13)
+    np.testing.assert_array_equal(a[0][:, :, :-1], 0.0)
+
+
+def test_causal_single_token():
+    """L = 1: out_1 = v_1 whatever q and k (positive features), so dv = dO and
+    dq = dk = 0."""
+    omega, q, k, v, g = _inputs(7, L=1)
+    dq, dk, dv = O.favor_causal_backward(q, k, v, g, omega, 0.9)
+    np.testing.assert_allclose(dv, g, rtol=1e-14)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-14)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-14)
+
+
+def test_causal_blocks_do_not_change_the_result():
+    """The reverse sweep carries its suffix sums block by block: block sizes
+    1, 5 and 512 give the same gradients (the same sums, regrouped)."""
+    omega, q, k, v, g = _inputs(8, L=23)
+    pq = O.feature_map(0.8 * q[0, 0], omega[0], "softmax_pos")
+    pk = O.feature_map(0.8 * k[0, 0], omega[0], "softmax_pos")
+    ref = O.attn_from_features_causal_vjp(pq, pk, v[0, 0], g[0, 0], block=512)
+    for blk in (1, 5):
+        got = O.attn_from_features_causal_vjp(pq, pk, v[0, 0], g[0, 0], block=blk)
+        for a, b in zip(got, ref):
+            np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-13)
+
+
+def test_relu_zero_denominator_rows_have_zero_gradient():
+    """ReLU features can give a causal row with den = 0 (its output is 0 by the
+    convention); that row contributes nothing to any gradient."""
+    d, m = 2, 2
+    omega = np.eye(2)[None]                      # phi(x) = max(x, 0) / sqrt(2)
+    q = np.array([[[[-1.0, -1.0], [1.0, 1.0], [1.0, 0.5]]]])
+    k = np.array([[[[1.0, 1.0], [2.0, 1.0], [0.5, 1.0]]]])
+    v = np.array([[[[1.0], [2.0], [3.0]]]])
+    g = np.array([[[[5.0], [0.0], [0.0]]]])      # only row 1, whose den is 0
+    dq, dk, dv = O.favor_causal_backward(q, k, v, g, omega, 1.0, "relu")
+    assert O.favor_causal(q, k, v, omega, 1.0, "relu")[0, 0, 0, 0] == 0.0
+    np.testing.assert_array_equal(dq, 0.0)
+    np.testing.assert_array_equal(dk, 0.0)
+    np.testing.assert_array_equal(dv, 0.0)
