@@ -173,6 +173,43 @@ FAVOR_API favor_status favor_attn_causal_step(favor_handle h, const void* q, con
                                               void* out, float* state, int B, int T, void* stream);
 
 /*
+ * favor_attn_bidir_backward / favor_attn_causal_backward -- gradients of
+ * favor_attn_bidir / favor_attn_causal with respect to q, k and v.
+ *
+ * Rethinking Attention with Performers times the backward pass (§4.1, Fig. 3)
+ * without printing its formulas; these calls return the exact derivative of
+ * the forward (App. B Alg. 1 and App. B.1 Eq. 11), up to rounding: for a loss
+ * with upstream gradient dO = dloss/dout,
+ *     D_i = [dO_i / den_i, -(dO_i . out_i) / den_i]       (0 where den_i == 0)
+ *     dphi(q_i) = G_i D_i,  G_i = sum over the keys row i sees of phi(k_j) [v_j 1]^T
+ *     dphi(k_j) = H_j [v_j 1],  dv_j = H_j^T phi(k_j),
+ *                 H_j = sum over the queries that see key j of phi(q_i) D_i^T
+ * then through the feature map (x = s*q): positive features
+ *     dq = s * ((dphi . phi) Omega - x sum_r (dphi . phi)_r),
+ * ReLU features dq = s * m^-1/2 (dphi . [Omega x > 0]) Omega (the derivative of
+ * max(u, 0) at u = 0 is taken as 0); likewise dk.
+ *
+ *   q, k, v    the forward's inputs, as passed to the forward call.
+ *   dout       dO [B,H,L,dv].
+ * The forward's output is not an argument: dO_i . out_i is computed inside,
+ * in fp32, as phi(q_i) . (G_i applied to dO_i) / den_i, so a rounded copy of
+ * out (e.g. bf16) cannot perturb the gradients.
+ *   dq, dk     [B,H,L,d], dv [B,H,L,dv]: written, never read; must not alias
+ *              any input.
+ * All tensors are contiguous device arrays of the handle's dtype; the
+ * arithmetic is fp32 on the CUDA cores whatever the dtype, with the forward's
+ * cancelling shifts.  Same argument checks, asynchrony and one-call-per-handle
+ * rule as the forward calls; the handle's workspace (allocated by
+ * favor_create) is reused, nothing is allocated.
+ */
+FAVOR_API favor_status favor_attn_bidir_backward(favor_handle h, const void* q, const void* k, const void* v,
+                                                 const void* dout, void* dq, void* dk, void* dv,
+                                                 int B, int L, void* stream);
+FAVOR_API favor_status favor_attn_causal_backward(favor_handle h, const void* q, const void* k, const void* v,
+                                                  const void* dout, void* dq, void* dk, void* dv,
+                                                  int B, int L, void* stream);
+
+/*
  * favor_attn_bidir_noalloc -- favor_attn_bidir without a handle and without
  * any allocation.  The pages have no counterpart: this is an interface
  * convenience.  It serves callers that may not allocate device memory through

@@ -107,6 +107,9 @@ static void free_handle(Handle* h) {
     cudaFree(h->dev_err);
     cudaFree(h->ws_partial);
     cudaFree(h->ws_state);
+    cudaFree(h->ws_partial2);
+    cudaFree(h->ws_dstate);
+    cudaFree(h->ws_rowstat);
     cudaFree(h->ws_tc);
     free(h->omega_sqnorm_half_host);
     if (h->prof) {
@@ -206,6 +209,11 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     if (e == cudaSuccess) e = cudaMemset(h->dev_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_partial, rows * st_elems * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_state, (size_t)max_B * H * st_elems * sizeof(float));
+    // Backward: a second set of per-segment states, the reduced sum of
+    // phi~_q D^T, and four floats per (head, query) for the causal key pass.
+    if (e == cudaSuccess) e = cudaMalloc(&h->ws_partial2, rows * st_elems * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->ws_dstate, (size_t)max_B * H * st_elems * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->ws_rowstat, (size_t)max_B * H * (size_t)max_L * 4 * sizeof(float));
     if (e != cudaSuccess) {
         favor_status st = (e == cudaErrorMemoryAllocation) ? FAVOR_ERR_NOMEM : FAVOR_ERR_CUDA;
         set_error(st, "favor_create: cudaMalloc: %s", cudaGetErrorString(e));
@@ -387,6 +395,29 @@ favor_status favor_attn_causal_step(favor_handle hd, const void* q, const void* 
     return simt_causal_step(h, q, k, v, out, state, B, T, reinterpret_cast<cudaStream_t>(stream));
 }
 
+static favor_status backward_call(const char* fn, bool causal, favor_handle hd, const void* q, const void* k,
+                                  const void* v, const void* dout, void* dq, void* dk, void* dv, int B, int L,
+                                  void* stream) {
+    favor_status st = check_call(fn, hd, B, L);
+    if (st != FAVOR_OK) return st;
+    if (!q || !k || !v || !dout || !dq || !dk || !dv)
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return causal ? simt_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, s)
+                  : simt_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
+}
+
+favor_status favor_attn_bidir_backward(favor_handle hd, const void* q, const void* k, const void* v,
+                                       const void* dout, void* dq, void* dk, void* dv, int B, int L, void* stream) {
+    return backward_call("favor_attn_bidir_backward", false, hd, q, k, v, dout, dq, dk, dv, B, L, stream);
+}
+
+favor_status favor_attn_causal_backward(favor_handle hd, const void* q, const void* k, const void* v,
+                                        const void* dout, void* dq, void* dk, void* dv, int B, int L, void* stream) {
+    return backward_call("favor_attn_causal_backward", true, hd, q, k, v, dout, dq, dk, dv, B, L, stream);
+}
+
 favor_status favor_device_error(favor_handle hd, int* code) {
     if (!hd || !code) return set_error(FAVOR_ERR_INVALID_ARG, "favor_device_error: null argument");
     const Handle* h = reinterpret_cast<const Handle*>(hd);
@@ -399,7 +430,8 @@ favor_status favor_device_error(favor_handle hd, int* code) {
 }
 
 static const char* kSlotNames[PROF_NSLOTS] = {"feature_map", "segment_state", "segment_combine",
-                                               "bidir_readout", "causal_chunks"};
+                                               "bidir_readout", "causal_chunks", "backward_query",
+                                               "backward_key"};
 
 int favor_profile_slots(void) { return PROF_NSLOTS; }
 

@@ -1,0 +1,676 @@
+// Backward of FAVOR+ attention on the CUDA cores (FFMA): dq, dk, dv of the
+// bidirectional and causal calls, for every supported shape, fp32 arithmetic.
+//
+// The gradients are the exact derivative of the forward of Rethinking Attention
+// with Performers, App. B Alg. 1 (bidirectional) and App. B.1 Eq. 11 (causal).
+// With C = [V 1], Buf2 = Q' (K'^T C) = [num den] and out = num / den:
+//   D_i   = [dO_i / den_i,  -(dO_i . out_i) / den_i]      (0 where den_i == 0)
+//   dQ'_i = G^PS_i D_i    with G^PS_i = sum_{j<=i} K'_j C_j^T (all j if bidirectional)
+//   dK'_j = H_j C_j       with H_j    = sum_{i>=j} Q'_i D_i^T (all i if bidirectional)
+//   dC_j  = H_j^T K'_j    (dv = its first dv columns)
+// and through the feature maps (x = s*q):
+//   positive  dq = s * (G Omega - x sum_r G_r),  G = dQ' * Q'   (elementwise)
+//   ReLU      dq = s * (dQ'~ * [Omega x > 0]) Omega
+// dO_i . out_i is not taken from the caller: with u_i = G^PS_i^T-applied dO_i,
+// i.e. u_i[r] = sum_e G^PS_i[r][e] dO_i[e], it is sum_r phi_q(i)[r] u_i[r] / den_i,
+// computed here in fp32 from the same features (the identity that makes
+// sum_r G_r vanish then holds to fp32 rounding).
+// The kernels use the same shifted features as the forward (a per-head key
+// shift kappa_h, a per-query row shift, no m^-1/2); every product above pairs a
+// feature with a quantity divided by the matching denominator, so the shifts
+// cancel exactly, as they do in the forward output.
+//
+// Work split: every (batch, head) row of tokens is cut into the forward's
+// segments; a segment is walked in tiles of TT tokens.  The query pass needs
+// G^PS at each query (the forward's per-segment prefix states, plus the
+// tile's own keys), the key pass needs H at each key (per-segment suffix sums
+// of phi~_q D^T, plus the tile's own queries): the chunked form of Eq. 11, in
+// which the within-tile terms are a masked TT x TT product and the rest is one
+// state per tile.  Bidirectional calls are the same passes with a single full
+// state and no within-tile terms.
+#include <cmath>
+
+#include "favor_internal.h"
+
+namespace favor {
+namespace {
+
+template <typename T> __device__ __forceinline__ float ldb(const T* p);
+template <> __device__ __forceinline__ float ldb<float>(const float* p) { return *p; }
+template <> __device__ __forceinline__ float ldb<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+template <typename T> __device__ __forceinline__ void stb(T* p, float x);
+template <> __device__ __forceinline__ void stb<float>(float* p, float x) { *p = x; }
+template <> __device__ __forceinline__ void stb<__nv_bfloat16>(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+template <int DV>
+struct BwdShape {
+    static constexpr int TT = DV >= 128 ? 16 : 32;   // tokens per tile
+    static constexpr int DVP = DV + 4;               // padded [V 1] / D row (16-byte rows)
+    static constexpr int W = DV + 1;                 // state row width
+};
+
+__device__ __forceinline__ float warp_sum(float a) {
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    return a;
+}
+__device__ __forceinline__ float warp_max(float a) {
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    return a;
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+// Shared-memory plan (floats) of one pass; every buffer starts 16-byte aligned.
+struct BwdSmem {
+    int xs, ys, cs, dd, fq, fk, ub, aa, mm, rs, zs, cq, den, go, kn, total;
+};
+
+__host__ __device__ inline int al4(int n) { return (n + 3) & ~3; }
+
+__host__ __device__ inline BwdSmem bwd_smem(int TT, int DVP, int W, int m, int d, bool causal, bool key_pass) {
+    BwdSmem p;
+    int o = 0;
+    const int MP = m + 1;
+    p.xs = o; o += al4(TT * d);                                   // query tile (raw)
+    p.ys = o; o += al4(TT * d);                                   // key tile (raw)
+    p.cs = o; o += al4(TT * DVP);                                 // [v 1 0 0 0] rows
+    p.dd = o; o += al4(TT * DVP);                                 // dO, then D = [dnum dden]
+    p.fq = o; o += al4(TT * MP);                                  // query features (then G on the query pass)
+    p.fk = o; o += al4(TT * MP);                                  // key features (then G on the key pass)
+    p.ub = o; o += key_pass ? 0 : al4(TT * MP);                   // u = G^PS dO (query pass)
+    p.aa = o; o += causal ? al4(TT * (TT + 1)) : 0;               // masked phi_q . phi_k
+    p.mm = o; o += causal ? al4(TT * (TT + 1)) : 0;               // masked dO . v (query) / D . C (key)
+    p.rs = o; o += key_pass ? al4(m * W) : 0;                     // H at the tile end (key pass)
+    p.zs = o; o += al4(m);                                        // z column of the query pass state
+    p.cq = o; o += al4(TT);
+    p.den = o; o += al4(TT);
+    p.go = o; o += al4(TT);
+    p.kn = o; o += al4(TT);
+    p.total = o;
+    return p;
+}
+
+// Projections s*(omega_r . x_j) for j < TT into buf[j][r] (row stride m+1).
+template <int TT>
+__device__ __forceinline__ void project_tile(const float* __restrict__ om, const float* xs, float* buf, int r, int m,
+                                             int d, float s) {
+    float p[TT];
+#pragma unroll
+    for (int j = 0; j < TT; ++j) p[j] = 0.f;
+    const float4* w4 = reinterpret_cast<const float4*>(om + (size_t)r * d);
+    const float4* x4 = reinterpret_cast<const float4*>(xs);
+    const int d4 = d >> 2;
+#pragma unroll 1
+    for (int c4 = 0; c4 < d4; ++c4) {
+        const float4 w = __ldg(w4 + c4);
+#pragma unroll
+        for (int j = 0; j < TT; ++j) p[j] += dot4(w, x4[j * d4 + c4]);
+    }
+#pragma unroll
+    for (int j = 0; j < TT; ++j) buf[j * (m + 1) + r] = s * p[j];
+}
+
+// Stage rows [t0, t0+nt) of a [BH, L, w] tensor into dst[TT][stride] as fp32;
+// rows past nt and columns [w, stride) are zero, column w is `one_col` if >= 0.
+template <typename T>
+__device__ __forceinline__ void stage_rows(const T* __restrict__ src, float* dst, int t0, int nt, int TT, int w,
+                                           int stride, float one_col) {
+    for (int idx = threadIdx.x; idx < TT * stride; idx += blockDim.x) {
+        const int j = idx / stride, c = idx - j * stride;
+        float x = 0.f;
+        if (j < nt) {
+            if (c < w) x = ldb(src + (size_t)(t0 + j) * w + c);
+            else if (c == w && one_col >= 0.f) x = one_col;
+        }
+        dst[idx] = x;
+    }
+}
+
+// Squared key norms kn_j of a staged key tile, one warp per token.
+__device__ __forceinline__ void key_norms(const float* ys, float* kn, int TT, int d) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int j = warp; j < TT; j += nw) {
+        float a = 0.f;
+        for (int c = lane; c < d; c += 32) a = fmaf(ys[j * d + c], ys[j * d + c], a);
+        a = warp_sum(a);
+        if (lane == 0) kn[j] = a;
+    }
+}
+
+// Row max of the raw query projections (positive features), one warp per token.
+__device__ __forceinline__ void row_shift(const float* fq, float* cq, int TT, int nt, int m) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int j = warp; j < TT; j += nw) {
+        float mx = -INFINITY;
+        for (int r = lane; r < m; r += 32) mx = fmaxf(mx, fq[j * (m + 1) + r]);
+        mx = warp_max(mx);
+        if (lane == 0) cq[j] = j < nt ? mx : 0.f;
+    }
+}
+
+// D rows from dO (in place in dd), den and go: D = [dO/den, -go/den, 0...].
+__device__ __forceinline__ void make_d(float* dd, const float* den, const float* go, int TT, int DV, int DVP) {
+    for (int idx = threadIdx.x; idx < TT * DVP; idx += blockDim.x) {
+        const int j = idx / DVP, e = idx - j * DVP;
+        const float dn = den[j];
+        float x = 0.f;
+        if (dn != 0.f) {
+            if (e < DV) x = dd[idx] / dn;
+            else if (e == DV) x = -go[j] / dn;
+        }
+        dd[idx] = x;
+    }
+}
+
+// dx rows from G (row stride m+1) for a tile: dx_j = s*(G_j Omega - s*x_j sum_r G_jr)
+// (positive) or s*G_j Omega (ReLU), written as rows [t0, t0+nt) of dst.
+template <typename T, int KIND>
+__device__ __forceinline__ void grad_inputs(const float* g, const float* xs, const float* __restrict__ om,
+                                            T* __restrict__ dst, int t0, int nt, int TT, int m, int d, float s) {
+    const int d4 = d >> 2;
+    const float4* w4 = reinterpret_cast<const float4*>(om);
+    for (int idx = threadIdx.x; idx < TT * d4; idx += blockDim.x) {
+        const int j = idx / d4, c4 = idx - j * d4;
+        if (j >= nt) continue;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        float gsum = 0.f;
+        const float* gj = g + j * (m + 1);
+#pragma unroll 4
+        for (int r = 0; r < m; ++r) {
+            const float gr = gj[r];
+            const float4 w = __ldg(w4 + r * d4 + c4);
+            a.x = fmaf(gr, w.x, a.x);
+            a.y = fmaf(gr, w.y, a.y);
+            a.z = fmaf(gr, w.z, a.z);
+            a.w = fmaf(gr, w.w, a.w);
+            gsum += gr;
+        }
+        const float* xj = xs + j * d + 4 * c4;
+        T* o = dst + (size_t)(t0 + j) * d + 4 * c4;
+        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+            const float t = s * gsum;
+            stb(o + 0, s * fmaf(-t, xj[0], a.x));
+            stb(o + 1, s * fmaf(-t, xj[1], a.y));
+            stb(o + 2, s * fmaf(-t, xj[2], a.z));
+            stb(o + 3, s * fmaf(-t, xj[3], a.w));
+        } else {
+            stb(o + 0, s * a.x);
+            stb(o + 1, s * a.y);
+            stb(o + 2, s * a.z);
+            stb(o + 3, s * a.w);
+        }
+    }
+}
+
+// ------------------------------------------------------------ query pass
+// grid (n_seg, B*H), blockDim = m rounded up to 32.  Thread r < m owns feature
+// r: the state row (G^PS at the tile start, or the full S~ | z~) and the
+// segment's running sum of phi~_q D^T.  Writes dq, the per-segment sums into
+// part, and (causal) the per-query (den~, shift, dO . out) for the key pass.
+template <typename T, int KIND, int DV, bool CAUSAL>
+__global__ void __launch_bounds__(256) k_bwd_query(const T* __restrict__ q, const T* __restrict__ k,
+                                                   const T* __restrict__ v, const T* __restrict__ dout,
+                                                   T* __restrict__ dq, const float* __restrict__ omega,
+                                                   const float* __restrict__ kshift, const float* __restrict__ state0,
+                                                   float* __restrict__ part, float4* __restrict__ rowstat, int H,
+                                                   int L, int m, int d, float s, int seg_len, int n_seg) {
+    using S = BwdShape<DV>;
+    constexpr int TT = S::TT, DVP = S::DVP, W = S::W;
+    extern __shared__ __align__(16) float sm[];
+    const BwdSmem P = bwd_smem(TT, DVP, W, m, d, CAUSAL, false);
+    float *xs = sm + P.xs, *ys = sm + P.ys, *cs = sm + P.cs, *dd = sm + P.dd, *fq = sm + P.fq, *fk = sm + P.fk;
+    float *ub = sm + P.ub, *aa = sm + P.aa, *mm = sm + P.mm, *zs = sm + P.zs, *cq = sm + P.cq, *den = sm + P.den,
+          *go = sm + P.go, *kn = sm + P.kn;
+    const int MP = m + 1;
+    const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int r = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const bool own = r < m;
+    const float* om = omega + (size_t)h * m * d;
+    const float kap = kshift[h];
+    const size_t row0 = (size_t)bh * L;
+
+    float st[W], acc[W];
+    {
+        const float* s0 = state0 + (CAUSAL ? ((size_t)bh * n_seg + seg) : (size_t)bh) * m * W + (size_t)r * W;
+#pragma unroll
+        for (int e = 0; e < W; ++e) {
+            st[e] = own ? s0[e] : 0.f;
+            acc[e] = 0.f;
+        }
+    }
+    const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    for (int t0 = j0; t0 < j1; t0 += TT) {
+        const int nt = min(TT, j1 - t0);
+        __syncthreads();   // the previous tile is done with every buffer
+        stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
+        stage_rows(dout + row0 * DV, dd, t0, nt, TT, DV, DVP, -1.f);
+        if (CAUSAL) {
+            stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
+            stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+        }
+        __syncthreads();
+        if (CAUSAL) key_norms(ys, kn, TT, d);
+        if (own) {
+            project_tile<TT>(om, xs, fq, r, m, d, s);
+            if (CAUSAL) project_tile<TT>(om, ys, fk, r, m, d, s);
+            zs[r] = st[DV];
+        }
+        __syncthreads();
+        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+            row_shift(fq, cq, TT, nt, m);
+            __syncthreads();
+        }
+        if (own) {
+#pragma unroll 4
+            for (int j = 0; j < TT; ++j) {
+                const float pq = fq[j * MP + r];
+                float f = 0.f;
+                if (j < nt) f = KIND == FAVOR_KERNEL_SOFTMAX_POS ? expf(pq - cq[j]) : fmaxf(pq, 0.f);
+                fq[j * MP + r] = f;
+                if (CAUSAL) {
+                    const float pk = fk[j * MP + r];
+                    float g = 0.f;
+                    if (j < nt)
+                        g = KIND == FAVOR_KERNEL_SOFTMAX_POS ? expf(pk - 0.5f * s * s * kn[j] - kap) : fmaxf(pk, 0.f);
+                    fk[j * MP + r] = g;
+                }
+            }
+        }
+        __syncthreads();
+        if (CAUSAL) {   // aa[j][i] = phi~_q(j) . phi~_k(i), mm[j][i] = dO_j . v_i, for i <= j
+            for (int idx = threadIdx.x; idx < TT * TT; idx += blockDim.x) {
+                const int j = idx / TT, i = idx - j * TT;
+                float a = 0.f, b = 0.f;
+                if (i <= j) {
+                    for (int rr = 0; rr < m; ++rr) a = fmaf(fq[j * MP + rr], fk[i * MP + rr], a);
+                    const float4* gj = reinterpret_cast<const float4*>(dd + j * DVP);
+                    const float4* ci = reinterpret_cast<const float4*>(cs + i * DVP);
+#pragma unroll 4
+                    for (int e4 = 0; e4 < DVP / 4; ++e4) b += dot4(gj[e4], ci[e4]);
+                }
+                aa[j * (TT + 1) + i] = a;
+                mm[j * (TT + 1) + i] = b;
+            }
+            __syncthreads();
+        }
+        // den~_j = phi~_q(j) . z(tile start) + sum_{i<=j} aa[j][i]
+        for (int j = warp; j < TT; j += nw) {
+            float a = 0.f;
+            for (int rr = lane; rr < m; rr += 32) a = fmaf(fq[j * MP + rr], zs[rr], a);
+            if (CAUSAL && lane <= j && lane < TT) a += aa[j * (TT + 1) + lane];
+            a = warp_sum(a);
+            if (lane == 0) den[j] = j < nt ? a : 0.f;
+        }
+        // u_j[r] = sum_e G^PS_j[r][e] dO_j[e] (value columns only)
+        if (own) {
+#pragma unroll 1
+            for (int j = 0; j < TT; ++j) {
+                const float4* gj = reinterpret_cast<const float4*>(dd + j * DVP);
+                float u = 0.f;
+#pragma unroll
+                for (int e4 = 0; e4 < DV / 4; ++e4) {
+                    const float4 x = gj[e4];
+                    u = fmaf(st[4 * e4 + 0], x.x, u);
+                    u = fmaf(st[4 * e4 + 1], x.y, u);
+                    u = fmaf(st[4 * e4 + 2], x.z, u);
+                    u = fmaf(st[4 * e4 + 3], x.w, u);
+                }
+                if (CAUSAL)
+                    for (int i = 0; i <= j; ++i) u = fmaf(fk[i * MP + r], mm[j * (TT + 1) + i], u);
+                ub[j * MP + r] = u;
+            }
+        }
+        __syncthreads();
+        // go_j = dO_j . out_j = phi~_q(j) . u_j / den~_j
+        for (int j = warp; j < TT; j += nw) {
+            float a = 0.f;
+            for (int rr = lane; rr < m; rr += 32) a = fmaf(fq[j * MP + rr], ub[j * MP + rr], a);
+            a = warp_sum(a);
+            if (lane == 0) {
+                const float dn = den[j];
+                const float g = dn != 0.f ? a / dn : 0.f;
+                go[j] = g;
+                if (CAUSAL && j < nt)
+                    rowstat[row0 + t0 + j] =
+                        make_float4(dn, KIND == FAVOR_KERNEL_SOFTMAX_POS ? cq[j] : 0.f, g, 0.f);
+            }
+        }
+        __syncthreads();
+        make_d(dd, den, go, TT, DV, DVP);
+        __syncthreads();
+        if (own) {
+            float zr = st[DV];   // z at query j: tile start plus the tile's keys i <= j
+#pragma unroll 1
+            for (int j = 0; j < TT; ++j) {
+                const float f = fq[j * MP + r];
+                if (CAUSAL) zr += fk[j * MP + r];
+                const float4* dj = reinterpret_cast<const float4*>(dd + j * DVP);
+#pragma unroll
+                for (int e4 = 0; e4 < DV / 4; ++e4) {
+                    const float4 x = dj[e4];
+                    acc[4 * e4 + 0] = fmaf(f, x.x, acc[4 * e4 + 0]);
+                    acc[4 * e4 + 1] = fmaf(f, x.y, acc[4 * e4 + 1]);
+                    acc[4 * e4 + 2] = fmaf(f, x.z, acc[4 * e4 + 2]);
+                    acc[4 * e4 + 3] = fmaf(f, x.w, acc[4 * e4 + 3]);
+                }
+                const float dz = dd[j * DVP + DV];   // -go_j / den_j
+                acc[DV] = fmaf(f, dz, acc[DV]);
+                const float dn = den[j];
+                const float dphi = dn != 0.f ? fmaf(zr, dz, ub[j * MP + r] / dn) : 0.f;
+                fq[j * MP + r] = KIND == FAVOR_KERNEL_SOFTMAX_POS ? dphi * f : (f > 0.f ? dphi : 0.f);
+            }
+            if (CAUSAL) {   // G^PS at the next tile start
+#pragma unroll 1
+                for (int i = 0; i < TT; ++i) {
+                    const float g = fk[i * MP + r];
+                    const float4* ci = reinterpret_cast<const float4*>(cs + i * DVP);
+#pragma unroll
+                    for (int e4 = 0; e4 < DV / 4; ++e4) {
+                        const float4 x = ci[e4];
+                        st[4 * e4 + 0] = fmaf(g, x.x, st[4 * e4 + 0]);
+                        st[4 * e4 + 1] = fmaf(g, x.y, st[4 * e4 + 1]);
+                        st[4 * e4 + 2] = fmaf(g, x.z, st[4 * e4 + 2]);
+                        st[4 * e4 + 3] = fmaf(g, x.w, st[4 * e4 + 3]);
+                    }
+                    st[DV] += g;
+                }
+            }
+        }
+        __syncthreads();
+        grad_inputs<T, KIND>(fq, xs, om, dq + row0 * d, t0, nt, TT, m, d, s);
+    }
+    if (own) {
+        float* o = part + ((size_t)bh * n_seg + seg) * m * W + (size_t)r * W;
+#pragma unroll
+        for (int e = 0; e < W; ++e) o[e] = acc[e];
+    }
+}
+
+// -------------------------------------------------------------- key pass
+// grid (n_seg, B*H), blockDim = m rounded up to 32.  Thread r < m owns row r of
+// H (the sum of phi~_q D^T over the queries after the current tile, or the
+// full sum when bidirectional).  Causal segments are walked backwards.
+template <typename T, int KIND, int DV, bool CAUSAL>
+__global__ void __launch_bounds__(256) k_bwd_key(const T* __restrict__ q, const T* __restrict__ k,
+                                                 const T* __restrict__ v, const T* __restrict__ dout,
+                                                 T* __restrict__ dk, T* __restrict__ dvv,
+                                                 const float* __restrict__ omega, const float* __restrict__ kshift,
+                                                 const float* __restrict__ hstate, const float4* __restrict__ rowstat,
+                                                 int H, int L, int m, int d, float s, int seg_len, int n_seg) {
+    using S = BwdShape<DV>;
+    constexpr int TT = S::TT, DVP = S::DVP, W = S::W;
+    extern __shared__ __align__(16) float sm[];
+    const BwdSmem P = bwd_smem(TT, DVP, W, m, d, CAUSAL, true);
+    float *xs = sm + P.xs, *ys = sm + P.ys, *cs = sm + P.cs, *dd = sm + P.dd, *fq = sm + P.fq, *fk = sm + P.fk;
+    float *aa = sm + P.aa, *mm = sm + P.mm, *rs = sm + P.rs, *cq = sm + P.cq, *den = sm + P.den, *go = sm + P.go,
+          *kn = sm + P.kn;
+    const int MP = m + 1;
+    const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int r = threadIdx.x;
+    const bool own = r < m;
+    const float* om = omega + (size_t)h * m * d;
+    const float kap = kshift[h];
+    const size_t row0 = (size_t)bh * L;
+
+    float hr[W];
+    {
+        const float* h0 = hstate + (CAUSAL ? ((size_t)bh * n_seg + seg) : (size_t)bh) * m * W + (size_t)r * W;
+#pragma unroll
+        for (int e = 0; e < W; ++e) hr[e] = own ? h0[e] : 0.f;
+    }
+    const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    if (j0 >= j1) return;
+    const int last = j0 + ((j1 - j0 - 1) / TT) * TT;
+    for (int t0 = CAUSAL ? last : j0; CAUSAL ? t0 >= j0 : t0 < j1; t0 += CAUSAL ? -TT : TT) {
+        const int nt = min(TT, j1 - t0);
+        __syncthreads();
+        stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
+        stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+        if (CAUSAL) {
+            stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
+            stage_rows(dout + row0 * DV, dd, t0, nt, TT, DV, DVP, -1.f);
+            for (int j = threadIdx.x; j < TT; j += blockDim.x) {
+                const float4 rsj = j < nt ? rowstat[row0 + t0 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                den[j] = rsj.x;
+                cq[j] = rsj.y;
+                go[j] = rsj.z;
+            }
+        }
+        if (own && (CAUSAL || t0 == j0)) {
+#pragma unroll
+            for (int e = 0; e < W; ++e) rs[r * W + e] = hr[e];
+        }
+        __syncthreads();
+        key_norms(ys, kn, TT, d);
+        if (own) {
+            project_tile<TT>(om, ys, fk, r, m, d, s);
+            if (CAUSAL) project_tile<TT>(om, xs, fq, r, m, d, s);
+        }
+        __syncthreads();
+        if (own) {
+#pragma unroll 4
+            for (int j = 0; j < TT; ++j) {
+                const float pk = fk[j * MP + r];
+                float g = 0.f;
+                if (j < nt)
+                    g = KIND == FAVOR_KERNEL_SOFTMAX_POS ? expf(pk - 0.5f * s * s * kn[j] - kap) : fmaxf(pk, 0.f);
+                fk[j * MP + r] = g;
+                if (CAUSAL) {
+                    const float pq = fq[j * MP + r];
+                    float f = 0.f;
+                    if (j < nt) f = KIND == FAVOR_KERNEL_SOFTMAX_POS ? expf(pq - cq[j]) : fmaxf(pq, 0.f);
+                    fq[j * MP + r] = f;
+                }
+            }
+        }
+        if (CAUSAL) make_d(dd, den, go, TT, DV, DVP);
+        __syncthreads();
+        if (CAUSAL) {   // aa[j][i] = phi~_q(i) . phi~_k(j), mm[j][i] = D_i . C_j, for i >= j
+            for (int idx = threadIdx.x; idx < TT * TT; idx += blockDim.x) {
+                const int j = idx / TT, i = idx - j * TT;
+                float a = 0.f, b = 0.f;
+                if (i >= j) {
+                    for (int rr = 0; rr < m; ++rr) a = fmaf(fq[i * MP + rr], fk[j * MP + rr], a);
+                    const float4* di = reinterpret_cast<const float4*>(dd + i * DVP);
+                    const float4* cj = reinterpret_cast<const float4*>(cs + j * DVP);
+#pragma unroll 4
+                    for (int e4 = 0; e4 < DVP / 4; ++e4) b += dot4(di[e4], cj[e4]);
+                }
+                aa[j * (TT + 1) + i] = a;
+                mm[j * (TT + 1) + i] = b;
+            }
+            __syncthreads();
+        }
+        // dv_j = H(tile end)^T phi~_k(j) + sum_{i>=j} aa[j][i] D_i
+        for (int idx = threadIdx.x; idx < TT * DV; idx += blockDim.x) {
+            const int j = idx / DV, e = idx - j * DV;
+            if (j >= nt) continue;
+            float a = 0.f;
+#pragma unroll 4
+            for (int rr = 0; rr < m; ++rr) a = fmaf(fk[j * MP + rr], rs[rr * W + e], a);
+            if (CAUSAL)
+                for (int i = j; i < TT; ++i) a = fmaf(aa[j * (TT + 1) + i], dd[i * DVP + e], a);
+            stb(dvv + (row0 + t0 + j) * DV + e, a);
+        }
+        __syncthreads();
+        if (own) {
+#pragma unroll 1
+            for (int j = 0; j < TT; ++j) {
+                const float g = fk[j * MP + r];
+                const float4* cj = reinterpret_cast<const float4*>(cs + j * DVP);
+                float dphi = 0.f;
+#pragma unroll
+                for (int e4 = 0; e4 < DV / 4; ++e4) {
+                    const float4 x = cj[e4];
+                    dphi = fmaf(hr[4 * e4 + 0], x.x, dphi);
+                    dphi = fmaf(hr[4 * e4 + 1], x.y, dphi);
+                    dphi = fmaf(hr[4 * e4 + 2], x.z, dphi);
+                    dphi = fmaf(hr[4 * e4 + 3], x.w, dphi);
+                }
+                dphi += j < nt ? hr[DV] : 0.f;
+                if (CAUSAL)
+                    for (int i = j; i < TT; ++i) dphi = fmaf(fq[i * MP + r], mm[j * (TT + 1) + i], dphi);
+                fk[j * MP + r] = KIND == FAVOR_KERNEL_SOFTMAX_POS ? dphi * g : (g > 0.f ? dphi : 0.f);
+            }
+            if (CAUSAL) {   // H at the previous tile's end
+#pragma unroll 1
+                for (int i = 0; i < TT; ++i) {
+                    const float f = fq[i * MP + r];
+                    const float4* di = reinterpret_cast<const float4*>(dd + i * DVP);
+#pragma unroll
+                    for (int e4 = 0; e4 < DV / 4; ++e4) {
+                        const float4 x = di[e4];
+                        hr[4 * e4 + 0] = fmaf(f, x.x, hr[4 * e4 + 0]);
+                        hr[4 * e4 + 1] = fmaf(f, x.y, hr[4 * e4 + 1]);
+                        hr[4 * e4 + 2] = fmaf(f, x.z, hr[4 * e4 + 2]);
+                        hr[4 * e4 + 3] = fmaf(f, x.w, hr[4 * e4 + 3]);
+                    }
+                    hr[DV] = fmaf(f, dd[i * DVP + DV], hr[DV]);
+                }
+            }
+        }
+        __syncthreads();
+        grad_inputs<T, KIND>(fk, ys, om, dk + row0 * d, t0, nt, TT, m, d, s);
+    }
+}
+
+// ------------------------------------------------------- segment combines
+// out[bh] = sum over segments (in order) of part[bh, seg].
+__global__ void k_bwd_reduce(const float* __restrict__ part, float* __restrict__ out, int n_seg, int n) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float* p = part + (size_t)bh * n_seg * n + i;
+    float a = 0.f;
+    for (int sg = 0; sg < n_seg; ++sg) a += p[(size_t)sg * n];
+    out[(size_t)bh * n + i] = a;
+}
+
+// part[bh, seg] <- sum of part[bh, seg+1 .. n_seg-1] (exclusive suffix, from the last segment back).
+__global__ void k_bwd_rscan(float* __restrict__ part, int n_seg, int n) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float* p = part + (size_t)bh * n_seg * n + i;
+    float run = 0.f;
+    for (int sg = n_seg - 1; sg >= 0; --sg) {
+        const float t = p[(size_t)sg * n];
+        p[(size_t)sg * n] = run;
+        run += t;
+    }
+}
+
+template <typename K>
+favor_status set_smem_bytes(K kern, size_t bytes) {
+    if (bytes > 227 * 1024) return set_error(FAVOR_ERR_UNSUPPORTED, "backward: %zu bytes of shared memory", bytes);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(FAVOR_ERR_CUDA, "backward: cannot set %zu bytes of shared memory", bytes);
+    }
+    return FAVOR_OK;
+}
+
+struct BwdCall {
+    const void *q, *k, *v, *dout;
+    void *dq, *dk, *dv;
+};
+
+template <typename T, int KIND, int DV, bool CAUSAL>
+favor_status bwd_passes(const Handle& h, const BwdCall& c, int BH, int L, const SegPlan& p, cudaStream_t st) {
+    using S = BwdShape<DV>;
+    const int threads = (h.m + 31) / 32 * 32;
+    const int n = h.m * (DV + 1);
+    const dim3 grid(p.n_seg, BH), cgrid((n + 255) / 256, BH);
+    const int seg_len = p.seg_tiles * 128;
+    float* qsum = CAUSAL ? h.ws_partial2 : h.ws_partial;     // per-segment sums of phi~_q D^T
+    float4* rowstat = reinterpret_cast<float4*>(h.ws_rowstat);
+    {
+        const BwdSmem P = bwd_smem(S::TT, S::DVP, S::W, h.m, h.d, CAUSAL, false);
+        auto kern = k_bwd_query<T, KIND, DV, CAUSAL>;
+        favor_status e = set_smem_bytes(kern, P.total * sizeof(float));
+        if (e != FAVOR_OK) return e;
+        ProfScope ps(h, PROF_BWD_QUERY, st);
+        kern<<<grid, threads, P.total * sizeof(float), st>>>(
+            (const T*)c.q, (const T*)c.k, (const T*)c.v, (const T*)c.dout, (T*)c.dq, h.omega_f32,
+            h.kshift, CAUSAL ? h.ws_partial : h.ws_state, qsum, rowstat, h.H, L, h.m, h.d, h.s, seg_len, p.n_seg);
+        count_launch();
+        e = check_launch("backward query kernel");
+        if (e != FAVOR_OK) return e;
+    }
+    {
+        ProfScope ps(h, PROF_COMBINE, st);
+        if (CAUSAL) k_bwd_rscan<<<cgrid, 256, 0, st>>>(qsum, p.n_seg, n);
+        else k_bwd_reduce<<<cgrid, 256, 0, st>>>(qsum, h.ws_dstate, p.n_seg, n);
+        count_launch();
+        favor_status e = check_launch("backward combine kernel");
+        if (e != FAVOR_OK) return e;
+    }
+    const BwdSmem P = bwd_smem(S::TT, S::DVP, S::W, h.m, h.d, CAUSAL, true);
+    auto kern = k_bwd_key<T, KIND, DV, CAUSAL>;
+    favor_status e = set_smem_bytes(kern, P.total * sizeof(float));
+    if (e != FAVOR_OK) return e;
+    ProfScope ps(h, PROF_BWD_KEY, st);
+    kern<<<grid, threads, P.total * sizeof(float), st>>>(
+        (const T*)c.q, (const T*)c.k, (const T*)c.v, (const T*)c.dout, (T*)c.dk, (T*)c.dv,
+        h.omega_f32, h.kshift, CAUSAL ? h.ws_partial2 : h.ws_dstate, rowstat, h.H, L, h.m, h.d, h.s, seg_len,
+        p.n_seg);
+    count_launch();
+    return check_launch("backward key kernel");
+}
+
+template <bool CAUSAL>
+favor_status bwd_dispatch(const Handle& h, const BwdCall& c, int BH, int L, const SegPlan& p, cudaStream_t st) {
+#define FAVOR_BWD_DV(T, KIND)                                                  \
+    switch (h.dv) {                                                            \
+        case 16: return bwd_passes<T, KIND, 16, CAUSAL>(h, c, BH, L, p, st);   \
+        case 32: return bwd_passes<T, KIND, 32, CAUSAL>(h, c, BH, L, p, st);   \
+        case 64: return bwd_passes<T, KIND, 64, CAUSAL>(h, c, BH, L, p, st);   \
+        case 128: return bwd_passes<T, KIND, 128, CAUSAL>(h, c, BH, L, p, st); \
+    }
+    if (h.dtype == FAVOR_DTYPE_F32) {
+        if (h.kind == FAVOR_KERNEL_SOFTMAX_POS) { FAVOR_BWD_DV(float, FAVOR_KERNEL_SOFTMAX_POS) }
+        else { FAVOR_BWD_DV(float, FAVOR_KERNEL_RELU) }
+    } else {
+        if (h.kind == FAVOR_KERNEL_SOFTMAX_POS) { FAVOR_BWD_DV(__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS) }
+        else { FAVOR_BWD_DV(__nv_bfloat16, FAVOR_KERNEL_RELU) }
+    }
+#undef FAVOR_BWD_DV
+    return set_error(FAVOR_ERR_UNSUPPORTED, "backward: unsupported dv=%d", h.dv);
+}
+
+}  // namespace
+
+favor_status simt_bidir_backward(const Handle& h, const void* q, const void* k, const void* v,
+                                 const void* dout, void* dq, void* dk, void* dv, int B, int L, cudaStream_t st) {
+    const int BH = B * h.H;
+    const SegPlan p = plan_segments(BH, L, h.num_sms);
+    favor_status s = simt_state_partials(h, k, v, BH, L, p, st);   // S~ | z~ per segment
+    if (s != FAVOR_OK) return s;
+    s = launch_reduce_segments(h, BH, p.n_seg, st);                // -> h.ws_state
+    if (s != FAVOR_OK) return s;
+    const BwdCall c{q, k, v, dout, dq, dk, dv};
+    return bwd_dispatch<false>(h, c, BH, L, p, st);
+}
+
+favor_status simt_causal_backward(const Handle& h, const void* q, const void* k, const void* v,
+                                  const void* dout, void* dq, void* dk, void* dv, int B, int L, cudaStream_t st) {
+    const int BH = B * h.H;
+    const SegPlan p = plan_segments(BH, L, h.num_sms);
+    favor_status s = FAVOR_OK;
+    if (p.n_seg > 1) {   // exclusive prefix states of the segments
+        s = simt_state_partials(h, k, v, BH, L, p, st);
+        if (s != FAVOR_OK) return s;
+        s = launch_scan_segments(h, BH, p.n_seg, st);
+    } else if (cudaMemsetAsync(h.ws_partial, 0, (size_t)BH * h.m * (h.dv + 1) * sizeof(float), st) != cudaSuccess) {
+        cudaGetLastError();
+        s = set_error(FAVOR_ERR_CUDA, "backward: cudaMemsetAsync failed");
+    }
+    if (s != FAVOR_OK) return s;
+    const BwdCall c{q, k, v, dout, dq, dk, dv};
+    return bwd_dispatch<true>(h, c, BH, L, p, st);
+}
+
+}  // namespace favor

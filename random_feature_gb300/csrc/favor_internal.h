@@ -18,6 +18,8 @@ enum ProfSlot {
     PROF_COMBINE,       // fixed-order reduce / exclusive scan of segment states
     PROF_READOUT,       // bidirectional query readout
     PROF_CAUSAL,        // causal chunked attention
+    PROF_BWD_QUERY,     // backward: query-side pass (dq, per-segment phi_q D^T sums)
+    PROF_BWD_KEY,       // backward: key-side pass (dk, dv)
     PROF_NSLOTS
 };
 
@@ -55,6 +57,9 @@ struct Handle {
                               // row-major [m][dv+1] on the CUDA-core path, column-major [dv+1][m]
                               // on the tensor-core path (coalesced by feature)
     float* ws_state;          // [max_B*H][m][dv+1] reduced bidirectional states
+    float* ws_partial2;       // like ws_partial (row-major): backward per-segment sums of phi~_q D^T
+    float* ws_dstate;         // [max_B*H][m][dv+1] backward: reduced sum of phi~_q D^T (bidirectional)
+    float* ws_rowstat;        // [max_B*H*max_L][4] backward (causal): per query (den~, row shift, dO . out, 0)
     size_t ws_partial_rows;   // capacity of ws_partial in (head, segment) rows
     void* ws_tc;              // tensor-core path scratch (bf16 operand copies), may be null
     size_t ws_tc_bytes;
@@ -97,6 +102,16 @@ favor_status simt_bidir(const Handle& h, const void* q, const void* k, const voi
                         int B, int L, cudaStream_t st);
 favor_status simt_causal(const Handle& h, const void* q, const void* k, const void* v, void* out,
                          int B, int L, cudaStream_t st);
+
+// Per-segment key/value states of the CUDA-core path into h.ws_partial (row-major).
+favor_status simt_state_partials(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan& p,
+                                 cudaStream_t st);
+
+// ---- backward (gradients of the bidirectional / causal call), CUDA cores ----
+favor_status simt_bidir_backward(const Handle& h, const void* q, const void* k, const void* v, const void* dout,
+                                 void* dq, void* dk, void* dv, int B, int L, cudaStream_t st);
+favor_status simt_causal_backward(const Handle& h, const void* q, const void* k, const void* v, const void* dout,
+                                  void* dq, void* dk, void* dv, int B, int L, cudaStream_t st);
 
 // ---- stateful calls: public state [B*H][m][dv+1] fp32 (S | z), see favor.h ----
 favor_status simt_kv_state(const Handle& h, const void* k, const void* v, float* state, int B, int L,

@@ -609,6 +609,11 @@ favor_status causal_step_t(const Handle& h, const void* q, const void* k, const 
 
 }  // namespace
 
+favor_status simt_state_partials(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan& p,
+                                 cudaStream_t st) {
+    return dispatch3<StateF>(h, k, v, BH, L, &p, st);
+}
+
 favor_status simt_kv_state(const Handle& h, const void* k, const void* v, float* state, int B, int L,
                            cudaStream_t st) {
     const int BH = B * h.H;

@@ -24,6 +24,7 @@ __all__ = [
     "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
     "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc",
     "favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
+    "favor_attn_bidir_backward", "favor_attn_causal_backward",
 ]
 
 FAVOR_OK, FAVOR_ERR_INVALID_ARG, FAVOR_ERR_UNSUPPORTED, FAVOR_ERR_NOMEM, FAVOR_ERR_CUDA = range(5)
@@ -36,7 +37,8 @@ EXPORTED_SYMBOLS = ("favor_create", "favor_feature_map", "favor_attn_bidir", "fa
                     "favor_destroy", "favor_status_str", "favor_last_error", "favor_launch_count",
                     "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
                     "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc",
-                    "favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step")
+                    "favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
+                    "favor_attn_bidir_backward", "favor_attn_causal_backward")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -96,7 +98,10 @@ def lib() -> ctypes.CDLL:
         L.favor_kv_state.argtypes = [vp, vp, vp, vp, i, i, vp]
         L.favor_attn_from_state.argtypes = [vp, vp, vp, vp, i, i, vp]
         L.favor_attn_causal_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, vp]
-        for fn in ("favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step"):
+        for fn in ("favor_attn_bidir_backward", "favor_attn_causal_backward"):
+            getattr(L, fn).argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp]
+        for fn in ("favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
+                   "favor_attn_bidir_backward", "favor_attn_causal_backward"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -191,6 +196,16 @@ def favor_attn_causal_step(h, q, k, v, out, state, B, T, stream=None) -> None:
                                         _stream(stream, q)), "favor_attn_causal_step")
 
 
+def favor_attn_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, stream=None) -> None:
+    _check(lib().favor_attn_bidir_backward(h, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                           int(B), int(L), _stream(stream, q)), "favor_attn_bidir_backward")
+
+
+def favor_attn_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, stream=None) -> None:
+    _check(lib().favor_attn_causal_backward(h, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                            int(B), int(L), _stream(stream, q)), "favor_attn_causal_backward")
+
+
 def favor_destroy(h) -> None:
     _check(lib().favor_destroy(h), "favor_destroy")
 
@@ -267,6 +282,23 @@ class Favor:
         out = self._new(q, B, L, self.dv, out)
         (favor_attn_causal if causal else favor_attn_bidir)(self.handle, q, k, v, out, B, L, stream)
         return out
+
+    def attn_backward(self, q, k, v, dout, causal=False, grads=None, stream=None):
+        """(dq, dk, dv) of attn(q, k, v, causal) for the upstream gradient dout.
+        ``grads`` may give the three output tensors."""
+        B, _, L, _ = q.shape
+        for t, w, name in ((q, self.d, "q"), (k, self.d, "k"), (v, self.dv, "v"), (dout, self.dv, "dout")):
+            self._chk(t, B, L, w, name)
+        if grads is None:
+            grads = (self._new(q, B, L, self.d, None), self._new(q, B, L, self.d, None),
+                     self._new(q, B, L, self.dv, None))
+        dq, dk, dv = grads
+        self._chk(dq, B, L, self.d, "dq")
+        self._chk(dk, B, L, self.d, "dk")
+        self._chk(dv, B, L, self.dv, "dv")
+        fn = favor_attn_causal_backward if causal else favor_attn_bidir_backward
+        fn(self.handle, q, k, v, dout, dq, dk, dv, B, L, stream)
+        return dq, dk, dv
 
     def new_state(self, B):
         """A zero (empty) state [B, H, m, dv+1] float32 on the current CUDA device."""

@@ -1,0 +1,132 @@
+"""GPU parity of the backward calls (dq, dk, dv of the bidirectional and causal
+attention) against the float64 oracle's exact derivative.
+
+Error measure for a gradient tensor: per (b, h) slice, max over rows i of
+max_c |g_ic - o_ic| / max(max_c |o_ic|, 1e-3 * max |o| over the slice).  The
+slice floor covers rows whose gradient vanishes by structure (causal query 0:
+out_0 = v_0 whatever q_0, so dq_0 = 0 exactly and the device returns rounding
+noise there).
+
+Tolerances: bf16 2e-2 as for the forward.  fp32 1e-3, ten times the forward's:
+the step dphi_r = (u_r - z_r (dO . out)) / den subtracts two nearly equal
+terms (their difference is sum_j phi_j[r] (v_j - out) . dO); over the shapes
+below its condition number reaches 3.2e3 (d = 128, positive features), so
+fp32 rounding alone gives up to 2^-24 * 3.2e3 = 1.9e-4, and 1e-3 leaves a 5x
+margin.  Every other step of dq, dk, dv has condition below 10.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import random_feature_gb300 as R
+from synth import CONFIGS, make_upstream_grad, make_workload
+
+from _util import to_dev, to_host
+
+TOL_GRAD = {"f32": 1e-3, "bf16": 2e-2}
+
+SHAPES = [
+    # (name, base config, overrides): the tensor-core forward shape, CUDA-core
+    # shapes with m not a multiple of 32, dv = 128 (16-token tiles), fp32
+    ("d64_m256_bf16", "bidir_bf16", dict(B=2, H=2)),
+    ("d32_m48_bf16", "bidir_bf16", dict(B=1, H=3, d=32, dv=16, m=48)),
+    ("d16_m64_f32", "approx_f32", dict(B=2, H=2, m=64, dv=32)),
+    ("d128_dv128_f32", "approx_f32", dict(B=1, H=2, d=128, dv=128, m=256)),
+]
+
+
+def grad_err(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    B, H = ref.shape[:2]
+    worst = 0.0
+    for b in range(B):
+        for h in range(H):
+            g, o = got[b, h], ref[b, h]
+            floor = 1e-3 * np.max(np.abs(o))
+            scale = np.maximum(np.max(np.abs(o), axis=1), floor)
+            scale = np.where(scale > 0, scale, 1.0)
+            worst = max(worst, float(np.max(np.abs(g - o).max(axis=1) / scale)))
+    return worst
+
+
+def _run(shape, kind, causal, L, seed):
+    _, base, over = shape
+    w = CONFIGS[base].replace(L=L, **over)
+    omega, q, k, v = make_workload(w, seed)
+    g = make_upstream_grad(w, seed)
+    bwd = O.favor_causal_backward if causal else O.favor_bidir_backward
+    ref = bwd(q, k, v, g, omega, w.data_scale, kind)
+    with R.Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, omega, w.data_scale, w.B, w.L) as f:
+        dev = [to_dev(a, w.dtype) for a in (q, k, v, g)]
+        got = f.attn_backward(*dev, causal=causal)
+        got = [to_host(t) for t in got]
+        assert R.favor_device_error(f.handle) == 0
+    return w, got, ref
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
+@pytest.mark.parametrize("kind", O.KINDS)
+@pytest.mark.parametrize("causal", [False, True], ids=["bidir", "causal"])
+def test_backward_matches_oracle(shape, kind, causal):
+    # 1100 tokens: several 128-token segments per head and a ragged last tile
+    L = 1100 if shape[0] != "d128_dv128_f32" else 333
+    w, got, ref = _run(shape, kind, causal, L, 31)
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        e = grad_err(a, b)
+        assert e <= TOL_GRAD[w.dtype], (name, e)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("L", [2, 31, 33])
+def test_backward_short_sequences(L):
+    shape = SHAPES[0]
+    for causal in (False, True):
+        w, got, ref = _run(shape, "softmax_pos", causal, L, 32 + L)
+        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+            assert grad_err(a, b) <= TOL_GRAD[w.dtype], (name, causal, L)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True], ids=["bidir", "causal"])
+def test_backward_single_token_is_identity_on_v(causal):
+    """L = 1: out = v whatever q and k, so dv = dO and dq = dk = 0 (the device
+    returns rounding noise for the zero gradients)."""
+    w, got, ref = _run(SHAPES[2], "softmax_pos", causal, 1, 40)
+    np.testing.assert_allclose(got[2], ref[2], rtol=1e-6, atol=1e-6)
+    assert np.max(np.abs(got[0])) < 1e-5 and np.max(np.abs(got[1])) < 1e-5
+
+
+@pytest.mark.gpu
+def test_backward_is_deterministic():
+    shape = SHAPES[0]
+    _, base, over = shape
+    w = CONFIGS[base].replace(L=900, **over)
+    omega, q, k, v = make_workload(w, 41)
+    g = make_upstream_grad(w, 41)
+    with R.Favor(w.H, w.m, w.d, w.dv, "softmax_pos", w.dtype, omega, w.data_scale, w.B, w.L) as f:
+        dev = [to_dev(a, w.dtype) for a in (q, k, v, g)]
+        a = [t.clone() for t in f.attn_backward(*dev, causal=True)]
+        b = f.attn_backward(*dev, causal=True)
+        for x, y in zip(a, b):
+            assert bool((x == y).all())
+
+
+@pytest.mark.gpu
+def test_backward_argument_checks():
+    shape = SHAPES[0]
+    _, base, over = shape
+    w = CONFIGS[base].replace(L=64, **over)
+    omega, q, k, v = make_workload(w, 42)
+    with R.Favor(w.H, w.m, w.d, w.dv, "softmax_pos", w.dtype, omega, w.data_scale, w.B, w.L) as f:
+        dev = [to_dev(a, w.dtype) for a in (q, k, v, v)]
+        dq, dk, dv = (to_dev(np.zeros_like(a), w.dtype) for a in (q, k, v))
+        n0 = R.favor_launch_count()
+        with pytest.raises(R.FavorError) as ei:
+            R.favor_attn_bidir_backward(f.handle, *dev[:3], 0, dq, dk, dv, w.B, w.L)
+        assert ei.value.status == R.FAVOR_ERR_INVALID_ARG
+        with pytest.raises(R.FavorError) as ei:
+            R.favor_attn_causal_backward(f.handle, *dev, dq, dk, dv, w.B, w.L + 1)
+        assert ei.value.status == R.FAVOR_ERR_INVALID_ARG
+        assert R.favor_launch_count() == n0
