@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--decode-steps", type=int, default=200,
                     help="one-token causal steps timed for the decode line (0 = skip)")
+    ap.add_argument("--backward-steps", type=int, default=2,
+                    help="timed repetitions of the backward line (bidir + causal gradients; 0 = skip)")
     ap.add_argument("--e2e-groups", type=int, default=4,
                     help="head groups pipelined over upload / compute / download streams in the e2e leg")
     ap.add_argument("--cpu-heads", type=int, default=2, help="heads of the workload in the CPU oracle sample")
@@ -153,6 +155,16 @@ def per_token_head(w, slot, kind):
     if slot == "feature_map":
         return d * b + m * b, 2 * m * d, e
     return 0, 0, 0
+
+
+def backward_flops_per_token_head(w):
+    """Algorithmic flops of one backward call per token*head: the recomputed
+    features (2md each for q and k), the forward state (2m(dv+1)), and the
+    gradient contractions u = S dO (2m dv), sum phi_q D^T (2m(dv+1)),
+    dq = G Omega (2md), dphi_k = H [v 1] (2m(dv+1)), dv = H^T phi_k (2m dv),
+    dk = G_k Omega (2md)."""
+    d, dv, m = w.d, w.dv, w.m
+    return 8 * m * d + 6 * m * (dv + 1) + 4 * m * dv
 
 
 def source_digest():
@@ -320,6 +332,53 @@ def run_ours(args):
                   "state_bytes_read_written": nbytes, "state_gbs": nbytes / (us * 1e-6) / 1e9,
                   "config": f"B={w.B} H={w.H} m={w.m} d={w.d} dv={w.dv}, one token per step, positive features"}
 
+    # Backward (gradients of the bidirectional and causal calls, positive
+    # features) on the same workload: CUDA-core kernels, so the roofline is
+    # the FP32 FFMA peak of the SMs at the sampled clock.
+    backward = None
+    if args.backward_steps > 0:
+        hd_ = handles["softmax_pos"]
+        gd = torch.randn((w.B, w.H, w.L, w.dv), device=dev, dtype=torch.float32).to(tdt)
+        grads = tuple(torch.empty_like(t) for t in (qd, kd, vd))
+        R.favor_profile_reset(hd_.handle)
+        for causal in (False, True):
+            hd_.attn_backward(qd, kd, vd, gd, causal=causal, grads=grads, stream=stream)
+        torch.cuda.synchronize(dev)
+        R.favor_profile_reset(hd_.handle)
+        R.favor_profile_enable(hd_.handle, True)
+        per = {}
+        for causal in (False, True):
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(args.backward_steps):
+                hd_.attn_backward(qd, kd, vd, gd, causal=causal, grads=grads, stream=stream)
+            b1.record(stream)
+            torch.cuda.synchronize(dev)
+            per["causal" if causal else "bidir"] = b0.elapsed_time(b1) / args.backward_steps
+        R.favor_profile_enable(hd_.handle, False)
+        bk = {}
+        for sl in range(R.favor_profile_slots()):
+            ms, n = R.favor_profile_read(hd_.handle, sl)
+            if n:
+                bk[R.favor_profile_name(sl)] = {"ms_total": ms, "launches": n}
+        tot = sum(x["ms_total"] for x in bk.values())
+        for x in bk.values():
+            x["share"] = x["ms_total"] / max(tot, 1e-12)
+        T = w.B * w.H * w.L
+        ms_pair = per["bidir"] + per["causal"]
+        flops = 2 * T * backward_flops_per_token_head(w)
+        bw_mhz = sampler.samples[-1][1] if sampler.samples else peaks["sm_max_mhz"]
+        fp32_peak = GB300_SMS * 128 * 2 * bw_mhz * 1e6
+        backward = {"value": 2 * T / (ms_pair / 1e3), "unit": UNIT, "ms_per_call": per,
+                    "flops_per_token_head": backward_flops_per_token_head(w),
+                    "roofline": {"bound": "alu", "achieved": flops / (ms_pair / 1e3) / 1e12,
+                                 "peak": fp32_peak / 1e12, "unit": "TFLOP/s",
+                                 "frac": flops / (ms_pair / 1e3) / fp32_peak,
+                                 "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 flops x SM clock"},
+                    "kernels": bk,
+                    "config": f"{w.name}: B={w.B} H={w.H} L={w.L}, dq/dk/dv of one bidirectional and one "
+                              f"causal call, positive features, dO ~ N(0,1)"}
+
     # End to end through the public API: pinned host inputs in, outputs back, every
     # step.  The heads are split into groups, one library handle per group (its
     # slice of omega), and three streams overlap the upload of group g+1, the four
@@ -443,7 +502,8 @@ def run_ours(args):
                                    f"calls per step: bidir+causal x softmax_pos+relu",
                        "global_batch": w.B * world, "seq_len": w.L, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (Q,K,V 384 MB per replica)"},
-            "clocks": clocks, "e2e": e2e, "decode": decode, "gpu_launches": launches, "roofline": roofline,
+            "clocks": clocks, "e2e": e2e, "decode": decode, "backward": backward, "gpu_launches": launches,
+            "roofline": roofline,
             "roofline_all": roofline_all, "kernels": kernels, "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
     for hd in handles.values():
