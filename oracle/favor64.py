@@ -42,9 +42,13 @@ __all__ = [
     "softmax_attention", "row_rel_err", "KINDS",
     "feature_map_vjp", "attn_from_features_bidir_vjp", "attn_from_features_causal_vjp",
     "favor_bidir_backward", "favor_causal_backward",
+    "feature_map_hyperbolic", "feature_map_trig", "VARIANT_KINDS", "n_features",
 ]
 
 KINDS = ("softmax_pos", "relu")
+# Feature maps with l = 2 functions per projection row (Eq. 5): omega has M rows
+# and the map has 2M features.
+VARIANT_KINDS = ("softmax_hyp", "softmax_trig")
 
 
 def _f64(a):
@@ -79,11 +83,48 @@ def feature_map_relu(x, omega):
     return np.maximum(x @ omega.T, 0.0) / np.sqrt(m)
 
 
+def feature_map_hyperbolic(x, omega):
+    """Hyperbolic positive features SM^hyp+ ([P] Lemma 1, second form): Eq. 5 with
+    h(x) = 2^-1/2 exp(-||x||^2/2), l = 2, f1(u) = exp(u), f2(u) = exp(-u):
+        phi(x) = M^-1/2 h(x) (exp(omega_1.x), ..., exp(omega_M.x), exp(-omega_1.x), ..., exp(-omega_M.x))
+    for the M rows of omega: 2M features.
+    """
+    x = _f64(x)
+    omega = _f64(omega)
+    M = omega.shape[0]
+    proj = x @ omega.T
+    sq = 0.5 * np.sum(x * x, axis=-1, keepdims=True)
+    return np.concatenate([np.exp(proj - sq), np.exp(-proj - sq)], axis=-1) / np.sqrt(2.0 * M)
+
+
+def feature_map_trig(x, omega):
+    """Trigonometric features SM^trig ([P] §2.3 after Eq. 6): Eq. 5 with
+    h(x) = exp(||x||^2/2), l = 2, f1 = sin, f2 = cos:
+        phi(x) = M^-1/2 exp(||x||^2/2) (sin(omega_1.x), ..., sin(omega_M.x), cos(omega_1.x), ..., cos(omega_M.x))
+    for the M rows of omega: 2M features, of either sign.
+    """
+    x = _f64(x)
+    omega = _f64(omega)
+    M = omega.shape[0]
+    proj = x @ omega.T
+    h = np.exp(0.5 * np.sum(x * x, axis=-1, keepdims=True))
+    return h * np.concatenate([np.sin(proj), np.cos(proj)], axis=-1) / np.sqrt(M)
+
+
+def n_features(kind, omega_rows):
+    """Number of features of the map for ``omega_rows`` projection rows."""
+    return 2 * omega_rows if kind in VARIANT_KINDS else omega_rows
+
+
 def feature_map(x, omega, kind):
     if kind == "softmax_pos":
         return feature_map_positive(x, omega)
     if kind == "relu":
         return feature_map_relu(x, omega)
+    if kind == "softmax_hyp":
+        return feature_map_hyperbolic(x, omega)
+    if kind == "softmax_trig":
+        return feature_map_trig(x, omega)
     raise ValueError(f"unknown feature kind {kind!r}")
 
 
@@ -200,7 +241,7 @@ def favor_feature_map(x, omega, data_scale, kind="softmax_pos"):
     x = _f64(x)
     omega = _f64(omega)
     B, H, L, _ = x.shape
-    out = np.empty((B, H, L, omega.shape[1]))
+    out = np.empty((B, H, L, n_features(kind, omega.shape[1])))
     for h in range(H):
         out[:, h] = feature_map(data_scale * x[:, h], omega[h], kind)
     return out
@@ -212,7 +253,7 @@ def favor_kv_state(k, v, omega, data_scale, kind="softmax_pos"):
     and column dv holds z = sum_j phi(k_j) ([EX] §2).  -> [B,H,m,dv+1]."""
     k, v, omega = _f64(k), _f64(v), _f64(omega)
     B, H, L, _ = k.shape
-    m, dv = omega.shape[1], v.shape[-1]
+    m, dv = n_features(kind, omega.shape[1]), v.shape[-1]
     out = np.empty((B, H, m, dv + 1))
     for b in range(B):
         for h in range(H):
@@ -284,7 +325,12 @@ def feature_map_vjp(x, omega, kind, dphi):
     if kind == "relu":
         mask = (x @ omega.T) > 0.0
         return (np.where(mask, dphi, 0.0) @ omega) / np.sqrt(omega.shape[0])
-    raise ValueError(f"unknown feature kind {kind!r}")
+    if kind == "softmax_hyp":
+        # phi_r = (2M)^-1/2 exp(+-omega_r . x - ||x||^2/2): d phi_r / d x = phi_r (+-omega_r - x)
+        g = dphi * feature_map_hyperbolic(x, omega)
+        M = omega.shape[0]
+        return g[:, :M] @ omega - g[:, M:] @ omega - x * g.sum(axis=1, keepdims=True)
+    raise ValueError(f"no derivative for feature kind {kind!r}")
 
 
 def _dbuf2(buf2, dout):

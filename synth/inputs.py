@@ -15,6 +15,9 @@ Projection matrix omega (per head, shape [m, d]):
     have independent lengths).  m > d stacks ceil(m/d) independent blocks; a
     partial last block keeps its first rows.
   * iid: every entry N(0, 1) (§2.3, Eq. 5 with D = N(0, I_d)).
+  * regularized (SMREG, §2.3 after Lemma 1): omega replaced by
+    sqrt(d) omega / ||omega||, i.e. D = Unif(sqrt(d) S^{d-1}); with orthogonal
+    blocks the rows keep their orthogonality and all have length sqrt(d).
 
 Random stream order for one workload: a single numpy Generator(PCG64(seed))
 draws omega for heads h = 0..H-1 in order, then Q, K, V, then (if asked)
@@ -45,8 +48,8 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32)
 
 
-def make_omega_orf(rng: np.random.Generator, m: int, d: int) -> np.ndarray:
-    """Orthogonal Gaussian projection rows [m, d] (float64)."""
+def make_omega_orf(rng: np.random.Generator, m: int, d: int, regularized: bool = False) -> np.ndarray:
+    """Orthogonal Gaussian projection rows [m, d] (float64); lengths sqrt(d) if regularized."""
     nblocks = -(-m // d)
     rows = []
     for _ in range(nblocks):
@@ -55,13 +58,18 @@ def make_omega_orf(rng: np.random.Generator, m: int, d: int) -> np.ndarray:
         qmat = qmat * np.sign(np.diag(rmat))[None, :]
         block = qmat.T                      # rows are orthonormal
         lengths = np.linalg.norm(rng.standard_normal((d, d)), axis=1)
+        if regularized:
+            lengths = np.full(d, np.sqrt(d))
         rows.append(block * lengths[:, None])
     return np.concatenate(rows, axis=0)[:m]
 
 
-def make_omega_iid(rng: np.random.Generator, m: int, d: int) -> np.ndarray:
-    """Independent N(0, 1) projection rows [m, d] (float64)."""
-    return rng.standard_normal((m, d))
+def make_omega_iid(rng: np.random.Generator, m: int, d: int, regularized: bool = False) -> np.ndarray:
+    """Independent N(0, 1) projection rows [m, d] (float64); rescaled to length sqrt(d) if regularized."""
+    w = rng.standard_normal((m, d))
+    if regularized:
+        w = w * (np.sqrt(d) / np.linalg.norm(w, axis=1, keepdims=True))
+    return w
 
 
 def make_qkv(rng: np.random.Generator, B: int, H: int, L: int, d: int, dv: int,
@@ -103,6 +111,7 @@ class Workload:
     input_scale: float         # Q, K, V multiplied by this at generation
     data_scale: float          # s passed to the library: x = s*q, y = s*k
     ortho: bool = True
+    regularized: bool = False      # SMREG projection rows (length sqrt(d))
     sharp_frac: float = 0.0
     sharp_mult: float = 1.0
     modes: tuple = ("bidir",)
@@ -141,7 +150,7 @@ def make_workload(w: Workload, seed: int = 0):
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     make = make_omega_orf if w.ortho else make_omega_iid
-    omega = np.stack([make(rng, w.m, w.d) for _ in range(w.H)]).astype(np.float32)
+    omega = np.stack([make(rng, w.m, w.d, w.regularized) for _ in range(w.H)]).astype(np.float32)
     q, k, v = make_qkv(rng, w.B, w.H, w.L, w.d, w.dv, w.std, w.sharp_frac, w.sharp_mult)
     if w.input_scale != 1.0:
         sc = np.float32(w.input_scale)

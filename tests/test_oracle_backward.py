@@ -28,7 +28,7 @@ BWD = {"bidir": O.favor_bidir_backward, "causal": O.favor_causal_backward}
 
 
 @pytest.mark.parametrize("mode", ["bidir", "causal"])
-@pytest.mark.parametrize("kind", O.KINDS)
+@pytest.mark.parametrize("kind", O.KINDS + ("softmax_hyp",))
 def test_gradients_match_central_differences(mode, kind):
     """<grad, u> equals (f(x + h u) - f(x - h u)) / 2h for the loss <dO, out>,
     along random directions u of q, k and v (every element perturbed)."""
