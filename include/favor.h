@@ -49,10 +49,16 @@ typedef enum {
     FAVOR_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
 } favor_status;
 
-/* Feature map f in Eq. 5 of Rethinking Attention with Performers. */
+/* Feature map f in Eq. 5 of Rethinking Attention with Performers.  The last
+ * two have l = 2 functions per projection row: omega has m/2 rows and the map
+ * has m features. */
 typedef enum {
     FAVOR_KERNEL_SOFTMAX_POS = 0,  /* positive random features for the softmax kernel (Lemma 1) */
-    FAVOR_KERNEL_RELU = 1          /* generalized attention with f = ReLU (§4.4, App. A.4) */
+    FAVOR_KERNEL_RELU = 1,         /* generalized attention with f = ReLU (§4.4, App. A.4) */
+    FAVOR_KERNEL_SOFTMAX_HYP = 2,  /* hyperbolic positive features SM^hyp+ (Lemma 1, second form):
+                                      (2M)^-1/2 exp(-||x||^2/2) (exp(omega x), exp(-omega x)), M = m/2 */
+    FAVOR_KERNEL_SOFTMAX_TRIG = 3  /* trigonometric features SM^trig (§2.3): M^-1/2 exp(||x||^2/2)
+                                      (sin(omega x), cos(omega x)), M = m/2; features of either sign */
 } favor_kernel;
 
 /* Storage type of q, k, v, out, x and phi.  Arithmetic: F32 computes in fp32
@@ -71,14 +77,23 @@ typedef struct favor_handle_s* favor_handle;
  *
  *   omega_host  host float array [H, m, d], row r of head h is omega_r
  *               (Eq. 5; drawn by the caller, e.g. orthogonal blocks as in §2.4
- *               and App. B.2 (1)).  Copied synchronously; the caller may free
- *               it on return.  The BF16 dtype rounds omega to bf16 (nearest
- *               even) for the tensor-core projection.
+ *               and App. B.2 (1), or rows of length sqrt(d) for the
+ *               regularized kernel SMREG of §2.3).  [H, m/2, d] for the
+ *               hyperbolic and trigonometric kinds (m features from m/2
+ *               rows).  Copied synchronously; the caller may free it on
+ *               return.  The BF16 dtype rounds omega to bf16 (nearest even)
+ *               for the tensor-core projection.
  *   data_scale  s > 0: features are taken of s*q and s*k.
  *   max_B, max_L  upper bounds for later calls; they size the workspace.
  *
  * Supported: d, dv in {16, 32, 64, 128}; m a multiple of 16 in [16, 256];
- * H >= 1.  Anything else gives FAVOR_ERR_UNSUPPORTED (enum values out of
+ * H >= 1.  The hyperbolic kind runs every call the positive kind runs (on the
+ * rows [omega; -omega]).  The trigonometric kind runs on the CUDA cores only;
+ * its key features carry exp(||s k||^2/2) unshifted, so keys with
+ * ||s k||^2 above about 170 overflow fp32; its denominators can be zero or
+ * negative (the instability §2.3 describes), and a zero one gives a zero row
+ * as for ReLU.  It has no backward and no handle-free call
+ * (FAVOR_ERR_UNSUPPORTED).  Anything else gives FAVOR_ERR_UNSUPPORTED (enum values out of
  * range: FAVOR_ERR_INVALID_ARG).  Fails with FAVOR_ERR_NOMEM if device memory
  * runs out, FAVOR_ERR_CUDA if no device is usable.  *out is set to NULL on
  * any failure.

@@ -1,6 +1,7 @@
 // Host side of the C ABI: argument checks, handle lifetime, workspace, dispatch.
 //
 // Every check runs before anything is enqueued; a failing call launches nothing.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -130,7 +131,8 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     if (H < 1 || m < 1 || d < 1 || dv < 1 || max_B < 1 || max_L < 1)
         return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: sizes must be >= 1 (H=%d m=%d d=%d dv=%d max_B=%d max_L=%d)",
                          H, m, d, dv, max_B, max_L);
-    if (kind != FAVOR_KERNEL_SOFTMAX_POS && kind != FAVOR_KERNEL_RELU)
+    if (kind != FAVOR_KERNEL_SOFTMAX_POS && kind != FAVOR_KERNEL_RELU && kind != FAVOR_KERNEL_SOFTMAX_HYP &&
+        kind != FAVOR_KERNEL_SOFTMAX_TRIG)
         return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: unknown kernel kind %d", (int)kind);
     if (dtype != FAVOR_DTYPE_F32 && dtype != FAVOR_DTYPE_BF16)
         return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: unknown dtype %d", (int)dtype);
@@ -153,19 +155,38 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     std::memset(h, 0, sizeof(*h));
     h->prof = new (std::nothrow) Profile();
     if (!h->prof) { delete h; return set_error(FAVOR_ERR_NOMEM, "favor_create: host allocation failed"); }
-    h->H = H; h->m = m; h->d = d; h->dv = dv; h->kind = kind; h->dtype = dtype;
+    const bool two_fn = kind == FAVOR_KERNEL_SOFTMAX_HYP || kind == FAVOR_KERNEL_SOFTMAX_TRIG;
+    h->H = H; h->m = m; h->d = d; h->dv = dv; h->dtype = dtype; h->features = kind;
+    h->kind = kind == FAVOR_KERNEL_SOFTMAX_HYP ? FAVOR_KERNEL_SOFTMAX_POS : kind;
     h->s = data_scale; h->max_B = max_B; h->max_L = max_L; h->device = dev;
     cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (h->num_sms < 1) h->num_sms = 1;
     cudaDeviceGetAttribute(&h->cc_major, cudaDevAttrComputeCapabilityMajor, dev);
 
     const size_t n_om = (size_t)H * m * d;
-    std::vector<float> om(omega_host, omega_host + n_om);
-    for (size_t i = 0; i < n_om; ++i) {
-        if (!std::isfinite(om[i])) {
+    // The two-function kinds get m/2 rows per head and run on [omega; -omega]
+    // (hyperbolic: exp(-omega.x) = exp((-omega).x)) or [omega; omega]
+    // (trigonometric: sin on the first half, cos on the second).
+    const size_t n_in = two_fn ? n_om / 2 : n_om;
+    for (size_t i = 0; i < n_in; ++i) {
+        if (!std::isfinite(omega_host[i])) {
             free_handle(h);
             return set_error(FAVOR_ERR_INVALID_ARG, "favor_create: omega has a non-finite entry at %zu", i);
         }
+    }
+    std::vector<float> om(n_om);
+    if (!two_fn) {
+        std::copy(omega_host, omega_host + n_om, om.begin());
+    } else {
+        const int M = m / 2;
+        const float sign = kind == FAVOR_KERNEL_SOFTMAX_HYP ? -1.f : 1.f;
+        for (int hh = 0; hh < H; ++hh)
+            for (int r = 0; r < M; ++r)
+                for (int c = 0; c < d; ++c) {
+                    const float w = omega_host[((size_t)hh * M + r) * d + c];
+                    om[((size_t)hh * m + r) * d + c] = w;
+                    om[((size_t)hh * m + M + r) * d + c] = sign * w;
+                }
     }
     std::vector<__nv_bfloat16> om_bf;
     if (dtype == FAVOR_DTYPE_BF16) {
@@ -191,7 +212,7 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
         }
         h->omega_sqnorm_half_host[hh] = (float)(0.5 * mx);
         double k = 0.5 * mx - (double)KSHIFT_HEADROOM;
-        ks[hh] = (float)(k > 0.0 ? k : 0.0);
+        ks[hh] = (float)(k > 0.0 && kind != FAVOR_KERNEL_SOFTMAX_TRIG ? k : 0.0);
     }
 
     // Workspace: per-(head, segment) states.  Both work splits stay within
@@ -322,6 +343,8 @@ favor_status favor_attn_bidir_noalloc(const float* omega, int H, int m, int d, i
     if (H < 1 || m < 1 || d < 1 || dv < 1 || B < 1 || L < 1)
         return set_error(FAVOR_ERR_INVALID_ARG, "%s: sizes must be >= 1 (H=%d m=%d d=%d dv=%d B=%d L=%d)", fn, H, m,
                          d, dv, B, L);
+    if (kind == FAVOR_KERNEL_SOFTMAX_HYP || kind == FAVOR_KERNEL_SOFTMAX_TRIG)
+        return set_error(FAVOR_ERR_UNSUPPORTED, "%s: kind %d needs a handle (favor_create)", fn, (int)kind);
     if (kind != FAVOR_KERNEL_SOFTMAX_POS && kind != FAVOR_KERNEL_RELU)
         return set_error(FAVOR_ERR_INVALID_ARG, "%s: unknown kernel kind %d", fn, (int)kind);
     if (dtype != FAVOR_DTYPE_F32 && dtype != FAVOR_DTYPE_BF16)
@@ -347,7 +370,7 @@ favor_status favor_attn_bidir_noalloc(const float* omega, int H, int m, int d, i
     }
     Handle h;
     std::memset(&h, 0, sizeof(h));
-    h.H = H; h.m = m; h.d = d; h.dv = dv; h.kind = kind; h.dtype = dtype; h.s = data_scale;
+    h.H = H; h.m = m; h.d = d; h.dv = dv; h.kind = kind; h.features = kind; h.dtype = dtype; h.s = data_scale;
     h.max_B = B; h.max_L = L; h.device = dev;
     cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (h.num_sms < 1) h.num_sms = 1;
@@ -403,6 +426,8 @@ static favor_status backward_call(const char* fn, bool causal, favor_handle hd, 
     if (!q || !k || !v || !dout || !dq || !dk || !dv)
         return set_error(FAVOR_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    if (h.kind == FAVOR_KERNEL_SOFTMAX_TRIG)
+        return set_error(FAVOR_ERR_UNSUPPORTED, "%s: no backward for trigonometric features", fn);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return causal ? simt_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, s)
                   : simt_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);

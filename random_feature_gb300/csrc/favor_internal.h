@@ -39,7 +39,8 @@ struct Profile {
 // Everything a handle owns.  Device pointers unless noted.
 struct Handle {
     int H, m, d, dv;
-    favor_kernel kind;
+    favor_kernel kind;        // computation kind: SOFTMAX_POS, RELU or SOFTMAX_TRIG (HYP runs as POS)
+    favor_kernel features;    // the kind the handle was created with
     favor_dtype dtype;
     float s;                  // data scale: x = s*q, y = s*k
     int max_B, max_L;

@@ -28,6 +28,37 @@ template <> __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16* p,
 
 constexpr int kTokTile = 32;  // tokens staged per shared-memory tile in the state/causal kernels
 
+// Feature values by computation kind, from the unscaled projection p = omega_r . x
+// (r the feature index of m).  The hyperbolic map runs as the positive kind on
+// the mirrored rows [omega; -omega].  The trigonometric kind holds the rows
+// [omega; omega]: features r < m/2 take sin, the others cos, of the same
+// projection, and its key features carry h(y) = exp(||y||^2/2) with no shift.
+template <int KIND>
+__device__ __forceinline__ float key_feat(float p, float nrm, float s, float kap, int r, int m) {
+    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) return expf(s * p - 0.5f * s * s * nrm - kap);
+    if (KIND == FAVOR_KERNEL_RELU) return fmaxf(s * p, 0.f);
+    const float a = s * p;
+    return (r < (m >> 1) ? sinf(a) : cosf(a)) * expf(0.5f * s * s * nrm);
+}
+
+// Query features up to a factor common to the row (the shift mx, m^-1/2, and
+// for the trigonometric kind h(x)): they cancel in num / den.
+template <int KIND>
+__device__ __forceinline__ float query_feat(float sp, float mx, int r, int m) {
+    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) return expf(sp - mx);
+    if (KIND == FAVOR_KERNEL_RELU) return fmaxf(sp, 0.f);
+    return r < (m >> 1) ? sinf(sp) : cosf(sp);
+}
+
+// The plain definition (favor_feature_map).
+template <int KIND>
+__device__ __forceinline__ float plain_feat(float p, float nrm, float s, int r, int m) {
+    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) return expf(s * p - 0.5f * s * s * nrm) * rsqrtf((float)m);
+    if (KIND == FAVOR_KERNEL_RELU) return fmaxf(s * p, 0.f) * rsqrtf((float)m);
+    const float a = s * p;
+    return (r < (m >> 1) ? sinf(a) : cosf(a)) * expf(0.5f * s * s * nrm) * rsqrtf((float)(m >> 1));
+}
+
 // ---------------------------------------------------------------- feature map
 // grid (ceil(L/16), B*H), 256 threads.  Output phi[bh, i, r] = plain definition.
 template <typename T, int KIND>
@@ -50,17 +81,13 @@ __global__ void __launch_bounds__(256) k_feature_map(const T* __restrict__ x, T*
         nrm[threadIdx.x] = a;
     }
     __syncthreads();
-    const float inv_sqrt_m = rsqrtf((float)m);
     const float* om = omega + (size_t)h * m * d;
     T* out = phi + ((size_t)bh * L + i0) * m;
     for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) {
         const int i = idx / m, r = idx - i * m;
         float p = 0.f;
         for (int c = 0; c < d; ++c) p = fmaf(__ldg(om + r * d + c), xs[i * d + c], p);
-        float f;
-        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) f = expf(s * p - 0.5f * s * s * nrm[i]) * inv_sqrt_m;
-        else f = fmaxf(s * p, 0.f) * inv_sqrt_m;
-        stf(out + idx, f);
+        stf(out + idx, plain_feat<KIND>(p, nrm[i], s, r, m));
     }
 }
 
@@ -105,9 +132,7 @@ __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, 
         for (int j = 0; j < nt; ++j) {
             float p = 0.f;
             for (int c = 0; c < d; ++c) p = fmaf(oms[r * dp + c], ks[j * d + c], p);
-            float f;
-            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) f = expf(s * p - 0.5f * s * s * nrm[j] - kap);
-            else f = fmaxf(s * p, 0.f);
+            const float f = key_feat<KIND>(p, nrm[j], s, kap, r, m);
 #pragma unroll
             for (int e = 0; e < DV; ++e) S[e] = fmaf(f, vs[j * DV + e], S[e]);
             z += f;
@@ -185,7 +210,8 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
         __syncthreads();
         for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) fq[idx] = expf(fq[idx] - rmax[idx / m]);
     } else {
-        for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) fq[idx] = fmaxf(fq[idx], 0.f);
+        for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x)
+            fq[idx] = query_feat<KIND>(fq[idx], 0.f, idx % m, m);
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < nq * sw; idx += blockDim.x) {
@@ -259,9 +285,7 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
                 pk = fmaf(oms[r * dp + c], ks[j * d + c], pk);
                 pq = fmaf(oms[r * dp + c], qs[j * d + c], pq);
             }
-            float fk;
-            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) fk = expf(s * pk - 0.5f * s * s * nrm[j] - kap);
-            else fk = fmaxf(s * pk, 0.f);
+            const float fk = key_feat<KIND>(pk, nrm[j], s, kap, r, m);
 #pragma unroll
             for (int e = 0; e < DV; ++e) S[e] = fmaf(fk, vs[j * DV + e], S[e]);
             z += fk;
@@ -275,7 +299,7 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
                 for (int w = 1; w < nwarps; ++w) mx = fmaxf(mx, wmax[w]);
                 fq = expf(s * pq - mx);
             } else {
-                fq = fmaxf(s * pq, 0.f);
+                fq = query_feat<KIND>(s * pq, 0.f, r, m);
             }
             // sum over r of fq * [S | z]: warp shuffles, then across warps in smem.
 #pragma unroll
@@ -368,14 +392,29 @@ favor_status dispatch3(const Handle& h, A... a) {
     }
     if (h.dtype == FAVOR_DTYPE_F32) {
         if (h.kind == FAVOR_KERNEL_SOFTMAX_POS) { FAVOR_DV_CASES(float, FAVOR_KERNEL_SOFTMAX_POS) }
-        else { FAVOR_DV_CASES(float, FAVOR_KERNEL_RELU) }
+        else if (h.kind == FAVOR_KERNEL_RELU) { FAVOR_DV_CASES(float, FAVOR_KERNEL_RELU) }
+        else { FAVOR_DV_CASES(float, FAVOR_KERNEL_SOFTMAX_TRIG) }
     } else {
         if (h.kind == FAVOR_KERNEL_SOFTMAX_POS) { FAVOR_DV_CASES(__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS) }
-        else { FAVOR_DV_CASES(__nv_bfloat16, FAVOR_KERNEL_RELU) }
+        else if (h.kind == FAVOR_KERNEL_RELU) { FAVOR_DV_CASES(__nv_bfloat16, FAVOR_KERNEL_RELU) }
+        else { FAVOR_DV_CASES(__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_TRIG) }
     }
 #undef FAVOR_DV_CASES
     return set_error(FAVOR_ERR_UNSUPPORTED, "unsupported dv=%d", h.dv);
 }
+
+// (dtype, kind) -> FN<T, KIND>(args...), for launchers templated on both.
+#define FAVOR_KIND_DISPATCH(hh, FN, ...)                                                             \
+    do {                                                                                            \
+        if ((hh).dtype == FAVOR_DTYPE_F32) {                                                        \
+            if ((hh).kind == FAVOR_KERNEL_SOFTMAX_POS) return FN<float, FAVOR_KERNEL_SOFTMAX_POS>(__VA_ARGS__); \
+            if ((hh).kind == FAVOR_KERNEL_RELU) return FN<float, FAVOR_KERNEL_RELU>(__VA_ARGS__);    \
+            return FN<float, FAVOR_KERNEL_SOFTMAX_TRIG>(__VA_ARGS__);                               \
+        }                                                                                           \
+        if ((hh).kind == FAVOR_KERNEL_SOFTMAX_POS) return FN<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(__VA_ARGS__); \
+        if ((hh).kind == FAVOR_KERNEL_RELU) return FN<__nv_bfloat16, FAVOR_KERNEL_RELU>(__VA_ARGS__); \
+        return FN<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_TRIG>(__VA_ARGS__);                           \
+    } while (0)
 
 template <typename T, int KIND, int DV>
 struct StateF {
@@ -414,12 +453,7 @@ favor_status launch_scan_segments(const Handle& h, int BH, int n_seg, cudaStream
 }
 
 favor_status simt_feature_map(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st) {
-    if (h.dtype == FAVOR_DTYPE_F32)
-        return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? feature_map_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, x, phi, B, L, st)
-                                                  : feature_map_t<float, FAVOR_KERNEL_RELU>(h, x, phi, B, L, st);
-    return h.kind == FAVOR_KERNEL_SOFTMAX_POS
-               ? feature_map_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, x, phi, B, L, st)
-               : feature_map_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, x, phi, B, L, st);
+    FAVOR_KIND_DISPATCH(h, feature_map_t, h, x, phi, B, L, st);
 }
 
 favor_status simt_bidir(const Handle& h, const void* q, const void* k, const void* v, void* out, int B, int L,
@@ -430,11 +464,7 @@ favor_status simt_bidir(const Handle& h, const void* q, const void* k, const voi
     if (s != FAVOR_OK) return s;
     s = launch_reduce_segments(h, BH, p.n_seg, st);
     if (s != FAVOR_OK) return s;
-    if (h.dtype == FAVOR_DTYPE_F32)
-        return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
-                                                  : readout_t<float, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
-    return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
-                                              : readout_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
+    FAVOR_KIND_DISPATCH(h, readout_t, h, q, out, BH, L, st);
 }
 
 favor_status simt_causal(const Handle& h, const void* q, const void* k, const void* v, void* out, int B, int L,
@@ -527,7 +557,7 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
             o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
         }
     }
-    const float inv_sqrt_m = 1.f / sqrtf((float)m);
+    const float inv_sqrt_m = 1.f / sqrtf((float)(KIND == FAVOR_KERNEL_SOFTMAX_TRIG ? m / 2 : m));
     const float kap = kshift[h];
     const int rr = tid < m ? tid : 0;
     for (int t = 0; t < Tn; ++t) {
@@ -561,14 +591,10 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
         const float qx = s * pq;
         const float mx = KIND == FAVOR_KERNEL_SOFTMAX_POS ? block_max(tid < m ? qx : -INFINITY, red) : 0.f;
         if (tid < m) {
-            float fk, f;
-            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-                fk = inv_sqrt_m * expf(s * pk - 0.5f * s * s * nk - kap);
-                f = expf(qx - mx);   // a per-query shift: cancels in num / den
-            } else {
-                fk = inv_sqrt_m * fmaxf(s * pk, 0.f);
-                f = fmaxf(qx, 0.f);
-            }
+            // the state holds the plain features (m^-1/2, or (m/2)^-1/2 for the
+            // trigonometric map); the query side drops row-common factors.
+            const float fk = inv_sqrt_m * key_feat<KIND>(pk, nk, s, kap, tid, m);
+            const float f = query_feat<KIND>(qx, mx, tid, m);   // mx: a per-query shift, cancels
             float* Sr = S + tid * dp;
             for (int e = 0; e < dv; ++e) Sr[e] = fmaf(fk, xv[e], Sr[e]);
             Sr[dv] += fk;
@@ -623,7 +649,8 @@ favor_status simt_kv_state(const Handle& h, const void* k, const void* v, float*
     const int n = h.m * (h.dv + 1);
     dim3 grid((n + 255) / 256, BH);
     ProfScope ps(h, PROF_COMBINE, st);
-    k_accum_rows<<<grid, 256, 0, st>>>(h.ws_partial, state, p.n_seg, n, 1.f / sqrtf((float)h.m));
+    const int m_norm = h.kind == FAVOR_KERNEL_SOFTMAX_TRIG ? h.m / 2 : h.m;   // the plain map's 1/sqrt
+    k_accum_rows<<<grid, 256, 0, st>>>(h.ws_partial, state, p.n_seg, n, 1.f / sqrtf((float)m_norm));
     count_launch();
     return check_launch("state accumulate kernel");
 }
@@ -633,23 +660,13 @@ favor_status simt_attn_from_state(const Handle& proto, const void* q, const floa
     Handle h = proto;
     h.ws_state = const_cast<float*>(state);   // the readout only reads it
     const int BH = B * h.H;
-    if (h.dtype == FAVOR_DTYPE_F32)
-        return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
-                                                  : readout_t<float, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
-    return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
-                                              : readout_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
+    FAVOR_KIND_DISPATCH(h, readout_t, h, q, out, BH, L, st);
 }
 
 favor_status simt_causal_step(const Handle& h, const void* q, const void* k, const void* v, void* out, float* state,
                               int B, int Tn, cudaStream_t st) {
     const int BH = B * h.H;
-    if (h.dtype == FAVOR_DTYPE_F32)
-        return h.kind == FAVOR_KERNEL_SOFTMAX_POS
-                   ? causal_step_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, q, k, v, out, state, BH, Tn, st)
-                   : causal_step_t<float, FAVOR_KERNEL_RELU>(h, q, k, v, out, state, BH, Tn, st);
-    return h.kind == FAVOR_KERNEL_SOFTMAX_POS
-               ? causal_step_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, q, k, v, out, state, BH, Tn, st)
-               : causal_step_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, q, k, v, out, state, BH, Tn, st);
+    FAVOR_KIND_DISPATCH(h, causal_step_t, h, q, k, v, out, state, BH, Tn, st);
 }
 
 // ------------------------------------------------ bidirectional call, fixed scratch
@@ -748,11 +765,7 @@ favor_status simt_bidir_fixed_scratch(const Handle& proto, const void* q, const 
     if (s != FAVOR_OK) return s;
     s = launch_reduce_segments(h, BH, p.n_seg, st);
     if (s != FAVOR_OK) return s;
-    if (h.dtype == FAVOR_DTYPE_F32)
-        return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<float, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
-                                                  : readout_t<float, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
-    return h.kind == FAVOR_KERNEL_SOFTMAX_POS ? readout_t<__nv_bfloat16, FAVOR_KERNEL_SOFTMAX_POS>(h, q, out, BH, L, st)
-                                              : readout_t<__nv_bfloat16, FAVOR_KERNEL_RELU>(h, q, out, BH, L, st);
+    FAVOR_KIND_DISPATCH(h, readout_t, h, q, out, BH, L, st);
 }
 
 }  // namespace favor

@@ -1669,7 +1669,7 @@ favor_status launch_state(const Handle& h, const CUtensorMap& mk, const CUtensor
 
 bool tc_supported(const Handle& h) {
     return h.dtype == FAVOR_DTYPE_BF16 && h.d == kD && h.dv == kDV && h.m == kM && h.cc_major >= 10 &&
-           encode_fn() != nullptr;
+           h.kind != FAVOR_KERNEL_SOFTMAX_TRIG && encode_fn() != nullptr;
 }
 
 favor_status tc_feature_map(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st) {

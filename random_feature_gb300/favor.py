@@ -17,7 +17,8 @@ import numpy as np
 
 __all__ = [
     "FAVOR_OK", "FAVOR_ERR_INVALID_ARG", "FAVOR_ERR_UNSUPPORTED", "FAVOR_ERR_NOMEM", "FAVOR_ERR_CUDA",
-    "FAVOR_KERNEL_SOFTMAX_POS", "FAVOR_KERNEL_RELU", "FAVOR_DTYPE_F32", "FAVOR_DTYPE_BF16",
+    "FAVOR_KERNEL_SOFTMAX_POS", "FAVOR_KERNEL_RELU", "FAVOR_KERNEL_SOFTMAX_HYP", "FAVOR_KERNEL_SOFTMAX_TRIG",
+    "FAVOR_DTYPE_F32", "FAVOR_DTYPE_BF16",
     "FavorError", "FavorLibraryMissing", "lib", "lib_path",
     "favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal", "favor_destroy",
     "favor_status_str", "favor_last_error", "favor_launch_count", "Favor", "EXPORTED_SYMBOLS",
@@ -28,9 +29,10 @@ __all__ = [
 ]
 
 FAVOR_OK, FAVOR_ERR_INVALID_ARG, FAVOR_ERR_UNSUPPORTED, FAVOR_ERR_NOMEM, FAVOR_ERR_CUDA = range(5)
-FAVOR_KERNEL_SOFTMAX_POS, FAVOR_KERNEL_RELU = 0, 1
+FAVOR_KERNEL_SOFTMAX_POS, FAVOR_KERNEL_RELU, FAVOR_KERNEL_SOFTMAX_HYP, FAVOR_KERNEL_SOFTMAX_TRIG = 0, 1, 2, 3
 FAVOR_DTYPE_F32, FAVOR_DTYPE_BF16 = 0, 1
-KIND_CODES = {"softmax_pos": FAVOR_KERNEL_SOFTMAX_POS, "relu": FAVOR_KERNEL_RELU}
+KIND_CODES = {"softmax_pos": FAVOR_KERNEL_SOFTMAX_POS, "relu": FAVOR_KERNEL_RELU,
+              "softmax_hyp": FAVOR_KERNEL_SOFTMAX_HYP, "softmax_trig": FAVOR_KERNEL_SOFTMAX_TRIG}
 DTYPE_CODES = {"f32": FAVOR_DTYPE_F32, "bf16": FAVOR_DTYPE_BF16}
 
 EXPORTED_SYMBOLS = ("favor_create", "favor_feature_map", "favor_attn_bidir", "favor_attn_causal",
@@ -143,12 +145,14 @@ def _stream(stream, like):
 
 
 def favor_create(H, m, d, dv, kind, dtype, omega, data_scale, max_B, max_L) -> int:
-    """Create a handle; ``omega`` is a host float32 array [H, m, d].  Returns the handle (int)."""
+    """Create a handle; ``omega`` is a host float32 array [H, m, d] ([H, m/2, d] for the
+    hyperbolic and trigonometric kinds).  Returns the handle (int)."""
     kind = KIND_CODES.get(kind, kind)
     dtype = DTYPE_CODES.get(dtype, dtype)
     om = np.ascontiguousarray(omega, dtype=np.float32)
-    if om.shape != (H, m, d):
-        raise ValueError(f"omega must have shape {(H, m, d)}, got {om.shape}")
+    rows = m // 2 if kind in (FAVOR_KERNEL_SOFTMAX_HYP, FAVOR_KERNEL_SOFTMAX_TRIG) else m
+    if om.shape != (H, rows, d):
+        raise ValueError(f"omega must have shape {(H, rows, d)}, got {om.shape}")
     h = ctypes.c_void_p()
     st = lib().favor_create(ctypes.byref(h), int(H), int(m), int(d), int(dv), int(kind), int(dtype),
                             om.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), float(data_scale),
