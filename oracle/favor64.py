@@ -43,6 +43,8 @@ __all__ = [
     "feature_map_vjp", "attn_from_features_bidir_vjp", "attn_from_features_causal_vjp",
     "favor_bidir_backward", "favor_causal_backward",
     "feature_map_hyperbolic", "feature_map_trig", "VARIANT_KINDS", "n_features",
+    "gated_causal_from_features", "favor_causal_gated", "permutation_power", "permute_features",
+    "favor_permute",
 ]
 
 KINDS = ("softmax_pos", "relu")
@@ -419,6 +421,96 @@ def favor_bidir_backward(q, k, v, dout, omega, data_scale, kind="softmax_pos"):
 def favor_causal_backward(q, k, v, dout, omega, data_scale, kind="softmax_pos"):
     """(dq, dk, dv) of favor_causal for the upstream gradient dout [B,H,L,dv]."""
     return _per_head_backward(q, k, v, dout, omega, data_scale, kind, attn_from_features_causal_vjp)
+
+
+# ------------------------------------------------------------ gated causal (RFA-Gate)
+def gated_causal_from_features(phi_q, phi_k, v, gate):
+    """Causal attention with a gated (decaying) state, token by token.
+
+    [RFA] §3.2 RFA-GATE: scalar gates g_t in [0, 1], computed by the model from
+    the timestep's input, decay the history of both the value state and the
+    normalisation state.  Reading taken (the page states the gate only in
+    words): the gate interpolates between the history and the current token,
+        S_t = g_t S_{t-1} + (1 - g_t) phi(k_t) v_t^T,
+        z_t = g_t z_{t-1} + (1 - g_t) phi(k_t),
+        out_t = phi(q_t)^T S_t / phi(q_t)^T z_t   (0 if the denominator is 0),
+    with S_0 = 0, z_0 = 0 as in [RFA] A.3.  A pure-Python loop over t.
+    phi_q, phi_k [L, m], v [L, dv], gate [L] -> out [L, dv].
+    """
+    phi_q, phi_k, v, gate = _f64(phi_q), _f64(phi_k), _f64(v), _f64(gate)
+    L, m = phi_q.shape
+    s = np.zeros((m, v.shape[1]))
+    z = np.zeros(m)
+    out = np.zeros((L, v.shape[1]))
+    for t in range(L):
+        g = gate[t]
+        s = g * s + (1.0 - g) * np.outer(phi_k[t], v[t])
+        z = g * z + (1.0 - g) * phi_k[t]
+        den = phi_q[t] @ z
+        out[t] = (phi_q[t] @ s) / den if den != 0.0 else 0.0
+    return out
+
+
+def favor_causal_gated(q, k, v, gate, omega, data_scale, kind="softmax_pos"):
+    """RFA-Gate causal attention on [B,H,L,*] inputs with gates [B,H,L]."""
+    q, k, v, gate, omega = _f64(q), _f64(k), _f64(v), _f64(gate), _f64(omega)
+    B, H, L, _ = q.shape
+    out = np.empty((B, H, L, v.shape[-1]))
+    for b in range(B):
+        for h in range(H):
+            pq = feature_map(data_scale * q[b, h], omega[h], kind)
+            pk = feature_map(data_scale * k[b, h], omega[h], kind)
+            out[b, h] = gated_causal_from_features(pq, pk, v[b, h], gate[b, h])
+    return out
+
+
+# ------------------------------------------------------------ PermuteFormer
+def permutation_power(perm, i):
+    """pi^i as an index array: pi^i(a) = pi(pi(...pi(a))) (i times); pi^0 = identity.
+    [PF] §Computational cost: powers of a permutation are permutations, composed
+    by indexing."""
+    perm = np.asarray(perm)
+    out = np.arange(len(perm))
+    for _ in range(i):
+        out = perm[out]
+    return out
+
+
+def permute_features(phi, perm, r, sign):
+    """Position-dependent transform of PermuteFormer ([PF] §PermuteFormer, the
+    solution chosen for Eq. 9-10): row i of phi [L, m] becomes
+    r^(sign*i) P_pi^i phi_i, where P_pi has P_ab = 1 iff pi(a) = b, so
+    (P_pi^i phi)_a = phi_{pi^i(a)} (a gather by pi^i).  Queries take sign = +1
+    and keys sign = -1, so that the similarity of query i and key j is
+    r^(i-j) phi(q_i)^T P_pi^(j-i) phi(k_j): it depends on i - j only.
+    Positions i count from 0 (only differences matter)."""
+    phi = _f64(phi)
+    out = np.empty_like(phi)
+    idx = np.arange(phi.shape[1])
+    perm = np.asarray(perm)
+    for i in range(phi.shape[0]):
+        out[i] = (float(r) ** (sign * i)) * phi[i, idx]
+        idx = perm[idx]           # pi^(i+1)
+    return out
+
+
+def favor_permute(q, k, v, omega, data_scale, perm, r, causal, kind="softmax_pos"):
+    """PermuteFormer attention ([PF] §PermuteFormer): Performer features of q
+    and k, transformed by permute_features (r applies to causal attention; the
+    page takes r = 1 for bidirectional models), then the usual bidirectional
+    (Alg. 1) or causal (Eq. 11) attention from features.  perm [H, m] holds one
+    permutation of the feature indices per head, r [H] one decay per head."""
+    q, k, v, omega = _f64(q), _f64(k), _f64(v), _f64(omega)
+    B, H, L, _ = q.shape
+    out = np.empty((B, H, L, v.shape[-1]))
+    for b in range(B):
+        for h in range(H):
+            rr = float(r[h]) if causal else 1.0
+            pq = permute_features(feature_map(data_scale * q[b, h], omega[h], kind), perm[h], rr, +1)
+            pk = permute_features(feature_map(data_scale * k[b, h], omega[h], kind), perm[h], rr, -1)
+            fn = attn_from_features_causal if causal else attn_from_features_bidir
+            out[b, h] = fn(pq, pk, v[b, h])
+    return out
 
 
 def softmax_attention(q, k, v, data_scale, causal=False):
