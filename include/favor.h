@@ -188,6 +188,53 @@ FAVOR_API favor_status favor_attn_causal_step(favor_handle h, const void* q, con
                                               void* out, float* state, int B, int T, void* stream);
 
 /*
+ * favor_attn_causal_gated -- causal attention with a gated, decaying state
+ * (RFA-Gate, Random Feature Attention §3.2).  The page describes the gate in
+ * words: scalar gates g_t in [0, 1], computed by the model from the timestep's
+ * input, decay the history of both the value state and the normalisation
+ * state.  The reading implemented (the gate interpolates between history and
+ * the current token):
+ *     S_t = g_t S_{t-1} + (1 - g_t) phi(k_t) v_t^T,   z_t = g_t z_{t-1} + (1 - g_t) phi(k_t),
+ *     out_t = phi(q_t)^T S_t / phi(q_t)^T z_t                (0 where the denominator is 0)
+ *   gate   DEVICE float array [B,H,L] (fp32 whatever the dtype), caller-owned,
+ *          read only; values outside [0, 1] are not checked.
+ * Other arguments as favor_attn_causal.  Runs on the CUDA cores (chunked: the
+ * segments' states are combined with the products of their gates).  Not
+ * combined with favor_set_relpos (FAVOR_ERR_UNSUPPORTED while it is set).
+ *
+ * favor_attn_causal_step_gated -- favor_attn_causal_step with the same gated
+ * update; gate [B,H,T].
+ */
+FAVOR_API favor_status favor_attn_causal_gated(favor_handle h, const void* q, const void* k, const void* v,
+                                               const float* gate, void* out, int B, int L, void* stream);
+FAVOR_API favor_status favor_attn_causal_step_gated(favor_handle h, const void* q, const void* k, const void* v,
+                                                    const float* gate, void* out, float* state, int B, int T,
+                                                    void* stream);
+
+/*
+ * favor_set_relpos -- PermuteFormer relative position encoding (PermuteFormer:
+ * Efficient Relative Position Encoding for Long Sequences, §PermuteFormer).
+ * Query and key features at position i are transformed by r^i P_pi^i and
+ * r^-i P_pi^i, P_pi the permutation matrix of pi ((P_pi phi)_a = phi_pi(a)),
+ * so the similarity of query i and key j is r^(i-j) phi(q_i)^T P_pi^(j-i) phi(k_j):
+ * it depends on i - j only.  Positions count from 0 within each call.
+ *   perm  HOST int array [H, m]: row h is a permutation of 0..m-1 (NULL: the
+ *         identity).  Stored as each permutation's cycles (O(H m) device
+ *         memory); pi^i(a) is looked up from a's cycle, not precomputed per
+ *         position.
+ *   r     HOST float array [H], 0 < r <= 1 (NULL: 1).  Applies to causal calls
+ *         (a state decayed by r per token); bidirectional calls use r = 1, as
+ *         the page prescribes for bidirectional models.
+ * Both NULL clears the setting.  While set, favor_attn_bidir and
+ * favor_attn_causal apply it (on the CUDA cores); favor_feature_map still
+ * returns the plain phi; the gated, state, step and backward calls fail with
+ * FAVOR_ERR_UNSUPPORTED.  Synchronises the handle's device and allocates, like
+ * favor_create; call it with no call of the handle in flight.
+ * INVALID_ARG for a row that is not a permutation or an r outside (0, 1].
+ */
+FAVOR_API favor_status favor_set_relpos(favor_handle h, const int* perm, const float* r);
+
+/*
  * favor_attn_bidir_backward / favor_attn_causal_backward -- gradients of
  * favor_attn_bidir / favor_attn_causal with respect to q, k and v.
  *

@@ -111,6 +111,10 @@ static void free_handle(Handle* h) {
     cudaFree(h->ws_partial2);
     cudaFree(h->ws_dstate);
     cudaFree(h->ws_rowstat);
+    cudaFree(h->ws_segdecay);
+    cudaFree(h->perm_cyc);
+    cudaFree(h->perm_meta);
+    cudaFree(h->relpos_r);
     cudaFree(h->ws_tc);
     free(h->omega_sqnorm_half_host);
     if (h->prof) {
@@ -235,6 +239,7 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_partial2, rows * st_elems * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_dstate, (size_t)max_B * H * st_elems * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_rowstat, (size_t)max_B * H * (size_t)max_L * 4 * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->ws_segdecay, rows * sizeof(float));
     if (e != cudaSuccess) {
         favor_status st = (e == cudaErrorMemoryAllocation) ? FAVOR_ERR_NOMEM : FAVOR_ERR_CUDA;
         set_error(st, "favor_create: cudaMalloc: %s", cudaGetErrorString(e));
@@ -285,6 +290,8 @@ favor_status favor_destroy(favor_handle hd) {
     return FAVOR_OK;
 }
 
+static bool relpos_on(const Handle& h) { return h.perm_cyc != nullptr || h.relpos_r != nullptr; }
+
 static favor_status check_call(const char* fn, favor_handle hd, int B, int L) {
     g_err[0] = 0;
     if (!hd) return set_error(FAVOR_ERR_INVALID_ARG, "%s: handle is NULL", fn);
@@ -319,7 +326,7 @@ favor_status favor_attn_bidir(favor_handle hd, const void* q, const void* k, con
     if (!q || !k || !v || !out) return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_bidir: null tensor pointer");
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (tc_supported(h)) return tc_bidir(h, q, k, v, out, B, L, s);
+    if (tc_supported(h) && !relpos_on(h)) return tc_bidir(h, q, k, v, out, B, L, s);
     return simt_bidir(h, q, k, v, out, B, L, s);
 }
 
@@ -330,8 +337,97 @@ favor_status favor_attn_causal(favor_handle hd, const void* q, const void* k, co
     if (!q || !k || !v || !out) return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_causal: null tensor pointer");
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (tc_supported(h)) return tc_causal(h, q, k, v, out, B, L, s);
+    if (tc_supported(h) && !relpos_on(h)) return tc_causal(h, q, k, v, out, B, L, s);
     return simt_causal(h, q, k, v, out, B, L, s);
+}
+
+favor_status favor_attn_causal_gated(favor_handle hd, const void* q, const void* k, const void* v, const float* gate,
+                                     void* out, int B, int L, void* stream) {
+    favor_status st = check_call("favor_attn_causal_gated", hd, B, L);
+    if (st != FAVOR_OK) return st;
+    if (!q || !k || !v || !gate || !out)
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_causal_gated: null pointer");
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    if (relpos_on(h)) return set_error(FAVOR_ERR_UNSUPPORTED, "favor_attn_causal_gated: relative positions are set");
+    return simt_causal(h, q, k, v, out, B, L, reinterpret_cast<cudaStream_t>(stream), gate);
+}
+
+favor_status favor_set_relpos(favor_handle hd, const int* perm, const float* r) {
+    g_err[0] = 0;
+    if (!hd) return set_error(FAVOR_ERR_INVALID_ARG, "favor_set_relpos: handle is NULL");
+    Handle* h = reinterpret_cast<Handle*>(hd);
+    const int H = h->H, m = h->m;
+    if (r) {
+        for (int i = 0; i < H; ++i)
+            if (!(r[i] > 0.f && r[i] <= 1.f))
+                return set_error(FAVOR_ERR_INVALID_ARG, "favor_set_relpos: r[%d] = %g is not in (0, 1]", i, (double)r[i]);
+    }
+    // cycle tables: per head, the permutation written cycle by cycle, and per
+    // feature (start of its cycle, cycle length, its place in the cycle)
+    std::vector<int> cyc, meta;
+    if (perm) {
+        cyc.resize((size_t)H * m);
+        meta.resize((size_t)H * m * 4);
+        std::vector<char> seen(m);
+        for (int hh = 0; hh < H; ++hh) {
+            const int* p = perm + (size_t)hh * m;
+            std::fill(seen.begin(), seen.end(), 0);
+            for (int a = 0; a < m; ++a) {
+                if (p[a] < 0 || p[a] >= m || seen[p[a]])
+                    return set_error(FAVOR_ERR_INVALID_ARG, "favor_set_relpos: row %d is not a permutation of 0..%d",
+                                     hh, m - 1);
+                seen[p[a]] = 1;
+            }
+            std::fill(seen.begin(), seen.end(), 0);
+            int fill = 0;
+            for (int a0 = 0; a0 < m; ++a0) {
+                if (seen[a0]) continue;
+                const int start = fill;
+                int a = a0;
+                do {
+                    seen[a] = 1;
+                    cyc[(size_t)hh * m + fill++] = a;
+                    a = p[a];
+                } while (a != a0);
+                const int len = fill - start;
+                for (int t = 0; t < len; ++t) {
+                    int* mt = &meta[((size_t)hh * m + cyc[(size_t)hh * m + start + t]) * 4];
+                    mt[0] = start; mt[1] = len; mt[2] = t; mt[3] = 0;
+                }
+            }
+        }
+    }
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != h->device) cudaSetDevice(h->device);
+    cudaDeviceSynchronize();   // no call of this handle may still read the old tables
+    cudaFree(h->perm_cyc);
+    cudaFree(h->perm_meta);
+    cudaFree(h->relpos_r);
+    h->perm_cyc = nullptr;
+    h->perm_meta = nullptr;
+    h->relpos_r = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (perm) {
+        e = cudaMalloc(&h->perm_cyc, cyc.size() * sizeof(int));
+        if (e == cudaSuccess) e = cudaMalloc(&h->perm_meta, meta.size() * sizeof(int));
+        if (e == cudaSuccess) e = cudaMemcpy(h->perm_cyc, cyc.data(), cyc.size() * sizeof(int), cudaMemcpyHostToDevice);
+        if (e == cudaSuccess)
+            e = cudaMemcpy(h->perm_meta, meta.data(), meta.size() * sizeof(int), cudaMemcpyHostToDevice);
+    }
+    if (e == cudaSuccess && r) {
+        e = cudaMalloc(&h->relpos_r, H * sizeof(float));
+        if (e == cudaSuccess) e = cudaMemcpy(h->relpos_r, r, H * sizeof(float), cudaMemcpyHostToDevice);
+    }
+    if (cur != h->device) cudaSetDevice(cur);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->perm_cyc); cudaFree(h->perm_meta); cudaFree(h->relpos_r);
+        h->perm_cyc = nullptr; h->perm_meta = nullptr; h->relpos_r = nullptr;
+        return set_error(e == cudaErrorMemoryAllocation ? FAVOR_ERR_NOMEM : FAVOR_ERR_CUDA, "favor_set_relpos: %s",
+                         cudaGetErrorString(e));
+    }
+    return FAVOR_OK;
 }
 
 favor_status favor_attn_bidir_noalloc(const float* omega, int H, int m, int d, int dv, favor_kernel kind,
@@ -388,6 +484,7 @@ favor_status favor_kv_state(favor_handle hd, const void* k, const void* v, float
     if (reinterpret_cast<uintptr_t>(state) % 16)
         return set_error(FAVOR_ERR_INVALID_ARG, "favor_kv_state: state must be 16-byte aligned");
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    if (relpos_on(h)) return set_error(FAVOR_ERR_UNSUPPORTED, "favor_kv_state: relative positions are set");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tc_supported(h)) return tc_kv_state(h, k, v, state, B, L, s);
     return simt_kv_state(h, k, v, state, B, L, s);
@@ -401,21 +498,33 @@ favor_status favor_attn_from_state(favor_handle hd, const void* q, const float* 
     if (reinterpret_cast<uintptr_t>(state) % 16)
         return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_from_state: state must be 16-byte aligned");
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    if (relpos_on(h)) return set_error(FAVOR_ERR_UNSUPPORTED, "favor_attn_from_state: relative positions are set");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tc_supported(h)) return tc_attn_from_state(h, q, state, out, B, L, s);
     return simt_attn_from_state(h, q, state, out, B, L, s);
 }
 
+static favor_status causal_step_call(const char* fn, favor_handle hd, const void* q, const void* k, const void* v,
+                                     const float* gate, bool gated, void* out, float* state, int B, int T,
+                                     void* stream) {
+    favor_status st = check_call(fn, hd, B, T);
+    if (st != FAVOR_OK) return st;
+    if (!q || !k || !v || !out || !state || (gated && !gate)) return set_error(FAVOR_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (reinterpret_cast<uintptr_t>(state) % 16)
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: state must be 16-byte aligned", fn);
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    if (relpos_on(h)) return set_error(FAVOR_ERR_UNSUPPORTED, "%s: relative positions are set", fn);
+    return simt_causal_step(h, q, k, v, out, state, B, T, reinterpret_cast<cudaStream_t>(stream), gate);
+}
+
 favor_status favor_attn_causal_step(favor_handle hd, const void* q, const void* k, const void* v, void* out,
                                     float* state, int B, int T, void* stream) {
-    favor_status st = check_call("favor_attn_causal_step", hd, B, T);
-    if (st != FAVOR_OK) return st;
-    if (!q || !k || !v || !out || !state)
-        return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_causal_step: null pointer");
-    if (reinterpret_cast<uintptr_t>(state) % 16)
-        return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_causal_step: state must be 16-byte aligned");
-    const Handle& h = *reinterpret_cast<const Handle*>(hd);
-    return simt_causal_step(h, q, k, v, out, state, B, T, reinterpret_cast<cudaStream_t>(stream));
+    return causal_step_call("favor_attn_causal_step", hd, q, k, v, nullptr, false, out, state, B, T, stream);
+}
+
+favor_status favor_attn_causal_step_gated(favor_handle hd, const void* q, const void* k, const void* v,
+                                          const float* gate, void* out, float* state, int B, int T, void* stream) {
+    return causal_step_call("favor_attn_causal_step_gated", hd, q, k, v, gate, true, out, state, B, T, stream);
 }
 
 static favor_status backward_call(const char* fn, bool causal, favor_handle hd, const void* q, const void* k,
@@ -428,6 +537,7 @@ static favor_status backward_call(const char* fn, bool causal, favor_handle hd, 
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_TRIG)
         return set_error(FAVOR_ERR_UNSUPPORTED, "%s: no backward for trigonometric features", fn);
+    if (relpos_on(h)) return set_error(FAVOR_ERR_UNSUPPORTED, "%s: relative positions are set", fn);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return causal ? simt_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, s)
                   : simt_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);

@@ -62,6 +62,11 @@ struct Handle {
     float* ws_dstate;         // [max_B*H][m][dv+1] backward: reduced sum of phi~_q D^T (bidirectional)
     float* ws_rowstat;        // [max_B*H*max_L][4] backward (causal): per query (den~, row shift, dO . out, 0)
     size_t ws_partial_rows;   // capacity of ws_partial in (head, segment) rows
+    float* ws_segdecay;       // [rows] per-segment products of a decaying causal state's factors
+    // PermuteFormer relative positions (favor_set_relpos); null when unset.
+    int* perm_cyc;            // [H*m] each head's permutation written cycle by cycle
+    int4* perm_meta;          // [H*m] per feature: (cycle start, cycle length, place in the cycle, 0)
+    float* relpos_r;          // [H] decay r of causal calls (null: 1)
     void* ws_tc;              // tensor-core path scratch (bf16 operand copies), may be null
     size_t ws_tc_bytes;
     Profile* prof;            // per-kernel timing (host object)
@@ -102,7 +107,16 @@ favor_status simt_feature_map(const Handle& h, const void* x, void* phi, int B, 
 favor_status simt_bidir(const Handle& h, const void* q, const void* k, const void* v, void* out,
                         int B, int L, cudaStream_t st);
 favor_status simt_causal(const Handle& h, const void* q, const void* k, const void* v, void* out,
-                         int B, int L, cudaStream_t st);
+                         int B, int L, cudaStream_t st, const float* gate = nullptr);
+
+// Optional position-dependent inputs of the CUDA-core segment kernels.
+struct RelposArgs {
+    const int* cyc = nullptr;      // PermuteFormer permutation cycles (null: identity)
+    const int4* meta = nullptr;
+    const float* gate = nullptr;   // RFA-Gate gates [B*H*L] (null: none)
+    const float* rdec = nullptr;   // per-head decay r (null: 1)
+    float* segdecay = nullptr;     // out: per-segment decay products (decaying causal calls)
+};
 
 // Per-segment key/value states of the CUDA-core path into h.ws_partial (row-major).
 favor_status simt_state_partials(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan& p,
@@ -120,7 +134,7 @@ favor_status simt_kv_state(const Handle& h, const void* k, const void* v, float*
 favor_status simt_attn_from_state(const Handle& h, const void* q, const float* state, void* out, int B, int L,
                                   cudaStream_t st);
 favor_status simt_causal_step(const Handle& h, const void* q, const void* k, const void* v, void* out, float* state,
-                              int B, int Tn, cudaStream_t st);
+                              int B, int Tn, cudaStream_t st, const float* gate = nullptr);
 favor_status tc_kv_state(const Handle& h, const void* k, const void* v, float* state, int B, int L, cudaStream_t st);
 favor_status tc_attn_from_state(const Handle& h, const void* q, const float* state, void* out, int B, int L,
                                 cudaStream_t st);

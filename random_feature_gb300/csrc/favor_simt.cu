@@ -59,6 +59,37 @@ __device__ __forceinline__ float plain_feat(float p, float nrm, float s, int r, 
     return (r < (m >> 1) ? sinf(a) : cosf(a)) * expf(0.5f * s * s * nrm) * rsqrtf((float)(m >> 1));
 }
 
+// Position-dependent feature order of PermuteFormer: at position j the slot r
+// holds feature pi^j(r).  Per head, the permutation's cycles are listed in
+// cyc[h*m + ...]; meta[h*m + r] = (start of r's cycle, its length, r's place in
+// it, 0), so pi^j(r) = cyc[h*m + start + (place + j) mod length].
+struct PermCursor {
+    const int* cyc;   // null: identity
+    int base, len, idx;
+    __device__ __forceinline__ void init(const int* c, const int4* meta, int h, int m, int r, long long j) {
+        cyc = c;
+        base = 0; len = 1; idx = 0;
+        if (c) {
+            const int4 mt = meta[(size_t)h * m + r];
+            base = h * m + mt.x;
+            len = mt.y;
+            idx = (int)((mt.z + j) % mt.y);
+        }
+    }
+    __device__ __forceinline__ int row(int r) const { return cyc ? cyc[base + idx] : r; }
+    __device__ __forceinline__ void next() {
+        if (cyc && ++idx == len) idx = 0;
+    }
+};
+
+// Per-token decay of a causal state: S_j = a_j S_{j-1} + b_j phi(k_j) [v_j 1]^T
+// with a_j = r_h g_j and b_j = 1 - g_j (RFA-Gate gates g, PermuteFormer r).
+__device__ __forceinline__ void token_decay(const float* gate, size_t gidx, float rd, float* a, float* b) {
+    const float g = gate ? gate[gidx] : 0.f;
+    *a = rd * (gate ? g : 1.f);
+    *b = gate ? 1.f - g : 1.f;
+}
+
 // ---------------------------------------------------------------- feature map
 // grid (ceil(L/16), B*H), 256 threads.  Output phi[bh, i, r] = plain definition.
 template <typename T, int KIND>
@@ -98,7 +129,10 @@ template <typename T, int KIND, int DV>
 __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, const T* __restrict__ v,
                                                        const float* __restrict__ omega,
                                                        const float* __restrict__ kshift, float* __restrict__ part,
-                                                       int H, int L, int m, int d, float s, int seg_len, int n_seg) {
+                                                       int H, int L, int m, int d, float s, int seg_len, int n_seg,
+                                                       const int* __restrict__ pcyc, const int4* __restrict__ pmeta,
+                                                       const float* __restrict__ gate, const float* __restrict__ rdec,
+                                                       float* __restrict__ segdecay) {
     extern __shared__ float sm[];
     const int dp = d + 1;
     float* oms = sm;                       // [m][d+1]
@@ -115,6 +149,11 @@ __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, 
     for (int e = 0; e < DV; ++e) S[e] = 0.f;
     float z = 0.f;
     const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    PermCursor pc;
+    pc.init(pcyc, pmeta, h, m, r, j0);
+    const bool decay = gate || rdec;
+    const float rd = rdec ? rdec[h] : 1.f;
+    float A = 1.f;   // product of the segment's a_j
     for (int t0 = j0; t0 < j1; t0 += kTokTile) {
         const int nt = min(kTokTile, j1 - t0);
         __syncthreads();
@@ -130,18 +169,31 @@ __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, 
         }
         __syncthreads();
         for (int j = 0; j < nt; ++j) {
+            const int row = pc.row(r);
             float p = 0.f;
-            for (int c = 0; c < d; ++c) p = fmaf(oms[r * dp + c], ks[j * d + c], p);
-            const float f = key_feat<KIND>(p, nrm[j], s, kap, r, m);
+            for (int c = 0; c < d; ++c) p = fmaf(oms[row * dp + c], ks[j * d + c], p);
+            const float f = key_feat<KIND>(p, nrm[j], s, kap, row, m);
+            if (decay) {
+                float a, b;
+                token_decay(gate, (size_t)bh * L + t0 + j, rd, &a, &b);
+                const float fb = f * b;
 #pragma unroll
-            for (int e = 0; e < DV; ++e) S[e] = fmaf(f, vs[j * DV + e], S[e]);
-            z += f;
+                for (int e = 0; e < DV; ++e) S[e] = fmaf(a, S[e], fb * vs[j * DV + e]);
+                z = fmaf(a, z, fb);
+                A *= a;
+            } else {
+#pragma unroll
+                for (int e = 0; e < DV; ++e) S[e] = fmaf(f, vs[j * DV + e], S[e]);
+                z += f;
+            }
+            pc.next();
         }
     }
     float* o = part + ((size_t)bh * n_seg + seg) * m * (DV + 1) + (size_t)r * (DV + 1);
 #pragma unroll
     for (int e = 0; e < DV; ++e) o[e] = S[e];
     o[DV] = z;
+    if (segdecay && r == 0) segdecay[(size_t)bh * n_seg + seg] = A;
 }
 
 // ------------------------------------------------- fixed-order segment combines
@@ -170,12 +222,30 @@ __global__ void k_scan_segments(float* __restrict__ part, int n_seg, int n) {
     }
 }
 
+// Causal with a decaying state: prefix[seg+1] = A_seg prefix[seg] + total[seg],
+// A_seg the product of the segment's per-token decays.
+__global__ void k_scan_segments_decay(float* __restrict__ part, const float* __restrict__ segdecay, int n_seg,
+                                      int n) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float* p = part + (size_t)bh * n_seg * n + i;
+    const float* a = segdecay + (size_t)bh * n_seg;
+    float run = 0.f;
+    for (int sg = 0; sg < n_seg; ++sg) {
+        const float t = p[(size_t)sg * n];
+        p[(size_t)sg * n] = run;
+        run = fmaf(a[sg], run, t);
+    }
+}
+
 // ------------------------------------------------------- bidirectional readout
 // grid (ceil(L/16), B*H), 256 threads.  out_i = phi(q_i)^T S / phi(q_i)^T z.
 template <typename T, int KIND>
 __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const float* __restrict__ state,
                                                  const float* __restrict__ omega, T* __restrict__ out,
-                                                 int H, int L, int m, int d, int dv, float s) {
+                                                 int H, int L, int m, int d, int dv, float s,
+                                                 const int* __restrict__ pcyc, const int4* __restrict__ pmeta) {
     constexpr int TQ = 16;
     extern __shared__ float sm[];
     const int sw = dv + 1;
@@ -194,8 +264,11 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
     const float* om = omega + (size_t)h * m * d;
     for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) {
         const int i = idx / m, r = idx - i * m;
+        PermCursor pc;
+        pc.init(pcyc, pmeta, h, m, r, i0 + i);
+        const int row = pc.row(r);
         float p = 0.f;
-        for (int c = 0; c < d; ++c) p = fmaf(__ldg(om + r * d + c), xs[i * d + c], p);
+        for (int c = 0; c < d; ++c) p = fmaf(__ldg(om + row * d + c), xs[i * d + c], p);
         fq[idx] = s * p;
     }
     __syncthreads();
@@ -210,8 +283,12 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
         __syncthreads();
         for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) fq[idx] = expf(fq[idx] - rmax[idx / m]);
     } else {
-        for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x)
-            fq[idx] = query_feat<KIND>(fq[idx], 0.f, idx % m, m);
+        for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) {
+            const int i = idx / m, r = idx - i * m;
+            PermCursor pc;
+            pc.init(pcyc, pmeta, h, m, r, i0 + i);
+            fq[idx] = query_feat<KIND>(fq[idx], 0.f, pc.row(r), m);
+        }
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < nq * sw; idx += blockDim.x) {
@@ -238,7 +315,10 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
                                                         const T* __restrict__ v, const float* __restrict__ omega,
                                                         const float* __restrict__ kshift,
                                                         const float* __restrict__ prefix, T* __restrict__ out,
-                                                        int H, int L, int m, int d, float s, int seg_len, int n_seg) {
+                                                        int H, int L, int m, int d, float s, int seg_len, int n_seg,
+                                                        const int* __restrict__ pcyc, const int4* __restrict__ pmeta,
+                                                        const float* __restrict__ gate,
+                                                        const float* __restrict__ rdec) {
     extern __shared__ float sm[];
     const int dp = d + 1;
     const int nwarps = (m + 31) / 32;
@@ -263,6 +343,10 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
     const int width = (m % 32 != 0 && warp == nwarps - 1) ? 16 : 32;
     const unsigned full = width == 32 ? 0xffffffffu : 0x0000ffffu;
     const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    PermCursor pc;
+    pc.init(pcyc, pmeta, h, m, r, j0);
+    const bool decay = gate || rdec;
+    const float rd = rdec ? rdec[h] : 1.f;
     for (int t0 = j0; t0 < j1; t0 += kTokTile) {
         const int nt = min(kTokTile, j1 - t0);
         __syncthreads();
@@ -280,15 +364,26 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
         }
         __syncthreads();
         for (int j = 0; j < nt; ++j) {
+            const int row = pc.row(r);   // query and key at one position share pi^j
             float pk = 0.f, pq = 0.f;
             for (int c = 0; c < d; ++c) {
-                pk = fmaf(oms[r * dp + c], ks[j * d + c], pk);
-                pq = fmaf(oms[r * dp + c], qs[j * d + c], pq);
+                pk = fmaf(oms[row * dp + c], ks[j * d + c], pk);
+                pq = fmaf(oms[row * dp + c], qs[j * d + c], pq);
             }
-            const float fk = key_feat<KIND>(pk, nrm[j], s, kap, r, m);
+            const float fk = key_feat<KIND>(pk, nrm[j], s, kap, row, m);
+            if (decay) {
+                float a, b;
+                token_decay(gate, (size_t)bh * L + t0 + j, rd, &a, &b);
+                const float fb = fk * b;
 #pragma unroll
-            for (int e = 0; e < DV; ++e) S[e] = fmaf(fk, vs[j * DV + e], S[e]);
-            z += fk;
+                for (int e = 0; e < DV; ++e) S[e] = fmaf(a, S[e], fb * vs[j * DV + e]);
+                z = fmaf(a, z, fb);
+            } else {
+#pragma unroll
+                for (int e = 0; e < DV; ++e) S[e] = fmaf(fk, vs[j * DV + e], S[e]);
+                z += fk;
+            }
+            pc.next();
             float fq;
             if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
                 float mx = s * pq;
@@ -299,7 +394,7 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
                 for (int w = 1; w < nwarps; ++w) mx = fmaxf(mx, wmax[w]);
                 fq = expf(s * pq - mx);
             } else {
-                fq = query_feat<KIND>(s * pq, 0.f, r, m);
+                fq = query_feat<KIND>(s * pq, 0.f, row, m);
             }
             // sum over r of fq * [S | z]: warp shuffles, then across warps in smem.
 #pragma unroll
@@ -339,34 +434,37 @@ favor_status feature_map_t(const Handle& h, const void* x, void* phi, int B, int
 
 template <typename T, int KIND, int DV>
 favor_status state_t(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan& p,
-                     cudaStream_t st) {
+                     const RelposArgs& rp, cudaStream_t st) {
     const size_t smem = (size_t)(h.m * (h.d + 1) + kTokTile * h.d + kTokTile * DV + kTokTile) * sizeof(float);
     auto kern = k_segment_state<T, KIND, DV>;
     set_smem(kern, smem);
     dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_STATE, st);
     kern<<<grid, h.m, smem, st>>>((const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial, h.H, L, h.m,
-                                  h.d, h.s, p.seg_tiles * 128, p.n_seg);
+                                  h.d, h.s, p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta, rp.gate, rp.rdec,
+                                  rp.segdecay);
     count_launch();
     return check_launch("segment state kernel");
 }
 
 template <typename T, int KIND>
-favor_status readout_t(const Handle& h, const void* q, void* out, int BH, int L, cudaStream_t st) {
+favor_status readout_t(const Handle& h, const void* q, void* out, int BH, int L, cudaStream_t st,
+                       const RelposArgs& rp = RelposArgs()) {
     const int sw = h.dv + 1;
     const size_t smem = (size_t)(h.m * sw + 16 * h.m + 16 * h.d + 16 * sw + 16) * sizeof(float);
     auto kern = k_readout<T, KIND>;
     set_smem(kern, smem);
     dim3 grid((L + 15) / 16, BH);
     ProfScope ps(h, PROF_READOUT, st);
-    kern<<<grid, 256, smem, st>>>((const T*)q, h.ws_state, h.omega_f32, (T*)out, h.H, L, h.m, h.d, h.dv, h.s);
+    kern<<<grid, 256, smem, st>>>((const T*)q, h.ws_state, h.omega_f32, (T*)out, h.H, L, h.m, h.d, h.dv, h.s,
+                                  rp.cyc, rp.meta);
     count_launch();
     return check_launch("readout kernel");
 }
 
 template <typename T, int KIND, int DV>
 favor_status causal_t(const Handle& h, const void* q, const void* k, const void* v, void* out, int BH, int L,
-                      const SegPlan& p, cudaStream_t st) {
+                      const SegPlan& p, const RelposArgs& rp, cudaStream_t st) {
     const int nwarps = (h.m + 31) / 32;
     const size_t smem = (size_t)(h.m * (h.d + 1) + 2 * kTokTile * h.d + kTokTile * DV + kTokTile +
                                  nwarps * (DV + 1) + nwarps) * sizeof(float);
@@ -375,7 +473,8 @@ favor_status causal_t(const Handle& h, const void* q, const void* k, const void*
     dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_CAUSAL, st);
     kern<<<grid, h.m, smem, st>>>((const T*)q, (const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial,
-                                  (T*)out, h.H, L, h.m, h.d, h.s, p.seg_tiles * 128, p.n_seg);
+                                  (T*)out, h.H, L, h.m, h.d, h.s, p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta,
+                                  rp.gate, rp.rdec);
     count_launch();
     return check_launch("causal segment kernel");
 }
@@ -419,16 +518,16 @@ favor_status dispatch3(const Handle& h, A... a) {
 template <typename T, int KIND, int DV>
 struct StateF {
     static favor_status run(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan* p,
-                            cudaStream_t st) {
-        return state_t<T, KIND, DV>(h, k, v, BH, L, *p, st);
+                            const RelposArgs* rp, cudaStream_t st) {
+        return state_t<T, KIND, DV>(h, k, v, BH, L, *p, *rp, st);
     }
 };
 
 template <typename T, int KIND, int DV>
 struct CausalF {
     static favor_status run(const Handle& h, const void* q, const void* k, const void* v, void* out, int BH,
-                            int L, const SegPlan* p, cudaStream_t st) {
-        return causal_t<T, KIND, DV>(h, q, k, v, out, BH, L, *p, st);
+                            int L, const SegPlan* p, const RelposArgs* rp, cudaStream_t st) {
+        return causal_t<T, KIND, DV>(h, q, k, v, out, BH, L, *p, *rp, st);
     }
 };
 
@@ -460,29 +559,48 @@ favor_status simt_bidir(const Handle& h, const void* q, const void* k, const voi
                         cudaStream_t st) {
     const int BH = B * h.H;
     SegPlan p = plan_segments(BH, L, h.num_sms);
-    favor_status s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, st);
+    RelposArgs rp;   // bidirectional: the permutation only (r = 1)
+    rp.cyc = h.perm_cyc;
+    rp.meta = h.perm_meta;
+    favor_status s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, (const RelposArgs*)&rp, st);
     if (s != FAVOR_OK) return s;
     s = launch_reduce_segments(h, BH, p.n_seg, st);
     if (s != FAVOR_OK) return s;
-    FAVOR_KIND_DISPATCH(h, readout_t, h, q, out, BH, L, st);
+    FAVOR_KIND_DISPATCH(h, readout_t, h, q, out, BH, L, st, rp);
 }
 
 favor_status simt_causal(const Handle& h, const void* q, const void* k, const void* v, void* out, int B, int L,
-                         cudaStream_t st) {
+                         cudaStream_t st, const float* gate) {
     const int BH = B * h.H;
     SegPlan p = plan_segments(BH, L, h.num_sms);
+    RelposArgs rp;
+    rp.cyc = h.perm_cyc;
+    rp.meta = h.perm_meta;
+    rp.gate = gate;
+    rp.rdec = h.relpos_r;
+    const bool decay = gate || h.relpos_r;
+    rp.segdecay = decay ? h.ws_segdecay : nullptr;
     favor_status s = FAVOR_OK;
     if (p.n_seg > 1) {
-        s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, st);
+        s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, (const RelposArgs*)&rp, st);
         if (s != FAVOR_OK) return s;
-        s = launch_scan_segments(h, BH, p.n_seg, st);
+        if (decay) {
+            const int n = h.m * (h.dv + 1);
+            dim3 grid((n + 255) / 256, BH);
+            ProfScope ps(h, PROF_COMBINE, st);
+            k_scan_segments_decay<<<grid, 256, 0, st>>>(h.ws_partial, h.ws_segdecay, p.n_seg, n);
+            count_launch();
+            s = check_launch("segment scan kernel");
+        } else {
+            s = launch_scan_segments(h, BH, p.n_seg, st);
+        }
     } else {
         s = cudaMemsetAsync(h.ws_partial, 0, (size_t)BH * h.m * (h.dv + 1) * sizeof(float), st) == cudaSuccess
                 ? FAVOR_OK
                 : set_error(FAVOR_ERR_CUDA, "cudaMemsetAsync failed");
     }
     if (s != FAVOR_OK) return s;
-    return dispatch3<CausalF>(h, q, k, v, out, BH, L, (const SegPlan*)&p, st);
+    return dispatch3<CausalF>(h, q, k, v, out, BH, L, (const SegPlan*)&p, (const RelposArgs*)&rp, st);
 }
 
 // ------------------------------------------------------- stateful calls
@@ -528,7 +646,8 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
                                                      const T* __restrict__ v, T* __restrict__ out,
                                                      float* __restrict__ state, const float* __restrict__ omega,
                                                      const float* __restrict__ kshift, int H, int Tn, int m, int d,
-                                                     int dv, float s, int omega_in_smem) {
+                                                     int dv, float s, int omega_in_smem,
+                                                     const float* __restrict__ gate) {
     extern __shared__ float sm[];
     const int dp = dv + 1, wp = d + 1;
     float* S = sm;             // [m][dv+1]
@@ -596,8 +715,14 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
             const float fk = inv_sqrt_m * key_feat<KIND>(pk, nk, s, kap, tid, m);
             const float f = query_feat<KIND>(qx, mx, tid, m);   // mx: a per-query shift, cancels
             float* Sr = S + tid * dp;
-            for (int e = 0; e < dv; ++e) Sr[e] = fmaf(fk, xv[e], Sr[e]);
-            Sr[dv] += fk;
+            if (gate) {   // RFA-Gate: S = g S + (1 - g) phi(k) [v 1]^T
+                const float g = gate[row], fb = (1.f - g) * fk;
+                for (int e = 0; e < dv; ++e) Sr[e] = fmaf(g, Sr[e], fb * xv[e]);
+                Sr[dv] = fmaf(g, Sr[dv], fb);
+            } else {
+                for (int e = 0; e < dv; ++e) Sr[e] = fmaf(fk, xv[e], Sr[e]);
+                Sr[dv] += fk;
+            }
             fq[tid] = f;
         }
         __syncthreads();
@@ -619,7 +744,7 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
 
 template <typename T, int KIND>
 favor_status causal_step_t(const Handle& h, const void* q, const void* k, const void* v, void* out, float* state,
-                           int BH, int Tn, cudaStream_t st) {
+                           int BH, int Tn, cudaStream_t st, const float* gate) {
     const size_t base = (size_t)(h.m * (h.dv + 1) + 2 * h.d + h.dv + h.m + (h.dv + 1) + 32) * sizeof(float);
     const size_t wbytes = (size_t)h.m * (h.d + 1) * sizeof(float);
     const int in_smem = base + wbytes <= 200 * 1024 ? 1 : 0;
@@ -628,7 +753,7 @@ favor_status causal_step_t(const Handle& h, const void* q, const void* k, const 
     set_smem(kern, smem);
     ProfScope ps(h, PROF_CAUSAL, st);
     kern<<<BH, 256, smem, st>>>((const T*)q, (const T*)k, (const T*)v, (T*)out, state, h.omega_f32, h.kshift, h.H,
-                                Tn, h.m, h.d, h.dv, h.s, in_smem);
+                                Tn, h.m, h.d, h.dv, h.s, in_smem, gate);
     count_launch();
     return check_launch("causal step kernel");
 }
@@ -637,14 +762,16 @@ favor_status causal_step_t(const Handle& h, const void* q, const void* k, const 
 
 favor_status simt_state_partials(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan& p,
                                  cudaStream_t st) {
-    return dispatch3<StateF>(h, k, v, BH, L, &p, st);
+    const RelposArgs rp;
+    return dispatch3<StateF>(h, k, v, BH, L, &p, &rp, st);
 }
 
 favor_status simt_kv_state(const Handle& h, const void* k, const void* v, float* state, int B, int L,
                            cudaStream_t st) {
     const int BH = B * h.H;
     SegPlan p = plan_segments(BH, L, h.num_sms);
-    favor_status s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, st);
+    const RelposArgs rp;
+    favor_status s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, &rp, st);
     if (s != FAVOR_OK) return s;
     const int n = h.m * (h.dv + 1);
     dim3 grid((n + 255) / 256, BH);
@@ -664,9 +791,9 @@ favor_status simt_attn_from_state(const Handle& proto, const void* q, const floa
 }
 
 favor_status simt_causal_step(const Handle& h, const void* q, const void* k, const void* v, void* out, float* state,
-                              int B, int Tn, cudaStream_t st) {
+                              int B, int Tn, cudaStream_t st, const float* gate) {
     const int BH = B * h.H;
-    FAVOR_KIND_DISPATCH(h, causal_step_t, h, q, k, v, out, state, BH, Tn, st);
+    FAVOR_KIND_DISPATCH(h, causal_step_t, h, q, k, v, out, state, BH, Tn, st, gate);
 }
 
 // ------------------------------------------------ bidirectional call, fixed scratch
@@ -761,7 +888,8 @@ favor_status simt_bidir_fixed_scratch(const Handle& proto, const void* q, const 
     count_launch();
     s = check_launch("key shift kernel");
     if (s != FAVOR_OK) return s;
-    s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, st);
+    const RelposArgs rp;
+    s = dispatch3<StateF>(h, k, v, BH, L, (const SegPlan*)&p, &rp, st);
     if (s != FAVOR_OK) return s;
     s = launch_reduce_segments(h, BH, p.n_seg, st);
     if (s != FAVOR_OK) return s;

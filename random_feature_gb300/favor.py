@@ -26,6 +26,7 @@ __all__ = [
     "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc",
     "favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
     "favor_attn_bidir_backward", "favor_attn_causal_backward",
+    "favor_attn_causal_gated", "favor_attn_causal_step_gated", "favor_set_relpos",
 ]
 
 FAVOR_OK, FAVOR_ERR_INVALID_ARG, FAVOR_ERR_UNSUPPORTED, FAVOR_ERR_NOMEM, FAVOR_ERR_CUDA = range(5)
@@ -40,7 +41,8 @@ EXPORTED_SYMBOLS = ("favor_create", "favor_feature_map", "favor_attn_bidir", "fa
                     "favor_profile_enable", "favor_profile_reset", "favor_profile_read", "favor_profile_slots",
                     "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc",
                     "favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
-                    "favor_attn_bidir_backward", "favor_attn_causal_backward")
+                    "favor_attn_bidir_backward", "favor_attn_causal_backward",
+                    "favor_attn_causal_gated", "favor_attn_causal_step_gated", "favor_set_relpos")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -102,8 +104,12 @@ def lib() -> ctypes.CDLL:
         L.favor_attn_causal_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, vp]
         for fn in ("favor_attn_bidir_backward", "favor_attn_causal_backward"):
             getattr(L, fn).argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp]
+        L.favor_attn_causal_gated.argtypes = [vp, vp, vp, vp, vp, vp, i, i, vp]
+        L.favor_attn_causal_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, vp]
+        L.favor_set_relpos.argtypes = [vp, vp, vp]
         for fn in ("favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
-                   "favor_attn_bidir_backward", "favor_attn_causal_backward"):
+                   "favor_attn_bidir_backward", "favor_attn_causal_backward", "favor_attn_causal_gated",
+                   "favor_attn_causal_step_gated", "favor_set_relpos"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -210,6 +216,24 @@ def favor_attn_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, stream=None) 
                                             int(B), int(L), _stream(stream, q)), "favor_attn_causal_backward")
 
 
+def favor_attn_causal_gated(h, q, k, v, gate, out, B, L, stream=None) -> None:
+    _check(lib().favor_attn_causal_gated(h, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), int(B), int(L),
+                                         _stream(stream, q)), "favor_attn_causal_gated")
+
+
+def favor_attn_causal_step_gated(h, q, k, v, gate, out, state, B, T, stream=None) -> None:
+    _check(lib().favor_attn_causal_step_gated(h, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), _ptr(state),
+                                              int(B), int(T), _stream(stream, q)), "favor_attn_causal_step_gated")
+
+
+def favor_set_relpos(h, perm=None, r=None) -> None:
+    """PermuteFormer setting: host int [H, m] permutations (or None) and host float [H] decays (or None)."""
+    pa = None if perm is None else np.ascontiguousarray(perm, dtype=np.int32)
+    ra = None if r is None else np.ascontiguousarray(r, dtype=np.float32)
+    _check(lib().favor_set_relpos(h, None if pa is None else pa.ctypes.data, None if ra is None else ra.ctypes.data),
+           "favor_set_relpos")
+
+
 def favor_destroy(h) -> None:
     _check(lib().favor_destroy(h), "favor_destroy")
 
@@ -303,6 +327,37 @@ class Favor:
         fn = favor_attn_causal_backward if causal else favor_attn_bidir_backward
         fn(self.handle, q, k, v, dout, dq, dk, dv, B, L, stream)
         return dq, dk, dv
+
+    def attn_causal_gated(self, q, k, v, gate, out=None, stream=None):
+        """RFA-Gate causal attention; gate is a CUDA float32 [B, H, L] tensor."""
+        import torch
+        B, _, L, _ = q.shape
+        self._chk(q, B, L, self.d, "q")
+        self._chk(k, B, L, self.d, "k")
+        self._chk(v, B, L, self.dv, "v")
+        if tuple(gate.shape) != (B, self.H, L) or gate.dtype != torch.float32 or not gate.is_cuda \
+                or not gate.is_contiguous():
+            raise ValueError(f"gate: expected contiguous CUDA float32 [{B},{self.H},{L}]")
+        out = self._new(q, B, L, self.dv, out)
+        favor_attn_causal_gated(self.handle, q, k, v, gate, out, B, L, stream)
+        return out
+
+    def causal_step_gated(self, q, k, v, gate, state, out=None, stream=None):
+        import torch
+        B, _, T, _ = q.shape
+        self._chk(q, B, T, self.d, "q")
+        self._chk(k, B, T, self.d, "k")
+        self._chk(v, B, T, self.dv, "v")
+        self._chk_state(state, B)
+        if tuple(gate.shape) != (B, self.H, T) or gate.dtype != torch.float32 or not gate.is_cuda \
+                or not gate.is_contiguous():
+            raise ValueError(f"gate: expected contiguous CUDA float32 [{B},{self.H},{T}]")
+        out = self._new(q, B, T, self.dv, out)
+        favor_attn_causal_step_gated(self.handle, q, k, v, gate, out, state, B, T, stream)
+        return out
+
+    def set_relpos(self, perm=None, r=None):
+        favor_set_relpos(self.handle, perm, r)
 
     def new_state(self, B):
         """A zero (empty) state [B, H, m, dv+1] float32 on the current CUDA device."""
