@@ -60,6 +60,8 @@ def parse():
                     help="one-token causal steps timed for the decode line (0 = skip)")
     ap.add_argument("--backward-steps", type=int, default=2,
                     help="timed repetitions of the backward line (bidir + causal gradients; 0 = skip)")
+    ap.add_argument("--variant-steps", type=int, default=2,
+                    help="timed repetitions of each feature-variant / relative-position call (0 = skip)")
     ap.add_argument("--e2e-groups", type=int, default=4,
                     help="head groups pipelined over upload / compute / download streams in the e2e leg")
     ap.add_argument("--cpu-heads", type=int, default=2, help="heads of the workload in the CPU oracle sample")
@@ -379,6 +381,57 @@ def run_ours(args):
                     "config": f"{w.name}: B={w.B} H={w.H} L={w.L}, dq/dk/dv of one bidirectional and one "
                               f"causal call, positive features, dO ~ N(0,1)"}
 
+    # Feature variants and relative positions on the same workload, one line each:
+    # hyperbolic features (tensor cores), trigonometric features, RFA-Gate gated
+    # causal and PermuteFormer (CUDA cores).  Roofline: the forward's flops per
+    # token*head (4md + 4m(dv+1)) against the tensor peak (tensor-core calls) or
+    # the FP32 FFMA peak (CUDA-core calls).
+    variants = None
+    if args.variant_steps > 0:
+        variants = {}
+        T = w.B * w.H * w.L
+        fl = 4 * w.m * w.d + 4 * w.m * (w.dv + 1)
+        vmhz = sampler.samples[-1][1] if sampler.samples else peaks["sm_max_mhz"]
+        fp32_peak = GB300_SMS * 128 * 2 * vmhz * 1e6
+        gate = torch.rand((w.B, w.H, w.L), device=dev, dtype=torch.float32) * 0.2 + 0.8
+        rng_v = np.random.default_rng(1)
+        perm = np.stack([rng_v.permutation(w.m) for _ in range(w.H)]).astype(np.int32)
+        rdec = np.full(w.H, 0.999, np.float32)
+        half = np.ascontiguousarray(omega[:, : w.m // 2])
+        cases = [("hyperbolic", "softmax_hyp", half, None), ("trigonometric", "softmax_trig", half, None),
+                 ("rfa_gate", "softmax_pos", omega, "gate"), ("permuteformer", "softmax_pos", omega, "relpos")]
+        vout = torch.empty_like(vd)
+        for name, kind, om_, extra in cases:
+            hv = R.Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, om_, w.data_scale, w.B, w.L)
+            if extra == "relpos":
+                hv.set_relpos(perm, rdec)
+            modes = ("causal",) if extra == "gate" else ("bidir", "causal")
+            res = {}
+            for mode in modes:
+                def call():
+                    if extra == "gate":
+                        hv.attn_causal_gated(qd, kd, vd, gate, out=vout, stream=stream)
+                    else:
+                        hv.attn(qd, kd, vd, causal=(mode == "causal"), out=vout, stream=stream)
+                call()
+                torch.cuda.synchronize(dev)
+                c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                for _ in range(args.variant_steps):
+                    call()
+                c1.record(stream)
+                torch.cuda.synchronize(dev)
+                ms = c0.elapsed_time(c1) / args.variant_steps
+                tc = kind == "softmax_hyp" and w.dtype == "bf16" and (w.d, w.dv, w.m) == (64, 64, 256)
+                pk = peaks["bf16_tflops_sustained"] * 1e12 if tc else fp32_peak
+                res[mode] = {"ms": ms, "value": T / (ms / 1e3), "unit": UNIT,
+                             "path": "tensor cores" if tc else "CUDA cores",
+                             "roofline": {"bound": "tensor" if tc else "alu",
+                                          "achieved": fl * T / (ms / 1e3) / 1e12, "peak": pk / 1e12,
+                                          "unit": "TFLOP/s", "frac": fl * T / (ms / 1e3) / pk}}
+            variants[name] = res
+            hv.close()
+
     # End to end through the public API: pinned host inputs in, outputs back, every
     # step.  The heads are split into groups, one library handle per group (its
     # slice of omega), and three streams overlap the upload of group g+1, the four
@@ -502,7 +555,8 @@ def run_ours(args):
                                    f"calls per step: bidir+causal x softmax_pos+relu",
                        "global_batch": w.B * world, "seq_len": w.L, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (Q,K,V 384 MB per replica)"},
-            "clocks": clocks, "e2e": e2e, "decode": decode, "backward": backward, "gpu_launches": launches,
+            "clocks": clocks, "e2e": e2e, "decode": decode, "backward": backward, "variants": variants,
+            "gpu_launches": launches,
             "roofline": roofline,
             "roofline_all": roofline_all, "kernels": kernels, "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
