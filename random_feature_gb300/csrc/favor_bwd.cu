@@ -31,17 +31,10 @@
 #include <cmath>
 
 #include "favor_internal.h"
+#include "simt_common.cuh"
 
 namespace favor {
 namespace {
-
-template <typename T> __device__ __forceinline__ float ldb(const T* p);
-template <> __device__ __forceinline__ float ldb<float>(const float* p) { return *p; }
-template <> __device__ __forceinline__ float ldb<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-
-template <typename T> __device__ __forceinline__ void stb(T* p, float x);
-template <> __device__ __forceinline__ void stb<float>(float* p, float x) { *p = x; }
-template <> __device__ __forceinline__ void stb<__nv_bfloat16>(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
 template <int DV>
 struct BwdShape {
@@ -49,18 +42,6 @@ struct BwdShape {
     static constexpr int DVP = DV + 4;               // padded [V 1] / D row (16-byte rows)
     static constexpr int W = DV + 1;                 // state row width
 };
-
-__device__ __forceinline__ float warp_sum(float a) {
-    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-    return a;
-}
-__device__ __forceinline__ float warp_max(float a) {
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    return a;
-}
-__device__ __forceinline__ float dot4(float4 a, float4 b) {
-    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
-}
 
 // Shared-memory plan (floats) of one pass; every buffer starts 16-byte aligned.
 struct BwdSmem {
@@ -90,64 +71,6 @@ __host__ __device__ inline BwdSmem bwd_smem(int TT, int DVP, int W, int m, int d
     p.kn = o; o += al4(TT);
     p.total = o;
     return p;
-}
-
-// Projections s*(omega_r . x_j) for j < TT into buf[j][r] (row stride m+1).
-template <int TT>
-__device__ __forceinline__ void project_tile(const float* __restrict__ om, const float* xs, float* buf, int r, int m,
-                                             int d, float s) {
-    float p[TT];
-#pragma unroll
-    for (int j = 0; j < TT; ++j) p[j] = 0.f;
-    const float4* w4 = reinterpret_cast<const float4*>(om + (size_t)r * d);
-    const float4* x4 = reinterpret_cast<const float4*>(xs);
-    const int d4 = d >> 2;
-#pragma unroll 1
-    for (int c4 = 0; c4 < d4; ++c4) {
-        const float4 w = __ldg(w4 + c4);
-#pragma unroll
-        for (int j = 0; j < TT; ++j) p[j] += dot4(w, x4[j * d4 + c4]);
-    }
-#pragma unroll
-    for (int j = 0; j < TT; ++j) buf[j * (m + 1) + r] = s * p[j];
-}
-
-// Stage rows [t0, t0+nt) of a [BH, L, w] tensor into dst[TT][stride] as fp32;
-// rows past nt and columns [w, stride) are zero, column w is `one_col` if >= 0.
-template <typename T>
-__device__ __forceinline__ void stage_rows(const T* __restrict__ src, float* dst, int t0, int nt, int TT, int w,
-                                           int stride, float one_col) {
-    for (int idx = threadIdx.x; idx < TT * stride; idx += blockDim.x) {
-        const int j = idx / stride, c = idx - j * stride;
-        float x = 0.f;
-        if (j < nt) {
-            if (c < w) x = ldb(src + (size_t)(t0 + j) * w + c);
-            else if (c == w && one_col >= 0.f) x = one_col;
-        }
-        dst[idx] = x;
-    }
-}
-
-// Squared key norms kn_j of a staged key tile, one warp per token.
-__device__ __forceinline__ void key_norms(const float* ys, float* kn, int TT, int d) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    for (int j = warp; j < TT; j += nw) {
-        float a = 0.f;
-        for (int c = lane; c < d; c += 32) a = fmaf(ys[j * d + c], ys[j * d + c], a);
-        a = warp_sum(a);
-        if (lane == 0) kn[j] = a;
-    }
-}
-
-// Row max of the raw query projections (positive features), one warp per token.
-__device__ __forceinline__ void row_shift(const float* fq, float* cq, int TT, int nt, int m) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    for (int j = warp; j < TT; j += nw) {
-        float mx = -INFINITY;
-        for (int r = lane; r < m; r += 32) mx = fmaxf(mx, fq[j * (m + 1) + r]);
-        mx = warp_max(mx);
-        if (lane == 0) cq[j] = j < nt ? mx : 0.f;
-    }
 }
 
 // D rows from dO (in place in dd), den and go: D = [dO/den, -go/den, 0...].
@@ -191,15 +114,15 @@ __device__ __forceinline__ void grad_inputs(const float* g, const float* xs, con
         T* o = dst + (size_t)(t0 + j) * d + 4 * c4;
         if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
             const float t = s * gsum;
-            stb(o + 0, s * fmaf(-t, xj[0], a.x));
-            stb(o + 1, s * fmaf(-t, xj[1], a.y));
-            stb(o + 2, s * fmaf(-t, xj[2], a.z));
-            stb(o + 3, s * fmaf(-t, xj[3], a.w));
+            stf(o + 0, s * fmaf(-t, xj[0], a.x));
+            stf(o + 1, s * fmaf(-t, xj[1], a.y));
+            stf(o + 2, s * fmaf(-t, xj[2], a.z));
+            stf(o + 3, s * fmaf(-t, xj[3], a.w));
         } else {
-            stb(o + 0, s * a.x);
-            stb(o + 1, s * a.y);
-            stb(o + 2, s * a.z);
-            stb(o + 3, s * a.w);
+            stf(o + 0, s * a.x);
+            stf(o + 1, s * a.y);
+            stf(o + 2, s * a.z);
+            stf(o + 3, s * a.w);
         }
     }
 }
@@ -493,7 +416,7 @@ __global__ void __launch_bounds__(256) k_bwd_key(const T* __restrict__ q, const 
             for (int rr = 0; rr < m; ++rr) a = fmaf(fk[j * MP + rr], rs[rr * W + e], a);
             if (CAUSAL)
                 for (int i = j; i < TT; ++i) a = fmaf(aa[j * (TT + 1) + i], dd[i * DVP + e], a);
-            stb(dvv + (row0 + t0 + j) * DV + e, a);
+            stf(dvv + (row0 + t0 + j) * DV + e, a);
         }
         __syncthreads();
         if (own) {

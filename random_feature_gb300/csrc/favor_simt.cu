@@ -14,81 +14,12 @@
 #include <mutex>
 
 #include "favor_internal.h"
+#include "simt_common.cuh"
 
 namespace favor {
 namespace {
 
-template <typename T> __device__ __forceinline__ float ldf(const T* p);
-template <> __device__ __forceinline__ float ldf<float>(const float* p) { return *p; }
-template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-
-template <typename T> __device__ __forceinline__ void stf(T* p, float x);
-template <> __device__ __forceinline__ void stf<float>(float* p, float x) { *p = x; }
-template <> __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
-
 constexpr int kTokTile = 32;  // tokens staged per shared-memory tile in the state/causal kernels
-
-// Feature values by computation kind, from the unscaled projection p = omega_r . x
-// (r the feature index of m).  The hyperbolic map runs as the positive kind on
-// the mirrored rows [omega; -omega].  The trigonometric kind holds the rows
-// [omega; omega]: features r < m/2 take sin, the others cos, of the same
-// projection, and its key features carry h(y) = exp(||y||^2/2) with no shift.
-template <int KIND>
-__device__ __forceinline__ float key_feat(float p, float nrm, float s, float kap, int r, int m) {
-    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) return expf(s * p - 0.5f * s * s * nrm - kap);
-    if (KIND == FAVOR_KERNEL_RELU) return fmaxf(s * p, 0.f);
-    const float a = s * p;
-    return (r < (m >> 1) ? sinf(a) : cosf(a)) * expf(0.5f * s * s * nrm);
-}
-
-// Query features up to a factor common to the row (the shift mx, m^-1/2, and
-// for the trigonometric kind h(x)): they cancel in num / den.
-template <int KIND>
-__device__ __forceinline__ float query_feat(float sp, float mx, int r, int m) {
-    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) return expf(sp - mx);
-    if (KIND == FAVOR_KERNEL_RELU) return fmaxf(sp, 0.f);
-    return r < (m >> 1) ? sinf(sp) : cosf(sp);
-}
-
-// The plain definition (favor_feature_map).
-template <int KIND>
-__device__ __forceinline__ float plain_feat(float p, float nrm, float s, int r, int m) {
-    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) return expf(s * p - 0.5f * s * s * nrm) * rsqrtf((float)m);
-    if (KIND == FAVOR_KERNEL_RELU) return fmaxf(s * p, 0.f) * rsqrtf((float)m);
-    const float a = s * p;
-    return (r < (m >> 1) ? sinf(a) : cosf(a)) * expf(0.5f * s * s * nrm) * rsqrtf((float)(m >> 1));
-}
-
-// Position-dependent feature order of PermuteFormer: at position j the slot r
-// holds feature pi^j(r).  Per head, the permutation's cycles are listed in
-// cyc[h*m + ...]; meta[h*m + r] = (start of r's cycle, its length, r's place in
-// it, 0), so pi^j(r) = cyc[h*m + start + (place + j) mod length].
-struct PermCursor {
-    const int* cyc;   // null: identity
-    int base, len, idx;
-    __device__ __forceinline__ void init(const int* c, const int4* meta, int h, int m, int r, long long j) {
-        cyc = c;
-        base = 0; len = 1; idx = 0;
-        if (c) {
-            const int4 mt = meta[(size_t)h * m + r];
-            base = h * m + mt.x;
-            len = mt.y;
-            idx = (int)((mt.z + j) % mt.y);
-        }
-    }
-    __device__ __forceinline__ int row(int r) const { return cyc ? cyc[base + idx] : r; }
-    __device__ __forceinline__ void next() {
-        if (cyc && ++idx == len) idx = 0;
-    }
-};
-
-// Per-token decay of a causal state: S_j = a_j S_{j-1} + b_j phi(k_j) [v_j 1]^T
-// with a_j = r_h g_j and b_j = 1 - g_j (RFA-Gate gates g, PermuteFormer r).
-__device__ __forceinline__ void token_decay(const float* gate, size_t gidx, float rd, float* a, float* b) {
-    const float g = gate ? gate[gidx] : 0.f;
-    *a = rd * (gate ? g : 1.f);
-    *b = gate ? 1.f - g : 1.f;
-}
 
 // ---------------------------------------------------------------- feature map
 // grid (ceil(L/16), B*H), 256 threads.  Output phi[bh, i, r] = plain definition.
@@ -122,9 +53,25 @@ __global__ void __launch_bounds__(256) k_feature_map(const T* __restrict__ x, T*
     }
 }
 
+// Tiled shape of the CUDA-core segment kernels: tokens per tile and padded
+// [v 1] / state row widths (16-byte rows for float4 access).
+template <int DV>
+struct FwdShape {
+    static constexpr int TT = DV >= 128 ? 16 : 32;
+    static constexpr int DVP = DV + 4;
+    static constexpr int W = DV + 1;
+};
+
+__host__ __device__ inline int al4f(int n) { return (n + 3) & ~3; }
+
 // ------------------------------------------------------- per-segment key state
-// grid (n_seg, B*H), m threads.  Thread r accumulates S[r, 0:dv] and z[r] over
-// its segment's keys and writes them to part[(bh*n_seg + seg)][r][0:dv+1].
+// grid (n_seg, B*H), 256 threads.  Per tile of TT keys, thread `row` projects
+// its omega row on every key (float4 row against broadcast key rows), takes
+// the key feature and places it in slot pi^-j(row) (PermuteFormer; the
+// identity otherwise); thread r then folds slot r's features into its state
+// row in token order: S = a_j S + b_j f_j [v_j 1] (a = b = 1 without decay),
+// and writes it to part[(bh*n_seg + seg)][r][0:dv+1].  With decay the product
+// of the segment's a_j goes to segdecay[bh*n_seg + seg].
 template <typename T, int KIND, int DV>
 __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, const T* __restrict__ v,
                                                        const float* __restrict__ omega,
@@ -133,67 +80,85 @@ __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, 
                                                        const int* __restrict__ pcyc, const int4* __restrict__ pmeta,
                                                        const float* __restrict__ gate, const float* __restrict__ rdec,
                                                        float* __restrict__ segdecay) {
-    extern __shared__ float sm[];
-    const int dp = d + 1;
-    float* oms = sm;                       // [m][d+1]
-    float* ks = oms + m * dp;              // [kTokTile][d]
-    float* vs = ks + kTokTile * d;         // [kTokTile][DV]
-    float* nrm = vs + kTokTile * DV;       // [kTokTile]
+    using F = FwdShape<DV>;
+    constexpr int TT = F::TT, DVP = F::DVP, W = F::W;
+    extern __shared__ __align__(16) float sm[];
+    const int MP = m + 1;
+    float* ys = sm;                          // [TT][d]
+    float* cs = ys + TT * d;                 // [TT][DVP]: v, 1, 0...
+    float* fk = cs + TT * DVP;               // [TT][m+1] key features by slot
+    float* kn = fk + al4f(TT * MP);          // [TT]
+    float* ga = kn + TT;                     // [TT] a_j
+    float* gb = ga + TT;                     // [TT] b_j
     const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
     const int r = threadIdx.x;
-    for (int idx = threadIdx.x; idx < m * d; idx += blockDim.x)
-        oms[(idx / d) * dp + idx % d] = omega[(size_t)h * m * d + idx];
+    const bool own = r < m;
+    const float* om = omega + (size_t)h * m * d;
     const float kap = kshift[h];
-    float S[DV];
-#pragma unroll
-    for (int e = 0; e < DV; ++e) S[e] = 0.f;
-    float z = 0.f;
-    const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
-    PermCursor pc;
-    pc.init(pcyc, pmeta, h, m, r, j0);
+    const size_t row0 = (size_t)bh * L;
     const bool decay = gate || rdec;
     const float rd = rdec ? rdec[h] : 1.f;
-    float A = 1.f;   // product of the segment's a_j
-    for (int t0 = j0; t0 < j1; t0 += kTokTile) {
-        const int nt = min(kTokTile, j1 - t0);
+    float st[W];
+#pragma unroll
+    for (int e = 0; e < W; ++e) st[e] = 0.f;
+    float A = 1.f;
+    const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    PermCursor pc;
+    pc.init_inv(pcyc, pmeta, h, m, own ? r : 0, j0);
+    for (int t0 = j0; t0 < j1; t0 += TT) {
+        const int nt = min(TT, j1 - t0);
         __syncthreads();
-        for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x)
-            ks[idx] = ldf(k + ((size_t)bh * L + t0) * d + idx);
-        for (int idx = threadIdx.x; idx < nt * DV; idx += blockDim.x)
-            vs[idx] = ldf(v + ((size_t)bh * L + t0) * DV + idx);
+        stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
+        stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+        if (decay)
+            for (int j = threadIdx.x; j < TT; j += blockDim.x) {
+                float a = 1.f, b = 0.f;
+                if (j < nt) token_decay(gate, row0 + t0 + j, rd, &a, &b);
+                ga[j] = a;
+                gb[j] = b;
+            }
         __syncthreads();
-        for (int j = threadIdx.x; j < nt; j += blockDim.x) {   // blockDim may be below kTokTile
-            float a = 0.f;
-            for (int c = 0; c < d; ++c) a = fmaf(ks[j * d + c], ks[j * d + c], a);
-            nrm[j] = a;
+        key_norms(ys, kn, TT, d);
+        __syncthreads();
+        if (own) {
+            float p[TT];
+            project_regs<TT>(om, ys, r, d, p);
+#pragma unroll
+            for (int j = 0; j < TT; ++j) {
+                fk[j * MP + pc.row(r)] = j < nt ? key_feat<KIND>(p[j], kn[j], s, kap, r, m) : 0.f;
+                pc.prev();
+            }
         }
         __syncthreads();
-        for (int j = 0; j < nt; ++j) {
-            const int row = pc.row(r);
-            float p = 0.f;
-            for (int c = 0; c < d; ++c) p = fmaf(oms[row * dp + c], ks[j * d + c], p);
-            const float f = key_feat<KIND>(p, nrm[j], s, kap, row, m);
-            if (decay) {
-                float a, b;
-                token_decay(gate, (size_t)bh * L + t0 + j, rd, &a, &b);
-                const float fb = f * b;
+        if (own) {
+#pragma unroll 1
+            for (int j = 0; j < TT; ++j) {
+                const float f = fk[j * MP + r];
+                const float4* cj = reinterpret_cast<const float4*>(cs + j * DVP);
+                float a = 1.f, fb = f;
+                if (decay) {
+                    a = ga[j];
+                    fb = f * gb[j];
+                    A *= a;
+                }
 #pragma unroll
-                for (int e = 0; e < DV; ++e) S[e] = fmaf(a, S[e], fb * vs[j * DV + e]);
-                z = fmaf(a, z, fb);
-                A *= a;
-            } else {
-#pragma unroll
-                for (int e = 0; e < DV; ++e) S[e] = fmaf(f, vs[j * DV + e], S[e]);
-                z += f;
+                for (int e4 = 0; e4 < DV / 4; ++e4) {
+                    const float4 c = cj[e4];
+                    st[4 * e4 + 0] = fmaf(a, st[4 * e4 + 0], fb * c.x);
+                    st[4 * e4 + 1] = fmaf(a, st[4 * e4 + 1], fb * c.y);
+                    st[4 * e4 + 2] = fmaf(a, st[4 * e4 + 2], fb * c.z);
+                    st[4 * e4 + 3] = fmaf(a, st[4 * e4 + 3], fb * c.w);
+                }
+                st[DV] = fmaf(a, st[DV], fb);
             }
-            pc.next();
         }
     }
-    float* o = part + ((size_t)bh * n_seg + seg) * m * (DV + 1) + (size_t)r * (DV + 1);
+    if (own) {
+        float* o = part + ((size_t)bh * n_seg + seg) * m * W + (size_t)r * W;
 #pragma unroll
-    for (int e = 0; e < DV; ++e) o[e] = S[e];
-    o[DV] = z;
-    if (segdecay && r == 0) segdecay[(size_t)bh * n_seg + seg] = A;
+        for (int e = 0; e < W; ++e) o[e] = st[e];
+        if (segdecay && r == 0) segdecay[(size_t)bh * n_seg + seg] = A;
+    }
 }
 
 // ------------------------------------------------- fixed-order segment combines
@@ -240,76 +205,111 @@ __global__ void k_scan_segments_decay(float* __restrict__ part, const float* __r
 }
 
 // ------------------------------------------------------- bidirectional readout
-// grid (ceil(L/16), B*H), 256 threads.  out_i = phi(q_i)^T S / phi(q_i)^T z.
-template <typename T, int KIND>
+// grid (n_seg, B*H), 256 threads.  The state [m][dv+1] (row-major, fp32) is
+// staged once per CTA; per tile of TT queries: projections (thread per
+// feature row), row shift, features placed by slot, den by one warp per query,
+// and out_j[e..e+3] for two queries per thread as sums over the features.
+template <typename T, int KIND, int DV>
 __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const float* __restrict__ state,
                                                  const float* __restrict__ omega, T* __restrict__ out,
-                                                 int H, int L, int m, int d, int dv, float s,
+                                                 int H, int L, int m, int d, float s, int seg_len, int n_seg,
                                                  const int* __restrict__ pcyc, const int4* __restrict__ pmeta) {
-    constexpr int TQ = 16;
-    extern __shared__ float sm[];
-    const int sw = dv + 1;
-    float* sts = sm;                 // [m][dv+1]
-    float* fq = sts + m * sw;        // [TQ][m]
-    float* xs = fq + TQ * m;         // [TQ][d]
-    float* num = xs + TQ * d;        // [TQ][dv+1]
-    float* rmax = num + TQ * sw;     // [TQ]
-    const int bh = blockIdx.y, h = bh % H;
-    const int i0 = blockIdx.x * TQ;
-    const int nq = min(TQ, L - i0);
-    const float* stg = state + (size_t)bh * m * sw;
-    for (int idx = threadIdx.x; idx < m * sw; idx += blockDim.x) sts[idx] = stg[idx];
-    for (int idx = threadIdx.x; idx < nq * d; idx += blockDim.x) xs[idx] = ldf(q + ((size_t)bh * L + i0) * d + idx);
-    __syncthreads();
+    using F = FwdShape<DV>;
+    constexpr int TT = F::TT, DVP = F::DVP, W = F::W;
+    extern __shared__ __align__(16) float sm[];
+    const int MP = m + 1;
+    float* ss = sm;                          // [m][DVP] state rows
+    float* xs = ss + m * DVP;                // [TT][d]
+    float* raw = xs + TT * d;                // [TT][m+1] s * projections
+    float* fq = raw + al4f(TT * MP);         // [TT][m+1] features by slot
+    float* cq = fq + al4f(TT * MP);          // [TT]
+    float* den = cq + TT;                    // [TT]
+    const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int r = threadIdx.x;
+    const bool own = r < m;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const float* om = omega + (size_t)h * m * d;
-    for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) {
-        const int i = idx / m, r = idx - i * m;
-        PermCursor pc;
-        pc.init(pcyc, pmeta, h, m, r, i0 + i);
-        const int row = pc.row(r);
-        float p = 0.f;
-        for (int c = 0; c < d; ++c) p = fmaf(__ldg(om + row * d + c), xs[i * d + c], p);
-        fq[idx] = s * p;
+    const size_t row0 = (size_t)bh * L;
+    {
+        const float* sg = state + (size_t)bh * m * W;
+        for (int idx = threadIdx.x; idx < m * DVP; idx += blockDim.x) {
+            const int rr = idx / DVP, e = idx - rr * DVP;
+            ss[idx] = e < W ? sg[rr * W + e] : 0.f;
+        }
     }
-    __syncthreads();
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-        for (int i = warp; i < nq; i += blockDim.x / 32) {
-            float mx = -INFINITY;
-            for (int r = lane; r < m; r += 32) mx = fmaxf(mx, fq[i * m + r]);
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) rmax[i] = mx;
+    const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    PermCursor pc;
+    pc.init_inv(pcyc, pmeta, h, m, own ? r : 0, j0);
+    for (int t0 = j0; t0 < j1; t0 += TT) {
+        const int nt = min(TT, j1 - t0);
+        __syncthreads();
+        stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
+        __syncthreads();
+        float p[TT];
+        if (own) {
+            project_regs<TT>(om, xs, r, d, p);
+#pragma unroll
+            for (int j = 0; j < TT; ++j) raw[j * MP + r] = s * p[j];
         }
         __syncthreads();
-        for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) fq[idx] = expf(fq[idx] - rmax[idx / m]);
-    } else {
-        for (int idx = threadIdx.x; idx < nq * m; idx += blockDim.x) {
-            const int i = idx / m, r = idx - i * m;
-            PermCursor pc;
-            pc.init(pcyc, pmeta, h, m, r, i0 + i);
-            fq[idx] = query_feat<KIND>(fq[idx], 0.f, pc.row(r), m);
+        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+            row_shift(raw, cq, TT, nt, m);
+            __syncthreads();
         }
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < nq * sw; idx += blockDim.x) {
-        const int i = idx / sw, e = idx - i * sw;
-        float a = 0.f;
-        for (int r = 0; r < m; ++r) a = fmaf(fq[i * m + r], sts[r * sw + e], a);
-        num[idx] = a;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < nq * dv; idx += blockDim.x) {
-        const int i = idx / dv, e = idx - i * dv;
-        const float den = num[i * sw + dv];
-        stf(out + ((size_t)bh * L + i0) * dv + idx, den != 0.f ? num[i * sw + e] / den : 0.f);
+        if (own) {
+#pragma unroll
+            for (int j = 0; j < TT; ++j) {
+                const float mx = KIND == FAVOR_KERNEL_SOFTMAX_POS ? cq[j] : 0.f;
+                fq[j * MP + pc.row(r)] = j < nt ? query_feat<KIND>(s * p[j], mx, r, m) : 0.f;
+                pc.prev();
+            }
+        }
+        __syncthreads();
+        for (int j = warp; j < TT; j += nw) {
+            float a = 0.f;
+            for (int rr = lane; rr < m; rr += 32) a = fmaf(fq[j * MP + rr], ss[rr * DVP + DV], a);
+            a = warp_sum(a);
+            if (lane == 0) den[j] = a;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < (TT / 2) * (DV / 4); idx += blockDim.x) {
+            const int jp = idx / (DV / 4), e4 = idx - jp * (DV / 4);
+            const int ja = 2 * jp, jb = ja + 1;
+            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll 4
+            for (int rr = 0; rr < m; ++rr) {
+                const float4 sv = *reinterpret_cast<const float4*>(ss + rr * DVP + 4 * e4);
+                const float f0 = fq[ja * MP + rr], f1 = fq[jb * MP + rr];
+                a0.x = fmaf(f0, sv.x, a0.x); a0.y = fmaf(f0, sv.y, a0.y);
+                a0.z = fmaf(f0, sv.z, a0.z); a0.w = fmaf(f0, sv.w, a0.w);
+                a1.x = fmaf(f1, sv.x, a1.x); a1.y = fmaf(f1, sv.y, a1.y);
+                a1.z = fmaf(f1, sv.z, a1.z); a1.w = fmaf(f1, sv.w, a1.w);
+            }
+            if (ja < nt) {
+                const float dn = den[ja];
+                T* o = out + (row0 + t0 + ja) * DV + 4 * e4;
+                stf(o + 0, dn != 0.f ? a0.x / dn : 0.f); stf(o + 1, dn != 0.f ? a0.y / dn : 0.f);
+                stf(o + 2, dn != 0.f ? a0.z / dn : 0.f); stf(o + 3, dn != 0.f ? a0.w / dn : 0.f);
+            }
+            if (jb < nt) {
+                const float dn = den[jb];
+                T* o = out + (row0 + t0 + jb) * DV + 4 * e4;
+                stf(o + 0, dn != 0.f ? a1.x / dn : 0.f); stf(o + 1, dn != 0.f ? a1.y / dn : 0.f);
+                stf(o + 2, dn != 0.f ? a1.z / dn : 0.f); stf(o + 3, dn != 0.f ? a1.w / dn : 0.f);
+            }
+        }
     }
 }
 
 // --------------------------------------------------------- causal, per segment
-// grid (n_seg, B*H), m threads.  Thread r holds S[r, :], z[r] starting from the
-// segment's exclusive prefix state and walks the segment token by token:
-// S += phi(k_i) v_i^T, z += phi(k_i) (inclusive of i), then
-// out_i = phi(q_i)^T S / phi(q_i)^T z, the sum over r done across the block.
+// grid (n_seg, B*H), 256 threads.  The state at the tile start (the segment's
+// exclusive prefix, then carried) lives in shared memory; per tile of TT
+// tokens (the chunked form of App. B.1 Eq. 11):
+//   num_j = P_j phi~_q(j) S + sum_{i<=j} D_ji (phi~_q(j) . phi~_k(i)) [v_i 1],
+//   S <- P_tile S + sum_i w_i phi~_k(i) [v_i 1]^T,
+// with the decay weights P_j = prod_{l<=j} a_l, D_ji = b_i prod_{i<l<=j} a_l,
+// w_i = D_{last,i} and P_tile = prod_l a_l (all 1 without decay), out_j =
+// num_j / den_j (den the last column).  No per-token block reductions.
 template <typename T, int KIND, int DV>
 __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q, const T* __restrict__ k,
                                                         const T* __restrict__ v, const float* __restrict__ omega,
@@ -319,100 +319,172 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
                                                         const int* __restrict__ pcyc, const int4* __restrict__ pmeta,
                                                         const float* __restrict__ gate,
                                                         const float* __restrict__ rdec) {
-    extern __shared__ float sm[];
-    const int dp = d + 1;
-    const int nwarps = (m + 31) / 32;
-    float* oms = sm;                        // [m][d+1]
-    float* qs = oms + m * dp;               // [kTokTile][d]
-    float* ks = qs + kTokTile * d;          // [kTokTile][d]
-    float* vs = ks + kTokTile * d;          // [kTokTile][DV]
-    float* nrm = vs + kTokTile * DV;        // [kTokTile]
-    float* red = nrm + kTokTile;            // [nwarps][DV+1]
-    float* wmax = red + nwarps * (DV + 1);  // [nwarps]
+    using F = FwdShape<DV>;
+    constexpr int TT = F::TT, DVP = F::DVP, W = F::W;
+    extern __shared__ __align__(16) float sm[];
+    const int MP = m + 1;
+    float* ss = sm;                          // [m][DVP] state at the tile start
+    float* xs = ss + m * DVP;                // [TT][d] queries
+    float* ys = xs + TT * d;                 // [TT][d] keys
+    float* cs = ys + TT * d;                 // [TT][DVP] v, 1, 0...
+    float* raw = cs + TT * DVP;              // [TT][m+1] s * query projections
+    float* fq = raw + al4f(TT * MP);         // [TT][m+1] query features by slot
+    float* fk = fq + al4f(TT * MP);          // [TT][m+1] key features by slot
+    float* aa = fk + al4f(TT * MP);          // [TT][TT+1] D_ji phi_q(j).phi_k(i), i <= j
+    float* cq = aa + al4f(TT * (TT + 1));    // [TT]
+    float* den = cq + TT;                    // [TT]
+    float* kn = den + TT;                    // [TT]
+    float* ga = kn + TT;                     // [TT] a_j
+    float* gb = ga + TT;                     // [TT] b_j
+    float* pj = gb + TT;                     // [TT] P_j
+    float* wi = pj + TT;                     // [TT] w_i
+    float* pt = wi + TT;                     // [4] P_tile
     const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
-    const int r = threadIdx.x, warp = r / 32, lane = r % 32;
-    for (int idx = threadIdx.x; idx < m * d; idx += blockDim.x)
-        oms[(idx / d) * dp + idx % d] = omega[(size_t)h * m * d + idx];
+    const int r = threadIdx.x;
+    const bool own = r < m;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const float* om = omega + (size_t)h * m * d;
     const float kap = kshift[h];
-    float S[DV];
-    const float* pre = prefix + ((size_t)bh * n_seg + seg) * m * (DV + 1) + (size_t)r * (DV + 1);
-#pragma unroll
-    for (int e = 0; e < DV; ++e) S[e] = pre[e];
-    float z = pre[DV];
-    // m is a multiple of 16, so only a last warp of 16 lanes can be partial.
-    const int width = (m % 32 != 0 && warp == nwarps - 1) ? 16 : 32;
-    const unsigned full = width == 32 ? 0xffffffffu : 0x0000ffffu;
-    const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
-    PermCursor pc;
-    pc.init(pcyc, pmeta, h, m, r, j0);
+    const size_t row0 = (size_t)bh * L;
     const bool decay = gate || rdec;
     const float rd = rdec ? rdec[h] : 1.f;
-    for (int t0 = j0; t0 < j1; t0 += kTokTile) {
-        const int nt = min(kTokTile, j1 - t0);
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < nt * d; idx += blockDim.x) {
-            qs[idx] = ldf(q + ((size_t)bh * L + t0) * d + idx);
-            ks[idx] = ldf(k + ((size_t)bh * L + t0) * d + idx);
+    {
+        const float* pre = prefix + ((size_t)bh * n_seg + seg) * m * W;
+        for (int idx = threadIdx.x; idx < m * DVP; idx += blockDim.x) {
+            const int rr = idx / DVP, e = idx - rr * DVP;
+            ss[idx] = e < W ? pre[rr * W + e] : 0.f;
         }
-        for (int idx = threadIdx.x; idx < nt * DV; idx += blockDim.x)
-            vs[idx] = ldf(v + ((size_t)bh * L + t0) * DV + idx);
+    }
+    const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    PermCursor pc;
+    pc.init_inv(pcyc, pmeta, h, m, own ? r : 0, j0);
+    for (int t0 = j0; t0 < j1; t0 += TT) {
+        const int nt = min(TT, j1 - t0);
+        __syncthreads();   // the previous tile's state update is done
+        stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
+        stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
+        stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+        for (int j = threadIdx.x; j < TT; j += blockDim.x) {
+            float a = 1.f, b = j < nt ? 1.f : 0.f;
+            if (decay && j < nt) token_decay(gate, row0 + t0 + j, rd, &a, &b);
+            ga[j] = a;
+            gb[j] = b;
+        }
         __syncthreads();
-        for (int j = threadIdx.x; j < nt; j += blockDim.x) {   // blockDim may be below kTokTile
+        key_norms(ys, kn, TT, d);
+        if (threadIdx.x == 32 * (nw - 1)) {   // decay weights, one thread (TT <= 32 steps)
+            float P = 1.f;
+            for (int j = 0; j < TT; ++j) {
+                P *= ga[j];
+                pj[j] = P;
+            }
+            pt[0] = P;
+            float tail = 1.f;
+            for (int i = TT - 1; i >= 0; --i) {
+                wi[i] = gb[i] * tail;
+                tail *= ga[i];
+            }
+        }
+        float pq[TT], pk[TT];
+        if (own) {
+            project_regs<TT>(om, xs, r, d, pq);
+            project_regs<TT>(om, ys, r, d, pk);
+#pragma unroll
+            for (int j = 0; j < TT; ++j) raw[j * MP + r] = s * pq[j];
+        }
+        __syncthreads();
+        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+            row_shift(raw, cq, TT, nt, m);
+            __syncthreads();
+        }
+        if (own) {
+#pragma unroll
+            for (int j = 0; j < TT; ++j) {
+                const int slot = pc.row(r);   // query and key at one position share pi^j
+                const float mx = KIND == FAVOR_KERNEL_SOFTMAX_POS ? cq[j] : 0.f;
+                fq[j * MP + slot] = j < nt ? query_feat<KIND>(s * pq[j], mx, r, m) : 0.f;
+                fk[j * MP + slot] = j < nt ? key_feat<KIND>(pk[j], kn[j], s, kap, r, m) : 0.f;
+                pc.prev();
+            }
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < TT * TT; idx += blockDim.x) {
+            const int j = idx / TT, i = idx - j * TT;
             float a = 0.f;
-            for (int c = 0; c < d; ++c) a = fmaf(ks[j * d + c], ks[j * d + c], a);
-            nrm[j] = a;
+            if (i <= j) {
+                for (int rr = 0; rr < m; ++rr) a = fmaf(fq[j * MP + rr], fk[i * MP + rr], a);
+                float wgt = gb[i];
+                for (int l = i + 1; l <= j; ++l) wgt *= ga[l];
+                a *= wgt;
+            }
+            aa[j * (TT + 1) + i] = a;
         }
         __syncthreads();
-        for (int j = 0; j < nt; ++j) {
-            const int row = pc.row(r);   // query and key at one position share pi^j
-            float pk = 0.f, pq = 0.f;
-            for (int c = 0; c < d; ++c) {
-                pk = fmaf(oms[row * dp + c], ks[j * d + c], pk);
-                pq = fmaf(oms[row * dp + c], qs[j * d + c], pq);
+        for (int j = warp; j < TT; j += nw) {
+            float a = 0.f;
+            for (int rr = lane; rr < m; rr += 32) a = fmaf(fq[j * MP + rr], ss[rr * DVP + DV], a);
+            a *= pj[j];
+            if (lane <= j && lane < TT) a += aa[j * (TT + 1) + lane];
+            a = warp_sum(a);
+            if (lane == 0) den[j] = a;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < (TT / 2) * (DV / 4); idx += blockDim.x) {
+            const int jp = idx / (DV / 4), e4 = idx - jp * (DV / 4);
+            const int ja = 2 * jp, jb = ja + 1;
+            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll 4
+            for (int rr = 0; rr < m; ++rr) {
+                const float4 sv = *reinterpret_cast<const float4*>(ss + rr * DVP + 4 * e4);
+                const float f0 = fq[ja * MP + rr], f1 = fq[jb * MP + rr];
+                a0.x = fmaf(f0, sv.x, a0.x); a0.y = fmaf(f0, sv.y, a0.y);
+                a0.z = fmaf(f0, sv.z, a0.z); a0.w = fmaf(f0, sv.w, a0.w);
+                a1.x = fmaf(f1, sv.x, a1.x); a1.y = fmaf(f1, sv.y, a1.y);
+                a1.z = fmaf(f1, sv.z, a1.z); a1.w = fmaf(f1, sv.w, a1.w);
             }
-            const float fk = key_feat<KIND>(pk, nrm[j], s, kap, row, m);
-            if (decay) {
-                float a, b;
-                token_decay(gate, (size_t)bh * L + t0 + j, rd, &a, &b);
-                const float fb = fk * b;
+            const float p0 = pj[ja], p1 = pj[jb];
+            a0.x *= p0; a0.y *= p0; a0.z *= p0; a0.w *= p0;
+            a1.x *= p1; a1.y *= p1; a1.z *= p1; a1.w *= p1;
+            for (int i = 0; i <= jb; ++i) {
+                const float4 c = *reinterpret_cast<const float4*>(cs + i * DVP + 4 * e4);
+                const float w0 = i <= ja ? aa[ja * (TT + 1) + i] : 0.f, w1 = aa[jb * (TT + 1) + i];
+                a0.x = fmaf(w0, c.x, a0.x); a0.y = fmaf(w0, c.y, a0.y);
+                a0.z = fmaf(w0, c.z, a0.z); a0.w = fmaf(w0, c.w, a0.w);
+                a1.x = fmaf(w1, c.x, a1.x); a1.y = fmaf(w1, c.y, a1.y);
+                a1.z = fmaf(w1, c.z, a1.z); a1.w = fmaf(w1, c.w, a1.w);
+            }
+            if (ja < nt) {
+                const float dn = den[ja];
+                T* o = out + (row0 + t0 + ja) * DV + 4 * e4;
+                stf(o + 0, dn != 0.f ? a0.x / dn : 0.f); stf(o + 1, dn != 0.f ? a0.y / dn : 0.f);
+                stf(o + 2, dn != 0.f ? a0.z / dn : 0.f); stf(o + 3, dn != 0.f ? a0.w / dn : 0.f);
+            }
+            if (jb < nt) {
+                const float dn = den[jb];
+                T* o = out + (row0 + t0 + jb) * DV + 4 * e4;
+                stf(o + 0, dn != 0.f ? a1.x / dn : 0.f); stf(o + 1, dn != 0.f ? a1.y / dn : 0.f);
+                stf(o + 2, dn != 0.f ? a1.z / dn : 0.f); stf(o + 3, dn != 0.f ? a1.w / dn : 0.f);
+            }
+        }
+        __syncthreads();   // every output read the state at the tile start
+        if (own) {
+            float wf[TT];
 #pragma unroll
-                for (int e = 0; e < DV; ++e) S[e] = fmaf(a, S[e], fb * vs[j * DV + e]);
-                z = fmaf(a, z, fb);
-            } else {
+            for (int i = 0; i < TT; ++i) wf[i] = wi[i] * fk[i * MP + r];
+            const float P = pt[0];
+            float4* srow = reinterpret_cast<float4*>(ss + r * DVP);
+#pragma unroll 1
+            for (int e4 = 0; e4 < DVP / 4; ++e4) {
+                float4 a = srow[e4];
+                a.x *= P; a.y *= P; a.z *= P; a.w *= P;
 #pragma unroll
-                for (int e = 0; e < DV; ++e) S[e] = fmaf(fk, vs[j * DV + e], S[e]);
-                z += fk;
-            }
-            pc.next();
-            float fq;
-            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-                float mx = s * pq;
-                for (int o = width / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(full, mx, o));
-                if (lane == 0) wmax[warp] = mx;
-                __syncthreads();
-                mx = wmax[0];
-                for (int w = 1; w < nwarps; ++w) mx = fmaxf(mx, wmax[w]);
-                fq = expf(s * pq - mx);
-            } else {
-                fq = query_feat<KIND>(s * pq, 0.f, row, m);
-            }
-            // sum over r of fq * [S | z]: warp shuffles, then across warps in smem.
-#pragma unroll
-            for (int e = 0; e <= DV; ++e) {
-                float a = fq * (e < DV ? S[e] : z);
-                for (int o = width / 2; o > 0; o >>= 1) a += __shfl_xor_sync(full, a, o);
-                if (lane == 0) red[warp * (DV + 1) + e] = a;
-            }
-            __syncthreads();
-            for (int e = threadIdx.x; e < DV; e += blockDim.x) {   // blockDim = m may be below DV
-                float a = 0.f, den = 0.f;
-                for (int w = 0; w < nwarps; ++w) {
-                    a += red[w * (DV + 1) + e];
-                    den += red[w * (DV + 1) + DV];
+                for (int i = 0; i < TT; ++i) {
+                    const float4 c = *reinterpret_cast<const float4*>(cs + i * DVP + 4 * e4);
+                    a.x = fmaf(wf[i], c.x, a.x); a.y = fmaf(wf[i], c.y, a.y);
+                    a.z = fmaf(wf[i], c.z, a.z); a.w = fmaf(wf[i], c.w, a.w);
                 }
-                stf(out + ((size_t)bh * L + t0 + j) * DV + e, den != 0.f ? a / den : 0.f);
+                srow[e4] = a;
             }
-            __syncthreads();
         }
     }
 }
@@ -435,44 +507,61 @@ favor_status feature_map_t(const Handle& h, const void* x, void* phi, int B, int
 template <typename T, int KIND, int DV>
 favor_status state_t(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan& p,
                      const RelposArgs& rp, cudaStream_t st) {
-    const size_t smem = (size_t)(h.m * (h.d + 1) + kTokTile * h.d + kTokTile * DV + kTokTile) * sizeof(float);
+    using F = FwdShape<DV>;
+    const size_t smem = (size_t)(F::TT * h.d + F::TT * F::DVP + al4f(F::TT * (h.m + 1)) + 3 * F::TT) * sizeof(float);
     auto kern = k_segment_state<T, KIND, DV>;
     set_smem(kern, smem);
     dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_STATE, st);
-    kern<<<grid, h.m, smem, st>>>((const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial, h.H, L, h.m,
+    kern<<<grid, 256, smem, st>>>((const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial, h.H, L, h.m,
                                   h.d, h.s, p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta, rp.gate, rp.rdec,
                                   rp.segdecay);
     count_launch();
     return check_launch("segment state kernel");
 }
 
+template <typename T, int KIND, int DV>
+favor_status readout_dv(const Handle& h, const void* q, void* out, int BH, int L, cudaStream_t st,
+                        const RelposArgs& rp) {
+    using F = FwdShape<DV>;
+    const SegPlan p = plan_segments(BH, L, h.num_sms);
+    const size_t smem = (size_t)(h.m * F::DVP + F::TT * h.d + 2 * al4f(F::TT * (h.m + 1)) + 2 * F::TT) * sizeof(float);
+    auto kern = k_readout<T, KIND, DV>;
+    set_smem(kern, smem);
+    dim3 grid(p.n_seg, BH);
+    ProfScope ps(h, PROF_READOUT, st);
+    kern<<<grid, 256, smem, st>>>((const T*)q, h.ws_state, h.omega_f32, (T*)out, h.H, L, h.m, h.d, h.s,
+                                  p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta);
+    count_launch();
+    return check_launch("readout kernel");
+}
+
 template <typename T, int KIND>
 favor_status readout_t(const Handle& h, const void* q, void* out, int BH, int L, cudaStream_t st,
                        const RelposArgs& rp = RelposArgs()) {
-    const int sw = h.dv + 1;
-    const size_t smem = (size_t)(h.m * sw + 16 * h.m + 16 * h.d + 16 * sw + 16) * sizeof(float);
-    auto kern = k_readout<T, KIND>;
-    set_smem(kern, smem);
-    dim3 grid((L + 15) / 16, BH);
-    ProfScope ps(h, PROF_READOUT, st);
-    kern<<<grid, 256, smem, st>>>((const T*)q, h.ws_state, h.omega_f32, (T*)out, h.H, L, h.m, h.d, h.dv, h.s,
-                                  rp.cyc, rp.meta);
-    count_launch();
-    return check_launch("readout kernel");
+    switch (h.dv) {
+        case 16: return readout_dv<T, KIND, 16>(h, q, out, BH, L, st, rp);
+        case 32: return readout_dv<T, KIND, 32>(h, q, out, BH, L, st, rp);
+        case 64: return readout_dv<T, KIND, 64>(h, q, out, BH, L, st, rp);
+        case 128: return readout_dv<T, KIND, 128>(h, q, out, BH, L, st, rp);
+    }
+    return set_error(FAVOR_ERR_UNSUPPORTED, "readout: unsupported dv=%d", h.dv);
 }
 
 template <typename T, int KIND, int DV>
 favor_status causal_t(const Handle& h, const void* q, const void* k, const void* v, void* out, int BH, int L,
                       const SegPlan& p, const RelposArgs& rp, cudaStream_t st) {
-    const int nwarps = (h.m + 31) / 32;
-    const size_t smem = (size_t)(h.m * (h.d + 1) + 2 * kTokTile * h.d + kTokTile * DV + kTokTile +
-                                 nwarps * (DV + 1) + nwarps) * sizeof(float);
+    using F = FwdShape<DV>;
+    const int TT = F::TT;
+    const size_t smem = (size_t)(h.m * F::DVP + 2 * TT * h.d + TT * F::DVP + 3 * al4f(TT * (h.m + 1)) +
+                                 al4f(TT * (TT + 1)) + 8 * TT + 4) * sizeof(float);
+    if (smem > 227 * 1024)
+        return set_error(FAVOR_ERR_UNSUPPORTED, "causal: %zu bytes of shared memory", smem);
     auto kern = k_causal_segment<T, KIND, DV>;
     set_smem(kern, smem);
     dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_CAUSAL, st);
-    kern<<<grid, h.m, smem, st>>>((const T*)q, (const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial,
+    kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial,
                                   (T*)out, h.H, L, h.m, h.d, h.s, p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta,
                                   rp.gate, rp.rdec);
     count_launch();
