@@ -63,7 +63,7 @@ __host__ __device__ inline BwdSmem bwd_smem(int TT, int DVP, int W, int m, int d
     p.ub = o; o += key_pass ? 0 : al4(TT * MP);                   // u = G^PS dO (query pass)
     p.aa = o; o += causal ? al4(TT * (TT + 1)) : 0;               // masked phi_q . phi_k
     p.mm = o; o += causal ? al4(TT * (TT + 1)) : 0;               // masked dO . v (query) / D . C (key)
-    p.rs = o; o += key_pass ? al4(m * W) : 0;                     // H at the tile end (key pass)
+    p.rs = o; o += key_pass ? al4(m * DVP) : 0;                   // H at the tile end, value columns (key pass)
     p.zs = o; o += al4(m);                                        // z column of the query pass state
     p.cq = o; o += al4(TT);
     p.den = o; o += al4(TT);
@@ -88,41 +88,51 @@ __device__ __forceinline__ void make_d(float* dd, const float* den, const float*
 }
 
 // dx rows from G (row stride m+1) for a tile: dx_j = s*(G_j Omega - s*x_j sum_r G_jr)
-// (positive) or s*G_j Omega (ReLU), written as rows [t0, t0+nt) of dst.
+// (positive) or s*G_j Omega (ReLU), written as rows [t0, t0+nt) of dst; two
+// tokens x four columns per thread (one float4 omega load feeds 8 FMAs).
 template <typename T, int KIND>
 __device__ __forceinline__ void grad_inputs(const float* g, const float* xs, const float* __restrict__ om,
                                             T* __restrict__ dst, int t0, int nt, int TT, int m, int d, float s) {
     const int d4 = d >> 2;
     const float4* w4 = reinterpret_cast<const float4*>(om);
-    for (int idx = threadIdx.x; idx < TT * d4; idx += blockDim.x) {
-        const int j = idx / d4, c4 = idx - j * d4;
-        if (j >= nt) continue;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        float gsum = 0.f;
-        const float* gj = g + j * (m + 1);
+    for (int idx = threadIdx.x; idx < (TT / 2) * d4; idx += blockDim.x) {
+        const int jp = idx / d4, c4 = idx - jp * d4;
+        const int ja = 2 * jp, jb = ja + 1;
+        if (ja >= nt) continue;
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+        float gs0 = 0.f, gs1 = 0.f;
+        const float* g0 = g + ja * (m + 1);
+        const float* g1 = g + jb * (m + 1);
 #pragma unroll 4
         for (int r = 0; r < m; ++r) {
-            const float gr = gj[r];
+            const float x0 = g0[r], x1 = g1[r];
             const float4 w = __ldg(w4 + r * d4 + c4);
-            a.x = fmaf(gr, w.x, a.x);
-            a.y = fmaf(gr, w.y, a.y);
-            a.z = fmaf(gr, w.z, a.z);
-            a.w = fmaf(gr, w.w, a.w);
-            gsum += gr;
+            a0.x = fmaf(x0, w.x, a0.x); a0.y = fmaf(x0, w.y, a0.y);
+            a0.z = fmaf(x0, w.z, a0.z); a0.w = fmaf(x0, w.w, a0.w);
+            a1.x = fmaf(x1, w.x, a1.x); a1.y = fmaf(x1, w.y, a1.y);
+            a1.z = fmaf(x1, w.z, a1.z); a1.w = fmaf(x1, w.w, a1.w);
+            gs0 += x0;
+            gs1 += x1;
         }
-        const float* xj = xs + j * d + 4 * c4;
-        T* o = dst + (size_t)(t0 + j) * d + 4 * c4;
-        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-            const float t = s * gsum;
-            stf(o + 0, s * fmaf(-t, xj[0], a.x));
-            stf(o + 1, s * fmaf(-t, xj[1], a.y));
-            stf(o + 2, s * fmaf(-t, xj[2], a.z));
-            stf(o + 3, s * fmaf(-t, xj[3], a.w));
-        } else {
-            stf(o + 0, s * a.x);
-            stf(o + 1, s * a.y);
-            stf(o + 2, s * a.z);
-            stf(o + 3, s * a.w);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int j = ja + t;
+            if (j >= nt) break;
+            const float4 a = t == 0 ? a0 : a1;
+            const float* xj = xs + j * d + 4 * c4;
+            T* o = dst + (size_t)(t0 + j) * d + 4 * c4;
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                const float u = s * (t == 0 ? gs0 : gs1);
+                stf(o + 0, s * fmaf(-u, xj[0], a.x));
+                stf(o + 1, s * fmaf(-u, xj[1], a.y));
+                stf(o + 2, s * fmaf(-u, xj[2], a.z));
+                stf(o + 3, s * fmaf(-u, xj[3], a.w));
+            } else {
+                stf(o + 0, s * a.x);
+                stf(o + 1, s * a.y);
+                stf(o + 2, s * a.z);
+                stf(o + 3, s * a.w);
+            }
         }
     }
 }
@@ -364,7 +374,7 @@ __global__ void __launch_bounds__(256) k_bwd_key(const T* __restrict__ q, const 
         }
         if (own && (CAUSAL || t0 == j0)) {
 #pragma unroll
-            for (int e = 0; e < W; ++e) rs[r * W + e] = hr[e];
+            for (int e = 0; e < DVP; ++e) rs[r * DVP + e] = e < DV ? hr[e < W ? e : 0] : 0.f;
         }
         __syncthreads();
         key_norms(ys, kn, TT, d);
@@ -407,16 +417,37 @@ __global__ void __launch_bounds__(256) k_bwd_key(const T* __restrict__ q, const 
             }
             __syncthreads();
         }
-        // dv_j = H(tile end)^T phi~_k(j) + sum_{i>=j} aa[j][i] D_i
-        for (int idx = threadIdx.x; idx < TT * DV; idx += blockDim.x) {
-            const int j = idx / DV, e = idx - j * DV;
-            if (j >= nt) continue;
-            float a = 0.f;
+        // dv_j = H(tile end)^T phi~_k(j) + sum_{i>=j} aa[j][i] D_i, two keys x four columns per thread
+        for (int idx = threadIdx.x; idx < (TT / 2) * (DV / 4); idx += blockDim.x) {
+            const int jp = idx / (DV / 4), e4 = idx - jp * (DV / 4);
+            const int ja = 2 * jp, jb = ja + 1;
+            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
 #pragma unroll 4
-            for (int rr = 0; rr < m; ++rr) a = fmaf(fk[j * MP + rr], rs[rr * W + e], a);
+            for (int rr = 0; rr < m; ++rr) {
+                const float4 hv = *reinterpret_cast<const float4*>(rs + rr * DVP + 4 * e4);
+                const float f0 = fk[ja * MP + rr], f1 = fk[jb * MP + rr];
+                a0.x = fmaf(f0, hv.x, a0.x); a0.y = fmaf(f0, hv.y, a0.y);
+                a0.z = fmaf(f0, hv.z, a0.z); a0.w = fmaf(f0, hv.w, a0.w);
+                a1.x = fmaf(f1, hv.x, a1.x); a1.y = fmaf(f1, hv.y, a1.y);
+                a1.z = fmaf(f1, hv.z, a1.z); a1.w = fmaf(f1, hv.w, a1.w);
+            }
             if (CAUSAL)
-                for (int i = j; i < TT; ++i) a = fmaf(aa[j * (TT + 1) + i], dd[i * DVP + e], a);
-            stf(dvv + (row0 + t0 + j) * DV + e, a);
+                for (int i = ja; i < TT; ++i) {
+                    const float4 dvec = *reinterpret_cast<const float4*>(dd + i * DVP + 4 * e4);
+                    const float w0 = aa[ja * (TT + 1) + i], w1 = i >= jb ? aa[jb * (TT + 1) + i] : 0.f;
+                    a0.x = fmaf(w0, dvec.x, a0.x); a0.y = fmaf(w0, dvec.y, a0.y);
+                    a0.z = fmaf(w0, dvec.z, a0.z); a0.w = fmaf(w0, dvec.w, a0.w);
+                    a1.x = fmaf(w1, dvec.x, a1.x); a1.y = fmaf(w1, dvec.y, a1.y);
+                    a1.z = fmaf(w1, dvec.z, a1.z); a1.w = fmaf(w1, dvec.w, a1.w);
+                }
+            if (ja < nt) {
+                T* o = dvv + (row0 + t0 + ja) * DV + 4 * e4;
+                stf(o + 0, a0.x); stf(o + 1, a0.y); stf(o + 2, a0.z); stf(o + 3, a0.w);
+            }
+            if (jb < nt) {
+                T* o = dvv + (row0 + t0 + jb) * DV + 4 * e4;
+                stf(o + 0, a1.x); stf(o + 1, a1.y); stf(o + 2, a1.z); stf(o + 3, a1.w);
+            }
         }
         __syncthreads();
         if (own) {
