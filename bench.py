@@ -169,10 +169,15 @@ def backward_flops_per_token_head(w):
     return 8 * m * d + 6 * m * (dv + 1) + 4 * m * dv
 
 
+# Source files that define the tensor-core kernels whose DRAM traffic
+# profiles/ncu_traffic.json records: a change to any of them voids the record.
+TC_SOURCES = ("favor_tc.cu", "tc_ptx.cuh", "favor_internal.h")
+
+
 def source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "random_feature_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in TC_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
