@@ -116,6 +116,7 @@ static void free_handle(Handle* h) {
     cudaFree(h->perm_meta);
     cudaFree(h->relpos_r);
     cudaFree(h->ws_tc);
+    cudaFree(h->ws_bimg);
     free(h->omega_sqnorm_half_host);
     if (h->prof) {
         for (auto& pe : h->prof->pending) { cudaEventDestroy(pe.a); cudaEventDestroy(pe.b); }
@@ -254,6 +255,8 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
         h->ws_tc_bytes = (size_t)max_B * H * 128 * m * sizeof(__nv_bfloat16);
         e = cudaMalloc(&h->ws_tc, h->ws_tc_bytes);
         if (e == cudaSuccess) e = cudaMemset(h->ws_tc, 0, h->ws_tc_bytes);
+        // backward: per head S~ (then dS~) as bf16 hi / lo operand images + the fp32 z column
+        if (e == cudaSuccess) e = cudaMalloc(&h->ws_bimg, tc_bwd_image_bytes((size_t)max_B * H));
         if (e != cudaSuccess) {
             favor_status st = (e == cudaErrorMemoryAllocation) ? FAVOR_ERR_NOMEM : FAVOR_ERR_CUDA;
             set_error(st, "favor_create: cudaMalloc: %s", cudaGetErrorString(e));
@@ -539,8 +542,9 @@ static favor_status backward_call(const char* fn, bool causal, favor_handle hd, 
         return set_error(FAVOR_ERR_UNSUPPORTED, "%s: no backward for trigonometric features", fn);
     if (relpos_on(h)) return set_error(FAVOR_ERR_UNSUPPORTED, "%s: relative positions are set", fn);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return causal ? simt_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, s)
-                  : simt_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
+    if (causal) return simt_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
+    if (tc_supported(h)) return tc_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
+    return simt_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
 }
 
 favor_status favor_attn_bidir_backward(favor_handle hd, const void* q, const void* k, const void* v,

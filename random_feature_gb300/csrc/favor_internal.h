@@ -68,6 +68,7 @@ struct Handle {
     int4* perm_meta;          // [H*m] per feature: (cycle start, cycle length, place in the cycle, 0)
     float* relpos_r;          // [H] decay r of causal calls (null: 1)
     void* ws_tc;              // tensor-core path scratch (bf16 operand copies), may be null
+    void* ws_bimg;            // tensor-core backward: per head S (or dS) hi / lo images + z, may be null
     size_t ws_tc_bytes;
     Profile* prof;            // per-kernel timing (host object)
 };
@@ -156,6 +157,10 @@ favor_status tc_bidir(const Handle& h, const void* q, const void* k, const void*
                       int B, int L, cudaStream_t st);
 favor_status tc_causal(const Handle& h, const void* q, const void* k, const void* v, void* out,
                        int B, int L, cudaStream_t st);
+// Tensor-core bidirectional backward (falls back to the CUDA-core one for unaligned pointers).
+favor_status tc_bidir_backward(const Handle& h, const void* q, const void* k, const void* v, const void* dout,
+                               void* dq, void* dk, void* dv, int B, int L, cudaStream_t st);
+size_t tc_bwd_image_bytes(size_t BH);
 
 // ---- fixed-order combines of per-segment states (shared by both paths) ----
 favor_status launch_reduce_segments(const Handle& h, int BH, int n_seg, cudaStream_t st);

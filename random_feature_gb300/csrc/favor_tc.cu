@@ -1562,6 +1562,580 @@ k_tc_feature_map(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     teardown(bars, tmem, 256);
 }
 
+// ============================================================ backward (bidirectional)
+// The gradients of Alg. 1 (see favor_bwd.cu for the formulas) on the tensor
+// cores.  Two steps subtract nearly equal terms (u - z (dO . out) on the query
+// side, dS~ [v 1] on the key side), so their operands enter the contractions as
+// bf16 pairs hi + lo (hi = bf16(x), lo = bf16(x - hi)): S~, dS~, the features
+// that build them, G and D.  Column sums (z, dz) accumulate in fp32 registers.
+//
+//   k_tc_bstate<MODE 0>  K, V            -> pieces of [S~ | z~]   (features from fp32, hi + lo)
+//   k_tc_bstate<MODE 1>  Q, dO, rowstat  -> pieces of [dS~ | dz~] (D = [dO/den, -go/den], hi + lo)
+//   k_bwd_reduce_pack    pieces          -> per head: S hi, S lo images (SW128 [256][64]) + z fp32
+//   k_tc_bwd_q           Q, dO, image    -> dq, rowstat (den~, row shift, dO . out)
+//   k_tc_bwd_k           K, V, image     -> dk, dv
+constexpr uint32_t kBImg = 2 * kSBytes + kM * 4;   // S hi | S lo | z (fp32)
+constexpr int kBStateThreads = 256;
+
+struct BwBars {
+    uint64_t tma;
+    uint64_t mma;
+    uint32_t tmem_base;
+    uint32_t pad;
+};
+
+// Split x into bf16 hi + lo and pack pairs: (x0, x1) -> hi word, lo word.
+__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16(x0, x1);
+    lo = pack_bf16(x0 - bf16lo(hi), x1 - bf16hi(hi));
+}
+
+// Transposed projection + features + state contraction.  grid R.G, 256 threads;
+// warp w owns features 128*(w/4) + 32*(w%4) + lane (tensor-memory lane = feature).
+// Tensor memory: half h: P^T_h [128h, 128h+128) (fp32, column = token), then the
+// packed features hi [128h, 128h+64) and lo [128h+64, 128h+128); accumulators
+// [256 + 64h, 256 + 64h + 64).
+template <int KIND, int MODE>
+__global__ void __launch_bounds__(kBStateThreads, 1)
+k_tc_bstate(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+            const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ kshift,
+            const float4* __restrict__ rowstat, float* __restrict__ part, int H, int L, float s, Ranges R, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1k(smem_raw);
+    const uint32_t s_w = smem_u32(sm);
+    const uint32_t s_x = s_w + kOmegaBytes;
+    const uint32_t s_y = s_x + kTileBytes;
+    const uint32_t s_dlo = s_y + kTileBytes;
+    float* s_c = reinterpret_cast<float*>(sm + kOmegaBytes + 3 * kTileBytes);   // [128] exponent offsets
+    float* s_wz = s_c + kTile;                                                  // [128] z-column weights
+    BwBars* bars = reinterpret_cast<BwBars*>(s_wz + kTile);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = warp >> 2, quad = warp & 3;
+    const int cta = blockIdx.x;
+    const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
+
+    if (tid == 0) {
+        mbar_init(&bars->tma, 1);
+        mbar_init(&bars->mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t t_lane = (uint32_t)(32 * quad) << 16;
+    const uint32_t t_ph = tmem + t_lane + 128 * half;           // this warp's P^T / feature columns
+    const uint32_t t_acc = tmem + t_lane + 256 + 64 * half;     // this warp's accumulator columns
+    const int r_feat = 128 * half + 32 * quad + lane;
+    const float a = s * kLog2e;
+
+    bool ok = true;
+    float zacc = 0.f;
+    bool first = true;
+    int loaded_h = -1;
+    uint32_t it = 0;
+    for (int g = g0; g < g1 && ok; ++g, ++it) {
+        const int bh = g / R.tph, tile = g - bh * R.tph, h = bh % H;
+        const int tok0 = tile * kTile;
+        if (tid == 0) {
+            uint32_t bytes = 2 * kTileBytes;
+            if (h != loaded_h) bytes += kOmegaBytes;
+            mbar_expect_tx(&bars->tma, bytes);
+            if (h != loaded_h) tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
+            tma_load_3d(sm + kOmegaBytes, &tm_x, &bars->tma, 0, tok0, bh);
+            tma_load_3d(sm + kOmegaBytes + kTileBytes, &tm_y, &bars->tma, 0, tok0, bh);
+        }
+        loaded_h = h;
+        ok = __syncthreads_and(mbar_wait(&bars->tma, it & 1, err, 41));
+        if (!ok) break;
+        if (tid < kTile) {
+            const int t = tid, tok = tok0 + t;
+            const bool live = tok < L;
+            float c = -INFINITY, wz = 0.f;
+            if (MODE == 0) {
+                if (live) {
+                    c = -(0.5f * s * s * row_sqnorm(s_x, t) + kshift[h]) * kLog2e;
+                    wz = 1.f;
+                }
+            } else {
+                float inv = 0.f;
+                if (live) {
+                    const float4 rs = rowstat[(size_t)bh * L + tok];
+                    c = -rs.y * kLog2e;
+                    inv = rs.x != 0.f ? 1.f / rs.x : 0.f;
+                    wz = -rs.z * inv;
+                }
+                // D row t = dO_t / den_t as hi (in place) + lo
+#pragma unroll
+                for (uint32_t ch = 0; ch < 8; ++ch) {
+                    const uint32_t off = sw128(t, ch);
+                    const uint4 x = ld_shared_v4(s_y + off);
+                    const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) split_pack(bf16lo(xin[i]) * inv, bf16hi(xin[i]) * inv, hi[i], lo[i]);
+                    st_shared_v4(s_y + off, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(s_dlo + off, lo[0], lo[1], lo[2], lo[3]);
+                }
+                fence_async_smem();
+            }
+            s_c[t] = c;
+            s_wz[t] = wz;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id_p = make_idesc(128, 128, 0, 0);
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+                const uint64_t a0 = make_desc(s_w + hp * 128 * 128, 16, 1024, SW_128B);
+                const uint64_t b0 = make_desc(s_x, 16, 1024, SW_128B);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 128 * hp, a0 + 2 * kk, b0 + 2 * kk, id_p, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, 0, err, 42));
+        if (!ok) break;
+        tc_fence_after();
+        {
+            float f[128];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pw[32];
+                tmem_ld32(t_ph + 32 * cc, pw);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = 32 * cc + i;
+                    const float pv = __uint_as_float(pw[i]);
+                    float x;
+                    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) x = ex2(fmaf(pv, a, s_c[t]));   // 0 for dead tokens (c = -inf)
+                    else x = s_wz[t] != 0.f || MODE == 1 ? fmaxf(s * pv, 0.f) : 0.f;
+                    f[t] = x;
+                    zacc = fmaf(x, s_wz[t], zacc);
+                }
+            }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t hw[16], lw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) split_pack(f[32 * cc + 2 * i], f[32 * cc + 2 * i + 1], hw[i], lw[i]);
+                tmem_st16(t_ph + 16 * cc, hw);
+                tmem_st16(t_ph + 64 + 16 * cc, lw);
+            }
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id_s = make_idesc(128, 64, 0, 1);
+            const uint64_t by = make_desc(s_y, 8192, 1024, SW_128B);
+            const uint64_t bl = make_desc(s_dlo, 8192, 1024, SW_128B);
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+                const uint32_t d = tmem + 256 + 64 * hp;
+                const uint32_t ahi = tmem + 128 * hp, alo = tmem + 128 * hp + 64;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) mma_ts(d, ahi + 8 * kk, by + 128 * kk, id_s, (first && kk == 0) ? 0u : 1u);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) mma_ts(d, alo + 8 * kk, by + 128 * kk, id_s, 1u);
+                if (MODE == 1) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) mma_ts(d, ahi + 8 * kk, bl + 128 * kk, id_s, 1u);
+                }
+            }
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, 1, err, 43));
+        if (!ok) break;
+        tc_fence_after();
+        first = false;
+        const bool piece_end = (g + 1 == g1) || ((g + 1) / R.tph != bh);
+        if (piece_end) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(t_acc, v0);
+            tmem_ld32(t_acc + 32, v1);
+            tmem_ld_wait();
+            const int piece = cta - first_cta(R, bh);
+            float* o = part + ((size_t)bh * R.pstride + piece) * (kM * (kDV + 1)) + (size_t)r_feat * (kDV + 1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                o[i] = __uint_as_float(v0[i]);
+                o[32 + i] = __uint_as_float(v1[i]);
+            }
+            o[kDV] = zacc;
+            zacc = 0.f;
+            first = true;
+            tc_fence_before();
+            __syncthreads();   // the accumulator is read before the next piece overwrites it
+            tc_fence_after();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// Fixed-order sum of a head's pieces (row-major [m][dv+1]) -> hi / lo SW128
+// images of the value columns and the z column in fp32.  grid (m*(dv+1)/256 up, B*H).
+__global__ void k_bwd_reduce_pack(const float* __restrict__ part, uint8_t* __restrict__ img, Ranges R) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= kM * (kDV + 1)) return;
+    const int np = last_cta(R, bh) - first_cta(R, bh) + 1;
+    const float* p = part + (size_t)bh * R.pstride * (kM * (kDV + 1)) + i;
+    float acc = 0.f;
+    for (int k = 0; k < np; ++k) acc += p[(size_t)k * (kM * (kDV + 1))];
+    const int r = i / (kDV + 1), c = i - r * (kDV + 1);
+    uint8_t* base = img + (size_t)bh * kBImg;
+    if (c == kDV) {
+        reinterpret_cast<float*>(base + 2 * kSBytes)[r] = acc;
+    } else {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
+        const uint32_t off = sw128((uint32_t)r, (uint32_t)c >> 3) + 2 * (c & 7);
+        *reinterpret_cast<__nv_bfloat16*>(base + off) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(base + kSBytes + off) = lo;
+    }
+}
+
+constexpr int kBwdThreads = 128;
+
+// Query pass, one 128-query tile per CTA.  grid (tiles, B*H), 128 threads; thread = query row.
+// Tensor memory: P [0,256), U = dO (S hi + S lo)^T [256,512); then G hi [0,128), G lo
+// [256,384) (packed, in place), dq accumulator [128,192).
+template <int KIND>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+k_tc_bwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+           const __grid_constant__ CUtensorMap tm_w, const uint8_t* __restrict__ img, __nv_bfloat16* __restrict__ dq,
+           float4* __restrict__ rowstat, int H, int L, float s, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1k(smem_raw);
+    const uint32_t s_w = smem_u32(sm);
+    const uint32_t s_img = s_w + kOmegaBytes;
+    const uint32_t s_q = s_img + kBImg;
+    const uint32_t s_do = s_q + kTileBytes;
+    const float* z = reinterpret_cast<const float*>(sm + kOmegaBytes + 2 * kSBytes);
+    BwBars* bars = reinterpret_cast<BwBars*>(sm + kOmegaBytes + kBImg + 2 * kTileBytes);
+    const int tile = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tok0 = tile * kTile, tok = tok0 + tid;
+    const bool live = tok < L;
+
+    if (tid == 0) {
+        mbar_init(&bars->tma, 1);
+        mbar_init(&bars->mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+    if (tid == 0) {
+        mbar_expect_tx(&bars->tma, kOmegaBytes + kBImg + 2 * kTileBytes);
+        tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
+        bulk_load(sm + kOmegaBytes, img + (size_t)bh * kBImg, kBImg, &bars->tma);
+        tma_load_3d(sm + kOmegaBytes + kBImg, &tm_q, &bars->tma, 0, tok0, bh);
+        tma_load_3d(sm + kOmegaBytes + kBImg + kTileBytes, &tm_do, &bars->tma, 0, tok0, bh);
+    }
+    bool ok = __syncthreads_and(mbar_wait(&bars->tma, 0, err, 44));
+    if (ok && tid == 0) {
+        tc_fence_after();
+        issue_projection(tmem, s_q, s_w, 256);
+        const uint32_t id_u = make_idesc(128, 256, 0, 0);
+        const uint64_t a0 = make_desc(s_do, 16, 1024, SW_128B);
+        const uint64_t bh0 = make_desc(s_img, 16, 1024, SW_128B);
+        const uint64_t bl0 = make_desc(s_img + kSBytes, 16, 1024, SW_128B);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bh0 + 2 * kk, id_u, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bl0 + 2 * kk, id_u, 1u);
+        mma_commit(&bars->mma);
+    }
+    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 0, err, 45));
+    tc_fence_after();
+    float gsum = 0.f;
+    if (ok) {
+        const float a = s * kLog2e;
+        float mx = 0.f;
+        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+            mx = -INFINITY;
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t pw[32];
+                tmem_ld32(tl + 32 * cc, pw);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(pw[i]));
+            }
+        }
+        const float c = -mx * a;
+        float den = 0.f, fu = 0.f;
+        for (int cc = 0; cc < 8; ++cc) {
+            uint32_t pw[32], uw[32];
+            tmem_ld32(tl + 32 * cc, pw);
+            tmem_ld32(tl + 256 + 32 * cc, uw);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float pv = __uint_as_float(pw[i]);
+                const float f = KIND == FAVOR_KERNEL_SOFTMAX_POS ? ex2(fmaf(pv, a, c)) : fmaxf(s * pv, 0.f);
+                den = fmaf(f, z[32 * cc + i], den);
+                fu = fmaf(f, __uint_as_float(uw[i]), fu);
+            }
+        }
+        const float inv = den != 0.f ? 1.f / den : 0.f;
+        const float go = fu * inv;
+        for (int cc = 0; cc < 8; ++cc) {
+            uint32_t pw[32], uw[32];
+            tmem_ld32(tl + 32 * cc, pw);
+            tmem_ld32(tl + 256 + 32 * cc, uw);
+            tmem_ld_wait();
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float gg[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 2 * i + e;
+                    const float pv = __uint_as_float(pw[k]);
+                    const float dphi = (__uint_as_float(uw[k]) - z[32 * cc + k] * go) * inv;
+                    float gv;
+                    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) gv = dphi * ex2(fmaf(pv, a, c));
+                    else gv = pv > 0.f ? dphi : 0.f;
+                    gg[e] = gv;
+                    gsum += gv;
+                }
+                split_pack(gg[0], gg[1], hw[i], lw[i]);
+            }
+            tmem_st16(tl + 16 * cc, hw);
+            tmem_st16(tl + 256 + 16 * cc, lw);
+        }
+        tmem_st_wait();
+        if (live) rowstat[(size_t)bh * L + tok] = make_float4(den, KIND == FAVOR_KERNEL_SOFTMAX_POS ? s * mx : 0.f, go, 0.f);
+    }
+    tc_fence_before();
+    ok = __syncthreads_and(ok);
+    if (ok && tid == 0) {
+        tc_fence_after();
+        const uint32_t id_q = make_idesc(128, 64, 0, 1);
+        const uint64_t bw = make_desc(s_w, 8192, 1024, SW_128B);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 8 * kk, bw + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 256 + 8 * kk, bw + 128 * kk, id_q, 1u);
+        mma_commit(&bars->mma);
+    }
+    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 1, err, 46));
+    tc_fence_after();
+    if (ok) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tl + 128, v0);
+        tmem_ld32(tl + 160, v1);
+        tmem_ld_wait();
+        if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)bh * L + tok) * kD);
+#pragma unroll
+            for (uint32_t ch = 0; ch < 8; ++ch) {
+                const uint4 x = ld_shared_v4(s_q + sw128((uint32_t)tid, ch));
+                const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c0 = 8 * ch + 2 * i;
+                    const float acc0 = __uint_as_float(c0 < 32 ? v0[c0] : v1[c0 - 32]);
+                    const float acc1 = __uint_as_float(c0 + 1 < 32 ? v0[c0 + 1] : v1[c0 + 1 - 32]);
+                    float d0 = s * acc0, d1 = s * acc1;
+                    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                        d0 = s * fmaf(-s * gsum, bf16lo(xin[i]), acc0);
+                        d1 = s * fmaf(-s * gsum, bf16hi(xin[i]), acc1);
+                    }
+                    w[i] = pack_bf16(d0, d1);
+                }
+                dst[ch] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// Key pass, one 128-key tile per CTA.  grid (tiles, B*H), 128 threads; thread = key row.
+// Tensor memory: P [0,256), dphi = V (dS hi + dS lo)^T [256,512); then G hi [0,128),
+// G lo [256,384), dk accumulator [128,192), dv accumulator [192,256).
+template <int KIND>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+k_tc_bwd_k(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+           const __grid_constant__ CUtensorMap tm_w, const uint8_t* __restrict__ img,
+           const float* __restrict__ kshift, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dvv, int H,
+           int L, float s, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1k(smem_raw);
+    const uint32_t s_w = smem_u32(sm);
+    const uint32_t s_img = s_w + kOmegaBytes;
+    const uint32_t s_k = s_img + kBImg;
+    const uint32_t s_v = s_k + kTileBytes;
+    const uint32_t s_phi = s_v + kTileBytes;   // [128 keys][256 features] bf16, four SW128 blocks
+    const float* dz = reinterpret_cast<const float*>(sm + kOmegaBytes + 2 * kSBytes);
+    BwBars* bars = reinterpret_cast<BwBars*>(sm + kOmegaBytes + kBImg + 2 * kTileBytes + 4 * kPhiBlock);
+    const int tile = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tok0 = tile * kTile, tok = tok0 + tid;
+    const bool live = tok < L;
+
+    if (tid == 0) {
+        mbar_init(&bars->tma, 1);
+        mbar_init(&bars->mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+    if (tid == 0) {
+        mbar_expect_tx(&bars->tma, kOmegaBytes + kBImg + 2 * kTileBytes);
+        tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
+        bulk_load(sm + kOmegaBytes, img + (size_t)bh * kBImg, kBImg, &bars->tma);
+        tma_load_3d(sm + kOmegaBytes + kBImg, &tm_k, &bars->tma, 0, tok0, bh);
+        tma_load_3d(sm + kOmegaBytes + kBImg + kTileBytes, &tm_v, &bars->tma, 0, tok0, bh);
+    }
+    bool ok = __syncthreads_and(mbar_wait(&bars->tma, 0, err, 47));
+    if (ok && tid == 0) {
+        tc_fence_after();
+        issue_projection(tmem, s_k, s_w, 256);
+        const uint32_t id_u = make_idesc(128, 256, 0, 0);
+        const uint64_t a0 = make_desc(s_v, 16, 1024, SW_128B);
+        const uint64_t bh0 = make_desc(s_img, 16, 1024, SW_128B);
+        const uint64_t bl0 = make_desc(s_img + kSBytes, 16, 1024, SW_128B);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bh0 + 2 * kk, id_u, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bl0 + 2 * kk, id_u, 1u);
+        mma_commit(&bars->mma);
+    }
+    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 0, err, 48));
+    tc_fence_after();
+    float gsum = 0.f;
+    if (ok) {
+        const float a = s * kLog2e;
+        const float c = live ? -(0.5f * s * s * row_sqnorm(s_k, (uint32_t)tid) + kshift[h]) * kLog2e : -INFINITY;
+        for (int cc = 0; cc < 8; ++cc) {
+            uint32_t pw[32], uw[32];
+            tmem_ld32(tl + 32 * cc, pw);
+            tmem_ld32(tl + 256 + 32 * cc, uw);
+            tmem_ld_wait();
+            uint32_t hw[16], lw[16], fw[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float gg[2], ff[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 2 * i + e;
+                    const float pv = __uint_as_float(pw[k]);
+                    const float dphi = __uint_as_float(uw[k]) + dz[32 * cc + k];
+                    float f, gv;
+                    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                        f = ex2(fmaf(pv, a, c));
+                        gv = dphi * f;
+                    } else {
+                        f = live ? fmaxf(s * pv, 0.f) : 0.f;
+                        gv = live && pv > 0.f ? dphi : 0.f;
+                    }
+                    ff[e] = f;
+                    gg[e] = gv;
+                    gsum += gv;
+                }
+                split_pack(gg[0], gg[1], hw[i], lw[i]);
+                fw[i] = pack_bf16(ff[0], ff[1]);
+            }
+            tmem_st16(tl + 16 * cc, hw);
+            tmem_st16(tl + 256 + 16 * cc, lw);
+            // features of this row, 32 columns = chunks 4*(cc%2) .. +3 of block cc/2
+            const uint32_t blk = s_phi + (uint32_t)(cc >> 1) * kPhiBlock;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st_shared_v4(blk + sw128((uint32_t)tid, (uint32_t)(4 * (cc & 1) + q)), fw[4 * q], fw[4 * q + 1],
+                             fw[4 * q + 2], fw[4 * q + 3]);
+        }
+        tmem_st_wait();
+        fence_async_smem();
+    }
+    tc_fence_before();
+    ok = __syncthreads_and(ok);
+    if (ok && tid == 0) {
+        tc_fence_after();
+        const uint32_t id_q = make_idesc(128, 64, 0, 1);
+        const uint64_t bw = make_desc(s_w, 8192, 1024, SW_128B);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 8 * kk, bw + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 256 + 8 * kk, bw + 128 * kk, id_q, 1u);
+        const uint64_t bs = make_desc(s_img, 8192, 1024, SW_128B);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const uint64_t af = make_desc(s_phi + (uint32_t)(kk >> 2) * kPhiBlock + (uint32_t)(kk & 3) * 32, 16, 1024,
+                                          SW_128B);
+            mma_ss(tmem + 192, af, bs + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->mma);
+    }
+    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 1, err, 49));
+    tc_fence_after();
+    if (ok) {
+        uint32_t v0[32], v1[32], w0[32], w1[32];
+        tmem_ld32(tl + 128, v0);
+        tmem_ld32(tl + 160, v1);
+        tmem_ld32(tl + 192, w0);
+        tmem_ld32(tl + 224, w1);
+        tmem_ld_wait();
+        if (live) {
+            uint4* dstk = reinterpret_cast<uint4*>(dk + ((size_t)bh * L + tok) * kD);
+            uint4* dstv = reinterpret_cast<uint4*>(dvv + ((size_t)bh * L + tok) * kDV);
+#pragma unroll
+            for (uint32_t ch = 0; ch < 8; ++ch) {
+                const uint4 x = ld_shared_v4(s_k + sw128((uint32_t)tid, ch));
+                const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
+                uint32_t wk[4], wv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c0 = 8 * ch + 2 * i;
+                    const float k0 = __uint_as_float(c0 < 32 ? v0[c0] : v1[c0 - 32]);
+                    const float k1 = __uint_as_float(c0 + 1 < 32 ? v0[c0 + 1] : v1[c0 + 1 - 32]);
+                    float d0 = s * k0, d1 = s * k1;
+                    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                        d0 = s * fmaf(-s * gsum, bf16lo(xin[i]), k0);
+                        d1 = s * fmaf(-s * gsum, bf16hi(xin[i]), k1);
+                    }
+                    wk[i] = pack_bf16(d0, d1);
+                    wv[i] = pack_bf16(__uint_as_float(c0 < 32 ? w0[c0] : w1[c0 - 32]),
+                                      __uint_as_float(c0 + 1 < 32 ? w0[c0 + 1] : w1[c0 + 1 - 32]));
+                }
+                dstk[ch] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                dstv[ch] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // ================================================================ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1610,6 +2184,13 @@ constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kRStages * kTileBytes + kRI
 constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kSBytes + kExtStage + kExtOmega +
                                 kM * 4 + 2 * kTileBytes + sizeof(CaBars);
 static_assert(kSmemCausal <= 232448, "causal shared memory");
+// the state kernel asks for more than half an SM's shared memory so that two
+// CTAs (each allocating all 512 tensor-memory columns) never share an SM
+constexpr size_t kSmemBState = 120 * 1024;
+static_assert(1024 + kOmegaBytes + 3 * kTileBytes + 2 * kTile * 4 + sizeof(BwBars) <= kSmemBState, "bstate smem");
+constexpr size_t kSmemBwdQ = 1024 + kOmegaBytes + kBImg + 2 * kTileBytes + sizeof(BwBars);
+constexpr size_t kSmemBwdK = 1024 + kOmegaBytes + kBImg + 2 * kTileBytes + 4 * kPhiBlock + sizeof(BwBars);
+static_assert(kSmemBwdK <= 232448, "backward key pass shared memory");
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
 
 template <typename K>
@@ -1628,6 +2209,14 @@ void allow_all_once() {
         allow_smem(k_tc_causal<FAVOR_KERNEL_RELU>, kSmemCausal);
         allow_smem(k_tc_feature_map<FAVOR_KERNEL_SOFTMAX_POS>, kSmemFmap);
         allow_smem(k_tc_feature_map<FAVOR_KERNEL_RELU>, kSmemFmap);
+        allow_smem(k_tc_bstate<FAVOR_KERNEL_SOFTMAX_POS, 0>, kSmemBState);
+        allow_smem(k_tc_bstate<FAVOR_KERNEL_SOFTMAX_POS, 1>, kSmemBState);
+        allow_smem(k_tc_bstate<FAVOR_KERNEL_RELU, 0>, kSmemBState);
+        allow_smem(k_tc_bstate<FAVOR_KERNEL_RELU, 1>, kSmemBState);
+        allow_smem(k_tc_bwd_q<FAVOR_KERNEL_SOFTMAX_POS>, kSmemBwdQ);
+        allow_smem(k_tc_bwd_q<FAVOR_KERNEL_RELU>, kSmemBwdQ);
+        allow_smem(k_tc_bwd_k<FAVOR_KERNEL_SOFTMAX_POS>, kSmemBwdK);
+        allow_smem(k_tc_bwd_k<FAVOR_KERNEL_RELU>, kSmemBwdK);
         cudaGetLastError();
     });
 }
@@ -1665,7 +2254,74 @@ favor_status launch_state(const Handle& h, const CUtensorMap& mk, const CUtensor
     return check_launch("tensor-core state kernel");
 }
 
+template <int KIND>
+favor_status tc_bidir_backward_t(const Handle& h, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                 const CUtensorMap& mdo, const CUtensorMap& mw, void* dq, void* dk, void* dv, int BH,
+                                 int L, const Ranges& R, cudaStream_t st) {
+    float4* rowstat = reinterpret_cast<float4*>(h.ws_rowstat);
+    uint8_t* img = reinterpret_cast<uint8_t*>(h.ws_bimg);
+    const dim3 cgrid((kM * (kDV + 1) + 255) / 256, BH);
+    const dim3 tgrid(R.tph, BH);
+    favor_status e;
+    {
+        ProfScope ps(h, PROF_STATE, st);
+        k_tc_bstate<KIND, 0><<<R.G, kBStateThreads, kSmemBState, st>>>(mk, mv, mw, h.kshift, nullptr, h.ws_partial,
+                                                                         h.H, L, h.s, R, h.dev_err);
+        count_launch();
+        if ((e = check_launch("backward state kernel")) != FAVOR_OK) return e;
+    }
+    {
+        ProfScope ps(h, PROF_COMBINE, st);
+        k_bwd_reduce_pack<<<cgrid, 256, 0, st>>>(h.ws_partial, img, R);
+        count_launch();
+        if ((e = check_launch("backward reduce/pack kernel")) != FAVOR_OK) return e;
+    }
+    {
+        ProfScope ps(h, PROF_BWD_QUERY, st);
+        k_tc_bwd_q<KIND><<<tgrid, kBwdThreads, kSmemBwdQ, st>>>(mq, mdo, mw, img, (__nv_bfloat16*)dq, rowstat, h.H,
+                                                                  L, h.s, h.dev_err);
+        count_launch();
+        if ((e = check_launch("backward query kernel")) != FAVOR_OK) return e;
+        k_tc_bstate<KIND, 1><<<R.G, kBStateThreads, kSmemBState, st>>>(mq, mdo, mw, h.kshift, rowstat, h.ws_partial,
+                                                                         h.H, L, h.s, R, h.dev_err);
+        count_launch();
+        if ((e = check_launch("backward query-state kernel")) != FAVOR_OK) return e;
+    }
+    {
+        ProfScope ps(h, PROF_COMBINE, st);
+        k_bwd_reduce_pack<<<cgrid, 256, 0, st>>>(h.ws_partial, img, R);
+        count_launch();
+        if ((e = check_launch("backward reduce/pack kernel")) != FAVOR_OK) return e;
+    }
+    ProfScope ps(h, PROF_BWD_KEY, st);
+    k_tc_bwd_k<KIND><<<tgrid, kBwdThreads, kSmemBwdK, st>>>(mk, mv, mw, img, h.kshift, (__nv_bfloat16*)dk,
+                                                              (__nv_bfloat16*)dv, h.H, L, h.s, h.dev_err);
+    count_launch();
+    return check_launch("backward key kernel");
+}
+
 }  // namespace
+
+size_t tc_bwd_image_bytes(size_t BH) { return BH * kBImg; }
+
+favor_status tc_bidir_backward(const Handle& h, const void* q, const void* k, const void* v, const void* dout,
+                               void* dq, void* dk, void* dv, int B, int L, cudaStream_t st) {
+    if (!h.ws_bimg || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv))
+        return simt_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, st);
+    allow_all_once();
+    const int BH = B * h.H;
+    const Ranges R = plan_ranges(BH, L, h.num_sms);
+    if ((size_t)BH * R.pstride > h.ws_partial_rows)
+        return set_error(FAVOR_ERR_INVALID_ARG, "backward workspace too small (%d x %d rows)", BH, R.pstride);
+    CUtensorMap mq, mk, mv, mdo, mw;
+    if (!map_tokens(&mq, q, BH, L) || !map_tokens(&mk, k, BH, L) || !map_tokens(&mv, v, BH, L) ||
+        !map_tokens(&mdo, dout, BH, L) || !map_omega(&mw, h.omega_bf16, h.H))
+        return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
+        return tc_bidir_backward_t<FAVOR_KERNEL_SOFTMAX_POS>(h, mq, mk, mv, mdo, mw, dq, dk, dv, BH, L, R, st);
+    return tc_bidir_backward_t<FAVOR_KERNEL_RELU>(h, mq, mk, mv, mdo, mw, dq, dk, dv, BH, L, R, st);
+}
 
 bool tc_supported(const Handle& h) {
     return h.dtype == FAVOR_DTYPE_BF16 && h.d == kD && h.dv == kDV && h.m == kM && h.cc_major >= 10 &&

@@ -130,3 +130,26 @@ def test_backward_argument_checks():
             R.favor_attn_causal_backward(f.handle, *dev, dq, dk, dv, w.B, w.L + 1)
         assert ei.value.status == R.FAVOR_ERR_INVALID_ARG
         assert R.favor_launch_count() == n0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True], ids=["bidir", "causal"])
+def test_backward_full_size_sampled_heads(causal):
+    """The bench workload (B=1, H=16, L=65536, bf16, d=dv=64, m=256) in the
+    bench's launch configuration; the oracle recomputes heads 0 and 9."""
+    import torch
+    w = CONFIGS["long_bf16"]
+    omega, q, k, v = make_workload(w, 0)
+    g = make_upstream_grad(w, 0)
+    with R.Favor(w.H, w.m, w.d, w.dv, "softmax_pos", w.dtype, omega, w.data_scale, w.B, w.L) as f:
+        dev = [to_dev(a, w.dtype) for a in (q, k, v, g)]
+        got = f.attn_backward(*dev, causal=causal)
+        torch.cuda.synchronize()
+        assert R.favor_device_error(f.handle) == 0
+        heads = [0, 9]
+        got = [to_host(t[:, heads]) for t in got]
+    sel = lambda a: np.ascontiguousarray(a[:, heads])
+    ref = (O.favor_causal_backward if causal else O.favor_bidir_backward)(
+        sel(q), sel(k), sel(v), sel(g), omega[heads], w.data_scale)
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        assert grad_err(a, b) <= TOL_GRAD[w.dtype], name
