@@ -340,51 +340,53 @@ def run_ours(args):
                   "config": f"B={w.B} H={w.H} m={w.m} d={w.d} dv={w.dv}, one token per step, positive features"}
 
     # Backward (gradients of the bidirectional and causal calls, positive
-    # features) on the same workload: CUDA-core kernels, so the roofline is
-    # the FP32 FFMA peak of the SMs at the sampled clock.
+    # features) on the same workload, one entry per call with the roofline of
+    # the unit it runs on: the bidirectional backward on the tensor cores
+    # (bf16 shape) against the sustained bf16 peak, the causal one on the CUDA
+    # cores against the FP32 FFMA peak of the SMs at the sampled clock.
     backward = None
     if args.backward_steps > 0:
         hd_ = handles["softmax_pos"]
         gd = torch.randn((w.B, w.H, w.L, w.dv), device=dev, dtype=torch.float32).to(tdt)
         grads = tuple(torch.empty_like(t) for t in (qd, kd, vd))
-        R.favor_profile_reset(hd_.handle)
         for causal in (False, True):
             hd_.attn_backward(qd, kd, vd, gd, causal=causal, grads=grads, stream=stream)
         torch.cuda.synchronize(dev)
-        R.favor_profile_reset(hd_.handle)
-        R.favor_profile_enable(hd_.handle, True)
-        per = {}
+        T = w.B * w.H * w.L
+        fpt = backward_flops_per_token_head(w)
+        bw_mhz = sampler.samples[-1][1] if sampler.samples else peaks["sm_max_mhz"]
+        fp32_peak = GB300_SMS * 128 * 2 * bw_mhz * 1e6
+        tc_shape = w.dtype == "bf16" and (w.d, w.dv, w.m) == (64, 64, 256)
+        backward = {"unit": UNIT, "flops_per_token_head": fpt,
+                    "config": f"{w.name}: B={w.B} H={w.H} L={w.L}, dq/dk/dv of one call, positive features, "
+                              f"dO ~ N(0,1)"}
         for causal in (False, True):
+            R.favor_profile_reset(hd_.handle)
+            R.favor_profile_enable(hd_.handle, True)
             b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             b0.record(stream)
             for _ in range(args.backward_steps):
                 hd_.attn_backward(qd, kd, vd, gd, causal=causal, grads=grads, stream=stream)
             b1.record(stream)
             torch.cuda.synchronize(dev)
-            per["causal" if causal else "bidir"] = b0.elapsed_time(b1) / args.backward_steps
-        R.favor_profile_enable(hd_.handle, False)
-        bk = {}
-        for sl in range(R.favor_profile_slots()):
-            ms, n = R.favor_profile_read(hd_.handle, sl)
-            if n:
-                bk[R.favor_profile_name(sl)] = {"ms_total": ms, "launches": n}
-        tot = sum(x["ms_total"] for x in bk.values())
-        for x in bk.values():
-            x["share"] = x["ms_total"] / max(tot, 1e-12)
-        T = w.B * w.H * w.L
-        ms_pair = per["bidir"] + per["causal"]
-        flops = 2 * T * backward_flops_per_token_head(w)
-        bw_mhz = sampler.samples[-1][1] if sampler.samples else peaks["sm_max_mhz"]
-        fp32_peak = GB300_SMS * 128 * 2 * bw_mhz * 1e6
-        backward = {"value": 2 * T / (ms_pair / 1e3), "unit": UNIT, "ms_per_call": per,
-                    "flops_per_token_head": backward_flops_per_token_head(w),
-                    "roofline": {"bound": "alu", "achieved": flops / (ms_pair / 1e3) / 1e12,
-                                 "peak": fp32_peak / 1e12, "unit": "TFLOP/s",
-                                 "frac": flops / (ms_pair / 1e3) / fp32_peak,
-                                 "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 flops x SM clock"},
-                    "kernels": bk,
-                    "config": f"{w.name}: B={w.B} H={w.H} L={w.L}, dq/dk/dv of one bidirectional and one "
-                              f"causal call, positive features, dO ~ N(0,1)"}
+            R.favor_profile_enable(hd_.handle, False)
+            ms = b0.elapsed_time(b1) / args.backward_steps
+            bk = {}
+            for sl in range(R.favor_profile_slots()):
+                kms, n = R.favor_profile_read(hd_.handle, sl)
+                if n:
+                    bk[R.favor_profile_name(sl)] = {"ms_per_call": kms / args.backward_steps,
+                                                    "launches_per_call": n / args.backward_steps}
+            tc = tc_shape and not causal
+            pk = peaks["bf16_tflops_sustained"] * 1e12 if tc else fp32_peak
+            ach = fpt * T / (ms / 1e3)
+            backward["causal" if causal else "bidir"] = {
+                "ms": ms, "value": T / (ms / 1e3), "path": "tensor cores" if tc else "CUDA cores",
+                "roofline": {"bound": "tensor" if tc else "alu", "achieved": ach / 1e12, "peak": pk / 1e12,
+                             "unit": "TFLOP/s", "frac": ach / pk,
+                             "peak_source": ("measured sustained bf16" if tc else
+                                             "FP32 FFMA: 152 SMs x 128 lanes x 2 flops x SM clock")},
+                "kernels": bk}
 
     # Feature variants and relative positions on the same workload, one line each:
     # hyperbolic features (tensor cores), trigonometric features, RFA-Gate gated
