@@ -1578,11 +1578,50 @@ constexpr uint32_t kBImg = 2 * kSBytes + kM * 4;   // S hi | S lo | z (fp32)
 constexpr int kBStateThreads = 256;
 
 struct BwBars {
-    uint64_t tma;
+    uint64_t head;      // per-head operands (omega, images)
+    uint64_t tile[2];   // double-buffered token tiles
     uint64_t mma;
     uint32_t tmem_base;
     uint32_t pad;
 };
+
+// Persistent loop bookkeeping of the backward kernels: the flattened (head,
+// tile) range of this CTA; token tiles are double-buffered (tile g+1 loads
+// while tile g computes), per-head operands reload only when the head changes.
+__device__ __forceinline__ void bw_init_bars(BwBars* bars) {
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->head, 1);
+        mbar_init(&bars->tile[0], 1);
+        mbar_init(&bars->tile[1], 1);
+        mbar_init(&bars->mma, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x / 32 == 0) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+}
+
+// Loads issued and not yet waited for, tracked by the issuing thread so that a
+// kernel whose bounded wait gave up still waits (bounded) for its own copies
+// before it exits: parity of the pending phase per barrier, -1 when none.
+struct BwPending {
+    int head = -1, tile[2] = {-1, -1};
+    __device__ __forceinline__ void drain(BwBars* bars, int* err, int code) {
+        if (head >= 0) mbar_wait(&bars->head, (uint32_t)head, err, code);
+        for (int b = 0; b < 2; ++b)
+            if (tile[b] >= 0) mbar_wait(&bars->tile[b], (uint32_t)tile[b], err, code);
+    }
+};
+
+// Two token tiles (x, y) of flattened tile g into buffer `dst` (x at dst, y at dst + 16 KB).
+__device__ __forceinline__ void bw_load_tiles(const CUtensorMap* mx, const CUtensorMap* my, uint8_t* dst,
+                                              uint64_t* bar, int g, int tph) {
+    const int bh = g / tph, tile = g - bh * tph;
+    mbar_expect_tx(bar, 2 * kTileBytes);
+    tma_load_3d(dst, mx, bar, 0, tile * kTile, bh);
+    tma_load_3d(dst + kTileBytes, my, bar, 0, tile * kTile, bh);
+}
 
 // Split x into bf16 hi + lo and pack pairs: (x0, x1) -> hi word, lo word.
 __device__ __forceinline__ void split_pack(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -1603,10 +1642,9 @@ k_tc_bstate(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
-    const uint32_t s_x = s_w + kOmegaBytes;
-    const uint32_t s_y = s_x + kTileBytes;
-    const uint32_t s_dlo = s_y + kTileBytes;
-    float* s_c = reinterpret_cast<float*>(sm + kOmegaBytes + 3 * kTileBytes);   // [128] exponent offsets
+    uint8_t* buf = sm + kOmegaBytes;                              // 2 x [x tile | y tile]
+    const uint32_t s_dlo = s_w + kOmegaBytes + 4 * kTileBytes;
+    float* s_c = reinterpret_cast<float*>(sm + kOmegaBytes + 5 * kTileBytes);   // [128] exponent offsets
     float* s_wz = s_c + kTile;                                                  // [128] z-column weights
     BwBars* bars = reinterpret_cast<BwBars*>(s_wz + kTile);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1614,15 +1652,7 @@ k_tc_bstate(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int cta = blockIdx.x;
     const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
 
-    if (tid == 0) {
-        mbar_init(&bars->tma, 1);
-        mbar_init(&bars->mma, 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(&bars->tmem_base, 512);
-        tmem_relinquish();
-    }
+    bw_init_bars(bars);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1632,26 +1662,48 @@ k_tc_bstate(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const uint32_t t_acc = tmem + t_lane + 256 + 64 * half;     // this warp's accumulator columns
     const int r_feat = 128 * half + 32 * quad + lane;
     const float a = s * kLog2e;
+    BwPending pend;
+    if (tid == 0 && g0 < g1) {
+        mbar_expect_tx(&bars->head, kOmegaBytes);
+        tma_load_2d(sm, &tm_w, &bars->head, 0, ((g0 / R.tph) % H) * kM);
+        pend.head = 0;
+        bw_load_tiles(&tm_x, &tm_y, buf, &bars->tile[0], g0, R.tph);
+        pend.tile[0] = 0;
+    }
 
     bool ok = true;
     float zacc = 0.f;
     bool first = true;
     int loaded_h = -1;
-    uint32_t it = 0;
-    for (int g = g0; g < g1 && ok; ++g, ++it) {
+    uint32_t nhead = 0;
+    for (int g = g0, it = 0; g < g1; ++g, ++it) {
+        const int b = it & 1;
         const int bh = g / R.tph, tile = g - bh * R.tph, h = bh % H;
         const int tok0 = tile * kTile;
+        const uint32_t s_x = s_w + kOmegaBytes + b * 2 * kTileBytes, s_y = s_x + kTileBytes;
+        __syncthreads();   // the previous tile is done with its buffers and tensor memory
+        const bool new_head = h != loaded_h;
         if (tid == 0) {
-            uint32_t bytes = 2 * kTileBytes;
-            if (h != loaded_h) bytes += kOmegaBytes;
-            mbar_expect_tx(&bars->tma, bytes);
-            if (h != loaded_h) tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
-            tma_load_3d(sm + kOmegaBytes, &tm_x, &bars->tma, 0, tok0, bh);
-            tma_load_3d(sm + kOmegaBytes + kTileBytes, &tm_y, &bars->tma, 0, tok0, bh);
+            if (new_head && it > 0) {
+                mbar_expect_tx(&bars->head, kOmegaBytes);
+                tma_load_2d(sm, &tm_w, &bars->head, 0, h * kM);
+                pend.head = (int)(nhead & 1);
+            }
+            if (g + 1 < g1) {
+                bw_load_tiles(&tm_x, &tm_y, buf + (b ^ 1) * 2 * kTileBytes, &bars->tile[b ^ 1], g + 1, R.tph);
+                pend.tile[b ^ 1] = ((it + 1) >> 1) & 1;
+            }
         }
-        loaded_h = h;
-        ok = __syncthreads_and(mbar_wait(&bars->tma, it & 1, err, 41));
+        if (new_head) {
+            ok = __syncthreads_and(mbar_wait(&bars->head, nhead & 1, err, 40));
+            ++nhead;
+            loaded_h = h;
+            if (!ok) break;
+            pend.head = -1;
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->tile[b], (it >> 1) & 1, err, 41));
         if (!ok) break;
+        pend.tile[b] = -1;
         if (tid < kTile) {
             const int t = tid, tok = tok0 + t;
             const bool live = tok < L;
@@ -1772,11 +1824,10 @@ k_tc_bstate(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             o[kDV] = zacc;
             zacc = 0.f;
             first = true;
-            tc_fence_before();
-            __syncthreads();   // the accumulator is read before the next piece overwrites it
-            tc_fence_after();
+            tc_fence_before();   // the next piece's first MMA overwrites the accumulator after the loop-top barrier
         }
     }
+    if (!ok && tid == 0) pend.drain(bars, err, 40);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
@@ -1805,332 +1856,416 @@ __global__ void k_bwd_reduce_pack(const float* __restrict__ part, uint8_t* __res
     }
 }
 
-constexpr int kBwdThreads = 128;
+constexpr int kBwdThreads = 256;   // two threads per row: features [0,128) and [128,256)
 
-// Query pass, one 128-query tile per CTA.  grid (tiles, B*H), 128 threads; thread = query row.
-// Tensor memory: P [0,256), U = dO (S hi + S lo)^T [256,512); then G hi [0,128), G lo
-// [256,384) (packed, in place), dq accumulator [128,192).
+// Per-head operands of the backward passes: omega (TMA) and the state image (bulk copy).
+__device__ __forceinline__ void bw_load_head(const CUtensorMap* mw, const uint8_t* img, uint8_t* sm, BwBars* bars,
+                                             int bh, int h) {
+    mbar_expect_tx(&bars->head, kOmegaBytes + kBImg);
+    tma_load_2d(sm, mw, &bars->head, 0, h * kM);
+    bulk_load(sm + kOmegaBytes, img + (size_t)bh * kBImg, kBImg, &bars->head);
+}
+
+// Query pass, persistent over the call's tile ranges (grid R.G, 256 threads: thread t
+// takes query row t % 128 and features 128*(t/128) .. +127 of it).  Tensor memory per
+// tile: P [0,256), U = dO (S hi + S lo)^T [256,512); each thread then writes the packed
+// G of its features as lo over its P columns (from 128 ch) and hi over its U columns
+// (from 256 + 128 ch), 64 columns each, at or behind the columns it has read; the dq
+// accumulator takes the freed [64,128).
 template <int KIND>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 k_tc_bwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
            const __grid_constant__ CUtensorMap tm_w, const uint8_t* __restrict__ img, __nv_bfloat16* __restrict__ dq,
-           float4* __restrict__ rowstat, int H, int L, float s, int* err) {
+           float4* __restrict__ rowstat, int H, int L, float s, Ranges R, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
     const uint32_t s_img = s_w + kOmegaBytes;
-    const uint32_t s_q = s_img + kBImg;
-    const uint32_t s_do = s_q + kTileBytes;
+    uint8_t* buf = sm + kOmegaBytes + kBImg;                      // 2 x [q tile | dO tile]
     const float* z = reinterpret_cast<const float*>(sm + kOmegaBytes + 2 * kSBytes);
-    BwBars* bars = reinterpret_cast<BwBars*>(sm + kOmegaBytes + kBImg + 2 * kTileBytes);
-    const int tile = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    float* red = reinterpret_cast<float*>(sm + kOmegaBytes + kBImg + 4 * kTileBytes);   // [3][2][128] row partials
+    BwBars* bars = reinterpret_cast<BwBars*>(red + 3 * 2 * kTile);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int tok0 = tile * kTile, tok = tok0 + tid;
-    const bool live = tok < L;
+    const int row = tid & (kTile - 1), ch = tid >> 7;
+    const int g0 = blockIdx.x * R.per, g1 = min(R.T, g0 + R.per);
 
-    if (tid == 0) {
-        mbar_init(&bars->tma, 1);
-        mbar_init(&bars->mma, 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(&bars->tmem_base, 512);
-        tmem_relinquish();
-    }
+    bw_init_bars(bars);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
-    if (tid == 0) {
-        mbar_expect_tx(&bars->tma, kOmegaBytes + kBImg + 2 * kTileBytes);
-        tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
-        bulk_load(sm + kOmegaBytes, img + (size_t)bh * kBImg, kBImg, &bars->tma);
-        tma_load_3d(sm + kOmegaBytes + kBImg, &tm_q, &bars->tma, 0, tok0, bh);
-        tma_load_3d(sm + kOmegaBytes + kBImg + kTileBytes, &tm_do, &bars->tma, 0, tok0, bh);
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t tp = tl + 128 * ch, tu = tl + 256 + 128 * ch;   // this thread's P and U columns
+    const float a = s * kLog2e;
+    BwPending pend;
+    if (tid == 0 && g0 < g1) {
+        bw_load_head(&tm_w, img, sm, bars, g0 / R.tph, (g0 / R.tph) % H);
+        pend.head = 0;
+        bw_load_tiles(&tm_q, &tm_do, buf, &bars->tile[0], g0, R.tph);
+        pend.tile[0] = 0;
     }
-    bool ok = __syncthreads_and(mbar_wait(&bars->tma, 0, err, 44));
-    if (ok && tid == 0) {
+    bool ok = true;
+    int loaded_bh = -1;
+    uint32_t nhead = 0;
+    for (int g = g0, it = 0; g < g1; ++g, ++it) {
+        const int b = it & 1;
+        const int bh = g / R.tph, tile = g - bh * R.tph, h = bh % H;
+        const int tok = tile * kTile + row;
+        const bool live = tok < L;
+        const uint32_t s_q = s_img + kBImg + b * 2 * kTileBytes, s_do = s_q + kTileBytes;
+        __syncthreads();   // the previous tile is done with its buffers and tensor memory
+        const bool new_head = bh != loaded_bh;
+        if (tid == 0) {
+            if (new_head && it > 0) {
+                bw_load_head(&tm_w, img, sm, bars, bh, h);
+                pend.head = (int)(nhead & 1);
+            }
+            if (g + 1 < g1) {
+                bw_load_tiles(&tm_q, &tm_do, buf + (b ^ 1) * 2 * kTileBytes, &bars->tile[b ^ 1], g + 1, R.tph);
+                pend.tile[b ^ 1] = ((it + 1) >> 1) & 1;
+            }
+        }
+        if (new_head) {
+            ok = __syncthreads_and(mbar_wait(&bars->head, nhead & 1, err, 44));
+            ++nhead;
+            loaded_bh = bh;
+            if (!ok) break;
+            pend.head = -1;
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->tile[b], (it >> 1) & 1, err, 50));
+        if (!ok) break;
+        pend.tile[b] = -1;
+        if (tid == 0) {
+            tc_fence_after();
+            issue_projection(tmem, s_q, s_w, 256);
+            const uint32_t id_u = make_idesc(128, 256, 0, 0);
+            const uint64_t a0 = make_desc(s_do, 16, 1024, SW_128B);
+            const uint64_t bh0 = make_desc(s_img, 16, 1024, SW_128B);
+            const uint64_t bl0 = make_desc(s_img + kSBytes, 16, 1024, SW_128B);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bh0 + 2 * kk, id_u, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bl0 + 2 * kk, id_u, 1u);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, 0, err, 45));
+        if (!ok) break;
         tc_fence_after();
-        issue_projection(tmem, s_q, s_w, 256);
-        const uint32_t id_u = make_idesc(128, 256, 0, 0);
-        const uint64_t a0 = make_desc(s_do, 16, 1024, SW_128B);
-        const uint64_t bh0 = make_desc(s_img, 16, 1024, SW_128B);
-        const uint64_t bl0 = make_desc(s_img + kSBytes, 16, 1024, SW_128B);
+        float gsum = 0.f;
+        {
+            float mx = 0.f;
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                mx = -INFINITY;
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t pw[32];
+                    tmem_ld32(tp + 32 * cc, pw);
+                    tmem_ld_wait();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bh0 + 2 * kk, id_u, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bl0 + 2 * kk, id_u, 1u);
-        mma_commit(&bars->mma);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 0, err, 45));
-    tc_fence_after();
-    float gsum = 0.f;
-    if (ok) {
-        const float a = s * kLog2e;
-        float mx = 0.f;
-        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-            mx = -INFINITY;
-            for (int cc = 0; cc < 8; ++cc) {
-                uint32_t pw[32];
-                tmem_ld32(tl + 32 * cc, pw);
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(pw[i]));
+                }
+                red[ch * kTile + row] = mx;
+                __syncthreads();
+                mx = fmaxf(red[row], red[kTile + row]);
+            }
+            const float c = -mx * a;
+            float den = 0.f, fu = 0.f;
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pw[32], uw[32];
+                tmem_ld32(tp + 32 * cc, pw);
+                tmem_ld32(tu + 32 * cc, uw);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(pw[i]));
-            }
-        }
-        const float c = -mx * a;
-        float den = 0.f, fu = 0.f;
-        for (int cc = 0; cc < 8; ++cc) {
-            uint32_t pw[32], uw[32];
-            tmem_ld32(tl + 32 * cc, pw);
-            tmem_ld32(tl + 256 + 32 * cc, uw);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float pv = __uint_as_float(pw[i]);
-                const float f = KIND == FAVOR_KERNEL_SOFTMAX_POS ? ex2(fmaf(pv, a, c)) : fmaxf(s * pv, 0.f);
-                den = fmaf(f, z[32 * cc + i], den);
-                fu = fmaf(f, __uint_as_float(uw[i]), fu);
-            }
-        }
-        const float inv = den != 0.f ? 1.f / den : 0.f;
-        const float go = fu * inv;
-        for (int cc = 0; cc < 8; ++cc) {
-            uint32_t pw[32], uw[32];
-            tmem_ld32(tl + 32 * cc, pw);
-            tmem_ld32(tl + 256 + 32 * cc, uw);
-            tmem_ld_wait();
-            uint32_t hw[16], lw[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float gg[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int k = 2 * i + e;
-                    const float pv = __uint_as_float(pw[k]);
-                    const float dphi = (__uint_as_float(uw[k]) - z[32 * cc + k] * go) * inv;
-                    float gv;
-                    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) gv = dphi * ex2(fmaf(pv, a, c));
-                    else gv = pv > 0.f ? dphi : 0.f;
-                    gg[e] = gv;
-                    gsum += gv;
+                for (int i = 0; i < 32; ++i) {
+                    const float pv = __uint_as_float(pw[i]);
+                    const float f = KIND == FAVOR_KERNEL_SOFTMAX_POS ? ex2(fmaf(pv, a, c)) : fmaxf(s * pv, 0.f);
+                    den = fmaf(f, z[128 * ch + 32 * cc + i], den);
+                    fu = fmaf(f, __uint_as_float(uw[i]), fu);
                 }
-                split_pack(gg[0], gg[1], hw[i], lw[i]);
             }
-            tmem_st16(tl + 16 * cc, hw);
-            tmem_st16(tl + 256 + 16 * cc, lw);
-        }
-        tmem_st_wait();
-        if (live) rowstat[(size_t)bh * L + tok] = make_float4(den, KIND == FAVOR_KERNEL_SOFTMAX_POS ? s * mx : 0.f, go, 0.f);
-    }
-    tc_fence_before();
-    ok = __syncthreads_and(ok);
-    if (ok && tid == 0) {
-        tc_fence_after();
-        const uint32_t id_q = make_idesc(128, 64, 0, 1);
-        const uint64_t bw = make_desc(s_w, 8192, 1024, SW_128B);
+            red[2 * kTile + ch * kTile + row] = den;
+            red[4 * kTile + ch * kTile + row] = fu;
+            __syncthreads();
+            den = red[2 * kTile + row] + red[3 * kTile + row];
+            fu = red[4 * kTile + row] + red[5 * kTile + row];
+            const float inv = den != 0.f ? 1.f / den : 0.f;
+            const float go = fu * inv;
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pw[32], uw[32];
+                tmem_ld32(tp + 32 * cc, pw);
+                tmem_ld32(tu + 32 * cc, uw);
+                tmem_ld_wait();
+                uint32_t hw[16], lw[16];
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 8 * kk, bw + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+                for (int i = 0; i < 16; ++i) {
+                    float gg[2];
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 256 + 8 * kk, bw + 128 * kk, id_q, 1u);
-        mma_commit(&bars->mma);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 1, err, 46));
-    tc_fence_after();
-    if (ok) {
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tl + 128, v0);
-        tmem_ld32(tl + 160, v1);
-        tmem_ld_wait();
-        if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)bh * L + tok) * kD);
-#pragma unroll
-            for (uint32_t ch = 0; ch < 8; ++ch) {
-                const uint4 x = ld_shared_v4(s_q + sw128((uint32_t)tid, ch));
-                const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c0 = 8 * ch + 2 * i;
-                    const float acc0 = __uint_as_float(c0 < 32 ? v0[c0] : v1[c0 - 32]);
-                    const float acc1 = __uint_as_float(c0 + 1 < 32 ? v0[c0 + 1] : v1[c0 + 1 - 32]);
-                    float d0 = s * acc0, d1 = s * acc1;
-                    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-                        d0 = s * fmaf(-s * gsum, bf16lo(xin[i]), acc0);
-                        d1 = s * fmaf(-s * gsum, bf16hi(xin[i]), acc1);
+                    for (int e = 0; e < 2; ++e) {
+                        const int k = 2 * i + e;
+                        const float pv = __uint_as_float(pw[k]);
+                        const float dphi = (__uint_as_float(uw[k]) - z[128 * ch + 32 * cc + k] * go) * inv;
+                        float gv;
+                        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) gv = dphi * ex2(fmaf(pv, a, c));
+                        else gv = pv > 0.f ? dphi : 0.f;
+                        gg[e] = gv;
+                        gsum += gv;
                     }
-                    w[i] = pack_bf16(d0, d1);
+                    split_pack(gg[0], gg[1], hw[i], lw[i]);
                 }
-                dst[ch] = make_uint4(w[0], w[1], w[2], w[3]);
+                tmem_st16(tu + 16 * cc, hw);
+                tmem_st16(tp + 16 * cc, lw);
+            }
+            tmem_st_wait();
+            if (live && ch == 0)
+                rowstat[(size_t)bh * L + tok] = make_float4(den, KIND == FAVOR_KERNEL_SOFTMAX_POS ? s * mx : 0.f, go, 0.f);
+            __syncthreads();   // the den / fu partials are read; reuse red for gsum
+            red[ch * kTile + row] = gsum;
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id_q = make_idesc(128, 64, 0, 1);
+            const uint64_t bw = make_desc(s_w, 8192, 1024, SW_128B);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)   // G hi: features 16 kk .. +15 at 256 + 128 (kk / 8) + 8 (kk % 8)
+                mma_ts(tmem + 64, tmem + 256 + 128 * (kk >> 3) + 8 * (kk & 7), bw + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)   // G lo at 128 (kk / 8) + 8 (kk % 8)
+                mma_ts(tmem + 64, tmem + 128 * (kk >> 3) + 8 * (kk & 7), bw + 128 * kk, id_q, 1u);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, 1, err, 46));
+        if (!ok) break;
+        tc_fence_after();
+        gsum = red[row] + red[kTile + row];
+        {
+            // thread half ch writes columns 32 ch .. 32 ch + 31 of its row's dq
+            uint32_t v0[32];
+            tmem_ld32(tl + 64 + 32 * ch, v0);
+            tmem_ld_wait();
+            if (live) {
+                uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)bh * L + tok) * kD);
+#pragma unroll
+                for (uint32_t c4 = 0; c4 < 4; ++c4) {
+                    const uint32_t chk = 4 * ch + c4;
+                    const uint4 x = ld_shared_v4(s_q + sw128((uint32_t)row, chk));
+                    const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c0 = 8 * c4 + 2 * i;
+                        const float acc0 = __uint_as_float(v0[c0]), acc1 = __uint_as_float(v0[c0 + 1]);
+                        float d0 = s * acc0, d1 = s * acc1;
+                        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                            d0 = s * fmaf(-s * gsum, bf16lo(xin[i]), acc0);
+                            d1 = s * fmaf(-s * gsum, bf16hi(xin[i]), acc1);
+                        }
+                        w[i] = pack_bf16(d0, d1);
+                    }
+                    dst[chk] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
             }
         }
+        tc_fence_before();
     }
+    if (!ok && tid == 0) pend.drain(bars, err, 44);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// Key pass, one 128-key tile per CTA.  grid (tiles, B*H), 128 threads; thread = key row.
-// Tensor memory: P [0,256), dphi = V (dS hi + dS lo)^T [256,512); then G hi [0,128),
-// G lo [256,384), dk accumulator [128,192), dv accumulator [192,256).
+// Key pass, persistent over the call's tile ranges (grid R.G, 256 threads: thread t takes
+// key row t % 128 and features 128*(t/128) .. +127 of it).  Tensor memory per tile:
+// P [0,256), dphi = V (dS hi + dS lo)^T [256,512); G packed as in the query pass (lo
+// over the thread's P columns, hi over its dphi columns), dk [64,128), dv [192,256).
 template <int KIND>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 k_tc_bwd_k(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const __grid_constant__ CUtensorMap tm_w, const uint8_t* __restrict__ img,
            const float* __restrict__ kshift, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dvv, int H,
-           int L, float s, int* err) {
+           int L, float s, Ranges R, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
     const uint32_t s_img = s_w + kOmegaBytes;
-    const uint32_t s_k = s_img + kBImg;
-    const uint32_t s_v = s_k + kTileBytes;
-    const uint32_t s_phi = s_v + kTileBytes;   // [128 keys][256 features] bf16, four SW128 blocks
+    uint8_t* buf = sm + kOmegaBytes + kBImg;                      // 2 x [k tile | v tile]
+    const uint32_t s_phi = s_img + kBImg + 4 * kTileBytes;       // [128 keys][256 features] bf16, four SW128 blocks
     const float* dz = reinterpret_cast<const float*>(sm + kOmegaBytes + 2 * kSBytes);
-    BwBars* bars = reinterpret_cast<BwBars*>(sm + kOmegaBytes + kBImg + 2 * kTileBytes + 4 * kPhiBlock);
-    const int tile = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    BwBars* bars = reinterpret_cast<BwBars*>(sm + kOmegaBytes + kBImg + 4 * kTileBytes + 4 * kPhiBlock);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int tok0 = tile * kTile, tok = tok0 + tid;
-    const bool live = tok < L;
+    const int row = tid & (kTile - 1), ch = tid >> 7;
+    const int g0 = blockIdx.x * R.per, g1 = min(R.T, g0 + R.per);
 
-    if (tid == 0) {
-        mbar_init(&bars->tma, 1);
-        mbar_init(&bars->mma, 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(&bars->tmem_base, 512);
-        tmem_relinquish();
-    }
+    bw_init_bars(bars);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
-    if (tid == 0) {
-        mbar_expect_tx(&bars->tma, kOmegaBytes + kBImg + 2 * kTileBytes);
-        tma_load_2d(sm, &tm_w, &bars->tma, 0, h * kM);
-        bulk_load(sm + kOmegaBytes, img + (size_t)bh * kBImg, kBImg, &bars->tma);
-        tma_load_3d(sm + kOmegaBytes + kBImg, &tm_k, &bars->tma, 0, tok0, bh);
-        tma_load_3d(sm + kOmegaBytes + kBImg + kTileBytes, &tm_v, &bars->tma, 0, tok0, bh);
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t tp = tl + 128 * ch, tu = tl + 256 + 128 * ch;   // this thread's P and dphi columns
+    const float a = s * kLog2e;
+    BwPending pend;
+    if (tid == 0 && g0 < g1) {
+        bw_load_head(&tm_w, img, sm, bars, g0 / R.tph, (g0 / R.tph) % H);
+        pend.head = 0;
+        bw_load_tiles(&tm_k, &tm_v, buf, &bars->tile[0], g0, R.tph);
+        pend.tile[0] = 0;
     }
-    bool ok = __syncthreads_and(mbar_wait(&bars->tma, 0, err, 47));
-    if (ok && tid == 0) {
+    bool ok = true;
+    int loaded_bh = -1;
+    uint32_t nhead = 0;
+    for (int g = g0, it = 0; g < g1; ++g, ++it) {
+        const int b = it & 1;
+        const int bh = g / R.tph, tile = g - bh * R.tph, h = bh % H;
+        const int tok = tile * kTile + row;
+        const bool live = tok < L;
+        const uint32_t s_k = s_img + kBImg + b * 2 * kTileBytes, s_v = s_k + kTileBytes;
+        // row partials [2][128]: in this tile's v buffer, which nothing reads after the dphi MMA
+        float* red = reinterpret_cast<float*>(buf + b * 2 * kTileBytes + kTileBytes);
+        __syncthreads();   // the previous tile is done with its buffers, features and tensor memory
+        const bool new_head = bh != loaded_bh;
+        if (tid == 0) {
+            if (new_head && it > 0) {
+                bw_load_head(&tm_w, img, sm, bars, bh, h);
+                pend.head = (int)(nhead & 1);
+            }
+            if (g + 1 < g1) {
+                bw_load_tiles(&tm_k, &tm_v, buf + (b ^ 1) * 2 * kTileBytes, &bars->tile[b ^ 1], g + 1, R.tph);
+                pend.tile[b ^ 1] = ((it + 1) >> 1) & 1;
+            }
+        }
+        if (new_head) {
+            ok = __syncthreads_and(mbar_wait(&bars->head, nhead & 1, err, 47));
+            ++nhead;
+            loaded_bh = bh;
+            if (!ok) break;
+            pend.head = -1;
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->tile[b], (it >> 1) & 1, err, 51));
+        if (!ok) break;
+        pend.tile[b] = -1;
+        if (tid == 0) {
+            tc_fence_after();
+            issue_projection(tmem, s_k, s_w, 256);
+            const uint32_t id_u = make_idesc(128, 256, 0, 0);
+            const uint64_t a0 = make_desc(s_v, 16, 1024, SW_128B);
+            const uint64_t bh0 = make_desc(s_img, 16, 1024, SW_128B);
+            const uint64_t bl0 = make_desc(s_img + kSBytes, 16, 1024, SW_128B);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bh0 + 2 * kk, id_u, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bl0 + 2 * kk, id_u, 1u);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, 0, err, 48));
+        if (!ok) break;
         tc_fence_after();
-        issue_projection(tmem, s_k, s_w, 256);
-        const uint32_t id_u = make_idesc(128, 256, 0, 0);
-        const uint64_t a0 = make_desc(s_v, 16, 1024, SW_128B);
-        const uint64_t bh0 = make_desc(s_img, 16, 1024, SW_128B);
-        const uint64_t bl0 = make_desc(s_img + kSBytes, 16, 1024, SW_128B);
+        float gsum = 0.f;
+        {
+            const float c = live ? -(0.5f * s * s * row_sqnorm(s_k, (uint32_t)row) + kshift[h]) * kLog2e : -INFINITY;
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pw[32], uw[32];
+                tmem_ld32(tp + 32 * cc, pw);
+                tmem_ld32(tu + 32 * cc, uw);
+                tmem_ld_wait();
+                uint32_t hw[16], lw[16], fw[16];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bh0 + 2 * kk, id_u, kk > 0 ? 1u : 0u);
+                for (int i = 0; i < 16; ++i) {
+                    float gg[2], ff[2];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + 256, a0 + 2 * kk, bl0 + 2 * kk, id_u, 1u);
-        mma_commit(&bars->mma);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 0, err, 48));
-    tc_fence_after();
-    float gsum = 0.f;
-    if (ok) {
-        const float a = s * kLog2e;
-        const float c = live ? -(0.5f * s * s * row_sqnorm(s_k, (uint32_t)tid) + kshift[h]) * kLog2e : -INFINITY;
-        for (int cc = 0; cc < 8; ++cc) {
-            uint32_t pw[32], uw[32];
-            tmem_ld32(tl + 32 * cc, pw);
-            tmem_ld32(tl + 256 + 32 * cc, uw);
+                    for (int e = 0; e < 2; ++e) {
+                        const int k = 2 * i + e;
+                        const float pv = __uint_as_float(pw[k]);
+                        const float dphi = __uint_as_float(uw[k]) + dz[128 * ch + 32 * cc + k];
+                        float f, gv;
+                        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                            f = ex2(fmaf(pv, a, c));
+                            gv = dphi * f;
+                        } else {
+                            f = live ? fmaxf(s * pv, 0.f) : 0.f;
+                            gv = live && pv > 0.f ? dphi : 0.f;
+                        }
+                        ff[e] = f;
+                        gg[e] = gv;
+                        gsum += gv;
+                    }
+                    split_pack(gg[0], gg[1], hw[i], lw[i]);
+                    fw[i] = pack_bf16(ff[0], ff[1]);
+                }
+                tmem_st16(tu + 16 * cc, hw);
+                tmem_st16(tp + 16 * cc, lw);
+                // features of this row: global 32-column chunk gc = 4 ch + cc = chunks 4 (gc % 2) .. +3 of block gc / 2
+                const int gc = 4 * ch + cc;
+                const uint32_t blk = s_phi + (uint32_t)(gc >> 1) * kPhiBlock;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st_shared_v4(blk + sw128((uint32_t)row, (uint32_t)(4 * (gc & 1) + q)), fw[4 * q], fw[4 * q + 1],
+                                 fw[4 * q + 2], fw[4 * q + 3]);
+            }
+            tmem_st_wait();
+            red[ch * kTile + row] = gsum;
+            fence_async_smem();   // generic writes (features, partials) before later async-proxy use
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id_q = make_idesc(128, 64, 0, 1);
+            const uint64_t bw = make_desc(s_w, 8192, 1024, SW_128B);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                mma_ts(tmem + 64, tmem + 256 + 128 * (kk >> 3) + 8 * (kk & 7), bw + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                mma_ts(tmem + 64, tmem + 128 * (kk >> 3) + 8 * (kk & 7), bw + 128 * kk, id_q, 1u);
+            const uint64_t bs = make_desc(s_img, 8192, 1024, SW_128B);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+                const uint64_t af = make_desc(s_phi + (uint32_t)(kk >> 2) * kPhiBlock + (uint32_t)(kk & 3) * 32, 16,
+                                              1024, SW_128B);
+                mma_ss(tmem + 192, af, bs + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, 1, err, 49));
+        if (!ok) break;
+        tc_fence_after();
+        gsum = red[row] + red[kTile + row];
+        {
+            // thread half ch writes columns 32 ch .. 32 ch + 31 of its row's dk and dv
+            uint32_t v0[32], w0[32];
+            tmem_ld32(tl + 64 + 32 * ch, v0);
+            tmem_ld32(tl + 192 + 32 * ch, w0);
             tmem_ld_wait();
-            uint32_t hw[16], lw[16], fw[16];
+            if (live) {
+                uint4* dstk = reinterpret_cast<uint4*>(dk + ((size_t)bh * L + tok) * kD);
+                uint4* dstv = reinterpret_cast<uint4*>(dvv + ((size_t)bh * L + tok) * kDV);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float gg[2], ff[2];
+                for (uint32_t c4 = 0; c4 < 4; ++c4) {
+                    const uint32_t chk = 4 * ch + c4;
+                    const uint4 x = ld_shared_v4(s_k + sw128((uint32_t)row, chk));
+                    const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t wk[4], wv[4];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int k = 2 * i + e;
-                    const float pv = __uint_as_float(pw[k]);
-                    const float dphi = __uint_as_float(uw[k]) + dz[32 * cc + k];
-                    float f, gv;
-                    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-                        f = ex2(fmaf(pv, a, c));
-                        gv = dphi * f;
-                    } else {
-                        f = live ? fmaxf(s * pv, 0.f) : 0.f;
-                        gv = live && pv > 0.f ? dphi : 0.f;
+                    for (int i = 0; i < 4; ++i) {
+                        const int c0 = 8 * c4 + 2 * i;
+                        const float k0 = __uint_as_float(v0[c0]), k1 = __uint_as_float(v0[c0 + 1]);
+                        float d0 = s * k0, d1 = s * k1;
+                        if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                            d0 = s * fmaf(-s * gsum, bf16lo(xin[i]), k0);
+                            d1 = s * fmaf(-s * gsum, bf16hi(xin[i]), k1);
+                        }
+                        wk[i] = pack_bf16(d0, d1);
+                        wv[i] = pack_bf16(__uint_as_float(w0[c0]), __uint_as_float(w0[c0 + 1]));
                     }
-                    ff[e] = f;
-                    gg[e] = gv;
-                    gsum += gv;
+                    dstk[chk] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                    dstv[chk] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
-                split_pack(gg[0], gg[1], hw[i], lw[i]);
-                fw[i] = pack_bf16(ff[0], ff[1]);
-            }
-            tmem_st16(tl + 16 * cc, hw);
-            tmem_st16(tl + 256 + 16 * cc, lw);
-            // features of this row, 32 columns = chunks 4*(cc%2) .. +3 of block cc/2
-            const uint32_t blk = s_phi + (uint32_t)(cc >> 1) * kPhiBlock;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                st_shared_v4(blk + sw128((uint32_t)tid, (uint32_t)(4 * (cc & 1) + q)), fw[4 * q], fw[4 * q + 1],
-                             fw[4 * q + 2], fw[4 * q + 3]);
-        }
-        tmem_st_wait();
-        fence_async_smem();
-    }
-    tc_fence_before();
-    ok = __syncthreads_and(ok);
-    if (ok && tid == 0) {
-        tc_fence_after();
-        const uint32_t id_q = make_idesc(128, 64, 0, 1);
-        const uint64_t bw = make_desc(s_w, 8192, 1024, SW_128B);
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 8 * kk, bw + 128 * kk, id_q, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) mma_ts(tmem + 128, tmem + 256 + 8 * kk, bw + 128 * kk, id_q, 1u);
-        const uint64_t bs = make_desc(s_img, 8192, 1024, SW_128B);
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            const uint64_t af = make_desc(s_phi + (uint32_t)(kk >> 2) * kPhiBlock + (uint32_t)(kk & 3) * 32, 16, 1024,
-                                          SW_128B);
-            mma_ss(tmem + 192, af, bs + 128 * kk, id_q, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars->mma);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(&bars->mma, 1, err, 49));
-    tc_fence_after();
-    if (ok) {
-        uint32_t v0[32], v1[32], w0[32], w1[32];
-        tmem_ld32(tl + 128, v0);
-        tmem_ld32(tl + 160, v1);
-        tmem_ld32(tl + 192, w0);
-        tmem_ld32(tl + 224, w1);
-        tmem_ld_wait();
-        if (live) {
-            uint4* dstk = reinterpret_cast<uint4*>(dk + ((size_t)bh * L + tok) * kD);
-            uint4* dstv = reinterpret_cast<uint4*>(dvv + ((size_t)bh * L + tok) * kDV);
-#pragma unroll
-            for (uint32_t ch = 0; ch < 8; ++ch) {
-                const uint4 x = ld_shared_v4(s_k + sw128((uint32_t)tid, ch));
-                const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
-                uint32_t wk[4], wv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c0 = 8 * ch + 2 * i;
-                    const float k0 = __uint_as_float(c0 < 32 ? v0[c0] : v1[c0 - 32]);
-                    const float k1 = __uint_as_float(c0 + 1 < 32 ? v0[c0 + 1] : v1[c0 + 1 - 32]);
-                    float d0 = s * k0, d1 = s * k1;
-                    if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-                        d0 = s * fmaf(-s * gsum, bf16lo(xin[i]), k0);
-                        d1 = s * fmaf(-s * gsum, bf16hi(xin[i]), k1);
-                    }
-                    wk[i] = pack_bf16(d0, d1);
-                    wv[i] = pack_bf16(__uint_as_float(c0 < 32 ? w0[c0] : w1[c0 - 32]),
-                                      __uint_as_float(c0 + 1 < 32 ? w0[c0 + 1] : w1[c0 + 1 - 32]));
-                }
-                dstk[ch] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-                dstv[ch] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
         }
+        tc_fence_before();
     }
+    if (!ok && tid == 0) pend.drain(bars, err, 47);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
@@ -2187,9 +2322,9 @@ static_assert(kSmemCausal <= 232448, "causal shared memory");
 // the state kernel asks for more than half an SM's shared memory so that two
 // CTAs (each allocating all 512 tensor-memory columns) never share an SM
 constexpr size_t kSmemBState = 120 * 1024;
-static_assert(1024 + kOmegaBytes + 3 * kTileBytes + 2 * kTile * 4 + sizeof(BwBars) <= kSmemBState, "bstate smem");
-constexpr size_t kSmemBwdQ = 1024 + kOmegaBytes + kBImg + 2 * kTileBytes + sizeof(BwBars);
-constexpr size_t kSmemBwdK = 1024 + kOmegaBytes + kBImg + 2 * kTileBytes + 4 * kPhiBlock + sizeof(BwBars);
+static_assert(1024 + kOmegaBytes + 5 * kTileBytes + 2 * kTile * 4 + sizeof(BwBars) <= kSmemBState, "bstate smem");
+constexpr size_t kSmemBwdQ = 1024 + kOmegaBytes + kBImg + 4 * kTileBytes + 3 * 2 * kTile * 4 + sizeof(BwBars);
+constexpr size_t kSmemBwdK = 1024 + kOmegaBytes + kBImg + 4 * kTileBytes + 4 * kPhiBlock + sizeof(BwBars);
 static_assert(kSmemBwdK <= 232448, "backward key pass shared memory");
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
 
@@ -2261,7 +2396,6 @@ favor_status tc_bidir_backward_t(const Handle& h, const CUtensorMap& mq, const C
     float4* rowstat = reinterpret_cast<float4*>(h.ws_rowstat);
     uint8_t* img = reinterpret_cast<uint8_t*>(h.ws_bimg);
     const dim3 cgrid((kM * (kDV + 1) + 255) / 256, BH);
-    const dim3 tgrid(R.tph, BH);
     favor_status e;
     {
         ProfScope ps(h, PROF_STATE, st);
@@ -2278,8 +2412,8 @@ favor_status tc_bidir_backward_t(const Handle& h, const CUtensorMap& mq, const C
     }
     {
         ProfScope ps(h, PROF_BWD_QUERY, st);
-        k_tc_bwd_q<KIND><<<tgrid, kBwdThreads, kSmemBwdQ, st>>>(mq, mdo, mw, img, (__nv_bfloat16*)dq, rowstat, h.H,
-                                                                  L, h.s, h.dev_err);
+        k_tc_bwd_q<KIND><<<R.G, kBwdThreads, kSmemBwdQ, st>>>(mq, mdo, mw, img, (__nv_bfloat16*)dq, rowstat, h.H,
+                                                                L, h.s, R, h.dev_err);
         count_launch();
         if ((e = check_launch("backward query kernel")) != FAVOR_OK) return e;
         k_tc_bstate<KIND, 1><<<R.G, kBStateThreads, kSmemBState, st>>>(mq, mdo, mw, h.kshift, rowstat, h.ws_partial,
@@ -2294,8 +2428,8 @@ favor_status tc_bidir_backward_t(const Handle& h, const CUtensorMap& mq, const C
         if ((e = check_launch("backward reduce/pack kernel")) != FAVOR_OK) return e;
     }
     ProfScope ps(h, PROF_BWD_KEY, st);
-    k_tc_bwd_k<KIND><<<tgrid, kBwdThreads, kSmemBwdK, st>>>(mk, mv, mw, img, h.kshift, (__nv_bfloat16*)dk,
-                                                              (__nv_bfloat16*)dv, h.H, L, h.s, h.dev_err);
+    k_tc_bwd_k<KIND><<<R.G, kBwdThreads, kSmemBwdK, st>>>(mk, mv, mw, img, h.kshift, (__nv_bfloat16*)dk,
+                                                            (__nv_bfloat16*)dv, h.H, L, h.s, R, h.dev_err);
     count_launch();
     return check_launch("backward key kernel");
 }
