@@ -787,12 +787,13 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
                     nk = fmaf(xk[c], xk[c], nk);
                 }
             } else {
-                const float* w = wg + (size_t)rr * d;
-                for (int c = 0; c < d; ++c) {
-                    const float wc = __ldg(w + c);
-                    pq = fmaf(wc, xq[c], pq);
-                    pk = fmaf(wc, xk[c], pk);
-                    nk = fmaf(xk[c], xk[c], nk);
+                const float4* w4 = reinterpret_cast<const float4*>(wg + (size_t)rr * d);   // d is a multiple of 16
+                for (int c4 = 0; c4 < d / 4; ++c4) {
+                    const float4 w = __ldg(w4 + c4);
+                    const int c = 4 * c4;
+                    pq = fmaf(w.x, xq[c], fmaf(w.y, xq[c + 1], fmaf(w.z, xq[c + 2], fmaf(w.w, xq[c + 3], pq))));
+                    pk = fmaf(w.x, xk[c], fmaf(w.y, xk[c + 1], fmaf(w.z, xk[c + 2], fmaf(w.w, xk[c + 3], pk))));
+                    nk = fmaf(xk[c], xk[c], fmaf(xk[c + 1], xk[c + 1], fmaf(xk[c + 2], xk[c + 2], fmaf(xk[c + 3], xk[c + 3], nk))));
                 }
             }
         }
@@ -815,10 +816,15 @@ __global__ void __launch_bounds__(256) k_causal_step(const T* __restrict__ q, co
             fq[tid] = f;
         }
         __syncthreads();
-        if (tid <= dv) {
-            float acc = 0.f;
-            for (int r = 0; r < m; ++r) acc = fmaf(fq[r], S[r * dp + tid], acc);
-            rs[tid] = acc;
+        // readout sums rs[e] = sum_r fq[r] S[r][e]: one warp per column, lanes over features
+        {
+            const int warp = tid >> 5, lane = tid & 31, nw = nt >> 5;
+            for (int e = warp; e <= dv; e += nw) {
+                float acc = 0.f;
+                for (int r = lane; r < m; r += 32) acc = fmaf(fq[r], S[r * dp + e], acc);
+                acc = warp_sum(acc);
+                if (lane == 0) rs[e] = acc;
+            }
         }
         __syncthreads();
         if (tid < dv) {
