@@ -171,7 +171,7 @@ def backward_flops_per_token_head(w):
 
 # Source files that define the tensor-core kernels whose DRAM traffic
 # profiles/ncu_traffic.json records: a change to any of them voids the record.
-TC_SOURCES = ("favor_tc.cu", "tc_ptx.cuh", "favor_internal.h")
+TC_SOURCES = ("favor_tc.cu", "tc_common.cuh", "tc_ptx.cuh")
 
 
 def source_digest():
