@@ -87,3 +87,16 @@ def test_launch_counter_is_monotone():
 def test_python_binding_has_c_names():
     for name in R.EXPORTED_SYMBOLS:
         assert callable(getattr(R, name))
+
+
+def test_bench_algorithmic_counts():
+    """The bench's per-token*head work counts, against hand arithmetic for the
+    bench shape (d = dv = 64, m = 256, bf16)."""
+    import bench
+    from synth import CONFIGS
+    w = CONFIGS["long_bf16"]
+    b, f, e = bench.per_token_head(w, "causal_chunks", "softmax_pos")
+    assert (b, f, e) == ((2 * 64 + 2 * 64) * 2, 4 * 256 * 64 + 4 * 256 * 65, 2 * 256)
+    b, f, e = bench.per_token_head(w, "bidir_readout", "relu")
+    assert (b, f, e) == ((64 + 64) * 2, 2 * 256 * 64 + 2 * 256 * 65, 0)
+    assert bench.backward_flops_per_token_head(w) == 8 * 256 * 64 + 6 * 256 * 65 + 4 * 256 * 64 == 296448
