@@ -120,3 +120,40 @@ def test_relpos_checks_and_clearing():
         f.set_relpos(None, None)            # cleared: the plain (tensor-core) path again
         again = to_host(f.attn(*dev, causal=True))
         np.testing.assert_array_equal(again, plain)
+
+
+def test_variants_full_size_sampled_heads():
+    """The bench workload (B=1, H=16, L=65536, bf16) through the calls the
+    bench's variants line times; the oracle recomputes heads 0 and 9."""
+    import torch
+    w = CONFIGS["long_bf16"]
+    omega, q, k, v = make_workload(w, 0)
+    heads = [0, 9]
+    sel = lambda a: np.ascontiguousarray(a[:, heads])
+    dev = [to_dev(a, w.dtype) for a in (q, k, v)]
+    rng = np.random.default_rng(3)
+    gate = rng.uniform(0.8, 1.0, (w.B, w.H, w.L)).astype(np.float32)
+    perm = np.stack([rng.permutation(w.m) for _ in range(w.H)]).astype(np.int32)
+    r = np.full(w.H, 0.999, np.float32)
+    half = np.ascontiguousarray(omega[:, : w.m // 2])
+    cases = [
+        ("softmax_hyp", half, "causal", lambda: O.favor_causal(sel(q), sel(k), sel(v), half[heads], w.data_scale,
+                                                               "softmax_hyp")),
+        ("softmax_trig", half, "causal", lambda: O.favor_causal(sel(q), sel(k), sel(v), half[heads], w.data_scale,
+                                                                "softmax_trig")),
+        ("softmax_pos", omega, "gate", lambda: O.favor_causal_gated(sel(q), sel(k), sel(v), sel(gate), omega[heads],
+                                                                    w.data_scale)),
+        ("softmax_pos", omega, "relpos", lambda: O.favor_permute(sel(q), sel(k), sel(v), omega[heads], w.data_scale,
+                                                                 perm[heads], r[heads], True)),
+    ]
+    for kind, om, mode, ref_fn in cases:
+        with R.Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, om, w.data_scale, w.B, w.L) as f:
+            if mode == "gate":
+                out = f.attn_causal_gated(*dev, torch.from_numpy(gate).cuda())
+            else:
+                if mode == "relpos":
+                    f.set_relpos(perm, r)
+                out = f.attn(*dev, causal=True)
+            got = to_host(out[:, heads])
+        ref = ref_fn()
+        assert O.row_rel_err(got, ref) <= TOL[w.dtype], (kind, mode)
