@@ -214,10 +214,11 @@ __global__ void __launch_bounds__(256) k_bwd_query(const T* __restrict__ q, cons
         }
         __syncthreads();
         if (CAUSAL) {   // aa[j][i] = phi~_q(j) . phi~_k(i), mm[j][i] = dO_j . v_i, for i <= j
-            for (int idx = threadIdx.x; idx < TT * TT; idx += blockDim.x) {
-                const int j = idx / TT, i = idx - j * TT;
+            for (int idx = threadIdx.x; idx < TT * (TT + 1) / 2; idx += blockDim.x) {   // pairs i <= j only
+                int j, i;
+                tri_pair(idx, j, i);
                 float a = 0.f, b = 0.f;
-                if (i <= j) {
+                {
                     for (int rr = 0; rr < m; ++rr) a = fmaf(fq[j * MP + rr], fk[i * MP + rr], a);
                     const float4* gj = reinterpret_cast<const float4*>(dd + j * DVP);
                     const float4* ci = reinterpret_cast<const float4*>(cs + i * DVP);
@@ -402,10 +403,11 @@ __global__ void __launch_bounds__(256) k_bwd_key(const T* __restrict__ q, const 
         if (CAUSAL) make_d(dd, den, go, TT, DV, DVP);
         __syncthreads();
         if (CAUSAL) {   // aa[j][i] = phi~_q(i) . phi~_k(j), mm[j][i] = D_i . C_j, for i >= j
-            for (int idx = threadIdx.x; idx < TT * TT; idx += blockDim.x) {
-                const int j = idx / TT, i = idx - j * TT;
+            for (int idx = threadIdx.x; idx < TT * (TT + 1) / 2; idx += blockDim.x) {   // pairs i >= j only
+                int i, j;
+                tri_pair(idx, i, j);
                 float a = 0.f, b = 0.f;
-                if (i >= j) {
+                {
                     for (int rr = 0; rr < m; ++rr) a = fmaf(fq[i * MP + rr], fk[j * MP + rr], a);
                     const float4* di = reinterpret_cast<const float4*>(dd + i * DVP);
                     const float4* cj = reinterpret_cast<const float4*>(cs + j * DVP);

@@ -408,16 +408,14 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
             }
         }
         __syncthreads();
-        for (int idx = threadIdx.x; idx < TT * TT; idx += blockDim.x) {
-            const int j = idx / TT, i = idx - j * TT;
+        for (int idx = threadIdx.x; idx < TT * (TT + 1) / 2; idx += blockDim.x) {   // pairs i <= j only
+            int j, i;
+            tri_pair(idx, j, i);
             float a = 0.f;
-            if (i <= j) {
-                for (int rr = 0; rr < m; ++rr) a = fmaf(fq[j * MP + rr], fk[i * MP + rr], a);
-                float wgt = gb[i];
-                for (int l = i + 1; l <= j; ++l) wgt *= ga[l];
-                a *= wgt;
-            }
-            aa[j * (TT + 1) + i] = a;
+            for (int rr = 0; rr < m; ++rr) a = fmaf(fq[j * MP + rr], fk[i * MP + rr], a);
+            float wgt = gb[i];
+            for (int l = i + 1; l <= j; ++l) wgt *= ga[l];
+            aa[j * (TT + 1) + i] = a * wgt;
         }
         __syncthreads();
         for (int j = warp; j < TT; j += nw) {

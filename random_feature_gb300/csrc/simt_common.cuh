@@ -108,6 +108,16 @@ __device__ __forceinline__ void token_decay(const float* gate, size_t gidx, floa
     *b = gate ? 1.f - g : 1.f;
 }
 
+// Pair number idx of the lower triangle (diagonal included), row by row:
+// (0,0), (1,0), (1,1), (2,0), ... -> (hi, lo) with lo <= hi.
+__device__ __forceinline__ void tri_pair(int idx, int& hi, int& lo) {
+    int a = (int)((sqrtf(8.f * (float)idx + 1.f) - 1.f) * 0.5f);
+    while ((a + 1) * (a + 2) / 2 <= idx) ++a;   // float rounding guards
+    while (a * (a + 1) / 2 > idx) --a;
+    hi = a;
+    lo = idx - a * (a + 1) / 2;
+}
+
 // Unscaled projections p[j] = omega_r . x_j, j < TT, of a staged token tile
 // (float4 omega row against broadcast token rows).
 template <int TT>
