@@ -88,6 +88,28 @@ def relu_kink_rows_ok(got, ref, x, omega, dphi, s, tol):
     return bad
 
 
+def check_grads(w, kind, causal, got, ref, q, k, v, g, omega):
+    """dq, dk, dv against the oracle.  ReLU dq and dk go row by row, with
+    projections on the kink allowed either way; dv has no kink dependence
+    (phi_k is continuous there)."""
+    assert grad_err(got[2], ref[2]) <= TOL_GRAD[w.dtype], "dv"
+    if kind != "relu":
+        for name, a, b in zip(("dq", "dk"), got[:2], ref[:2]):
+            assert grad_err(a, b) <= TOL_GRAD[w.dtype], name
+        return
+    vjp = O.attn_from_features_causal_vjp if causal else O.attn_from_features_bidir_vjp
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            x = w.data_scale * q[b, h].astype(np.float64)
+            y = w.data_scale * k[b, h].astype(np.float64)
+            om = omega[h].astype(np.float64)
+            pq, pk = O.feature_map(x, om, kind), O.feature_map(y, om, kind)
+            dpq, dpk, _ = vjp(pq, pk, v[b, h], g[b, h])
+            tol = TOL_GRAD[w.dtype]
+            assert relu_kink_rows_ok(got[0][b, h], ref[0][b, h], x, om, dpq, w.data_scale, tol) == 0, ("dq", b, h)
+            assert relu_kink_rows_ok(got[1][b, h], ref[1][b, h], y, om, dpk, w.data_scale, tol) == 0, ("dk", b, h)
+
+
 def _run(shape, kind, causal, L, seed):
     _, base, over = shape
     w = CONFIGS[base].replace(L=L, **over)
@@ -190,17 +212,17 @@ def test_backward_full_size_sampled_heads(causal, kind):
     sel = lambda a: np.ascontiguousarray(a[:, heads])
     ref = (O.favor_causal_backward if causal else O.favor_bidir_backward)(
         sel(q), sel(k), sel(v), sel(g), omega[heads], w.data_scale, kind)
-    assert grad_err(got[2], ref[2]) <= TOL_GRAD[w.dtype], "dv"
-    if kind == "softmax_pos":
-        for name, a, b in zip(("dq", "dk"), got[:2], ref[:2]):
-            assert grad_err(a, b) <= TOL_GRAD[w.dtype], name
-        return
-    # ReLU: dq and dk row by row, with projections on the kink allowed either way
-    vjp = O.attn_from_features_causal_vjp if causal else O.attn_from_features_bidir_vjp
-    for t, h in enumerate(heads):
-        x, y = w.data_scale * sel(q)[0, t].astype(np.float64), w.data_scale * sel(k)[0, t].astype(np.float64)
-        om = omega[h].astype(np.float64)
-        pq, pk = O.feature_map(x, om, kind), O.feature_map(y, om, kind)
-        dpq, dpk, _ = vjp(pq, pk, sel(v)[0, t], sel(g)[0, t])
-        assert relu_kink_rows_ok(got[0][0, t], ref[0][0, t], x, om, dpq, w.data_scale, TOL_GRAD[w.dtype]) == 0, "dq"
-        assert relu_kink_rows_ok(got[1][0, t], ref[1][0, t], y, om, dpk, w.data_scale, TOL_GRAD[w.dtype]) == 0, "dk"
+    check_grads(w, kind, causal, got, ref, sel(q), sel(k), sel(v), sel(g), omega[heads])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", O.KINDS)
+def test_backward_ranges_cross_heads_with_ragged_tiles(kind):
+    """B=4, H=16, L=1100 on the tensor-core shape: 576 tiles over the SMs, so a
+    CTA's range of tiles crosses head boundaries and every head ends in a
+    ragged tile (the per-head operands reload mid-range, pieces are combined
+    across CTAs)."""
+    shape = ("d64_m256_bf16", "bidir_bf16", dict(B=4, H=16))
+    w, got, ref = _run(shape, kind, False, 1100, 77)
+    omega, q, k, v = make_workload(w, 77)
+    check_grads(w, kind, False, got, ref, q, k, v, make_upstream_grad(w, 77), omega)
