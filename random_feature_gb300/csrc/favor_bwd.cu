@@ -45,12 +45,14 @@ struct BwdShape {
 
 // Shared-memory plan (floats) of one pass; every buffer starts 16-byte aligned.
 struct BwdSmem {
-    int xs, ys, cs, dd, fq, fk, ub, aa, mm, rs, zs, cq, den, go, kn, total;
+    int xs, ys, cs, dd, fq, fk, ub, aa, mm, rs, zs, cq, den, go, kn, raw, total;
 };
 
 __host__ __device__ inline int al4(int n) { return (n + 3) & ~3; }
 
-__host__ __device__ inline BwdSmem bwd_smem(int TT, int DVP, int W, int m, int d, bool causal, bool key_pass) {
+// raw_bytes: the asynchronous staging area of one tile's input rows (0: staged synchronously).
+__host__ __device__ inline BwdSmem bwd_smem(int TT, int DVP, int W, int m, int d, bool causal, bool key_pass,
+                                           int raw_bytes) {
     BwdSmem p;
     int o = 0;
     const int MP = m + 1;
@@ -69,8 +71,20 @@ __host__ __device__ inline BwdSmem bwd_smem(int TT, int DVP, int W, int m, int d
     p.den = o; o += al4(TT);
     p.go = o; o += al4(TT);
     p.kn = o; o += al4(TT);
+    p.raw = o; o += al4(raw_bytes / 4);
     p.total = o;
     return p;
+}
+
+// Raw staging bytes of one tile: the query pass reads q, dO (and k, v when
+// causal), the key pass k, v (and q, dO and the per-query row statistics when
+// causal).
+template <typename T>
+__host__ __device__ inline int bwd_raw_bytes(int TT, int d, int DV, bool causal, bool key_pass) {
+    int b = raw_rows_bytes<T>(TT, d) + raw_rows_bytes<T>(TT, DV);
+    if (causal) b *= 2;
+    if (causal && key_pass) b += TT * 16;
+    return b;
 }
 
 // D rows from dO (in place in dd), den and go: D = [dO/den, -go/den, 0...].
@@ -89,7 +103,8 @@ __device__ __forceinline__ void make_d(float* dd, const float* den, const float*
 
 // dx rows from G (row stride m+1) for a tile: dx_j = s*(G_j Omega - s*x_j sum_r G_jr)
 // (positive) or s*G_j Omega (ReLU), written as rows [t0, t0+nt) of dst; two
-// tokens x four columns per thread (one float4 omega load feeds 8 FMAs).
+// tokens x four columns per thread (one float4 omega load feeds 8 FMAs; eight
+// omega rows are in flight before the first use, m being a multiple of 16).
 template <typename T, int KIND>
 __device__ __forceinline__ void grad_inputs(const float* g, const float* xs, const float* __restrict__ om,
                                             T* __restrict__ dst, int t0, int nt, int TT, int m, int d, float s) {
@@ -103,16 +118,21 @@ __device__ __forceinline__ void grad_inputs(const float* g, const float* xs, con
         float gs0 = 0.f, gs1 = 0.f;
         const float* g0 = g + ja * (m + 1);
         const float* g1 = g + jb * (m + 1);
-#pragma unroll 4
-        for (int r = 0; r < m; ++r) {
-            const float x0 = g0[r], x1 = g1[r];
-            const float4 w = __ldg(w4 + r * d4 + c4);
-            a0.x = fmaf(x0, w.x, a0.x); a0.y = fmaf(x0, w.y, a0.y);
-            a0.z = fmaf(x0, w.z, a0.z); a0.w = fmaf(x0, w.w, a0.w);
-            a1.x = fmaf(x1, w.x, a1.x); a1.y = fmaf(x1, w.y, a1.y);
-            a1.z = fmaf(x1, w.z, a1.z); a1.w = fmaf(x1, w.w, a1.w);
-            gs0 += x0;
-            gs1 += x1;
+#pragma unroll 1
+        for (int r0 = 0; r0 < m; r0 += 8) {
+            float4 w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) w[u] = __ldg(w4 + (r0 + u) * d4 + c4);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float x0 = g0[r0 + u], x1 = g1[r0 + u];
+                a0.x = fmaf(x0, w[u].x, a0.x); a0.y = fmaf(x0, w[u].y, a0.y);
+                a0.z = fmaf(x0, w[u].z, a0.z); a0.w = fmaf(x0, w[u].w, a0.w);
+                a1.x = fmaf(x1, w[u].x, a1.x); a1.y = fmaf(x1, w[u].y, a1.y);
+                a1.z = fmaf(x1, w[u].z, a1.z); a1.w = fmaf(x1, w[u].w, a1.w);
+                gs0 += x0;
+                gs1 += x1;
+            }
         }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -148,11 +168,13 @@ __global__ void __launch_bounds__(256) k_bwd_query(const T* __restrict__ q, cons
                                                    T* __restrict__ dq, const float* __restrict__ omega,
                                                    const float* __restrict__ kshift, const float* __restrict__ state0,
                                                    float* __restrict__ part, float4* __restrict__ rowstat, int H,
-                                                   int L, int m, int d, float s, int seg_len, int n_seg) {
+                                                   int L, int m, int d, float s, int seg_len, int n_seg,
+                                                   int async_stage) {
     using S = BwdShape<DV>;
     constexpr int TT = S::TT, DVP = S::DVP, W = S::W;
     extern __shared__ __align__(16) float sm[];
-    const BwdSmem P = bwd_smem(TT, DVP, W, m, d, CAUSAL, false);
+    const BwdSmem P =
+        bwd_smem(TT, DVP, W, m, d, CAUSAL, false, async_stage ? bwd_raw_bytes<T>(TT, d, DV, CAUSAL, false) : 0);
     float *xs = sm + P.xs, *ys = sm + P.ys, *cs = sm + P.cs, *dd = sm + P.dd, *fq = sm + P.fq, *fk = sm + P.fk;
     float *ub = sm + P.ub, *aa = sm + P.aa, *mm = sm + P.mm, *zs = sm + P.zs, *cq = sm + P.cq, *den = sm + P.den,
           *go = sm + P.go, *kn = sm + P.kn;
@@ -175,16 +197,44 @@ __global__ void __launch_bounds__(256) k_bwd_query(const T* __restrict__ q, cons
         }
     }
     const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
+    // asynchronous staging: raw q | dO | k | v rows of the next tile
+    uint8_t* rq = reinterpret_cast<uint8_t*>(sm + P.raw);
+    uint8_t* rdo = rq + raw_rows_bytes<T>(TT, d);
+    uint8_t* rk = rdo + raw_rows_bytes<T>(TT, DV);
+    uint8_t* rv = rk + raw_rows_bytes<T>(TT, d);
+    auto prefetch = [&](int t) {
+        const int n = min(TT, j1 - t);
+        prefetch_rows(q + row0 * d, rq, t, n, TT, d);
+        prefetch_rows(dout + row0 * DV, rdo, t, n, TT, DV);
+        if (CAUSAL) {
+            prefetch_rows(k + row0 * d, rk, t, n, TT, d);
+            prefetch_rows(v + row0 * DV, rv, t, n, TT, DV);
+        }
+        cp_async_commit();
+    };
+    if (async_stage && j0 < j1) prefetch(j0);
     for (int t0 = j0; t0 < j1; t0 += TT) {
         const int nt = min(TT, j1 - t0);
         __syncthreads();   // the previous tile is done with every buffer
-        stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
-        stage_rows(dout + row0 * DV, dd, t0, nt, TT, DV, DVP, -1.f);
-        if (CAUSAL) {
-            stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
-            stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+        if (async_stage) {
+            cp_async_wait_all();
+            __syncthreads();   // every thread's copies of this tile have landed
+            unpack_rows<T>(rq, xs, TT, d, d, -1.f, nt);
+            unpack_rows<T>(rdo, dd, TT, DV, DVP, -1.f, nt);
+            if (CAUSAL) {
+                unpack_rows<T>(rk, ys, TT, d, d, -1.f, nt);
+                unpack_rows<T>(rv, cs, TT, DV, DVP, 1.f, nt);
+            }
+        } else {
+            stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
+            stage_rows(dout + row0 * DV, dd, t0, nt, TT, DV, DVP, -1.f);
+            if (CAUSAL) {
+                stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
+                stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+            }
         }
         __syncthreads();
+        if (async_stage && t0 + TT < j1) prefetch(t0 + TT);   // lands while this tile computes
         if (CAUSAL) key_norms(ys, kn, TT, d);
         if (own) {
             project_tile<TT>(om, xs, fq, r, m, d, s);
@@ -243,18 +293,25 @@ __global__ void __launch_bounds__(256) k_bwd_query(const T* __restrict__ q, cons
 #pragma unroll 1
             for (int j = 0; j < TT; ++j) {
                 const float4* gj = reinterpret_cast<const float4*>(dd + j * DVP);
-                float u = 0.f;
+                float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;   // independent partial sums
 #pragma unroll
                 for (int e4 = 0; e4 < DV / 4; ++e4) {
                     const float4 x = gj[e4];
-                    u = fmaf(st[4 * e4 + 0], x.x, u);
-                    u = fmaf(st[4 * e4 + 1], x.y, u);
-                    u = fmaf(st[4 * e4 + 2], x.z, u);
-                    u = fmaf(st[4 * e4 + 3], x.w, u);
+                    u0 = fmaf(st[4 * e4 + 0], x.x, u0);
+                    u1 = fmaf(st[4 * e4 + 1], x.y, u1);
+                    u2 = fmaf(st[4 * e4 + 2], x.z, u2);
+                    u3 = fmaf(st[4 * e4 + 3], x.w, u3);
                 }
-                if (CAUSAL)
-                    for (int i = 0; i <= j; ++i) u = fmaf(fk[i * MP + r], mm[j * (TT + 1) + i], u);
-                ub[j * MP + r] = u;
+                if (CAUSAL) {
+                    const float* mj = mm + j * (TT + 1);
+                    int i = 0;
+                    for (; i + 1 <= j; i += 2) {
+                        u0 = fmaf(fk[i * MP + r], mj[i], u0);
+                        u1 = fmaf(fk[(i + 1) * MP + r], mj[i + 1], u1);
+                    }
+                    if (i <= j) u2 = fmaf(fk[i * MP + r], mj[i], u2);
+                }
+                ub[j * MP + r] = (u0 + u1) + (u2 + u3);
             }
         }
         __syncthreads();
@@ -333,11 +390,13 @@ __global__ void __launch_bounds__(256) k_bwd_key(const T* __restrict__ q, const 
                                                  T* __restrict__ dk, T* __restrict__ dvv,
                                                  const float* __restrict__ omega, const float* __restrict__ kshift,
                                                  const float* __restrict__ hstate, const float4* __restrict__ rowstat,
-                                                 int H, int L, int m, int d, float s, int seg_len, int n_seg) {
+                                                 int H, int L, int m, int d, float s, int seg_len, int n_seg,
+                                                 int async_stage) {
     using S = BwdShape<DV>;
     constexpr int TT = S::TT, DVP = S::DVP, W = S::W;
     extern __shared__ __align__(16) float sm[];
-    const BwdSmem P = bwd_smem(TT, DVP, W, m, d, CAUSAL, true);
+    const BwdSmem P =
+        bwd_smem(TT, DVP, W, m, d, CAUSAL, true, async_stage ? bwd_raw_bytes<T>(TT, d, DV, CAUSAL, true) : 0);
     float *xs = sm + P.xs, *ys = sm + P.ys, *cs = sm + P.cs, *dd = sm + P.dd, *fq = sm + P.fq, *fk = sm + P.fk;
     float *aa = sm + P.aa, *mm = sm + P.mm, *rs = sm + P.rs, *cq = sm + P.cq, *den = sm + P.den, *go = sm + P.go,
           *kn = sm + P.kn;
@@ -358,19 +417,55 @@ __global__ void __launch_bounds__(256) k_bwd_key(const T* __restrict__ q, const 
     const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
     if (j0 >= j1) return;
     const int last = j0 + ((j1 - j0 - 1) / TT) * TT;
+    // asynchronous staging: raw k | v | q | dO rows and row statistics of the next tile
+    uint8_t* rk = reinterpret_cast<uint8_t*>(sm + P.raw);
+    uint8_t* rv = rk + raw_rows_bytes<T>(TT, d);
+    uint8_t* rq = rv + raw_rows_bytes<T>(TT, DV);
+    uint8_t* rdo = rq + raw_rows_bytes<T>(TT, d);
+    uint8_t* rst = rdo + raw_rows_bytes<T>(TT, DV);
+    auto prefetch = [&](int t) {
+        const int n = min(TT, j1 - t);
+        prefetch_rows(k + row0 * d, rk, t, n, TT, d);
+        prefetch_rows(v + row0 * DV, rv, t, n, TT, DV);
+        if (CAUSAL) {
+            prefetch_rows(q + row0 * d, rq, t, n, TT, d);
+            prefetch_rows(dout + row0 * DV, rdo, t, n, TT, DV);
+            for (int j = threadIdx.x; j < TT; j += blockDim.x)
+                cp_async16(rst + 16 * j, rowstat + row0 + t + (j < n ? j : 0), j < n ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    if (async_stage) prefetch(CAUSAL ? last : j0);
     for (int t0 = CAUSAL ? last : j0; CAUSAL ? t0 >= j0 : t0 < j1; t0 += CAUSAL ? -TT : TT) {
         const int nt = min(TT, j1 - t0);
         __syncthreads();
-        stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
-        stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
-        if (CAUSAL) {
-            stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
-            stage_rows(dout + row0 * DV, dd, t0, nt, TT, DV, DVP, -1.f);
-            for (int j = threadIdx.x; j < TT; j += blockDim.x) {
-                const float4 rsj = j < nt ? rowstat[row0 + t0 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
-                den[j] = rsj.x;
-                cq[j] = rsj.y;
-                go[j] = rsj.z;
+        if (async_stage) {
+            cp_async_wait_all();
+            __syncthreads();   // every thread's copies of this tile have landed
+            unpack_rows<T>(rk, ys, TT, d, d, -1.f, nt);
+            unpack_rows<T>(rv, cs, TT, DV, DVP, 1.f, nt);
+            if (CAUSAL) {
+                unpack_rows<T>(rq, xs, TT, d, d, -1.f, nt);
+                unpack_rows<T>(rdo, dd, TT, DV, DVP, -1.f, nt);
+                for (int j = threadIdx.x; j < TT; j += blockDim.x) {
+                    const float4 rsj = reinterpret_cast<const float4*>(rst)[j];   // zeros past nt
+                    den[j] = rsj.x;
+                    cq[j] = rsj.y;
+                    go[j] = rsj.z;
+                }
+            }
+        } else {
+            stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
+            stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+            if (CAUSAL) {
+                stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
+                stage_rows(dout + row0 * DV, dd, t0, nt, TT, DV, DVP, -1.f);
+                for (int j = threadIdx.x; j < TT; j += blockDim.x) {
+                    const float4 rsj = j < nt ? rowstat[row0 + t0 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    den[j] = rsj.x;
+                    cq[j] = rsj.y;
+                    go[j] = rsj.z;
+                }
             }
         }
         if (own && (CAUSAL || t0 == j0)) {
@@ -378,6 +473,10 @@ __global__ void __launch_bounds__(256) k_bwd_key(const T* __restrict__ q, const 
             for (int e = 0; e < DVP; ++e) rs[r * DVP + e] = e < DV ? hr[e < W ? e : 0] : 0.f;
         }
         __syncthreads();
+        if (async_stage) {   // the next tile lands while this one computes
+            const int nx = CAUSAL ? t0 - TT : t0 + TT;
+            if (CAUSAL ? nx >= j0 : nx < j1) prefetch(nx);
+        }
         key_norms(ys, kn, TT, d);
         if (own) {
             project_tile<TT>(om, ys, fk, r, m, d, s);
@@ -457,18 +556,26 @@ __global__ void __launch_bounds__(256) k_bwd_key(const T* __restrict__ q, const 
             for (int j = 0; j < TT; ++j) {
                 const float g = fk[j * MP + r];
                 const float4* cj = reinterpret_cast<const float4*>(cs + j * DVP);
-                float dphi = 0.f;
+                float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;   // independent partial sums
 #pragma unroll
                 for (int e4 = 0; e4 < DV / 4; ++e4) {
                     const float4 x = cj[e4];
-                    dphi = fmaf(hr[4 * e4 + 0], x.x, dphi);
-                    dphi = fmaf(hr[4 * e4 + 1], x.y, dphi);
-                    dphi = fmaf(hr[4 * e4 + 2], x.z, dphi);
-                    dphi = fmaf(hr[4 * e4 + 3], x.w, dphi);
+                    p0 = fmaf(hr[4 * e4 + 0], x.x, p0);
+                    p1 = fmaf(hr[4 * e4 + 1], x.y, p1);
+                    p2 = fmaf(hr[4 * e4 + 2], x.z, p2);
+                    p3 = fmaf(hr[4 * e4 + 3], x.w, p3);
                 }
-                dphi += j < nt ? hr[DV] : 0.f;
-                if (CAUSAL)
-                    for (int i = j; i < TT; ++i) dphi = fmaf(fq[i * MP + r], mm[j * (TT + 1) + i], dphi);
+                p3 += j < nt ? hr[DV] : 0.f;
+                if (CAUSAL) {
+                    const float* mj = mm + j * (TT + 1);
+                    int i = j;
+                    for (; i + 1 < TT; i += 2) {
+                        p0 = fmaf(fq[i * MP + r], mj[i], p0);
+                        p1 = fmaf(fq[(i + 1) * MP + r], mj[i + 1], p1);
+                    }
+                    if (i < TT) p2 = fmaf(fq[i * MP + r], mj[i], p2);
+                }
+                const float dphi = (p0 + p1) + (p2 + p3);
                 fk[j * MP + r] = KIND == FAVOR_KERNEL_SOFTMAX_POS ? dphi * g : (g > 0.f ? dphi : 0.f);
             }
             if (CAUSAL) {   // H at the previous tile's end
@@ -534,6 +641,19 @@ struct BwdCall {
     void *dq, *dk, *dv;
 };
 
+// Shared-memory plan of one pass.  Tiles are staged asynchronously when every
+// input is 16-byte aligned and the raw area still fits; otherwise synchronously.
+template <typename T, int DV, bool CAUSAL>
+BwdSmem pass_plan(const Handle& h, const BwdCall& c, bool key_pass, int* async_stage) {
+    using S = BwdShape<DV>;
+    const bool aligned = is_aligned16(c.q) && is_aligned16(c.k) && is_aligned16(c.v) && is_aligned16(c.dout);
+    const int raw = bwd_raw_bytes<T>(S::TT, h.d, DV, CAUSAL, key_pass);
+    BwdSmem P = bwd_smem(S::TT, S::DVP, S::W, h.m, h.d, CAUSAL, key_pass, raw);
+    *async_stage = aligned && P.total * sizeof(float) <= 227 * 1024 ? 1 : 0;
+    if (!*async_stage) P = bwd_smem(S::TT, S::DVP, S::W, h.m, h.d, CAUSAL, key_pass, 0);
+    return P;
+}
+
 template <typename T, int KIND, int DV, bool CAUSAL>
 favor_status bwd_passes(const Handle& h, const BwdCall& c, int BH, int L, const SegPlan& p, cudaStream_t st) {
     using S = BwdShape<DV>;
@@ -544,14 +664,15 @@ favor_status bwd_passes(const Handle& h, const BwdCall& c, int BH, int L, const 
     float* qsum = CAUSAL ? h.ws_partial2 : h.ws_partial;     // per-segment sums of phi~_q D^T
     float4* rowstat = reinterpret_cast<float4*>(h.ws_rowstat);
     {
-        const BwdSmem P = bwd_smem(S::TT, S::DVP, S::W, h.m, h.d, CAUSAL, false);
+        int as = 0;
+        const BwdSmem P = pass_plan<T, DV, CAUSAL>(h, c, false, &as);
         auto kern = k_bwd_query<T, KIND, DV, CAUSAL>;
         favor_status e = set_smem_bytes(kern, P.total * sizeof(float));
         if (e != FAVOR_OK) return e;
         ProfScope ps(h, PROF_BWD_QUERY, st);
         kern<<<grid, threads, P.total * sizeof(float), st>>>(
             (const T*)c.q, (const T*)c.k, (const T*)c.v, (const T*)c.dout, (T*)c.dq, h.omega_f32,
-            h.kshift, CAUSAL ? h.ws_partial : h.ws_state, qsum, rowstat, h.H, L, h.m, h.d, h.s, seg_len, p.n_seg);
+            h.kshift, CAUSAL ? h.ws_partial : h.ws_state, qsum, rowstat, h.H, L, h.m, h.d, h.s, seg_len, p.n_seg, as);
         count_launch();
         e = check_launch("backward query kernel");
         if (e != FAVOR_OK) return e;
@@ -564,7 +685,8 @@ favor_status bwd_passes(const Handle& h, const BwdCall& c, int BH, int L, const 
         favor_status e = check_launch("backward combine kernel");
         if (e != FAVOR_OK) return e;
     }
-    const BwdSmem P = bwd_smem(S::TT, S::DVP, S::W, h.m, h.d, CAUSAL, true);
+    int as = 0;
+    const BwdSmem P = pass_plan<T, DV, CAUSAL>(h, c, true, &as);
     auto kern = k_bwd_key<T, KIND, DV, CAUSAL>;
     favor_status e = set_smem_bytes(kern, P.total * sizeof(float));
     if (e != FAVOR_OK) return e;
@@ -572,7 +694,7 @@ favor_status bwd_passes(const Handle& h, const BwdCall& c, int BH, int L, const 
     kern<<<grid, threads, P.total * sizeof(float), st>>>(
         (const T*)c.q, (const T*)c.k, (const T*)c.v, (const T*)c.dout, (T*)c.dk, (T*)c.dv,
         h.omega_f32, h.kshift, CAUSAL ? h.ws_partial2 : h.ws_dstate, rowstat, h.H, L, h.m, h.d, h.s, seg_len,
-        p.n_seg);
+        p.n_seg, as);
     count_launch();
     return check_launch("backward key kernel");
 }

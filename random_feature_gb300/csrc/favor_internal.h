@@ -95,6 +95,8 @@ SegPlan plan_segments(int BH, int L, int num_sms);
 
 // Bookkeeping shared by every launcher.
 void count_launch(int n = 1);
+// 16-byte alignment of a device pointer (asynchronous 16-byte copies need it).
+inline bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 favor_status set_error(favor_status st, const char* fmt, ...);
 favor_status check_launch(const char* what);
 

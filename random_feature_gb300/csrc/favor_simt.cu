@@ -19,8 +19,6 @@
 namespace favor {
 namespace {
 
-constexpr int kTokTile = 32;  // tokens staged per shared-memory tile in the state/causal kernels
-
 // ---------------------------------------------------------------- feature map
 // grid (ceil(L/16), B*H), 256 threads.  Output phi[bh, i, r] = plain definition.
 template <typename T, int KIND>
@@ -79,7 +77,7 @@ __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, 
                                                        int H, int L, int m, int d, float s, int seg_len, int n_seg,
                                                        const int* __restrict__ pcyc, const int4* __restrict__ pmeta,
                                                        const float* __restrict__ gate, const float* __restrict__ rdec,
-                                                       float* __restrict__ segdecay) {
+                                                       float* __restrict__ segdecay, int async_stage) {
     using F = FwdShape<DV>;
     constexpr int TT = F::TT, DVP = F::DVP, W = F::W;
     extern __shared__ __align__(16) float sm[];
@@ -90,6 +88,8 @@ __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, 
     float* kn = fk + al4f(TT * MP);          // [TT]
     float* ga = kn + TT;                     // [TT] a_j
     float* gb = ga + TT;                     // [TT] b_j
+    uint8_t* rk = reinterpret_cast<uint8_t*>(gb + TT);   // raw k | v rows of the next tile (async staging)
+    uint8_t* rv = rk + raw_rows_bytes<T>(TT, d);
     const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
     const int r = threadIdx.x;
     const bool own = r < m;
@@ -105,11 +105,25 @@ __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, 
     const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
     PermCursor pc;
     pc.init_inv(pcyc, pmeta, h, m, own ? r : 0, j0);
+    auto prefetch = [&](int t) {
+        const int n = min(TT, j1 - t);
+        prefetch_rows(k + row0 * d, rk, t, n, TT, d);
+        prefetch_rows(v + row0 * DV, rv, t, n, TT, DV);
+        cp_async_commit();
+    };
+    if (async_stage && j0 < j1) prefetch(j0);
     for (int t0 = j0; t0 < j1; t0 += TT) {
         const int nt = min(TT, j1 - t0);
         __syncthreads();
-        stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
-        stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+        if (async_stage) {
+            cp_async_wait_all();
+            __syncthreads();   // every thread's copies of this tile have landed
+            unpack_rows<T>(rk, ys, TT, d, d, -1.f, nt);
+            unpack_rows<T>(rv, cs, TT, DV, DVP, 1.f, nt);
+        } else {
+            stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
+            stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+        }
         if (decay)
             for (int j = threadIdx.x; j < TT; j += blockDim.x) {
                 float a = 1.f, b = 0.f;
@@ -118,6 +132,7 @@ __global__ void __launch_bounds__(256) k_segment_state(const T* __restrict__ k, 
                 gb[j] = b;
             }
         __syncthreads();
+        if (async_stage && t0 + TT < j1) prefetch(t0 + TT);   // lands while this tile computes
         key_norms(ys, kn, TT, d);
         __syncthreads();
         if (own) {
@@ -213,7 +228,8 @@ template <typename T, int KIND, int DV>
 __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const float* __restrict__ state,
                                                  const float* __restrict__ omega, T* __restrict__ out,
                                                  int H, int L, int m, int d, float s, int seg_len, int n_seg,
-                                                 const int* __restrict__ pcyc, const int4* __restrict__ pmeta) {
+                                                 const int* __restrict__ pcyc, const int4* __restrict__ pmeta,
+                                                 int async_stage) {
     using F = FwdShape<DV>;
     constexpr int TT = F::TT, DVP = F::DVP, W = F::W;
     extern __shared__ __align__(16) float sm[];
@@ -224,6 +240,7 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
     float* fq = raw + al4f(TT * MP);         // [TT][m+1] features by slot
     float* cq = fq + al4f(TT * MP);          // [TT]
     float* den = cq + TT;                    // [TT]
+    uint8_t* rq = reinterpret_cast<uint8_t*>(den + TT);   // raw q rows of the next tile (async staging)
     const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
     const int r = threadIdx.x;
     const bool own = r < m;
@@ -240,11 +257,23 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
     const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
     PermCursor pc;
     pc.init_inv(pcyc, pmeta, h, m, own ? r : 0, j0);
+    auto prefetch = [&](int t) {
+        prefetch_rows(q + row0 * d, rq, t, min(TT, j1 - t), TT, d);
+        cp_async_commit();
+    };
+    if (async_stage && j0 < j1) prefetch(j0);
     for (int t0 = j0; t0 < j1; t0 += TT) {
         const int nt = min(TT, j1 - t0);
         __syncthreads();
-        stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
+        if (async_stage) {
+            cp_async_wait_all();
+            __syncthreads();   // every thread's copies of this tile have landed
+            unpack_rows<T>(rq, xs, TT, d, d, -1.f, nt);
+        } else {
+            stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
+        }
         __syncthreads();
+        if (async_stage && t0 + TT < j1) prefetch(t0 + TT);   // lands while this tile computes
         float p[TT];
         if (own) {
             project_regs<TT>(om, xs, r, d, p);
@@ -318,7 +347,7 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
                                                         int H, int L, int m, int d, float s, int seg_len, int n_seg,
                                                         const int* __restrict__ pcyc, const int4* __restrict__ pmeta,
                                                         const float* __restrict__ gate,
-                                                        const float* __restrict__ rdec) {
+                                                        const float* __restrict__ rdec, int async_stage) {
     using F = FwdShape<DV>;
     constexpr int TT = F::TT, DVP = F::DVP, W = F::W;
     extern __shared__ __align__(16) float sm[];
@@ -339,6 +368,9 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
     float* pj = gb + TT;                     // [TT] P_j
     float* wi = pj + TT;                     // [TT] w_i
     float* pt = wi + TT;                     // [4] P_tile
+    uint8_t* rq = reinterpret_cast<uint8_t*>(pt + 4);   // raw q | k | v rows of the next tile (async staging)
+    uint8_t* rk = rq + raw_rows_bytes<T>(TT, d);
+    uint8_t* rv = rk + raw_rows_bytes<T>(TT, d);
     const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
     const int r = threadIdx.x;
     const bool own = r < m;
@@ -358,12 +390,28 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
     const int j0 = seg * seg_len, j1 = min(L, j0 + seg_len);
     PermCursor pc;
     pc.init_inv(pcyc, pmeta, h, m, own ? r : 0, j0);
+    auto prefetch = [&](int t) {
+        const int n = min(TT, j1 - t);
+        prefetch_rows(q + row0 * d, rq, t, n, TT, d);
+        prefetch_rows(k + row0 * d, rk, t, n, TT, d);
+        prefetch_rows(v + row0 * DV, rv, t, n, TT, DV);
+        cp_async_commit();
+    };
+    if (async_stage && j0 < j1) prefetch(j0);
     for (int t0 = j0; t0 < j1; t0 += TT) {
         const int nt = min(TT, j1 - t0);
         __syncthreads();   // the previous tile's state update is done
-        stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
-        stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
-        stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+        if (async_stage) {
+            cp_async_wait_all();
+            __syncthreads();   // every thread's copies of this tile have landed
+            unpack_rows<T>(rq, xs, TT, d, d, -1.f, nt);
+            unpack_rows<T>(rk, ys, TT, d, d, -1.f, nt);
+            unpack_rows<T>(rv, cs, TT, DV, DVP, 1.f, nt);
+        } else {
+            stage_rows(q + row0 * d, xs, t0, nt, TT, d, d, -1.f);
+            stage_rows(k + row0 * d, ys, t0, nt, TT, d, d, -1.f);
+            stage_rows(v + row0 * DV, cs, t0, nt, TT, DV, DVP, 1.f);
+        }
         for (int j = threadIdx.x; j < TT; j += blockDim.x) {
             float a = 1.f, b = j < nt ? 1.f : 0.f;
             if (decay && j < nt) token_decay(gate, row0 + t0 + j, rd, &a, &b);
@@ -371,6 +419,7 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
             gb[j] = b;
         }
         __syncthreads();
+        if (async_stage && t0 + TT < j1) prefetch(t0 + TT);   // lands while this tile computes
         key_norms(ys, kn, TT, d);
         if (threadIdx.x == 32 * (nw - 1)) {   // decay weights, one thread (TT <= 32 steps)
             float P = 1.f;
@@ -492,6 +541,14 @@ static void set_smem(K kern, size_t bytes) {
     if (bytes > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// Asynchronous staging of a segment kernel's input tiles: on when every input
+// is 16-byte aligned and the raw area (raw_bytes) still fits next to the
+// kernel's buffers (base bytes); the returned size includes it when on.
+static size_t with_raw(size_t base, size_t raw_bytes, bool aligned, int* async_stage) {
+    *async_stage = aligned && base + raw_bytes <= 227 * 1024 ? 1 : 0;
+    return *async_stage ? base + raw_bytes : base;
+}
+
 template <typename T, int KIND>
 favor_status feature_map_t(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st) {
     const size_t smem = (16 * h.d + 16) * sizeof(float);
@@ -506,14 +563,17 @@ template <typename T, int KIND, int DV>
 favor_status state_t(const Handle& h, const void* k, const void* v, int BH, int L, const SegPlan& p,
                      const RelposArgs& rp, cudaStream_t st) {
     using F = FwdShape<DV>;
-    const size_t smem = (size_t)(F::TT * h.d + F::TT * F::DVP + al4f(F::TT * (h.m + 1)) + 3 * F::TT) * sizeof(float);
+    int as = 0;
+    const size_t smem = with_raw(
+        (size_t)(F::TT * h.d + F::TT * F::DVP + al4f(F::TT * (h.m + 1)) + 3 * F::TT) * sizeof(float),
+        raw_rows_bytes<T>(F::TT, h.d) + raw_rows_bytes<T>(F::TT, DV), is_aligned16(k) && is_aligned16(v), &as);
     auto kern = k_segment_state<T, KIND, DV>;
     set_smem(kern, smem);
     dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_STATE, st);
     kern<<<grid, 256, smem, st>>>((const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial, h.H, L, h.m,
                                   h.d, h.s, p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta, rp.gate, rp.rdec,
-                                  rp.segdecay);
+                                  rp.segdecay, as);
     count_launch();
     return check_launch("segment state kernel");
 }
@@ -523,13 +583,16 @@ favor_status readout_dv(const Handle& h, const void* q, void* out, int BH, int L
                         const RelposArgs& rp) {
     using F = FwdShape<DV>;
     const SegPlan p = plan_segments(BH, L, h.num_sms);
-    const size_t smem = (size_t)(h.m * F::DVP + F::TT * h.d + 2 * al4f(F::TT * (h.m + 1)) + 2 * F::TT) * sizeof(float);
+    int as = 0;
+    const size_t smem =
+        with_raw((size_t)(h.m * F::DVP + F::TT * h.d + 2 * al4f(F::TT * (h.m + 1)) + 2 * F::TT) * sizeof(float),
+                 raw_rows_bytes<T>(F::TT, h.d), is_aligned16(q), &as);
     auto kern = k_readout<T, KIND, DV>;
     set_smem(kern, smem);
     dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_READOUT, st);
     kern<<<grid, 256, smem, st>>>((const T*)q, h.ws_state, h.omega_f32, (T*)out, h.H, L, h.m, h.d, h.s,
-                                  p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta);
+                                  p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta, as);
     count_launch();
     return check_launch("readout kernel");
 }
@@ -551,17 +614,20 @@ favor_status causal_t(const Handle& h, const void* q, const void* k, const void*
                       const SegPlan& p, const RelposArgs& rp, cudaStream_t st) {
     using F = FwdShape<DV>;
     const int TT = F::TT;
-    const size_t smem = (size_t)(h.m * F::DVP + 2 * TT * h.d + TT * F::DVP + 3 * al4f(TT * (h.m + 1)) +
+    const size_t base = (size_t)(h.m * F::DVP + 2 * TT * h.d + TT * F::DVP + 3 * al4f(TT * (h.m + 1)) +
                                  al4f(TT * (TT + 1)) + 8 * TT + 4) * sizeof(float);
-    if (smem > 227 * 1024)
-        return set_error(FAVOR_ERR_UNSUPPORTED, "causal: %zu bytes of shared memory", smem);
+    if (base > 227 * 1024)
+        return set_error(FAVOR_ERR_UNSUPPORTED, "causal: %zu bytes of shared memory", base);
+    int as = 0;
+    const size_t smem = with_raw(base, 2 * raw_rows_bytes<T>(TT, h.d) + raw_rows_bytes<T>(TT, DV),
+                                 is_aligned16(q) && is_aligned16(k) && is_aligned16(v), &as);
     auto kern = k_causal_segment<T, KIND, DV>;
     set_smem(kern, smem);
     dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_CAUSAL, st);
     kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial,
                                   (T*)out, h.H, L, h.m, h.d, h.s, p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta,
-                                  rp.gate, rp.rdec);
+                                  rp.gate, rp.rdec, as);
     count_launch();
     return check_launch("causal segment kernel");
 }

@@ -151,17 +151,7 @@ template <int TT>
 __device__ __forceinline__ void project_tile(const float* __restrict__ om, const float* xs, float* buf, int r, int m,
                                              int d, float s) {
     float p[TT];
-#pragma unroll
-    for (int j = 0; j < TT; ++j) p[j] = 0.f;
-    const float4* w4 = reinterpret_cast<const float4*>(om + (size_t)r * d);
-    const float4* x4 = reinterpret_cast<const float4*>(xs);
-    const int d4 = d >> 2;
-#pragma unroll 1
-    for (int c4 = 0; c4 < d4; ++c4) {
-        const float4 w = __ldg(w4 + c4);
-#pragma unroll
-        for (int j = 0; j < TT; ++j) p[j] += dot4(w, x4[j * d4 + c4]);
-    }
+    project_regs<TT>(om, xs, r, d, p);
 #pragma unroll
     for (int j = 0; j < TT; ++j) buf[j * (m + 1) + r] = s * p[j];
 }
@@ -179,6 +169,58 @@ __device__ __forceinline__ void stage_rows(const T* __restrict__ src, float* dst
             else if (c == w && one_col >= 0.f) x = one_col;
         }
         dst[idx] = x;
+    }
+}
+
+// Asynchronous tile staging: the rows of the next tile are copied into a raw
+// shared-memory area while the current tile computes, then unpacked to fp32.
+// 16-byte copies; a copy with src_bytes = 0 reads nothing and writes zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(a), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// Bytes of a raw tile of TT rows of w elements.
+template <typename T>
+__host__ __device__ __forceinline__ int raw_rows_bytes(int TT, int w) { return TT * w * (int)sizeof(T); }
+
+// Start copying rows [t0, t0+nt) of a [BH, L, w] tensor (16-byte aligned base,
+// w * sizeof(T) a multiple of 16) into raw[TT][w]; rows past nt become zeros.
+template <typename T>
+__device__ __forceinline__ void prefetch_rows(const T* __restrict__ src, uint8_t* raw, int t0, int nt, int TT, int w) {
+    const int cpr = w * (int)sizeof(T) / 16;
+    for (int idx = threadIdx.x; idx < TT * cpr; idx += blockDim.x) {
+        const int j = idx / cpr, c = idx - j * cpr;
+        const bool live = j < nt;
+        const uint8_t* g = reinterpret_cast<const uint8_t*>(src + (size_t)(t0 + (live ? j : 0)) * w) + 16 * c;
+        cp_async16(raw + (size_t)idx * 16, g, live ? 16 : 0);
+    }
+}
+
+// raw[TT][w] -> dst[TT][stride] as fp32; columns [w, stride) are zero, column w
+// is one_col (if >= 0) on rows below nt.  Equals stage_rows of the same rows.
+template <typename T>
+__device__ __forceinline__ void unpack_rows(const uint8_t* raw, float* dst, int TT, int w, int stride, float one_col,
+                                            int nt) {
+    const int s4 = stride >> 2;
+    for (int idx = threadIdx.x; idx < TT * s4; idx += blockDim.x) {
+        const int j = idx / s4, c = 4 * (idx - j * s4);
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < w) {
+            const uint8_t* e = raw + ((size_t)j * w + c) * sizeof(T);
+            if (sizeof(T) == 4) {
+                x = *reinterpret_cast<const float4*>(e);
+            } else {
+                const uint2 b = *reinterpret_cast<const uint2*>(e);
+                x = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xffff0000u),
+                                __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xffff0000u));
+            }
+        } else if (c == w && one_col >= 0.f && j < nt) {
+            x.x = one_col;
+        }
+        *reinterpret_cast<float4*>(dst + (size_t)j * stride + c) = x;
     }
 }
 

@@ -14,3 +14,15 @@ def to_dev(a, dtype):
 def to_host(t):
     import torch
     return t.to(torch.float32).cpu().numpy().astype(np.float64)
+
+
+def to_dev_unaligned(a, dtype):
+    """Like to_dev, but the tensor starts one element past a 16-byte boundary
+    (the calls must take their paths for unaligned pointers)."""
+    import torch
+    t = to_dev(a, dtype)
+    buf = torch.empty(t.numel() + 16, dtype=t.dtype, device=t.device)
+    u = buf[1:1 + t.numel()].view(t.shape)
+    u.copy_(t)
+    assert u.data_ptr() % 16 != 0
+    return u

@@ -21,7 +21,7 @@ import oracle as O
 import random_feature_gb300 as R
 from synth import CONFIGS, make_upstream_grad, make_workload
 
-from _util import to_dev, to_host
+from _util import to_dev, to_dev_unaligned, to_host
 
 TOL_GRAD = {"f32": 1e-3, "bf16": 2e-2}
 
@@ -226,3 +226,24 @@ def test_backward_ranges_cross_heads_with_ragged_tiles(kind):
     w, got, ref = _run(shape, kind, False, 1100, 77)
     omega, q, k, v = make_workload(w, 77)
     check_grads(w, kind, False, got, ref, q, k, v, make_upstream_grad(w, 77), omega)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", [SHAPES[0], SHAPES[2]], ids=[SHAPES[0][0], SHAPES[2][0]])
+@pytest.mark.parametrize("causal", [False, True], ids=["bidir", "causal"])
+def test_backward_unaligned_inputs(shape, causal):
+    """q, k, v, dO one element past a 16-byte boundary: tiles are staged with
+    plain loads instead of asynchronous copies (and the tensor-core shape runs
+    on the CUDA cores); same gradients."""
+    _, base, over = shape
+    w = CONFIGS[base].replace(L=700, **over)
+    omega, q, k, v = make_workload(w, 23)
+    g = make_upstream_grad(w, 23)
+    bwd = O.favor_causal_backward if causal else O.favor_bidir_backward
+    ref = bwd(q, k, v, g, omega, w.data_scale, "softmax_pos")
+    with R.Favor(w.H, w.m, w.d, w.dv, "softmax_pos", w.dtype, omega, w.data_scale, w.B, w.L) as f:
+        dev = [to_dev_unaligned(a, w.dtype) for a in (q, k, v, g)]
+        got = [to_host(t) for t in f.attn_backward(*dev, causal=causal)]
+        assert R.favor_device_error(f.handle) == 0
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        assert grad_err(a, b) <= TOL_GRAD[w.dtype], name

@@ -10,7 +10,7 @@ import pytest
 
 import oracle as O
 from synth import CONFIGS, make_workload
-from _util import TOL, to_dev, to_host
+from _util import TOL, to_dev, to_dev_unaligned, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -152,3 +152,21 @@ def test_call_errors_on_device():
             f.attn(qd, kd, vd)           # B=2 > max_B=1
         assert e.value.status == FAVOR_ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+@pytest.mark.parametrize("kind", ["softmax_pos", "relu"])
+def test_unaligned_inputs_bf16(mode, kind):
+    """Inputs one element past a 16-byte boundary: the tensor-core shape runs
+    on the CUDA-core kernels (no TMA on such pointers); same result."""
+    import torch
+    from random_feature_gb300 import Favor
+    w = CONFIGS["bidir_bf16"].replace(B=1, H=2, L=1000)
+    omega, q, k, v = make_workload(w, 17)
+    with Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, omega, w.data_scale, w.B, w.L) as f:
+        qd, kd, vd = (to_dev_unaligned(a, w.dtype) for a in (q, k, v))
+        out = f.attn(qd, kd, vd, causal=(mode == "causal"))
+        torch.cuda.synchronize()
+        got = to_host(out)
+    err = O.row_rel_err(got, _oracle(mode, kind, q, k, v, omega, w.data_scale))
+    assert err <= TOL[w.dtype], err
