@@ -220,12 +220,13 @@ __global__ void k_scan_segments_decay(float* __restrict__ part, const float* __r
 }
 
 // ------------------------------------------------------- bidirectional readout
-// grid (n_seg, B*H), 256 threads.  The state [m][dv+1] (row-major, fp32) is
-// staged once per CTA; per tile of TT queries: projections (thread per
-// feature row), row shift, features placed by slot, den by one warp per query,
-// and out_j[e..e+3] for two queries per thread as sums over the features.
+// grid (n_seg, B*H), 512 threads.  The state [m][dv+1] (row-major, fp32) is
+// staged once per CTA; per tile of TT queries: projections (thread (r, half)
+// takes feature row r for its half of the tile's queries), row shift,
+// features placed by slot, den by one warp per query, and out_j[e..e+3] for
+// two queries per thread as sums over the features.
 template <typename T, int KIND, int DV>
-__global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const float* __restrict__ state,
+__global__ void __launch_bounds__(512) k_readout(const T* __restrict__ q, const float* __restrict__ state,
                                                  const float* __restrict__ omega, T* __restrict__ out,
                                                  int H, int L, int m, int d, float s, int seg_len, int n_seg,
                                                  const int* __restrict__ pcyc, const int4* __restrict__ pmeta,
@@ -241,8 +242,9 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
     float* cq = fq + al4f(TT * MP);          // [TT]
     float* den = cq + TT;                    // [TT]
     uint8_t* rq = reinterpret_cast<uint8_t*>(den + TT);   // raw q rows of the next tile (async staging)
+    constexpr int TH = TT / 2;               // queries of a tile per half
     const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
-    const int r = threadIdx.x;
+    const int r = threadIdx.x & 255, hf = threadIdx.x >> 8;
     const bool own = r < m;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const float* om = omega + (size_t)h * m * d;
@@ -274,11 +276,12 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
         }
         __syncthreads();
         if (async_stage && t0 + TT < j1) prefetch(t0 + TT);   // lands while this tile computes
-        float p[TT];
+        float p[TH];
+        const int jb = hf * TH;   // this half's first query of the tile
         if (own) {
-            project_regs<TT>(om, xs, r, d, p);
+            project_regs<TH>(om, xs + jb * d, r, d, p);
 #pragma unroll
-            for (int j = 0; j < TT; ++j) raw[j * MP + r] = s * p[j];
+            for (int j = 0; j < TH; ++j) raw[(jb + j) * MP + r] = s * p[j];
         }
         __syncthreads();
         if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
@@ -286,12 +289,18 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
             __syncthreads();
         }
         if (own) {
+            // the cursor walks every query of the tile: half 1 passes half 0's first
+            if (hf)
+                for (int j = 0; j < TH; ++j) pc.prev();
 #pragma unroll
-            for (int j = 0; j < TT; ++j) {
+            for (int jj = 0; jj < TH; ++jj) {
+                const int j = jb + jj;
                 const float mx = KIND == FAVOR_KERNEL_SOFTMAX_POS ? cq[j] : 0.f;
-                fq[j * MP + pc.row(r)] = j < nt ? query_feat<KIND>(s * p[j], mx, r, m) : 0.f;
+                fq[j * MP + pc.row(r)] = j < nt ? query_feat<KIND>(s * p[jj], mx, r, m) : 0.f;
                 pc.prev();
             }
+            if (!hf)
+                for (int j = 0; j < TH; ++j) pc.prev();
         }
         __syncthreads();
         for (int j = warp; j < TT; j += nw) {
@@ -331,7 +340,9 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
 }
 
 // --------------------------------------------------------- causal, per segment
-// grid (n_seg, B*H), 256 threads.  The state at the tile start (the segment's
+// grid (n_seg, B*H), 512 threads: thread (r, half) owns feature row r for the
+// tokens of its half of each tile (projections, features) and half of the
+// state row's columns (update).  The state at the tile start (the segment's
 // exclusive prefix, then carried) lives in shared memory; per tile of TT
 // tokens (the chunked form of App. B.1 Eq. 11):
 //   num_j = P_j phi~_q(j) S + sum_{i<=j} D_ji (phi~_q(j) . phi~_k(i)) [v_i 1],
@@ -340,7 +351,7 @@ __global__ void __launch_bounds__(256) k_readout(const T* __restrict__ q, const 
 // w_i = D_{last,i} and P_tile = prod_l a_l (all 1 without decay), out_j =
 // num_j / den_j (den the last column).  No per-token block reductions.
 template <typename T, int KIND, int DV>
-__global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q, const T* __restrict__ k,
+__global__ void __launch_bounds__(512) k_causal_segment(const T* __restrict__ q, const T* __restrict__ k,
                                                         const T* __restrict__ v, const float* __restrict__ omega,
                                                         const float* __restrict__ kshift,
                                                         const float* __restrict__ prefix, T* __restrict__ out,
@@ -371,8 +382,9 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
     uint8_t* rq = reinterpret_cast<uint8_t*>(pt + 4);   // raw q | k | v rows of the next tile (async staging)
     uint8_t* rk = rq + raw_rows_bytes<T>(TT, d);
     uint8_t* rv = rk + raw_rows_bytes<T>(TT, d);
+    constexpr int TH = TT / 2;               // tokens of a tile per half
     const int seg = blockIdx.x, bh = blockIdx.y, h = bh % H;
-    const int r = threadIdx.x;
+    const int r = threadIdx.x & 255, hf = threadIdx.x >> 8;
     const bool own = r < m;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const float* om = omega + (size_t)h * m * d;
@@ -434,12 +446,13 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
                 tail *= ga[i];
             }
         }
-        float pq[TT], pk[TT];
+        float pq[TH], pk[TH];
+        const int jb = hf * TH;   // this half's first token of the tile
         if (own) {
-            project_regs<TT>(om, xs, r, d, pq);
-            project_regs<TT>(om, ys, r, d, pk);
+            project_regs<TH>(om, xs + jb * d, r, d, pq);
+            project_regs<TH>(om, ys + jb * d, r, d, pk);
 #pragma unroll
-            for (int j = 0; j < TT; ++j) raw[j * MP + r] = s * pq[j];
+            for (int j = 0; j < TH; ++j) raw[(jb + j) * MP + r] = s * pq[j];
         }
         __syncthreads();
         if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
@@ -447,14 +460,20 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
             __syncthreads();
         }
         if (own) {
+            // the cursor walks every token of the tile: half 1 passes half 0's first
+            if (hf)
+                for (int j = 0; j < TH; ++j) pc.prev();
 #pragma unroll
-            for (int j = 0; j < TT; ++j) {
+            for (int jj = 0; jj < TH; ++jj) {
+                const int j = jb + jj;
                 const int slot = pc.row(r);   // query and key at one position share pi^j
                 const float mx = KIND == FAVOR_KERNEL_SOFTMAX_POS ? cq[j] : 0.f;
-                fq[j * MP + slot] = j < nt ? query_feat<KIND>(s * pq[j], mx, r, m) : 0.f;
-                fk[j * MP + slot] = j < nt ? key_feat<KIND>(pk[j], kn[j], s, kap, r, m) : 0.f;
+                fq[j * MP + slot] = j < nt ? query_feat<KIND>(s * pq[jj], mx, r, m) : 0.f;
+                fk[j * MP + slot] = j < nt ? key_feat<KIND>(pk[jj], kn[j], s, kap, r, m) : 0.f;
                 pc.prev();
             }
+            if (!hf)
+                for (int j = 0; j < TH; ++j) pc.prev();
         }
         __syncthreads();
         for (int idx = threadIdx.x; idx < TT * (TT + 1) / 2; idx += blockDim.x) {   // pairs i <= j only
@@ -520,8 +539,9 @@ __global__ void __launch_bounds__(256) k_causal_segment(const T* __restrict__ q,
             for (int i = 0; i < TT; ++i) wf[i] = wi[i] * fk[i * MP + r];
             const float P = pt[0];
             float4* srow = reinterpret_cast<float4*>(ss + r * DVP);
+            constexpr int G4 = DVP / 4, G0 = G4 / 2;   // float4 groups of the row: [0, G0) half 0, [G0, G4) half 1
 #pragma unroll 1
-            for (int e4 = 0; e4 < DVP / 4; ++e4) {
+            for (int e4 = hf ? G0 : 0; e4 < (hf ? G4 : G0); ++e4) {
                 float4 a = srow[e4];
                 a.x *= P; a.y *= P; a.z *= P; a.w *= P;
 #pragma unroll
@@ -591,7 +611,7 @@ favor_status readout_dv(const Handle& h, const void* q, void* out, int BH, int L
     set_smem(kern, smem);
     dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_READOUT, st);
-    kern<<<grid, 256, smem, st>>>((const T*)q, h.ws_state, h.omega_f32, (T*)out, h.H, L, h.m, h.d, h.s,
+    kern<<<grid, 512, smem, st>>>((const T*)q, h.ws_state, h.omega_f32, (T*)out, h.H, L, h.m, h.d, h.s,
                                   p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta, as);
     count_launch();
     return check_launch("readout kernel");
@@ -625,7 +645,7 @@ favor_status causal_t(const Handle& h, const void* q, const void* k, const void*
     set_smem(kern, smem);
     dim3 grid(p.n_seg, BH);
     ProfScope ps(h, PROF_CAUSAL, st);
-    kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial,
+    kern<<<grid, 512, smem, st>>>((const T*)q, (const T*)k, (const T*)v, h.omega_f32, h.kshift, h.ws_partial,
                                   (T*)out, h.H, L, h.m, h.d, h.s, p.seg_tiles * 128, p.n_seg, rp.cyc, rp.meta,
                                   rp.gate, rp.rdec, as);
     count_launch();
