@@ -195,6 +195,28 @@ def ncu_traffic(slot):
 
 
 # --------------------------------------------------------------- CPU oracle arm
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it: the model name, else (Arm hosts)
+    the implementer and part codes, else the machine type."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            lines = f.read().splitlines()
+    except OSError:
+        lines = []
+    fields = {}
+    for line in lines:
+        if ":" in line:
+            key, val = (x.strip() for x in line.split(":", 1))
+            fields.setdefault(key, val)
+    for key in ("model name", "Model"):
+        if fields.get(key):
+            return fields[key]
+    if "CPU implementer" in fields or "CPU part" in fields:
+        return f"{platform.machine()} implementer {fields.get('CPU implementer')} part {fields.get('CPU part')}"
+    return platform.machine() or "unknown"
+
+
 def cpu_sample(w, heads, seed=0):
     """Time the oracle on the first `heads` heads of the workload, all four calls."""
     import oracle as O
@@ -231,7 +253,7 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "sample_heads": heads},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -581,7 +603,8 @@ def run_ours(args):
         heads = max(1, min(args.cpu_heads, w.H))
         cval, cdt, _ = cpu_sample(w, heads)
         cpu = {"value": cval, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{heads} of {w.H} heads of {w.name}, all four calls, float64 NumPy, {cdt:.1f} s"}
+               "sample": f"{heads} of {w.H} heads of {w.name}, all four calls, float64 NumPy, {cdt:.1f} s",
+               "cpu_model": cpu_model()}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

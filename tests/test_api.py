@@ -100,3 +100,11 @@ def test_bench_algorithmic_counts():
     b, f, e = bench.per_token_head(w, "bidir_readout", "relu")
     assert (b, f, e) == ((64 + 64) * 2, 2 * 256 * 64 + 2 * 256 * 65, 0)
     assert bench.backward_flops_per_token_head(w) == 8 * 256 * 64 + 6 * 256 * 65 + 4 * 256 * 64 == 296448
+
+
+def test_bench_cpu_model_names_the_host():
+    """The oracle baseline names the host CPU (model name, or the Arm
+    implementer/part codes when /proc/cpuinfo has no model name)."""
+    import bench
+    name = bench.cpu_model()
+    assert isinstance(name, str) and name.strip() and name != "unknown"
