@@ -62,6 +62,12 @@ def _raw_create(H=1, m=32, d=16, dv=16, kind=0, dtype=0, omega=True, s=1.0, max_
     (dict(dv=8), R.FAVOR_ERR_UNSUPPORTED),
     (dict(m=24), R.FAVOR_ERR_UNSUPPORTED),
     (dict(m=512), R.FAVOR_ERR_UNSUPPORTED),
+    (dict(m=0), R.FAVOR_ERR_INVALID_ARG),
+    (dict(d=0), R.FAVOR_ERR_INVALID_ARG),
+    (dict(dv=0), R.FAVOR_ERR_INVALID_ARG),
+    (dict(max_B=0), R.FAVOR_ERR_INVALID_ARG),
+    # max_B * H * max_L * max(d, dv) above 2^40: refused before any allocation
+    (dict(max_B=1 << 20, max_L=1 << 20), R.FAVOR_ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_arguments(kw, want):
     st, h = _raw_create(**kw)
@@ -77,6 +83,20 @@ def test_calls_reject_null_handle():
     assert L.favor_attn_causal(None, 1, 1, 1, 1, 1, 1, None) == R.FAVOR_ERR_INVALID_ARG
     assert L.favor_feature_map(None, 1, 1, 1, 1, None) == R.FAVOR_ERR_INVALID_ARG
     assert L.favor_destroy(None) == R.FAVOR_OK
+
+
+def test_stateful_backward_variant_calls_reject_null_handle():
+    """Every call past the forward ones checks its handle first (no CUDA call)."""
+    L = R.lib()
+    bad = R.FAVOR_ERR_INVALID_ARG
+    assert L.favor_kv_state(None, 1, 1, 1, 1, 1, None) == bad
+    assert L.favor_attn_from_state(None, 1, 1, 1, 1, 1, None) == bad
+    assert L.favor_attn_causal_step(None, 1, 1, 1, 1, 1, 1, 1, None) == bad
+    assert L.favor_attn_bidir_backward(None, 1, 1, 1, 1, 1, 1, 1, 1, 1, None) == bad
+    assert L.favor_attn_causal_backward(None, 1, 1, 1, 1, 1, 1, 1, 1, 1, None) == bad
+    assert L.favor_attn_causal_gated(None, 1, 1, 1, 1, 1, 1, 1, None) == bad
+    assert L.favor_attn_causal_step_gated(None, 1, 1, 1, 1, 1, 1, 1, 1, None) == bad
+    assert L.favor_set_relpos(None, None, None) == bad
 
 
 def test_launch_counter_is_monotone():
