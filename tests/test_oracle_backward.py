@@ -163,3 +163,35 @@ def test_relu_zero_denominator_rows_have_zero_gradient():
     np.testing.assert_array_equal(dq, 0.0)
     np.testing.assert_array_equal(dk, 0.0)
     np.testing.assert_array_equal(dv, 0.0)
+
+
+@pytest.mark.parametrize("mode", ["bidir", "causal"])
+@pytest.mark.parametrize("kind", O.KINDS)
+def test_gradients_match_reverse_mode_autodiff(mode, kind):
+    """Every element of dq, dk, dv against reverse-mode differentiation
+    (PyTorch autograd, float64, CPU) of a forward written here from the
+    definitions: the features of Lemma 1 (or the ReLU map), the explicit
+    L x L matrix A = phi(x) phi(y)^T (its lower triangle, diagonal included,
+    for causal), out = A V / A 1.  Nothing is shared with the oracle."""
+    torch = pytest.importorskip("torch")
+    omega, q, k, v, g = _inputs(3)
+    s = 0.8
+    m = omega.shape[1]
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    om = torch.tensor(omega, dtype=torch.float64)
+
+    def feat(x):
+        proj = torch.einsum("bhld,hmd->bhlm", x, om)
+        if kind == "softmax_pos":
+            return torch.exp(proj - 0.5 * (x * x).sum(-1, keepdim=True)) / m ** 0.5
+        return torch.relu(proj) / m ** 0.5
+
+    A = torch.einsum("bhim,bhjm->bhij", feat(s * tq), feat(s * tk))
+    if mode == "causal":
+        A = torch.tril(A)
+    den = A.sum(-1, keepdim=True)
+    assert bool((den > 0).all())   # the seed gives no zero denominator (ReLU)
+    ((A @ tv) / den * torch.tensor(g)).sum().backward()
+    got = BWD[mode](q, k, v, g, omega, s, kind)
+    for name, a, b in zip(("dq", "dk", "dv"), got, (tq.grad, tk.grad, tv.grad)):
+        np.testing.assert_allclose(a, b.numpy(), rtol=1e-9, atol=1e-12, err_msg=name)
