@@ -166,11 +166,12 @@ def test_relu_zero_denominator_rows_have_zero_gradient():
 
 
 @pytest.mark.parametrize("mode", ["bidir", "causal"])
-@pytest.mark.parametrize("kind", O.KINDS)
+@pytest.mark.parametrize("kind", O.KINDS + ("softmax_hyp",))
 def test_gradients_match_reverse_mode_autodiff(mode, kind):
     """Every element of dq, dk, dv against reverse-mode differentiation
     (PyTorch autograd, float64, CPU) of a forward written here from the
-    definitions: the features of Lemma 1 (or the ReLU map), the explicit
+    definitions: the features of Lemma 1 (its first form, its hyperbolic
+    second form with 2m features, or the ReLU map), the explicit
     L x L matrix A = phi(x) phi(y)^T (its lower triangle, diagonal included,
     for causal), out = A V / A 1.  Nothing is shared with the oracle."""
     torch = pytest.importorskip("torch")
@@ -182,8 +183,11 @@ def test_gradients_match_reverse_mode_autodiff(mode, kind):
 
     def feat(x):
         proj = torch.einsum("bhld,hmd->bhlm", x, om)
+        half = 0.5 * (x * x).sum(-1, keepdim=True)
         if kind == "softmax_pos":
-            return torch.exp(proj - 0.5 * (x * x).sum(-1, keepdim=True)) / m ** 0.5
+            return torch.exp(proj - half) / m ** 0.5
+        if kind == "softmax_hyp":
+            return torch.cat([torch.exp(proj - half), torch.exp(-proj - half)], dim=-1) / (2 * m) ** 0.5
         return torch.relu(proj) / m ** 0.5
 
     A = torch.einsum("bhim,bhjm->bhij", feat(s * tq), feat(s * tk))
