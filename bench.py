@@ -5,7 +5,13 @@ One step = one pass of the whole forward hot path over one batch of the
 very-long-context workload (B=1, H=16, L=65536, d=dv=64, m=256, bf16,
 Q/K/V ~ N(0, 0.5^2), orthogonal omega per head): bidirectional and causal
 attention, each with positive softmax features and with ReLU features (four
-library calls).  value = token*heads processed per second, whole job.
+library calls).  value = token*heads processed per second, whole job, timed
+with CUDA events around the steps and nothing else on the stream.
+
+Beside the headline: per-kernel times from a separate pass with the
+library's event hooks on, each call of the step timed on its own with its
+whole-call roofline, and the same per-call numbers for the other workloads
+(tiny_f32, approx_f32 over m, bidir_bf16, causal_bf16).
 
 Arms:
   --impl ours (default)  the CUDA library through its C ABI, inputs resident
@@ -65,6 +71,8 @@ def parse():
     ap.add_argument("--e2e-groups", type=int, default=4,
                     help="head groups pipelined over upload / compute / download streams in the e2e leg")
     ap.add_argument("--cpu-heads", type=int, default=2, help="heads of the workload in the CPU oracle sample")
+    ap.add_argument("--no-config-lines", dest="config_lines", action="store_false",
+                    help="skip the per-configuration lines (tiny_f32, approx_f32, bidir_bf16, causal_bf16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -157,6 +165,63 @@ def per_token_head(w, slot, kind):
     if slot == "feature_map":
         return d * b + m * b, 2 * m * d, e
     return 0, 0, 0
+
+
+FP64_NOMINAL_TFLOPS = 1.25   # GB300 FP64 (datasheet); the fp32-storage path computes in float64
+
+
+def compute_path(w, kind="softmax_pos"):
+    """Which units a forward call of workload w runs on."""
+    if w.dtype == "bf16" and (w.d, w.dv, w.m) == (64, 64, 256) and kind != "softmax_trig":
+        return "tensor cores"
+    if w.dtype == "f32" and kind in ("softmax_pos", "relu", "softmax_hyp"):
+        return "CUDA cores, float64"
+    return "CUDA cores, fp32"
+
+
+def call_roofline(w, kind, ms, peaks, sm_mhz):
+    """Roofline of one whole forward call (every kernel it launches) from its
+    algorithmic work per token*head: bytes (2d + 2dv) * sizeof(dtype) (read Q,
+    K, V, write out), flops 4md + 4m(dv+1), exps 2m (exp features only).  The
+    roofline time is the largest of bytes / HBM, flops / compute peak and exps /
+    exp2 peak; frac = roofline time / measured time."""
+    T = w.B * w.H * w.L
+    b = 2 if w.dtype == "bf16" else 4
+    nbytes = (2 * w.d + 2 * w.dv) * b * T
+    flops = (4 * w.m * w.d + 4 * w.m * (w.dv + 1)) * T
+    exps = (2 * w.m if kind in ("softmax_pos", "softmax_hyp", "softmax_trig") else 0) * T
+    path = compute_path(w, kind)
+    sec = ms / 1e3
+    sfu = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * sm_mhz * 1e6
+    if path == "tensor cores":
+        cpeak, cname = peaks["bf16_tflops"] * 1e12, "bf16 tensor (measured burst)"
+    elif path == "CUDA cores, float64":
+        cpeak, cname, sfu = FP64_NOMINAL_TFLOPS * 1e12, "FP64 (nominal 1.25 TFLOP/s)", None
+    else:
+        cpeak, cname = GB300_SMS * 128 * 2 * sm_mhz * 1e6, "FP32 FFMA (152 SMs x 128 lanes x 2 x SM clock)"
+    times = {"hbm": nbytes / (peaks["hbm_gbs"] * 1e9), "compute": flops / cpeak}
+    if sfu and exps:
+        times["exp2"] = exps / sfu
+    bound = max(times, key=times.get)
+    return {"bound": bound, "roofline_us": times[bound] * 1e6, "measured_us": ms * 1e3,
+            "frac": times[bound] / sec, "path": path, "compute_peak": cname,
+            "achieved": {"GB/s": nbytes / sec / 1e9, "TFLOP/s": flops / sec / 1e12,
+                         "Gexp/s": exps / sec / 1e9},
+            "per_token_head": {"bytes": nbytes // T, "flops": flops // T, "exps": exps // T}}
+
+
+def time_calls(fn, reps, stream, warm=2):
+    """Average device time (ms) of fn() over reps calls, CUDA events on `stream`."""
+    import torch
+    for _ in range(warm):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
 
 
 def backward_flops_per_token_head(w):
@@ -300,9 +365,7 @@ def run_ours(args):
         step()
     torch.cuda.synchronize(dev)
 
-    for hd in handles.values():
-        R.favor_profile_reset(hd.handle)
-        R.favor_profile_enable(hd.handle, True)
+    # The timed region: library profiling hooks off (no events between kernels).
     launches0 = R.favor_launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -318,12 +381,32 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     launches = R.favor_launch_count() - launches0
-    sampler.stop()
     ms_total = ev0.elapsed_time(ev1)
+
+    # Per-kernel device times from a separate pass of the same steps with the
+    # library's event hooks on (an event pair around every kernel).
+    prof_steps = max(3, min(args.steps, 20))
+    for hd in handles.values():
+        R.favor_profile_reset(hd.handle)
+        R.favor_profile_enable(hd.handle, True)
+    for _ in range(prof_steps):
+        step()
+    torch.cuda.synchronize(dev)
     for hd in handles.values():
         R.favor_profile_enable(hd.handle, False)
 
-    # per-kernel device time over the timed region
+    # Each call of the step on its own (hooks off): whole-call time and roofline.
+    sm_mhz_now = sampler.samples[-1][1] if sampler.samples else peaks["sm_max_mhz"]
+    calls = {}
+    for (mode, kind), o in zip(STEP_CALLS, outs):
+        def one(mode=mode, kind=kind, o=o):
+            handles[kind].attn(qd, kd, vd, causal=(mode == "causal"), out=o, stream=stream)
+        ms_c = time_calls(one, max(5, min(args.steps, 50)), stream)
+        calls[f"{mode}_{kind}"] = {"ms": ms_c, "value": w.B * w.H * w.L / (ms_c / 1e3), "unit": UNIT,
+                                   "roofline": call_roofline(w, kind, ms_c, peaks, sm_mhz_now)}
+    sampler.stop()
+
+    # per-kernel device time over the profiled pass
     slots = {}
     for hd in handles.values():
         for sl in range(R.favor_profile_slots()):
@@ -337,6 +420,41 @@ def run_ours(args):
     units_step = len(STEP_CALLS) * w.B * w.H * w.L
     job_units, ms_step = job_aggregate(units_step, ms_total / args.steps, device=dev)
     value = job_units / (ms_step / 1e3)
+
+    # The other workloads, each call timed on its own (hooks off): throughput and
+    # whole-call roofline.  tiny_f32 and approx_f32 are parity cases on the
+    # float64 CUDA-core path (no roofline target); bidir_bf16 and causal_bf16
+    # are the L >= 4096 bf16 configurations next to long_bf16.
+    configs = None
+    if args.config_lines and world == 1:
+        configs = {}
+        plan = [("tiny_f32", None), ("approx_f32", (16, 32, 64, 128, 256)), ("bidir_bf16", None),
+                ("causal_bf16", None)]
+        for cname, msweep in plan:
+            base = CONFIGS[cname]
+            entry = {}
+            for m_ in (msweep or (base.m,)):
+                wc = base.replace(m=m_)
+                om_c, qc, kc, vc = make_workload(wc, 0)
+                tdc = torch.bfloat16 if wc.dtype == "bf16" else torch.float32
+                qcd, kcd, vcd = (torch.from_numpy(a).to(device=dev, dtype=tdc).contiguous() for a in (qc, kc, vc))
+                oc = torch.empty((wc.B, wc.H, wc.L, wc.dv), dtype=tdc, device=dev)
+                with R.Favor(wc.H, wc.m, wc.d, wc.dv, "softmax_pos", wc.dtype, om_c, wc.data_scale, wc.B,
+                             wc.L) as fc:
+                    for mode in wc.modes:
+                        def one(mode=mode):
+                            fc.attn(qcd, kcd, vcd, causal=(mode == "causal"), out=oc, stream=stream)
+                        reps = 3 if wc.dtype == "f32" and wc.L > 1024 else 20
+                        ms_c = time_calls(one, reps, stream)
+                        key = mode if msweep is None else f"m{m_}_{mode}"
+                        entry[key] = {"ms": ms_c, "value": wc.B * wc.H * wc.L / (ms_c / 1e3), "unit": UNIT,
+                                      "roofline": call_roofline(wc, "softmax_pos", ms_c, peaks, sm_mhz_now)}
+                del qcd, kcd, vcd, oc
+            entry["config"] = (f"B={base.B} H={base.H} L={base.L} d={base.d} dv={base.dv} "
+                               f"m={'/'.join(map(str, msweep)) if msweep else base.m} {base.dtype}, positive "
+                               f"features, seed 0")
+            configs[cname] = entry
+        torch.cuda.synchronize(dev)
 
     # Decoding: one new token per step continuing from a resident state
     # (favor_attn_causal_step, T = 1), positive features, state prefilled from
@@ -583,8 +701,8 @@ def run_ours(args):
     sfu_peak = GB300_SMS * SFU_EX2_PER_CLK_PER_SM * sm_mhz * 1e6
     cands = {
         "hbm": (bytes_l / sec / 1e9, peaks["hbm_gbs"], "GB/s", bytes_l / (peaks["hbm_gbs"] * 1e9)),
-        "tensor": (flops_l / sec / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s",
-                   flops_l / (peaks["bf16_tflops_sustained"] * 1e12)),
+        "tensor": (flops_l / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s",
+                   flops_l / (peaks["bf16_tflops"] * 1e12)),
         "alu": (exps_l / sec / 1e9, sfu_peak / 1e9, "Gexp/s", exps_l / sfu_peak),
     }
     bound = max(cands, key=lambda kk: cands[kk][3])
@@ -592,11 +710,15 @@ def run_ours(args):
     traffic = ncu_traffic(dname)
     roofline = {"bound": bound, "achieved": ach, "peak": pk, "unit": unit, "frac": ach / pk,
                 "traffic": traffic, "kernel": dname, "launch_ms": per_launch_ms,
-                "peak_source": peaks["source"] + (" (sustained bf16)" if bound == "tensor" else "")
+                "peak_source": peaks["source"] + (" (burst bf16: a launch of well under a millisecond)"
+                                                  if bound == "tensor" else "")
                 + (" (32 ex2/clk/SM x 152 SMs x median SM clock)" if bound == "alu" else "")}
     roofline_all = {kk: {"achieved": c[0], "peak": c[1], "unit": c[2], "frac": c[0] / c[1]} for kk, c in cands.items()}
-    kernels = {name: {"ms_total": v_[0], "launches": v_[1], "share": v_[0] / max(1e-12, sum(x[0] for x in slots.values()))}
+    kernels = {name: {"ms_total": v_[0], "launches": v_[1], "ms_per_launch": v_[0] / v_[1],
+                      "share": v_[0] / max(1e-12, sum(x[0] for x in slots.values()))}
                for name, v_ in slots.items() if v_[1]}
+    kernels["_pass"] = (f"{prof_steps} steps with the library's per-kernel event hooks on, after the timed "
+                        f"region (which ran with them off)")
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -613,7 +735,8 @@ def run_ours(args):
                                    f"calls per step: bidir+causal x softmax_pos+relu",
                        "global_batch": w.B * world, "seq_len": w.L, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (Q,K,V 384 MB per replica)"},
-            "clocks": clocks, "e2e": e2e, "decode": decode, "backward": backward, "variants": variants,
+            "clocks": clocks, "e2e": e2e, "calls": calls, "configs": configs, "decode": decode,
+            "backward": backward, "variants": variants,
             "gpu_launches": launches,
             "roofline": roofline,
             "roofline_all": roofline_all, "kernels": kernels, "cpu_baseline": cpu}

@@ -273,7 +273,7 @@ FAVOR_API favor_status favor_attn_causal_backward(favor_handle h, const void* q,
 
 /*
  * favor_attn_bidir_noalloc -- favor_attn_bidir without a handle and without
- * any allocation.  The pages have no counterpart: this is an interface
+ * any allocation.  The paper has no counterpart: this is an interface
  * convenience.  It serves callers that may not allocate device memory through
  * this library, e.g. a host framework whose caching allocator owns the device
  * memory, or a serving process that reserves the device memory up front.
@@ -282,12 +282,14 @@ FAVOR_API favor_status favor_attn_causal_backward(favor_handle h, const void* q,
  *
  *   omega       DEVICE float array [H, m, d] (caller-owned, read only), used
  *               as given (favor_create's bf16 rounding of omega is not
- *               applied); entries must be finite.
+ *               applied); entries must be finite.  It must be 16-byte aligned
+ *               memory of the current device (device or managed); anything
+ *               else fails with FAVOR_ERR_INVALID_ARG before any launch.
  *   H, m, d, dv, kind, dtype, data_scale   as in favor_create, same limits.
  *   q, k, v, out, B, L, stream             as in favor_attn_bidir.
  *
- * Computes what favor_attn_bidir computes (Eq. 4 of Rethinking Attention with
- * Performers), on the CUDA-core kernels, with the same zero-denominator rule and
+ * Computes what favor_attn_bidir computes, on the CUDA-core kernels (fp32
+ * arithmetic for both dtypes), with the same zero-denominator rule and
  * the same cancelling shifts (the per-head key shift is derived on the device
  * from omega).  Scratch is one fixed 16 MiB device array inside the library
  * (4,194,304 floats): calls need H (rounded up to 64) + 2*B*H*m*(dv+1) floats at
@@ -295,8 +297,9 @@ FAVOR_API favor_status favor_attn_causal_backward(favor_handle h, const void* q,
  * launched; the work split is narrowed to fit.  No part of the array needs to
  * start at zero.  Every device has its own copy.  Its address is looked up
  * the first time the call runs on a device (cudaGetSymbolAddress, which may
- * load the library's device code there); make that first call before any
- * stream capture begins.  Calls on one device share the array: two calls
+ * load the library's device code there), and again the first time after the
+ * device's context was made anew (e.g. after cudaDeviceReset); make that first
+ * call before any stream capture begins.  Calls on one device share the array: two calls
  * that overlap in time on the device race and give wrong results, so order
  * them (one stream, or events).
  */
@@ -329,6 +332,21 @@ FAVOR_API unsigned long long favor_launch_count(void);
  * an error instead of a hang.
  */
 FAVOR_API favor_status favor_device_error(favor_handle h, int* code);
+
+/*
+ * favor_check_bounded_wait -- exercise the failure path of the kernels'
+ * bounded waits without faulting anything (no counterpart on the pages).
+ * Enqueues on `stream` one single-thread kernel that waits on an mbarrier
+ * phase nothing completes, with a limit of limit_cycles SM clock cycles
+ * (1000 <= limit_cycles <= 2^24, else FAVOR_ERR_INVALID_ARG).  The wait gives
+ * up, the kernel writes FAVOR_WAIT_CHECK_CODE to the handle's device error
+ * word (unless an earlier failure already left its code there) and returns; the
+ * context stays usable.  favor_device_error then reports the code.  The
+ * handle's error word is not cleared afterwards: use a handle made for the
+ * check.
+ */
+#define FAVOR_WAIT_CHECK_CODE 901
+FAVOR_API favor_status favor_check_bounded_wait(favor_handle h, int limit_cycles, void* stream);
 
 /*
  * Per-kernel timing for measurement (no counterpart on the pages).

@@ -24,8 +24,11 @@ Readings taken where the pages are silent or garbled:
   * a denominator that is exactly 0 (possible only for ReLU features) gives an
     output row of zeros.
   * causal attention includes the diagonal ([P] Eq. 2, tril keeps it).
-  * the error measure is row-normwise: max over rows i and columns e of
-    |g_ie - o_ie| / max_e' |o_ie'|.
+  * two error measures.  Element-wise with a floor (the measure for fp32
+    storage): max over elements of |g_ie - o_ie| / max(|o_ie|, 1e-2 max_e'|o_ie'|);
+    the floor keeps the ratio defined where a signed output cancels to about
+    zero.  Row-normwise (the measure for bf16 storage): max over rows i and
+    columns e of |g_ie - o_ie| / max_e' |o_ie'|.
 
 Every function takes float arrays of any float dtype and computes in float64.
 """
@@ -39,7 +42,7 @@ __all__ = [
     "explicit_from_features", "rnn_causal_from_features",
     "favor_bidir", "favor_causal", "favor_feature_map",
     "favor_kv_state", "favor_attn_from_state", "favor_causal_from_state",
-    "softmax_attention", "row_rel_err", "KINDS",
+    "softmax_attention", "row_rel_err", "elem_rel_err", "KINDS",
     "feature_map_vjp", "attn_from_features_bidir_vjp", "attn_from_features_causal_vjp",
     "favor_bidir_backward", "favor_causal_backward",
     "feature_map_hyperbolic", "feature_map_trig", "VARIANT_KINDS", "n_features",
@@ -546,3 +549,21 @@ def row_rel_err(got, ref):
     scale = np.max(np.abs(ref), axis=-1, keepdims=True)
     scale = np.where(scale > 0, scale, 1.0)
     return float(np.max(np.abs(got - ref) / scale)) if ref.size else 0.0
+
+
+def elem_rel_err(got, ref, floor=1e-2):
+    """max over elements of |got_ie - ref_ie| / max(|ref_ie|, floor * max_e' |ref_ie'|).
+
+    The element-wise relative error, with each element's divisor held at least
+    at `floor` times the largest magnitude of its row (last axis), so that
+    entries of a signed output that cancel to about zero do not make the ratio
+    unbounded.  Rows whose reference is all zeros use an absolute error.
+    """
+    got = _f64(got)
+    ref = _f64(ref)
+    if not ref.size:
+        return 0.0
+    rmax = np.max(np.abs(ref), axis=-1, keepdims=True)
+    scale = np.maximum(np.abs(ref), floor * rmax)
+    scale = np.where(scale > 0, scale, 1.0)
+    return float(np.max(np.abs(got - ref) / scale))

@@ -21,7 +21,7 @@ OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "libfavor.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["favor_api.cu", "favor_simt.cu", "favor_tc.cu", "favor_tc_bwd.cu", "favor_bwd.cu"]
+SOURCES = ["favor_api.cu", "favor_simt.cu", "favor_tc.cu", "favor_tc_bwd.cu", "favor_bwd.cu", "favor_f64.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
           "--expt-relaxed-constexpr", "-I", INCLUDE]

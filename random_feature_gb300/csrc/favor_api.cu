@@ -115,6 +115,8 @@ static void free_handle(Handle* h) {
     cudaFree(h->perm_cyc);
     cudaFree(h->perm_meta);
     cudaFree(h->relpos_r);
+    cudaFree(h->ws64);
+    cudaFree(h->ws64_state);
     cudaFree(h->ws_tc);
     cudaFree(h->ws_bimg);
     free(h->omega_sqnorm_half_host);
@@ -241,6 +243,11 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_dstate, (size_t)max_B * H * st_elems * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_rowstat, (size_t)max_B * H * (size_t)max_L * 4 * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_segdecay, rows * sizeof(float));
+    // fp32 storage: float64 per-segment and reduced states of the bidirectional and causal calls
+    if (e == cudaSuccess && dtype == FAVOR_DTYPE_F32 && kind != FAVOR_KERNEL_SOFTMAX_TRIG) {
+        e = cudaMalloc(&h->ws64, f64_workspace_rows(max_B * H, h->num_sms) * st_elems * sizeof(double));
+        if (e == cudaSuccess) e = cudaMalloc(&h->ws64_state, (size_t)max_B * H * st_elems * sizeof(double));
+    }
     if (e != cudaSuccess) {
         favor_status st = (e == cudaErrorMemoryAllocation) ? FAVOR_ERR_NOMEM : FAVOR_ERR_CUDA;
         set_error(st, "favor_create: cudaMalloc: %s", cudaGetErrorString(e));
@@ -330,6 +337,7 @@ favor_status favor_attn_bidir(favor_handle hd, const void* q, const void* k, con
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tc_supported(h) && !relpos_on(h)) return tc_bidir(h, q, k, v, out, B, L, s);
+    if (f64_supported(h) && !relpos_on(h)) return f64_bidir(h, q, k, v, out, B, L, s);
     return simt_bidir(h, q, k, v, out, B, L, s);
 }
 
@@ -341,6 +349,7 @@ favor_status favor_attn_causal(favor_handle hd, const void* q, const void* k, co
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tc_supported(h) && !relpos_on(h)) return tc_causal(h, q, k, v, out, B, L, s);
+    if (f64_supported(h) && !relpos_on(h)) return f64_causal(h, q, k, v, out, B, L, s);
     return simt_causal(h, q, k, v, out, B, L, s);
 }
 
@@ -462,10 +471,25 @@ favor_status favor_attn_bidir_noalloc(const float* omega, int H, int m, int d, i
                          "%s: B*H*m*(dv+1) = %lld needs more than the fixed scratch of %zu floats (at most %zu "
                          "per state copy, two copies)", fn, BH * m * (dv + 1), kFixedScratchFloats,
                          (kFixedScratchFloats - ((size_t)H + 63) / 64 * 64) / 2);
+    // omega is read as float4 rows by the kernels: it must be 16-byte aligned
+    // memory of the current device (a host or misaligned address would fault
+    // on the device instead of failing here)
+    if (reinterpret_cast<uintptr_t>(omega) % 16 != 0)
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: omega must be 16-byte aligned", fn);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
-        return set_error(FAVOR_ERR_CUDA, "%s: no usable CUDA device", fn);
+        return set_error(FAVOR_ERR_INVALID_ARG, "%s: no usable CUDA device, so omega cannot be device memory", fn);
+    }
+    {
+        cudaPointerAttributes pa;
+        std::memset(&pa, 0, sizeof(pa));
+        const cudaError_t e = cudaPointerGetAttributes(&pa, omega);
+        cudaGetLastError();
+        if (e != cudaSuccess || (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged) ||
+            pa.device != dev)
+            return set_error(FAVOR_ERR_INVALID_ARG, "%s: omega is not device (or managed) memory of device %d", fn,
+                             dev);
     }
     Handle h;
     std::memset(&h, 0, sizeof(h));
@@ -566,6 +590,21 @@ favor_status favor_device_error(favor_handle hd, int* code) {
         return set_error(FAVOR_ERR_CUDA, "favor_device_error: %s", cudaGetErrorString(e));
     }
     return FAVOR_OK;
+}
+
+favor_status favor_check_bounded_wait(favor_handle hd, int limit_cycles, void* stream) {
+    g_err[0] = 0;
+    if (!hd) return set_error(FAVOR_ERR_INVALID_ARG, "favor_check_bounded_wait: handle is NULL");
+    if (limit_cycles < 1000 || limit_cycles > (1 << 24))
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_check_bounded_wait: limit_cycles=%d outside [1000, 2^24]",
+                         limit_cycles);
+    const Handle& h = *reinterpret_cast<const Handle*>(hd);
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h.device) {
+        cudaGetLastError();
+        return set_error(FAVOR_ERR_INVALID_ARG, "favor_check_bounded_wait: current device %d is not the handle's", cur);
+    }
+    return launch_wait_expiry(h, limit_cycles, FAVOR_WAIT_CHECK_CODE, reinterpret_cast<cudaStream_t>(stream));
 }
 
 static const char* kSlotNames[PROF_NSLOTS] = {"feature_map", "segment_state", "segment_combine",

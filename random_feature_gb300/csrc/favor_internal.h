@@ -67,6 +67,8 @@ struct Handle {
     int* perm_cyc;            // [H*m] each head's permutation written cycle by cycle
     int4* perm_meta;          // [H*m] per feature: (cycle start, cycle length, place in the cycle, 0)
     float* relpos_r;          // [H] decay r of causal calls (null: 1)
+    double* ws64;             // FP32 dtype: [rows][m][dv+1] float64 per-segment states
+    double* ws64_state;       // FP32 dtype: [max_B*H][m][dv+1] float64 reduced bidirectional states
     void* ws_tc;              // tensor-core path scratch (bf16 operand copies), may be null
     void* ws_bimg;            // tensor-core backward: per head S (or dS) hi / lo images + z, may be null
     size_t ws_tc_bytes;
@@ -142,6 +144,14 @@ favor_status tc_kv_state(const Handle& h, const void* k, const void* v, float* s
 favor_status tc_attn_from_state(const Handle& h, const void* q, const float* state, void* out, int B, int L,
                                 cudaStream_t st);
 
+// ---- fp32 storage with float64 arithmetic (bidirectional and causal, positive / ReLU) ----
+size_t f64_workspace_rows(int max_BH, int num_sms);
+bool f64_supported(const Handle& h);
+favor_status f64_bidir(const Handle& h, const void* q, const void* k, const void* v, void* out, int B, int L,
+                       cudaStream_t st);
+favor_status f64_causal(const Handle& h, const void* q, const void* k, const void* v, void* out, int B, int L,
+                        cudaStream_t st);
+
 // ---- bidirectional call on a fixed, statically sized device scratch array ----
 // 16 MiB: enough for B*H*m*(dv+1)*(1 + n_seg) + H floats with n_seg >= 1 up to
 // B*H = 63 at m = 256, dv = 128 (more heads at smaller m, dv).
@@ -153,6 +163,9 @@ favor_status simt_bidir_fixed_scratch(const Handle& proto, const void* q, const 
                                       void* out, int B, int L, cudaStream_t st);
 
 // ---- tensor-core (tcgen05) kernels: bf16, d = dv = 64, m = 256 ----
+// One-thread kernel whose mbarrier wait has no arriver: it gives up after
+// `limit` cycles and writes `code` to the handle's error word.
+favor_status launch_wait_expiry(const Handle& h, long long limit, int code, cudaStream_t st);
 bool tc_supported(const Handle& h);
 favor_status tc_feature_map(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st);
 favor_status tc_bidir(const Handle& h, const void* q, const void* k, const void* v, void* out,

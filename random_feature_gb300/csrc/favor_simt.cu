@@ -991,24 +991,57 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_fixed_mu;
-float* g_fixed_ptr[kMaxDevices] = {};
+
+// The device address of g_fixed_scratch, looked up (cudaGetSymbolAddress) once
+// per device and CUDA context: a context torn down and made again (for
+// instance after cudaDeviceReset) loads the module anew, possibly elsewhere,
+// so the cached address is only reused while the current context is the one
+// it was taken in.
+struct FixedScratchSlot {
+    void* ctx;
+    float* ptr;
+};
+FixedScratchSlot g_fixed[kMaxDevices] = {};
+
+using CtxGetCurrentFn = int (*)(void**);
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
 
 favor_status fixed_scratch_ptr(int dev, float** out) {
     if (dev < 0 || dev >= kMaxDevices)
         return set_error(FAVOR_ERR_UNSUPPORTED, "favor_attn_bidir_noalloc: device ordinal %d above %d", dev,
                          kMaxDevices - 1);
+    CtxGetCurrentFn get = ctx_get_current_fn();
+    if (!get) return set_error(FAVOR_ERR_CUDA, "favor_attn_bidir_noalloc: cuCtxGetCurrent is not available");
+    void* ctx = nullptr;
+    if (get(&ctx) != 0) ctx = nullptr;   // null: no context is current yet
     std::lock_guard<std::mutex> lk(g_fixed_mu);
-    if (!g_fixed_ptr[dev]) {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_fixed_scratch);
-        if (e != cudaSuccess || !p) {
-            cudaGetLastError();
-            return set_error(FAVOR_ERR_CUDA, "favor_attn_bidir_noalloc: cudaGetSymbolAddress: %s",
-                             cudaGetErrorString(e));
-        }
-        g_fixed_ptr[dev] = static_cast<float*>(p);
+    if (ctx && g_fixed[dev].ptr && g_fixed[dev].ctx == ctx) {
+        *out = g_fixed[dev].ptr;
+        return FAVOR_OK;
     }
-    *out = g_fixed_ptr[dev];
+    // set-up: the lookup makes the device's primary context current if it was not
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_fixed_scratch);
+    if (e != cudaSuccess || !p) {
+        cudaGetLastError();
+        return set_error(FAVOR_ERR_CUDA, "favor_attn_bidir_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    }
+    if (get(&ctx) != 0 || !ctx) return set_error(FAVOR_ERR_CUDA, "favor_attn_bidir_noalloc: no current CUDA context");
+    g_fixed[dev].ctx = ctx;
+    g_fixed[dev].ptr = static_cast<float*>(p);
+    *out = g_fixed[dev].ptr;
     return FAVOR_OK;
 }
 

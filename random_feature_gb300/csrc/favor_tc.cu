@@ -593,7 +593,7 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 } else {
                     __nanosleep(64);
                     if (clock64() - t0 > (4LL << 30)) {
-                        atomicExch(err, 301);
+                        atomicCAS(err, 0, 301);
                         break;
                     }
                 }
@@ -1105,7 +1105,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 } else {
                     __nanosleep(32);
                     if (clock64() - t0 > (4LL << 30)) {
-                        atomicExch(err, 201);
+                        atomicCAS(err, 0, 201);
                         break;
                     }
                 }
@@ -1471,6 +1471,20 @@ k_tc_feature_map(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     teardown(bars, tmem, 256);
 }
 
+// ======================================================== bounded-wait check
+// One thread waits on an mbarrier phase that nothing completes, with a limit
+// of `limit` cycles: the wait must give up, write `code` to the error word and
+// return.  No copies, tensor memory or other warps are involved.
+__global__ void k_wait_expiry(int* err, long long limit, int code) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_for(&bar, 0, err, code, limit);
+}
+
 // ================================================================ host side
 constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * kExtStage + kExtOmega + sizeof(StBars);
 constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kRStages * kTileBytes + kRImage + 2 * kTileBytes +
@@ -1511,6 +1525,12 @@ favor_status launch_state(const Handle& h, const CUtensorMap& mk, const CUtensor
 }
 
 }  // namespace
+
+favor_status launch_wait_expiry(const Handle& h, long long limit, int code, cudaStream_t st) {
+    k_wait_expiry<<<1, 32, 0, st>>>(h.dev_err, limit, code);
+    count_launch();
+    return check_launch("bounded-wait check kernel");
+}
 
 bool tc_supported(const Handle& h) {
     return h.dtype == FAVOR_DTYPE_BF16 && h.d == kD && h.dv == kDV && h.m == kM && h.cc_major >= 10 &&

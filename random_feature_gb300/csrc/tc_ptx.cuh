@@ -56,21 +56,26 @@ __device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parit
     return ok;
 }
 
-// Wait for the phase with the given parity to complete, giving up after about
-// two seconds of SM clock: then the error word gets `code` and false returns.
+// Wait for the phase with the given parity to complete, giving up after
+// `limit` SM clock cycles: then the error word gets `code` and false returns.
 // try_wait suspends the warp in hardware until the phase completes or a
 // system-dependent time limit passes, so a waiting warp takes no issue slots
 // from the warps that do the work.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int* err, int code, long long limit) {
     if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > (4LL << 30)) {
-            if (err) atomicExch(err, code);
+        if (clock64() - t0 > limit) {
+            if (err) atomicCAS(err, 0, code);   // the first wait that gave up keeps its code
             return false;
         }
     }
     return true;
+}
+
+// The kernels' bounded wait: about two seconds of SM clock.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+    return mbar_wait_for(bar, parity, err, code, 4LL << 30);
 }
 
 // ---------------------------------------------------------------------- TMA

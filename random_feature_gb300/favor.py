@@ -27,6 +27,7 @@ __all__ = [
     "favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
     "favor_attn_bidir_backward", "favor_attn_causal_backward",
     "favor_attn_causal_gated", "favor_attn_causal_step_gated", "favor_set_relpos",
+    "favor_check_bounded_wait", "FAVOR_WAIT_CHECK_CODE",
 ]
 
 FAVOR_OK, FAVOR_ERR_INVALID_ARG, FAVOR_ERR_UNSUPPORTED, FAVOR_ERR_NOMEM, FAVOR_ERR_CUDA = range(5)
@@ -42,7 +43,8 @@ EXPORTED_SYMBOLS = ("favor_create", "favor_feature_map", "favor_attn_bidir", "fa
                     "favor_profile_name", "favor_device_error", "favor_attn_bidir_noalloc",
                     "favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
                     "favor_attn_bidir_backward", "favor_attn_causal_backward",
-                    "favor_attn_causal_gated", "favor_attn_causal_step_gated", "favor_set_relpos")
+                    "favor_attn_causal_gated", "favor_attn_causal_step_gated", "favor_set_relpos",
+                    "favor_check_bounded_wait")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -107,6 +109,8 @@ def lib() -> ctypes.CDLL:
         L.favor_attn_causal_gated.argtypes = [vp, vp, vp, vp, vp, vp, i, i, vp]
         L.favor_attn_causal_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, vp]
         L.favor_set_relpos.argtypes = [vp, vp, vp]
+        L.favor_check_bounded_wait.argtypes = [vp, i, vp]
+        L.favor_check_bounded_wait.restype = ctypes.c_int
         for fn in ("favor_kv_state", "favor_attn_from_state", "favor_attn_causal_step",
                    "favor_attn_bidir_backward", "favor_attn_causal_backward", "favor_attn_causal_gated",
                    "favor_attn_causal_step_gated", "favor_set_relpos"):
@@ -259,6 +263,16 @@ def favor_device_error(h) -> int:
     code = ctypes.c_int()
     _check(lib().favor_device_error(h, ctypes.byref(code)), "favor_device_error")
     return code.value
+
+
+FAVOR_WAIT_CHECK_CODE = 901
+
+
+def favor_check_bounded_wait(h, limit_cycles: int, stream=None) -> None:
+    """Enqueue the bounded-wait check kernel (a wait that nothing completes gives
+    up after limit_cycles cycles and writes FAVOR_WAIT_CHECK_CODE to the
+    handle's device error word)."""
+    _check(lib().favor_check_bounded_wait(h, int(limit_cycles), _stream(stream, None)), "favor_check_bounded_wait")
 
 
 def favor_profile_slots() -> int:

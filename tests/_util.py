@@ -5,6 +5,15 @@ import numpy as np
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 
 
+def forward_err(got, ref, dtype):
+    """Error of a forward output under its dtype's measure: element-wise with a
+    1%-of-row floor (oracle.elem_rel_err) for fp32 storage, row-normwise
+    (oracle.row_rel_err) for bf16 storage, where rounding the features to
+    bf16 alone moves an element-wise ratio far past 2e-2."""
+    import oracle as O
+    return O.elem_rel_err(got, ref) if dtype == "f32" else O.row_rel_err(got, ref)
+
+
 def to_dev(a, dtype):
     import torch
     t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))

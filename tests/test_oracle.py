@@ -380,3 +380,22 @@ def test_row_rel_err():
     got = np.array([[1.1, -2.0], [0.0, 0.5]])
     assert O.row_rel_err(got, ref) == pytest.approx(0.5)
     assert O.row_rel_err(got[:1], ref[:1]) == pytest.approx(0.05)
+
+
+def test_elem_rel_err_hand_computed():
+    """Element-wise measure with the 1%-of-row floor, values worked by hand.
+    Row 0: max |o| = 2, floor 0.02.  Element 0: |1.1 - 1| / 1 = 0.1; element 1:
+    |0.003 - 0.001| / max(0.001, 0.02) = 0.1; element 2: 0.  Row 1 (all-zero
+    reference): absolute error 0.25.  Row 2: |0.5 - 0.4| / 0.4 = 0.25."""
+    ref = np.array([[1.0, 0.001, -2.0], [0.0, 0.0, 0.0], [0.4, -0.1, 0.2]])
+    got = np.array([[1.1, 0.003, -2.0], [0.0, 0.25, 0.0], [0.5, -0.1, 0.2]])
+    assert O.elem_rel_err(got[:1], ref[:1]) == pytest.approx(0.1)
+    assert O.elem_rel_err(got[1:2], ref[1:2]) == pytest.approx(0.25)
+    assert O.elem_rel_err(got[2:], ref[2:]) == pytest.approx(0.25)
+    assert O.elem_rel_err(got, ref) == pytest.approx(0.25)
+    # the floor: an error of 1e-5 on an element of 1e-6 in a row of max 1 counts as 1e-5 / 1e-2
+    assert O.elem_rel_err(np.array([[1.0, 1.1e-5]]), np.array([[1.0, 1e-6]])) == pytest.approx(1e-3)
+    # a plain element-wise ratio where every element is above the floor
+    assert O.elem_rel_err(np.array([[2.0, -3.3]]), np.array([[2.0, -3.0]])) == pytest.approx(0.1)
+    assert O.elem_rel_err(np.zeros((0, 3)), np.zeros((0, 3))) == 0.0
+

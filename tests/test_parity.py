@@ -1,8 +1,9 @@
 """GPU parity: the CUDA library (through its C ABI) against the float64 oracle.
 
-Tolerance: row-normwise max relative error (oracle.row_rel_err) <= 1e-4 for
-fp32 storage and <= 2e-2 for bf16 storage with fp32 accumulation.  Inputs are
-the seeded synthetic workloads; bf16 inputs and omega are bf16 values, so
+Tolerance: for fp32 storage, the element-wise relative error with a
+1%-of-row floor (oracle.elem_rel_err) <= 1e-4; for bf16 storage with fp32
+accumulation, the row-normwise error (oracle.row_rel_err) <= 2e-2.  Inputs
+are the seeded synthetic workloads; bf16 inputs and omega are bf16 values, so
 both sides see identical numbers.
 """
 import numpy as np
@@ -10,7 +11,7 @@ import pytest
 
 import oracle as O
 from synth import CONFIGS, make_workload
-from _util import TOL, to_dev, to_dev_unaligned, to_host
+from _util import TOL, forward_err, to_dev, to_dev_unaligned, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -35,8 +36,8 @@ def _check(w, mode, kind, seed=0):
     got = _run(w, mode, kind, omega, q, k, v)
     ref = _oracle(mode, kind, q, k, v, omega, w.data_scale)
     assert np.isfinite(got).all()
-    err = O.row_rel_err(got, ref)
-    assert err <= TOL[w.dtype], f"{w.name} {mode} {kind}: row-normwise error {err:.3e}"
+    err = forward_err(got, ref, w.dtype)
+    assert err <= TOL[w.dtype], f"{w.name} {mode} {kind}: error {err:.3e}"
     return err
 
 
@@ -115,8 +116,8 @@ def test_feature_map(dtype, kind):
         got = to_host(f.feature_map(to_dev(q, dtype)))
     torch.cuda.synchronize()
     ref = O.favor_feature_map(q, omega, w.data_scale, kind)
-    err = O.row_rel_err(got, ref)
-    assert err <= (1e-5 if dtype == "f32" else 8e-3), err
+    err = forward_err(got, ref, dtype) if dtype == "f32" else O.row_rel_err(got, ref)
+    assert err <= (TOL["f32"] if dtype == "f32" else 8e-3), err
 
 
 def test_relu_zero_denominator_row_is_zero():
@@ -129,7 +130,7 @@ def test_relu_zero_denominator_row_is_zero():
     got = _run(w, "bidir", "relu", omega, q, k, v)
     ref = _oracle("bidir", "relu", q, k, v, omega, 1.0)
     assert np.all(ref[0, 0, 5] == 0) and np.all(got[0, 0, 5] == 0)
-    assert O.row_rel_err(got, ref) <= 1e-4
+    assert O.elem_rel_err(got, ref) <= 1e-4
 
 
 @pytest.mark.parametrize("mode", ["bidir", "causal"])
@@ -168,5 +169,28 @@ def test_unaligned_inputs_bf16(mode, kind):
         out = f.attn(qd, kd, vd, causal=(mode == "causal"))
         torch.cuda.synchronize()
         got = to_host(out)
-    err = O.row_rel_err(got, _oracle(mode, kind, q, k, v, omega, w.data_scale))
+    err = forward_err(got, _oracle(mode, kind, q, k, v, omega, w.data_scale), w.dtype)
     assert err <= TOL[w.dtype], err
+
+
+def test_fig4_shape_as_written_parity():
+    """The approximation-error workload as written (N(0,1) * 16^-1/4 inputs,
+    H = 8, L = 4096, d = 16), ORF and iid, at the ends and middle of the m
+    sweep, two samples: every point meets the fp32 bar against the FAVOR+
+    oracle, and the error against exact softmax is finite and below the
+    output's own scale."""
+    import approx_report as AR
+    res = AR.curve(seeds=range(2), ms=(16, 64, 256))
+    for key, ent in res.items():
+        assert ent["parity"] <= TOL["f32"], (key, ent["parity"])
+        assert all(np.isfinite(x) and x < 1.0 for x in ent["mse"]), (key, ent["mse"])
+
+
+@pytest.mark.parametrize("L", [1, 33, 1000])
+@pytest.mark.parametrize("kind", ["softmax_pos", "relu"])
+def test_f32_causal_segments(L, kind):
+    """fp32 causal attention over several segments and ragged tiles (float64
+    arithmetic path): a sequence of 1000 tokens over 2 heads spans 32 tiles."""
+    w = CONFIGS["approx_f32"].replace(H=2, L=L, m=64)
+    _check(w, "causal", kind)
+    _check(w, "bidir", kind)

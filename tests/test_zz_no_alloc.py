@@ -36,6 +36,31 @@ def test_rejects_null_omega():
     assert e.value.status == R.FAVOR_ERR_INVALID_ARG
 
 
+def test_rejects_misaligned_omega():
+    """An omega address off a 16-byte boundary is refused before any launch
+    (the kernels read omega rows as 16-byte vectors)."""
+    n0 = R.favor_launch_count()
+    with pytest.raises(R.FavorError) as e:
+        R.favor_attn_bidir_noalloc(4, 2, 64, 32, 32, "softmax_pos", "f32", 1.0, 1, 1, 1, 1, 1, 128, stream=0)
+    assert e.value.status == R.FAVOR_ERR_INVALID_ARG
+    assert "aligned" in R.favor_last_error()
+    assert R.favor_launch_count() == n0
+
+
+def test_rejects_host_omega():
+    """A host buffer (16-byte aligned) is not device memory: refused before any
+    launch, on a machine with or without a GPU."""
+    om = np.zeros(2 * 64 * 32 + 16, dtype=np.float32)
+    addr = om.ctypes.data
+    addr += (-addr) % 16
+    n0 = R.favor_launch_count()
+    with pytest.raises(R.FavorError) as e:
+        R.favor_attn_bidir_noalloc(addr, 2, 64, 32, 32, "softmax_pos", "f32", 1.0, 1, 1, 1, 1, 1, 128, stream=0)
+    assert e.value.status == R.FAVOR_ERR_INVALID_ARG
+    assert "device" in R.favor_last_error()
+    assert R.favor_launch_count() == n0
+
+
 CASES = [
     # (config, overrides, kind): the tensor-core shape in bf16, with a split narrowed
     # to fit the scratch (B*H = 32, m = 256, dv = 64 leaves room for 6 segments per head),
