@@ -105,6 +105,7 @@ static void free_handle(Handle* h) {
     cudaFree(h->omega_f32);
     cudaFree(h->omega_bf16);
     cudaFree(h->kshift);
+    cudaFree(h->omega_wmax);
     cudaFree(h->dev_err);
     cudaFree(h->ws_partial);
     cudaFree(h->ws_state);
@@ -204,7 +205,7 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
         }
     }
     // Per-head key shift: kappa_h = max(0, max_r ||omega_r||^2/2 - headroom).
-    std::vector<float> ks(H);
+    std::vector<float> ks(H), wmax(H);
     h->omega_sqnorm_half_host = (float*)malloc(sizeof(float) * H);
     if (!h->omega_sqnorm_half_host) { free_handle(h); return set_error(FAVOR_ERR_NOMEM, "favor_create: host allocation failed"); }
     for (int hh = 0; hh < H; ++hh) {
@@ -218,6 +219,8 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
             if (acc > mx) mx = acc;
         }
         h->omega_sqnorm_half_host[hh] = (float)(0.5 * mx);
+        // largest row length, rounded up (its only use is an upper bound)
+        wmax[hh] = (float)(std::sqrt(mx) * (1.0 + 1e-6));
         double k = 0.5 * mx - (double)KSHIFT_HEADROOM;
         ks[hh] = (float)(k > 0.0 && kind != FAVOR_KERNEL_SOFTMAX_TRIG ? k : 0.0);
     }
@@ -233,6 +236,7 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     if (e == cudaSuccess) e = cudaMalloc(&h->omega_f32, n_om * sizeof(float));
     if (e == cudaSuccess && dtype == FAVOR_DTYPE_BF16) e = cudaMalloc(&h->omega_bf16, n_om * sizeof(__nv_bfloat16));
     if (e == cudaSuccess) e = cudaMalloc(&h->kshift, H * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->omega_wmax, H * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&h->dev_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->dev_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMalloc(&h->ws_partial, rows * st_elems * sizeof(float));
@@ -276,6 +280,7 @@ favor_status favor_create(favor_handle* out, int H, int m, int d, int dv, favor_
     if (e == cudaSuccess && dtype == FAVOR_DTYPE_BF16)
         e = cudaMemcpy(h->omega_bf16, om_bf.data(), n_om * sizeof(__nv_bfloat16), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(h->kshift, ks.data(), H * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(h->omega_wmax, wmax.data(), H * sizeof(float), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         set_error(FAVOR_ERR_CUDA, "favor_create: cudaMemcpy: %s", cudaGetErrorString(e));
         cudaGetLastError();

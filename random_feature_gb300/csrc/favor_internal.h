@@ -52,6 +52,7 @@ struct Handle {
     float* omega_f32;         // [H, m, d] (bf16-rounded values for the BF16 dtype)
     __nv_bfloat16* omega_bf16;// [H, m, d] (BF16 dtype only)
     float* kshift;            // [H] per-head key shift kappa_h (natural-log units)
+    float* omega_wmax;        // [H] per head, a bound W_h >= max_r ||omega_r|| (query shift of the causal kernel)
     float* omega_sqnorm_half_host; // host [H]: max_r ||omega_r||^2 / 2
 
     float* ws_partial;        // [rows][m * (dv+1)] per-segment states (bidir partials / causal prefixes):

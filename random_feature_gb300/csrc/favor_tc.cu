@@ -764,39 +764,48 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 //   out = num / den,   S(t+1) = S(t) + Phi_K^T V,   z(t+1) = z(t) + Phi_K^T 1
 // (App. B.1 Eq. 11 of Rethinking Attention with Performers, taken chunk by chunk).
 //
-// Roles (384 threads):
-//   warp 0: TMA producer; lanes 0, 1, 2 own the Q, K, V tiles, lane 0 also omega
-//   warp 1: MMAs P_Q = Q omega^T, one 128-feature half at a time
-//   warp 2: MMAs P_K^T = omega K^T (+ key offsets) per half, then S += Phi_K^T V
-//   warp 3: MMAs A = Phi_Q Phi_K^T, num = Phi_Q S~, num += tril(A) V
-//   warps 4..7  (lane = query): query features and Phi_Q z, causal mask and its row sums,
-//               output tile (staged in shared memory, one TMA store; rows past L are clipped)
-//   warps 8..11 (lane = key for the norms, = feature otherwise): key offsets, key
-//               features and z, S~ / z~ refresh from the fp32 state
+// Roles (576 threads, 18 warps):
+//   warp 0      TMA producer: one thread keeps the Q, K and V streams and omega independent
+//   warp 1      the MMA issuer: one thread issues every contraction in a fixed order
+//   warps 2..5  query group A (lane = query row): norm shift, features of half 0 and their
+//               part of Phi_Q z, then the causal mask of A and its row sums
+//   warps 6..9  query group B: norm shift, features of half 1 and their part of Phi_Q z,
+//               then the output rows (num / den, stored from registers)
+//   warps 10..17 key warps, two per lane quarter: warps 10..13 take tokens 0..63 of the
+//               tile, warps 14..17 tokens 64..127 (lane = feature of the quarter); key norms
+//               (first four), key features into Phi_K, z, and the S~ / z~ refresh
 //
 // Tensor memory: three rotating 128-column slots and the fp32 state in
-// [384,512) (two halves of 64 columns, lane = feature).  Chunk t uses slots
+// [384,512) (two halves of 64 columns, lane = feature).  Chunk t uses
 //   X: P_Q half 0 -> Phi_Q half 0 packed in [0,64); num in [64,128)
 //   Y: P_Q half 1 -> Phi_Q half 1 packed in [0,64)
-//   Z: P_K^T half 0, half 1, then A, then tril(A) packed in [0,64)
-// and chunk t+1 takes X' = Z (free once the intra term has read tril(A)),
-// Y' = X (free once num was read), Z' = Y (free once A and the inter term have
-// read Phi_Q), so the projections of chunk t+1 overlap the tail of chunk t.
+//   Z: P_K^T half 0, then half 1, then A, then tril(A) packed in [0,64)
+// and chunk t+1 takes X' = Z, Y' = X, Z' = Y.  One thread issues all MMAs, and
+// tcgen05.mma from one thread run in issue order, so a projection of chunk
+// t+1 that is issued after the last MMA of chunk t reading its slot needs no
+// wait for that MMA; it waits only for CUDA-core reads of the slot.  Issue
+// order of iteration t:
+//   A(t) over feature half 0 (as soon as half 0's query features are in), A
+//   over half 1, the inter term (once the S~ image of t is in), key projection
+//   half 0 of t+1, the state update of t, key projection half 1 of t+1, the
+//   intra term of t, query projection halves 0 and 1 of t+1.
+// The key warps run one step ahead of the state: they compute chunk t+1's
+// features while the state update of t is queued, holding them in registers
+// until that update has read Phi_K, then refresh S~ and publish z~ of t+2.
 //
-// Query shift: a half's features are exp2(a p - c) with an integer c.  Half 0
-// takes c0 = ceil(a max p) + kQMargin; half 1 keeps c0 unless its own maximum
-// exceeds it, and then takes c1 = ceil(a max p) and multiplies the packed half 0
-// by 2^(c0 - c1), which is exact in bf16.  Every feature is at most 1 and the
-// largest of a row at least 2^-(kQMargin+1), as with a row-max shift; the
-// common factor cancels between num and den.
-constexpr int kCausalThreads = 384;
-constexpr float kQMargin = 16.f;
+// Query shift: features are exp2(a p - c) with c = a W_h ||q|| and W_h the
+// largest row norm of the head's omega, so omega_r . q <= W_h ||q|| (Cauchy-
+// Schwarz) keeps every feature at most 1 without a pass over the row; c is a
+// per-row constant, so it cancels between num and den.  Key features are
+// exp2(a p + c_j) with the per-token offset c_j = -(s^2 ||k_j||^2 / 2 +
+// kappa_h) log2(e) taken from shared memory (-1e30 for rows past L).
+constexpr int kCausalThreads = 576;
 
 struct CaBars {
-    uint64_t q_full, k_full, v_full, q_empty, k_empty, v_empty, w_full, w_empty;
-    uint64_t ext_full, pk_full, pk_free, phik_full, phik_free, s_full, s_ready, st_full;
-    uint64_t pq0_full, pq1_full, phiq_full, a_full, ai_done, am_full, o_full, o_empty;
-    uint64_t stage_full, stage_free[2];
+    uint64_t q_full, k_full, v_full, w_full, q_empty, k_empty, v_empty, w_empty;
+    uint64_t pq0_full, pq1_full, phiq0_full, phiq1_full, pk_full, pk_free, cs_full, phik_full;
+    uint64_t phik_free, a_full, am_full, s_full, st_full, ai_done, o_full, o_empty;
+    uint64_t z_full, zx_full, mma_done, stage_full, stage_free[2];
     uint32_t tmem_base;
 };
 
@@ -805,29 +814,6 @@ __device__ __forceinline__ uint32_t ca_slot(int role, int r3) {
     int i = role - r3;
     i += (i < 0) ? 3 : 0;
     return 128u * (uint32_t)i;
-}
-
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&p)[128]) {
-    tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-    tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
-    tmem_ld32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&p[64]));
-    tmem_ld32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&p[96]));
-}
-
-// Largest of the 128 fp32 columns at taddr (one row per thread).
-__device__ __forceinline__ float tmem_rowmax128(uint32_t taddr) {
-    uint32_t p[128];
-    tmem_ld128(taddr, p);
-    tmem_ld_wait();
-    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 128; i += 4) {
-        m0 = fmaxf(m0, __uint_as_float(p[i]));
-        m1 = fmaxf(m1, __uint_as_float(p[i + 1]));
-        m2 = fmaxf(m2, __uint_as_float(p[i + 2]));
-        m3 = fmaxf(m3, __uint_as_float(p[i + 3]));
-    }
-    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
 // Features of one query half, 32 projections at a time, packed in place into
@@ -873,19 +859,6 @@ __device__ __noinline__ float query_half(uint32_t taddr, float a, float c, uint3
     return d0 + d1;
 }
 
-// Multiply the 64 packed bf16 columns at taddr by sc (an exact power of two).
-__device__ __noinline__ void scale_packed64(uint32_t taddr, float sc) {
-#pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-        uint32_t w[16];
-        tmem_ld16(taddr + 16 * blk, w);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pack_bf16(bf16lo(w[i]) * sc, bf16hi(w[i]) * sc);
-        tmem_st16(taddr + 16 * blk, w);
-    }
-}
-
 // Causal mask of one row of A (fp32, 128 columns at taddr), packed in place into
 // [0,64); returns the row sum of the kept bf16-rounded values.  Blocks of keys
 // entirely after every row of the warp (blk > q) are written as zeros unread.
@@ -916,65 +889,69 @@ __device__ __noinline__ float mask_row(uint32_t taddr, int row, int q) {
     return s0 + s1;
 }
 
-// Row `row` of the output tile (num / den, num = 64 fp32 columns at taddr)
-// into a [128][64] bf16 staging image in the 128-byte swizzled layout of the
-// output tensor map.  The columns are read first and `done` (the slot's
-// release) is arrived before the shared-memory writes.
-__device__ __noinline__ void stage_out_row(uint32_t taddr, uint32_t stage, uint32_t row, float den, uint64_t* done) {
-    uint32_t nv[64];
-    tmem_ld64(taddr, nv);
-    tmem_ld_wait();
-    tc_fence_before();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(done);
-    const float inv = den != 0.f ? 1.f / den : 0.f;
-#pragma unroll
-    for (uint32_t c = 0; c < 8; ++c)
-        st_shared_v4(stage + sw128(row, c),
-                     pack_bf16(__uint_as_float(nv[8 * c + 0]) * inv, __uint_as_float(nv[8 * c + 1]) * inv),
-                     pack_bf16(__uint_as_float(nv[8 * c + 2]) * inv, __uint_as_float(nv[8 * c + 3]) * inv),
-                     pack_bf16(__uint_as_float(nv[8 * c + 4]) * inv, __uint_as_float(nv[8 * c + 5]) * inv),
-                     pack_bf16(__uint_as_float(nv[8 * c + 6]) * inv, __uint_as_float(nv[8 * c + 7]) * inv));
-}
-
-// Key features of feature row r over the 128 tokens at taddr (fp32, offsets
-// already folded in) into Phi_K [feature][token] (two token blocks of 64);
-// returns their sum.
+// Key features of feature row r for the 64 tokens [64u, 64u + 64) of the tile
+// (their projections: 64 fp32 columns at taddr, offsets folded in by c_j), 32
+// columns at a time; `release` (if not null) is arrived once both blocks are in
+// registers, so the slot may take the next projection while the rest is
+// computed.  f = exp2(a p + c_j) (positive, c_j from cs) or max(p, 0) (ReLU),
+// packed to bf16 in registers; then, after `gate` (if not null: Phi_K's
+// previous contents are no longer read) has completed the phase of parity
+// gate_par, stored into Phi_K [feature][token] (token block u of 64, 128-byte
+// swizzle).  Returns the sum of the features; *ok = false if the gate's wait
+// gave up (nothing stored).
 template <int KIND>
-__device__ __noinline__ float key_row(uint32_t taddr, uint32_t phi, uint32_t r, float a) {
+__device__ __noinline__ float key_half_row(uint32_t taddr, uint64_t* release, uint64_t* gate, uint32_t gate_par,
+                                           int* err, bool* ok, uint32_t phi, uint32_t r, float a, uint32_t cs) {
+    uint32_t w[32];
     float z0 = 0.f, z1 = 0.f;
-#pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
         uint32_t p[32];
         tmem_ld32(taddr + 32 * blk, p);
         tmem_ld_wait();
-        const uint32_t base = phi + (uint32_t)(blk >> 1) * 2 * kPhiBlock;
+        if (blk == 1 && release) {
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(release);
+        }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-            uint32_t w4[4];
+            float c8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                const uint32_t ca_addr = cs + 4 * (32 * blk + 8 * cc);
+                const uint4 ca = ld_shared_v4(ca_addr), cb = ld_shared_v4(ca_addr + 16);
+                c8[0] = __uint_as_float(ca.x); c8[1] = __uint_as_float(ca.y);
+                c8[2] = __uint_as_float(ca.z); c8[3] = __uint_as_float(ca.w);
+                c8[4] = __uint_as_float(cb.x); c8[5] = __uint_as_float(cb.y);
+                c8[6] = __uint_as_float(cb.z); c8[7] = __uint_as_float(cb.w);
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float x0 = __uint_as_float(p[8 * cc + 2 * i]);
-                const float x1 = __uint_as_float(p[8 * cc + 2 * i + 1]);
+                const float x0 = __uint_as_float(p[8 * cc + 2 * i]), x1 = __uint_as_float(p[8 * cc + 2 * i + 1]);
                 float f0, f1;
                 if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
-                    f0 = ex2(x0 * a);
-                    f1 = ex2(x1 * a);
+                    f0 = ex2(fmaf(x0, a, c8[2 * i]));
+                    f1 = ex2(fmaf(x1, a, c8[2 * i + 1]));
                 } else {
                     f0 = fmaxf(x0, 0.f);
                     f1 = fmaxf(x1, 0.f);
                 }
                 z0 += f0;
                 z1 += f1;
-                w4[i] = pack_bf16(f0, f1);
+                w[16 * blk + 4 * cc + i] = pack_bf16(f0, f1);
             }
-            st_shared_v4(base + sw128(r, (uint32_t)(4 * (blk & 1) + cc)), w4[0], w4[1], w4[2], w4[3]);
         }
     }
+    if (gate && !mbar_wait(gate, gate_par, err, 258)) {
+        *ok = false;
+        return 0.f;
+    }
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) st_shared_v4(phi + sw128(r, (uint32_t)cc), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
     return z0 + z1;
 }
 
-// S~ image row r and z~[r] from the fp32 state row (64 columns at taddr).
+// S~ image row r from the fp32 state row (64 columns at taddr).
 __device__ __noinline__ void refresh_row(uint32_t taddr, uint32_t img, uint32_t r) {
 #pragma unroll 1
     for (int blk = 0; blk < 2; ++blk) {
@@ -1010,11 +987,49 @@ __device__ __noinline__ void load_prefix_row(const float* src, uint32_t taddr, u
     }
 }
 
+// Output row `row` of a chunk: num (64 fp32 columns at taddr) / den as bf16,
+// written into a [128][64] staging image in the 128-byte swizzled layout of
+// the output tensor map (one TMA store per chunk writes it out; rows past L
+// are clipped by the map).  32 columns at a time; `done` (the slot's release)
+// is arrived once both blocks are in registers.
+__device__ __noinline__ void out_row(uint32_t taddr, uint32_t stage, uint32_t row, float den, uint64_t* done) {
+    const float inv = den != 0.f ? 1.f / den : 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 2; ++blk) {
+        uint32_t nv[32];
+        tmem_ld32(taddr + 32 * blk, nv);
+        tmem_ld_wait();
+        if (blk == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(done);
+        }
+#pragma unroll
+        for (uint32_t c = 0; c < 4; ++c)
+            st_shared_v4(stage + sw128(row, 4 * blk + c),
+                         pack_bf16(__uint_as_float(nv[8 * c + 0]) * inv, __uint_as_float(nv[8 * c + 1]) * inv),
+                         pack_bf16(__uint_as_float(nv[8 * c + 2]) * inv, __uint_as_float(nv[8 * c + 3]) * inv),
+                         pack_bf16(__uint_as_float(nv[8 * c + 4]) * inv, __uint_as_float(nv[8 * c + 5]) * inv),
+                         pack_bf16(__uint_as_float(nv[8 * c + 6]) * inv, __uint_as_float(nv[8 * c + 7]) * inv));
+    }
+}
+
+// MMAs of the causal kernel (issued by one thread).
+//   D[128 x 128] = X tile [128 rows][64] . omega rows [w0, w0+128) -- a projection of
+//   128 rows (query rows of a Q tile, or transposed: features of omega against a K tile)
+__device__ __forceinline__ void ca_project(uint32_t d, uint32_t a_tile, uint32_t b_tile) {
+    const uint32_t id = make_idesc(128, 128, 0, 0);
+    const uint64_t a0 = make_desc(a_tile, 16, 1024, SW_128B);
+    const uint64_t b0 = make_desc(b_tile, 16, 1024, SW_128B);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(d, a0 + 2 * kk, b0 + 2 * kk, id, kk > 0 ? 1u : 0u);
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(kCausalThreads, 1)
 k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
-            const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ kshift,
+            const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ kshift, const float* __restrict__ wmax,
             const float* __restrict__ prefix, int H, int L, float s, Ranges R, int* err) {
     constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
     extern __shared__ uint8_t smem_raw[];
@@ -1025,22 +1040,28 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t s_v = s_k + kTileBytes;
     const uint32_t s_phi = s_v + kTileBytes;                  // Phi_K [256 features][128 tokens]: 2 blocks of 64 tokens
     const uint32_t s_st = s_phi + 4 * kPhiBlock;              // S~ [256 features][64], MN-major B operand
-    const uint32_t s_ext = s_st + kSBytes;                    // key offsets [128][16]
-    const uint32_t s_wext = s_ext + kExtStage;                // omega side [256][16]
-    const uint32_t s_z = s_wext + kExtOmega;                  // z~ fp32 [256]
-    const uint32_t s_stage = s_z + kM * 4;                    // output staging, 2 x [128][64] bf16 (1 KB aligned)
-    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_stage - s_w) + 2 * kTileBytes);
+    const uint32_t s_stage = s_st + kSBytes;                  // output staging, 2 x [128][64] bf16 (1 KB aligned)
+    const uint32_t s_cs = s_stage + 2 * kTileBytes;           // key offsets c_j, [2 chunk parities][128]
+    const uint32_t s_z = s_cs + 2 * kTile * 4;                // z~ fp32 [2 chunk parities][256]
+    const uint32_t s_zp = s_z + 2 * kM * 4;                   // key-warp z exchange [256]
+    const uint32_t s_dsh = s_zp + kM * 4;                     // group A's den part per row [128]
+    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_dsh - s_w) + kTile * 4);
     const int cta = blockIdx.x;
     const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
     const int n = g1 - g0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const float a = s * kLog2e;
+    const bool multi_head = H > 1;
 
     if (threadIdx.x == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bars);
         // order and arrival counts follow the fields of CaBars
-        // (each barrier completes at most once per chunk, so a parity wait cannot miss a phase)
-        const int counts[] = {1, 1, 1, 1, 5, 2, 1, 2,   4, 1, 4, 4, 2, 1, 4, 4,   1, 1, 4, 1, 1, 4, 1, 4,   4, 1, 1};
+        // (each barrier completes once per chunk -- pk_full twice, at parities 0 and 1 --
+        // so a parity wait cannot miss a phase)
+        const int counts[] = {1, 1, 1, 1, POS ? 9 : 1, POS ? 5 : 1, 1, 1,
+                              1, 1, 4, 4, 1, 8, 4, 8,
+                              1, 1, 4, 1, 8, 1, 1, 4,
+                              8, 8, 1, 4, 1, 1};
         static_assert(sizeof(counts) / sizeof(int) * sizeof(uint64_t) == offsetof(CaBars, tmem_base), "barrier table");
         for (int i = 0; i < (int)(sizeof(counts) / sizeof(int)); ++i) mbar_init(b + i, counts[i]);
         fence_mbar_init();
@@ -1049,35 +1070,28 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tmem_alloc(&bars->tmem_base, 512);
         tmem_relinquish();
     }
-    if (warp >= 4) {
-        const int t = threadIdx.x - 128, nt = kCausalThreads - 128;
-        uint32_t* e = reinterpret_cast<uint32_t*>(sm + (s_ext - s_w));
-        for (int i = t; i < (int)(kExtStage / 4); i += nt) e[i] = 0u;
-        uint32_t* wx = reinterpret_cast<uint32_t*>(sm + (s_wext - s_w));
-        for (int i = t; i < (int)(kExtOmega / 4); i += nt) wx[i] = ((i & 63) < 32 && (i & 3) == 0) ? 0x3F803F80u : 0u;
-        fence_async_smem();
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const bool multi_head = H > 1;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // One thread keeps the Q, K and V streams independent: it polls each
-        // stream's empty barrier and issues whichever next load is free.  Lane
-        // 0 also reloads omega at a head change, before the first Q tile of
-        // the new head.  Gives up after about two seconds without progress.
+        // stream's empty barrier and issues whichever next load is free.  It
+        // also reloads omega at a head change, before the first Q tile of the
+        // new head.  Gives up after about two seconds without progress, then
+        // waits (bounded) for the loads it issued.
         if (lane == 0) {
             const CUtensorMap* maps[3] = {&tm_q, &tm_k, &tm_v};
             uint64_t* fulls[3] = {&bars->q_full, &bars->k_full, &bars->v_full};
             uint64_t* empties[3] = {&bars->q_empty, &bars->k_empty, &bars->v_empty};
             const uint32_t dsts[3] = {s_q - s_w, s_k - s_w, s_v - s_w};
             int next[3] = {0, 0, 0};
-            int cur_h = -1;
+            int cur_h = -1, wloads = 0;
             uint32_t wph = 0;
             long long t0 = clock64();
+            bool failed = false;
             while (next[0] < n || next[1] < n || next[2] < n) {
                 bool progress = false;
 #pragma unroll
@@ -1094,6 +1108,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         mbar_expect_tx(&bars->w_full, kOmegaBytes);
                         tma_load_2d(sm, &tm_w, &bars->w_full, 0, h * kM);
                         cur_h = h;
+                        ++wloads;
                     }
                     mbar_expect_tx(fulls[sidx], kTileBytes);
                     tma_load_3d(sm + dsts[sidx], maps[sidx], fulls[sidx], 0, tok0, bh);
@@ -1106,85 +1121,91 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     __nanosleep(32);
                     if (clock64() - t0 > (4LL << 30)) {
                         atomicCAS(err, 0, 201);
+                        failed = true;
                         break;
                     }
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------- query projection MMAs
-        if (lane == 0) {
-            const uint32_t id_p = make_idesc(128, 128, 0, 0);
-            uint32_t wph = 0;
-            int tih = g0 % R.tph, r3 = 0;
-            for (int t = 0; t < n; ++t) {
-                const uint32_t ph = t & 1, pp = (t - 1) & 1;
-                if (t == 0 || (tih == 0 && multi_head)) {
-                    if (!mbar_wait(&bars->w_full, wph, err, 211)) break;
-                    wph ^= 1;
-                }
-                if (!mbar_wait(&bars->q_full, ph, err, 212)) break;
-                // half 0 into X (= Z of the previous chunk: free once the intra term read tril(A))
-                if (t > 0 && !mbar_wait(&bars->o_full, pp, err, 213)) break;
-                tc_fence_after();
-                const uint64_t a0 = make_desc(s_q, 16, 1024, SW_128B);
-                const uint64_t b0 = make_desc(s_w, 16, 1024, SW_128B);
-                const uint32_t dX = tmem + ca_slot(0, r3), dY = tmem + ca_slot(1, r3);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) mma_ss(dX, a0 + 2 * kk, b0 + 2 * kk, id_p, kk > 0 ? 1u : 0u);
-                mma_commit(&bars->pq0_full);
-                // half 1 into Y (= X of the previous chunk: free once num was read)
-                if (t > 0 && !mbar_wait(&bars->o_empty, pp, err, 214)) break;
-                tc_fence_after();
-                const uint64_t b1 = make_desc(s_w + 128 * 128, 16, 1024, SW_128B);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) mma_ss(dY, a0 + 2 * kk, b1 + 2 * kk, id_p, kk > 0 ? 1u : 0u);
-                mma_commit(&bars->pq1_full);
-                mma_commit(&bars->q_empty);
-                if (t + 1 < n && tih == R.tph - 1 && multi_head) mma_commit(&bars->w_empty);
-                tih = (tih + 1 == R.tph) ? 0 : tih + 1;
-                r3 = (r3 == 2) ? 0 : r3 + 1;
+            if (failed) {
+                // no copy may still be writing shared memory when the block exits
+                for (int sidx = 0; sidx < 3; ++sidx)
+                    if (next[sidx] > 0) mbar_wait_for(fulls[sidx], (next[sidx] - 1) & 1, nullptr, 0, 1LL << 28);
+                if (wloads > 0) mbar_wait_for(&bars->w_full, (wloads - 1) & 1, nullptr, 0, 1LL << 28);
             }
         }
-    } else if (warp == 2) {
-        // ------------------------------------------- key projection + state MMAs
-        if (lane == 0) {
-            const uint32_t id_k = make_idesc(128, 128, 0, 0);
-            const uint32_t id_s = make_idesc(128, 64, 0, 1);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n > 0) {
+            const uint32_t id_a = make_idesc(128, 128, 0, 1);
+            const uint32_t id_o = make_idesc(128, 64, 0, 1);
+            const uint64_t bk = make_desc(s_phi, 2 * kPhiBlock, 1024, SW_128B);   // Phi_K, N = token (2 blocks)
+            const uint64_t bs = make_desc(s_st, 8192, 1024, SW_128B);             // S~, N = value column
+            const uint64_t bv = make_desc(s_v, 8192, 1024, SW_128B);              // V, N = value column
             uint32_t wph = 0;
-            int tih = g0 % R.tph, r3 = 0, done = 0;
-            for (int t = 0; t < n; ++t) {
-                const uint32_t ph = t & 1, pp = (t - 1) & 1;
-                if (t == 0 || (tih == 0 && multi_head)) {
-                    if (!mbar_wait(&bars->w_full, wph, err, 221)) break;
-                    wph ^= 1;
-                }
-                if (!mbar_wait(&bars->k_full, ph, err, 222)) break;
-                if (!mbar_wait(&bars->ext_full, ph, err, 223)) break;
-                // Z (= Y of the previous chunk) is free once A and the inter term read Phi_Q
-                if (t > 0 && !mbar_wait(&bars->ai_done, pp, err, 224)) break;
-                const uint32_t dZ = tmem + ca_slot(2, r3);
-                bool ok = true;
-                for (int hp = 0; hp < 2; ++hp) {
-                    if (hp == 1 && !mbar_wait(&bars->pk_free, ph, err, 225)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t a0 = make_desc(s_w + hp * 128 * 128, 16, 1024, SW_128B);
-                    const uint64_t b0 = make_desc(s_k, 16, 1024, SW_128B);
+            bool ok = true;
+            int t = 0;
+            // projections of chunk 0
+            do {
+                ok = mbar_wait(&bars->w_full, wph, err, 211) && mbar_wait(&bars->k_full, 0, err, 212);
+                if (!ok) break;
+                wph ^= 1;
+                tc_fence_after();
+                ca_project(tmem + ca_slot(2, 0), s_w, s_k);                    // P_K^T half 0 -> Z
+                mma_commit(&bars->pk_full);
+                if (!(ok = mbar_wait(&bars->q_full, 0, err, 213))) break;
+                tc_fence_after();
+                ca_project(tmem + ca_slot(0, 0), s_q, s_w);                    // P_Q half 0 -> X
+                mma_commit(&bars->pq0_full);
+                if (!(ok = mbar_wait(&bars->pk_free, 0, err, 214))) break;
+                tc_fence_after();
+                ca_project(tmem + ca_slot(2, 0), s_w + 128 * 128, s_k);        // P_K^T half 1 -> Z
+                mma_commit(&bars->pk_full);
+                mma_commit(&bars->k_empty);
+                ca_project(tmem + ca_slot(1, 0), s_q, s_w + 128 * 128);        // P_Q half 1 -> Y
+                mma_commit(&bars->pq1_full);
+                mma_commit(&bars->q_empty);
+                if (n > 1 && multi_head && (g0 + 1) % R.tph == 0) mma_commit(&bars->w_empty);
+            } while (0);
+            for (t = 0; t < n && ok; ++t) {
+                const uint32_t ph = t & 1;
+                const int r3 = t % 3, r3n = (t + 1) % 3;
+                const uint32_t X = tmem + ca_slot(0, r3), Y = tmem + ca_slot(1, r3), Z = tmem + ca_slot(2, r3);
+                const bool more = t + 1 < n;
+                const bool new_w = more && multi_head && (g0 + t + 1) % R.tph == 0;
+                const uint32_t Xn = tmem + ca_slot(0, r3n), Yn = tmem + ca_slot(1, r3n), Zn = tmem + ca_slot(2, r3n);
+                // A = Phi_Q Phi_K^T, feature half 0 as soon as its query features are in, then half 1
+                if (!(ok = mbar_wait(&bars->phiq0_full, ph, err, 221) && mbar_wait(&bars->phik_full, ph, err, 222))) break;
+                tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) mma_ss(dZ, a0 + 2 * kk, b0 + 2 * kk, id_k, kk > 0 ? 1u : 0u);
-                    mma_ss(dZ, make_desc(s_wext + hp * 128 * 32, 128, 256, SW_NONE), make_desc(s_ext, 128, 256, SW_NONE),
-                           id_k, 1u);
+                for (int kk = 0; kk < 8; ++kk) mma_ts(Z, X + 8 * kk, bk + 128 * kk, id_a, kk > 0 ? 1u : 0u);
+                if (!(ok = mbar_wait(&bars->phiq1_full, ph, err, 224))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 8; kk < 16; ++kk) mma_ts(Z, Y + 8 * (kk - 8), bk + 128 * kk, id_a, 1u);
+                mma_commit(&bars->a_full);
+                // inter term num = Phi_Q S~(t) once the S~ / z~ image of this chunk is in
+                if (!(ok = mbar_wait(&bars->st_full, ph, err, 223))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) mma_ts(X + 64, X + 8 * kk, bs + 128 * kk, id_o, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 8; kk < 16; ++kk) mma_ts(X + 64, Y + 8 * (kk - 8), bs + 128 * kk, id_o, 1u);
+                mma_commit(&bars->ai_done);
+                if (more) {
+                    // key projection half 0 of chunk t+1 into Z' = Y (its last reader, the inter term, is issued)
+                    if (new_w) {
+                        if (!(ok = mbar_wait(&bars->w_full, wph, err, 226))) break;
+                        wph ^= 1;
+                    }
+                    if (!(ok = mbar_wait(&bars->k_full, (t + 1) & 1, err, 227))) break;
+                    tc_fence_after();
+                    ca_project(Zn, s_w, s_k);
                     mma_commit(&bars->pk_full);
                 }
-                if (!ok) break;
-                mma_commit(&bars->k_empty);
-                if (t + 1 < n && tih == R.tph - 1 && multi_head) mma_commit(&bars->w_empty);
-                // state: S_h += Phi_K^T_h V (A = Phi_K rows of half h, K-major over tokens)
-                if (!mbar_wait(&bars->phik_full, ph, err, 226)) break;
-                if (!mbar_wait(&bars->v_full, ph, err, 227)) break;
-                if (!mbar_wait(&bars->s_ready, ph, err, 228)) break;
+                // state: S_h += Phi_K^T_h V (A = Phi_K rows of half h, K-major over tokens); the key
+                // warps keep chunk t+1's features in registers until it has read Phi_K
+                if (!(ok = mbar_wait(&bars->v_full, ph, err, 225))) break;
                 tc_fence_after();
-                const uint64_t bv = make_desc(s_v, 8192, 1024, SW_128B);
 #pragma unroll
                 for (int hp = 0; hp < 2; ++hp) {
                     const uint64_t a0 = make_desc(s_phi + hp * 128 * 128, 16, 1024, SW_128B);
@@ -1192,215 +1213,231 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(d, a0 + (uint64_t)((((kk >> 2) * 2 * kPhiBlock) + (kk & 3) * 32) >> 4), bv + 128 * kk,
-                               id_s, 1u);
+                               id_o, 1u);
                 }
                 mma_commit(&bars->s_full);
                 mma_commit(&bars->phik_free);
-                mma_commit(&bars->v_empty);
-                tih = (tih + 1 == R.tph) ? 0 : tih + 1;
-                r3 = (r3 == 2) ? 0 : r3 + 1;
-                done = t + 1;
-            }
-            // nobody else waits for the last state update: let it finish before tensor memory is freed
-            if (n > 0 && done == n) mbar_wait(&bars->s_full, (n - 1) & 1, err, 229);
-        }
-    } else if (warp == 3) {
-        // ----------------------------------------------- A, inter and intra MMAs
-        if (lane == 0) {
-            const uint32_t id_a = make_idesc(128, 128, 0, 1);
-            const uint32_t id_o = make_idesc(128, 64, 0, 1);
-            int r3 = 0;
-            for (int t = 0; t < n; ++t) {
-                const uint32_t ph = t & 1;
-                const uint32_t dX = tmem + ca_slot(0, r3), dY = tmem + ca_slot(1, r3), dZ = tmem + ca_slot(2, r3);
-                if (!mbar_wait(&bars->phiq_full, ph, err, 231)) break;
-                if (!mbar_wait(&bars->phik_full, ph, err, 232)) break;
+                if (more) {
+                    // key projection half 1 of t+1 once half 0's projections are in registers
+                    if (!(ok = mbar_wait(&bars->pk_free, (t + 1) & 1, err, 230))) break;
+                    tc_fence_after();
+                    ca_project(Zn, s_w + 128 * 128, s_k);
+                    mma_commit(&bars->pk_full);
+                    mma_commit(&bars->k_empty);
+                }
+                // intra term: num += tril(A) V
+                if (!(ok = mbar_wait(&bars->am_full, ph, err, 228))) break;
                 tc_fence_after();
-                // A = Phi_Q Phi_K^T into Z; B = Phi_K [feature][token]: N = token (2 blocks, LBO), K = feature
-                const uint64_t bk = make_desc(s_phi, 2 * kPhiBlock, 1024, SW_128B);
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
-                    mma_ts(dZ, kk < 8 ? dX + 8 * kk : dY + 8 * (kk - 8), bk + 128 * kk, id_a, kk > 0 ? 1u : 0u);
-                mma_commit(&bars->a_full);
-                mma_commit(&bars->phik_free);
-                // inter: num = Phi_Q S~ into X[64,128)
-                if (!mbar_wait(&bars->st_full, ph, err, 233)) break;
-                tc_fence_after();
-                const uint64_t bs = make_desc(s_st, 8192, 1024, SW_128B);
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
-                    mma_ts(dX + 64, kk < 8 ? dX + 8 * kk : dY + 8 * (kk - 8), bs + 128 * kk, id_o, kk > 0 ? 1u : 0u);
-                mma_commit(&bars->ai_done);
-                // intra: num += tril(A) V
-                if (!mbar_wait(&bars->am_full, ph, err, 234)) break;
-                if (!mbar_wait(&bars->v_full, ph, err, 235)) break;
-                tc_fence_after();
-                const uint64_t bv = make_desc(s_v, 8192, 1024, SW_128B);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) mma_ts(dX + 64, dZ + 8 * kk, bv + 128 * kk, id_o, 1u);
+                for (int kk = 0; kk < 8; ++kk) mma_ts(X + 64, Z + 8 * kk, bv + 128 * kk, id_o, 1u);
                 mma_commit(&bars->o_full);
                 mma_commit(&bars->v_empty);
-                r3 = (r3 == 2) ? 0 : r3 + 1;
+                if (more) {
+                    // query projection half 0 of t+1 into X' = Z (tril(A) read above, mask read before am_full)
+                    if (!(ok = mbar_wait(&bars->q_full, (t + 1) & 1, err, 229))) break;
+                    tc_fence_after();
+                    ca_project(Xn, s_q, s_w);
+                    mma_commit(&bars->pq0_full);
+                    // query projection half 1 of t+1 into Y' = X once the output has read num
+                    if (!(ok = mbar_wait(&bars->o_empty, ph, err, 231))) break;
+                    tc_fence_after();
+                    ca_project(Yn, s_q, s_w + 128 * 128);
+                    mma_commit(&bars->pq1_full);
+                    mma_commit(&bars->q_empty);
+                    if (t + 2 < n && multi_head && (g0 + t + 2) % R.tph == 0) mma_commit(&bars->w_empty);
+                }
             }
+            // every MMA issued has completed before tensor memory is freed
+            mma_commit(&bars->mma_done);
+            mbar_wait_for(&bars->mma_done, 0, ok ? err : nullptr, 232, ok ? (4LL << 30) : (1LL << 28));
         }
-    } else if (warp < 8) {
-        // ---------------------------------------------------------- query side
+    } else if (warp < 10) {
+        // ----------------------------------------------------------- query groups
+        const bool grpA = warp < 6;
         const int q = warp & 3;
         const uint32_t row = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-        int r3 = 0;
+        float* dsh = reinterpret_cast<float*>(sm + (s_dsh - s_w));
+        int wh = -1;
+        float W = 0.f;
         for (int t = 0; t < n; ++t) {
             const uint32_t ph = t & 1;
-            const int g = g0 + t, bh = g / R.tph, tok0 = (g % R.tph) * kTile;
-            const uint32_t X = tl + ca_slot(0, r3), Y = tl + ca_slot(1, r3), Z = tl + ca_slot(2, r3);
-            if (!mbar_wait(&bars->st_full, ph, err, 241)) break;   // z~ of this chunk's state
-            if (!mbar_wait(&bars->pq0_full, ph, err, 242)) break;
-            tc_fence_after();
-            float c0 = 0.f, den;
-            if (POS) c0 = ceilf(tmem_rowmax128(X) * a) + kQMargin;
-            den = query_half<KIND>(X, a, c0, s_z);
-            if (!mbar_wait(&bars->pq1_full, ph, err, 243)) break;
-            tc_fence_after();
-            {
-                float c1 = c0;
-                if (POS) {
-                    const float need = ceilf(tmem_rowmax128(Y) * a);
-                    c1 = need > c0 ? need : c0;
+            const int g = g0 + t, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
+            const int r3 = t % 3;
+            // row shift from the query norm (positive features)
+            float c = 0.f;
+            if (POS) {
+                if (!mbar_wait(&bars->q_full, ph, err, 241)) break;
+                if (h != wh) {
+                    W = __ldg(wmax + h);
+                    wh = h;
                 }
-                const float d1 = query_half<KIND>(Y, a, c1, s_z + 4 * 128);
-                if (POS && __any_sync(0xffffffffu, c1 > c0)) {
-                    // half 1 holds the row's maximum: scale the packed half 0 by 2^(c0 - c1) (exact)
-                    const int e = (int)(c0 - c1);
-                    const float sc = e >= -126 ? __int_as_float((127 + e) << 23) : 0.f;
-                    tmem_st_wait();
-                    scale_packed64(X, sc);
-                    den *= sc;
-                }
-                den += d1;
+                c = a * W * sqrtf(row_sqnorm(s_q, row));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->q_empty);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->phiq_full);
-            // causal mask: keep key j <= query row, packed in place into Z[0,64); row sums into den
-            if (!mbar_wait(&bars->a_full, ph, err, 244)) break;
-            tc_fence_after();
-            den += mask_row(Z, (int)row, q);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->am_full);
-            // output tile: num / den staged in shared memory, written by one TMA store
-            if (!mbar_wait(&bars->o_full, ph, err, 245)) break;
-            tc_fence_after();
-            if (t >= 2 && !mbar_wait(&bars->stage_free[t & 1], ((t >> 1) - 1) & 1, err, 246)) break;
-            {
-                const uint32_t stage = s_stage + (uint32_t)(t & 1) * kTileBytes;
-                stage_out_row(X + 64, stage, row, den, &bars->o_empty);
+            if (!mbar_wait(&bars->z_full, ph, err, 242)) break;   // z~ of this chunk
+            const uint32_t zt = s_z + ph * kM * 4;
+            if (grpA) {
+                if (!mbar_wait(&bars->pq0_full, ph, err, 243)) break;
+                tc_fence_after();
+                const float dA = query_half<KIND>(tl + ca_slot(0, r3), a, c, zt);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->phiq0_full);
+                // causal mask: keep key j <= query row, packed in place into Z[0,64)
+                if (!mbar_wait(&bars->a_full, ph, err, 244)) break;
+                tc_fence_after();
+                const float rs = mask_row(tl + ca_slot(2, r3), (int)row, q);
+                dsh[row] = dA + rs;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->am_full);
+            } else {
+                if (!mbar_wait(&bars->pq1_full, ph, err, 245)) break;
+                tc_fence_after();
+                const float dB = query_half<KIND>(tl + ca_slot(1, r3), a, c, zt + 4 * 128);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->phiq1_full);
+                // output rows: num / den, den = this half + group A's half and row sum
+                if (!mbar_wait(&bars->o_full, ph, err, 246)) break;
+                if (!mbar_wait(&bars->am_full, ph, err, 247)) break;   // dsh of this chunk is visible
+                tc_fence_after();
+                // num / den staged in shared memory, written by one TMA store (rows past L are clipped)
+                if (t >= 2 && !mbar_wait(&bars->stage_free[ph], ((t >> 1) - 1) & 1, err, 248)) break;
+                const uint32_t stage = s_stage + ph * kTileBytes;
+                out_row(tl + ca_slot(0, r3) + 64, stage, row, dB + dsh[row], &bars->o_empty);
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->stage_full);
-                if (warp == 4 && lane == 0) {
-                    if (!mbar_wait(&bars->stage_full, t & 1, err, 247)) break;
+                if (warp == 6 && lane == 0) {
+                    if (!mbar_wait(&bars->stage_full, ph, err, 249)) break;
                     tma_store_3d(&tm_o, stage, 0, tok0, bh);
                     bulk_commit();
                     bulk_wait_read<1>();   // the previous chunk's store has read its buffer
-                    if (t >= 1) mbar_arrive(&bars->stage_free[(t - 1) & 1]);
+                    if (t >= 1) mbar_arrive(&bars->stage_free[ph ^ 1]);
                 }
             }
-            r3 = (r3 == 2) ? 0 : r3 + 1;
         }
     } else {
-        // ------------------------------------------------------------ key side
-        // thread owns key row r0 of the tile (offsets) and features r0, r0 + 128
-        const int q = warp & 3;
+        // ------------------------------------------------------------- key warps
+        // lane quarter q = warp % 4.  Warps 10..13 (u = 0): tokens [0,64) of the tile,
+        // features r0 = 32q + lane (half 0) and r0 + 128 (half 1); warps 14..17 (u = 1):
+        // tokens [64,128).  The u = 0 warps compute the key offsets and own row r0 of
+        // S~ / z~, the u = 1 warps row r0 + 128.  Per chunk t: the key features of t
+        // (held in registers until the state update of t-1 has read Phi_K), then the
+        // S~ refresh of t (the inter term of t waits for it, the state update of t
+        // follows that), then z~ of t+1 for the query groups.
+        const int q = warp & 3, u = (warp - 10) >> 2;
         const uint32_t r0 = 32 * q + lane;
+        const uint32_t rown = r0 + 128 * (uint32_t)u;        // the state row this thread owns
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
         float* zs = reinterpret_cast<float*>(sm + (s_z - s_w));
-        const float inv_s = 1.f / s;
-        float z[2] = {0.f, 0.f};
-        int cur_bh = -1, kap_h = -1, r3 = 0;
+        float* zp = reinterpret_cast<float*>(sm + (s_zp - s_w));
+        float* cs = reinterpret_cast<float*>(sm + (s_cs - s_w));
+        float zpre = 0.f;           // z of the piece's prefix for row rown
+        float zr[2] = {0.f, 0.f};   // this thread's running sums over its tokens, rows r0 and r0 + 128
+        int cur_bh = -1, kap_h = -1, nzx = 0;
         float kap = 0.f;
-        for (int t = 0; t < n; ++t) {
-            const uint32_t ph = t & 1, pp = (t - 1) & 1;
+        bool ok = true;
+        for (int t = 0; t < n && ok; ++t) {
+            const uint32_t ph = t & 1;
             const int g = g0 + t, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
+            const int r3 = t % 3;
             const uint32_t Z = tl + ca_slot(2, r3);
-            // key offsets of this chunk: -(s^2 ||k||^2 / 2 + kappa_h) / s as bf16 hi + lo
-            if (!mbar_wait(&bars->k_full, ph, err, 251)) break;
-            if (POS) {
+            // key offsets of this chunk (tokens 32q + lane), in cs[t & 1]
+            if (POS && u == 0) {
+                if (!(ok = mbar_wait(&bars->k_full, ph, err, 251))) break;
                 if (h != kap_h) {
                     kap = __ldg(kshift + h);
                     kap_h = h;
                 }
                 const float nrm = row_sqnorm(s_k, r0);
-                const float x = (tok0 + (int)r0 < L) ? -(0.5f * s * nrm + kap * inv_s) : -1.0e30f;
-                const float hi = __bfloat162float(__float2bfloat16_rn(x));
-                st_shared_v4(s_ext + ext_row(r0), pack_bf16(hi, x - hi), 0u, 0u, 0u);
-                fence_async_smem();
+                cs[ph * kTile + r0] = (tok0 + (int)r0 < L) ? -(0.5f * s * s * nrm + kap) * kLog2e : -1.0e30f;
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars->k_empty);
+                    mbar_arrive(&bars->cs_full);
+                }
             }
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars->ext_full);
-                mbar_arrive(&bars->k_empty);
-            }
-            // this chunk's state: the piece's prefix at a piece start, else S(t) from the master
-            if (t > 0) {
-                if (!mbar_wait(&bars->s_full, pp, err, 252)) break;
-                if (!mbar_wait(&bars->ai_done, pp, err, 253)) break;
-                tc_fence_after();
-            }
-            if (bh != cur_bh) {
+            const bool piece_start = bh != cur_bh;
+            if (piece_start) {
+                // the piece's prefix: fp32 state row and S~ image row, z~ of this chunk
+                if (t > 0) {
+                    ok = mbar_wait(&bars->s_full, ph ^ 1, err, 252) && mbar_wait(&bars->ai_done, ph ^ 1, err, 253);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
                 const float* pre = prefix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1));
-#pragma unroll 1
-                for (int hp = 0; hp < 2; ++hp) {
-                    const uint32_t r = r0 + 128 * hp;
-                    load_prefix_row(pre + r, tl + 384 + 64 * hp, s_st, r);
-                    z[hp] = pre[(size_t)64 * kM + r];
-                    zs[r] = z[hp];
-                }
+                load_prefix_row(pre + rown, tl + 384 + 64 * u, s_st, rown);
+                zpre = pre[(size_t)64 * kM + rown];
+                zr[0] = zr[1] = 0.f;
+                zs[ph * kM + rown] = zpre;
                 tmem_st_wait();
-                cur_bh = bh;
-            } else {
-#pragma unroll 1
-                for (int hp = 0; hp < 2; ++hp) {
-                    const uint32_t r = r0 + 128 * hp;
-                    refresh_row(tl + 384 + 64 * hp, s_st, r);
-                    zs[r] = z[hp];
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars->s_ready);
-                mbar_arrive(&bars->st_full);
-            }
-            // key features of both halves -> Phi_K [feature][token] in shared memory, z
-            bool ok = mbar_wait(&bars->pk_full, 0, err, 254);
-            if (ok) {
-                tc_fence_after();
-                if (t > 0) ok = mbar_wait(&bars->phik_free, pp, err, 255);
-            }
-            if (ok) {
-                z[0] += key_row<KIND>(Z, s_phi, r0, a);
+                fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->pk_free);
-                ok = mbar_wait(&bars->pk_full, 1, err, 256);
+                if (lane == 0) {
+                    mbar_arrive(&bars->st_full);
+                    mbar_arrive(&bars->z_full);
+                }
+                cur_bh = bh;
             }
-            if (ok) {
+            // key features, half 0 then half 1, of this warp's 64 tokens
+            float zc[2];
+#pragma unroll 1
+            for (int hp = 0; hp < 2; ++hp) {
+                if (!(ok = mbar_wait(&bars->pk_full, (uint32_t)hp, err, 255 + hp))) break;
+                if (hp == 0 && POS && !(ok = mbar_wait(&bars->cs_full, ph, err, 257))) break;
                 tc_fence_after();
-                z[1] += key_row<KIND>(Z, s_phi, r0 + 128, a);
+                // half 0's projections go to registers first (then the slot may take half 1);
+                // stores into Phi_K wait until the state update of t-1 has read it
+                zc[hp] = key_half_row<KIND>(Z + 64 * (uint32_t)u, hp == 0 ? &bars->pk_free : nullptr,
+                                            (hp == 0 && t > 0) ? &bars->phik_free : nullptr, ph ^ 1, err, &ok,
+                                            s_phi + (uint32_t)u * 2 * kPhiBlock, r0 + 128 * (uint32_t)hp, a,
+                                            s_cs + (ph * kTile + 64 * (uint32_t)u) * 4);
+                if (!ok) break;
             }
             if (!ok) break;
+            zr[0] += zc[0];
+            zr[1] += zc[1];
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->phik_full);
-            r3 = (r3 == 2) ? 0 : r3 + 1;
+            // S~ image of this chunk from the running state S(t) (after the state update of t-1;
+            // the inter term of t-1 has read the previous image)
+            if (!piece_start) {
+                ok = mbar_wait(&bars->s_full, ph ^ 1, err, 252) && mbar_wait(&bars->ai_done, ph ^ 1, err, 253);
+                if (!ok) break;
+                tc_fence_after();
+                refresh_row(tl + 384 + 64 * u, s_st, rown);
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->st_full);
+            }
+            // z~ of chunk t+1 (same piece): this thread's sums plus the partner warp's for row rown
+            if (t + 1 < n && (g + 1) / R.tph == bh) {
+                // both query groups are past their wait for z~ of t (A(t) needed their features),
+                // so the next phase of z_full cannot be mistaken for this one
+                if (!(ok = mbar_wait(&bars->a_full, ph, err, 260))) break;
+                zp[r0 + 128 * (uint32_t)(1 - u)] = zr[1 - u];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->zx_full);
+                if (!(ok = mbar_wait(&bars->zx_full, (uint32_t)(nzx & 1), err, 259))) break;
+                ++nzx;
+                zs[(ph ^ 1) * kM + rown] = zpre + zr[u] + zp[rown];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->z_full);
+            }
         }
     }
-    if (threadIdx.x == 4 * 32) bulk_wait<0>();   // output stores complete before exit
+    if (threadIdx.x == 6 * 32) bulk_wait<0>();   // output stores complete before exit
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, 512);
@@ -1489,8 +1526,8 @@ __global__ void k_wait_expiry(int* err, long long limit, int code) {
 constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * kExtStage + kExtOmega + sizeof(StBars);
 constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kRStages * kTileBytes + kRImage + 2 * kTileBytes +
                                  2 * 4 * kTile * 4 + sizeof(RdBars);
-constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kSBytes + kExtStage + kExtOmega +
-                                kM * 4 + 2 * kTileBytes + sizeof(CaBars);
+constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kSBytes + 2 * kTileBytes + 2 * kTile * 4 +
+                                3 * kM * 4 + kTile * 4 + sizeof(CaBars);
 static_assert(kSmemCausal <= 232448, "causal shared memory");
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
 
@@ -1619,10 +1656,10 @@ favor_status tc_causal(const Handle& h, const void* q, const void* k, const void
     ProfScope ps(h, PROF_CAUSAL, st);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
         k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kCausalThreads, kSmemCausal, st>>>(
-            mq, mk, mv, mw, mo, h.kshift, h.ws_partial, h.H, L, h.s, R, h.dev_err);
+            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, h.H, L, h.s, R, h.dev_err);
     else
         k_tc_causal<FAVOR_KERNEL_RELU><<<R.G, kCausalThreads, kSmemCausal, st>>>(
-            mq, mk, mv, mw, mo, h.kshift, h.ws_partial, h.H, L, h.s, R, h.dev_err);
+            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, h.H, L, h.s, R, h.dev_err);
     count_launch();
     return check_launch("tensor-core causal kernel");
 }
