@@ -172,7 +172,7 @@ FP64_NOMINAL_TFLOPS = 1.25   # GB300 FP64 (datasheet); the fp32-storage path com
 
 def compute_path(w, kind="softmax_pos"):
     """Which units a forward call of workload w runs on."""
-    if w.dtype == "bf16" and (w.d, w.dv, w.m) == (64, 64, 256) and kind != "softmax_trig":
+    if w.dtype == "bf16" and (w.d, w.dv, w.m) == (64, 64, 256):
         return "tensor cores"
     if w.dtype == "f32" and kind in ("softmax_pos", "relu", "softmax_hyp"):
         return "CUDA cores, float64"
@@ -557,8 +557,8 @@ def run_ours(args):
                 "kernels": bk}
 
     # Feature variants and relative positions on the same workload, one line each:
-    # hyperbolic features (tensor cores), trigonometric features, RFA-Gate gated
-    # causal and PermuteFormer (CUDA cores).  Roofline: the forward's flops per
+    # hyperbolic and trigonometric features (tensor cores), RFA-Gate gated causal
+    # and PermuteFormer (CUDA cores).  Roofline: the forward's flops per
     # token*head (4md + 4m(dv+1)) against the tensor peak (tensor-core calls) or
     # the FP32 FFMA peak (CUDA-core calls).
     variants = None
@@ -597,7 +597,8 @@ def run_ours(args):
                 c1.record(stream)
                 torch.cuda.synchronize(dev)
                 ms = c0.elapsed_time(c1) / args.variant_steps
-                tc = kind == "softmax_hyp" and w.dtype == "bf16" and (w.d, w.dv, w.m) == (64, 64, 256)
+                tc = (kind in ("softmax_hyp", "softmax_trig") and extra is None and w.dtype == "bf16"
+                      and (w.d, w.dv, w.m) == (64, 64, 256))
                 pk = peaks["bf16_tflops_sustained"] * 1e12 if tc else fp32_peak
                 res[mode] = {"ms": ms, "value": T / (ms / 1e3), "unit": UNIT,
                              "path": "tensor cores" if tc else "CUDA cores",

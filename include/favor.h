@@ -88,8 +88,12 @@ typedef struct favor_handle_s* favor_handle;
  *
  * Supported: d, dv in {16, 32, 64, 128}; m a multiple of 16 in [16, 256];
  * H >= 1.  The hyperbolic kind runs every call the positive kind runs (on the
- * rows [omega; -omega]).  The trigonometric kind runs on the CUDA cores only;
- * its key features carry exp(||s k||^2/2) unshifted, so keys with
+ * rows [omega; -omega]).  The trigonometric kind runs on the rows
+ * [omega; omega] (sin on the first m/2 features, cos on the others): its
+ * forward calls take the tensor-core kernels for bf16 with d = dv = 64 and
+ * m = 256 (features rounded to bf16 there, so a row's rounding error grows
+ * with its cancellation) and the CUDA cores otherwise; the plain feature map
+ * stays on the CUDA cores.  Its key features carry exp(||s k||^2/2) unshifted, so keys with
  * ||s k||^2 above about 170 overflow fp32; its denominators can be zero or
  * negative (the instability §2.3 describes), and a zero one gives a zero row
  * as for ReLU.  It has no backward and no handle-free call

@@ -91,10 +91,12 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
 // Feature warps then need only f = 2^(a * D): they read a slot once
 // (releasing it at once for the next tile's projection), accumulate z_r in
 // registers, and write the features packed (bf16) to Phi0 / Phi1, the A
-// operand (tensor memory) of S_half += Phi^T_half V.
+// operand (tensor memory) of S_half += Phi^T_half V.  Trigonometric features
+// (rows [omega; omega]) take sin of s D in half 0 and cos in half 1, times the
+// token's h(s k_j) = exp(s^2 ||k_j||^2 / 2), which the norm warp writes per stage.
 //   tensor memory: P0 [0,128) P1 [128,256) Phi0 [256,320) Phi1 [320,384) S0 [384,448) S1 [448,512)
 //   warp 0: TMA producer   warp 1: projection MMAs   warp 2: state MMAs
-//   warp 3: key norms -> offsets (positive features)
+//   warp 3: key norms -> offsets (positive features) or h(s k_j) (trigonometric)
 //   warps 4..11: features; lane quarter q = warp % 4, half h = (warp - 4) / 4
 // The two MMA streams are independent (projections read omega and K, state
 // updates read Phi and V) and a single issuing thread is the bottleneck, so each
@@ -124,6 +126,7 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
            const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ kshift, float* __restrict__ part,
            int H, int L, float s, Ranges R, int* err) {
     constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
+    constexpr bool TRIG = KIND == FAVOR_KERNEL_SOFTMAX_TRIG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
@@ -279,10 +282,11 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         }
     } else if (warp == 3) {
         // ---------------------------------------------------------- key norms
-        // Per token: x = c_j / a with c_j = -(s^2 ||k_j||^2 / 2 + kappa_h) log2(e)
-        // (a huge negative value past L), written as bf16 hi + lo into the
-        // stage's K-side extra block.  Four tokens per lane.
-        if (POS) {
+        // Per token, positive features: x = c_j / a with c_j = -(s^2 ||k_j||^2 / 2 +
+        // kappa_h) log2(e) (a huge negative value past L), written as bf16 hi + lo
+        // into the stage's K-side extra block; trigonometric features: the factor
+        // h(s k_j) as fp32 in the same block, for the feature warps.  Four tokens per lane.
+        if (POS || TRIG) {
             int kap_h = -1;
             float kap = 0.f;
             const float inv_s = 1.f / s;
@@ -300,10 +304,16 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const uint32_t j = (uint32_t)(lane + 32 * t);
-                    const float x = (tok0 + (int)j < L) ? -(0.5f * s * nrm[t] + kap * inv_s) : -1.0e30f;
-                    const float hi = __bfloat162float(__float2bfloat16_rn(x));
-                    const float lo = x - hi;
-                    st_shared_v4(s_ext + st * kExtStage + ext_row(j), pack_bf16(hi, lo), 0u, 0u, 0u);
+                    if (TRIG) {
+                        // h(s k_j) = exp(s^2 ||k_j||^2 / 2), 0 past L, one fp32 per token
+                        const float hk = (tok0 + (int)j < L) ? expf(0.5f * s * s * nrm[t]) : 0.f;
+                        reinterpret_cast<float*>(sm + (s_ext - s_w) + st * kExtStage)[j] = hk;
+                    } else {
+                        const float x = (tok0 + (int)j < L) ? -(0.5f * s * nrm[t] + kap * inv_s) : -1.0e30f;
+                        const float hi = __bfloat162float(__float2bfloat16_rn(x));
+                        const float lo = x - hi;
+                        st_shared_v4(s_ext + st * kExtStage + ext_row(j), pack_bf16(hi, lo), 0u, 0u, 0u);
+                    }
                 }
                 fence_async_smem();
                 __syncwarp();
@@ -342,21 +352,42 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             // features into registers first: the exps overlap the previous tile's
             // state MMAs, which still read this warp's Phi region
             uint32_t w[64];
+            if (TRIG) {
+                // sin (half 0) or cos (half 1) of s p, times h(s k_j) of the token
+                const int st = i % kNS;
+                if (!mbar_wait(&bars->ext_full[st], (i / kNS) & 1, err, 122)) break;
+                const float4* hk = reinterpret_cast<const float4*>(sm + (s_ext - s_w) + st * kExtStage);
 #pragma unroll
-            for (int k2 = 0; k2 < 64; ++k2) {
-                const float x0 = __uint_as_float(p[2 * k2]), x1 = __uint_as_float(p[2 * k2 + 1]);
-                float f0, f1;
-                if (POS) {
-                    f0 = ex2(x0 * a);
-                    f1 = ex2(x1 * a);
-                } else {
-                    // ReLU: rows past L are zero (TMA fill), so their projection is 0
-                    f0 = fmaxf(x0, 0.f);
-                    f1 = fmaxf(x1, 0.f);
+                for (int k4 = 0; k4 < 32; ++k4) {
+                    const float4 h4 = hk[k4];
+                    const float hh[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k2 = 2 * k4 + e;
+                        const float f0 = sincos_reduced(s * __uint_as_float(p[2 * k2]), hp == 1) * hh[2 * e];
+                        const float f1 = sincos_reduced(s * __uint_as_float(p[2 * k2 + 1]), hp == 1) * hh[2 * e + 1];
+                        z0 += f0;
+                        z1 += f1;
+                        w[k2] = pack_bf16(f0, f1);
+                    }
                 }
-                z0 += f0;
-                z1 += f1;
-                w[k2] = pack_bf16(f0, f1);
+            } else {
+#pragma unroll
+                for (int k2 = 0; k2 < 64; ++k2) {
+                    const float x0 = __uint_as_float(p[2 * k2]), x1 = __uint_as_float(p[2 * k2 + 1]);
+                    float f0, f1;
+                    if (POS) {
+                        f0 = ex2(x0 * a);
+                        f1 = ex2(x1 * a);
+                    } else {
+                        // ReLU: rows past L are zero (TMA fill), so their projection is 0
+                        f0 = fmaxf(x0, 0.f);
+                        f1 = fmaxf(x1, 0.f);
+                    }
+                    z0 += f0;
+                    z1 += f1;
+                    w[k2] = pack_bf16(f0, f1);
+                }
             }
             if (i > 0 && !mbar_wait(&bars->phi_empty[hp], (i - 1) & 1, err, 123)) break;
             tc_fence_after();
@@ -494,6 +525,8 @@ __global__ void k_pack_state(const float* __restrict__ state, uint8_t* __restric
 // to another head.  Per 128-query tile t (tensor-memory slot t mod 2, 256 columns):
 //   P = Q omega^T (N = 256)                     -> slot [0,256)
 //   Phi_Q = exp2(a P - a max_r P) packed bf16   -> [0,64) (features 0..127), [192,256) (128..255)
+//           (ReLU: max(P, 0); trigonometric, rows [omega; omega]: sin / cos of s P,
+//           without h(x), a factor of the row that cancels in num / den)
 //   [num | den] = Phi_Q [S~ | z~] (N = 80)      -> [64,144)
 //   out = num / den, staged in shared memory and written by one TMA store
 // (Eq. 4 of Rethinking Attention with Performers).  The feature and output
@@ -525,6 +558,7 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              const __grid_constant__ CUtensorMap tm_o, const uint8_t* __restrict__ image, int H, int L, float s,
              Ranges R, int* err) {
     constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
+    constexpr bool TRIG = KIND == FAVOR_KERNEL_SOFTMAX_TRIG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
@@ -697,6 +731,10 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     if (POS) {
                         f0 = ex2(fmaf(__uint_as_float(p[32 * k + 2 * i]), a, -c));
                         f1 = ex2(fmaf(__uint_as_float(p[32 * k + 2 * i + 1]), a, -c));
+                    } else if (TRIG) {
+                        // groups 0, 1: sin of s p (rows 0..127); groups 2, 3: cos (the same rows repeated)
+                        f0 = sincos_reduced(s * __uint_as_float(p[32 * k + 2 * i]), grp >= 2);
+                        f1 = sincos_reduced(s * __uint_as_float(p[32 * k + 2 * i + 1]), grp >= 2);
                     } else {
                         f0 = fmaxf(__uint_as_float(p[32 * k + 2 * i]), 0.f);
                         f1 = fmaxf(__uint_as_float(p[32 * k + 2 * i + 1]), 0.f);
@@ -819,10 +857,12 @@ __device__ __forceinline__ uint32_t ca_slot(int role, int r3) {
 // Features of one query half, 32 projections at a time, packed in place into
 // the first 64 columns at taddr; returns sum_r f_r z~_r over the half's z~
 // (fp32 in shared memory at zaddr), taken over the bf16-rounded features.
+// Positive: exp2(a p - c); ReLU: max(p, 0); trigonometric: sin (half 0) or cos
+// (half 1, `cosine`) of a p, where the caller passes a = s.
 // The block loop stays rolled: the kernel's roles run different code at the
 // same time, and unrolled bodies overflow the instruction cache.
 template <int KIND>
-__device__ __noinline__ float query_half(uint32_t taddr, float a, float c, uint32_t zaddr) {
+__device__ __noinline__ float query_half(uint32_t taddr, float a, float c, uint32_t zaddr, bool cosine) {
     float d0 = 0.f, d1 = 0.f;
 #pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {
@@ -843,6 +883,9 @@ __device__ __noinline__ float query_half(uint32_t taddr, float a, float c, uint3
                 if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
                     f0 = ex2(fmaf(__uint_as_float(p[e]), a, -c));
                     f1 = ex2(fmaf(__uint_as_float(p[e + 1]), a, -c));
+                } else if (KIND == FAVOR_KERNEL_SOFTMAX_TRIG) {
+                    f0 = sincos_reduced(a * __uint_as_float(p[e]), cosine);
+                    f1 = sincos_reduced(a * __uint_as_float(p[e + 1]), cosine);
                 } else {
                     f0 = fmaxf(__uint_as_float(p[e]), 0.f);
                     f1 = fmaxf(__uint_as_float(p[e + 1]), 0.f);
@@ -898,10 +941,12 @@ __device__ __noinline__ float mask_row(uint32_t taddr, int row, int q) {
 // previous contents are no longer read) has completed the phase of parity
 // gate_par, stored into Phi_K [feature][token] (token block u of 64, 128-byte
 // swizzle).  Returns the sum of the features; *ok = false if the gate's wait
-// gave up (nothing stored).
+// gave up (nothing stored).  Trigonometric features: sin (or cos, `cosine`) of
+// a p times the token's h(s k_j) from cs, where the caller passes a = s.
 template <int KIND>
 __device__ __noinline__ float key_half_row(uint32_t taddr, uint64_t* release, uint64_t* gate, uint32_t gate_par,
-                                           int* err, bool* ok, uint32_t phi, uint32_t r, float a, uint32_t cs) {
+                                           int* err, bool* ok, uint32_t phi, uint32_t r, float a, bool cosine,
+                                           uint32_t cs) {
     uint32_t w[32];
     float z0 = 0.f, z1 = 0.f;
 #pragma unroll
@@ -917,7 +962,7 @@ __device__ __noinline__ float key_half_row(uint32_t taddr, uint64_t* release, ui
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
             float c8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS || KIND == FAVOR_KERNEL_SOFTMAX_TRIG) {
                 const uint32_t ca_addr = cs + 4 * (32 * blk + 8 * cc);
                 const uint4 ca = ld_shared_v4(ca_addr), cb = ld_shared_v4(ca_addr + 16);
                 c8[0] = __uint_as_float(ca.x); c8[1] = __uint_as_float(ca.y);
@@ -932,6 +977,9 @@ __device__ __noinline__ float key_half_row(uint32_t taddr, uint64_t* release, ui
                 if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
                     f0 = ex2(fmaf(x0, a, c8[2 * i]));
                     f1 = ex2(fmaf(x1, a, c8[2 * i + 1]));
+                } else if (KIND == FAVOR_KERNEL_SOFTMAX_TRIG) {
+                    f0 = sincos_reduced(a * x0, cosine) * c8[2 * i];
+                    f1 = sincos_reduced(a * x1, cosine) * c8[2 * i + 1];
                 } else {
                     f0 = fmaxf(x0, 0.f);
                     f1 = fmaxf(x1, 0.f);
@@ -1032,6 +1080,8 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ kshift, const float* __restrict__ wmax,
             const float* __restrict__ prefix, int H, int L, float s, Ranges R, int* err) {
     constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
+    constexpr bool TRIG = KIND == FAVOR_KERNEL_SOFTMAX_TRIG;
+    constexpr bool KOFF = POS || TRIG;   // per-key terms from the K tile: offsets, or h(s k_j)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1k(smem_raw);
     const uint32_t s_w = smem_u32(sm);
@@ -1051,6 +1101,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int n = g1 - g0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const float a = s * kLog2e;
+    const float fa = TRIG ? s : a;   // the feature functions' scale of the projection
     const bool multi_head = H > 1;
 
     if (threadIdx.x == 0) {
@@ -1058,7 +1109,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         // order and arrival counts follow the fields of CaBars
         // (each barrier completes once per chunk -- pk_full twice, at parities 0 and 1 --
         // so a parity wait cannot miss a phase)
-        const int counts[] = {1, 1, 1, 1, POS ? 9 : 1, POS ? 5 : 1, 1, 1,
+        const int counts[] = {1, 1, 1, 1, POS ? 9 : 1, KOFF ? 5 : 1, 1, 1,
                               1, 1, 4, 4, 1, 8, 4, 8,
                               1, 1, 4, 1, 8, 1, 1, 4,
                               8, 8, 1, 4, 1, 1};
@@ -1281,7 +1332,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (grpA) {
                 if (!mbar_wait(&bars->pq0_full, ph, err, 243)) break;
                 tc_fence_after();
-                const float dA = query_half<KIND>(tl + ca_slot(0, r3), a, c, zt);
+                const float dA = query_half<KIND>(tl + ca_slot(0, r3), fa, c, zt, false);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -1298,7 +1349,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             } else {
                 if (!mbar_wait(&bars->pq1_full, ph, err, 245)) break;
                 tc_fence_after();
-                const float dB = query_half<KIND>(tl + ca_slot(1, r3), a, c, zt + 4 * 128);
+                const float dB = query_half<KIND>(tl + ca_slot(1, r3), fa, c, zt + 4 * 128, true);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -1349,15 +1400,18 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const int g = g0 + t, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
             const int r3 = t % 3;
             const uint32_t Z = tl + ca_slot(2, r3);
-            // key offsets of this chunk (tokens 32q + lane), in cs[t & 1]
-            if (POS && u == 0) {
+            // key offsets of this chunk (tokens 32q + lane), in cs[t & 1]: exponent offsets
+            // (positive features) or the factors h(s k_j) (trigonometric)
+            if (KOFF && u == 0) {
                 if (!(ok = mbar_wait(&bars->k_full, ph, err, 251))) break;
                 if (h != kap_h) {
                     kap = __ldg(kshift + h);
                     kap_h = h;
                 }
                 const float nrm = row_sqnorm(s_k, r0);
-                cs[ph * kTile + r0] = (tok0 + (int)r0 < L) ? -(0.5f * s * s * nrm + kap) * kLog2e : -1.0e30f;
+                const bool live = tok0 + (int)r0 < L;
+                cs[ph * kTile + r0] = TRIG ? (live ? expf(0.5f * s * s * nrm) : 0.f)
+                                           : (live ? -(0.5f * s * s * nrm + kap) * kLog2e : -1.0e30f);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&bars->k_empty);
@@ -1392,13 +1446,13 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll 1
             for (int hp = 0; hp < 2; ++hp) {
                 if (!(ok = mbar_wait(&bars->pk_full, (uint32_t)hp, err, 255 + hp))) break;
-                if (hp == 0 && POS && !(ok = mbar_wait(&bars->cs_full, ph, err, 257))) break;
+                if (hp == 0 && KOFF && !(ok = mbar_wait(&bars->cs_full, ph, err, 257))) break;
                 tc_fence_after();
                 // half 0's projections go to registers first (then the slot may take half 1);
                 // stores into Phi_K wait until the state update of t-1 has read it
                 zc[hp] = key_half_row<KIND>(Z + 64 * (uint32_t)u, hp == 0 ? &bars->pk_free : nullptr,
                                             (hp == 0 && t > 0) ? &bars->phik_free : nullptr, ph ^ 1, err, &ok,
-                                            s_phi + (uint32_t)u * 2 * kPhiBlock, r0 + 128 * (uint32_t)hp, a,
+                                            s_phi + (uint32_t)u * 2 * kPhiBlock, r0 + 128 * (uint32_t)hp, fa, hp == 1,
                                             s_cs + (ph * kTile + 64 * (uint32_t)u) * 4);
                 if (!ok) break;
             }
@@ -1536,10 +1590,13 @@ void allow_all_once() {
     std::call_once(once, [] {
         allow_smem(k_tc_state<FAVOR_KERNEL_SOFTMAX_POS>, kSmemState);
         allow_smem(k_tc_state<FAVOR_KERNEL_RELU>, kSmemState);
+        allow_smem(k_tc_state<FAVOR_KERNEL_SOFTMAX_TRIG>, kSmemState);
         allow_smem(k_tc_readout<FAVOR_KERNEL_SOFTMAX_POS>, kSmemReadout);
         allow_smem(k_tc_readout<FAVOR_KERNEL_RELU>, kSmemReadout);
+        allow_smem(k_tc_readout<FAVOR_KERNEL_SOFTMAX_TRIG>, kSmemReadout);
         allow_smem(k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS>, kSmemCausal);
         allow_smem(k_tc_causal<FAVOR_KERNEL_RELU>, kSmemCausal);
+        allow_smem(k_tc_causal<FAVOR_KERNEL_SOFTMAX_TRIG>, kSmemCausal);
         allow_smem(k_tc_feature_map<FAVOR_KERNEL_SOFTMAX_POS>, kSmemFmap);
         allow_smem(k_tc_feature_map<FAVOR_KERNEL_RELU>, kSmemFmap);
         cudaGetLastError();
@@ -1554,6 +1611,9 @@ favor_status launch_state(const Handle& h, const CUtensorMap& mk, const CUtensor
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
         k_tc_state<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kStateThreads, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial,
                                                                                       h.H, L, h.s, R, h.dev_err);
+    else if (h.kind == FAVOR_KERNEL_SOFTMAX_TRIG)
+        k_tc_state<FAVOR_KERNEL_SOFTMAX_TRIG><<<R.G, kStateThreads, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial,
+                                                                                       h.H, L, h.s, R, h.dev_err);
     else
         k_tc_state<FAVOR_KERNEL_RELU><<<R.G, kStateThreads, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial, h.H,
                                                                                L, h.s, R, h.dev_err);
@@ -1571,11 +1631,13 @@ favor_status launch_wait_expiry(const Handle& h, long long limit, int code, cuda
 
 bool tc_supported(const Handle& h) {
     return h.dtype == FAVOR_DTYPE_BF16 && h.d == kD && h.dv == kDV && h.m == kM && h.cc_major >= 10 &&
-           h.kind != FAVOR_KERNEL_SOFTMAX_TRIG && encode_fn() != nullptr;
+           encode_fn() != nullptr;
 }
 
 favor_status tc_feature_map(const Handle& h, const void* x, void* phi, int B, int L, cudaStream_t st) {
-    if (!aligned16(x) || !aligned16(phi)) return simt_feature_map(h, x, phi, B, L, st);
+    // the plain trigonometric map (with h(x)) stays on the CUDA cores
+    if (!aligned16(x) || !aligned16(phi) || h.kind == FAVOR_KERNEL_SOFTMAX_TRIG)
+        return simt_feature_map(h, x, phi, B, L, st);
     allow_all_once();
     const int BH = B * h.H;
     CUtensorMap mx, mw;
@@ -1620,6 +1682,9 @@ favor_status tc_bidir(const Handle& h, const void* q, const void* k, const void*
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
         k_tc_readout<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kReadoutThreads, kSmemReadout, st>>>(
             mq, mw, mo, (const uint8_t*)h.ws_tc, h.H, L, h.s, R, h.dev_err);
+    else if (h.kind == FAVOR_KERNEL_SOFTMAX_TRIG)
+        k_tc_readout<FAVOR_KERNEL_SOFTMAX_TRIG><<<R.G, kReadoutThreads, kSmemReadout, st>>>(
+            mq, mw, mo, (const uint8_t*)h.ws_tc, h.H, L, h.s, R, h.dev_err);
     else
         k_tc_readout<FAVOR_KERNEL_RELU><<<R.G, kReadoutThreads, kSmemReadout, st>>>(
             mq, mw, mo, (const uint8_t*)h.ws_tc, h.H, L, h.s, R, h.dev_err);
@@ -1657,6 +1722,9 @@ favor_status tc_causal(const Handle& h, const void* q, const void* k, const void
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
         k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kCausalThreads, kSmemCausal, st>>>(
             mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, h.H, L, h.s, R, h.dev_err);
+    else if (h.kind == FAVOR_KERNEL_SOFTMAX_TRIG)
+        k_tc_causal<FAVOR_KERNEL_SOFTMAX_TRIG><<<R.G, kCausalThreads, kSmemCausal, st>>>(
+            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, h.H, L, h.s, R, h.dev_err);
     else
         k_tc_causal<FAVOR_KERNEL_RELU><<<R.G, kCausalThreads, kSmemCausal, st>>>(
             mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, h.H, L, h.s, R, h.dev_err);
@@ -1674,8 +1742,10 @@ favor_status tc_kv_state(const Handle& h, const void* k, const void* v, float* s
         return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     favor_status s = launch_state(h, mk, mv, mw, BH, L, R, st);
     if (s != FAVOR_OK) return s;
-    // the state kernel leaves out m^-1/2, and its ReLU features are of k, not s*k
-    const float scale = (h.kind == FAVOR_KERNEL_RELU ? h.s : 1.f) / sqrtf((float)kM);
+    // the state kernel leaves out m^-1/2 (trigonometric: (m/2)^-1/2), and its ReLU
+    // features are of k, not s*k
+    const float scale = (h.kind == FAVOR_KERNEL_RELU ? h.s : 1.f) /
+                        sqrtf((float)(h.kind == FAVOR_KERNEL_SOFTMAX_TRIG ? kM / 2 : kM));
     dim3 grid((kM * (kDV + 1) + 255) / 256, BH);
     ProfScope ps(h, PROF_COMBINE, st);
     k_accum_cols<<<grid, 256, 0, st>>>(h.ws_partial, state, R, scale);
@@ -1703,6 +1773,9 @@ favor_status tc_attn_from_state(const Handle& h, const void* q, const float* sta
     ProfScope ps(h, PROF_READOUT, st);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
         k_tc_readout<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kReadoutThreads, kSmemReadout, st>>>(
+            mq, mw, mo, (const uint8_t*)h.ws_tc, h.H, L, h.s, R, h.dev_err);
+    else if (h.kind == FAVOR_KERNEL_SOFTMAX_TRIG)
+        k_tc_readout<FAVOR_KERNEL_SOFTMAX_TRIG><<<R.G, kReadoutThreads, kSmemReadout, st>>>(
             mq, mw, mo, (const uint8_t*)h.ws_tc, h.H, L, h.s, R, h.dev_err);
     else
         k_tc_readout<FAVOR_KERNEL_RELU><<<R.G, kReadoutThreads, kSmemReadout, st>>>(

@@ -28,6 +28,19 @@ constexpr uint32_t kPhiBlock = kTile * 128;       // one 64-column image of a 12
 constexpr uint32_t kSBytes = kM * 128;            // S~ image [256 rows][64] = 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
 
+// sin(x) (cosine = false) or cos(x) for the trigonometric features: x is first
+// reduced to [-pi, pi] by Cody and Waite's method (x - n 2pi with 2pi split in
+// two parts, the leading one 201/32, so that n times it is exact for |n| < 2^15),
+// then the hardware approximation, accurate on that interval, is taken.
+__device__ __forceinline__ float sincos_reduced(float x, bool cosine) {
+    constexpr float kInvTwoPi = 0.15915494309189535f;
+    constexpr float kTwoPiHi = 6.28125f;
+    constexpr float kTwoPiLo = 1.9353071795864769e-3f;   // 2pi - kTwoPiHi
+    const float n = rintf(x * kInvTwoPi);
+    const float r = fmaf(-n, kTwoPiLo, fmaf(-n, kTwoPiHi, x));
+    return cosine ? __cosf(r) : __sinf(r);
+}
+
 // byte offset of chunk `c` (16 B) of row `r` inside an SW128 image
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
 
