@@ -92,8 +92,10 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
 // (releasing it at once for the next tile's projection), accumulate z_r in
 // registers, and write the features packed (bf16) to Phi0 / Phi1, the A
 // operand (tensor memory) of S_half += Phi^T_half V.  Trigonometric features
-// (rows [omega; omega]) take sin of s D in half 0 and cos in half 1, times the
-// token's h(s k_j) = exp(s^2 ||k_j||^2 / 2), which the norm warp writes per stage.
+// (rows [omega; omega]): only P0 is projected (the rows repeat), and the two
+// warps of a lane quarter split its tokens, each writing sin of s D into Phi0
+// and cos into Phi1 from one range reduction, times the token's
+// h(s k_j) = exp(s^2 ||k_j||^2 / 2), which the norm warp writes per stage.
 //   tensor memory: P0 [0,128) P1 [128,256) Phi0 [256,320) Phi1 [320,384) S0 [384,448) S1 [448,512)
 //   warp 0: TMA producer   warp 1: projection MMAs   warp 2: state MMAs
 //   warp 3: key norms -> offsets (positive features) or h(s k_j) (trigonometric)
@@ -149,10 +151,11 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         }
         mbar_init(&bars->w_full, 1);
         mbar_init(&bars->w_empty, 1);
+        // trigonometric: all eight feature warps read P0 and write both Phi halves
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->p_full[i], 1);
-            mbar_init(&bars->p_empty[i], 4);
-            mbar_init(&bars->phi_full[i], 4);
+            mbar_init(&bars->p_empty[i], TRIG ? 8 : 4);
+            mbar_init(&bars->phi_full[i], TRIG ? 8 : 4);
             mbar_init(&bars->phi_empty[i], 1);
         }
         mbar_init(&bars->acc_full, 1);
@@ -217,7 +220,7 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
                 if (!mbar_wait(&bars->kv_full[st], (i / kNS) & 1, err, 112)) break;
                 if (POS && !mbar_wait(&bars->ext_full[st], (i / kNS) & 1, err, 113)) break;
                 bool ok = true;
-                for (int hp = 0; hp < 2; ++hp) {
+                for (int hp = 0; hp < (TRIG ? 1 : 2); ++hp) {   // trigonometric: rows 128.. repeat 0..127
                     if (i > 0 && !mbar_wait(&bars->p_empty[hp], (i - 1) & 1, err, 114 + hp)) {
                         ok = false;
                         break;
@@ -328,10 +331,92 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         const uint32_t tp = tmem + lane_off + 128 * hp;           // projection slot
         const uint32_t tf = tmem + lane_off + 256 + 64 * hp;      // packed features
         int piece = 0;
-        float z0 = 0.f, z1 = 0.f;
+        float z0 = 0.f, z1 = 0.f, zc0 = 0.f, zc1 = 0.f;   // zc: cos sums (trigonometric)
         for (int i = 0; i < n; ++i) {
             const int g = g0 + i, bh = g / R.tph;
             const bool last = (i == n - 1) || ((g + 1) / R.tph) != bh;
+            if (TRIG) {
+                // P0 holds the 128 distinct projections; warp (q, h) takes tokens [64h, 64h+64)
+                // and writes sin into Phi0 and cos into Phi1 (one range reduction per pair),
+                // times the token's h(s k_j)
+                if (!mbar_wait(&bars->p_full[0], i & 1, err, 121)) break;
+                tc_fence_after();
+                uint32_t p[64];
+                tmem_ld64(tmem + lane_off + 64 * hp, p);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->p_empty[0]);
+                const int st = i % kNS;
+                if (!mbar_wait(&bars->ext_full[st], (i / kNS) & 1, err, 122)) break;
+                const float4* hk = reinterpret_cast<const float4*>(sm + (s_ext - s_w) + st * kExtStage) + 16 * hp;
+                uint32_t ws[32], wc[32];
+#pragma unroll
+                for (int k4 = 0; k4 < 16; ++k4) {
+                    const float4 h4 = hk[k4];
+                    const float hh[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k2 = 2 * k4 + e;
+                        float s0, c0, s1, c1;
+                        sincos_pair(s * __uint_as_float(p[2 * k2]), s0, c0);
+                        sincos_pair(s * __uint_as_float(p[2 * k2 + 1]), s1, c1);
+                        s0 *= hh[2 * e];
+                        c0 *= hh[2 * e];
+                        s1 *= hh[2 * e + 1];
+                        c1 *= hh[2 * e + 1];
+                        z0 += s0;
+                        z1 += s1;
+                        zc0 += c0;
+                        zc1 += c1;
+                        ws[k2] = pack_bf16(s0, s1);
+                        wc[k2] = pack_bf16(c0, c1);
+                    }
+                }
+                if (i > 0 && !(mbar_wait(&bars->phi_empty[0], (i - 1) & 1, err, 123) &&
+                               mbar_wait(&bars->phi_empty[1], (i - 1) & 1, err, 123)))
+                    break;
+                tc_fence_after();
+                const uint32_t t0 = tmem + lane_off + 256 + 32 * hp, t1 = t0 + 64;
+                tmem_st16(t0, *reinterpret_cast<uint32_t(*)[16]>(&ws[0]));
+                tmem_st16(t0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&ws[16]));
+                tmem_st16(t1, *reinterpret_cast<uint32_t(*)[16]>(&wc[0]));
+                tmem_st16(t1 + 16, *reinterpret_cast<uint32_t(*)[16]>(&wc[16]));
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars->phi_full[0]);
+                    mbar_arrive(&bars->phi_full[1]);
+                }
+                if (last) {
+                    if (!mbar_wait(&bars->acc_full, piece & 1, err, 124)) break;
+                    tc_fence_after();
+                    uint32_t sv[64];
+                    tmem_ld64(tmem + lane_off + 384 + 64 * hp, sv);
+                    tmem_ld_wait();
+                    // z of this warp's feature row (sin row r for h = 0, cos row 128 + r for
+                    // h = 1): its own token half plus the partner warp's, handed over in the
+                    // omega-side extra block (unused by this kind)
+                    float* zx = reinterpret_cast<float*>(sm + (s_wext - s_w));
+                    const uint32_t r = 32 * q + lane;
+                    if (hp == 0) zx[128 + r] = zc0 + zc1;
+                    else zx[r] = z0 + z1;
+                    asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight feature warps
+                    const float zt = hp == 0 ? (z0 + z1) + zx[r] : (zc0 + zc1) + zx[128 + r];
+                    const int pc = c - first_cta(R, bh);
+                    float* o = part + ((size_t)bh * R.pstride + pc) * (kM * (kDV + 1)) + (128 * hp + r);
+#pragma unroll
+                    for (int k2 = 0; k2 < 64; ++k2) o[(size_t)k2 * kM] = __uint_as_float(sv[k2]);
+                    o[(size_t)64 * kM] = zt;
+                    z0 = z1 = zc0 = zc1 = 0.f;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->acc_empty);
+                    ++piece;
+                }
+                continue;
+            }
             if (!mbar_wait(&bars->p_full[hp], i & 1, err, 121)) break;
             tc_fence_after();
             uint32_t p[128];
@@ -352,26 +437,7 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             // features into registers first: the exps overlap the previous tile's
             // state MMAs, which still read this warp's Phi region
             uint32_t w[64];
-            if (TRIG) {
-                // sin (half 0) or cos (half 1) of s p, times h(s k_j) of the token
-                const int st = i % kNS;
-                if (!mbar_wait(&bars->ext_full[st], (i / kNS) & 1, err, 122)) break;
-                const float4* hk = reinterpret_cast<const float4*>(sm + (s_ext - s_w) + st * kExtStage);
-#pragma unroll
-                for (int k4 = 0; k4 < 32; ++k4) {
-                    const float4 h4 = hk[k4];
-                    const float hh[4] = {h4.x, h4.y, h4.z, h4.w};
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int k2 = 2 * k4 + e;
-                        const float f0 = sincos_reduced(s * __uint_as_float(p[2 * k2]), hp == 1) * hh[2 * e];
-                        const float f1 = sincos_reduced(s * __uint_as_float(p[2 * k2 + 1]), hp == 1) * hh[2 * e + 1];
-                        z0 += f0;
-                        z1 += f1;
-                        w[k2] = pack_bf16(f0, f1);
-                    }
-                }
-            } else {
+            {
 #pragma unroll
                 for (int k2 = 0; k2 < 64; ++k2) {
                     const float x0 = __uint_as_float(p[2 * k2]), x1 = __uint_as_float(p[2 * k2 + 1]);
@@ -525,8 +591,9 @@ __global__ void k_pack_state(const float* __restrict__ state, uint8_t* __restric
 // to another head.  Per 128-query tile t (tensor-memory slot t mod 2, 256 columns):
 //   P = Q omega^T (N = 256)                     -> slot [0,256)
 //   Phi_Q = exp2(a P - a max_r P) packed bf16   -> [0,64) (features 0..127), [192,256) (128..255)
-//           (ReLU: max(P, 0); trigonometric, rows [omega; omega]: sin / cos of s P,
-//           without h(x), a factor of the row that cancels in num / den)
+//           (ReLU: max(P, 0); trigonometric, rows [omega; omega]: P of the first 128
+//           rows only, then sin and cos of s P from one range reduction, without
+//           h(x), a factor of the row that cancels in num / den)
 //   [num | den] = Phi_Q [S~ | z~] (N = 80)      -> [64,144)
 //   out = num / den, staged in shared memory and written by one TMA store
 // (Eq. 4 of Rethinking Attention with Performers).  The feature and output
@@ -650,7 +717,8 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 if (!mbar_wait(&bars->q_full[u % kRStages], (u / kRStages) & 1, err, 312)) break;
                 if (u >= 2 && !mbar_wait(&bars->slot_free[u & 1], ((u >> 1) - 1) & 1, err, 313)) break;
                 tc_fence_after();
-                issue_projection(sl, s_q + (u % kRStages) * kTileBytes, s_w, 256);
+                // trigonometric: the rows repeat after 128, so project the first 128 only
+                issue_projection(sl, s_q + (u % kRStages) * kTileBytes, s_w, TRIG ? 128 : 256);
                 mma_commit(&bars->pq_full[u & 1]);
                 mma_commit(&bars->q_empty[u % kRStages]);
                 if (seg_end) mma_commit(&bars->w_empty);
@@ -693,6 +761,34 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint32_t sl = tl + 256u * (uint32_t)(u & 1);
             if (!mbar_wait(&bars->pq_full[u & 1], (u >> 1) & 1, err, 321)) return false;
             tc_fence_after();
+            if (TRIG) {
+                // group g: projections [32g, 32g+32) -> sin features [32g, ..) packed in
+                // [16g, 16g+16), cos features [128 + 32g, ..) packed in [192 + 16g, ..)
+                uint32_t p[32];
+                tmem_ld32(sl + 32u * (uint32_t)grp, p);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->mxb);   // every group's projections are in registers
+                if (!mbar_wait(&bars->mxb, u & 1, err, 322)) return false;
+                tc_fence_after();
+                uint32_t ws[16], wc[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float s0, c0, s1, c1;
+                    sincos_pair(s * __uint_as_float(p[2 * i]), s0, c0);
+                    sincos_pair(s * __uint_as_float(p[2 * i + 1]), s1, c1);
+                    ws[i] = pack_bf16(s0, s1);
+                    wc[i] = pack_bf16(c0, c1);
+                }
+                tmem_st16(sl + 16u * (uint32_t)grp, ws);
+                tmem_st16(sl + 192u + 16u * (uint32_t)grp, wc);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->phiq_full[u & 1]);
+                return true;
+            }
             uint32_t p[64];
             tmem_ld64(sl + 64u * (uint32_t)grp, p);
             tmem_ld_wait();
@@ -731,10 +827,6 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     if (POS) {
                         f0 = ex2(fmaf(__uint_as_float(p[32 * k + 2 * i]), a, -c));
                         f1 = ex2(fmaf(__uint_as_float(p[32 * k + 2 * i + 1]), a, -c));
-                    } else if (TRIG) {
-                        // groups 0, 1: sin of s p (rows 0..127); groups 2, 3: cos (the same rows repeated)
-                        f0 = sincos_reduced(s * __uint_as_float(p[32 * k + 2 * i]), grp >= 2);
-                        f1 = sincos_reduced(s * __uint_as_float(p[32 * k + 2 * i + 1]), grp >= 2);
                     } else {
                         f0 = fmaxf(__uint_as_float(p[32 * k + 2 * i]), 0.f);
                         f1 = fmaxf(__uint_as_float(p[32 * k + 2 * i + 1]), 0.f);

@@ -41,6 +41,17 @@ __device__ __forceinline__ float sincos_reduced(float x, bool cosine) {
     return cosine ? __cosf(r) : __sinf(r);
 }
 
+// sin(x) and cos(x) from one reduction (as sincos_reduced).
+__device__ __forceinline__ void sincos_pair(float x, float& sn, float& cs) {
+    constexpr float kInvTwoPi = 0.15915494309189535f;
+    constexpr float kTwoPiHi = 6.28125f;
+    constexpr float kTwoPiLo = 1.9353071795864769e-3f;
+    const float n = rintf(x * kInvTwoPi);
+    const float r = fmaf(-n, kTwoPiLo, fmaf(-n, kTwoPiHi, x));
+    sn = __sinf(r);
+    cs = __cosf(r);
+}
+
 // byte offset of chunk `c` (16 B) of row `r` inside an SW128 image
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
 
