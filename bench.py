@@ -557,8 +557,8 @@ def run_ours(args):
                 "kernels": bk}
 
     # Feature variants and relative positions on the same workload, one line each:
-    # hyperbolic and trigonometric features (tensor cores), RFA-Gate gated causal
-    # and PermuteFormer (CUDA cores).  Roofline: the forward's flops per
+    # hyperbolic and trigonometric features and RFA-Gate gated causal (tensor
+    # cores), PermuteFormer (CUDA cores).  Roofline: the forward's flops per
     # token*head (4md + 4m(dv+1)) against the tensor peak (tensor-core calls) or
     # the FP32 FFMA peak (CUDA-core calls).
     variants = None
@@ -597,8 +597,7 @@ def run_ours(args):
                 c1.record(stream)
                 torch.cuda.synchronize(dev)
                 ms = c0.elapsed_time(c1) / args.variant_steps
-                tc = (kind in ("softmax_hyp", "softmax_trig") and extra is None and w.dtype == "bf16"
-                      and (w.d, w.dv, w.m) == (64, 64, 256))
+                tc = (extra != "relpos" and w.dtype == "bf16" and (w.d, w.dv, w.m) == (64, 64, 256))
                 pk = peaks["bf16_tflops_sustained"] * 1e12 if tc else fp32_peak
                 res[mode] = {"ms": ms, "value": T / (ms / 1e3), "unit": UNIT,
                              "path": "tensor cores" if tc else "CUDA cores",

@@ -202,9 +202,13 @@ FAVOR_API favor_status favor_attn_causal_step(favor_handle h, const void* q, con
  *     out_t = phi(q_t)^T S_t / phi(q_t)^T z_t                (0 where the denominator is 0)
  *   gate   DEVICE float array [B,H,L] (fp32 whatever the dtype), caller-owned,
  *          read only; values outside [0, 1] are not checked.
- * Other arguments as favor_attn_causal.  Runs on the CUDA cores (chunked: the
- * segments' states are combined with the products of their gates).  Not
- * combined with favor_set_relpos (FAVOR_ERR_UNSUPPORTED while it is set).
+ * Other arguments as favor_attn_causal.  Chunked: the ranges' states are
+ * combined with the products of their gates.  Positive and ReLU features of
+ * the bf16 d = dv = 64, m = 256 shape run on the tensor cores (each chunk's
+ * gates scanned in log2, clamped below at 2^-126, the within-chunk decay
+ * applied per element of the masked product); every other case on the CUDA
+ * cores.  The gate pointer must stay valid until the call's work on the stream
+ * is done.  Not combined with favor_set_relpos (FAVOR_ERR_UNSUPPORTED while it is set).
  *
  * favor_attn_causal_step_gated -- favor_attn_causal_step with the same gated
  * update; gate [B,H,T].

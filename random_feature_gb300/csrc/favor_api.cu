@@ -366,6 +366,8 @@ favor_status favor_attn_causal_gated(favor_handle hd, const void* q, const void*
         return set_error(FAVOR_ERR_INVALID_ARG, "favor_attn_causal_gated: null pointer");
     const Handle& h = *reinterpret_cast<const Handle*>(hd);
     if (relpos_on(h)) return set_error(FAVOR_ERR_UNSUPPORTED, "favor_attn_causal_gated: relative positions are set");
+    if (tc_supported(h) && (h.kind == FAVOR_KERNEL_SOFTMAX_POS || h.kind == FAVOR_KERNEL_RELU))
+        return tc_causal_gated(h, q, k, v, gate, out, B, L, reinterpret_cast<cudaStream_t>(stream));
     return simt_causal(h, q, k, v, out, B, L, reinterpret_cast<cudaStream_t>(stream), gate);
 }
 

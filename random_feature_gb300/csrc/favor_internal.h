@@ -173,6 +173,9 @@ favor_status tc_bidir(const Handle& h, const void* q, const void* k, const void*
                       int B, int L, cudaStream_t st);
 favor_status tc_causal(const Handle& h, const void* q, const void* k, const void* v, void* out,
                        int B, int L, cudaStream_t st);
+// RFA-Gate causal call on the tensor cores (positive and ReLU kinds; gate [B*H, L] fp32).
+favor_status tc_causal_gated(const Handle& h, const void* q, const void* k, const void* v, const float* gate,
+                             void* out, int B, int L, cudaStream_t st);
 // Tensor-core bidirectional backward (falls back to the CUDA-core one for unaligned pointers).
 favor_status tc_bidir_backward(const Handle& h, const void* q, const void* k, const void* v, const void* dout,
                                void* dq, void* dk, void* dv, int B, int L, cudaStream_t st);

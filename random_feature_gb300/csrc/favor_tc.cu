@@ -119,14 +119,15 @@ struct StBars {
     uint64_t p_full[2], p_empty[2];
     uint64_t phi_full[2], phi_empty[2];
     uint64_t acc_full, acc_empty;
+    uint64_t zx;   // trigonometric: the feature warps' z hand-over at a piece end
     uint32_t tmem_base;
 };
 
-template <int KIND>
+template <int KIND, bool GATED = false>
 __global__ void __launch_bounds__(kStateThreads, 1)
 k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-           const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ kshift, float* __restrict__ part,
-           int H, int L, float s, Ranges R, int* err) {
+           const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ kshift, const float* __restrict__ wlog,
+           float* __restrict__ part, int H, int L, float s, Ranges R, int* err) {
     constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
     constexpr bool TRIG = KIND == FAVOR_KERNEL_SOFTMAX_TRIG;
     extern __shared__ uint8_t smem_raw[];
@@ -160,6 +161,7 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         }
         mbar_init(&bars->acc_full, 1);
         mbar_init(&bars->acc_empty, 8);
+        mbar_init(&bars->zx, 8);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -289,10 +291,10 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         // kappa_h) log2(e) (a huge negative value past L), written as bf16 hi + lo
         // into the stage's K-side extra block; trigonometric features: the factor
         // h(s k_j) as fp32 in the same block, for the feature warps.  Four tokens per lane.
-        if (POS || TRIG) {
+        if (POS || TRIG || GATED) {
             int kap_h = -1;
             float kap = 0.f;
-            const float inv_s = 1.f / s;
+            const float inv_s = 1.f / s, inv_a = 1.f / a;
             for (int i = 0; i < n; ++i) {
                 const int g = g0 + i, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
                 const int st = i % kNS;
@@ -301,18 +303,29 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
                     kap_h = h;
                 }
                 if (!mbar_wait(&bars->kv_full[st], (i / kNS) & 1, err, 131)) break;
-                float nrm[4];
-                row_sqnorm2(s_kv + 2 * st * kTileBytes, (uint32_t)lane, (uint32_t)(lane + 32), nrm[0], nrm[1]);
-                row_sqnorm2(s_kv + 2 * st * kTileBytes, (uint32_t)(lane + 64), (uint32_t)(lane + 96), nrm[2], nrm[3]);
+                float nrm[4] = {0.f, 0.f, 0.f, 0.f};
+                if (POS || TRIG) {
+                    row_sqnorm2(s_kv + 2 * st * kTileBytes, (uint32_t)lane, (uint32_t)(lane + 32), nrm[0], nrm[1]);
+                    row_sqnorm2(s_kv + 2 * st * kTileBytes, (uint32_t)(lane + 64), (uint32_t)(lane + 96), nrm[2], nrm[3]);
+                }
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const uint32_t j = (uint32_t)(lane + 32 * t);
-                    if (TRIG) {
+                    // gated calls: the key's log2 weight toward its piece's end
+                    const float wl = (GATED && tok0 + (int)j < L) ? __ldg(wlog + (size_t)bh * L + tok0 + j) : 0.f;
+                    if (GATED && !POS) {
+                        // ReLU: the weight itself, a column factor for the feature warps
+                        const float wk = (tok0 + (int)j < L && wl > -1.0e29f) ? exp2f(wl) : 0.f;
+                        reinterpret_cast<float*>(sm + (s_ext - s_w) + st * kExtStage)[j] = wk;
+                    } else if (TRIG) {
                         // h(s k_j) = exp(s^2 ||k_j||^2 / 2), 0 past L, one fp32 per token
                         const float hk = (tok0 + (int)j < L) ? expf(0.5f * s * s * nrm[t]) : 0.f;
                         reinterpret_cast<float*>(sm + (s_ext - s_w) + st * kExtStage)[j] = hk;
                     } else {
-                        const float x = (tok0 + (int)j < L) ? -(0.5f * s * nrm[t] + kap * inv_s) : -1.0e30f;
+                        // positive: the weight enters the exponent offset (x in projection units, f = 2^(a D))
+                        const float x = (tok0 + (int)j < L && wl > -1.0e29f)
+                                            ? -(0.5f * s * nrm[t] + kap * inv_s) + wl * inv_a
+                                            : -1.0e30f;
                         const float hi = __bfloat162float(__float2bfloat16_rn(x));
                         const float lo = x - hi;
                         st_shared_v4(s_ext + st * kExtStage + ext_row(j), pack_bf16(hi, lo), 0u, 0u, 0u);
@@ -402,7 +415,9 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
                     const uint32_t r = 32 * q + lane;
                     if (hp == 0) zx[128 + r] = zc0 + zc1;
                     else zx[r] = z0 + z1;
-                    asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight feature warps
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->zx);   // release: the warp's writes above
+                    if (!mbar_wait(&bars->zx, piece & 1, err, 125)) break;
                     const float zt = hp == 0 ? (z0 + z1) + zx[r] : (zc0 + zc1) + zx[128 + r];
                     const int pc = c - first_cta(R, bh);
                     float* o = part + ((size_t)bh * R.pstride + pc) * (kM * (kDV + 1)) + (128 * hp + r);
@@ -437,7 +452,26 @@ k_tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
             // features into registers first: the exps overlap the previous tile's
             // state MMAs, which still read this warp's Phi region
             uint32_t w[64];
-            {
+            if (GATED && !POS) {
+                // ReLU, gated: max(p, 0) times the key's weight toward its piece's end
+                const int st = i % kNS;
+                if (!mbar_wait(&bars->ext_full[st], (i / kNS) & 1, err, 122)) break;
+                const float4* wk = reinterpret_cast<const float4*>(sm + (s_ext - s_w) + st * kExtStage);
+#pragma unroll
+                for (int k4 = 0; k4 < 32; ++k4) {
+                    const float4 w4 = wk[k4];
+                    const float ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k2 = 2 * k4 + e;
+                        const float f0 = fmaxf(__uint_as_float(p[2 * k2]), 0.f) * ww[2 * e];
+                        const float f1 = fmaxf(__uint_as_float(p[2 * k2 + 1]), 0.f) * ww[2 * e + 1];
+                        z0 += f0;
+                        z1 += f1;
+                        w[k2] = pack_bf16(f0, f1);
+                    }
+                }
+            } else {
 #pragma unroll
                 for (int k2 = 0; k2 < 64; ++k2) {
                     const float x0 = __uint_as_float(p[2 * k2]), x1 = __uint_as_float(p[2 * k2 + 1]);
@@ -549,6 +583,70 @@ __global__ void k_scan_pieces(float* __restrict__ part, Ranges R) {
                 run.w += v[u].w;
             }
     }
+}
+
+// Gated causal calls (RFA-Gate): decayed prefix of pieces.  Piece j of head
+// bh <- prefix_j, prefix_0 = 0, prefix_{j+1} = d_j prefix_j + piece_j, with d_j
+// the product of piece j's gates (the pieces hold their keys weighted toward
+// their own end).  One thread per element.
+__global__ void k_scan_pieces_decay(float* __restrict__ part, const float* __restrict__ pdecay, Ranges R) {
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    constexpr int n = kM * (kDV + 1);
+    if (i >= n) return;
+    const int np = last_cta(R, bh) - first_cta(R, bh) + 1;
+    float* p = part + (size_t)bh * R.pstride * n + i;
+    const float* d = pdecay + (size_t)bh * R.pstride;
+    float run = 0.f;
+    for (int j = 0; j < np; ++j) {
+        const float v = p[(size_t)j * n];
+        p[(size_t)j * n] = run;
+        run = fmaf(run, d[j], v);
+    }
+}
+
+// Gated causal calls: per token of a piece (the ranges of the state kernel cut
+// at head boundaries), the log2 weight of its key toward the piece's end,
+//   wlog_j = sum_{l in (j, end]} log2 g_l + log2(1 - g_j)   (-1e30 where 1 - g_j = 0 or past L),
+// and per piece the product of its gates (pdecay, indexed like the piece
+// states).  Gates are clamped below at 2^-126, so a zero gate ends the history
+// without turning any sum into -inf.  grid R.G (one block per range), 128 threads.
+__global__ void __launch_bounds__(128) k_gate_weights(const float* __restrict__ gate, float* __restrict__ wlog,
+                                                      float* __restrict__ pdecay, int L, Ranges R) {
+    __shared__ float wsum[4];
+    const int cta = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
+    float run = 0.f;   // log2 of the product of the piece's gates after the current tile
+    int cur_bh = -1;
+    for (int g = g1 - 1; g >= g0; --g) {   // backwards: each piece from its end
+        const int bh = g / R.tph, tok = (g % R.tph) * kTile + tid;
+        if (bh != cur_bh) {
+            if (cur_bh >= 0 && tid == 0) pdecay[(size_t)cur_bh * R.pstride + (cta - first_cta(R, cur_bh))] = exp2f(run);
+            run = 0.f;
+            cur_bh = bh;
+        }
+        const bool live = tok < L;
+        const float gv = live ? gate[(size_t)bh * L + tok] : 1.f;
+        const float lg = log2f(fmaxf(gv, 1.17549435e-38f));
+        float sfx = lg;   // sum over tokens tid..(end of the warp)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_down_sync(0xffffffffu, sfx, o);
+            if (lane + o < 32) sfx += t;
+        }
+        if (lane == 0) wsum[warp] = sfx;
+        __syncthreads();
+        float later = 0.f;
+        for (int w = warp + 1; w < 4; ++w) later += wsum[w];
+        const float tile_sum = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]);
+        __syncthreads();
+        if (live) {
+            const float one_m = 1.f - gv;
+            wlog[(size_t)bh * L + tok] = one_m > 0.f ? (sfx + later - lg + run) + log2f(one_m) : -1.0e30f;
+        }
+        run += tile_sum;
+    }
+    if (cur_bh >= 0 && tid == 0) pdecay[(size_t)cur_bh * R.pstride + (cta - first_cta(R, cur_bh))] = exp2f(run);
 }
 
 // ============================================================ stateful calls
@@ -936,6 +1034,7 @@ struct CaBars {
     uint64_t pq0_full, pq1_full, phiq0_full, phiq1_full, pk_full, pk_free, cs_full, phik_full;
     uint64_t phik_free, a_full, am_full, s_full, st_full, ai_done, o_full, o_empty;
     uint64_t z_full, zx_full, mma_done, stage_full, stage_free[2];
+    uint64_t g_full[2], phiq_scaled, phik_w;   // gated calls only
     uint32_t tmem_base;
 };
 
@@ -1091,6 +1190,104 @@ __device__ __noinline__ float key_half_row(uint32_t taddr, uint64_t* release, ui
     return z0 + z1;
 }
 
+// Gated calls: packed bf16 feature row (64 columns at taddr) times f, in place.
+__device__ __noinline__ void scale_packed_row(uint32_t taddr, float f) {
+#pragma unroll 1
+    for (int blk = 0; blk < 2; ++blk) {
+        uint32_t w[32];
+        tmem_ld32(taddr + 32 * blk, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = pack_bf16(bf16lo(w[i]) * f, bf16hi(w[i]) * f);
+        tmem_st16(taddr + 32 * blk, *reinterpret_cast<uint32_t(*)[16]>(&w[0]));
+        tmem_st16(taddr + 32 * blk + 16, *reinterpret_cast<uint32_t(*)[16]>(&w[16]));
+    }
+}
+
+// Gated calls: the causal mask of one row of A with the decay of the gates,
+// A_ij 2^(C_i - T_j) for j <= i (C_i the row's cumulative log2 gate, T_j =
+// C_j - log2(1 - g_j) at tcol, fp32 in shared memory), packed in place into
+// [0,64); returns the row sum of the kept bf16-rounded values.
+__device__ __noinline__ float mask_row_gated(uint32_t taddr, int row, int q, float ci, uint32_t tcol) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t w[16];
+        if (blk <= q) {
+            uint32_t p[32];
+            tmem_ld32(taddr + 32 * blk, p);
+            tmem_ld_wait();
+            const int lim = row - 32 * blk;
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const uint4 t4 = ld_shared_v4(tcol + 4 * (32 * blk + 4 * j4));
+                const float tt[4] = {__uint_as_float(t4.x), __uint_as_float(t4.y), __uint_as_float(t4.z),
+                                     __uint_as_float(t4.w)};
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int i = 2 * j4 + e;
+                    const float f0 = (2 * i <= lim) ? __uint_as_float(p[2 * i]) * ex2(ci - tt[2 * e]) : 0.f;
+                    const float f1 = (2 * i + 1 <= lim) ? __uint_as_float(p[2 * i + 1]) * ex2(ci - tt[2 * e + 1]) : 0.f;
+                    w[i] = pack_bf16(f0, f1);
+                    s0 += bf16lo(w[i]);
+                    s1 += bf16hi(w[i]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = 0u;
+        }
+        tmem_st16(taddr + 16 * blk, w);
+    }
+    return s0 + s1;
+}
+
+// Gated calls: the S~ image row r from the fp32 state row (64 columns at
+// taddr), then the state row times the chunk's decay d, written back.
+__device__ __noinline__ void refresh_decay_row(uint32_t taddr, uint32_t img, uint32_t r, float d) {
+#pragma unroll 1
+    for (int blk = 0; blk < 2; ++blk) {
+        uint32_t sv[32];
+        tmem_ld32(taddr + 32 * blk, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (uint32_t c = 0; c < 4; ++c)
+            st_shared_v4(img + sw128(r, 4 * blk + c),
+                         pack_bf16(__uint_as_float(sv[8 * c]), __uint_as_float(sv[8 * c + 1])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 2]), __uint_as_float(sv[8 * c + 3])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 4]), __uint_as_float(sv[8 * c + 5])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 6]), __uint_as_float(sv[8 * c + 7])));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[i] = __float_as_uint(__uint_as_float(sv[i]) * d);
+        tmem_st16(taddr + 32 * blk, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
+        tmem_st16(taddr + 32 * blk + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
+    }
+}
+
+// Gated calls: Phi_K row r of token block u (64 tokens at phi) times the keys'
+// state weights (fp32 at wcol, the block's 64 tokens), in place; returns the
+// sum of the weighted bf16-rounded values.
+__device__ __noinline__ float weight_phik_row(uint32_t phi, uint32_t r, uint32_t wcol) {
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll 1
+    for (uint32_t cc = 0; cc < 8; ++cc) {
+        const uint4 v = ld_shared_v4(phi + sw128(r, cc));
+        const uint4 wa = ld_shared_v4(wcol + 4 * (8 * cc)), wb = ld_shared_v4(wcol + 4 * (8 * cc + 4));
+        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+        const float wt[8] = {__uint_as_float(wa.x), __uint_as_float(wa.y), __uint_as_float(wa.z), __uint_as_float(wa.w),
+                             __uint_as_float(wb.x), __uint_as_float(wb.y), __uint_as_float(wb.z), __uint_as_float(wb.w)};
+        uint32_t y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            y[i] = pack_bf16(bf16lo(x[i]) * wt[2 * i], bf16hi(x[i]) * wt[2 * i + 1]);
+            z0 += bf16lo(y[i]);
+            z1 += bf16hi(y[i]);
+        }
+        st_shared_v4(phi + sw128(r, cc), y[0], y[1], y[2], y[3]);
+    }
+    return z0 + z1;
+}
+
 // S~ image row r from the fp32 state row (64 columns at taddr).
 __device__ __noinline__ void refresh_row(uint32_t taddr, uint32_t img, uint32_t r) {
 #pragma unroll 1
@@ -1108,15 +1305,19 @@ __device__ __noinline__ void refresh_row(uint32_t taddr, uint32_t img, uint32_t 
     }
 }
 
-// fp32 state row (64 columns at taddr), S~ image row r from a prefix in global
-// memory stored column-major (element e of the row at src[e * 256]).
-__device__ __noinline__ void load_prefix_row(const float* src, uint32_t taddr, uint32_t img, uint32_t r) {
+// fp32 state row (64 columns at taddr, times d: the chunk's decay of a gated
+// call, else 1), S~ image row r from a prefix in global memory stored
+// column-major (element e of the row at src[e * 256]).
+__device__ __noinline__ void load_prefix_row(const float* src, uint32_t taddr, uint32_t img, uint32_t r, float d) {
 #pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {
         uint32_t sv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(src[(size_t)(16 * blk + i) * kM]);
-        tmem_st16(taddr + 16 * blk, sv);
+        uint32_t sd[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sd[i] = __float_as_uint(__uint_as_float(sv[i]) * d);
+        tmem_st16(taddr + 16 * blk, sd);
 #pragma unroll
         for (uint32_t c = 0; c < 2; ++c)
             st_shared_v4(img + sw128(r, 2 * blk + c),
@@ -1165,12 +1366,13 @@ __device__ __forceinline__ void ca_project(uint32_t d, uint32_t a_tile, uint32_t
     for (int kk = 0; kk < 4; ++kk) mma_ss(d, a0 + 2 * kk, b0 + 2 * kk, id, kk > 0 ? 1u : 0u);
 }
 
-template <int KIND>
+template <int KIND, bool GATED = false>
 __global__ void __launch_bounds__(kCausalThreads, 1)
 k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
             const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ kshift, const float* __restrict__ wmax,
-            const float* __restrict__ prefix, int H, int L, float s, Ranges R, int* err) {
+            const float* __restrict__ prefix, const float* __restrict__ gate, int H, int L, float s, Ranges R,
+            int* err) {
     constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
     constexpr bool TRIG = KIND == FAVOR_KERNEL_SOFTMAX_TRIG;
     constexpr bool KOFF = POS || TRIG;   // per-key terms from the K tile: offsets, or h(s k_j)
@@ -1187,7 +1389,13 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t s_z = s_cs + 2 * kTile * 4;                // z~ fp32 [2 chunk parities][256]
     const uint32_t s_zp = s_z + 2 * kM * 4;                   // key-warp z exchange [256]
     const uint32_t s_dsh = s_zp + kM * 4;                     // group A's den part per row [128]
-    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_dsh - s_w) + kTile * 4);
+    // gated calls, per chunk parity: C_i (cumulative log2 gate), T_j = C_j - log2(1 - g_j),
+    // the keys' state weights 2^(C_last - C_j) (1 - g_j), [2] chunk decays + [2][4] warp totals
+    const uint32_t s_gr = s_dsh + kTile * 4;
+    const uint32_t s_gt = s_gr + 2 * kTile * 4;
+    const uint32_t s_gb = s_gt + 2 * kTile * 4;
+    const uint32_t s_gd = s_gb + 2 * kTile * 4;
+    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_gd - s_w) + 64);
     const int cta = blockIdx.x;
     const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
     const int n = g1 - g0;
@@ -1204,7 +1412,8 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int counts[] = {1, 1, 1, 1, POS ? 9 : 1, KOFF ? 5 : 1, 1, 1,
                               1, 1, 4, 4, 1, 8, 4, 8,
                               1, 1, 4, 1, 8, 1, 1, 4,
-                              8, 8, 1, 4, 1, 1};
+                              8, 8, 1, 4, 1, 1,
+                              1, 1, 8, 8};
         static_assert(sizeof(counts) / sizeof(int) * sizeof(uint64_t) == offsetof(CaBars, tmem_base), "barrier table");
         for (int i = 0; i < (int)(sizeof(counts) / sizeof(int)); ++i) mbar_init(b + i, counts[i]);
         fence_mbar_init();
@@ -1326,8 +1535,10 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
                 for (int kk = 8; kk < 16; ++kk) mma_ts(Z, Y + 8 * (kk - 8), bk + 128 * kk, id_a, 1u);
                 mma_commit(&bars->a_full);
-                // inter term num = Phi_Q S~(t) once the S~ / z~ image of this chunk is in
+                // inter term num = Phi_Q S~(t) once the S~ / z~ image of this chunk is in (gated:
+                // and the query groups have scaled Phi_Q by 2^C_i, now that A has read it)
                 if (!(ok = mbar_wait(&bars->st_full, ph, err, 223))) break;
+                if (GATED && !(ok = mbar_wait(&bars->phiq_scaled, ph, err, 233))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) mma_ts(X + 64, X + 8 * kk, bs + 128 * kk, id_o, kk > 0 ? 1u : 0u);
@@ -1348,6 +1559,8 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 // state: S_h += Phi_K^T_h V (A = Phi_K rows of half h, K-major over tokens); the key
                 // warps keep chunk t+1's features in registers until it has read Phi_K
                 if (!(ok = mbar_wait(&bars->v_full, ph, err, 225))) break;
+                // gated: the key warps have weighted Phi_K toward the chunk's end
+                if (GATED && !(ok = mbar_wait(&bars->phik_w, ph, err, 234))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int hp = 0; hp < 2; ++hp) {
@@ -1432,8 +1645,22 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 // causal mask: keep key j <= query row, packed in place into Z[0,64)
                 if (!mbar_wait(&bars->a_full, ph, err, 244)) break;
                 tc_fence_after();
-                const float rs = mask_row(tl + ca_slot(2, r3), (int)row, q);
-                dsh[row] = dA + rs;
+                float rs, ei = 1.f;
+                if (GATED) {
+                    // A has read Phi_Q: scale it by 2^C_i for the inter term, then the decayed mask
+                    if (!mbar_wait(&bars->g_full[t & 1], (t >> 1) & 1, err, 247)) break;
+                    const float ci = reinterpret_cast<const float*>(sm + (s_gr - s_w))[(t & 1) * kTile + row];
+                    ei = exp2f(ci);
+                    scale_packed_row(tl + ca_slot(0, r3), ei);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->phiq_scaled);
+                    rs = mask_row_gated(tl + ca_slot(2, r3), (int)row, q, ci, s_gt + (t & 1) * kTile * 4);
+                } else {
+                    rs = mask_row(tl + ca_slot(2, r3), (int)row, q);
+                }
+                dsh[row] = ei * dA + rs;
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -1441,11 +1668,24 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             } else {
                 if (!mbar_wait(&bars->pq1_full, ph, err, 245)) break;
                 tc_fence_after();
-                const float dB = query_half<KIND>(tl + ca_slot(1, r3), fa, c, zt + 4 * 128, true);
+                float dB = query_half<KIND>(tl + ca_slot(1, r3), fa, c, zt + 4 * 128, true);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->phiq1_full);
+                if (GATED) {
+                    // once A has read Phi_Q: its half 1 times 2^C_i for the inter term
+                    if (!mbar_wait(&bars->a_full, ph, err, 250)) break;
+                    if (!mbar_wait(&bars->g_full[t & 1], (t >> 1) & 1, err, 247)) break;
+                    tc_fence_after();
+                    const float ei = exp2f(reinterpret_cast<const float*>(sm + (s_gr - s_w))[(t & 1) * kTile + row]);
+                    scale_packed_row(tl + ca_slot(1, r3), ei);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->phiq_scaled);
+                    dB *= ei;
+                }
                 // output rows: num / den, den = this half + group A's half and row sum
                 if (!mbar_wait(&bars->o_full, ph, err, 246)) break;
                 if (!mbar_wait(&bars->am_full, ph, err, 247)) break;   // dsh of this chunk is visible
@@ -1487,11 +1727,62 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         int cur_bh = -1, kap_h = -1, nzx = 0;
         float kap = 0.f;
         bool ok = true;
+        // gated calls: warp 10 scans each chunk's gates, four tokens per lane; the
+        // next chunk's gates are loaded a chunk ahead
+        const bool scanner = GATED && warp == 10;
+        float4 gnext = make_float4(1.f, 1.f, 1.f, 1.f);
+        auto load_gates = [&](int tt) {
+            const int gg = g0 + tt, bb = gg / R.tph, tk = (gg % R.tph) * kTile + 4 * lane;
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = tk + e < L ? __ldg(gate + (size_t)bb * L + tk + e) : 1.f;
+            return make_float4(v[0], v[1], v[2], v[3]);
+        };
+        if (scanner && n > 0) gnext = load_gates(0);
+        float* gflt = reinterpret_cast<float*>(sm + (s_gr - s_w));   // C_i | T_j | weights | decays, by parity
         for (int t = 0; t < n && ok; ++t) {
             const uint32_t ph = t & 1;
             const int g = g0 + t, bh = g / R.tph, h = bh % H, tok0 = (g % R.tph) * kTile;
             const int r3 = t % 3;
             const uint32_t Z = tl + ca_slot(2, r3);
+            if (scanner) {
+                // this chunk's cumulative log2 gates C_i (gates clamped below at 2^-126; past L a
+                // gate of 1 with weight 0), T_j = C_j - log2(1 - g_j), the keys' state weights
+                // 2^(C_last - C_j) (1 - g_j) and the chunk decay 2^C_last
+                const float4 g4 = gnext;
+                if (t + 1 < n) gnext = load_gates(t + 1);
+                const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+                float c[4], acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc += log2f(fmaxf(gv[e], 1.17549435e-38f));
+                    c[e] = acc;
+                }
+                float off = acc;   // inclusive scan of the lanes' sums
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float x = __shfl_up_sync(0xffffffffu, off, o);
+                    if (lane >= o) off += x;
+                }
+                const float total = __shfl_sync(0xffffffffu, off, 31);
+                off -= acc;   // exclusive
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = 4 * lane + e;
+                    const float ci = c[e] + off, om = 1.f - gv[e];
+                    gflt[ph * kTile + tok] = ci;
+                    gflt[2 * kTile + ph * kTile + tok] = om > 0.f ? ci - log2f(om) : 1.0e30f;
+                    gflt[4 * kTile + ph * kTile + tok] = om > 0.f ? exp2f(total - ci) * om : 0.f;
+                }
+                if (lane == 0) gflt[6 * kTile + ph] = exp2f(total);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->g_full[ph]);
+            }
+            float gdec = 1.f;   // the chunk's decay of the carried state (gated calls)
+            if (GATED) {
+                if (!(ok = mbar_wait(&bars->g_full[ph], (t >> 1) & 1, err, 261))) break;
+                gdec = gflt[6 * kTile + ph];
+            }
             // key offsets of this chunk (tokens 32q + lane), in cs[t & 1]: exponent offsets
             // (positive features) or the factors h(s k_j) (trigonometric)
             if (KOFF && u == 0) {
@@ -1519,7 +1810,7 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     tc_fence_after();
                 }
                 const float* pre = prefix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1));
-                load_prefix_row(pre + rown, tl + 384 + 64 * u, s_st, rown);
+                load_prefix_row(pre + rown, tl + 384 + 64 * u, s_st, rown, gdec);
                 zpre = pre[(size_t)64 * kM + rown];
                 zr[0] = zr[1] = 0.f;
                 zs[ph * kM + rown] = zpre;
@@ -1549,8 +1840,10 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (!ok) break;
             }
             if (!ok) break;
-            zr[0] += zc[0];
-            zr[1] += zc[1];
+            if (!GATED) {
+                zr[0] += zc[0];
+                zr[1] += zc[1];
+            }
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -1561,11 +1854,33 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 ok = mbar_wait(&bars->s_full, ph ^ 1, err, 252) && mbar_wait(&bars->ai_done, ph ^ 1, err, 253);
                 if (!ok) break;
                 tc_fence_after();
-                refresh_row(tl + 384 + 64 * u, s_st, rown);
+                if (GATED) {
+                    // the image of S(t-1) for the inter term, and S(t-1) times the chunk's decay
+                    // for the state update of t to accumulate onto
+                    refresh_decay_row(tl + 384 + 64 * u, s_st, rown, gdec);
+                    tmem_st_wait();
+                } else {
+                    refresh_row(tl + 384 + 64 * u, s_st, rown);
+                }
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->st_full);
+            }
+            if (GATED) {
+                // once A has read Phi_K: weight this thread's two rows of it by the keys' state
+                // weights (the state update reads them next); the running sums decay the same way
+                if (!(ok = mbar_wait(&bars->a_full, ph, err, 262))) break;
+                const uint32_t wcol = s_gr + (4 * kTile + ph * kTile + 64 * (uint32_t)u) * 4;
+                const uint32_t phi = s_phi + (uint32_t)u * 2 * kPhiBlock;
+                const float zw0 = weight_phik_row(phi, r0, wcol);
+                const float zw1 = weight_phik_row(phi, r0 + 128, wcol);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->phik_w);
+                zr[0] = fmaf(gdec, zr[0], zw0);
+                zr[1] = fmaf(gdec, zr[1], zw1);
+                zpre *= gdec;
             }
             // z~ of chunk t+1 (same piece): this thread's sums plus the partner warp's for row rown
             if (t + 1 < n && (g + 1) / R.tph == bh) {
@@ -1673,7 +1988,7 @@ constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * 
 constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kRStages * kTileBytes + kRImage + 2 * kTileBytes +
                                  2 * 4 * kTile * 4 + sizeof(RdBars);
 constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kSBytes + 2 * kTileBytes + 2 * kTile * 4 +
-                                3 * kM * 4 + kTile * 4 + sizeof(CaBars);
+                                3 * kM * 4 + kTile * 4 + 6 * kTile * 4 + 64 + sizeof(CaBars);
 static_assert(kSmemCausal <= 232448, "causal shared memory");
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
 
@@ -1683,32 +1998,44 @@ void allow_all_once() {
         allow_smem(k_tc_state<FAVOR_KERNEL_SOFTMAX_POS>, kSmemState);
         allow_smem(k_tc_state<FAVOR_KERNEL_RELU>, kSmemState);
         allow_smem(k_tc_state<FAVOR_KERNEL_SOFTMAX_TRIG>, kSmemState);
+        allow_smem(k_tc_state<FAVOR_KERNEL_SOFTMAX_POS, true>, kSmemState);
+        allow_smem(k_tc_state<FAVOR_KERNEL_RELU, true>, kSmemState);
         allow_smem(k_tc_readout<FAVOR_KERNEL_SOFTMAX_POS>, kSmemReadout);
         allow_smem(k_tc_readout<FAVOR_KERNEL_RELU>, kSmemReadout);
         allow_smem(k_tc_readout<FAVOR_KERNEL_SOFTMAX_TRIG>, kSmemReadout);
         allow_smem(k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS>, kSmemCausal);
         allow_smem(k_tc_causal<FAVOR_KERNEL_RELU>, kSmemCausal);
         allow_smem(k_tc_causal<FAVOR_KERNEL_SOFTMAX_TRIG>, kSmemCausal);
+        allow_smem(k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS, true>, kSmemCausal);
+        allow_smem(k_tc_causal<FAVOR_KERNEL_RELU, true>, kSmemCausal);
         allow_smem(k_tc_feature_map<FAVOR_KERNEL_SOFTMAX_POS>, kSmemFmap);
         allow_smem(k_tc_feature_map<FAVOR_KERNEL_RELU>, kSmemFmap);
         cudaGetLastError();
     });
 }
 
+// wlog: null, or the gated call's per-token log2 key weights (k_gate_weights).
 favor_status launch_state(const Handle& h, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mw,
-                          int BH, int L, const Ranges& R, cudaStream_t st) {
+                          int BH, int L, const Ranges& R, cudaStream_t st, const float* wlog = nullptr) {
     if ((size_t)BH * R.pstride > h.ws_partial_rows)
         return set_error(FAVOR_ERR_INVALID_ARG, "state workspace too small (%d x %d rows)", BH, R.pstride);
     ProfScope ps(h, PROF_STATE, st);
-    if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
-        k_tc_state<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kStateThreads, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial,
-                                                                                      h.H, L, h.s, R, h.dev_err);
+    const dim3 g(R.G), b(kStateThreads);
+    if (wlog && h.kind == FAVOR_KERNEL_SOFTMAX_POS)
+        k_tc_state<FAVOR_KERNEL_SOFTMAX_POS, true><<<g, b, kSmemState, st>>>(mk, mv, mw, h.kshift, wlog, h.ws_partial,
+                                                                            h.H, L, h.s, R, h.dev_err);
+    else if (wlog)
+        k_tc_state<FAVOR_KERNEL_RELU, true><<<g, b, kSmemState, st>>>(mk, mv, mw, h.kshift, wlog, h.ws_partial, h.H, L,
+                                                                     h.s, R, h.dev_err);
+    else if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
+        k_tc_state<FAVOR_KERNEL_SOFTMAX_POS><<<g, b, kSmemState, st>>>(mk, mv, mw, h.kshift, nullptr, h.ws_partial,
+                                                                      h.H, L, h.s, R, h.dev_err);
     else if (h.kind == FAVOR_KERNEL_SOFTMAX_TRIG)
-        k_tc_state<FAVOR_KERNEL_SOFTMAX_TRIG><<<R.G, kStateThreads, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial,
-                                                                                       h.H, L, h.s, R, h.dev_err);
+        k_tc_state<FAVOR_KERNEL_SOFTMAX_TRIG><<<g, b, kSmemState, st>>>(mk, mv, mw, h.kshift, nullptr, h.ws_partial,
+                                                                       h.H, L, h.s, R, h.dev_err);
     else
-        k_tc_state<FAVOR_KERNEL_RELU><<<R.G, kStateThreads, kSmemState, st>>>(mk, mv, mw, h.kshift, h.ws_partial, h.H,
-                                                                               L, h.s, R, h.dev_err);
+        k_tc_state<FAVOR_KERNEL_RELU><<<g, b, kSmemState, st>>>(mk, mv, mw, h.kshift, nullptr, h.ws_partial, h.H, L,
+                                                               h.s, R, h.dev_err);
     count_launch();
     return check_launch("tensor-core state kernel");
 }
@@ -1813,15 +2140,63 @@ favor_status tc_causal(const Handle& h, const void* q, const void* k, const void
     ProfScope ps(h, PROF_CAUSAL, st);
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
         k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS><<<R.G, kCausalThreads, kSmemCausal, st>>>(
-            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, h.H, L, h.s, R, h.dev_err);
+            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, nullptr, h.H, L, h.s, R, h.dev_err);
     else if (h.kind == FAVOR_KERNEL_SOFTMAX_TRIG)
         k_tc_causal<FAVOR_KERNEL_SOFTMAX_TRIG><<<R.G, kCausalThreads, kSmemCausal, st>>>(
-            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, h.H, L, h.s, R, h.dev_err);
+            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, nullptr, h.H, L, h.s, R, h.dev_err);
     else
         k_tc_causal<FAVOR_KERNEL_RELU><<<R.G, kCausalThreads, kSmemCausal, st>>>(
-            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, h.H, L, h.s, R, h.dev_err);
+            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, nullptr, h.H, L, h.s, R, h.dev_err);
     count_launch();
     return check_launch("tensor-core causal kernel");
+}
+
+// RFA-Gate causal attention on the tensor cores (positive and ReLU features):
+// per-token key weights toward each piece's end and the pieces' decays, the
+// weighted piece states, their decayed prefix, then the gated chunk kernel.
+favor_status tc_causal_gated(const Handle& h, const void* q, const void* k, const void* v, const float* gate, void* out,
+                             int B, int L, cudaStream_t st) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return simt_causal(h, q, k, v, out, B, L, st, gate);
+    allow_all_once();
+    const int BH = B * h.H;
+    Ranges R = plan_ranges(BH, L, h.num_sms);
+    CUtensorMap mq, mk, mv, mw, mo;
+    if (!map_tokens(&mq, q, BH, L) || !map_tokens(&mk, k, BH, L) || !map_tokens(&mv, v, BH, L) ||
+        !map_tokens(&mo, out, BH, L) || !map_omega(&mw, h.omega_bf16, h.H))
+        return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    favor_status s;
+    if (R.pstride > 1) {
+        {
+            ProfScope ps(h, PROF_COMBINE, st);
+            // the per-token log2 weights fit the causal backward's row statistics buffer
+            k_gate_weights<<<R.G, 128, 0, st>>>(gate, h.ws_rowstat, h.ws_segdecay, L, R);
+            count_launch();
+            s = check_launch("gate weights kernel");
+            if (s != FAVOR_OK) return s;
+        }
+        s = launch_state(h, mk, mv, mw, BH, L, R, st, h.ws_rowstat);
+        if (s != FAVOR_OK) return s;
+        dim3 g2((kM * (kDV + 1) + 255) / 256, BH);
+        ProfScope ps(h, PROF_COMBINE, st);
+        k_scan_pieces_decay<<<g2, 256, 0, st>>>(h.ws_partial, h.ws_segdecay, R);
+        count_launch();
+        s = check_launch("decayed piece scan kernel");
+    } else {
+        s = cudaMemsetAsync(h.ws_partial, 0, (size_t)BH * kM * (kDV + 1) * sizeof(float), st) == cudaSuccess
+                ? FAVOR_OK
+                : set_error(FAVOR_ERR_CUDA, "cudaMemsetAsync failed");
+    }
+    if (s != FAVOR_OK) return s;
+    ProfScope ps(h, PROF_CAUSAL, st);
+    if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
+        k_tc_causal<FAVOR_KERNEL_SOFTMAX_POS, true><<<R.G, kCausalThreads, kSmemCausal, st>>>(
+            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, gate, h.H, L, h.s, R, h.dev_err);
+    else
+        k_tc_causal<FAVOR_KERNEL_RELU, true><<<R.G, kCausalThreads, kSmemCausal, st>>>(
+            mq, mk, mv, mw, mo, h.kshift, h.omega_wmax, h.ws_partial, gate, h.H, L, h.s, R, h.dev_err);
+    count_launch();
+    return check_launch("tensor-core gated causal kernel");
 }
 
 favor_status tc_kv_state(const Handle& h, const void* k, const void* v, float* state, int B, int L, cudaStream_t st) {

@@ -59,6 +59,26 @@ def test_gated_causal_fast_decay():
     assert O.row_rel_err(out, ref) <= TOL[w.dtype]
 
 
+@pytest.mark.parametrize("kind", O.KINDS)
+@pytest.mark.parametrize("lo,hi", [(0.8, 1.0), (0.05, 0.6)], ids=["slow", "fast"])
+def test_gated_causal_many_chunks_per_range(kind, lo, hi):
+    """The tensor-core shape with several 128-token chunks per work range and a
+    ragged tail (2 heads x 38363 tokens over the SMs): the gated state is carried
+    from chunk to chunk inside a range (decayed in place) as well as across
+    ranges (the decayed prefix of the pieces).  Fast-decaying gates reach the
+    2^-126 clamp within a chunk."""
+    import torch
+    w = CONFIGS["bidir_bf16"].replace(B=1, H=2, L=38363)
+    omega, q, k, v = make_workload(w, 64)
+    g = _gates(w, 64, lo, hi)
+    with R.Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, omega, w.data_scale, w.B, w.L) as f:
+        out = to_host(f.attn_causal_gated(*(to_dev(a, w.dtype) for a in (q, k, v)), torch.from_numpy(g).cuda()))
+        assert R.favor_device_error(f.handle) == 0
+    ref = O.favor_causal_gated(q, k, v, g, omega, w.data_scale, kind)
+    assert np.isfinite(out).all()
+    assert O.row_rel_err(out, ref) <= TOL[w.dtype]
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
 def test_gated_steps_continue_a_state(shape):
     """Gated decode steps in blocks of 1, 5 and 34 tokens from a zero state give
