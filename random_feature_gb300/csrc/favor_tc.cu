@@ -1048,12 +1048,55 @@ __device__ __forceinline__ uint32_t ca_slot(int role, int r3) {
 // Features of one query half, 32 projections at a time, packed in place into
 // the first 64 columns at taddr; returns sum_r f_r z~_r over the half's z~
 // (fp32 in shared memory at zaddr), taken over the bf16-rounded features.
-// Positive: exp2(a p - c); ReLU: max(p, 0); trigonometric: sin (half 0) or cos
-// (half 1, `cosine`) of a p, where the caller passes a = s.
 // The block loop stays rolled: the kernel's roles run different code at the
 // same time, and unrolled bodies overflow the instruction cache.
 template <int KIND>
-__device__ __noinline__ float query_half(uint32_t taddr, float a, float c, uint32_t zaddr, bool cosine) {
+__device__ __noinline__ float query_half(uint32_t taddr, float a, float c, uint32_t zaddr) {
+    float d0 = 0.f, d1 = 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t p[32], w[16];
+        tmem_ld32(taddr + 32 * blk, p);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 z4a = ld_shared_v4(zaddr + 4 * (32 * blk + 8 * j));
+            const uint4 z4b = ld_shared_v4(zaddr + 4 * (32 * blk + 8 * j + 4));
+            const float zz[8] = {__uint_as_float(z4a.x), __uint_as_float(z4a.y), __uint_as_float(z4a.z),
+                                 __uint_as_float(z4a.w), __uint_as_float(z4b.x), __uint_as_float(z4b.y),
+                                 __uint_as_float(z4b.z), __uint_as_float(z4b.w)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = 8 * j + 2 * i;
+                float f0, f1;
+                if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                    f0 = ex2(fmaf(__uint_as_float(p[e]), a, -c));
+                    f1 = ex2(fmaf(__uint_as_float(p[e + 1]), a, -c));
+                } else {
+                    f0 = fmaxf(__uint_as_float(p[e]), 0.f);
+                    f1 = fmaxf(__uint_as_float(p[e + 1]), 0.f);
+                }
+                const uint32_t pk = pack_bf16(f0, f1);
+                d0 = fmaf(bf16lo(pk), zz[2 * i], d0);
+                d1 = fmaf(bf16hi(pk), zz[2 * i + 1], d1);
+                w[4 * j + i] = pk;
+            }
+        }
+        // packed block blk lands in columns [16 blk, 16 blk + 16), all of which were read already
+        tmem_st16(taddr + 16 * blk, w);
+    }
+    return d0 + d1;
+}
+
+// Features of one query half, 32 projections at a time, packed in place into
+// the first 64 columns at taddr; returns sum_r f_r z~_r over the half's z~
+// (fp32 in shared memory at zaddr), taken over the bf16-rounded features.
+// This copy serves the trigonometric kind: sin (half 0) or cos (half 1, COS)
+// of a p, where the caller passes a = s (c is unused).
+// The block loop stays rolled: the kernel's roles run different code at the
+// same time, and unrolled bodies overflow the instruction cache.
+template <int KIND, bool COS>
+__device__ __noinline__ float query_half_trig(uint32_t taddr, float a, float c, uint32_t zaddr) {
     float d0 = 0.f, d1 = 0.f;
 #pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {
@@ -1075,8 +1118,8 @@ __device__ __noinline__ float query_half(uint32_t taddr, float a, float c, uint3
                     f0 = ex2(fmaf(__uint_as_float(p[e]), a, -c));
                     f1 = ex2(fmaf(__uint_as_float(p[e + 1]), a, -c));
                 } else if (KIND == FAVOR_KERNEL_SOFTMAX_TRIG) {
-                    f0 = sincos_reduced(a * __uint_as_float(p[e]), cosine);
-                    f1 = sincos_reduced(a * __uint_as_float(p[e + 1]), cosine);
+                    f0 = sincos_reduced(a * __uint_as_float(p[e]), COS);
+                    f1 = sincos_reduced(a * __uint_as_float(p[e + 1]), COS);
                 } else {
                     f0 = fmaxf(__uint_as_float(p[e]), 0.f);
                     f1 = fmaxf(__uint_as_float(p[e + 1]), 0.f);
@@ -1132,12 +1175,73 @@ __device__ __noinline__ float mask_row(uint32_t taddr, int row, int q) {
 // previous contents are no longer read) has completed the phase of parity
 // gate_par, stored into Phi_K [feature][token] (token block u of 64, 128-byte
 // swizzle).  Returns the sum of the features; *ok = false if the gate's wait
-// gave up (nothing stored).  Trigonometric features: sin (or cos, `cosine`) of
-// a p times the token's h(s k_j) from cs, where the caller passes a = s.
+// gave up (nothing stored).
 template <int KIND>
 __device__ __noinline__ float key_half_row(uint32_t taddr, uint64_t* release, uint64_t* gate, uint32_t gate_par,
-                                           int* err, bool* ok, uint32_t phi, uint32_t r, float a, bool cosine,
-                                           uint32_t cs) {
+                                           int* err, bool* ok, uint32_t phi, uint32_t r, float a, uint32_t cs) {
+    uint32_t w[32];
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        uint32_t p[32];
+        tmem_ld32(taddr + 32 * blk, p);
+        tmem_ld_wait();
+        if (blk == 1 && release) {
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(release);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            float c8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                const uint32_t ca_addr = cs + 4 * (32 * blk + 8 * cc);
+                const uint4 ca = ld_shared_v4(ca_addr), cb = ld_shared_v4(ca_addr + 16);
+                c8[0] = __uint_as_float(ca.x); c8[1] = __uint_as_float(ca.y);
+                c8[2] = __uint_as_float(ca.z); c8[3] = __uint_as_float(ca.w);
+                c8[4] = __uint_as_float(cb.x); c8[5] = __uint_as_float(cb.y);
+                c8[6] = __uint_as_float(cb.z); c8[7] = __uint_as_float(cb.w);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x0 = __uint_as_float(p[8 * cc + 2 * i]), x1 = __uint_as_float(p[8 * cc + 2 * i + 1]);
+                float f0, f1;
+                if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                    f0 = ex2(fmaf(x0, a, c8[2 * i]));
+                    f1 = ex2(fmaf(x1, a, c8[2 * i + 1]));
+                } else {
+                    f0 = fmaxf(x0, 0.f);
+                    f1 = fmaxf(x1, 0.f);
+                }
+                z0 += f0;
+                z1 += f1;
+                w[16 * blk + 4 * cc + i] = pack_bf16(f0, f1);
+            }
+        }
+    }
+    if (gate && !mbar_wait(gate, gate_par, err, 258)) {
+        *ok = false;
+        return 0.f;
+    }
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) st_shared_v4(phi + sw128(r, (uint32_t)cc), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
+    return z0 + z1;
+}
+
+// Key features of feature row r for the 64 tokens [64u, 64u + 64) of the tile
+// (their projections: 64 fp32 columns at taddr, offsets folded in by c_j), 32
+// columns at a time; `release` (if not null) is arrived once both blocks are in
+// registers, so the slot may take the next projection while the rest is
+// computed.  f = exp2(a p + c_j) (positive, c_j from cs) or max(p, 0) (ReLU),
+// packed to bf16 in registers; then, after `gate` (if not null: Phi_K's
+// previous contents are no longer read) has completed the phase of parity
+// gate_par, stored into Phi_K [feature][token] (token block u of 64, 128-byte
+// swizzle).  Returns the sum of the features; *ok = false if the gate's wait
+// gave up (nothing stored).  This copy serves the trigonometric kind: sin (or
+// cos, COS) of a p times the token's h(s k_j) from cs, where the caller passes a = s.
+template <int KIND, bool COS>
+__device__ __noinline__ float key_half_row_trig(uint32_t taddr, uint64_t* release, uint64_t* gate, uint32_t gate_par,
+                                           int* err, bool* ok, uint32_t phi, uint32_t r, float a, uint32_t cs) {
     uint32_t w[32];
     float z0 = 0.f, z1 = 0.f;
 #pragma unroll
@@ -1169,8 +1273,8 @@ __device__ __noinline__ float key_half_row(uint32_t taddr, uint64_t* release, ui
                     f0 = ex2(fmaf(x0, a, c8[2 * i]));
                     f1 = ex2(fmaf(x1, a, c8[2 * i + 1]));
                 } else if (KIND == FAVOR_KERNEL_SOFTMAX_TRIG) {
-                    f0 = sincos_reduced(a * x0, cosine) * c8[2 * i];
-                    f1 = sincos_reduced(a * x1, cosine) * c8[2 * i + 1];
+                    f0 = sincos_reduced(a * x0, COS) * c8[2 * i];
+                    f1 = sincos_reduced(a * x1, COS) * c8[2 * i + 1];
                 } else {
                     f0 = fmaxf(x0, 0.f);
                     f1 = fmaxf(x1, 0.f);
@@ -1305,19 +1409,41 @@ __device__ __noinline__ void refresh_row(uint32_t taddr, uint32_t img, uint32_t 
     }
 }
 
-// fp32 state row (64 columns at taddr, times d: the chunk's decay of a gated
-// call, else 1), S~ image row r from a prefix in global memory stored
-// column-major (element e of the row at src[e * 256]).
-__device__ __noinline__ void load_prefix_row(const float* src, uint32_t taddr, uint32_t img, uint32_t r, float d) {
+// fp32 state row (64 columns at taddr), S~ image row r from a prefix in global
+// memory stored column-major (element e of the row at src[e * 256]).
+__device__ __noinline__ void load_prefix_row(const float* src, uint32_t taddr, uint32_t img, uint32_t r) {
 #pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {
         uint32_t sv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(src[(size_t)(16 * blk + i) * kM]);
-        uint32_t sd[16];
+        tmem_st16(taddr + 16 * blk, sv);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sd[i] = __float_as_uint(__uint_as_float(sv[i]) * d);
-        tmem_st16(taddr + 16 * blk, sd);
+        for (uint32_t c = 0; c < 2; ++c)
+            st_shared_v4(img + sw128(r, 2 * blk + c),
+                         pack_bf16(__uint_as_float(sv[8 * c]), __uint_as_float(sv[8 * c + 1])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 2]), __uint_as_float(sv[8 * c + 3])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 4]), __uint_as_float(sv[8 * c + 5])),
+                         pack_bf16(__uint_as_float(sv[8 * c + 6]), __uint_as_float(sv[8 * c + 7])));
+    }
+}
+
+// Gated calls: as load_prefix_row, the fp32 state row times the chunk's decay d.
+template <bool SCALED>
+__device__ __noinline__ void load_prefix_row_scaled(const float* src, uint32_t taddr, uint32_t img, uint32_t r, float d) {
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t sv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(src[(size_t)(16 * blk + i) * kM]);
+        if (SCALED) {
+            uint32_t sd[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sd[i] = __float_as_uint(__uint_as_float(sv[i]) * d);
+            tmem_st16(taddr + 16 * blk, sd);
+        } else {
+            tmem_st16(taddr + 16 * blk, sv);
+        }
 #pragma unroll
         for (uint32_t c = 0; c < 2; ++c)
             st_shared_v4(img + sw128(r, 2 * blk + c),
@@ -1389,13 +1515,12 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t s_z = s_cs + 2 * kTile * 4;                // z~ fp32 [2 chunk parities][256]
     const uint32_t s_zp = s_z + 2 * kM * 4;                   // key-warp z exchange [256]
     const uint32_t s_dsh = s_zp + kM * 4;                     // group A's den part per row [128]
+    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_dsh - s_w) + kTile * 4);
     // gated calls, per chunk parity: C_i (cumulative log2 gate), T_j = C_j - log2(1 - g_j),
-    // the keys' state weights 2^(C_last - C_j) (1 - g_j), [2] chunk decays + [2][4] warp totals
-    const uint32_t s_gr = s_dsh + kTile * 4;
+    // the keys' state weights 2^(C_last - C_j) (1 - g_j), then [2] chunk decays
+    const uint32_t s_gr = (s_dsh + kTile * 4 + (uint32_t)sizeof(CaBars) + 15u) & ~15u;
     const uint32_t s_gt = s_gr + 2 * kTile * 4;
     const uint32_t s_gb = s_gt + 2 * kTile * 4;
-    const uint32_t s_gd = s_gb + 2 * kTile * 4;
-    CaBars* bars = reinterpret_cast<CaBars*>(sm + (s_gd - s_w) + 64);
     const int cta = blockIdx.x;
     const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
     const int n = g1 - g0;
@@ -1637,7 +1762,9 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (grpA) {
                 if (!mbar_wait(&bars->pq0_full, ph, err, 243)) break;
                 tc_fence_after();
-                const float dA = query_half<KIND>(tl + ca_slot(0, r3), fa, c, zt, false);
+                float dA;
+                if constexpr (TRIG) dA = query_half_trig<KIND, false>(tl + ca_slot(0, r3), fa, c, zt);
+                else dA = query_half<KIND>(tl + ca_slot(0, r3), a, c, zt);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -1668,7 +1795,9 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             } else {
                 if (!mbar_wait(&bars->pq1_full, ph, err, 245)) break;
                 tc_fence_after();
-                float dB = query_half<KIND>(tl + ca_slot(1, r3), fa, c, zt + 4 * 128, true);
+                float dB;
+                if constexpr (TRIG) dB = query_half_trig<KIND, true>(tl + ca_slot(1, r3), fa, c, zt + 4 * 128);
+                else dB = query_half<KIND>(tl + ca_slot(1, r3), a, c, zt + 4 * 128);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -1792,9 +1921,10 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     kap_h = h;
                 }
                 const float nrm = row_sqnorm(s_k, r0);
-                const bool live = tok0 + (int)r0 < L;
-                cs[ph * kTile + r0] = TRIG ? (live ? expf(0.5f * s * s * nrm) : 0.f)
-                                           : (live ? -(0.5f * s * s * nrm + kap) * kLog2e : -1.0e30f);
+                if constexpr (TRIG)
+                    cs[ph * kTile + r0] = (tok0 + (int)r0 < L) ? expf(0.5f * s * s * nrm) : 0.f;
+                else
+                    cs[ph * kTile + r0] = (tok0 + (int)r0 < L) ? -(0.5f * s * s * nrm + kap) * kLog2e : -1.0e30f;
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&bars->k_empty);
@@ -1810,7 +1940,8 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     tc_fence_after();
                 }
                 const float* pre = prefix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1));
-                load_prefix_row(pre + rown, tl + 384 + 64 * u, s_st, rown, gdec);
+                if constexpr (GATED) load_prefix_row_scaled<true>(pre + rown, tl + 384 + 64 * u, s_st, rown, gdec);
+                else load_prefix_row(pre + rown, tl + 384 + 64 * u, s_st, rown);
                 zpre = pre[(size_t)64 * kM + rown];
                 zr[0] = zr[1] = 0.f;
                 zs[ph * kM + rown] = zpre;
@@ -1833,10 +1964,19 @@ k_tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tc_fence_after();
                 // half 0's projections go to registers first (then the slot may take half 1);
                 // stores into Phi_K wait until the state update of t-1 has read it
-                zc[hp] = key_half_row<KIND>(Z + 64 * (uint32_t)u, hp == 0 ? &bars->pk_free : nullptr,
-                                            (hp == 0 && t > 0) ? &bars->phik_free : nullptr, ph ^ 1, err, &ok,
-                                            s_phi + (uint32_t)u * 2 * kPhiBlock, r0 + 128 * (uint32_t)hp, fa, hp == 1,
-                                            s_cs + (ph * kTile + 64 * (uint32_t)u) * 4);
+                if constexpr (TRIG) {
+                    const uint32_t kt = Z + 64 * (uint32_t)u, kphi = s_phi + (uint32_t)u * 2 * kPhiBlock;
+                    const uint32_t kcs = s_cs + (ph * kTile + 64 * (uint32_t)u) * 4, kr = r0 + 128 * (uint32_t)hp;
+                    uint64_t* krel = hp == 0 ? &bars->pk_free : nullptr;
+                    uint64_t* kgate = (hp == 0 && t > 0) ? &bars->phik_free : nullptr;
+                    zc[hp] = hp == 1 ? key_half_row_trig<KIND, true>(kt, krel, kgate, ph ^ 1, err, &ok, kphi, kr, fa, kcs)
+                                     : key_half_row_trig<KIND, false>(kt, krel, kgate, ph ^ 1, err, &ok, kphi, kr, fa, kcs);
+                } else {
+                    zc[hp] = key_half_row<KIND>(Z + 64 * (uint32_t)u, hp == 0 ? &bars->pk_free : nullptr,
+                                                (hp == 0 && t > 0) ? &bars->phik_free : nullptr, ph ^ 1, err, &ok,
+                                                s_phi + (uint32_t)u * 2 * kPhiBlock, r0 + 128 * (uint32_t)hp, a,
+                                                s_cs + (ph * kTile + 64 * (uint32_t)u) * 4);
+                }
                 if (!ok) break;
             }
             if (!ok) break;
@@ -1988,7 +2128,7 @@ constexpr size_t kSmemState = 1024 + kOmegaBytes + kNS * 2 * kTileBytes + kNS * 
 constexpr size_t kSmemReadout = 1024 + kOmegaBytes + kRStages * kTileBytes + kRImage + 2 * kTileBytes +
                                  2 * 4 * kTile * 4 + sizeof(RdBars);
 constexpr size_t kSmemCausal = 1024 + kOmegaBytes + 3 * kTileBytes + 4 * kPhiBlock + kSBytes + 2 * kTileBytes + 2 * kTile * 4 +
-                                3 * kM * 4 + kTile * 4 + 6 * kTile * 4 + 64 + sizeof(CaBars);
+                                3 * kM * 4 + kTile * 4 + sizeof(CaBars) + 16 + 6 * kTile * 4 + 64;
 static_assert(kSmemCausal <= 232448, "causal shared memory");
 constexpr size_t kSmemFmap = 1024 + kOmegaBytes + kTileBytes + 64;
 
