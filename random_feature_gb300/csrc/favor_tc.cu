@@ -1027,6 +1027,18 @@ k_tc_readout(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 // per-row constant, so it cancels between num and den.  Key features are
 // exp2(a p + c_j) with the per-token offset c_j = -(s^2 ||k_j||^2 / 2 +
 // kappa_h) log2(e) taken from shared memory (-1e30 for rows past L).
+//
+// Trigonometric kind (rows [omega; omega]): sin of s p in half 0, cos in half
+// 1, the keys times h(s k_j) from cs (query_half_trig, key_half_row_trig).
+//
+// Gated calls (GATED, RFA-Gate): warp 10 scans each chunk's gates into C_i
+// (cumulative log2 gate), T_j = C_j - log2(1 - g_j), the keys' state weights
+// 2^(C_last - C_j) (1 - g_j) and the decay 2^C_last (g_full).  After A has read
+// Phi_Q the query groups scale it by 2^C_i (phiq_scaled: the inter term then
+// carries that row factor) and the mask multiplies A_ij by 2^(C_i - T_j);
+// after A has read Phi_K the key warps weight it for the state update
+// (phik_w); the refresh writes the S~ image of S and then S 2^C_last back for
+// the update to accumulate onto.
 constexpr int kCausalThreads = 576;
 
 struct CaBars {
