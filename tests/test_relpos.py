@@ -63,12 +63,14 @@ def test_gated_causal_fast_decay():
 @pytest.mark.parametrize("lo,hi", [(0.8, 1.0), (0.05, 0.6)], ids=["slow", "fast"])
 def test_gated_causal_many_chunks_per_range(kind, lo, hi):
     """The tensor-core shape with several 128-token chunks per work range and a
-    ragged tail (2 heads x 38363 tokens over the SMs): the gated state is carried
-    from chunk to chunk inside a range (decayed in place) as well as across
-    ranges (the decayed prefix of the pieces).  Fast-decaying gates reach the
-    2^-126 clamp within a chunk."""
+    ragged tail (2 heads x 38491 tokens: 301 tiles a head, ranges of 4 tiles,
+    so one range holds the end of head 0 and the start of head 1): the gated
+    state is carried from chunk to chunk inside a range (decayed in place), from
+    range to range (the decayed prefix of the pieces) and restarts at the head
+    boundary inside a range.  Fast-decaying gates reach the 2^-126 clamp within
+    a chunk."""
     import torch
-    w = CONFIGS["bidir_bf16"].replace(B=1, H=2, L=38363)
+    w = CONFIGS["bidir_bf16"].replace(B=1, H=2, L=38491)
     omega, q, k, v = make_workload(w, 64)
     g = _gates(w, 64, lo, hi)
     with R.Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, omega, w.data_scale, w.B, w.L) as f:
