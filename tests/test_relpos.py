@@ -9,6 +9,7 @@ import random_feature_gb300 as R
 from synth import CONFIGS, make_workload
 
 from _util import TOL, to_dev, to_host
+from test_variants import trig_row_condition
 
 pytestmark = pytest.mark.gpu
 
@@ -179,3 +180,36 @@ def test_variants_full_size_sampled_heads():
             got = to_host(out[:, heads])
         ref = ref_fn()
         assert O.row_rel_err(got, ref) <= TOL[w.dtype], (kind, mode)
+
+
+@pytest.mark.parametrize("L", [1, 127, 129, 300])
+def test_tensor_core_variants_short_and_ragged(L):
+    """Trigonometric (bidirectional and causal) and gated calls on the tensor-core
+    shape at one token, one chunk short of full, one token past a chunk and a
+    ragged multi-chunk length: rows past L must neither leak into the sums nor
+    be written, for the sin/cos epilogue, the key factors h(s k) and the gates'
+    scan alike."""
+    import torch
+    w = CONFIGS["bidir_bf16"].replace(B=2, H=3, L=L)
+    omega, q, k, v = make_workload(w, 65)
+    half = np.ascontiguousarray(omega[:, : w.m // 2])
+    dev = [to_dev(a, w.dtype) for a in (q, k, v)]
+    with R.Favor(w.H, w.m, w.d, w.dv, "softmax_trig", w.dtype, half, w.data_scale, w.B, w.L) as f:
+        for causal in (False, True):
+            out = to_host(f.attn(*dev, causal=causal))
+            ref = (O.favor_causal if causal else O.favor_bidir)(q, k, v, half, w.data_scale, "softmax_trig")
+            assert np.isfinite(out).all()
+            scale = np.maximum(np.abs(ref).max(axis=-1), 1e-300)
+            err = np.abs(out - ref).max(axis=-1) / scale
+            # bf16 operands amplified by each row's cancellation (as test_variants.assert_trig_rows)
+            cond = trig_row_condition(q, k, v, half, w.data_scale, causal)
+            assert np.all(err <= TOL[w.dtype] + 4 * 2.0 ** -9 * cond), (causal, float(np.max(err)))
+        assert R.favor_device_error(f.handle) == 0
+    g = _gates(w, 65, 0.3, 1.0)
+    for kind in O.KINDS:
+        with R.Favor(w.H, w.m, w.d, w.dv, kind, w.dtype, omega, w.data_scale, w.B, w.L) as f:
+            out = to_host(f.attn_causal_gated(*dev, torch.from_numpy(g).cuda()))
+            assert R.favor_device_error(f.handle) == 0
+        ref = O.favor_causal_gated(q, k, v, g, omega, w.data_scale, kind)
+        assert np.isfinite(out).all()
+        assert O.row_rel_err(out, ref) <= TOL[w.dtype], (kind, L)
