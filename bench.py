@@ -509,9 +509,9 @@ def run_ours(args):
 
     # Backward (gradients of the bidirectional and causal calls, positive
     # features) on the same workload, one entry per call with the roofline of
-    # the unit it runs on: the bidirectional backward on the tensor cores
-    # (bf16 shape) against the sustained bf16 peak, the causal one on the CUDA
-    # cores against the FP32 FFMA peak of the SMs at the sampled clock.
+    # the unit it runs on: on the tensor cores (bf16 shape) against the
+    # sustained bf16 peak, else on the CUDA cores against the FP32 FFMA peak of
+    # the SMs at the sampled clock.
     backward = None
     if args.backward_steps > 0:
         hd_ = handles["softmax_pos"]
@@ -545,7 +545,7 @@ def run_ours(args):
                 if n:
                     bk[R.favor_profile_name(sl)] = {"ms_per_call": kms / args.backward_steps,
                                                     "launches_per_call": n / args.backward_steps}
-            tc = tc_shape and not causal
+            tc = tc_shape
             pk = peaks["bf16_tflops_sustained"] * 1e12 if tc else fp32_peak
             ach = fpt * T / (ms / 1e3)
             backward["causal" if causal else "bidir"] = {

@@ -266,8 +266,13 @@ FAVOR_API favor_status favor_set_relpos(favor_handle h, const int* perm, const f
  * out (e.g. bf16) cannot perturb the gradients.
  *   dq, dk     [B,H,L,d], dv [B,H,L,dv]: written, never read; must not alias
  *              any input.
- * All tensors are contiguous device arrays of the handle's dtype; the
- * arithmetic is fp32 on the CUDA cores whatever the dtype, with the forward's
+ * All tensors are contiguous device arrays of the handle's dtype.  For bf16
+ * with d = dv = 64 and m = 256 (positive, hyperbolic and ReLU features) and
+ * 16-byte-aligned pointers both calls run on the tensor cores: bf16 operands
+ * with fp32 accumulation, the key/value and query states and G entering as
+ * bf16 pairs hi + lo; the causal call works in 128-token chunks (states of
+ * the earlier and later chunks, masked products inside the chunk).  Otherwise
+ * the arithmetic is fp32 on the CUDA cores.  Both use the forward's
  * cancelling shifts.  Same argument checks, asynchrony and one-call-per-handle
  * rule as the forward calls; the handle's workspace (allocated by
  * favor_create) is reused, nothing is allocated.

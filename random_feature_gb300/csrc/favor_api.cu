@@ -573,7 +573,10 @@ static favor_status backward_call(const char* fn, bool causal, favor_handle hd, 
         return set_error(FAVOR_ERR_UNSUPPORTED, "%s: no backward for trigonometric features", fn);
     if (relpos_on(h)) return set_error(FAVOR_ERR_UNSUPPORTED, "%s: relative positions are set", fn);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (causal) return simt_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
+    if (causal) {
+        if (tc_supported(h)) return tc_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
+        return simt_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
+    }
     if (tc_supported(h)) return tc_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
     return simt_bidir_backward(h, q, k, v, dout, dq, dk, dv, B, L, s);
 }

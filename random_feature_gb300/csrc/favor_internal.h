@@ -179,6 +179,9 @@ favor_status tc_causal_gated(const Handle& h, const void* q, const void* k, cons
 // Tensor-core bidirectional backward (falls back to the CUDA-core one for unaligned pointers).
 favor_status tc_bidir_backward(const Handle& h, const void* q, const void* k, const void* v, const void* dout,
                                void* dq, void* dk, void* dv, int B, int L, cudaStream_t st);
+// Tensor-core causal backward, chunked (falls back to the CUDA-core one for unaligned pointers).
+favor_status tc_causal_backward(const Handle& h, const void* q, const void* k, const void* v, const void* dout,
+                                void* dq, void* dk, void* dv, int B, int L, cudaStream_t st);
 size_t tc_bwd_image_bytes(size_t BH);
 
 // ---- fixed-order combines of per-segment states (shared by both paths) ----

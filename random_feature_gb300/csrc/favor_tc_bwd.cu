@@ -725,6 +725,1243 @@ k_tc_bwd_k(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// ============================================================ backward (causal)
+// The causal gradients of favor_bwd.cu, chunk by chunk (128 tokens) on the
+// tensor cores.  With A = Phi_Q Phi_K^T and C = dO V^T inside a chunk, the
+// exclusive prefix S, z of the keys before it (S = sum phi_k v^T, z = sum
+// phi_k) and the exclusive suffix T, t of the queries after it (T = sum
+// phi~_q dO^T, t = -sum phi~_q go, phi~_q = phi_q / den):
+//   den_i = phi_q,i . z + sum_{j<=i} A_ij
+//   go_i  = (phi_q,i . (S dO_i) + sum_{j<=i} A_ij C_ij) / den_i          (= dO_i . out_i)
+//   dphi_q,i = (S dO_i - z go_i + sum_{j<=i} (C_ij - go_i) phi_k,j) / den_i
+//   dphi_k,j = T v_j + t + sum_{i>=j} (C_ij - go_i) phi~_q,i
+//   dv_j     = T^T phi_k,j + sum_{i>=j} (phi_k,j . phi~_q,i) dO_i
+// The states of each CTA's piece of a head come from k_tc_bstate (MODE 0: S,
+// z; MODE 1: T, t) and a fixed-order scan over the pieces; inside the piece
+// the query pass carries S, z forward and the key pass carries T, t backward,
+// thread f holding feature row f in fp32 registers and writing the next
+// chunk's hi + lo image.  The subtractions S dO_i - z go_i and T v_j + t, as
+// in the bidirectional passes, need the states near fp32, so each chunk's
+// increment takes its features as hi + lo pairs (kept in tensor memory where
+// the transposed projection left them).  The in-chunk products of dq and dk
+// take f16 operands under power-of-two scales (see the passes); dv, which
+// subtracts nothing, takes bf16.
+//
+//   k_tc_bstate<MODE 0>, k_piece_scan<false>   K, V            -> prefix S, z per piece
+//   k_tc_cbwd_q                                Q, K, V, dO     -> dq, rowstat (den, row shift, go, f16 scale)
+//   k_tc_bstate<MODE 1>, k_piece_scan<true>    Q, dO, rowstat  -> suffix T, t per piece
+//   k_tc_cbwd_k                                Q, K, V, dO     -> dk
+//   k_tc_cbwd_v                                Q, K, dO        -> dv
+//
+// Shared memory of both passes (from a 1 KB boundary): omega 32 KB | state
+// image hi, lo 64 KB | Q, K, V, dO tiles 64 KB | features [2 token blocks][256]
+// [64] bf16 64 KB | z or t fp32 [256] | [128] fp32 column terms | barriers.
+// Each tile buffer is reloaded with the next chunk's tile as soon as the chunk
+// is done with it; the K tile (query pass) and the Q tile (key pass) also hold
+// row partials or the queries' statistics between their last read and that load.
+constexpr uint32_t kCbImgOff = kOmegaBytes;
+constexpr uint32_t kCbTiles = kCbImgOff + 2 * kSBytes;
+constexpr uint32_t kCbPhi = kCbTiles + 4 * kTileBytes;
+constexpr uint32_t kCbVec = kCbPhi + 4 * kPhiBlock;
+constexpr uint32_t kCbBars = kCbVec + kM * 4 + kTile * 4;
+enum { CB_Q = 0, CB_K = 1, CB_V = 2, CB_O = 3 };
+
+struct CbBars {
+    uint64_t w;         // omega
+    uint64_t tile[4];   // Q, K, V, dO buffers (one load per chunk each)
+    uint64_t mma;
+    uint32_t tmem_base;
+    uint32_t pad;
+};
+
+// Loads issued and not yet waited for (parity, -1 when none), drained
+// (bounded) by the issuing thread before a CTA whose wait gave up exits.
+struct CbPending {
+    int w = -1, tile[4] = {-1, -1, -1, -1};
+    __device__ __forceinline__ void drain(CbBars* bars, int* err, int code) {
+        if (w >= 0) mbar_wait(&bars->w, (uint32_t)w, err, code);
+        for (int b = 0; b < 4; ++b)
+            if (tile[b] >= 0) mbar_wait(&bars->tile[b], (uint32_t)tile[b], err, code);
+    }
+};
+
+__device__ __forceinline__ void cb_init(CbBars* bars) {
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->w, 1);
+        for (int b = 0; b < 4; ++b) mbar_init(&bars->tile[b], 1);
+        mbar_init(&bars->mma, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x / 32 == 0) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+}
+
+__device__ __forceinline__ void cb_load_tile(const CUtensorMap* m, uint8_t* sm, int buf, CbBars* bars, int g,
+                                             int tph) {
+    const int bh = g / tph, tile = g - bh * tph;
+    mbar_expect_tx(&bars->tile[buf], kTileBytes);
+    tma_load_3d(sm + kCbTiles + buf * kTileBytes, m, &bars->tile[buf], 0, tile * kTile, bh);
+}
+
+__device__ __forceinline__ void cb_load_omega(const CUtensorMap* m, uint8_t* sm, CbBars* bars, int h) {
+    mbar_expect_tx(&bars->w, kOmegaBytes);
+    tma_load_2d(sm, m, &bars->w, 0, h * kM);
+}
+
+// Two floats -> packed f16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Instruction descriptor of kind::f16 with f16 A and B (format 0), fp32 accumulator.
+__host__ __device__ constexpr uint32_t make_idesc_h(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// 2^e, e in [-126, 127] (exact); floor(log2 x) of a finite normal x > 0.
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+__device__ __forceinline__ int ilog2f(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 127; }
+
+// Power-of-two exponent e with m 2^-e in [2^13, 2^14) for m > 0 (0 for m = 0), clamped to +-100:
+// values up to m scaled by 2^-e stay inside f16's normal range with 11 significant bits.
+__device__ __forceinline__ int f16_scale_exp(float m) {
+    if (!(m > 0.f)) return 0;
+    return max(-100, min(100, ilog2f(m) - 13));
+}
+
+// D[128 x N] = A tile [128 rows][64] . B rows [N][64]^T (both K-major SW128), N = 64 or 128.
+__device__ __forceinline__ void cb_project(uint32_t d, uint32_t a_tile, uint32_t b_rows, int N) {
+    const uint32_t id = make_idesc(128, N, 0, 0);
+    const uint64_t a0 = make_desc(a_tile, 16, 1024, SW_128B);
+    const uint64_t b0 = make_desc(b_rows, 16, 1024, SW_128B);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(d, a0 + 2 * kk, b0 + 2 * kk, id, kk > 0 ? 1u : 0u);
+}
+
+// D[128 tokens][256 features] = X tile . (state hi + state lo)^T, the state image [256][64] K-major.
+__device__ __forceinline__ void cb_state_mult(uint32_t d, uint32_t x_tile, uint32_t img) {
+    const uint32_t id_u = make_idesc(128, 256, 0, 0);
+    const uint64_t a0 = make_desc(x_tile, 16, 1024, SW_128B);
+    const uint64_t bh0 = make_desc(img, 16, 1024, SW_128B);
+    const uint64_t bl0 = make_desc(img + kSBytes, 16, 1024, SW_128B);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(d, a0 + 2 * kk, bh0 + 2 * kk, id_u, kk > 0 ? 1u : 0u);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(d, a0 + 2 * kk, bl0 + 2 * kk, id_u, 1u);
+}
+
+// The chunk's state increment, half h of the features into d_h (128 lanes = features, 64
+// columns): D_h = F^T_h Y with the features F^T_h in tensor memory as hi + lo pairs (at x_h:
+// token block u at + 64 u, hi then lo, 8 columns per 16 tokens) and Y a token tile [128
+// tokens][64] (MN-major).
+__device__ __forceinline__ void cb_state_inc(uint32_t d0, uint32_t d1, uint32_t x0, uint32_t x1, uint32_t y_tile) {
+    const uint32_t id_o = make_idesc(128, 64, 0, 1);
+    const uint64_t by = make_desc(y_tile, 8192, 1024, SW_128B);
+#pragma unroll
+    for (int hp = 0; hp < 2; ++hp) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t hi = (hp ? x1 : x0) + 64 * (kk >> 2) + 8 * (kk & 3);
+            mma_ts(hp ? d1 : d0, hi, by + 128 * kk, id_o, kk > 0 ? 1u : 0u);
+            mma_ts(hp ? d1 : d0, hi + 32, by + 128 * kk, id_o, 1u);
+        }
+    }
+}
+
+// D[128 rows][128 tokens] = X . F where X is packed f16 (F16) or bf16 in tensor memory (features 0..127 at
+// x0, 128..255 at x1, 8 columns per 16 features) and F the features [feature][token] in shared
+// memory (MN-major, N = token in two 64-token blocks).
+template <bool F16>
+__device__ __forceinline__ void cb_scores(uint32_t d, uint32_t x0, uint32_t x1, uint32_t feat) {
+    const uint32_t id_a = F16 ? make_idesc_h(128, 128, 0, 1) : make_idesc(128, 128, 0, 1);
+    const uint64_t bf = make_desc(feat, 2 * kPhiBlock, 1024, SW_128B);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) mma_ts(d, kk < 8 ? x0 + 8 * kk : x1 + 8 * (kk - 8), bf + 128 * kk, id_a, kk > 0 ? 1u : 0u);
+}
+
+// D[128 rows][256 features] += W . F^T where W is packed f16 in tensor memory (tokens 0..63 at
+// w0, 64..127 at w1) and F the features [feature][token] in shared memory (K-major over tokens).
+__device__ __forceinline__ void cb_weighted_features(uint32_t d, uint32_t w0, uint32_t w1, uint32_t feat) {
+    const uint32_t id_b = make_idesc_h(128, 256, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_ts(d, (kk < 4 ? w0 : w1) + 8 * (kk & 3),
+               make_desc(feat + (uint32_t)(kk >> 2) * 2 * kPhiBlock + (uint32_t)(kk & 3) * 32, 16, 1024, SW_128B),
+               id_b, 1u);
+}
+
+// D[128 rows][64] = G . omega (G hi then lo, packed in tensor memory: features 16 kk .. +15 at
+// hi0/lo0 + 8 kk for kk < 8, hi1/lo1 + 8 (kk - 8) after).
+__device__ __forceinline__ void cb_grad_omega(uint32_t d, uint32_t hi0, uint32_t hi1, uint32_t lo0, uint32_t lo1,
+                                              uint32_t s_w) {
+    const uint32_t id_q = make_idesc(128, 64, 0, 1);
+    const uint64_t bw = make_desc(s_w, 8192, 1024, SW_128B);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) mma_ts(d, kk < 8 ? hi0 + 8 * kk : hi1 + 8 * (kk - 8), bw + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) mma_ts(d, kk < 8 ? lo0 + 8 * kk : lo1 + 8 * (kk - 8), bw + 128 * kk, id_q, 1u);
+}
+
+// Row r of the hi + lo state image from a fp32 state row times sc (a power of two).
+__device__ __forceinline__ void cb_write_image(uint32_t img, uint32_t r, const float (&x)[64], float sc) {
+#pragma unroll
+    for (uint32_t c = 0; c < 8; ++c) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_pack(x[8 * c + 2 * i] * sc, x[8 * c + 2 * i + 1] * sc, hi[i], lo[i]);
+        st_shared_v4(img + sw128(r, c), hi[0], hi[1], hi[2], hi[3]);
+        st_shared_v4(img + kSBytes + sw128(r, c), lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// Feature row f of 64 tokens (fp32 projections: 64 columns at taddr).  x_t = exp2(a p + off_t)
+// (positive) or max(p off_t, 0) (ReLU: off_t = the token's scale, 0 past L) goes to row f of the
+// features block `feat` ([feature][token], shared memory) as f16 (f16 true) or bf16; the value
+// e_t = x_t mt_t ms (mt may be null) goes over the row's own columns as a bf16 pair hi + lo (hi at
+// taddr, lo at taddr + 32, 8 columns per 16 tokens).  Returns sum_t e_t wt_t (wt null: weights 1).
+template <int KIND, bool F16>
+__device__ __forceinline__ float cb_feature_row(uint32_t taddr, uint32_t feat, uint32_t f, float a,
+                                                const float* off, const float* mt, float ms, const float* wt) {
+    uint32_t p0[32], p1[32];
+    tmem_ld32(taddr, p0);
+    tmem_ld32(taddr + 32, p1);
+    tmem_ld_wait();
+    float acc = 0.f;
+    uint32_t x0[16], x1[16], h0[16], h1[16], l0[16], l1[16];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float x[2], e[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int t = 2 * i + u;
+            const float pv = __uint_as_float(t < 32 ? p0[t] : p1[t - 32]);
+            x[u] = KIND == FAVOR_KERNEL_SOFTMAX_POS ? ex2(fmaf(pv, a, off[t])) : fmaxf(pv * off[t], 0.f);
+            e[u] = (mt ? x[u] * mt[t] : x[u]) * ms;
+            acc = wt ? fmaf(e[u], wt[t], acc) : acc + e[u];
+        }
+        const uint32_t xp = F16 ? pack_f16(x[0], x[1]) : pack_bf16(x[0], x[1]);
+        if (i < 16) {
+            x0[i] = xp;
+            split_pack(e[0], e[1], h0[i], l0[i]);
+        } else {
+            x1[i - 16] = xp;
+            split_pack(e[0], e[1], h1[i - 16], l1[i - 16]);
+        }
+    }
+#pragma unroll
+    for (uint32_t c = 0; c < 4; ++c) {
+        st_shared_v4(feat + sw128(f, c), x0[4 * c], x0[4 * c + 1], x0[4 * c + 2], x0[4 * c + 3]);
+        st_shared_v4(feat + sw128(f, 4 + c), x1[4 * c], x1[4 * c + 1], x1[4 * c + 2], x1[4 * c + 3]);
+    }
+    tmem_st16(taddr, h0);
+    tmem_st16(taddr + 16, h1);
+    tmem_st16(taddr + 32, l0);
+    tmem_st16(taddr + 48, l1);
+    return acc;
+}
+
+// Largest exp2 argument (positive) or product (ReLU) over the row's 128 projections at taddr.
+template <int KIND>
+__device__ __forceinline__ float cb_row_max_arg(uint32_t taddr, float a, const float* off) {
+    float m = KIND == FAVOR_KERNEL_SOFTMAX_POS ? -INFINITY : 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t p[32];
+        tmem_ld32(taddr + 32 * blk, p);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float pv = __uint_as_float(p[i]), o = off[32 * blk + i];
+            m = fmaxf(m, KIND == FAVOR_KERNEL_SOFTMAX_POS ? fmaf(pv, a, o) : pv * o);
+        }
+    }
+    return m;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+// dx row epilogue: columns 32 ch .. +31 of d = s (acc - s gsum x) (positive) or s acc (ReLU), bf16,
+// stored when dst_row is not null (the tensor-memory load is warp-wide).
+template <int KIND>
+__device__ __forceinline__ void cb_store_grad(__nv_bfloat16* dst_row, uint32_t taddr, int ch, float s, float gsum,
+                                              const uint4 (&xrow)[4]) {
+    uint32_t v0[32];
+    tmem_ld32(taddr, v0);
+    tmem_ld_wait();
+    if (!dst_row) return;
+    uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+    for (uint32_t c4 = 0; c4 < 4; ++c4) {
+        const uint32_t xin[4] = {xrow[c4].x, xrow[c4].y, xrow[c4].z, xrow[c4].w};
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c0 = 8 * c4 + 2 * i;
+            const float acc0 = __uint_as_float(v0[c0]), acc1 = __uint_as_float(v0[c0 + 1]);
+            float d0 = s * acc0, d1 = s * acc1;
+            if (KIND == FAVOR_KERNEL_SOFTMAX_POS) {
+                d0 = s * fmaf(-s * gsum, bf16lo(xin[i]), acc0);
+                d1 = s * fmaf(-s * gsum, bf16hi(xin[i]), acc1);
+            }
+            w[i] = pack_bf16(d0, d1);
+        }
+        dst[4 * ch + c4] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Query pass, persistent over the call's tile ranges (grid R.G, 256 threads).  Thread t is
+// query row t % 128 with features 128 (t / 128) .. +127 of it (the same split as the
+// bidirectional query pass), and feature row t of the key features and of the running prefix
+// state.  The in-chunk products take f16 operands (their 11 significant bits keep the rounding of
+// the features and of B below what the cancellation in dq amplifies): the key features scaled by
+// 2^-ek (the chunk's largest to [1/2, 1)), B row i by 2^-eb_i, and, so that U stays one sum, the
+// state image by 2^-ek and dO row i by 2^-eb_i.  Tensor memory per chunk (columns):
+//   P_K^T halves [0,128) [128,256) -> key features hi + lo in place (and f16 in shared memory)
+//   dS halves [256,320) [320,384), P_Q [0,256)
+//   U = dO S~^T [256,512) -> f16 Phi_Q over [0,64) [128,192)
+//   A [256,384), C [384,512) -> B = tril(C - go) over [384,416) [448,480)
+//   U = dO S~^T + B Phi_K [0,256), P_Q again [256,512) -> G hi over U, lo over P
+//   dq [64,128)
+template <int KIND>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+            const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ prefix,
+            const float* __restrict__ kshift, __nv_bfloat16* __restrict__ dq, float4* __restrict__ rowstat, int H,
+            int L, float s, Ranges R, int* err) {
+    constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1k(smem_raw);
+    const uint32_t s_w = smem_u32(sm);
+    const uint32_t s_img = s_w + kCbImgOff;
+    const uint32_t s_q = s_w + kCbTiles, s_k = s_q + kTileBytes, s_v = s_k + kTileBytes, s_do = s_v + kTileBytes;
+    const uint32_t s_phi = s_w + kCbPhi;
+    float* zv = reinterpret_cast<float*>(sm + kCbVec);                  // z of the chunk's prefix
+    float* kc = zv + kM;                                                 // key column terms
+    float* red = reinterpret_cast<float*>(sm + kCbTiles + kTileBytes);  // partials, in the K tile
+    float* redg = reinterpret_cast<float*>(sm + kCbPhi);                // gsum partials, in the features
+    CbBars* bars = reinterpret_cast<CbBars*>(sm + kCbBars);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = tid & (kTile - 1), ch = tid >> 7;
+    const int cta = blockIdx.x;
+    const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
+
+    cb_init(bars);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const float a = s * kLog2e;
+    CbPending pend;
+    int w_h = -1;
+    if (g0 < g1) {
+        w_h = (g0 / R.tph) % H;
+        if (tid == 0) {
+            cb_load_omega(&tm_w, sm, bars, w_h);
+            pend.w = 0;
+            for (int b = 0; b < 4; ++b) {
+                cb_load_tile(b == CB_Q ? &tm_q : b == CB_K ? &tm_k : b == CB_V ? &tm_v : &tm_do, sm, b, bars, g0, R.tph);
+                pend.tile[b] = 0;
+            }
+        }
+    }
+    bool w_wait = g0 < g1;
+    float srun[64];
+    float zrun = 0.f;
+    bool ok = true;
+    int cur_bh = -1;
+    uint32_t nw = 0, nmma = 0;
+    for (int g = g0, it = 0; g < g1; ++g, ++it) {
+        const int bh = g / R.tph, tile = g - bh * R.tph, h = bh % H;
+        const int tok0 = tile * kTile, tok = tok0 + row;
+        const bool live = tok < L;
+        const uint32_t tpar = (uint32_t)(it & 1);
+        const bool more = g + 1 < g1;
+        __syncthreads();   // the previous chunk is done with its buffers and tensor memory
+        if (bh != cur_bh) {
+            if (h != w_h) {
+                if (tid == 0) {
+                    cb_load_omega(&tm_w, sm, bars, h);
+                    pend.w = (int)(nw & 1);
+                }
+                w_h = h;
+                w_wait = true;
+            }
+            // the piece's prefix state, feature row tid
+            const float* pre = prefix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1)) +
+                               (size_t)tid * (kDV + 1);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) srun[c] = pre[c];
+            zrun = pre[kDV];
+            zv[tid] = zrun;
+            cur_bh = bh;
+            if (w_wait) {
+                ok = __syncthreads_and(mbar_wait(&bars->w, nw & 1, err, 60));
+                ++nw;
+                w_wait = false;
+                if (!ok) break;
+                pend.w = -1;
+            }
+        }
+        // ---- key projection (transposed) -> the chunk's scale, key features, their sums
+        ok = __syncthreads_and(mbar_wait(&bars->tile[CB_K], tpar, err, 61));
+        if (!ok) break;
+        pend.tile[CB_K] = -1;
+        if (tid == 0) {
+            tc_fence_after();
+            cb_project(tmem, s_w, s_k, 128);
+            cb_project(tmem + 128, s_w + 128 * 128, s_k, 128);
+            mma_commit(&bars->mma);
+        }
+        if (tid < kTile) {
+            const bool kl = tok0 + tid < L;
+            if (POS) kc[tid] = kl ? -(0.5f * s * s * row_sqnorm(s_k, (uint32_t)tid) + kshift[h]) * kLog2e : -INFINITY;
+            else kc[tid] = kl ? s : 0.f;
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 62));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        {
+            const float m = warp_max(cb_row_max_arg<KIND>(tl + 128 * ch, a, kc));
+            if (lane == 0) red[warp] = m;
+        }
+        __syncthreads();
+        int ek;
+        {
+            float m = red[0];
+#pragma unroll
+            for (int w8 = 1; w8 < 8; ++w8) m = fmaxf(m, red[w8]);
+            if (POS) ek = m > -1e30f ? max(-100, min(100, (int)ceilf(m))) : 0;
+            else ek = m > 0.f ? max(-100, min(100, ilog2f(m) + 1)) : 0;
+        }
+        __syncthreads();   // every thread has the scale before kc changes
+        if (tid < kTile) kc[tid] = POS ? kc[tid] - (float)ek : kc[tid] * exp2i(-ek);
+        __syncthreads();
+        const float sk = exp2i(ek);
+        float zc = 0.f;
+#pragma unroll 1
+        for (int u = 0; u < 2; ++u)
+            zc += cb_feature_row<KIND, true>(tl + 128 * ch + 64 * u, s_phi + (uint32_t)u * 2 * kPhiBlock,
+                                             (uint32_t)tid, a, kc + 64 * u, nullptr, sk, nullptr);
+        cb_write_image(s_img, (uint32_t)tid, srun, exp2i(-ek));   // S before this chunk, times 2^-ek
+        tmem_st_wait();
+        fence_async_smem();
+        tc_fence_before();
+        ok = __syncthreads_and(mbar_wait(&bars->tile[CB_Q], tpar, err, 63) &&
+                               mbar_wait(&bars->tile[CB_V], tpar, err, 58));
+        if (!ok) break;
+        pend.tile[CB_Q] = pend.tile[CB_V] = -1;
+        // ---- the chunk's state increment dS = Phi_K^T V (features hi + lo), the query projection
+        if (tid == 0) {
+            tc_fence_after();
+            cb_state_inc(tmem + 256, tmem + 320, tmem, tmem + 128, s_v);
+            issue_projection(tmem, s_q, s_w, 256);
+            mma_commit(&bars->mma);
+        }
+        uint4 qrow[4];
+#pragma unroll
+        for (uint32_t c4 = 0; c4 < 4; ++c4)
+            qrow[c4] = POS ? ld_shared_v4(s_q + sw128((uint32_t)row, 4 * (uint32_t)ch + c4)) : make_uint4(0, 0, 0, 0);
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 65));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        {
+            // feature row tid of the running state takes the chunk
+            uint32_t d0[32], d1[32];
+            tmem_ld32(tl + 256 + 64 * ch, d0);
+            tmem_ld32(tl + 288 + 64 * ch, d1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                srun[i] += __uint_as_float(d0[i]);
+                srun[32 + i] += __uint_as_float(d1[i]);
+            }
+            zrun += zc;
+        }
+        // the row's largest projection: exponent shift (positive) or f16 scale (ReLU)
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t pw[32];
+            tmem_ld32(tl + 128 * ch + 32 * cc, pw);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(pw[i]));
+        }
+        red[8 + ch * kTile + row] = mx;
+        tc_fence_before();
+        __syncthreads();
+        mx = fmaxf(red[8 + row], red[8 + kTile + row]);
+        const int eq = POS ? 0 : (s * mx > 0.f ? max(-100, min(100, ilog2f(s * mx) + 1)) : 0);
+        const float c = -mx * a;
+        ok = __syncthreads_and(mbar_wait(&bars->tile[CB_O], tpar, err, 64));
+        if (!ok) break;
+        pend.tile[CB_O] = -1;
+        if (tid == 0) {   // U = dO (2^-ek S~)^T
+            tc_fence_after();
+            cb_state_mult(tmem + 256, s_do, s_img);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 57));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        float den = 0.f, fu = 0.f;
+        {
+            const float q16 = exp2i(-eq);
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pw[32], uw[32];
+                tmem_ld32(tl + 128 * ch + 32 * cc, pw);
+                tmem_ld32(tl + 256 + 128 * ch + 32 * cc, uw);
+                tmem_ld_wait();
+                uint32_t fw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float f[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k = 2 * i + e;
+                        const float pv = __uint_as_float(pw[k]);
+                        f[e] = POS ? ex2(fmaf(pv, a, c)) : fmaxf(s * pv, 0.f);
+                        den = fmaf(f[e], zv[128 * ch + 32 * cc + k], den);
+                        fu = fmaf(f[e], __uint_as_float(uw[k]), fu);
+                    }
+                    fw[i] = pack_f16(f[0] * q16, f[1] * q16);
+                }
+                tmem_st16(tl + 128 * ch + 16 * cc, fw);
+            }
+            fu *= sk;   // U above carries 2^-ek
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncthreads();
+        // ---- A = Phi_Q Phi_K^T (f16, scaled 2^-(ek + eq_i)), C = dO V^T
+        if (tid == 0) {
+            tc_fence_after();
+            cb_scores<true>(tmem + 256, tmem, tmem + 128, s_phi);
+            cb_project(tmem + 384, s_do, s_v, 128);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 66));
+        ++nmma;
+        if (!ok) break;
+        if (tid == 0 && more) {
+            cb_load_tile(&tm_v, sm, CB_V, bars, g + 1, R.tph);
+            pend.tile[CB_V] = (int)(tpar ^ 1);
+        }
+        tc_fence_after();
+        {
+            const float ascale = exp2i(ek) * exp2i(eq);
+            float dpart = 0.f, fpart = 0.f;
+#pragma unroll 1
+            for (int blk = 0; blk < 2; ++blk) {
+                // keys 64 ch + 32 blk .. +31 of row `row`: the masked sums
+                uint32_t av[32], cv[32];
+                tmem_ld32(tl + 256 + 64 * ch + 32 * blk, av);
+                tmem_ld32(tl + 384 + 64 * ch + 32 * blk, cv);
+                tmem_ld_wait();
+                const int j0 = 64 * ch + 32 * blk;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    if (j0 + k <= row) {
+                        const float av_k = __uint_as_float(av[k]);
+                        dpart += av_k;
+                        fpart = fmaf(av_k, __uint_as_float(cv[k]), fpart);
+                    }
+                }
+            }
+            den = fmaf(dpart, ascale, den);
+            fu = fmaf(fpart, ascale, fu);
+        }
+        red[8 + 2 * kTile + ch * kTile + row] = den;
+        red[8 + 4 * kTile + ch * kTile + row] = fu;
+        __syncthreads();
+        den = red[8 + 2 * kTile + row] + red[8 + 3 * kTile + row];
+        fu = red[8 + 4 * kTile + row] + red[8 + 5 * kTile + row];
+        const float inv = den != 0.f ? 1.f / den : 0.f;
+        const float go = fu * inv;
+        if (live && ch == 0) rowstat[(size_t)bh * L + tok] = make_float4(den, POS ? s * mx : 0.f, go, (float)eq);
+        uint32_t c0[32], c1[32];
+        tmem_ld32(tl + 384 + 64 * ch, c0);
+        tmem_ld32(tl + 384 + 64 * ch + 32, c1);
+        tmem_ld_wait();
+        {
+            // the row's largest |C - go| over the keys it sees -> f16 scale of B (and of dO row)
+            float bm = 0.f;
+            const int j0 = 64 * ch;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                if (j0 + k <= row) bm = fmaxf(bm, fabsf(__uint_as_float(c0[k]) - go));
+                if (j0 + 32 + k <= row) bm = fmaxf(bm, fabsf(__uint_as_float(c1[k]) - go));
+            }
+            red[8 + 6 * kTile + ch * kTile + row] = bm;
+        }
+        __syncthreads();
+        const int eb = f16_scale_exp(fmaxf(red[8 + 6 * kTile + row], red[8 + 7 * kTile + row]));
+        fence_async_smem();   // the K tile's next load follows these generic accesses
+        {
+            // B = tril(C - go) 2^-eb for keys 64 ch .. +63, f16, over the row's first 32 C columns;
+            // this row's dO (columns 32 ch .. +31) times 2^-eb in place
+            const float bs = exp2i(-eb);
+            uint32_t b0[16], b1[16];
+            const int j0 = 64 * ch;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                b0[i] = pack_f16(j0 + 2 * i <= row ? (__uint_as_float(c0[2 * i]) - go) * bs : 0.f,
+                                 j0 + 2 * i + 1 <= row ? (__uint_as_float(c0[2 * i + 1]) - go) * bs : 0.f);
+                b1[i] = pack_f16(j0 + 32 + 2 * i <= row ? (__uint_as_float(c1[2 * i]) - go) * bs : 0.f,
+                                 j0 + 33 + 2 * i <= row ? (__uint_as_float(c1[2 * i + 1]) - go) * bs : 0.f);
+            }
+            tmem_st16(tl + 384 + 64 * ch, b0);
+            tmem_st16(tl + 384 + 64 * ch + 16, b1);
+#pragma unroll
+            for (uint32_t c4 = 0; c4 < 4; ++c4) {
+                const uint32_t addr = s_do + sw128((uint32_t)row, 4 * (uint32_t)ch + c4);
+                const uint4 x = ld_shared_v4(addr);
+                const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
+                uint32_t y[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) y[i] = pack_bf16(bf16lo(xin[i]) * bs, bf16hi(xin[i]) * bs);
+                st_shared_v4(addr, y[0], y[1], y[2], y[3]);
+            }
+            fence_async_smem();
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- U = dO' S~'^T + B' Phi_K' (= 2^-(ek + eb_i) U), the query projection again
+        if (tid == 0) {
+            tc_fence_after();
+            cb_state_mult(tmem, s_do, s_img);
+            cb_weighted_features(tmem, tmem + 384, tmem + 448, s_phi);
+            issue_projection(tmem + 256, s_q, s_w, 256);
+            mma_commit(&bars->mma);
+            if (more) {
+                cb_load_tile(&tm_k, sm, CB_K, bars, g + 1, R.tph);
+                pend.tile[CB_K] = (int)(tpar ^ 1);
+            }
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 67));
+        ++nmma;
+        if (!ok) break;
+        if (tid == 0 && more) {
+            cb_load_tile(&tm_q, sm, CB_Q, bars, g + 1, R.tph);
+            cb_load_tile(&tm_do, sm, CB_O, bars, g + 1, R.tph);
+            pend.tile[CB_Q] = pend.tile[CB_O] = (int)(tpar ^ 1);
+        }
+        tc_fence_after();
+        float gsum = 0.f;
+        {
+            const float us = exp2i(ek) * exp2i(eb);
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pw[32], uw[32];
+                tmem_ld32(tl + 256 + 128 * ch + 32 * cc, pw);
+                tmem_ld32(tl + 128 * ch + 32 * cc, uw);
+                tmem_ld_wait();
+                uint32_t hw[16], lw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float gg[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k = 2 * i + e;
+                        const float pv = __uint_as_float(pw[k]);
+                        const float dphi = fmaf(__uint_as_float(uw[k]), us, -zv[128 * ch + 32 * cc + k] * go) * inv;
+                        const float gv = POS ? dphi * ex2(fmaf(pv, a, c)) : (pv > 0.f ? dphi : 0.f);
+                        gg[e] = gv;
+                        gsum += gv;
+                    }
+                    split_pack(gg[0], gg[1], hw[i], lw[i]);
+                }
+                tmem_st16(tl + 128 * ch + 16 * cc, hw);
+                tmem_st16(tl + 256 + 128 * ch + 16 * cc, lw);
+            }
+        }
+        tmem_st_wait();
+        redg[ch * kTile + row] = gsum;
+        tc_fence_before();
+        __syncthreads();
+        // ---- dq = G omega
+        if (tid == 0) {
+            tc_fence_after();
+            cb_grad_omega(tmem + 64, tmem, tmem + 128, tmem + 256, tmem + 384, s_w);
+            mma_commit(&bars->mma);
+        }
+        zv[tid] = zrun;   // z of the next chunk's prefix (the current one is read)
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 68));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        gsum = redg[row] + redg[kTile + row];
+        cb_store_grad<KIND>(live ? dq + ((size_t)bh * L + tok) * kD : nullptr, tl + 64 + 32 * ch, ch, s, gsum, qrow);
+        tc_fence_before();
+    }
+    if (!ok && tid == 0) pend.drain(bars, err, 69);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// Key pass for dk, persistent over the call's tile ranges in reverse (grid R.G, 256 threads).
+// Thread t is key row t % 128 with features 128 (t / 128) .. +127 of it, and feature row t of the
+// query features and of the running suffix state.  The in-chunk term W Phi~_Q takes f16 operands:
+// the query features f as the query pass scaled them (2^-eq_i; positive: f <= 1), W_ji = (C_ji -
+// go_i) 2^eq_i / den_i times 2^-ew_j (the row's largest to [2^13, 2^14)), and V row j times
+// 2^-ew_j so that U stays one sum.  Tensor memory per chunk (columns):
+//   P_Q^T halves [256,384) [384,512) -> query features hi + lo in place (and f16 in shared memory)
+//   dT halves [0,64) [64,128), C^T = V dO^T [128,256) -> W over [128,160) [192,224)
+//   U = V T~^T + W Phi~_Q [256,512), P_K [0,256) -> G hi over U, lo over P
+//   dk [64,128)
+template <int KIND>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+k_tc_cbwd_k(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+            const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ suffix,
+            const float* __restrict__ kshift, const float4* __restrict__ rowstat, __nv_bfloat16* __restrict__ dk,
+            int H, int L, float s, Ranges R, int* err) {
+    constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1k(smem_raw);
+    const uint32_t s_w = smem_u32(sm);
+    const uint32_t s_img = s_w + kCbImgOff;
+    const uint32_t s_q = s_w + kCbTiles, s_k = s_q + kTileBytes, s_v = s_k + kTileBytes, s_do = s_v + kTileBytes;
+    const uint32_t s_phi = s_w + kCbPhi;
+    float* tv = reinterpret_cast<float*>(sm + kCbVec);                 // t of the chunk's suffix
+    float* qs = reinterpret_cast<float*>(sm + kCbTiles);               // query terms [3][128], W scales [2][128]
+    float* redg = reinterpret_cast<float*>(sm + kCbPhi);               // gsum partials, in the features
+    CbBars* bars = reinterpret_cast<CbBars*>(sm + kCbBars);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int row = tid & (kTile - 1), ch = tid >> 7;
+    const int cta = blockIdx.x;
+    const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
+
+    cb_init(bars);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const float a = s * kLog2e;
+    CbPending pend;
+    int w_h = -1;
+    if (g0 < g1) {
+        w_h = ((g1 - 1) / R.tph) % H;
+        if (tid == 0) {
+            cb_load_omega(&tm_w, sm, bars, w_h);
+            pend.w = 0;
+            for (int b = 0; b < 4; ++b) {
+                cb_load_tile(b == CB_Q ? &tm_q : b == CB_K ? &tm_k : b == CB_V ? &tm_v : &tm_do, sm, b, bars, g1 - 1,
+                             R.tph);
+                pend.tile[b] = 0;
+            }
+        }
+    }
+    bool w_wait = g0 < g1;
+    float trun[64];
+    float tz = 0.f;
+    bool ok = true;
+    int cur_bh = -1;
+    uint32_t nw = 0, nmma = 0;
+    for (int g = g1 - 1, it = 0; g >= g0; --g, ++it) {
+        const int bh = g / R.tph, tile = g - bh * R.tph, h = bh % H;
+        const int tok0 = tile * kTile, tok = tok0 + row;
+        const bool live = tok < L;
+        const uint32_t tpar = (uint32_t)(it & 1);
+        const bool more = g > g0;
+        __syncthreads();   // the previous chunk is done with its buffers and tensor memory
+        if (bh != cur_bh) {
+            if (h != w_h) {
+                if (tid == 0) {
+                    cb_load_omega(&tm_w, sm, bars, h);
+                    pend.w = (int)(nw & 1);
+                }
+                w_h = h;
+                w_wait = true;
+            }
+            // the piece's suffix state, feature row tid
+            const float* suf = suffix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1)) +
+                               (size_t)tid * (kDV + 1);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) trun[c] = suf[c];
+            tz = suf[kDV];
+            cb_write_image(s_img, (uint32_t)tid, trun, 1.f);
+            tv[tid] = tz;
+            fence_async_smem();
+            cur_bh = bh;
+            if (w_wait) {
+                ok = __syncthreads_and(mbar_wait(&bars->w, nw & 1, err, 70));
+                ++nw;
+                w_wait = false;
+                if (!ok) break;
+                pend.w = -1;
+            }
+        }
+        // ---- the transposed query projection -> query features
+        ok = __syncthreads_and(mbar_wait(&bars->tile[CB_Q], tpar, err, 71) &&
+                               mbar_wait(&bars->tile[CB_K], tpar, err, 72));
+        if (!ok) break;
+        pend.tile[CB_Q] = pend.tile[CB_K] = -1;
+        if (tid == 0) {
+            tc_fence_after();
+            cb_project(tmem + 256, s_w, s_q, 128);
+            cb_project(tmem + 384, s_w + 128 * 128, s_q, 128);
+            mma_commit(&bars->mma);
+        }
+        // query terms of token tok0 + tid (tid < 128): exponent offset (positive) or f16 scale
+        // (ReLU) of the query pass, 2^eq / den, -go; zero for tokens past L and zero denominators
+        float qoff = POS ? -INFINITY : 0.f, qmt = 0.f, qgo = 0.f;
+        if (tid < kTile && tok0 + tid < L) {
+            const float4 rs = rowstat[(size_t)bh * L + tok0 + tid];
+            const int eq = (int)rs.w;
+            qoff = POS ? -rs.y * kLog2e : s * exp2i(-eq);
+            qmt = rs.x != 0.f ? exp2i(eq) / rs.x : 0.f;
+            qgo = rs.z;
+        }
+        // this key row: exponent offset (or ReLU scale) and, for the epilogue, its half of k
+        const float kc = live ? (POS ? -(0.5f * s * s * row_sqnorm(s_k, (uint32_t)row) + kshift[h]) * kLog2e : s)
+                              : (POS ? -INFINITY : 0.f);
+        uint4 krow[4];
+#pragma unroll
+        for (uint32_t c4 = 0; c4 < 4; ++c4)
+            krow[c4] = POS ? ld_shared_v4(s_k + sw128((uint32_t)row, 4 * (uint32_t)ch + c4)) : make_uint4(0, 0, 0, 0);
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 73));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        if (tid < kTile) {   // the Q tile is read: it holds the query terms until the next load
+            qs[tid] = qoff;
+            qs[kTile + tid] = qmt;
+            qs[2 * kTile + tid] = -qgo;
+        }
+        __syncthreads();
+        float tzc = 0.f;
+#pragma unroll 1
+        for (int u = 0; u < 2; ++u)
+            tzc += cb_feature_row<KIND, true>(tl + 256 + 128 * ch + 64 * u, s_phi + (uint32_t)u * 2 * kPhiBlock,
+                                              (uint32_t)tid, a, qs + 64 * u, qs + kTile + 64 * u, 1.f,
+                                              qs + 2 * kTile + 64 * u);
+        tmem_st_wait();
+        fence_async_smem();
+        tc_fence_before();
+        ok = __syncthreads_and(mbar_wait(&bars->tile[CB_V], tpar, err, 78) &&
+                               mbar_wait(&bars->tile[CB_O], tpar, err, 78));
+        if (!ok) break;
+        pend.tile[CB_V] = pend.tile[CB_O] = -1;
+        // ---- dT = Phi~_Q^T dO (features hi + lo), C^T = V dO^T
+        if (tid == 0) {
+            tc_fence_after();
+            cb_state_inc(tmem, tmem + 64, tmem + 256, tmem + 384, s_do);
+            cb_project(tmem + 128, s_v, s_do, 128);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 74));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        {
+            uint32_t d0[32], d1[32];
+            tmem_ld32(tl + 64 * ch, d0);
+            tmem_ld32(tl + 32 + 64 * ch, d1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                trun[i] += __uint_as_float(d0[i]);
+                trun[32 + i] += __uint_as_float(d1[i]);
+            }
+            tz += tzc;
+        }
+        // queries 64 ch .. +63 of key row `row`: W = tril(C^T - go) 2^eq / den, its row scale
+        const uint32_t tcw = tl + 128 + 64 * ch;
+        uint32_t x0[32], x1[32];
+        tmem_ld32(tcw, x0);
+        tmem_ld32(tcw + 32, x1);
+        tmem_ld_wait();
+        const int i0 = 64 * ch;
+        {
+            const float* ngo = qs + 2 * kTile + i0;
+            const float* mt = qs + kTile + i0;
+            float bm = 0.f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float w0 = i0 + k >= row ? (__uint_as_float(x0[k]) + ngo[k]) * mt[k] : 0.f;
+                const float w1 = i0 + 32 + k >= row ? (__uint_as_float(x1[k]) + ngo[32 + k]) * mt[32 + k] : 0.f;
+                x0[k] = __float_as_uint(w0);
+                x1[k] = __float_as_uint(w1);
+                bm = fmaxf(bm, fmaxf(fabsf(w0), fabsf(w1)));
+            }
+            qs[3 * kTile + ch * kTile + row] = bm;
+        }
+        __syncthreads();
+        const int ew = f16_scale_exp(fmaxf(qs[3 * kTile + row], qs[4 * kTile + row]));
+        {
+            const float ws = exp2i(-ew);
+            uint32_t w0[16], w1[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                w0[i] = pack_f16(__uint_as_float(x0[2 * i]) * ws, __uint_as_float(x0[2 * i + 1]) * ws);
+                w1[i] = pack_f16(__uint_as_float(x1[2 * i]) * ws, __uint_as_float(x1[2 * i + 1]) * ws);
+            }
+            tmem_st16(tcw, w0);
+            tmem_st16(tcw + 16, w1);
+            // this key row's v (columns 32 ch .. +31) times 2^-ew in place
+#pragma unroll
+            for (uint32_t c4 = 0; c4 < 4; ++c4) {
+                const uint32_t addr = s_v + sw128((uint32_t)row, 4 * (uint32_t)ch + c4);
+                const uint4 x = ld_shared_v4(addr);
+                const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
+                uint32_t y[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) y[i] = pack_bf16(bf16lo(xin[i]) * ws, bf16hi(xin[i]) * ws);
+                st_shared_v4(addr, y[0], y[1], y[2], y[3]);
+            }
+            fence_async_smem();
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- U = V' T~^T + W' Phi~_Q (= 2^-ew_j U), the key projection
+        if (tid == 0) {
+            tc_fence_after();
+            if (more) {   // the query terms are read
+                cb_load_tile(&tm_q, sm, CB_Q, bars, g - 1, R.tph);
+                pend.tile[CB_Q] = (int)(tpar ^ 1);
+            }
+            cb_state_mult(tmem + 256, s_v, s_img);
+            cb_weighted_features(tmem + 256, tmem + 128, tmem + 192, s_phi);
+            issue_projection(tmem, s_k, s_w, 256);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 75));
+        ++nmma;
+        if (!ok) break;
+        if (tid == 0 && more) {
+            cb_load_tile(&tm_k, sm, CB_K, bars, g - 1, R.tph);
+            cb_load_tile(&tm_v, sm, CB_V, bars, g - 1, R.tph);
+            cb_load_tile(&tm_do, sm, CB_O, bars, g - 1, R.tph);
+            pend.tile[CB_K] = pend.tile[CB_V] = pend.tile[CB_O] = (int)(tpar ^ 1);
+        }
+        tc_fence_after();
+        float gsum = 0.f;
+        {
+            const float us = exp2i(ew);
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pw[32], uw[32];
+                tmem_ld32(tl + 128 * ch + 32 * cc, pw);
+                tmem_ld32(tl + 256 + 128 * ch + 32 * cc, uw);
+                tmem_ld_wait();
+                uint32_t hw[16], lw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float gg[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k = 2 * i + e;
+                        const float pv = __uint_as_float(pw[k]);
+                        const float dphi = fmaf(__uint_as_float(uw[k]), us, tv[128 * ch + 32 * cc + k]);
+                        const float gv = POS ? dphi * ex2(fmaf(pv, a, kc)) : (pv * kc > 0.f ? dphi : 0.f);
+                        gg[e] = gv;
+                        gsum += gv;
+                    }
+                    split_pack(gg[0], gg[1], hw[i], lw[i]);
+                }
+                tmem_st16(tl + 256 + 128 * ch + 16 * cc, hw);
+                tmem_st16(tl + 128 * ch + 16 * cc, lw);
+            }
+        }
+        tmem_st_wait();
+        cb_write_image(s_img, (uint32_t)tid, trun, 1.f);   // the previous chunk's suffix
+        fence_async_smem();
+        redg[ch * kTile + row] = gsum;
+        tc_fence_before();
+        __syncthreads();
+        // ---- dk = G omega
+        if (tid == 0) {
+            tc_fence_after();
+            cb_grad_omega(tmem + 64, tmem + 256, tmem + 384, tmem, tmem + 128, s_w);
+            mma_commit(&bars->mma);
+        }
+        tv[tid] = tz;   // t of the previous chunk's suffix (the current one is read)
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 77));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        gsum = redg[row] + redg[kTile + row];
+        cb_store_grad<KIND>(live ? dk + ((size_t)bh * L + tok) * kD : nullptr, tl + 64 + 32 * ch, ch, s, gsum, krow);
+        tc_fence_before();
+    }
+    if (!ok && tid == 0) pend.drain(bars, err, 79);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// Key pass for dv (bf16 operands: dv subtracts nothing), persistent over the call's tile ranges in
+// reverse (grid R.G, 256 threads), the same thread roles.  Tensor memory per chunk (columns):
+//   P_K [0,256), P_Q^T halves [256,384) [384,512) -> packed Phi_K over [0,64) [128,192), scaled
+//       query features hi + lo in place (and bf16 in shared memory)
+//   dT halves [64,128) [192,256), A^T = Phi_K Phi~_Q^T [256,384) -> tril over [256,288) [320,352)
+//   dv [64,128)
+template <int KIND>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+k_tc_cbwd_v(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_w,
+            const float* __restrict__ suffix, const float* __restrict__ kshift, const float4* __restrict__ rowstat,
+            __nv_bfloat16* __restrict__ dvv, int H, int L, float s, Ranges R, int* err) {
+    constexpr bool POS = KIND == FAVOR_KERNEL_SOFTMAX_POS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1k(smem_raw);
+    const uint32_t s_w = smem_u32(sm);
+    const uint32_t s_img = s_w + kCbImgOff;
+    const uint32_t s_q = s_w + kCbTiles, s_k = s_q + kTileBytes, s_do = s_k + 2 * kTileBytes;
+    const uint32_t s_phi = s_w + kCbPhi;
+    float* qs = reinterpret_cast<float*>(sm + kCbTiles);               // query terms [128], in the Q tile
+    CbBars* bars = reinterpret_cast<CbBars*>(sm + kCbBars);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int row = tid & (kTile - 1), ch = tid >> 7;
+    const int cta = blockIdx.x;
+    const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
+
+    cb_init(bars);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const float a = s * kLog2e;
+    CbPending pend;
+    int w_h = -1;
+    if (g0 < g1) {
+        w_h = ((g1 - 1) / R.tph) % H;
+        if (tid == 0) {
+            cb_load_omega(&tm_w, sm, bars, w_h);
+            pend.w = 0;
+            cb_load_tile(&tm_q, sm, CB_Q, bars, g1 - 1, R.tph);
+            cb_load_tile(&tm_k, sm, CB_K, bars, g1 - 1, R.tph);
+            cb_load_tile(&tm_do, sm, CB_O, bars, g1 - 1, R.tph);
+            pend.tile[CB_Q] = pend.tile[CB_K] = pend.tile[CB_O] = 0;
+        }
+    }
+    bool w_wait = g0 < g1;
+    float trun[64];
+    bool ok = true;
+    int cur_bh = -1;
+    uint32_t nw = 0, nmma = 0;
+    for (int g = g1 - 1, it = 0; g >= g0; --g, ++it) {
+        const int bh = g / R.tph, tile = g - bh * R.tph, h = bh % H;
+        const int tok0 = tile * kTile, tok = tok0 + row;
+        const bool live = tok < L;
+        const uint32_t tpar = (uint32_t)(it & 1);
+        const bool more = g > g0;
+        __syncthreads();   // the previous chunk is done with its buffers and tensor memory
+        if (bh != cur_bh) {
+            if (h != w_h) {
+                if (tid == 0) {
+                    cb_load_omega(&tm_w, sm, bars, h);
+                    pend.w = (int)(nw & 1);
+                }
+                w_h = h;
+                w_wait = true;
+            }
+            const float* suf = suffix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1)) +
+                               (size_t)tid * (kDV + 1);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) trun[c] = suf[c];
+            cb_write_image(s_img, (uint32_t)tid, trun, 1.f);
+            fence_async_smem();
+            cur_bh = bh;
+            if (w_wait) {
+                ok = __syncthreads_and(mbar_wait(&bars->w, nw & 1, err, 80));
+                ++nw;
+                w_wait = false;
+                if (!ok) break;
+                pend.w = -1;
+            }
+        }
+        // ---- key projection and the transposed query projection
+        ok = __syncthreads_and(mbar_wait(&bars->tile[CB_Q], tpar, err, 81) &&
+                               mbar_wait(&bars->tile[CB_K], tpar, err, 82));
+        if (!ok) break;
+        pend.tile[CB_Q] = pend.tile[CB_K] = -1;
+        if (tid == 0) {
+            tc_fence_after();
+            issue_projection(tmem, s_k, s_w, 256);
+            cb_project(tmem + 256, s_w, s_q, 128);
+            cb_project(tmem + 384, s_w + 128 * 128, s_q, 128);
+            mma_commit(&bars->mma);
+        }
+        // query term of token tok0 + tid (tid < 128): phi~ = phi / den directly, through the
+        // exponent offset (positive) or the scale (ReLU); zero past L and for zero denominators
+        float qoff = POS ? -INFINITY : 0.f;
+        if (tid < kTile && tok0 + tid < L) {
+            const float4 rs = rowstat[(size_t)bh * L + tok0 + tid];
+            if (rs.x > 0.f) qoff = POS ? -rs.y * kLog2e - log2f(rs.x) : s / rs.x;
+        }
+        const float kc = live ? (POS ? -(0.5f * s * s * row_sqnorm(s_k, (uint32_t)row) + kshift[h]) * kLog2e : s)
+                              : (POS ? -INFINITY : 0.f);
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 83));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        if (tid < kTile) qs[tid] = qoff;   // the Q tile is read
+        __syncthreads();
+#pragma unroll 1
+        for (int u = 0; u < 2; ++u)
+            cb_feature_row<KIND, false>(tl + 256 + 128 * ch + 64 * u, s_phi + (uint32_t)u * 2 * kPhiBlock,
+                                        (uint32_t)tid, a, qs + 64 * u, nullptr, 1.f, nullptr);
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t pw[32];
+            tmem_ld32(tl + 128 * ch + 32 * cc, pw);
+            tmem_ld_wait();
+            uint32_t fw[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float p0 = __uint_as_float(pw[2 * i]), p1 = __uint_as_float(pw[2 * i + 1]);
+                fw[i] = POS ? pack_bf16(ex2(fmaf(p0, a, kc)), ex2(fmaf(p1, a, kc)))
+                            : pack_bf16(fmaxf(p0 * kc, 0.f), fmaxf(p1 * kc, 0.f));
+            }
+            tmem_st16(tl + 128 * ch + 16 * cc, fw);
+        }
+        tmem_st_wait();
+        fence_async_smem();
+        tc_fence_before();
+        ok = __syncthreads_and(mbar_wait(&bars->tile[CB_O], tpar, err, 84));
+        if (!ok) break;
+        pend.tile[CB_O] = -1;
+        // ---- dT = Phi~_Q^T dO (features hi + lo), A^T = Phi_K Phi~_Q^T
+        if (tid == 0) {
+            tc_fence_after();
+            if (more) {   // the query terms are read
+                cb_load_tile(&tm_q, sm, CB_Q, bars, g - 1, R.tph);
+                pend.tile[CB_Q] = (int)(tpar ^ 1);
+            }
+            cb_state_inc(tmem + 64, tmem + 192, tmem + 256, tmem + 384, s_do);
+            cb_scores<false>(tmem + 256, tmem, tmem + 128, s_phi);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 85));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        {
+            uint32_t d0[32], d1[32];
+            tmem_ld32(tl + 64 + 128 * ch, d0);
+            tmem_ld32(tl + 96 + 128 * ch, d1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                trun[i] += __uint_as_float(d0[i]);
+                trun[32 + i] += __uint_as_float(d1[i]);
+            }
+        }
+        {
+            // tril(A^T) for queries 64 ch .. +63 of key row `row`, packed in place
+            const uint32_t ta = tl + 256 + 64 * ch;
+            uint32_t x0[32], x1[32];
+            tmem_ld32(ta, x0);
+            tmem_ld32(ta + 32, x1);
+            tmem_ld_wait();
+            const int i0 = 64 * ch;
+            uint32_t w0[16], w1[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                w0[i] = pack_bf16(i0 + 2 * i >= row ? __uint_as_float(x0[2 * i]) : 0.f,
+                                  i0 + 2 * i + 1 >= row ? __uint_as_float(x0[2 * i + 1]) : 0.f);
+                w1[i] = pack_bf16(i0 + 32 + 2 * i >= row ? __uint_as_float(x1[2 * i]) : 0.f,
+                                  i0 + 33 + 2 * i >= row ? __uint_as_float(x1[2 * i + 1]) : 0.f);
+            }
+            tmem_st16(ta, w0);
+            tmem_st16(ta + 16, w1);
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- dv = Phi_K T~ + tril(A^T) dO
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id_o = make_idesc(128, 64, 0, 1);
+            const uint64_t bth = make_desc(s_img, 8192, 1024, SW_128B), btl = make_desc(s_img + kSBytes, 8192, 1024, SW_128B);
+            const uint64_t bdo = make_desc(s_do, 8192, 1024, SW_128B);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                mma_ts(tmem + 64, kk < 8 ? tmem + 8 * kk : tmem + 128 + 8 * (kk - 8), bth + 128 * kk, id_o, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                mma_ts(tmem + 64, kk < 8 ? tmem + 8 * kk : tmem + 128 + 8 * (kk - 8), btl + 128 * kk, id_o, 1u);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ts(tmem + 64, tmem + 256 + 64 * (kk >> 2) + 8 * (kk & 3), bdo + 128 * kk, id_o, 1u);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 86));
+        ++nmma;
+        if (!ok) break;
+        if (tid == 0 && more) {
+            cb_load_tile(&tm_k, sm, CB_K, bars, g - 1, R.tph);
+            cb_load_tile(&tm_do, sm, CB_O, bars, g - 1, R.tph);
+            pend.tile[CB_K] = pend.tile[CB_O] = (int)(tpar ^ 1);
+        }
+        tc_fence_after();
+        {
+            uint32_t v0[32];
+            tmem_ld32(tl + 64 + 32 * ch, v0);
+            tmem_ld_wait();
+            if (live) {
+                uint4* dst = reinterpret_cast<uint4*>(dvv + ((size_t)bh * L + tok) * kDV);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        wv[i] = pack_bf16(__uint_as_float(v0[8 * c4 + 2 * i]), __uint_as_float(v0[8 * c4 + 2 * i + 1]));
+                    dst[4 * ch + c4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+            }
+        }
+        cb_write_image(s_img, (uint32_t)tid, trun, 1.f);   // the previous chunk's suffix
+        fence_async_smem();
+        tc_fence_before();
+    }
+    if (!ok && tid == 0) pend.drain(bars, err, 89);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// In place, per head: piece p <- the sum of the pieces before it (REV false) or after it (REV
+// true), fixed order.  grid (m (dv+1) / 256 up, B*H).
+template <bool REV>
+__global__ void k_piece_scan(float* __restrict__ part, Ranges R) {
+    constexpr int n = kM * (kDV + 1);
+    const int bh = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int np = last_cta(R, bh) - first_cta(R, bh) + 1;
+    float* p = part + (size_t)bh * R.pstride * n + i;
+    float run = 0.f;
+    for (int k = 0; k < np; ++k) {
+        const int q = REV ? np - 1 - k : k;
+        const float t = p[(size_t)q * n];
+        p[(size_t)q * n] = run;
+        run += t;
+    }
+}
+
 // ================================================================ host side
 // the state kernel asks for more than half an SM's shared memory so that two
 // CTAs (each allocating all 512 tensor-memory columns) never share an SM
@@ -794,6 +2031,71 @@ favor_status tc_bidir_backward_t(const Handle& h, const CUtensorMap& mq, const C
     return check_launch("backward key kernel");
 }
 
+constexpr size_t kSmemCb = 1024 + kCbBars + sizeof(CbBars);
+static_assert(kSmemCb <= 232448, "causal backward shared memory");
+static_assert(3 * kTile * 4 <= kTileBytes && 6 * kTile * 4 <= kTileBytes, "row partials fit a tile buffer");
+
+void allow_cbwd_once() {
+    static std::once_flag once;
+    std::call_once(once, [] {
+        allow_smem(k_tc_cbwd_q<FAVOR_KERNEL_SOFTMAX_POS>, kSmemCb);
+        allow_smem(k_tc_cbwd_q<FAVOR_KERNEL_RELU>, kSmemCb);
+        allow_smem(k_tc_cbwd_k<FAVOR_KERNEL_SOFTMAX_POS>, kSmemCb);
+        allow_smem(k_tc_cbwd_k<FAVOR_KERNEL_RELU>, kSmemCb);
+        allow_smem(k_tc_cbwd_v<FAVOR_KERNEL_SOFTMAX_POS>, kSmemCb);
+        allow_smem(k_tc_cbwd_v<FAVOR_KERNEL_RELU>, kSmemCb);
+        cudaGetLastError();
+    });
+}
+
+template <int KIND>
+favor_status tc_causal_backward_t(const Handle& h, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                  const CUtensorMap& mdo, const CUtensorMap& mw, void* dq, void* dk, void* dv, int BH,
+                                  int L, const Ranges& R, cudaStream_t st) {
+    float4* rowstat = reinterpret_cast<float4*>(h.ws_rowstat);
+    const dim3 sgrid((kM * (kDV + 1) + 255) / 256, BH);
+    favor_status e;
+    {
+        ProfScope ps(h, PROF_STATE, st);
+        k_tc_bstate<KIND, 0><<<R.G, kBStateThreads, kSmemBState, st>>>(mk, mv, mw, h.kshift, nullptr, h.ws_partial,
+                                                                         h.H, L, h.s, R, h.dev_err);
+        count_launch();
+        if ((e = check_launch("backward state kernel")) != FAVOR_OK) return e;
+    }
+    {
+        ProfScope ps(h, PROF_COMBINE, st);
+        k_piece_scan<false><<<sgrid, 256, 0, st>>>(h.ws_partial, R);
+        count_launch();
+        if ((e = check_launch("backward prefix scan kernel")) != FAVOR_OK) return e;
+    }
+    {
+        ProfScope ps(h, PROF_BWD_QUERY, st);
+        k_tc_cbwd_q<KIND><<<R.G, kBwdThreads, kSmemCb, st>>>(mq, mk, mv, mdo, mw, h.ws_partial, h.kshift,
+                                                               (__nv_bfloat16*)dq, rowstat, h.H, L, h.s, R, h.dev_err);
+        count_launch();
+        if ((e = check_launch("causal backward query kernel")) != FAVOR_OK) return e;
+        k_tc_bstate<KIND, 1><<<R.G, kBStateThreads, kSmemBState, st>>>(mq, mdo, mw, h.kshift, rowstat, h.ws_partial,
+                                                                         h.H, L, h.s, R, h.dev_err);
+        count_launch();
+        if ((e = check_launch("backward query-state kernel")) != FAVOR_OK) return e;
+    }
+    {
+        ProfScope ps(h, PROF_COMBINE, st);
+        k_piece_scan<true><<<sgrid, 256, 0, st>>>(h.ws_partial, R);
+        count_launch();
+        if ((e = check_launch("backward suffix scan kernel")) != FAVOR_OK) return e;
+    }
+    ProfScope ps(h, PROF_BWD_KEY, st);
+    k_tc_cbwd_k<KIND><<<R.G, kBwdThreads, kSmemCb, st>>>(mq, mk, mv, mdo, mw, h.ws_partial, h.kshift, rowstat,
+                                                           (__nv_bfloat16*)dk, h.H, L, h.s, R, h.dev_err);
+    count_launch();
+    if ((e = check_launch("causal backward key kernel")) != FAVOR_OK) return e;
+    k_tc_cbwd_v<KIND><<<R.G, kBwdThreads, kSmemCb, st>>>(mq, mk, mdo, mw, h.ws_partial, h.kshift, rowstat,
+                                                           (__nv_bfloat16*)dv, h.H, L, h.s, R, h.dev_err);
+    count_launch();
+    return check_launch("causal backward value kernel");
+}
+
 }  // namespace
 
 size_t tc_bwd_image_bytes(size_t BH) { return BH * kBImg; }
@@ -815,6 +2117,26 @@ favor_status tc_bidir_backward(const Handle& h, const void* q, const void* k, co
     if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
         return tc_bidir_backward_t<FAVOR_KERNEL_SOFTMAX_POS>(h, mq, mk, mv, mdo, mw, dq, dk, dv, BH, L, R, st);
     return tc_bidir_backward_t<FAVOR_KERNEL_RELU>(h, mq, mk, mv, mdo, mw, dq, dk, dv, BH, L, R, st);
+}
+
+favor_status tc_causal_backward(const Handle& h, const void* q, const void* k, const void* v, const void* dout,
+                                void* dq, void* dk, void* dv, int B, int L, cudaStream_t st) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv))
+        return simt_causal_backward(h, q, k, v, dout, dq, dk, dv, B, L, st);
+    allow_bwd_once();
+    allow_cbwd_once();
+    const int BH = B * h.H;
+    const Ranges R = plan_ranges(BH, L, h.num_sms);
+    if ((size_t)BH * R.pstride > h.ws_partial_rows)
+        return set_error(FAVOR_ERR_INVALID_ARG, "backward workspace too small (%d x %d rows)", BH, R.pstride);
+    CUtensorMap mq, mk, mv, mdo, mw;
+    if (!map_tokens(&mq, q, BH, L) || !map_tokens(&mk, k, BH, L) || !map_tokens(&mv, v, BH, L) ||
+        !map_tokens(&mdo, dout, BH, L) || !map_omega(&mw, h.omega_bf16, h.H))
+        return set_error(FAVOR_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    if (h.kind == FAVOR_KERNEL_SOFTMAX_POS)
+        return tc_causal_backward_t<FAVOR_KERNEL_SOFTMAX_POS>(h, mq, mk, mv, mdo, mw, dq, dk, dv, BH, L, R, st);
+    return tc_causal_backward_t<FAVOR_KERNEL_RELU>(h, mq, mk, mv, mdo, mw, dq, dk, dv, BH, L, R, st);
 }
 
 }  // namespace favor

@@ -217,15 +217,31 @@ def test_backward_full_size_sampled_heads(causal, kind):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("kind", O.KINDS)
-def test_backward_ranges_cross_heads_with_ragged_tiles(kind):
+@pytest.mark.parametrize("causal", [False, True], ids=["bidir", "causal"])
+def test_backward_ranges_cross_heads_with_ragged_tiles(kind, causal):
     """B=4, H=16, L=1100 on the tensor-core shape: 576 tiles over the SMs, so a
     CTA's range of tiles crosses head boundaries and every head ends in a
     ragged tile (the per-head operands reload mid-range, pieces are combined
-    across CTAs)."""
+    across CTAs; causal: the running prefix and suffix states are carried over
+    several chunks inside a range and restart at each head)."""
     shape = ("d64_m256_bf16", "bidir_bf16", dict(B=4, H=16))
-    w, got, ref = _run(shape, kind, False, 1100, 77)
+    w, got, ref = _run(shape, kind, causal, 1100, 77)
     omega, q, k, v = make_workload(w, 77)
-    check_grads(w, kind, False, got, ref, q, k, v, make_upstream_grad(w, 77), omega)
+    check_grads(w, kind, causal, got, ref, q, k, v, make_upstream_grad(w, 77), omega)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", ["softmax_pos", "relu"])
+def test_causal_backward_long_ranges(kind):
+    """One head pair over 40 chunks (B=1, H=2, L=5000): every CTA range is a
+    single chunk here, and with the sequence split over fewer CTAs (B=1, H=1,
+    L=40000: 313 chunks, three per range) the states cross ranges both
+    ways; both against the oracle."""
+    for H, L in ((2, 5000), (1, 40000)):
+        shape = ("d64_m256_bf16", "bidir_bf16", dict(B=1, H=H))
+        w, got, ref = _run(shape, kind, True, L, 91 + H)
+        omega, q, k, v = make_workload(w, 91 + H)
+        check_grads(w, kind, True, got, ref, q, k, v, make_upstream_grad(w, 91 + H), omega)
 
 
 @pytest.mark.gpu
