@@ -743,12 +743,13 @@ k_tc_bwd_k(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 // chunk's hi + lo image.  The subtractions S dO_i - z go_i and T v_j + t, as
 // in the bidirectional passes, need the states near fp32, so each chunk's
 // increment takes its features as hi + lo pairs (kept in tensor memory where
-// the transposed projection left them).  The in-chunk products of dq and dk
-// take f16 operands under power-of-two scales (see the passes); dv, which
-// subtracts nothing, takes bf16.
+// the transposed projection left them).  In the query pass the in-chunk
+// products take the key features and B as bf16 pairs too (dq cancels the
+// most); the key pass's in-chunk term of dk takes f16 operands under
+// power-of-two scales; dv, which subtracts nothing, takes bf16.
 //
 //   k_tc_bstate<MODE 0>, k_piece_scan<false>   K, V            -> prefix S, z per piece
-//   k_tc_cbwd_q                                Q, K, V, dO     -> dq, rowstat (den, row shift, go, f16 scale)
+//   k_tc_cbwd_q                                Q, K, V, dO     -> dq, rowstat (den, row shift, go, ReLU f16 scale)
 //   k_tc_bstate<MODE 1>, k_piece_scan<true>    Q, dO, rowstat  -> suffix T, t per piece
 //   k_tc_cbwd_k                                Q, K, V, dO     -> dk
 //   k_tc_cbwd_v                                Q, K, dO        -> dv
@@ -965,30 +966,6 @@ __device__ __forceinline__ float cb_feature_row(uint32_t taddr, uint32_t feat, u
     return acc;
 }
 
-// Largest exp2 argument (positive) or product (ReLU) over the row's 128 projections at taddr.
-template <int KIND>
-__device__ __forceinline__ float cb_row_max_arg(uint32_t taddr, float a, const float* off) {
-    float m = KIND == FAVOR_KERNEL_SOFTMAX_POS ? -INFINITY : 0.f;
-#pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-        uint32_t p[32];
-        tmem_ld32(taddr + 32 * blk, p);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float pv = __uint_as_float(p[i]), o = off[32 * blk + i];
-            m = fmaxf(m, KIND == FAVOR_KERNEL_SOFTMAX_POS ? fmaf(pv, a, o) : pv * o);
-        }
-    }
-    return m;
-}
-
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
-}
-
 // dx row epilogue: columns 32 ch .. +31 of d = s (acc - s gsum x) (positive) or s acc (ReLU), bf16,
 // stored when dst_row is not null (the tensor-memory load is warp-wide).
 template <int KIND>
@@ -1018,19 +995,127 @@ __device__ __forceinline__ void cb_store_grad(__nv_bfloat16* dst_row, uint32_t t
     }
 }
 
+// Key features of feature row f for 64 keys (fp32 projections: 64 columns at taddr): x_t =
+// exp2(a p + off_t) (positive) or max(p off_t, 0) (ReLU: off_t = s for a live key, 0 past L).
+// SMEM: the pair hi + lo of x into row f of the [256 features][64 keys] blocks hi_blk, lo_blk;
+// TMEM: the pair over the row's own columns (hi at taddr, lo at taddr + 32, 8 columns per 16
+// keys).  Returns sum_t x_t.
+template <int KIND, bool SMEM, bool TMEM>
+__device__ __forceinline__ float cb_key_row_hl(uint32_t taddr, uint32_t hi_blk, uint32_t lo_blk, uint32_t f,
+                                               float a, const float* off) {
+    uint32_t p0[32], p1[32];
+    tmem_ld32(taddr, p0);
+    tmem_ld32(taddr + 32, p1);
+    tmem_ld_wait();
+    float acc = 0.f;
+    uint32_t h0[16], h1[16], l0[16], l1[16];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float x[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int t = 2 * i + u;
+            const float pv = __uint_as_float(t < 32 ? p0[t] : p1[t - 32]);
+            x[u] = KIND == FAVOR_KERNEL_SOFTMAX_POS ? ex2(fmaf(pv, a, off[t])) : fmaxf(pv * off[t], 0.f);
+            acc += x[u];
+        }
+        if (i < 16) split_pack(x[0], x[1], h0[i], l0[i]);
+        else split_pack(x[0], x[1], h1[i - 16], l1[i - 16]);
+    }
+    if (SMEM) {
+#pragma unroll
+        for (uint32_t c = 0; c < 4; ++c) {
+            st_shared_v4(hi_blk + sw128(f, c), h0[4 * c], h0[4 * c + 1], h0[4 * c + 2], h0[4 * c + 3]);
+            st_shared_v4(hi_blk + sw128(f, 4 + c), h1[4 * c], h1[4 * c + 1], h1[4 * c + 2], h1[4 * c + 3]);
+            st_shared_v4(lo_blk + sw128(f, c), l0[4 * c], l0[4 * c + 1], l0[4 * c + 2], l0[4 * c + 3]);
+            st_shared_v4(lo_blk + sw128(f, 4 + c), l1[4 * c], l1[4 * c + 1], l1[4 * c + 2], l1[4 * c + 3]);
+        }
+    }
+    if (TMEM) {
+        tmem_st16(taddr, h0);
+        tmem_st16(taddr + 16, h1);
+        tmem_st16(taddr + 32, l0);
+        tmem_st16(taddr + 48, l1);
+    }
+    return acc;
+}
+
+// D[128 rows][64 keys] = X . (K_hi + K_lo) where X is packed bf16 in tensor memory (features
+// 0..127 at x0, 128..255 at x1, 8 columns per 16 features) and K_hi, K_lo the key features
+// [256 features][64 keys] in shared memory (MN-major, N = key).
+__device__ __forceinline__ void cb_scores_half(uint32_t d, uint32_t x0, uint32_t x1, uint32_t khi, uint32_t klo) {
+    const uint32_t id = make_idesc(128, 64, 0, 1);
+    const uint64_t bh0 = make_desc(khi, 8192, 1024, SW_128B), bl0 = make_desc(klo, 8192, 1024, SW_128B);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) mma_ts(d, kk < 8 ? x0 + 8 * kk : x1 + 8 * (kk - 8), bh0 + 128 * kk, id, kk > 0 ? 1u : 0u);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) mma_ts(d, kk < 8 ? x0 + 8 * kk : x1 + 8 * (kk - 8), bl0 + 128 * kk, id, 1u);
+}
+
+// D[128 rows][256 features] += W . F for 64 keys, W = W_hi + W_lo packed bf16 in tensor memory
+// (8 columns per 16 keys at whi, wlo) and F = F_hi + F_lo the keys' features [256 features][64
+// keys] in shared memory (K-major over keys): W_hi F_hi + W_lo F_hi + W_hi F_lo.
+__device__ __forceinline__ void cb_weighted_half(uint32_t d, uint32_t whi, uint32_t wlo, uint32_t fhi, uint32_t flo) {
+    const uint32_t id = make_idesc(128, 256, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bh = make_desc(fhi + (uint32_t)kk * 32, 16, 1024, SW_128B);
+        const uint64_t bl = make_desc(flo + (uint32_t)kk * 32, 16, 1024, SW_128B);
+        mma_ts(d, whi + 8 * kk, bh, id, 1u);
+        mma_ts(d, wlo + 8 * kk, bh, id, 1u);
+        mma_ts(d, whi + 8 * kk, bl, id, 1u);
+    }
+}
+
+// The masked sums of 32 keys j0 .. j0+31 of row `row`: den += sum_{j<=row} A_j, fu += sum_{j<=row} A_j C_j
+// (A at ta, C at tc, 32 fp32 columns each).
+__device__ __forceinline__ void cb_masked_sums(uint32_t ta, uint32_t tc, int j0, int row, float& den, float& fu) {
+    uint32_t av[32], cv[32];
+    tmem_ld32(ta, av);
+    tmem_ld32(tc, cv);
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        if (j0 + k <= row) {
+            const float av_k = __uint_as_float(av[k]);
+            den += av_k;
+            fu = fmaf(av_k, __uint_as_float(cv[k]), fu);
+        }
+    }
+}
+
+// Two / four consecutive tensor-memory columns of this thread's lane.
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, const uint32_t (&r)[2]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(r[0]), "r"(r[1])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
 // Query pass, persistent over the call's tile ranges (grid R.G, 256 threads).  Thread t is
 // query row t % 128 with features 128 (t / 128) .. +127 of it (the same split as the
 // bidirectional query pass), and feature row t of the key features and of the running prefix
-// state.  The in-chunk products take f16 operands (their 11 significant bits keep the rounding of
-// the features and of B below what the cancellation in dq amplifies): the key features scaled by
-// 2^-ek (the chunk's largest to [1/2, 1)), B row i by 2^-eb_i, and, so that U stays one sum, the
-// state image by 2^-ek and dO row i by 2^-eb_i.  Tensor memory per chunk (columns):
-//   P_K^T halves [0,128) [128,256) -> key features hi + lo in place (and f16 in shared memory)
-//   dS halves [256,320) [320,384), P_Q [0,256)
-//   U = dO S~^T [256,512) -> f16 Phi_Q over [0,64) [128,192)
-//   A [256,384), C [384,512) -> B = tril(C - go) over [384,416) [448,480)
-//   U = dO S~^T + B Phi_K [0,256), P_Q again [256,512) -> G hi over U, lo over P
-//   dq [64,128)
+// state.  dq cancels strongly (sum_f G_f (omega_f - s x) with sum_f G_f = 0), so every product
+// inside a chunk takes the key features as bf16 pairs hi + lo, and B as a pair too; the query
+// features enter A as bf16, and the parts from before the chunk take the same rounded values,
+// so that den and dO . out are exact for them.  Shared memory holds the pairs of 64 keys at a
+// time: the scores and B Phi_K run in two key halves, each half's features recomputed from its
+// projection when its turn comes.  Tensor memory per chunk (columns):
+//   P0  P_K^T halves [0,128) [128,256) -> key features hi + lo in place (keys 0..63 also in
+//       shared memory)
+//   P1  dS halves [256,320) [320,384), P_Q [0,256)
+//   P2  U = dO S~^T [256,512) -> bf16 Phi_Q over [0,64) [128,192)
+//   P3  A (keys 0..63) [256,320), C [384,512), P_K^T of keys 64..127 [320,384) [192,256)
+//   P4  A (keys 64..127) [256,320) -> B = tril(C - go) hi, lo over C: keys 64c .. +63 of
+//       thread half c at [384 + 64c, +32) and [416 + 64c, +32); row partials exchanged in
+//       columns 320..323
+//   P5  U = dO S~^T + B Phi_K (keys 64..127) [0,256), P_K^T of keys 0..63 [256,320) [320,384)
+//   P6  U += B Phi_K (keys 0..63), P_Q again [256,512) -> G hi over U, lo over P
+//   P7  dq [64,128)
 template <int KIND>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -1044,13 +1129,12 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t s_w = smem_u32(sm);
     const uint32_t s_img = s_w + kCbImgOff;
     const uint32_t s_q = s_w + kCbTiles, s_k = s_q + kTileBytes, s_v = s_k + kTileBytes, s_do = s_v + kTileBytes;
-    const uint32_t s_phi = s_w + kCbPhi;
-    float* zv = reinterpret_cast<float*>(sm + kCbVec);                  // z of the chunk's prefix
-    float* kc = zv + kM;                                                 // key column terms
-    float* red = reinterpret_cast<float*>(sm + kCbTiles + kTileBytes);  // partials, in the K tile
-    float* redg = reinterpret_cast<float*>(sm + kCbPhi);                // gsum partials, in the features
+    const uint32_t s_khi = s_w + kCbPhi, s_klo = s_khi + 2 * kPhiBlock;   // 64 keys' features hi | lo
+    float* zv = reinterpret_cast<float*>(sm + kCbVec);                     // z of the chunk's prefix
+    float* kc = zv + kM;                                                    // key column terms
+    float* redg = reinterpret_cast<float*>(sm + kCbPhi);                   // gsum partials, in the features
     CbBars* bars = reinterpret_cast<CbBars*>(sm + kCbBars);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int row = tid & (kTile - 1), ch = tid >> 7;
     const int cta = blockIdx.x;
     const int g0 = cta * R.per, g1 = min(R.T, g0 + R.per);
@@ -1097,13 +1181,15 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 w_h = h;
                 w_wait = true;
             }
-            // the piece's prefix state, feature row tid
+            // the piece's prefix state, feature row tid, and its image
             const float* pre = prefix + ((size_t)bh * R.pstride + (cta - first_cta(R, bh))) * (kM * (kDV + 1)) +
                                (size_t)tid * (kDV + 1);
 #pragma unroll
             for (int c = 0; c < 64; ++c) srun[c] = pre[c];
             zrun = pre[kDV];
+            cb_write_image(s_img, (uint32_t)tid, srun, 1.f);
             zv[tid] = zrun;
+            fence_async_smem();
             cur_bh = bh;
             if (w_wait) {
                 ok = __syncthreads_and(mbar_wait(&bars->w, nw & 1, err, 60));
@@ -1113,7 +1199,7 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 pend.w = -1;
             }
         }
-        // ---- key projection (transposed) -> the chunk's scale, key features, their sums
+        // ---- P0: key projection (transposed) -> key features (hi + lo), their sums
         ok = __syncthreads_and(mbar_wait(&bars->tile[CB_K], tpar, err, 61));
         if (!ok) break;
         pend.tile[CB_K] = -1;
@@ -1132,29 +1218,8 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         ++nmma;
         if (!ok) break;
         tc_fence_after();
-        {
-            const float m = warp_max(cb_row_max_arg<KIND>(tl + 128 * ch, a, kc));
-            if (lane == 0) red[warp] = m;
-        }
-        __syncthreads();
-        int ek;
-        {
-            float m = red[0];
-#pragma unroll
-            for (int w8 = 1; w8 < 8; ++w8) m = fmaxf(m, red[w8]);
-            if (POS) ek = m > -1e30f ? max(-100, min(100, (int)ceilf(m))) : 0;
-            else ek = m > 0.f ? max(-100, min(100, ilog2f(m) + 1)) : 0;
-        }
-        __syncthreads();   // every thread has the scale before kc changes
-        if (tid < kTile) kc[tid] = POS ? kc[tid] - (float)ek : kc[tid] * exp2i(-ek);
-        __syncthreads();
-        const float sk = exp2i(ek);
-        float zc = 0.f;
-#pragma unroll 1
-        for (int u = 0; u < 2; ++u)
-            zc += cb_feature_row<KIND, true>(tl + 128 * ch + 64 * u, s_phi + (uint32_t)u * 2 * kPhiBlock,
-                                             (uint32_t)tid, a, kc + 64 * u, nullptr, sk, nullptr);
-        cb_write_image(s_img, (uint32_t)tid, srun, exp2i(-ek));   // S before this chunk, times 2^-ek
+        float zc = cb_key_row_hl<KIND, true, true>(tl + 128 * ch, s_khi, s_klo, (uint32_t)tid, a, kc);
+        zc += cb_key_row_hl<KIND, false, true>(tl + 128 * ch + 64, s_khi, s_klo, (uint32_t)tid, a, kc + 64);
         tmem_st_wait();
         fence_async_smem();
         tc_fence_before();
@@ -1162,7 +1227,7 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                                mbar_wait(&bars->tile[CB_V], tpar, err, 58));
         if (!ok) break;
         pend.tile[CB_Q] = pend.tile[CB_V] = -1;
-        // ---- the chunk's state increment dS = Phi_K^T V (features hi + lo), the query projection
+        // ---- P1: the chunk's state increment dS = Phi_K^T V (hi + lo), the query projection
         if (tid == 0) {
             tc_fence_after();
             cb_state_inc(tmem + 256, tmem + 320, tmem, tmem + 128, s_v);
@@ -1178,7 +1243,6 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (!ok) break;
         tc_fence_after();
         {
-            // feature row tid of the running state takes the chunk
             uint32_t d0[32], d1[32];
             tmem_ld32(tl + 256 + 64 * ch, d0);
             tmem_ld32(tl + 288 + 64 * ch, d1);
@@ -1190,26 +1254,24 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             zrun += zc;
         }
-        // the row's largest projection: exponent shift (positive) or f16 scale (ReLU)
+        // the row's largest projection over all 256 features (both halves of the row are read)
         float mx = -INFINITY;
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 8; ++cc) {
             uint32_t pw[32];
-            tmem_ld32(tl + 128 * ch + 32 * cc, pw);
+            tmem_ld32(tl + 32 * cc, pw);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(pw[i]));
         }
-        red[8 + ch * kTile + row] = mx;
-        tc_fence_before();
-        __syncthreads();
-        mx = fmaxf(red[8 + row], red[8 + kTile + row]);
         const int eq = POS ? 0 : (s * mx > 0.f ? max(-100, min(100, ilog2f(s * mx) + 1)) : 0);
         const float c = -mx * a;
+        tc_fence_before();
         ok = __syncthreads_and(mbar_wait(&bars->tile[CB_O], tpar, err, 64));
         if (!ok) break;
         pend.tile[CB_O] = -1;
-        if (tid == 0) {   // U = dO (2^-ek S~)^T
+        // ---- P2: U = dO S~^T (the prefix part); query features, den and dO . out of the prefix
+        if (tid == 0) {
             tc_fence_after();
             cb_state_mult(tmem + 256, s_do, s_img);
             mma_commit(&bars->mma);
@@ -1218,41 +1280,36 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         ++nmma;
         if (!ok) break;
         tc_fence_after();
-        float den = 0.f, fu = 0.f;
-        {
-            const float q16 = exp2i(-eq);
+        float den = 0.f, fu = 0.f;   // from the bf16 query features, as A uses them
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t pw[32], uw[32];
-                tmem_ld32(tl + 128 * ch + 32 * cc, pw);
-                tmem_ld32(tl + 256 + 128 * ch + 32 * cc, uw);
-                tmem_ld_wait();
-                uint32_t fw[16];
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t pw[32], uw[32];
+            tmem_ld32(tl + 128 * ch + 32 * cc, pw);
+            tmem_ld32(tl + 256 + 128 * ch + 32 * cc, uw);
+            tmem_ld_wait();
+            uint32_t fw[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float f[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int k = 2 * i + e;
-                        const float pv = __uint_as_float(pw[k]);
-                        f[e] = POS ? ex2(fmaf(pv, a, c)) : fmaxf(s * pv, 0.f);
-                        den = fmaf(f[e], zv[128 * ch + 32 * cc + k], den);
-                        fu = fmaf(f[e], __uint_as_float(uw[k]), fu);
-                    }
-                    fw[i] = pack_f16(f[0] * q16, f[1] * q16);
-                }
-                tmem_st16(tl + 128 * ch + 16 * cc, fw);
+            for (int i = 0; i < 16; ++i) {
+                const float p0 = __uint_as_float(pw[2 * i]), p1 = __uint_as_float(pw[2 * i + 1]);
+                fw[i] = POS ? pack_bf16(ex2(fmaf(p0, a, c)), ex2(fmaf(p1, a, c)))
+                            : pack_bf16(fmaxf(s * p0, 0.f), fmaxf(s * p1, 0.f));
+                const float f0 = bf16lo(fw[i]), f1 = bf16hi(fw[i]);
+                const int k = 128 * ch + 32 * cc + 2 * i;
+                den = fmaf(f0, zv[k], fmaf(f1, zv[k + 1], den));
+                fu = fmaf(f0, __uint_as_float(uw[2 * i]), fmaf(f1, __uint_as_float(uw[2 * i + 1]), fu));
             }
-            fu *= sk;   // U above carries 2^-ek
+            tmem_st16(tl + 128 * ch + 16 * cc, fw);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncthreads();
-        // ---- A = Phi_Q Phi_K^T (f16, scaled 2^-(ek + eq_i)), C = dO V^T
+        // ---- P3: A for keys 0..63 (hi + lo), C = dO V^T, projections of keys 64..127
         if (tid == 0) {
             tc_fence_after();
-            cb_scores<true>(tmem + 256, tmem, tmem + 128, s_phi);
+            cb_scores_half(tmem + 256, tmem, tmem + 128, s_khi, s_klo);
             cb_project(tmem + 384, s_do, s_v, 128);
+            cb_project(tmem + 320, s_w, s_k + 64 * 128, 64);
+            cb_project(tmem + 192, s_w + 128 * 128, s_k + 64 * 128, 64);
             mma_commit(&bars->mma);
         }
         ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 66));
@@ -1263,98 +1320,92 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             pend.tile[CB_V] = (int)(tpar ^ 1);
         }
         tc_fence_after();
-        {
-            const float ascale = exp2i(ek) * exp2i(eq);
-            float dpart = 0.f, fpart = 0.f;
-#pragma unroll 1
-            for (int blk = 0; blk < 2; ++blk) {
-                // keys 64 ch + 32 blk .. +31 of row `row`: the masked sums
-                uint32_t av[32], cv[32];
-                tmem_ld32(tl + 256 + 64 * ch + 32 * blk, av);
-                tmem_ld32(tl + 384 + 64 * ch + 32 * blk, cv);
-                tmem_ld_wait();
-                const int j0 = 64 * ch + 32 * blk;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    if (j0 + k <= row) {
-                        const float av_k = __uint_as_float(av[k]);
-                        dpart += av_k;
-                        fpart = fmaf(av_k, __uint_as_float(cv[k]), fpart);
-                    }
-                }
-            }
-            den = fmaf(dpart, ascale, den);
-            fu = fmaf(fpart, ascale, fu);
-        }
-        red[8 + 2 * kTile + ch * kTile + row] = den;
-        red[8 + 4 * kTile + ch * kTile + row] = fu;
+        cb_masked_sums(tl + 256 + 32 * ch, tl + 384 + 32 * ch, 32 * ch, row, den, fu);
+        cb_key_row_hl<KIND, true, false>(ch == 0 ? tl + 320 : tl + 192, s_khi, s_klo, (uint32_t)tid, a, kc + 64);
+        fence_async_smem();
+        tc_fence_before();
         __syncthreads();
-        den = red[8 + 2 * kTile + row] + red[8 + 3 * kTile + row];
-        fu = red[8 + 4 * kTile + row] + red[8 + 5 * kTile + row];
-        const float inv = den != 0.f ? 1.f / den : 0.f;
-        const float go = fu * inv;
-        if (live && ch == 0) rowstat[(size_t)bh * L + tok] = make_float4(den, POS ? s * mx : 0.f, go, (float)eq);
-        uint32_t c0[32], c1[32];
-        tmem_ld32(tl + 384 + 64 * ch, c0);
-        tmem_ld32(tl + 384 + 64 * ch + 32, c1);
-        tmem_ld_wait();
-        {
-            // the row's largest |C - go| over the keys it sees -> f16 scale of B (and of dO row)
-            float bm = 0.f;
-            const int j0 = 64 * ch;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                if (j0 + k <= row) bm = fmaxf(bm, fabsf(__uint_as_float(c0[k]) - go));
-                if (j0 + 32 + k <= row) bm = fmaxf(bm, fabsf(__uint_as_float(c1[k]) - go));
-            }
-            red[8 + 6 * kTile + ch * kTile + row] = bm;
+        // ---- P4: A for keys 64..127; den, go; B = tril(C - go) as hi + lo
+        if (tid == 0) {
+            tc_fence_after();
+            cb_scores_half(tmem + 256, tmem, tmem + 128, s_khi, s_klo);
+            mma_commit(&bars->mma);
         }
-        __syncthreads();
-        const int eb = f16_scale_exp(fmaxf(red[8 + 6 * kTile + row], red[8 + 7 * kTile + row]));
-        fence_async_smem();   // the K tile's next load follows these generic accesses
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 59));
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        cb_masked_sums(tl + 256 + 32 * ch, tl + 448 + 32 * ch, 64 + 32 * ch, row, den, fu);
         {
-            // B = tril(C - go) 2^-eb for keys 64 ch .. +63, f16, over the row's first 32 C columns;
-            // this row's dO (columns 32 ch .. +31) times 2^-eb in place
-            const float bs = exp2i(-eb);
-            uint32_t b0[16], b1[16];
-            const int j0 = 64 * ch;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                b0[i] = pack_f16(j0 + 2 * i <= row ? (__uint_as_float(c0[2 * i]) - go) * bs : 0.f,
-                                 j0 + 2 * i + 1 <= row ? (__uint_as_float(c0[2 * i + 1]) - go) * bs : 0.f);
-                b1[i] = pack_f16(j0 + 32 + 2 * i <= row ? (__uint_as_float(c1[2 * i]) - go) * bs : 0.f,
-                                 j0 + 33 + 2 * i <= row ? (__uint_as_float(c1[2 * i + 1]) - go) * bs : 0.f);
-            }
-            tmem_st16(tl + 384 + 64 * ch, b0);
-            tmem_st16(tl + 384 + 64 * ch + 16, b1);
-#pragma unroll
-            for (uint32_t c4 = 0; c4 < 4; ++c4) {
-                const uint32_t addr = s_do + sw128((uint32_t)row, 4 * (uint32_t)ch + c4);
-                const uint4 x = ld_shared_v4(addr);
-                const uint32_t xin[4] = {x.x, x.y, x.z, x.w};
-                uint32_t y[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) y[i] = pack_bf16(bf16lo(xin[i]) * bs, bf16hi(xin[i]) * bs);
-                st_shared_v4(addr, y[0], y[1], y[2], y[3]);
-            }
-            fence_async_smem();
+            // the row's two partials through tensor-memory columns 320..323
+            const uint32_t xw[2] = {__float_as_uint(den), __float_as_uint(fu)};
+            tmem_st2(tl + 320 + 2 * ch, xw);
             tmem_st_wait();
         }
         tc_fence_before();
         __syncthreads();
-        // ---- U = dO' S~'^T + B' Phi_K' (= 2^-(ek + eb_i) U), the query projection again
+        tc_fence_after();
+        {
+            uint32_t xr[4];
+            tmem_ld4(tl + 320, xr);
+            tmem_ld_wait();
+            den = __uint_as_float(xr[0]) + __uint_as_float(xr[2]);
+            fu = __uint_as_float(xr[1]) + __uint_as_float(xr[3]);
+        }
+        const float inv = den != 0.f ? 1.f / den : 0.f;
+        const float go = fu * inv;
+        if (live && ch == 0) rowstat[(size_t)bh * L + tok] = make_float4(den, POS ? s * mx : 0.f, go, (float)eq);
+        {
+            uint32_t c0[32], c1[32];
+            tmem_ld32(tl + 384 + 64 * ch, c0);
+            tmem_ld32(tl + 416 + 64 * ch, c1);
+            tmem_ld_wait();
+            uint32_t h0[16], h1[16], l0[16], l1[16];
+            const int j0 = 64 * ch;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                split_pack(j0 + 2 * i <= row ? __uint_as_float(c0[2 * i]) - go : 0.f,
+                           j0 + 2 * i + 1 <= row ? __uint_as_float(c0[2 * i + 1]) - go : 0.f, h0[i], l0[i]);
+                split_pack(j0 + 32 + 2 * i <= row ? __uint_as_float(c1[2 * i]) - go : 0.f,
+                           j0 + 33 + 2 * i <= row ? __uint_as_float(c1[2 * i + 1]) - go : 0.f, h1[i], l1[i]);
+            }
+            tmem_st16(tl + 384 + 64 * ch, h0);
+            tmem_st16(tl + 400 + 64 * ch, h1);
+            tmem_st16(tl + 416 + 64 * ch, l0);
+            tmem_st16(tl + 432 + 64 * ch, l1);
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- P5: U = dO S~^T + B Phi_K (keys 64..127), projections of keys 0..63
         if (tid == 0) {
             tc_fence_after();
             cb_state_mult(tmem, s_do, s_img);
-            cb_weighted_features(tmem, tmem + 384, tmem + 448, s_phi);
-            issue_projection(tmem + 256, s_q, s_w, 256);
+            cb_weighted_half(tmem, tmem + 448, tmem + 480, s_khi, s_klo);
+            cb_project(tmem + 256, s_w, s_k, 64);
+            cb_project(tmem + 320, s_w + 128 * 128, s_k, 64);
             mma_commit(&bars->mma);
-            if (more) {
-                cb_load_tile(&tm_k, sm, CB_K, bars, g + 1, R.tph);
-                pend.tile[CB_K] = (int)(tpar ^ 1);
-            }
         }
         ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 67));
+        ++nmma;
+        if (!ok) break;
+        if (tid == 0 && more) {
+            cb_load_tile(&tm_k, sm, CB_K, bars, g + 1, R.tph);
+            pend.tile[CB_K] = (int)(tpar ^ 1);
+        }
+        tc_fence_after();
+        cb_key_row_hl<KIND, true, false>(tl + 256 + 64 * ch, s_khi, s_klo, (uint32_t)tid, a, kc);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- P6: U += B Phi_K (keys 0..63), the query projection again; G
+        if (tid == 0) {
+            tc_fence_after();
+            cb_weighted_half(tmem, tmem + 384, tmem + 416, s_khi, s_klo);
+            issue_projection(tmem + 256, s_q, s_w, 256);
+            mma_commit(&bars->mma);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 56));
         ++nmma;
         if (!ok) break;
         if (tid == 0 && more) {
@@ -1364,44 +1415,43 @@ k_tc_cbwd_q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         tc_fence_after();
         float gsum = 0.f;
-        {
-            const float us = exp2i(ek) * exp2i(eb);
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t pw[32], uw[32];
-                tmem_ld32(tl + 256 + 128 * ch + 32 * cc, pw);
-                tmem_ld32(tl + 128 * ch + 32 * cc, uw);
-                tmem_ld_wait();
-                uint32_t hw[16], lw[16];
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t pw[32], uw[32];
+            tmem_ld32(tl + 256 + 128 * ch + 32 * cc, pw);
+            tmem_ld32(tl + 128 * ch + 32 * cc, uw);
+            tmem_ld_wait();
+            uint32_t hw[16], lw[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float gg[2];
+            for (int i = 0; i < 16; ++i) {
+                float gg[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int k = 2 * i + e;
-                        const float pv = __uint_as_float(pw[k]);
-                        const float dphi = fmaf(__uint_as_float(uw[k]), us, -zv[128 * ch + 32 * cc + k] * go) * inv;
-                        const float gv = POS ? dphi * ex2(fmaf(pv, a, c)) : (pv > 0.f ? dphi : 0.f);
-                        gg[e] = gv;
-                        gsum += gv;
-                    }
-                    split_pack(gg[0], gg[1], hw[i], lw[i]);
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 2 * i + e;
+                    const float pv = __uint_as_float(pw[k]);
+                    const float dphi = (__uint_as_float(uw[k]) - zv[128 * ch + 32 * cc + k] * go) * inv;
+                    const float gv = POS ? dphi * ex2(fmaf(pv, a, c)) : (pv > 0.f ? dphi : 0.f);
+                    gg[e] = gv;
+                    gsum += gv;
                 }
-                tmem_st16(tl + 128 * ch + 16 * cc, hw);
-                tmem_st16(tl + 256 + 128 * ch + 16 * cc, lw);
+                split_pack(gg[0], gg[1], hw[i], lw[i]);
             }
+            tmem_st16(tl + 128 * ch + 16 * cc, hw);
+            tmem_st16(tl + 256 + 128 * ch + 16 * cc, lw);
         }
         tmem_st_wait();
         redg[ch * kTile + row] = gsum;
         tc_fence_before();
         __syncthreads();
-        // ---- dq = G omega
+        // ---- P7: dq = G omega; meanwhile the next chunk's prefix image
         if (tid == 0) {
             tc_fence_after();
             cb_grad_omega(tmem + 64, tmem, tmem + 128, tmem + 256, tmem + 384, s_w);
             mma_commit(&bars->mma);
         }
-        zv[tid] = zrun;   // z of the next chunk's prefix (the current one is read)
+        cb_write_image(s_img, (uint32_t)tid, srun, 1.f);
+        zv[tid] = zrun;
+        fence_async_smem();
         ok = __syncthreads_and(mbar_wait(&bars->mma, nmma & 1, err, 68));
         ++nmma;
         if (!ok) break;

@@ -265,29 +265,21 @@ def test_backward_unaligned_inputs(shape, causal):
         assert grad_err(a, b) <= TOL_GRAD[w.dtype], name
 
 
-_WIDE_POS_LIMIT = pytest.mark.xfail(
-    strict=True,
-    reason="the tensor-core causal backward rounds its in-chunk products to f16: with positive features at "
-           "twice the workloads' input spread the attention is sharp enough that dq cancels past what f16 "
-           "holds (7.2e-2 measured, 6.0e-2 in a float64 simulation of the roundings; hi + lo key features "
-           "would bring it to 5e-4 but need a second feature image in shared memory)")
-
-
 @pytest.mark.gpu
 @pytest.mark.parametrize("kind,base,over", [
     ("softmax_pos", "causal_bf16", dict(B=1, H=2, L=1100)),
     ("relu", "causal_bf16", dict(B=1, H=2, L=1100)),
-    pytest.param("softmax_pos", "bidir_bf16", dict(B=1, H=2, L=700, std=1.0), marks=_WIDE_POS_LIMIT),
+    ("softmax_pos", "bidir_bf16", dict(B=1, H=2, L=700, std=1.0)),
     ("relu", "bidir_bf16", dict(B=1, H=2, L=700, std=1.0)),
 ], ids=["sharp_keys-softmax_pos", "sharp_keys-relu", "wide_inputs-softmax_pos", "wide_inputs-relu"])
 def test_causal_backward_feature_range(kind, base, over):
     """Inputs whose features span a wider range than the default workloads:
     the causal config's sharp key rows (1% of keys x4) and inputs at twice the
-    default spread.  The tensor-core causal backward rounds its in-chunk
-    products to f16 under power-of-two scales taken from each chunk's largest
-    key feature and each row's largest weight; the gradients must meet the
-    bf16 bound against the oracle, except for positive features at twice the
-    spread (a known limit of the f16 in-chunk products, pinned as such)."""
+    default spread (sharper attention, so dq and dk cancel more).  The
+    tensor-core causal backward takes the key features of its in-chunk
+    products as bf16 pairs in the query pass and rounds the key pass's
+    in-chunk term to f16 under power-of-two scales; the gradients must meet
+    the bf16 bound against the oracle."""
     w = CONFIGS[base].replace(**over)
     omega, q, k, v = make_workload(w, 57)
     g = make_upstream_grad(w, 57)
