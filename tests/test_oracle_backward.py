@@ -199,3 +199,88 @@ def test_gradients_match_reverse_mode_autodiff(mode, kind):
     got = BWD[mode](q, k, v, g, omega, s, kind)
     for name, a, b in zip(("dq", "dk", "dv"), got, (tq.grad, tk.grad, tv.grad)):
         np.testing.assert_allclose(a, b.numpy(), rtol=1e-9, atol=1e-12, err_msg=name)
+
+
+def _chunked_causal_feature_grads(pq, pk, v, g, chunk, per):
+    """The causal gradients with respect to the features, evaluated chunk by
+    chunk the way the tensor-core passes evaluate them: exclusive prefix
+    states S, z of the keys before a chunk, exclusive suffix states T, t of
+    the queries after it (T = sum phi_q dO^T / den, t = -sum phi_q go / den),
+    carried across `per`-chunk pieces and rebuilt at each piece from the sums
+    of the other pieces, and the masked products inside the chunk:
+        den_i = phi_q,i . z + sum_{j<=i} A_ij,   A = Phi_Q Phi_K^T, C = dO V^T
+        go_i  = (phi_q,i . (S dO_i) + sum_{j<=i} A_ij C_ij) / den_i
+        dphi_q,i = (S dO_i - z go_i + sum_{j<=i} (C_ij - go_i) phi_k,j) / den_i
+        dphi_k,j = T v_j + t + sum_{i>=j} (C_ij - go_i) phi_q,i / den_i
+        dv_j     = T^T phi_k,j + sum_{i>=j} (phi_k,j . phi_q,i / den_i) dO_i"""
+    L, m = pq.shape
+    n_ch = -(-L // chunk)
+    pieces = [list(range(p, min(n_ch, p + per))) for p in range(0, n_ch, per)]
+    rows = lambda c: slice(c * chunk, min(L, (c + 1) * chunk))
+    # key pieces -> exclusive prefix per piece
+    tot = []
+    for pc in pieces:
+        S, z = np.zeros((m, v.shape[1])), np.zeros(m)
+        for c in pc:
+            S += pk[rows(c)].T @ v[rows(c)]
+            z += pk[rows(c)].sum(0)
+        tot.append((S, z))
+    dpq, den_all, go_all = np.zeros_like(pq), np.zeros(L), np.zeros(L)
+    for p, pc in enumerate(pieces):
+        S = sum((t[0] for t in tot[:p]), np.zeros((m, v.shape[1])))
+        z = sum((t[1] for t in tot[:p]), np.zeros(m))
+        for c in pc:
+            r = rows(c)
+            n = r.stop - r.start
+            Q, K, V, D = pq[r], pk[r], v[r], g[r]
+            M = np.tril(np.ones((n, n)))
+            A, Cm = Q @ K.T, D @ V.T
+            den = Q @ z + (M * A).sum(1)
+            go = ((Q * (D @ S.T)).sum(1) + (M * A * Cm).sum(1)) / den
+            dpq[r] = (D @ S.T - np.outer(go, z) + (M * (Cm - go[:, None])) @ K) / den[:, None]
+            den_all[r], go_all[r] = den, go
+            S = S + K.T @ V
+            z = z + K.sum(0)
+    pqt = pq / den_all[:, None]
+    tot = []
+    for pc in pieces:
+        T, t = np.zeros((m, v.shape[1])), np.zeros(m)
+        for c in pc:
+            T += pqt[rows(c)].T @ g[rows(c)]
+            t -= (pqt[rows(c)] * go_all[rows(c), None]).sum(0)
+        tot.append((T, t))
+    dpk, dv = np.zeros_like(pk), np.zeros_like(v)
+    for p, pc in enumerate(pieces):
+        T = sum((x[0] for x in tot[p + 1:]), np.zeros((m, v.shape[1])))
+        t = sum((x[1] for x in tot[p + 1:]), np.zeros(m))
+        for c in reversed(pc):
+            r = rows(c)
+            n = r.stop - r.start
+            Qt, K, V, D = pqt[r], pk[r], v[r], g[r]
+            Mt = np.triu(np.ones((n, n)))
+            W = Mt * (V @ D.T - go_all[r][None, :])
+            dpk[r] = V @ T.T + t[None, :] + W @ Qt
+            dv[r] = K @ T + (Mt * (K @ Qt.T)) @ D
+            T = T + Qt.T @ D
+            t = t - (Qt * go_all[r][:, None]).sum(0)
+    return dpq, dpk, dv
+
+
+@pytest.mark.parametrize("L,chunk,per", [(50, 8, 3), (64, 16, 1), (37, 8, 2)])
+def test_causal_chunk_split_matches_the_derivative(L, chunk, per):
+    """The chunked form of the causal gradients (prefix and suffix states of
+    whole pieces, states carried across chunks inside a piece, masked
+    products inside a chunk) gives the oracle's causal derivative on
+    features, with ragged last chunks and keys whose features vanish (keys
+    past the end of a tile)."""
+    rng = np.random.default_rng(L)
+    m, dv = 6, 3
+    pq = rng.random((L, m)) + 0.05
+    pk = rng.random((L, m)) + 0.05
+    pk[-3:] = 0.0
+    v = rng.normal(size=(L, dv))
+    g = rng.normal(size=(L, dv))
+    ref = O.attn_from_features_causal_vjp(pq, pk, v, g)
+    got = _chunked_causal_feature_grads(pq, pk, v, g, chunk, per)
+    for a, b in zip(got, ref):
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
